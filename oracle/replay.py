@@ -1,0 +1,113 @@
+"""Replay a workload through the oracle block manager, cache model and attention.
+
+Issue order inside a decode step: the step's copy-on-write frame copies are
+applied before the step's new rows are written (a copy reads the shared frame as
+it was before any writer of this step touched it).
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from .attention import paged_decode
+from .block_manager import OracleBlockManager
+from .cache import OracleKVCache
+
+
+@dataclass
+class ReplayResult:
+    bm: OracleBlockManager
+    cache: OracleKVCache | None
+    # per op index: {"slots": [...], "copies": [(src, dst), ...]} for add/step ops
+    trace: dict = field(default_factory=dict)
+    # per op index: BM snapshot after the op
+    snapshots: dict = field(default_factory=dict)
+    # per attend op index: float64 [n, H, D] (rows of sequences not kept are NaN)
+    outputs: dict = field(default_factory=dict)
+    # per attend op index: (tables, lens) the attention used, in the op's seq order
+    attend_meta: dict = field(default_factory=dict)
+
+
+def _kept_frames(w, keep_seqs):
+    """Frames whose contents reach the kept sequences: final tables + copy sources."""
+    bm = OracleBlockManager(w.num_blocks, w.block_size, w.free_order)
+    edges = []
+    seen = set()
+    for op in w.ops:
+        kind = op[0]
+        if kind == "add":
+            bm.add_seq(op[1], op[2])
+        elif kind == "fork":
+            bm.fork(op[1], op[2])
+        elif kind == "step":
+            _, copies = bm.step(op[1])
+            edges.extend(copies)
+        elif kind == "free":
+            bm.free(op[1])
+        elif kind == "attend":
+            for s in op[1]:
+                if s in keep_seqs:
+                    seen.update(bm.tables[s])
+    for s in keep_seqs:
+        if s in bm.tables:
+            seen.update(bm.tables[s])
+    changed = True
+    while changed:
+        changed = False
+        for src, dst in edges:
+            if dst in seen and src not in seen:
+                seen.add(src)
+                changed = True
+    return seen
+
+
+def replay(w, keep_seqs=None, with_cache: bool = True, snapshots: bool = False) -> ReplayResult:
+    """Run every op of ``w``; attention only for ``keep_seqs`` (all if None)."""
+    keep = None if keep_seqs is None else set(int(s) for s in keep_seqs)
+    frames = None if keep is None else _kept_frames(w, keep)
+    bm = OracleBlockManager(w.num_blocks, w.block_size, w.free_order)
+    cache = (OracleKVCache(w.num_blocks, w.block_size, w.num_heads, w.head_dim, w.dtype, keep=frames)
+             if with_cache else None)
+    res = ReplayResult(bm=bm, cache=cache)
+    B = w.block_size
+    for i, op in enumerate(w.ops):
+        kind = op[0]
+        if kind == "add":
+            slots = bm.add_seq(op[1], op[2])
+            res.trace[i] = {"slots": slots, "copies": []}
+            if cache is not None and slots and (frames is None or any(s // B in frames for s in slots)):
+                k, v = w.rows(i)
+                cache.write(slots, k, v)
+        elif kind == "fork":
+            bm.fork(op[1], op[2])
+        elif kind == "step":
+            slots, copies = bm.step(op[1])
+            res.trace[i] = {"slots": slots, "copies": copies}
+            if cache is not None:
+                for src, dst in copies:
+                    cache.copy_block(src, dst)
+                if frames is None or any(s // B in frames for s in slots):
+                    k, v = w.rows(i)
+                    cache.write(slots, k, v)
+        elif kind == "free":
+            bm.free(op[1])
+        elif kind == "attend":
+            seqs = op[1]
+            tables = [list(bm.tables[s]) for s in seqs]
+            lens = [bm.lens[s] for s in seqs]
+            res.attend_meta[i] = (tables, lens)
+            if cache is not None:
+                q = w.query(i)
+                out = np.full((len(seqs), w.num_heads, w.head_dim), np.nan)
+                idx = [j for j, s in enumerate(seqs) if keep is None or s in keep]
+                if idx:
+                    out[idx] = paged_decode(q[idx], cache, [tables[j] for j in idx],
+                                            [lens[j] for j in idx], w.scale)
+                res.outputs[i] = out
+        else:
+            raise ValueError(f"unknown op {op!r}")
+        if snapshots:
+            res.snapshots[i] = bm.snapshot()
+    return res

@@ -1,0 +1,234 @@
+"""Workload definitions and seeded draws.
+
+A workload is a list of operations on a paged KV cache plus the random payload
+each operation carries:
+
+* ``("add", seq, n)``     -- a new sequence with an ``n``-token prompt; the op's
+                             payload is ``n`` K rows and ``n`` V rows.
+* ``("fork", parent, child)`` -- the child shares the parent's blocks.
+* ``("step", seqs)``      -- one decode step: one new token for each listed
+                             sequence, in list order; payload: ``len(seqs)`` rows.
+* ``("attend", seqs)``    -- single-query decode attention for each listed
+                             sequence; payload: one query per sequence.
+* ``("free", seq)``       -- the sequence finishes.
+
+Payloads are drawn from a PCG64 stream keyed by ``(seed, op_index, kind)`` so any
+op's rows can be regenerated alone.  Values are drawn as float32 N(0, sigma^2)
+and rounded to nearest-even into the storage type; bf16 is carried as uint16 bit
+patterns because NumPy has no bf16 type.
+
+Shapes follow the five workloads of the paged-decode study (a 100-block toy
+trace, a 64-sequence decode batch, a 4x16k long-context batch, a 16-prompt
+parallel-sampling batch with copy-on-write, a 256-sequence serving mix), each with
+a scaled-down variant whose oracle finishes in seconds.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+DTYPES = ("f32", "f16", "bf16")
+CONFIG_IDS = (0, 1, "1x", 2, 3, 4)
+
+_KIND = {"k": 1, "v": 2, "q": 3}
+
+
+def storage_numpy_dtype(dtype: str):
+    """NumPy type that holds one element of the storage dtype."""
+    return {"f32": np.float32, "f16": np.float16, "bf16": np.uint16}[dtype]
+
+
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns, round to nearest even (inputs are finite)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    return ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+
+
+def _to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "f32":
+        return x.astype(np.float32, copy=False)
+    if dtype == "f16":
+        return x.astype(np.float16)
+    if dtype == "bf16":
+        return _bf16_bits(x)
+    raise ValueError(dtype)
+
+
+@dataclass
+class Workload:
+    name: str
+    num_heads: int
+    head_dim: int
+    block_size: int
+    dtype: str
+    sigma: float
+    num_blocks: int
+    free_order: np.ndarray
+    ops: list
+    seed: int
+    # float32 softmax scale handed to the decode call (1/sqrt(head_dim))
+    scale: float = field(default=0.0)
+    # context length each sequence ends with (for sizing and reporting only)
+    final_lens: dict = field(default_factory=dict)
+
+    def __post_init__(self):
+        if not self.scale:
+            self.scale = float(np.float32(1.0) / np.sqrt(np.float32(self.head_dim)))
+        self.free_order = np.asarray(self.free_order, dtype=np.int32)
+
+    # -- payloads ---------------------------------------------------------------
+    def _draw(self, op_index: int, kind: str, n: int) -> np.ndarray:
+        ss = np.random.SeedSequence([self.seed, op_index, _KIND[kind]])
+        g = np.random.Generator(np.random.PCG64(ss))
+        x = g.standard_normal(n * self.num_heads * self.head_dim, dtype=np.float32)
+        if self.sigma != 1.0:
+            x *= np.float32(self.sigma)
+        return _to_storage(x, self.dtype).reshape(n, self.num_heads, self.head_dim)
+
+    def rows(self, op_index: int):
+        """(k, v) rows carried by an ``add`` or ``step`` op, storage dtype."""
+        op = self.ops[op_index]
+        n = op[2] if op[0] == "add" else len(op[1])
+        return self._draw(op_index, "k", n), self._draw(op_index, "v", n)
+
+    def query(self, op_index: int) -> np.ndarray:
+        """Queries ``[len(seqs), H, D]`` carried by an ``attend`` op, storage dtype."""
+        op = self.ops[op_index]
+        assert op[0] == "attend"
+        return self._draw(op_index, "q", len(op[1]))
+
+    @property
+    def attend_ops(self):
+        return [i for i, op in enumerate(self.ops) if op[0] == "attend"]
+
+    @property
+    def elem_bytes(self) -> int:
+        return {"f32": 4, "f16": 2, "bf16": 2}[self.dtype]
+
+
+def _pool_size(final_lens, block_size: int, factor: float = 1.2) -> int:
+    # Pool sized with headroom over one private block list per sequence.
+    need = sum(-(-L // block_size) for L in final_lens)
+    return max(1, int(math.ceil(factor * need)))
+
+
+def _decode_batch(name, lengths, H, D, B, dtype, sigma, seed, *, shuffle=True,
+                  pool=None, free_order=None):
+    """Prefill ``L-1`` tokens per sequence, one decode step, one attention."""
+    lengths = [int(x) for x in lengths]
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0])))
+    nb = pool if pool is not None else _pool_size(lengths, B)
+    if free_order is None:
+        free_order = rng.permutation(nb).astype(np.int32) if shuffle else np.arange(nb, dtype=np.int32)
+    ops = []
+    for s, L in enumerate(lengths):
+        ops.append(("add", s, max(L - 1, 0)))
+    step = tuple(s for s, L in enumerate(lengths) if L >= 1)
+    if step:
+        ops.append(("step", step))
+    ops.append(("attend", tuple(range(len(lengths)))))
+    return Workload(name=name, num_heads=H, head_dim=D, block_size=B, dtype=dtype,
+                    sigma=sigma, num_blocks=nb, free_order=free_order, ops=ops, seed=seed,
+                    final_lens={s: L for s, L in enumerate(lengths)})
+
+
+def _toy(seed=1000):
+    # 100 blocks of 10 token slots, free list 0..99, prompts A:8 B:5 C:12 D:9,
+    # then three decode steps, each followed by attention over all four.
+    ops = [("add", 0, 8), ("add", 1, 5), ("add", 2, 12), ("add", 3, 9)]
+    for _ in range(3):
+        ops.append(("step", (0, 1, 2, 3)))
+        ops.append(("attend", (0, 1, 2, 3)))
+    return Workload(name="toy: 100 blocks x 10 slots, prompts 8/5/12/9 + 3 decode steps",
+                    num_heads=2, head_dim=64, block_size=10, dtype="f32", sigma=1.0,
+                    num_blocks=100, free_order=np.arange(100, dtype=np.int32), ops=ops,
+                    seed=seed, final_lens={0: 11, 1: 8, 2: 15, 3: 12})
+
+
+def _parallel_sampling(n_prompts, prompt_len, n_branch, r_max, H, D, B, dtype, seed, name):
+    """Prompts forked into branches that decode private tokens with copy-on-write.
+
+    Branch 0 of each prompt is the prompt sequence itself; branches 1.. are forks
+    taken right after the prompt is added.  Each branch draws r ~ U{0..r_max}
+    private tokens; decoding is step-major (prompts in order, branches in order),
+    then one attention over every branch.
+    """
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0])))
+    r = rng.integers(0, r_max + 1, size=n_prompts * n_branch)
+    ops = []
+    for p in range(n_prompts):
+        base = p * n_branch
+        ops.append(("add", base, prompt_len))
+        for b in range(1, n_branch):
+            ops.append(("fork", base, base + b))
+    for k in range(int(r.max()) if len(r) else 0):
+        seqs = tuple(s for s in range(n_prompts * n_branch) if r[s] > k)
+        ops.append(("step", seqs))
+    ops.append(("attend", tuple(range(n_prompts * n_branch))))
+    final = {s: prompt_len + int(r[s]) for s in range(n_prompts * n_branch)}
+    nb = _pool_size(final.values(), B)
+    free_order = rng.permutation(nb).astype(np.int32)
+    return Workload(name=name, num_heads=H, head_dim=D, block_size=B, dtype=dtype, sigma=1.0,
+                    num_blocks=nb, free_order=free_order, ops=ops, seed=seed, final_lens=final)
+
+
+def _log_uniform(rng, n, lo, hi):
+    x = np.floor(np.exp(rng.uniform(np.log(lo), np.log(hi), size=n))).astype(np.int64)
+    return np.clip(x, lo, hi)
+
+
+def build(cfg, small: bool = False) -> Workload:
+    """The five workloads (plus the fixed 64x2048 decode batch ``"1x"``).
+
+    ``small=True`` gives a scaled-down variant of the same structure whose oracle
+    runs in seconds: several thread-block tiles and a ragged last block remain.
+    """
+    seed = 1000 + (1 if cfg == "1x" else int(cfg)) + (500 if small else 0)
+    if cfg == 0:
+        return _toy(seed)
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 1])))
+    if cfg == 1:
+        if small:
+            L = rng.integers(40, 301, size=6)
+            return _decode_batch("decode batch (small): 6 seqs, L~U[40,300], H=4, D=128, B=16, f16",
+                                 L, 4, 128, 16, "f16", 1.0, seed)
+        L = rng.integers(512, 2049, size=64)
+        return _decode_batch("decode batch: 64 seqs, L~U[512,2048], H=32, D=128, B=16, f16",
+                             L, 32, 128, 16, "f16", 1.0, seed)
+    if cfg == "1x":
+        S, L = (4, 300) if small else (64, 2048)
+        return _decode_batch(f"decode batch: {S} seqs x {L} tokens, H=32, D=128, B=16, f16",
+                             [L] * S, 32 if not small else 4, 128, 16, "f16", 1.0, seed)
+    if cfg == 2:
+        if small:
+            return _decode_batch("long context (small): 2 seqs x 2500, H=2, D=128, B=32, bf16",
+                                 [2500, 2500], 2, 128, 32, "bf16", 1.0, seed)
+        return _decode_batch("long context: 4 seqs x 16384, H=32, D=128, B=32, bf16",
+                             [16384] * 4, 32, 128, 32, "bf16", 1.0, seed)
+    if cfg == 3:
+        if small:
+            return _parallel_sampling(3, 100, 4, 40, 2, 128, 16, "f16", seed,
+                                      "parallel sampling (small): 3 prompts x 100, 4 branches, r~U{0..40}")
+        return _parallel_sampling(16, 1000, 4, 256, 32, 128, 16, "f16", seed,
+                                  "parallel sampling: 16 prompts x 1000, 4 branches, r~U{0..256}, H=32, D=128, B=16, f16")
+    if cfg == 4:
+        if small:
+            L = _log_uniform(rng, 24, 16, 800)
+            return _decode_batch("serving mix (small): 24 seqs, L~logU[16,800], H=40, D=128, B=16, bf16",
+                                 L, 40, 128, 16, "bf16", 0.5, seed)
+        L = _log_uniform(rng, 256, 16, 8192)
+        return _decode_batch("serving mix: 256 seqs, L~logU[16,8192], H=40, D=128, B=16, bf16",
+                             L, 40, 128, 16, "bf16", 0.5, seed)
+    raise ValueError(f"unknown workload {cfg!r}")
+
+
+def custom(lengths, *, H=2, D=128, B=16, dtype="f16", sigma=1.0, seed=7, shuffle=True,
+           pool=None, free_order=None, name=None) -> Workload:
+    """Decode batch with explicit final context lengths (edge cases, sweeps)."""
+    return _decode_batch(name or f"custom L={list(lengths)[:6]}..., H={H}, D={D}, B={B}, {dtype}",
+                         lengths, H, D, B, dtype, sigma, seed, shuffle=shuffle, pool=pool,
+                         free_order=free_order)
