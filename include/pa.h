@@ -1,0 +1,240 @@
+/*
+ * pa.h -- C ABI of libpa: paged KV-cache append and single-query decode
+ * attention for NVIDIA GB300 (sm_103a), plus the host block manager that
+ * produces block tables and slot mappings.
+ *
+ * Sources (web pages on PagedAttention):
+ *   [VM]  "PagedAttention: Virtual Memory Guide for LLM Inference"
+ *   [MW]  "Solving the LLM Memory Wall: A Deep Dive into PagedAttention"
+ *   [SE]  "PagedAttention, simply explained"
+ *
+ * Conventions shared by every call:
+ *   - Return value: PA_OK (0) on success, a positive PA_WARN_* for a tolerated
+ *     no-op, a negative PA_ERR_* on failure.  A failing call changes nothing
+ *     (host state) and launches nothing (device).  pa_strerror() names a code.
+ *   - Tensors are described by pa_tensor (data pointer, dtype, shape, strides in
+ *     ELEMENTS).  The caller owns all tensor memory.  Device calls take device
+ *     pointers; pa_bm_* calls take host pointers.
+ *   - Device calls are asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).  They bounds-check indices read from device memory
+ *     (slots, block ids, context lengths); a bad index is skipped (and for
+ *     decode the affected output rows are written as zeros) and a bit is set in a
+ *     sticky per-device status word that pa_get_device_status() reads.  No kernel
+ *     traps or asserts.
+ *   - Cache layout [MW "The Architecture at a Glance"]: k_cache and v_cache are
+ *     separate contiguous tensors [num_blocks, block_size, num_heads, head_dim];
+ *     token i of a sequence sits at frame table[i / block_size], offset
+ *     i % block_size [VM "The Mathematics of Block Translation"]; its flat slot is
+ *     frame * block_size + offset.  head_dim * element size must be a multiple of
+ *     16 bytes and num_blocks * block_size must fit in int32.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- element types ---------------------------------------------------------------- */
+enum pa_dtype { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_I32 = 3 };
+
+/* ---- return codes ------------------------------------------------------------------ */
+#define PA_OK                 0
+#define PA_WARN_DOUBLE_FREE   1   /* pa_bm_free of a sequence that is not live: no-op */
+#define PA_ERR_INVALID       -1   /* null pointer, negative count, bad option */
+#define PA_ERR_DTYPE         -2
+#define PA_ERR_SHAPE         -3
+#define PA_ERR_STRIDE        -4
+#define PA_ERR_ALIGN         -5
+#define PA_ERR_OUT_OF_BLOCKS -6   /* free list cannot cover the request (state unchanged) */
+#define PA_ERR_UNKNOWN_SEQ   -7
+#define PA_ERR_SEQ_EXISTS    -8
+#define PA_ERR_CUDA          -9   /* a CUDA runtime call or launch failed */
+#define PA_ERR_UNSUPPORTED  -10   /* head_dim / dtype / size outside the built kernels */
+#define PA_ERR_CAPACITY     -11   /* caller-provided output buffer too small */
+
+/* ---- sticky device status bits (pa_get_device_status) ------------------------------ */
+#define PA_DEV_BAD_SLOT   0x1   /* append: slot >= num_blocks*block_size */
+#define PA_DEV_BAD_BLOCK  0x2   /* decode: block-table entry outside [0, num_blocks) */
+#define PA_DEV_BAD_LEN    0x4   /* decode: context_len < 0 or > max_blocks*block_size */
+#define PA_DEV_BAD_COPY   0x8   /* copy_blocks: frame id outside [0, num_blocks) */
+#define PA_DEV_TIMEOUT    0x10  /* a bounded wait inside a kernel gave up */
+
+typedef struct pa_tensor {
+  void*   data;       /* device (or host, where stated) pointer to element [0,...,0] */
+  int32_t dtype;      /* enum pa_dtype */
+  int32_t ndim;       /* 1..4 */
+  int64_t shape[4];
+  int64_t stride[4];  /* in elements */
+} pa_tensor;
+
+typedef void* pa_stream;   /* cudaStream_t */
+
+/* ===================================================================================
+ * Device path
+ * =================================================================================== */
+
+/*
+ * pa_cache_append -- write each new token's K and V rows into its paged slot.
+ * [MW "Implementation", PagedKVCache.update, batched over tokens; VM "Key
+ * Architectural Mechanics / 1. Demand Paging": the token lands at offset t mod B
+ * of its current frame, no reallocation or data movement.]
+ *
+ *   k_new, v_new   [T, H, D] (q/cache dtype); the [H, D] part contiguous, row
+ *                  stride (stride[0]) free but a multiple of 16 bytes.
+ *   slot_mapping   int32 [T]; k_cache.view(-1, H, D)[slot[t]] = k_new[t] (same for
+ *                  v).  slot < 0 = padding, skipped.  slot >= num_blocks*B sets
+ *                  PA_DEV_BAD_SLOT and is skipped.
+ *   k_cache, v_cache  [num_blocks, B, H, D], contiguous, same dtype as k_new.
+ * Slots within one call must be distinct (each is written by one thread block,
+ * in no particular order).  T == 0 is a no-op.
+ */
+int pa_cache_append(const pa_tensor* k_new, const pa_tensor* v_new,
+                    const pa_tensor* slot_mapping,
+                    const pa_tensor* k_cache, const pa_tensor* v_cache,
+                    pa_stream stream);
+
+/*
+ * pa_copy_blocks -- whole-frame copies for copy-on-write.
+ * [VM "Key Architectural Mechanics / 2. Zero-Copy Branching via Copy-on-Write":
+ * only the one shared frame being written is duplicated.]
+ *
+ *   pairs   int32 [n, 2], row = (src frame, dst frame); contiguous.  Both caches
+ *           get cache[dst] = cache[src].  Ids outside [0, num_blocks) set
+ *           PA_DEV_BAD_COPY and the pair is skipped.  Destinations must be
+ *           distinct and no destination may be another pair's source.
+ * Issue a decode step's copies BEFORE that step's pa_cache_append.
+ */
+int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache,
+                   const pa_tensor* pairs, pa_stream stream);
+
+/*
+ * pa_decode -- single-query decode attention over the paged cache.
+ * [MW "1. The Mathematical Foundation": a_j = q.k_j * scale, o = sum_j softmax(a)_j
+ *  v_j over the sequence's tokens; VM "3. PagedAttention CUDA Kernel Execution":
+ *  one fused kernel reads the block table and stages the frames on chip, with no
+ *  gathered copy of K/V in HBM.]
+ *
+ *   q             [S, H, D], row stride free (16-byte multiple), [H, D] contiguous.
+ *   k_cache, v_cache  [num_blocks, B, H, D] contiguous, same dtype as q.
+ *   block_tables  int32 [S, max_blocks], inner stride 1; row s lists the frames of
+ *                 sequence s in logical order; entries past ceil(L_s/B) unread.
+ *   context_lens  int32 [S], L_s = tokens attended (the newest appended included).
+ *                 L_s == 0 gives a zero output row.
+ *   scale         softmax scale, normally 1/sqrt(D).
+ *   out           [S, H, D], same dtype as q, [H, D] contiguous.
+ * Arithmetic: K/V/q converted to fp32, fp32 dot products, online softmax and
+ * accumulation in fp32, one rounding to the output dtype.  Long contexts are
+ * split into partitions processed by separate thread blocks and combined by a
+ * log-sum-exp merge kernel on the same stream.  The split needs a workspace that
+ * the library owns: one per (device, stream), grown with cudaMalloc on first use
+ * at a larger size (keep such first calls outside CUDA-graph capture), freed by
+ * pa_shutdown().
+ * Supported: dtype f32/f16/bf16; D in {64, 128, 256} (f32: {64, 128});
+ * 1 <= B <= 256.
+ */
+int pa_decode(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+              const pa_tensor* block_tables, const pa_tensor* context_lens,
+              float scale, const pa_tensor* out, pa_stream stream);
+
+/* Launch options for pa_decode_ex; 0 in any field = automatic choice. */
+typedef struct pa_decode_params {
+  int32_t partition_tokens;  /* >0: split context into partitions of this many tokens
+                                (rounded up to a multiple of B); -1: never split */
+  int32_t heads_per_cta;     /* 1, 2 or 4 (must divide H) */
+  int32_t warps_per_head;    /* 1, 2, 4 or 8 */
+  int32_t stages;            /* K/V staging buffers per thread block, 2..8 */
+  int32_t ctas_per_sm;       /* persistent grid = SMs x this (clamped to occupancy) */
+  int32_t reserved[3];
+} pa_decode_params;
+
+/* pa_decode with explicit launch options (tests, tuning).  params may be NULL. */
+int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                 const pa_tensor* block_tables, const pa_tensor* context_lens,
+                 float scale, const pa_tensor* out, const pa_decode_params* params,
+                 pa_stream stream);
+
+/* Synchronises `stream`, returns the current device's sticky PA_DEV_* bits in
+ * *status_out and clears them. */
+int pa_get_device_status(pa_stream stream, int32_t* status_out);
+
+/* Human-readable name of a return code (static storage). */
+const char* pa_strerror(int code);
+
+/* Number of kernels this library has launched in this process (all devices). */
+int64_t pa_launch_count(void);
+
+/* Frees the library-owned decode workspaces of every device.  Call only when no
+ * decode launched by this library is still running. */
+int pa_shutdown(void);
+
+/* ===================================================================================
+ * Host block manager (pure host code; no GPU needed)
+ * [VM "Reference Implementation: Block Table & Paged Cache Manager",
+ *  "Key Architectural Mechanics / 1-2"; MW "Implementation", BlockManager;
+ *  SE "How PagedAttention solves it"]
+ * Free frames leave from the front of the free list and return to its back when
+ * their reference count reaches zero.  Sequences are named by caller-chosen
+ * int64 ids.  Not thread-safe: one handle per thread, or external locking.
+ * =================================================================================== */
+typedef struct pa_bm pa_bm;
+
+/* free_order: NULL = 0,1,...,num_blocks-1; else a permutation of those ids that
+ * becomes the initial free list.  num_blocks * block_size must fit in int32. */
+int  pa_bm_create(int32_t num_blocks, int32_t block_size, const int32_t* free_order,
+                  pa_bm** bm_out);
+void pa_bm_destroy(pa_bm* bm);
+
+/* New sequence with a prompt of num_tokens: takes ceil(num_tokens/B) frames,
+ * all-or-nothing [MW BlockManager.allocate].  slots_out (nullable) receives the
+ * num_tokens flat slots of the prompt tokens. */
+int pa_bm_add_seq(pa_bm* bm, int64_t seq_id, int32_t num_tokens, int32_t* slots_out);
+
+/* One new token for seq_id [VM "1. Demand Paging", "2. Copy-on-Write"]:
+ *   t = current length; if t % B == 0 a frame is taken from the free list and
+ *   appended to the table; else if the tail frame is shared (refcount > 1) a
+ *   private frame is taken, the shared frame loses one reference and the private
+ *   one replaces it in the table; the caller must then copy the frame's data
+ *   (*cow_src -> *cow_dst, both -1 when there is nothing to copy).
+ *   *slot_out = flat slot of token t.  All-or-nothing. */
+int pa_bm_append(pa_bm* bm, int64_t seq_id, int32_t* slot_out,
+                 int32_t* cow_src, int32_t* cow_dst);
+
+/* One decode step: pa_bm_append for seq_ids[0..n) in that order, all-or-nothing
+ * (if any append would run out of frames or names an unknown sequence, nothing
+ * changes).  slots_out [n]; copies_out [n][2] receives the (src, dst) pairs in
+ * issue order, *n_copies_out their count. */
+int pa_bm_step(pa_bm* bm, const int64_t* seq_ids, int32_t n, int32_t* slots_out,
+               int32_t* copies_out, int32_t* n_copies_out);
+
+/* Zero-copy fork: child shares every frame of parent (each gains a reference)
+ * and inherits its length [VM "2. Zero-Copy Branching"]. */
+int pa_bm_fork(pa_bm* bm, int64_t parent_id, int64_t child_id);
+
+/* Release a finished sequence: each frame loses a reference, in table order;
+ * frames reaching zero return to the back of the free list.  An id that is not
+ * live is a no-op returning PA_WARN_DOUBLE_FREE. */
+int pa_bm_free(pa_bm* bm, int64_t seq_id);
+
+/* Block tables [n, max_blocks] (row-major, unused entries -1) and lengths [n] of
+ * the listed sequences, ready to upload for pa_decode.  PA_ERR_CAPACITY if a
+ * table is longer than max_blocks. lens_out may be NULL. */
+int pa_bm_block_tables(const pa_bm* bm, const int64_t* seq_ids, int32_t n,
+                       int32_t max_blocks, int32_t* tables_out, int32_t* lens_out);
+
+/* Queries. */
+int pa_bm_seq_info(const pa_bm* bm, int64_t seq_id, int32_t* len_out, int32_t* n_blocks_out);
+int pa_bm_table(const pa_bm* bm, int64_t seq_id, int32_t* out, int32_t cap, int32_t* n_out);
+int pa_bm_slot(const pa_bm* bm, int64_t seq_id, int32_t pos, int32_t* slot_out);
+int pa_bm_num_free(const pa_bm* bm, int32_t* n_out);
+int pa_bm_free_list(const pa_bm* bm, int32_t* out, int32_t cap, int32_t* n_out);  /* front first */
+int pa_bm_ref_counts(const pa_bm* bm, int32_t* out, int32_t cap);               /* [num_blocks] */
+int pa_bm_num_seqs(const pa_bm* bm, int32_t* n_out);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* PA_H_ */

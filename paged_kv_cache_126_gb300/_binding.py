@@ -1,0 +1,313 @@
+"""Thin ctypes binding of libpa (include/pa.h): argument marshalling only.
+
+Every device operation runs in libpa's CUDA kernels; this module turns torch
+tensors into ``pa_tensor`` descriptors and return codes into exceptions.  If
+``libpa.so`` is missing the import fails: there is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpa.so")
+
+PA_F32, PA_F16, PA_BF16, PA_I32 = 0, 1, 2, 3
+PA_OK = 0
+PA_WARN_DOUBLE_FREE = 1
+PA_ERR_OUT_OF_BLOCKS = -6
+PA_ERR_UNKNOWN_SEQ = -7
+PA_ERR_SEQ_EXISTS = -8
+
+PA_DEV_BAD_SLOT = 0x1
+PA_DEV_BAD_BLOCK = 0x2
+PA_DEV_BAD_LEN = 0x4
+PA_DEV_BAD_COPY = 0x8
+PA_DEV_TIMEOUT = 0x10
+
+_TORCH_DT = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.int32: PA_I32}
+
+
+class PaTensor(C.Structure):
+    _fields_ = [("data", C.c_void_p), ("dtype", C.c_int32), ("ndim", C.c_int32),
+                ("shape", C.c_int64 * 4), ("stride", C.c_int64 * 4)]
+
+
+class PaDecodeParams(C.Structure):
+    _fields_ = [("partition_tokens", C.c_int32), ("heads_per_cta", C.c_int32),
+                ("warps_per_head", C.c_int32), ("stages", C.c_int32), ("ctas_per_sm", C.c_int32),
+                ("reserved", C.c_int32 * 3)]
+
+
+class PAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} ({code})")
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"libpa.so not found at {_LIB_PATH}; build it first "
+                          "(python paged_kv_cache_126_gb300/build.py)")
+    lib = C.CDLL(_LIB_PATH)
+    P = C.POINTER(PaTensor)
+    i32p, i64p = C.POINTER(C.c_int32), C.POINTER(C.c_int64)
+    vp = C.c_void_p
+    sig = {
+        "pa_cache_append": ([P, P, P, P, P, vp], C.c_int),
+        "pa_copy_blocks": ([P, P, P, vp], C.c_int),
+        "pa_decode": ([P, P, P, P, P, C.c_float, P, vp], C.c_int),
+        "pa_decode_ex": ([P, P, P, P, P, C.c_float, P, C.POINTER(PaDecodeParams), vp], C.c_int),
+        "pa_get_device_status": ([vp, i32p], C.c_int),
+        "pa_strerror": ([C.c_int], C.c_char_p),
+        "pa_launch_count": ([], C.c_int64),
+        "pa_shutdown": ([], C.c_int),
+        "pa_bm_create": ([C.c_int32, C.c_int32, i32p, C.POINTER(vp)], C.c_int),
+        "pa_bm_destroy": ([vp], None),
+        "pa_bm_add_seq": ([vp, C.c_int64, C.c_int32, i32p], C.c_int),
+        "pa_bm_append": ([vp, C.c_int64, i32p, i32p, i32p], C.c_int),
+        "pa_bm_step": ([vp, i64p, C.c_int32, i32p, i32p, i32p], C.c_int),
+        "pa_bm_fork": ([vp, C.c_int64, C.c_int64], C.c_int),
+        "pa_bm_free": ([vp, C.c_int64], C.c_int),
+        "pa_bm_block_tables": ([vp, i64p, C.c_int32, C.c_int32, i32p, i32p], C.c_int),
+        "pa_bm_seq_info": ([vp, C.c_int64, i32p, i32p], C.c_int),
+        "pa_bm_table": ([vp, C.c_int64, i32p, C.c_int32, i32p], C.c_int),
+        "pa_bm_slot": ([vp, C.c_int64, C.c_int32, i32p], C.c_int),
+        "pa_bm_num_free": ([vp, i32p], C.c_int),
+        "pa_bm_free_list": ([vp, i32p, C.c_int32, i32p], C.c_int),
+        "pa_bm_ref_counts": ([vp, i32p, C.c_int32], C.c_int),
+        "pa_bm_num_seqs": ([vp, i32p], C.c_int),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+LIB = _load()
+EXPORTED = (
+    "pa_cache_append", "pa_copy_blocks", "pa_decode", "pa_decode_ex", "pa_get_device_status",
+    "pa_strerror", "pa_launch_count", "pa_shutdown", "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq",
+    "pa_bm_append", "pa_bm_step", "pa_bm_fork", "pa_bm_free", "pa_bm_block_tables", "pa_bm_seq_info",
+    "pa_bm_table", "pa_bm_slot", "pa_bm_num_free", "pa_bm_free_list", "pa_bm_ref_counts",
+    "pa_bm_num_seqs",
+)
+
+
+def strerror(code: int) -> str:
+    return LIB.pa_strerror(int(code)).decode()
+
+
+def _check(rc: int, where: str) -> int:
+    if rc < 0:
+        raise PAError(rc, where)
+    return rc
+
+
+def tensor_desc(t: torch.Tensor) -> PaTensor:
+    """pa_tensor describing a torch tensor (no copy)."""
+    if t.dtype not in _TORCH_DT:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    if t.dim() < 1 or t.dim() > 4:
+        raise ValueError("tensors must have 1..4 dims")
+    d = PaTensor()
+    d.data = t.data_ptr() or None
+    d.dtype = _TORCH_DT[t.dtype]
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _stream_of(t: torch.Tensor, stream):
+    if not t.is_cuda:
+        raise ValueError("device operations take CUDA tensors")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"tensor on {t.device} but the current device is cuda:{torch.cuda.current_device()}")
+    s = stream if stream is not None else torch.cuda.current_stream(t.device)
+    return C.c_void_p(s.cuda_stream)
+
+
+def _ref(d: PaTensor):
+    return C.byref(d)
+
+
+def pa_cache_append(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None) -> None:
+    st = _stream_of(k_cache, stream)
+    ds = [tensor_desc(t) for t in (k_new, v_new, slot_mapping, k_cache, v_cache)]
+    _check(LIB.pa_cache_append(*map(_ref, ds), st), "pa_cache_append")
+
+
+def pa_copy_blocks(k_cache, v_cache, pairs, stream=None) -> None:
+    st = _stream_of(k_cache, stream)
+    ds = [tensor_desc(t) for t in (k_cache, v_cache, pairs)]
+    _check(LIB.pa_copy_blocks(*map(_ref, ds), st), "pa_copy_blocks")
+
+
+def make_params(params) -> PaDecodeParams | None:
+    if params is None:
+        return None
+    if isinstance(params, PaDecodeParams):
+        return params
+    p = PaDecodeParams()
+    for k, v in dict(params).items():
+        setattr(p, k, int(v))
+    return p
+
+
+def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, stream=None, params=None):
+    st = _stream_of(q, stream)
+    ds = [tensor_desc(t) for t in (q, k_cache, v_cache, block_tables, context_lens)]
+    o = tensor_desc(out)
+    p = make_params(params)
+    if p is None:
+        rc = LIB.pa_decode(*map(_ref, ds), C.c_float(scale), C.byref(o), st)
+    else:
+        rc = LIB.pa_decode_ex(*map(_ref, ds), C.c_float(scale), C.byref(o), C.byref(p), st)
+    _check(rc, "pa_decode")
+    return out
+
+
+def pa_decode_ex(q, k_cache, v_cache, block_tables, context_lens, scale, out, params=None, stream=None):
+    return pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, stream=stream,
+                     params=params or {})
+
+
+def pa_get_device_status(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    v = C.c_int32(0)
+    _check(LIB.pa_get_device_status(C.c_void_p(s.cuda_stream), C.byref(v)), "pa_get_device_status")
+    return v.value
+
+
+def pa_launch_count() -> int:
+    return int(LIB.pa_launch_count())
+
+
+def pa_shutdown() -> None:
+    _check(LIB.pa_shutdown(), "pa_shutdown")
+
+
+def _i32(a: np.ndarray):
+    return a.ctypes.data_as(C.POINTER(C.c_int32))
+
+
+def _i64(a: np.ndarray):
+    return a.ctypes.data_as(C.POINTER(C.c_int64))
+
+
+class BlockManager:
+    """Host block manager of libpa (free list, refcounts, fork, copy-on-write)."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+        h = C.c_void_p()
+        order = None
+        if free_order is not None:
+            self._order = np.ascontiguousarray(free_order, dtype=np.int32)
+            if self._order.shape != (self.num_blocks,):
+                raise ValueError("free_order must list every block id once")
+            order = _i32(self._order)
+        _check(LIB.pa_bm_create(self.num_blocks, self.block_size, order, C.byref(h)), "pa_bm_create")
+        self._h = h
+
+    def close(self) -> None:
+        if self._h:
+            LIB.pa_bm_destroy(self._h)
+            self._h = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self):
+        return self._h
+
+    def add_seq(self, seq: int, num_tokens: int) -> np.ndarray:
+        slots = np.empty(max(int(num_tokens), 1), np.int32)
+        _check(LIB.pa_bm_add_seq(self._h, int(seq), int(num_tokens), _i32(slots)), "pa_bm_add_seq")
+        return slots[: int(num_tokens)]
+
+    def append(self, seq: int):
+        slot, src, dst = C.c_int32(), C.c_int32(), C.c_int32()
+        _check(LIB.pa_bm_append(self._h, int(seq), C.byref(slot), C.byref(src), C.byref(dst)), "pa_bm_append")
+        return slot.value, (None if src.value < 0 else (src.value, dst.value))
+
+    def step_into(self, ids: np.ndarray, slots_out: np.ndarray, copies_out: np.ndarray) -> int:
+        """One decode step; fills caller arrays, returns the number of copy pairs."""
+        nc = C.c_int32(0)
+        _check(LIB.pa_bm_step(self._h, _i64(ids), len(ids), _i32(slots_out), _i32(copies_out), C.byref(nc)),
+               "pa_bm_step")
+        return nc.value
+
+    def step(self, seqs):
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        slots = np.empty(max(len(ids), 1), np.int32)
+        copies = np.empty((max(len(ids), 1), 2), np.int32)
+        n = self.step_into(ids, slots, copies)
+        return slots[: len(ids)], copies[:n]
+
+    def fork(self, parent: int, child: int) -> None:
+        _check(LIB.pa_bm_fork(self._h, int(parent), int(child)), "pa_bm_fork")
+
+    def free(self, seq: int) -> int:
+        return _check(LIB.pa_bm_free(self._h, int(seq)), "pa_bm_free")
+
+    def block_tables_into(self, ids: np.ndarray, max_blocks: int, tables_out: np.ndarray, lens_out: np.ndarray):
+        _check(LIB.pa_bm_block_tables(self._h, _i64(ids), len(ids), int(max_blocks), _i32(tables_out),
+                                      _i32(lens_out)), "pa_bm_block_tables")
+
+    def block_tables(self, seqs, max_blocks: int):
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        tables = np.empty((max(len(ids), 1), max(int(max_blocks), 1)), np.int32)
+        lens = np.empty(max(len(ids), 1), np.int32)
+        self.block_tables_into(ids, max_blocks, tables, lens)
+        return tables[: len(ids), : int(max_blocks)], lens[: len(ids)]
+
+    def seq_info(self, seq: int):
+        L, nb = C.c_int32(), C.c_int32()
+        _check(LIB.pa_bm_seq_info(self._h, int(seq), C.byref(L), C.byref(nb)), "pa_bm_seq_info")
+        return L.value, nb.value
+
+    def table(self, seq: int) -> list:
+        _, nb = self.seq_info(seq)
+        out = np.empty(max(nb, 1), np.int32)
+        n = C.c_int32()
+        _check(LIB.pa_bm_table(self._h, int(seq), _i32(out), nb, C.byref(n)), "pa_bm_table")
+        return out[: n.value].tolist()
+
+    def slot(self, seq: int, pos: int) -> int:
+        s = C.c_int32()
+        _check(LIB.pa_bm_slot(self._h, int(seq), int(pos), C.byref(s)), "pa_bm_slot")
+        return s.value
+
+    @property
+    def num_free(self) -> int:
+        n = C.c_int32()
+        _check(LIB.pa_bm_num_free(self._h, C.byref(n)), "pa_bm_num_free")
+        return n.value
+
+    def free_list(self) -> list:
+        out = np.empty(self.num_blocks, np.int32)
+        n = C.c_int32()
+        _check(LIB.pa_bm_free_list(self._h, _i32(out), self.num_blocks, C.byref(n)), "pa_bm_free_list")
+        return out[: n.value].tolist()
+
+    def ref_counts(self) -> list:
+        out = np.empty(self.num_blocks, np.int32)
+        _check(LIB.pa_bm_ref_counts(self._h, _i32(out), self.num_blocks), "pa_bm_ref_counts")
+        return out.tolist()
+
+    @property
+    def num_seqs(self) -> int:
+        n = C.c_int32()
+        _check(LIB.pa_bm_num_seqs(self._h, C.byref(n)), "pa_bm_num_seqs")
+        return n.value

@@ -1,0 +1,435 @@
+// C ABI of libpa: argument validation, launch configuration, TMA descriptors,
+// the library-owned split workspace and the sticky device status word.
+// The operations themselves are specified in include/pa.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "decode_kernel.cuh"
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+// Sticky status word, one per device (each device holds its own copy of this
+// module's globals).  Kernels in other translation units receive its address.
+__device__ int32_t g_pa_status;
+
+constexpr int kMaxDevices = 64;
+
+std::atomic<int64_t> g_launches{0};
+
+struct DeviceState {
+  std::once_flag once;
+  int32_t* status = nullptr;
+  int num_sms = 0;
+  cudaError_t err = cudaSuccess;
+};
+DeviceState g_dev[kMaxDevices];
+
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return PA_ERR_CUDA;
+  DeviceState& d = g_dev[*dev];
+  std::call_once(d.once, [&] {
+    d.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_pa_status);
+    if (d.err == cudaSuccess) d.err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, *dev);
+  });
+  return d.err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// ---- TMA descriptor encoding (driver entry point, resolved once) -------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+// 3-D view [num_blocks*B, H, D] of a cache, box {D, hg, B}: one frame of hg heads.
+int make_cache_map(CUtensorMap* map, void* base, int dtype, int64_t nb, int64_t B, int64_t H, int64_t D, int hg) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return PA_ERR_CUDA;
+  CUtensorMapDataType t = dtype == PA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                          : dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int64_t e = dtype == PA_F32 ? 4 : 2;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(nb * B)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * e), static_cast<cuuint64_t>(H * D * e)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(hg), static_cast<cuuint32_t>(B)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, t, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
+}
+
+// ---- library-owned split workspace, one per (device, stream) ------------------------------
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+int workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
+  std::lock_guard<std::mutex> lk(g_ws_mu);
+  Workspace& w = g_ws[{dev, stream}];
+  if (w.bytes < bytes) {
+    if (w.ptr) {
+      // the old buffer may still be read by earlier launches on this stream
+      if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ERR_CUDA;
+      cudaFree(w.ptr);
+      w.ptr = nullptr;
+      w.bytes = 0;
+    }
+    const size_t grow = std::max(bytes, static_cast<size_t>(1) << 20);
+    if (cudaMalloc(&w.ptr, grow) != cudaSuccess) return PA_ERR_CUDA;
+    w.bytes = grow;
+  }
+  *out = w.ptr;
+  return PA_OK;
+}
+
+// ---- validation helpers ---------------------------------------------------------------------
+int elem_bytes(int dtype) { return dtype == PA_F32 || dtype == PA_I32 ? 4 : (dtype == PA_F16 || dtype == PA_BF16) ? 2 : 0; }
+bool is_float(int dtype) { return dtype == PA_F32 || dtype == PA_F16 || dtype == PA_BF16; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// [N, H, D] with the [H, D] part contiguous and a 16-byte-multiple row stride.
+int check_rows(const pa_tensor* t, int dtype, int64_t H, int64_t D) {
+  if (!t) return PA_ERR_INVALID;
+  if (t->dtype != dtype) return PA_ERR_DTYPE;
+  if (t->ndim != 3 || t->shape[1] != H || t->shape[2] != D || t->shape[0] < 0) return PA_ERR_SHAPE;
+  if (t->shape[0] == 0) return PA_OK;
+  if (!t->data) return PA_ERR_INVALID;
+  if (t->stride[2] != 1 || t->stride[1] != D || (t->shape[0] > 1 && t->stride[0] < H * D)) return PA_ERR_STRIDE;
+  if (!aligned16(t->data) || (t->stride[0] * elem_bytes(dtype)) % 16 != 0) return PA_ERR_ALIGN;
+  return PA_OK;
+}
+
+int check_cache(const pa_tensor* c, const pa_tensor* other) {
+  if (!c || !c->data) return PA_ERR_INVALID;
+  if (!is_float(c->dtype)) return PA_ERR_DTYPE;
+  if (c->ndim != 4) return PA_ERR_SHAPE;
+  for (int i = 0; i < 4; ++i)
+    if (c->shape[i] <= 0) return PA_ERR_SHAPE;
+  if (c->stride[3] != 1 || c->stride[2] != c->shape[3] || c->stride[1] != c->shape[2] * c->shape[3] ||
+      c->stride[0] != c->shape[1] * c->shape[2] * c->shape[3])
+    return PA_ERR_STRIDE;
+  if (!aligned16(c->data) || (c->shape[3] * elem_bytes(c->dtype)) % 16 != 0) return PA_ERR_ALIGN;
+  if (c->shape[0] * c->shape[1] > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (other) {
+    if (other->dtype != c->dtype) return PA_ERR_DTYPE;
+    for (int i = 0; i < 4; ++i)
+      if (other->shape[i] != c->shape[i]) return PA_ERR_SHAPE;
+  }
+  return PA_OK;
+}
+
+int check_i32(const pa_tensor* t, int ndim) {
+  if (!t || (!t->data && t->shape[0] > 0)) return PA_ERR_INVALID;
+  if (t->dtype != PA_I32) return PA_ERR_DTYPE;
+  if (t->ndim != ndim) return PA_ERR_SHAPE;
+  if (t->stride[ndim - 1] != 1) return PA_ERR_STRIDE;
+  return PA_OK;
+}
+
+#define PA_TRY(x)                  \
+  do {                             \
+    int _rc = (x);                 \
+    if (_rc != PA_OK) return _rc;  \
+  } while (0)
+
+int round_up(int64_t x, int64_t m) { return static_cast<int>(((x + m - 1) / m) * m); }
+
+cudaError_t dispatch_decode(const pa::DecodeArgs& a, const pa::DecodeCfg& c, const CUtensorMap& tk,
+                            const CUtensorMap& tv, cudaStream_t st, bool query_only, int* max_ctas) {
+  switch (c.dtype) {
+    case PA_F32: return pa::launch_decode_f32(a, c, tk, tv, st, query_only, max_ctas);
+    case PA_F16: return pa::launch_decode_f16(a, c, tk, tv, st, query_only, max_ctas);
+    case PA_BF16: return pa::launch_decode_bf16(a, c, tk, tv, st, query_only, max_ctas);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+bool combo_built(int hg, int wph) {
+  return (hg == 4 && (wph == 1 || wph == 2)) || (hg == 2 && (wph == 2 || wph == 4)) ||
+         (hg == 1 && (wph == 4 || wph == 8));
+}
+
+}  // namespace
+
+size_t pa::decode_smem_bytes(const DecodeCfg& c, int elem, int B, int S) {
+  const uint32_t stage_bytes = 2u * static_cast<uint32_t>(B) * c.heads_per_cta * c.D * elem;
+  const dk::Layout lay(c.stages, stage_bytes, S, c.heads_per_cta * c.warps_per_head, c.D);
+  return lay.total;
+}
+
+extern "C" {
+
+const char* pa_strerror(int code) {
+  switch (code) {
+    case PA_OK: return "ok";
+    case PA_WARN_DOUBLE_FREE: return "sequence not live (free was a no-op)";
+    case PA_ERR_INVALID: return "invalid argument";
+    case PA_ERR_DTYPE: return "unsupported or mismatched dtype";
+    case PA_ERR_SHAPE: return "bad shape";
+    case PA_ERR_STRIDE: return "bad stride (layout not supported)";
+    case PA_ERR_ALIGN: return "pointer or row stride not 16-byte aligned";
+    case PA_ERR_OUT_OF_BLOCKS: return "out of free blocks";
+    case PA_ERR_UNKNOWN_SEQ: return "unknown sequence id";
+    case PA_ERR_SEQ_EXISTS: return "sequence id already live";
+    case PA_ERR_CUDA: return "CUDA runtime error";
+    case PA_ERR_UNSUPPORTED: return "size or dtype outside the built kernels";
+    case PA_ERR_CAPACITY: return "output buffer too small";
+    default: return "unknown code";
+  }
+}
+
+int64_t pa_launch_count(void) { return g_launches.load(); }
+
+int pa_get_device_status(pa_stream stream, int32_t* status_out) {
+  if (!status_out) return PA_ERR_INVALID;
+  int dev;
+  PA_TRY(current_device(&dev));
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, g_dev[dev].status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaMemset(g_dev[dev].status, 0, sizeof(v)) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+  *status_out = v;
+  return PA_OK;
+}
+
+int pa_shutdown(void) {
+  std::lock_guard<std::mutex> lk(g_ws_mu);
+  int prev = -1;
+  cudaGetDevice(&prev);
+  for (auto& kv : g_ws) {
+    if (kv.second.ptr) {
+      cudaSetDevice(kv.first.first);
+      cudaFree(kv.second.ptr);
+    }
+  }
+  g_ws.clear();
+  if (prev >= 0) cudaSetDevice(prev);
+  return PA_OK;
+}
+
+int pa_cache_append(const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* slot_mapping,
+                    const pa_tensor* k_cache, const pa_tensor* v_cache, pa_stream stream) {
+  PA_TRY(check_cache(k_cache, v_cache));
+  const int dt = k_cache->dtype;
+  const int64_t H = k_cache->shape[2], D = k_cache->shape[3];
+  PA_TRY(check_rows(k_new, dt, H, D));
+  PA_TRY(check_rows(v_new, dt, H, D));
+  if (!slot_mapping) return PA_ERR_INVALID;
+  PA_TRY(check_i32(slot_mapping, 1));
+  const int64_t T = k_new->shape[0];
+  if (v_new->shape[0] != T || slot_mapping->shape[0] != T) return PA_ERR_SHAPE;
+  if (T > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (T == 0) return PA_OK;
+  int dev;
+  PA_TRY(current_device(&dev));
+  const int e = elem_bytes(dt);
+  pa::AppendArgs a;
+  a.k_new = static_cast<const unsigned char*>(k_new->data);
+  a.v_new = static_cast<const unsigned char*>(v_new->data);
+  a.k_pitch = k_new->stride[0] * e;
+  a.v_pitch = v_new->stride[0] * e;
+  a.slots = static_cast<const int32_t*>(slot_mapping->data);
+  a.k_cache = static_cast<unsigned char*>(k_cache->data);
+  a.v_cache = static_cast<unsigned char*>(v_cache->data);
+  a.row_bytes = H * D * e;
+  a.num_slots = k_cache->shape[0] * k_cache->shape[1];
+  a.T = static_cast<int32_t>(T);
+  a.status = g_dev[dev].status;
+  if (pa::launch_cache_append(a, g_dev[dev].num_sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return PA_OK;
+}
+
+int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_tensor* pairs, pa_stream stream) {
+  PA_TRY(check_cache(k_cache, v_cache));
+  if (!pairs) return PA_ERR_INVALID;
+  PA_TRY(check_i32(pairs, 2));
+  if (pairs->shape[1] != 2 || (pairs->shape[0] > 1 && pairs->stride[0] != 2)) return PA_ERR_SHAPE;
+  const int64_t n = pairs->shape[0];
+  if (n < 0 || n > INT32_MAX) return PA_ERR_SHAPE;
+  if (n == 0) return PA_OK;
+  int dev;
+  PA_TRY(current_device(&dev));
+  pa::CopyArgs a;
+  a.k_cache = static_cast<unsigned char*>(k_cache->data);
+  a.v_cache = static_cast<unsigned char*>(v_cache->data);
+  a.pairs = static_cast<const int32_t*>(pairs->data);
+  a.frame_bytes = k_cache->stride[0] * elem_bytes(k_cache->dtype);
+  a.n = static_cast<int32_t>(n);
+  a.num_blocks = static_cast<int32_t>(k_cache->shape[0]);
+  a.status = g_dev[dev].status;
+  if (pa::launch_copy_blocks(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return PA_OK;
+}
+
+int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                 const pa_tensor* block_tables, const pa_tensor* context_lens, float scale, const pa_tensor* out,
+                 const pa_decode_params* params, pa_stream stream) {
+  PA_TRY(check_cache(k_cache, v_cache));
+  const int dt = k_cache->dtype;
+  const int64_t nb = k_cache->shape[0], B = k_cache->shape[1], H = k_cache->shape[2], D = k_cache->shape[3];
+  PA_TRY(check_rows(q, dt, H, D));
+  PA_TRY(check_rows(out, dt, H, D));
+  if (!block_tables || !context_lens) return PA_ERR_INVALID;
+  PA_TRY(check_i32(block_tables, 2));
+  PA_TRY(check_i32(context_lens, 1));
+  const int64_t S = q->shape[0];
+  if (out->shape[0] != S || block_tables->shape[0] != S || context_lens->shape[0] != S) return PA_ERR_SHAPE;
+  const int64_t max_blocks = block_tables->shape[1];
+  if (max_blocks < 0 || (S > 1 && block_tables->stride[0] < max_blocks)) return PA_ERR_STRIDE;
+  if (B > 256) return PA_ERR_UNSUPPORTED;
+  if (!(D == 64 || D == 128 || (D == 256 && dt != PA_F32))) return PA_ERR_UNSUPPORTED;
+  if (max_blocks * B > INT32_MAX || S > 65536) return PA_ERR_UNSUPPORTED;
+  if (S == 0) return PA_OK;
+  if (max_blocks > 0 && !block_tables->data) return PA_ERR_INVALID;
+  pa_decode_params p;
+  std::memset(&p, 0, sizeof(p));
+  if (params) p = *params;
+  if (p.heads_per_cta < 0 || p.warps_per_head < 0 || p.stages < 0 || p.ctas_per_sm < 0) return PA_ERR_INVALID;
+
+  int dev;
+  PA_TRY(current_device(&dev));
+  const int e = elem_bytes(dt);
+
+  // ---- launch configuration -------------------------------------------------------------
+  pa::DecodeCfg c;
+  c.dtype = dt;
+  c.D = static_cast<int>(D);
+  if (p.heads_per_cta) {
+    if (!(p.heads_per_cta == 1 || p.heads_per_cta == 2 || p.heads_per_cta == 4) || H % p.heads_per_cta != 0)
+      return PA_ERR_INVALID;
+    c.heads_per_cta = p.heads_per_cta;
+  } else {
+    c.heads_per_cta = 1;
+    for (int hg : {4, 2}) {
+      if (H % hg == 0 && 2 * B * hg * D * e <= 32768) {
+        c.heads_per_cta = hg;
+        break;
+      }
+    }
+  }
+  c.warps_per_head = p.warps_per_head ? p.warps_per_head : 8 / c.heads_per_cta;
+  if (!combo_built(c.heads_per_cta, c.warps_per_head)) return PA_ERR_INVALID;
+  const int64_t stage_bytes = 2 * B * c.heads_per_cta * D * e;
+  c.stages = 1;
+  const size_t smem_cap = 227 * 1024;
+  if (p.stages) {
+    if (p.stages < 2 || p.stages > 8) return PA_ERR_INVALID;
+    c.stages = p.stages;
+  } else {
+    // two resident blocks per SM when the staging ring still holds >= 3 frames
+    for (int st = 8; st >= 2; --st) {
+      c.stages = st;
+      if (pa::decode_smem_bytes(c, e, static_cast<int>(B), static_cast<int>(S)) <= smem_cap / 2 - 1024 && st >= 3)
+        break;
+      c.stages = 0;
+    }
+    if (c.stages == 0) {
+      for (int st = 8; st >= 2; --st) {
+        c.stages = st;
+        if (pa::decode_smem_bytes(c, e, static_cast<int>(B), static_cast<int>(S)) <= smem_cap) break;
+        c.stages = 0;
+      }
+    }
+    if (c.stages == 0) return PA_ERR_UNSUPPORTED;
+  }
+  if (pa::decode_smem_bytes(c, e, static_cast<int>(B), static_cast<int>(S)) > smem_cap) return PA_ERR_UNSUPPORTED;
+  (void)stage_bytes;
+
+  pa::DecodeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = q->data;
+  a.out = out->data;
+  a.q_row = q->stride[0];
+  a.out_row = out->stride[0];
+  a.block_tables = static_cast<const int32_t*>(block_tables->data);
+  a.bt_row = block_tables->stride[0];
+  a.context_lens = static_cast<const int32_t*>(context_lens->data);
+  a.S = static_cast<int32_t>(S);
+  a.H = static_cast<int32_t>(H);
+  a.B = static_cast<int32_t>(B);
+  a.num_blocks = static_cast<int32_t>(nb);
+  a.max_blocks = static_cast<int32_t>(max_blocks);
+  a.G = static_cast<int32_t>(H / c.heads_per_cta);
+  a.qk_scale_log2 = scale * 1.4426950408889634f;
+  a.status = g_dev[dev].status;
+
+  CUtensorMap tk, tv;
+  PA_TRY(make_cache_map(&tk, k_cache->data, dt, nb, B, H, D, c.heads_per_cta));
+  PA_TRY(make_cache_map(&tv, v_cache->data, dt, nb, B, H, D, c.heads_per_cta));
+
+  int occ = 0;
+  if (dispatch_decode(a, c, tk, tv, nullptr, true, &occ) != cudaSuccess || occ <= 0) return PA_ERR_CUDA;
+  const int cps = p.ctas_per_sm ? std::min(p.ctas_per_sm, occ) : occ;
+  c.grid = g_dev[dev].num_sms * cps;
+
+  // ---- partitioning and workspace --------------------------------------------------------
+  const int64_t Lcap = max_blocks * B;
+  int64_t items_max = 0;
+  if (p.partition_tokens == -1 || Lcap == 0) {
+    a.fixed_part = static_cast<int32_t>(std::max<int64_t>(Lcap, B));
+  } else if (p.partition_tokens > 0) {
+    a.fixed_part = round_up(p.partition_tokens, B);
+    if (a.fixed_part < Lcap) items_max = S * a.G * ((Lcap + a.fixed_part - 1) / a.fixed_part);
+  } else if (p.partition_tokens == 0) {
+    a.fixed_part = 0;
+    a.target_items = 4 * c.grid;
+    a.min_part = round_up(256, B);
+    if (a.min_part < Lcap)
+      items_max = std::min<int64_t>(S * a.G * ((Lcap + a.min_part - 1) / a.min_part), a.target_items + S * a.G);
+  } else {
+    return PA_ERR_INVALID;
+  }
+  if (items_max > 0) {
+    const size_t ml_bytes = static_cast<size_t>(items_max) * c.heads_per_cta * 2 * sizeof(float);
+    const size_t o_bytes = static_cast<size_t>(items_max) * c.heads_per_cta * D * sizeof(float);
+    const size_t off_bytes = static_cast<size_t>(S + 2) * sizeof(int32_t);
+    void* ws = nullptr;
+    PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), o_bytes + ml_bytes + off_bytes + 256, &ws));
+    unsigned char* w = static_cast<unsigned char*>(ws);
+    a.ws_o = reinterpret_cast<float*>(w);
+    a.ws_ml = reinterpret_cast<float*>(w + o_bytes);
+    a.ws_off = reinterpret_cast<int32_t*>(w + o_bytes + ml_bytes);
+  }
+
+  if (dispatch_decode(a, c, tk, tv, static_cast<cudaStream_t>(stream), false, nullptr) != cudaSuccess)
+    return PA_ERR_CUDA;
+  g_launches.fetch_add(a.ws_off ? 2 : 1);
+  return PA_OK;
+}
+
+int pa_decode(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_tensor* block_tables,
+              const pa_tensor* context_lens, float scale, const pa_tensor* out, pa_stream stream) {
+  return pa_decode_ex(q, k_cache, v_cache, block_tables, context_lens, scale, out, nullptr, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// Cache append (scatter of new K/V rows into their slots) and whole-frame copies
+// for copy-on-write.
+//
+// "Solving the LLM Memory Wall" ("Implementation", PagedKVCache.update): a token's
+// k and v rows are written at [frame, offset]; batched here over all new tokens
+// of a step through a slot mapping (slot = frame * B + offset).
+// "PagedAttention: Virtual Memory Guide for LLM Inference" ("2. Zero-Copy
+// Branching via Copy-on-Write"): only the single shared frame being written is
+// duplicated.
+//
+// Both are pure data movement: 16-byte vector loads and stores, one thread block
+// per token row (append) or per slice of a frame (copy), 64-bit byte offsets.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+__global__ void __launch_bounds__(256) cache_append_kernel(const AppendArgs a) {
+  const int64_t nvec = a.row_bytes >> 4;
+  for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+    const int32_t slot = __ldg(a.slots + t);
+    if (slot < 0) continue;  // padding
+    if (slot >= a.num_slots) {
+      if (threadIdx.x == 0) atomicOr(a.status, kDevBadSlot);
+      continue;
+    }
+    const uint4* ks = reinterpret_cast<const uint4*>(a.k_new + static_cast<int64_t>(t) * a.k_pitch);
+    const uint4* vs = reinterpret_cast<const uint4*>(a.v_new + static_cast<int64_t>(t) * a.v_pitch);
+    uint4* kd = reinterpret_cast<uint4*>(a.k_cache + static_cast<int64_t>(slot) * a.row_bytes);
+    uint4* vd = reinterpret_cast<uint4*>(a.v_cache + static_cast<int64_t>(slot) * a.row_bytes);
+    for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+      const uint4 kv = __ldg(ks + i);
+      const uint4 vv = __ldg(vs + i);
+      kd[i] = kv;
+      vd[i] = vv;
+    }
+  }
+}
+
+// grid.x = pair, grid.y = slice of the frame, grid.z = 0 (K) / 1 (V)
+__global__ void __launch_bounds__(256) copy_blocks_kernel(const CopyArgs a, const int64_t slice_vecs) {
+  const int pair = blockIdx.x;
+  const int32_t src = __ldg(a.pairs + 2 * pair);
+  const int32_t dst = __ldg(a.pairs + 2 * pair + 1);
+  if (src < 0 || src >= a.num_blocks || dst < 0 || dst >= a.num_blocks) {
+    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) atomicOr(a.status, kDevBadCopy);
+    return;
+  }
+  unsigned char* base = blockIdx.z == 0 ? a.k_cache : a.v_cache;
+  const uint4* s = reinterpret_cast<const uint4*>(base + static_cast<int64_t>(src) * a.frame_bytes);
+  uint4* d = reinterpret_cast<uint4*>(base + static_cast<int64_t>(dst) * a.frame_bytes);
+  const int64_t nvec = a.frame_bytes >> 4;
+  const int64_t lo = static_cast<int64_t>(blockIdx.y) * slice_vecs;
+  const int64_t hi = lo + slice_vecs < nvec ? lo + slice_vecs : nvec;
+  for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) d[i] = s[i];
+}
+
+}  // namespace
+
+cudaError_t launch_cache_append(const AppendArgs& a, int num_sms, cudaStream_t stream) {
+  if (a.T <= 0) return cudaSuccess;
+  const int64_t nvec = a.row_bytes >> 4;
+  const int threads = nvec >= 256 ? 256 : static_cast<int>(((nvec + 31) / 32) * 32);
+  const int max_grid = num_sms * 16;
+  const int grid = a.T < max_grid ? a.T : max_grid;
+  cache_append_kernel<<<grid, threads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream) {
+  if (a.n <= 0) return cudaSuccess;
+  const int64_t nvec = a.frame_bytes >> 4;
+  const int64_t slice_vecs = 1024;  // 16 KiB per thread block
+  const int64_t slices = (nvec + slice_vecs - 1) / slice_vecs;
+  dim3 grid(a.n, static_cast<unsigned>(slices), 2);
+  copy_blocks_kernel<<<grid, 256, 0, stream>>>(a, slice_vecs);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,89 @@
+// Internal declarations shared by the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace pa {
+
+// ---- cache append / frame copy ---------------------------------------------------------
+struct AppendArgs {
+  const unsigned char* k_new;   // [T, row_bytes] with row pitch k_pitch
+  const unsigned char* v_new;
+  int64_t k_pitch, v_pitch;     // bytes between token rows
+  const int32_t* slots;         // [T]
+  unsigned char* k_cache;       // [num_slots, row_bytes]
+  unsigned char* v_cache;
+  int64_t row_bytes;            // H * D * elem (multiple of 16)
+  int64_t num_slots;            // num_blocks * B
+  int32_t T;
+  int32_t* status;
+};
+cudaError_t launch_cache_append(const AppendArgs& a, int num_sms, cudaStream_t stream);
+
+struct CopyArgs {
+  unsigned char* k_cache;
+  unsigned char* v_cache;
+  const int32_t* pairs;         // [n, 2]
+  int64_t frame_bytes;          // B * H * D * elem (multiple of 16)
+  int32_t n;
+  int32_t num_blocks;
+  int32_t* status;
+};
+cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream);
+
+// ---- decode ------------------------------------------------------------------------------
+struct DecodeArgs {
+  const void* q;                // [S, H, D], row stride q_row elements
+  void* out;                    // [S, H, D], row stride out_row elements
+  int64_t q_row, out_row;
+  const int32_t* block_tables;  // [S, max_blocks], row stride bt_row
+  int64_t bt_row;
+  const int32_t* context_lens;  // [S]
+  int32_t S, H, B, num_blocks, max_blocks;
+  int32_t G;                    // head groups per sequence = H / heads_per_cta
+  float qk_scale_log2;          // scale * log2(e)
+  // partitioning: fixed_part > 0 forces that many tokens per partition (multiple of
+  // B); otherwise partition length is chosen on the device from the lengths so that
+  // the work splits into about target_items items, never shorter than min_part.
+  int32_t fixed_part;
+  int32_t target_items;
+  int32_t min_part;
+  // split workspace (null when no sequence can be split)
+  float* ws_ml;                 // [items][HG][2] = (running max in log2 units, sum)
+  float* ws_o;                  // [items][HG][D] unnormalised partial outputs
+  int32_t* ws_off;              // [S + 2]: item offset per sequence, then the partition length
+  int32_t* status;
+};
+
+struct DecodeCfg {
+  int dtype;         // PA_F32 / PA_F16 / PA_BF16
+  int D;
+  int heads_per_cta;
+  int warps_per_head;
+  int stages;
+  int grid;          // persistent thread blocks
+};
+
+// per-dtype launchers (one translation unit each).  query_only: set the kernel's
+// shared-memory attribute and report resident blocks per SM in *max_ctas instead
+// of launching.
+cudaError_t launch_decode_f32(const DecodeArgs&, const DecodeCfg&, const CUtensorMap&, const CUtensorMap&,
+                              cudaStream_t, bool query_only, int* max_ctas);
+cudaError_t launch_decode_f16(const DecodeArgs&, const DecodeCfg&, const CUtensorMap&, const CUtensorMap&,
+                              cudaStream_t, bool query_only, int* max_ctas);
+cudaError_t launch_decode_bf16(const DecodeArgs&, const DecodeCfg&, const CUtensorMap&, const CUtensorMap&,
+                               cudaStream_t, bool query_only, int* max_ctas);
+// Dynamic shared memory of one decode thread block (mirrors the kernel's layout).
+size_t decode_smem_bytes(const DecodeCfg& c, int elem_bytes, int B, int S);
+
+// status bits (mirror pa.h)
+constexpr int32_t kDevBadSlot = 0x1;
+constexpr int32_t kDevBadBlock = 0x2;
+constexpr int32_t kDevBadLen = 0x4;
+constexpr int32_t kDevBadCopy = 0x8;
+constexpr int32_t kDevTimeout = 0x10;
+
+}  // namespace pa

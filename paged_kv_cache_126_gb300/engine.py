@@ -1,0 +1,195 @@
+"""PagedKVEngine: one device's paged K/V caches driven by libpa.
+
+The engine owns the two caches [num_blocks, B, H, D] (torch device memory) and a
+libpa host block manager.  A decode step is
+
+    host:   pa_bm_step (slots + copy-on-write pairs, in batch order)
+            pa_bm_block_tables (tables + context lengths)
+            -> one pinned staging buffer -> one async host-to-device copy
+    device: pa_copy_blocks (only if a shared tail was written)
+            pa_cache_append (the step's new K/V rows)
+            pa_decode (+ its merge kernel when a context is split)
+
+all on one stream.  Staging buffers form a ring guarded by CUDA events so the
+host can prepare step k+1 while the device still runs step k.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from ._binding import (
+    BlockManager,
+    pa_cache_append,
+    pa_copy_blocks,
+    pa_decode,
+)
+
+TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def to_device_rows(rows, dtype: str, device) -> torch.Tensor:
+    """[n, H, D] rows -> device tensor; NumPy bf16 arrives as uint16 bit patterns."""
+    if isinstance(rows, torch.Tensor):
+        return rows.to(device=device, dtype=TORCH_DTYPES[dtype], non_blocking=True)
+    a = np.ascontiguousarray(rows)
+    t = torch.from_numpy(a)
+    if dtype == "bf16":
+        t = t.view(torch.int16).view(torch.bfloat16) if a.dtype == np.uint16 else t.to(torch.bfloat16)
+    else:
+        t = t.to(TORCH_DTYPES[dtype])
+    return t.to(device)
+
+
+class PagedKVEngine:
+    def __init__(self, num_blocks: int, block_size: int, num_heads: int, head_dim: int, dtype: str = "f16", *,
+                 free_order=None, device=None, max_seqs: int = 256, max_blocks_per_seq: int | None = None,
+                 ring: int = 4, stream: torch.cuda.Stream | None = None):
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.num_blocks, self.B, self.H, self.D = int(num_blocks), int(block_size), int(num_heads), int(head_dim)
+        self.dtype = dtype
+        self.bm = BlockManager(num_blocks, block_size, free_order)
+        shape = (self.num_blocks, self.B, self.H, self.D)
+        self.k_cache = torch.zeros(shape, dtype=TORCH_DTYPES[dtype], device=self.device)
+        self.v_cache = torch.zeros(shape, dtype=TORCH_DTYPES[dtype], device=self.device)
+        self.max_blocks = int(max_blocks_per_seq or num_blocks)
+        self.max_seqs = int(max_seqs)
+        self.stream = stream
+        cap = self.max_seqs * (self.max_blocks + 4) + 64
+        self._pin = [torch.empty(cap, dtype=torch.int32, pin_memory=True) for _ in range(ring)]
+        self._pin_np = [p.numpy() for p in self._pin]
+        self._dev = torch.empty(cap, dtype=torch.int32, device=self.device)
+        self._events = [None] * ring
+        self._k = 0
+        self._ids_key = None
+        self._ids = None
+
+    # -- helpers ----------------------------------------------------------------------------
+    def _stream(self):
+        return self.stream if self.stream is not None else torch.cuda.current_stream(self.device)
+
+    def _ids_for(self, seqs) -> np.ndarray:
+        key = tuple(seqs) if not isinstance(seqs, np.ndarray) else None
+        if key is not None and key == self._ids_key:
+            return self._ids
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        if key is not None:
+            self._ids_key, self._ids = key, ids
+        return ids
+
+    def _stage(self):
+        """Next pinned staging buffer, once the copy that last read it has run."""
+        i = self._k % len(self._pin)
+        self._k += 1
+        ev = self._events[i]
+        if ev is not None:
+            ev.synchronize()
+        return i
+
+    def _upload(self, i: int, n: int) -> torch.Tensor:
+        st = self._stream()
+        with torch.cuda.stream(st):
+            self._dev[:n].copy_(self._pin[i][:n], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(st)
+        self._events[i] = ev
+        return self._dev
+
+    # -- sequence operations -------------------------------------------------------------------
+    def add_seq(self, seq: int, k_rows, v_rows) -> np.ndarray:
+        """New sequence with a prompt; writes its K/V rows. Returns the slots."""
+        k = to_device_rows(k_rows, self.dtype, self.device)
+        v = to_device_rows(v_rows, self.dtype, self.device)
+        slots = self.bm.add_seq(seq, k.shape[0])
+        if len(slots):
+            sd = torch.from_numpy(slots).to(self.device)
+            pa_cache_append(k, v, sd, self.k_cache, self.v_cache, stream=self._stream())
+        return slots
+
+    def fork(self, parent: int, child: int) -> None:
+        self.bm.fork(parent, child)
+
+    def free(self, seq: int) -> int:
+        return self.bm.free(seq)
+
+    def step(self, seqs, k_rows, v_rows):
+        """Append one token to each of seqs (batch order). Returns (slots, copies)."""
+        ids = self._ids_for(seqs)
+        n = len(ids)
+        i = self._stage()
+        buf = self._pin_np[i]
+        slots, copies = buf[:n], buf[n:3 * n].reshape(n, 2)
+        nc = self.bm.step_into(ids, slots, copies)
+        out_slots, out_copies = slots.copy(), copies[:nc].copy()
+        dev = self._upload(i, 3 * n)
+        st = self._stream()
+        if nc:
+            pa_copy_blocks(self.k_cache, self.v_cache, dev[n:n + 2 * nc].view(nc, 2), stream=st)
+        k = to_device_rows(k_rows, self.dtype, self.device)
+        v = to_device_rows(v_rows, self.dtype, self.device)
+        pa_cache_append(k, v, dev[:n], self.k_cache, self.v_cache, stream=st)
+        return out_slots, out_copies
+
+    def attend(self, seqs, q, scale: float, out=None, params=None) -> torch.Tensor:
+        """Decode attention for seqs with queries q [n, H, D]."""
+        ids = self._ids_for(seqs)
+        n = len(ids)
+        q = to_device_rows(q, self.dtype, self.device)
+        if out is None:
+            out = torch.empty_like(q)
+        i = self._stage()
+        buf = self._pin_np[i]
+        lens, tables = buf[:n], buf[n:n + n * self.max_blocks].reshape(n, self.max_blocks)
+        self.bm.block_tables_into(ids, self.max_blocks, tables, lens)
+        dev = self._upload(i, n + n * self.max_blocks)
+        pa_decode(q, self.k_cache, self.v_cache, dev[n:n + n * self.max_blocks].view(n, self.max_blocks),
+                  dev[:n], scale, out, stream=self._stream(), params=params)
+        return out
+
+    def decode_step(self, seqs, k_rows, v_rows, q, scale: float, out=None, params=None):
+        """append + attend with one staged upload: the whole hot path of one step."""
+        ids = self._ids_for(seqs)
+        n = len(ids)
+        mb = self.max_blocks
+        i = self._stage()
+        buf = self._pin_np[i]
+        slots, copies = buf[:n], buf[n:3 * n].reshape(n, 2)
+        lens = buf[3 * n:4 * n]
+        tables = buf[4 * n:4 * n + n * mb].reshape(n, mb)
+        nc = self.bm.step_into(ids, slots, copies)
+        self.bm.block_tables_into(ids, mb, tables, lens)
+        dev = self._upload(i, 4 * n + n * mb)
+        st = self._stream()
+        if nc:
+            pa_copy_blocks(self.k_cache, self.v_cache, dev[n:n + 2 * nc].view(nc, 2), stream=st)
+        pa_cache_append(k_rows, v_rows, dev[:n], self.k_cache, self.v_cache, stream=st)
+        if out is None:
+            out = torch.empty_like(q)
+        pa_decode(q, self.k_cache, self.v_cache, dev[4 * n:4 * n + n * mb].view(n, mb), dev[3 * n:4 * n],
+                  scale, out, stream=st, params=params)
+        return out, nc
+
+
+def run_workload_ops(engine: PagedKVEngine, w, attend_params=None):
+    """Replay a workload op list through the engine. Returns {attend op index: out}."""
+    outs = {}
+    trace = {}
+    for i, op in enumerate(w.ops):
+        kind = op[0]
+        if kind == "add":
+            k, v = w.rows(i)
+            trace[i] = {"slots": engine.add_seq(op[1], k, v).tolist(), "copies": []}
+        elif kind == "fork":
+            engine.fork(op[1], op[2])
+        elif kind == "step":
+            k, v = w.rows(i)
+            slots, copies = engine.step(op[1], k, v)
+            trace[i] = {"slots": slots.tolist(), "copies": [tuple(c) for c in copies.tolist()]}
+        elif kind == "free":
+            engine.free(op[1])
+        elif kind == "attend":
+            outs[i] = engine.attend(op[1], w.query(i), w.scale, params=attend_params)
+        else:
+            raise ValueError(op)
+    return outs, trace

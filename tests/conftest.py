@@ -1,3 +1,4 @@
+import importlib.util
 import os
 import sys
 
@@ -8,6 +9,14 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def _build_module():
+    spec = importlib.util.spec_from_file_location(
+        "_pa_build", os.path.join(ROOT, "paged_kv_cache_126_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
 
 
 def pytest_configure(config):
@@ -23,3 +32,11 @@ def golden():
         with open(os.path.join(GOLDEN, name)) as f:
             return json.load(f)
     return load
+
+
+@pytest.fixture(scope="session")
+def pa():
+    """The product package (builds libpa.so first if it is missing or stale)."""
+    _build_module().build()
+    import paged_kv_cache_126_gb300 as pkg
+    return pkg

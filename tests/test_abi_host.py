@@ -1,0 +1,179 @@
+"""C-ABI library checks that need no GPU (CPU only).
+
+* libpa.so loads and exports every function include/pa.h declares.
+* The C++ host block manager matches the oracle block manager bit for bit:
+  tables, lengths, free-list order, reference counts, slots and copy pairs, on
+  the pages' traces and on seeded random operation sequences.
+* Error behaviour: all-or-nothing steps and prompts, unknown / duplicate ids,
+  double free, bad arguments.
+"""
+
+import os
+import random
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+from oracle import DOUBLE_FREE, OracleBlockManager, OutOfBlocks, SequenceExists, UnknownSequence
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "pa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(pa):
+    names = _declared()
+    assert len(names) >= 20
+    nm = subprocess.run(["nm", "-D", "--defined-only", pa.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\b[TW] (pa_[a-z0-9_]+)$", nm, flags=re.M))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(pa.LIB, n)
+    assert sorted(pa.EXPORTED) == names
+
+
+def test_strerror_and_launch_count(pa):
+    assert pa.pa_strerror(0) == "ok"
+    assert "free blocks" in pa.pa_strerror(-6)
+    assert pa.pa_launch_count() >= 0
+
+
+# ------------------------------------------------------------------------------- parity
+def _same_state(bm, ob):
+    assert bm.num_free == ob.free_count
+    assert bm.free_list() == list(ob.free_list)
+    assert bm.ref_counts() == ob.refs
+    assert bm.num_seqs == len(ob.tables)
+    for s, t in ob.tables.items():
+        assert bm.table(s) == t
+        assert bm.seq_info(s) == (ob.lens[s], len(t))
+
+
+def test_worked_trace_bit_exact(pa, golden):
+    g = golden("worked_allocation_trace.json")
+    bm = pa.BlockManager(g["num_blocks"], g["block_size"])
+    ob = OracleBlockManager(g["num_blocks"], g["block_size"])
+    for i, name in enumerate(g["order"]):
+        assert bm.add_seq(i, g["prefill"][name]).tolist() == ob.add_seq(i, g["prefill"][name])
+    _same_state(bm, ob)
+    for _ in g["steps"]:
+        slots, copies = bm.step([0, 1, 2, 3])
+        oslots, ocopies = ob.step([0, 1, 2, 3])
+        assert slots.tolist() == oslots and copies.tolist() == [list(c) for c in ocopies]
+        _same_state(bm, ob)
+    assert {n: bm.table(i) for i, n in enumerate(g["order"])} == g["steps"][-1]["tables"]
+
+
+def test_cow_trace_bit_exact(pa, golden):
+    g = golden("cow_trace.json")
+    e = g["expect"]
+    bm = pa.BlockManager(g["num_blocks"], g["block_size"])
+    bm.add_seq(0, g["prompt"])
+    bm.fork(0, 1)
+    slot, cp = bm.append(0)
+    assert slot == e["append_alpha"]["slot"] and list(cp) == e["append_alpha"]["copy"]
+    assert bm.table(0) == e["append_alpha"]["alpha"] and bm.table(1) == e["append_alpha"]["beta"]
+    slot, cp = bm.append(1)
+    assert slot == e["append_beta"]["slot"] and cp is None
+    bm.free(0)
+    bm.free(1)
+    assert bm.free_list()[-3:] == e["free_tail_after_both"]
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_ops_bit_exact(pa, seed):
+    rnd = random.Random(1000 + seed)
+    B = rnd.choice([1, 2, 4, 10, 16, 32])
+    n = rnd.randint(8, 80)
+    order = rnd.sample(range(n), n)
+    bm = pa.BlockManager(n, B, order)
+    ob = OracleBlockManager(n, B, order)
+    next_id = 0
+    for _ in range(500):
+        r = rnd.random()
+        live = list(ob.tables)
+        if r < 0.2 or not live:
+            L = rnd.randint(0, 3 * B)
+            try:
+                want = ob.add_seq(next_id, L)
+            except OutOfBlocks:
+                with pytest.raises(pa.PAError) as ei:
+                    bm.add_seq(next_id, L)
+                assert ei.value.code == pa.PA_ERR_OUT_OF_BLOCKS
+            else:
+                assert bm.add_seq(next_id, L).tolist() == want
+            next_id += 1
+        elif r < 0.35:
+            p = rnd.choice(live)
+            ob.fork(p, next_id)
+            bm.fork(p, next_id)
+            next_id += 1
+        elif r < 0.45:
+            s = rnd.choice(live + [10 ** 6])
+            want = ob.free(s)
+            got = bm.free(s)
+            assert (got == pa.PA_WARN_DOUBLE_FREE) == (want == DOUBLE_FREE)
+        else:
+            seqs = [rnd.choice(live) for _ in range(rnd.randint(1, 5))]  # repeats allowed
+            try:
+                want = ob.step(seqs)
+            except OutOfBlocks:
+                with pytest.raises(pa.PAError) as ei:
+                    bm.step(seqs)
+                assert ei.value.code == pa.PA_ERR_OUT_OF_BLOCKS
+            else:
+                slots, copies = bm.step(seqs)
+                assert slots.tolist() == want[0]
+                assert [tuple(c) for c in copies.tolist()] == want[1]
+        _same_state(bm, ob)
+        for s in ob.tables:
+            if ob.lens[s]:
+                i = rnd.randrange(ob.lens[s])
+                assert bm.slot(s, i) == ob.slot(s, i)
+
+
+def test_block_tables_export(pa):
+    bm = pa.BlockManager(16, 4, list(range(15, -1, -1)))
+    bm.add_seq(7, 9)
+    bm.add_seq(3, 0)
+    tables, lens = bm.block_tables([7, 3], 5)
+    assert tables.tolist() == [[15, 14, 13, -1, -1], [-1] * 5]
+    assert lens.tolist() == [9, 0]
+    with pytest.raises(pa.PAError):
+        bm.block_tables([7], 2)                 # table longer than max_blocks
+
+
+def test_errors_leave_state_unchanged(pa):
+    bm = pa.BlockManager(3, 2)
+    bm.add_seq(0, 2)
+    bm.add_seq(1, 2)
+    before = (bm.free_list(), bm.ref_counts(), bm.table(0), bm.table(1))
+    with pytest.raises(pa.PAError) as ei:
+        bm.step([0, 1])                         # second spill has no frame left
+    assert ei.value.code == pa.PA_ERR_OUT_OF_BLOCKS
+    assert (bm.free_list(), bm.ref_counts(), bm.table(0), bm.table(1)) == before
+    with pytest.raises(pa.PAError) as ei:
+        bm.step([0, 99])
+    assert ei.value.code == pa.PA_ERR_UNKNOWN_SEQ
+    assert (bm.free_list(), bm.ref_counts(), bm.table(0), bm.table(1)) == before
+    with pytest.raises(pa.PAError) as ei:
+        bm.add_seq(0, 1)
+    assert ei.value.code == pa.PA_ERR_SEQ_EXISTS
+    with pytest.raises(pa.PAError):
+        bm.add_seq(5, 7)                        # needs 4 frames, 1 free
+    assert (bm.free_list(), bm.ref_counts()) == before[:2]
+    with pytest.raises(pa.PAError):
+        bm.fork(42, 43)
+    with pytest.raises(pa.PAError):
+        pa.BlockManager(4, 2, [0, 1, 1, 2])     # not a permutation
+    with pytest.raises(pa.PAError):
+        pa.BlockManager(0, 2)
+    assert bm.free(0) == 0
+    assert bm.free(0) == pa.PA_WARN_DOUBLE_FREE
