@@ -1,0 +1,516 @@
+#!/usr/bin/env python
+"""Benchmark of the paged decode hot path on GB300.
+
+One step = one decode step of a 64-sequence batch through libpa: host block
+manager step (slots, copy-on-write pairs, block tables) -> one staged upload ->
+pa_cache_append of the 64 new K/V rows -> pa_decode (+ merge).  The workload is
+the decode batch of 64 sequences with context lengths ~U[512, 2048], 32 heads,
+head_dim 128, block_size 16, fp16 K/V/q, physical frames handed out in shuffled
+order from a pool 1.2x the need.
+
+The bench keeps R independent copies of that batch resident and decodes them in
+rotation, so every step reads a different ~1.3 GB batch (far beyond the 129 MB
+L2: no flush needed) and each batch's lengths drift only K/R tokens over the run;
+prefill lengths are centred so that the mean attended length over the timed
+steps equals the sampled length.
+
+Printed: one JSON line (rank 0) with the throughput of the whole step (value),
+the decode op's roofline figure, the end-to-end figure through host buffers,
+the oracle's CPU baseline, launch count and SM clocks sampled during the timed
+region.  ``--impl reference`` times the CPU oracle instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: KV bytes GB/s (% of GB300 HBM peak); seqs/sec at 64×2k"
+UNIT = "GB/s"
+
+
+def algorithmic_bytes(lens, H, D, B, e_kv, e_q=None, e_out=None) -> int:
+    """K and V rows of every attended token, the block-table entries read, the
+    context lengths, q and out.  Tail padding of the last frame and split
+    workspace traffic are not counted."""
+    e_q = e_kv if e_q is None else e_q
+    e_out = e_kv if e_out is None else e_out
+    total = 0
+    for L in lens:
+        L = int(L)
+        total += 2 * L * H * D * e_kv + 4 * (-(-L // B))
+    S = len(lens)
+    return total + 4 * S + S * H * D * (e_q + e_out)
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return 6800.0, "fallback (6.8 TB/s)"
+
+
+def _kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("decode_kernel.cuh", "api.cu"):
+        with open(os.path.join(ROOT, "paged_kv_cache_126_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def _profile_traffic(workload_key: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_kernel_decode_batch_64.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m_src = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", txt)
+    m_tr = re.search(rf"traffic_bytes_per_launch\[{re.escape(workload_key)}\]:\s*([0-9.eE+]+)", txt)
+    if not m_src or not m_tr or m_src.group(1) != _kernel_source_hash():
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
+        self.gpu, self.interval, self.proc, self.out = str(gpu_index), interval_ms, None, ""
+        try:  # the CUDA ordinal need not match nvidia-smi's index; the UUID does
+            import torch
+            self.gpu = "GPU-" + str(torch.cuda.get_device_properties(gpu_index).uuid)
+        except Exception:
+            pass
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 f"-lms={self.interval}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)  # let the first sample land before the timed region
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def _oracle_sample(cfg, n_seqs, seed_shift=0):
+    """A few sequences of the bench workload with host data, replayed by the oracle."""
+    import numpy as np
+
+    import workloads
+    from oracle import replay
+
+    w = workloads.build(cfg)
+    rng = np.random.default_rng(99 + seed_shift)
+    keep = sorted(rng.choice(len(w.final_lens), n_seqs, replace=False).tolist())
+    ref = replay(w, keep_seqs=keep, with_cache=True)
+    op = w.attend_ops[-1]
+    q = w.query(op)
+    tables, lens = ref.attend_meta[op]
+    return w, ref, keep, q[keep], [tables[j] for j in keep], [lens[j] for j in keep]
+
+
+def cpu_baseline_worker(cfg, budget_s: float, per_step: bool = False, steps: int = 0):
+    """Time the oracle's paged decode (gather + fp64 softmax attention) on host cores."""
+    from oracle import paged_decode
+
+    w, ref, keep, q, tables, lens = _oracle_sample(cfg, 4 if not per_step else 8)
+    bytes_per_seq = [algorithmic_bytes([L], w.num_heads, w.head_dim, w.block_size, w.elem_bytes) for L in lens]
+    if per_step:
+        times, byts = [], []
+        for k in range(steps):
+            j = k % len(keep)
+            t0 = time.perf_counter()
+            paged_decode(q[j:j + 1], ref.cache, [tables[j]], [lens[j]], w.scale)
+            times.append(time.perf_counter() - t0)
+            byts.append(bytes_per_seq[j])
+        return {"times": times, "bytes": byts, "sample": f"1 of {len(keep)} sampled sequences per step "
+                                                         f"(lengths {lens}), {w.num_heads} heads"}
+    done, elapsed, nbytes = 0, 0.0, 0
+    while elapsed < budget_s:
+        j = done % len(keep)
+        t0 = time.perf_counter()
+        paged_decode(q[j:j + 1], ref.cache, [tables[j]], [lens[j]], w.scale)
+        elapsed += time.perf_counter() - t0
+        nbytes += bytes_per_seq[j]
+        done += 1
+    return {"value": nbytes / elapsed / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} single-sequence oracle decodes cycling over {len(keep)} sampled sequences "
+                      f"(lengths {lens}) of the bench workload, {elapsed:.1f} s, one thread",
+            "seqs_per_sec": done / elapsed}
+
+
+def run_cpu_baseline(cfg, budget_s: float):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", str(cfg), "--cpu-budget", str(budget_s)]
+    res = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=max(600, 20 * budget_s))
+    if res.returncode != 0:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "error": res.stderr[-400:]}
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def _dist_init():
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, local, world
+
+
+def reduce_max_sum(max_val: float, sum_val: float, device=None):
+    """(max over ranks of max_val, sum over ranks of sum_val); identity at world 1."""
+    import torch
+    import torch.distributed as dist
+
+    if not dist.is_initialized() or dist.get_world_size() == 1:
+        return max_val, sum_val
+    t = torch.tensor([max_val], dtype=torch.float64, device=device)
+    u = torch.tensor([sum_val], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank decodes its own batches (weak scaling by sequences)."""
+    return base + 7919 * rank
+
+
+class DecodeBench:
+    """R resident copies of the decode batch on one device, decoded in rotation."""
+
+    def __init__(self, cfg, R, steps_per_batch_max, centre_steps, seed, device):
+        import numpy as np
+        import torch
+
+        import paged_kv_cache_126_gb300 as pa
+        import workloads
+
+        self.pa, self.torch = pa, torch
+        w = workloads.build(cfg)
+        self.w = w
+        S = len(w.final_lens)
+        self.S, self.H, self.D, self.B = S, w.num_heads, w.head_dim, w.block_size
+        self.e = w.elem_bytes
+        self.R = R
+        L = np.array([w.final_lens[s] for s in range(S)], dtype=np.int64)
+        self.L = L
+        prefill = np.maximum(L - 1 - centre_steps, 0)
+        final = prefill + steps_per_batch_max
+        need = int(sum(-(-int(x) // self.B) for x in final)) * R
+        nb = int(math.ceil(1.2 * need)) + R * S
+        rng = np.random.default_rng(seed)
+        order = rng.permutation(nb).astype(np.int32)
+        max_blocks = int(-(-int(final.max()) // self.B)) + 1
+        self.eng = pa.PagedKVEngine(nb, self.B, self.H, self.D, w.dtype, free_order=order, device=device,
+                                    max_seqs=S, max_blocks_per_seq=max_blocks)
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        dt = pa.engine.TORCH_DTYPES[w.dtype]
+        self.batches = []
+        for r in range(R):
+            ids = list(range(r * S, (r + 1) * S))
+            for j, s in enumerate(ids):
+                n = int(prefill[j])
+                k = torch.randn(n, self.H, self.D, generator=g, device=device).to(dt)
+                v = torch.randn(n, self.H, self.D, generator=g, device=device).to(dt)
+                self.eng.add_seq(s, k, v)
+            self.batches.append(ids)
+        self.inputs = []
+        for _ in range(4):
+            mk = lambda: torch.randn(S, self.H, self.D, generator=g, device=device).to(dt)  # noqa: E731
+            self.inputs.append((mk(), mk(), mk()))
+        self.out = torch.empty(S, self.H, self.D, dtype=dt, device=device)
+        self.scale = w.scale
+        torch.cuda.synchronize()
+
+    def step(self, k, events=None):
+        kn, vn, q = self.inputs[k % 4]
+        out, nc, lens = self.eng.decode_step(self.batches[k % self.R], kn, vn, q, self.scale, self.out,
+                                             events=events)
+        return algorithmic_bytes(lens, self.H, self.D, self.B, self.e), lens
+
+
+def gpu_arm(args):
+    import numpy as np
+    import torch
+
+    rank, local, world = _dist_init()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import paged_kv_cache_126_gb300 as pa
+
+    K, W = args.steps, args.warmup
+    R = args.batches
+    k_e2e = max(args.e2e_steps, R)
+    per_batch = -(-(W + K + k_e2e) // R) + 2
+    centre = -(-W // R) + (K // R + 1) // 2
+    bench = DecodeBench(args.config, R, per_batch, centre, rank_seed(1234, rank), device)
+    st = torch.cuda.current_stream(device)
+
+    for k in range(W):
+        bench.step(k)
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, inputs resident in HBM --------------------------------------
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    n_launch0 = pa.pa_launch_count()
+    step_bytes, all_lens = [], []
+    t_start.record(st)
+    for k in range(K):
+        b, lens = bench.step(W + k, events=ev[k])
+        step_bytes.append(b)
+        all_lens.append(float(np.mean(lens)))
+    t_end.record(st)
+    torch.cuda.synchronize()
+    barrier()
+    launches = pa.pa_launch_count() - n_launch0
+    clk = clocks.stop() if rank == 0 else None
+    ms = t_start.elapsed_time(t_end)
+    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    my_bytes = float(sum(step_bytes))
+    max_ms, tot_bytes = reduce_max_sum(ms, my_bytes, device)
+
+    # ---- end to end: host buffers, copies inside the timed region ---------------------------
+    dt = bench.inputs[0][0].dtype
+    S, H, D = bench.S, bench.H, bench.D
+    host_in = [tuple(x.cpu().pin_memory() for x in trip) for trip in bench.inputs]
+    dev_in = [torch.empty(S, H, D, dtype=dt, device=device) for _ in range(3)]
+    host_out = torch.empty(S, H, D, dtype=dt).pin_memory()
+    mb = bench.eng.max_blocks
+    h2d = 3 * S * H * D * bench.e + 4 * (4 * S + S * mb)
+    d2h = S * H * D * bench.e
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_bytes = 0
+    e0.record(st)
+    for k in range(k_e2e):
+        kh, vh, qh = host_in[k % 4]
+        dev_in[0].copy_(kh, non_blocking=True)
+        dev_in[1].copy_(vh, non_blocking=True)
+        dev_in[2].copy_(qh, non_blocking=True)
+        out, _, lens = bench.eng.decode_step(bench.batches[(W + K + k) % R], dev_in[0], dev_in[1], dev_in[2],
+                                             bench.scale, bench.out)
+        e2e_bytes += algorithmic_bytes(lens, H, D, bench.B, bench.e)
+        host_out.copy_(out, non_blocking=True)
+    e1.record(st)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    e2e_max_ms, e2e_tot = reduce_max_sum(e2e_ms, float(e2e_bytes), device)
+
+    if rank != 0:
+        return
+    peak, peak_src = _peaks()
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    achieved = (my_bytes / K) / (dec_avg_ms * 1e-3) / 1e9
+    traffic = _profile_traffic("decode batch 64 x U[512,2048]")
+    value = tot_bytes / (max_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(max_ms / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic (seeded; K/V/q ~ N(0,1) fp16; lengths and shuffled free order from the workload generator)",
+        "config": {
+            "workload": "decode batch: 64 seqs, context ~U[512,2048], 32 heads, head_dim 128, block_size 16, fp16",
+            "seqs_per_step": S,
+            "mean_attended_len": round(float(np.mean(all_lens)), 1),
+            "sampled_mean_len": round(float(bench.L.mean()), 1),
+            "resident_batches": R,
+            "l2": f"inputs larger than L2: each step reads a different ~{my_bytes / K / 1e9:.2f} GB batch",
+            "parallelism": f"replicas by sequence batch x{world}",
+        },
+        "seqs_per_sec": round(S * K * world / (max_ms * 1e-3), 1),
+        "pct_of_hbm_peak": round(100 * value / peak, 2),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "pa_decode (decode_kernel + merge_kernel), CUDA events around each call",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "peak_source": peak_src,
+            "decode_us_per_launch": round(1000 * dec_avg_ms, 2),
+            "algorithmic_bytes_per_launch": round(my_bytes / K),
+        },
+        "e2e": {
+            "value": round(e2e_tot / (e2e_max_ms * 1e-3) / 1e9, 1),
+            "unit": UNIT,
+            "steps": k_e2e,
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "api": "PagedKVEngine.decode_step with q/k/v copied from pinned host buffers and out copied back",
+        },
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if not args.no_extra:
+        line["extra"] = {"fixed_64x2048": fixed_variant(args, device)}
+    if not args.no_cpu:
+        line["cpu_baseline"] = run_cpu_baseline(args.config, args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+def fixed_variant(args, device):
+    """The same step on 64 sequences of exactly 2048 tokens (the '64x2k' figure)."""
+    import numpy as np
+    import torch
+
+    R, K = 4, max(40, args.steps // 8)
+    bench = DecodeBench("1x", R, -(-(K + 8) // R) + 2, 2 + (K // R + 1) // 2, 4321, device)
+    st = torch.cuda.current_stream(device)
+    for k in range(8):
+        bench.step(k)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    tot = 0
+    e0.record(st)
+    for k in range(K):
+        b, _ = bench.step(8 + k, events=ev[k])
+        tot += b
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    dec = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    res = {"steps": K, "gbps": round(tot / (ms * 1e-3) / 1e9, 1), "seqs_per_sec": round(64 * K / (ms * 1e-3), 1),
+           "decode_us_per_launch": round(1000 * dec, 2),
+           "decode_gbps": round(tot / K / (dec * 1e-3) / 1e9, 1)}
+    del bench
+    torch.cuda.empty_cache()
+    return res
+
+
+# ----------------------------------------------------------------------------- reference arm
+def reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    budget_steps = args.steps + args.warmup
+    res = cpu_baseline_worker(args.config, 0, per_step=True, steps=budget_steps)
+    times, byts = res["times"][args.warmup:], res["bytes"][args.warmup:]
+    total_t = sum(times)
+    value = sum(byts) / total_t / 1e9
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": UNIT,
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1000 * total_t / max(1, len(times)), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded, same generator as the GPU arm)",
+        "config": {"workload": "decode batch: 64 seqs, context ~U[512,2048], 32 heads, head_dim 128, "
+                               "block_size 16, fp16 storage",
+                   "step": "one sequence of the batch per step (bounded sample)"},
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": res["sample"], "value": round(value, 4),
+                         "unit": UNIT},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1600)
+    ap.add_argument("--warmup", type=int, default=32)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batches", type=int, default=16, help="resident copies of the batch decoded in rotation")
+    ap.add_argument("--e2e-steps", type=int, default=400)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--config", default="1")
+    ap.add_argument("--cpu-worker", default=None)
+    args = ap.parse_args()
+    if args.config not in ("1", "1x"):
+        raise SystemExit("the bench times the decode batch workload (1) or its fixed 64x2048 form (1x)")
+    args.config = 1 if args.config == "1" else "1x"
+    if args.cpu_worker is not None:
+        cfg = 1 if args.cpu_worker == "1" else "1x"
+        print(json.dumps(cpu_baseline_worker(cfg, args.cpu_budget)), flush=True)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

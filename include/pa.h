@@ -128,10 +128,13 @@ int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache,
  * Arithmetic: K/V/q converted to fp32, fp32 dot products, online softmax and
  * accumulation in fp32, one rounding to the output dtype.  Long contexts are
  * split into partitions processed by separate thread blocks and combined by a
- * log-sum-exp merge kernel on the same stream.  The split needs a workspace that
- * the library owns: one per (device, stream), grown with cudaMalloc on first use
- * at a larger size (keep such first calls outside CUDA-graph capture), freed by
- * pa_shutdown().
+ * log-sum-exp merge kernel on the same stream.  Work is handed to a persistent
+ * grid through an atomic counter.  Counter and split partials live in a
+ * workspace the library owns: one per (device, stream), allocated (cudaMalloc)
+ * and zeroed on the first call with that pair and grown on the first call that
+ * needs more (keep such calls outside CUDA-graph capture), freed by
+ * pa_shutdown().  Calls on one stream run in order; calls on different streams
+ * use different workspaces.
  * Supported: dtype f32/f16/bf16; D in {64, 128, 256} (f32: {64, 128});
  * 1 <= B <= 256.
  */
@@ -147,7 +150,10 @@ typedef struct pa_decode_params {
   int32_t warps_per_head;    /* 1, 2, 4 or 8 */
   int32_t stages;            /* K/V staging buffers per thread block, 2..8 */
   int32_t ctas_per_sm;       /* persistent grid = SMs x this (clamped to occupancy) */
-  int32_t reserved[3];
+  int32_t items_per_cta;     /* automatic partition length aims at this many work items per
+                                thread block (default 4) */
+  int32_t generic_only;      /* 1: never take the unrolled full-frame path (testing) */
+  int32_t reserved;
 } pa_decode_params;
 
 /* pa_decode with explicit launch options (tests, tuning).  params may be NULL. */

@@ -39,7 +39,7 @@ class PaTensor(C.Structure):
 class PaDecodeParams(C.Structure):
     _fields_ = [("partition_tokens", C.c_int32), ("heads_per_cta", C.c_int32),
                 ("warps_per_head", C.c_int32), ("stages", C.c_int32), ("ctas_per_sm", C.c_int32),
-                ("reserved", C.c_int32 * 3)]
+                ("items_per_cta", C.c_int32), ("generic_only", C.c_int32), ("reserved", C.c_int32)]
 
 
 class PAError(RuntimeError):

@@ -81,7 +81,11 @@ int make_cache_map(CUtensorMap* map, void* base, int dtype, int64_t nb, int64_t 
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
 }
 
-// ---- library-owned split workspace, one per (device, stream) ------------------------------
+// ---- library-owned workspace, one per (device, stream) -------------------------------------
+// Layout: [0, 256) scheduler counters (zeroed at allocation; each decode launch
+// leaves them zero), then the per-launch offsets and split partials.
+constexpr size_t kSchedBytes = 256;
+
 struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
@@ -94,7 +98,7 @@ int workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
   Workspace& w = g_ws[{dev, stream}];
   if (w.bytes < bytes) {
     if (w.ptr) {
-      // the old buffer may still be read by earlier launches on this stream
+      // the old buffer may still be used by earlier launches on this stream
       if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ERR_CUDA;
       cudaFree(w.ptr);
       w.ptr = nullptr;
@@ -102,6 +106,7 @@ int workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
     }
     const size_t grow = std::max(bytes, static_cast<size_t>(1) << 20);
     if (cudaMalloc(&w.ptr, grow) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaMemsetAsync(w.ptr, 0, kSchedBytes, stream) != cudaSuccess) return PA_ERR_CUDA;
     w.bytes = grow;
   }
   *out = w.ptr;
@@ -171,8 +176,8 @@ cudaError_t dispatch_decode(const pa::DecodeArgs& a, const pa::DecodeCfg& c, con
 }
 
 bool combo_built(int hg, int wph) {
-  return (hg == 4 && (wph == 1 || wph == 2)) || (hg == 2 && (wph == 2 || wph == 4)) ||
-         (hg == 1 && (wph == 4 || wph == 8));
+  return (hg == 4 && (wph == 1 || wph == 2)) || (hg == 2 && (wph == 1 || wph == 2 || wph == 4)) ||
+         (hg == 1 && (wph == 1 || wph == 2 || wph == 4 || wph == 8));
 }
 
 }  // namespace
@@ -337,7 +342,16 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
       }
     }
   }
-  c.warps_per_head = p.warps_per_head ? p.warps_per_head : 8 / c.heads_per_cta;
+  // Unrolled full-frame path: 256-byte rows and B = 16 * warps_per_head.
+  const bool fast_rows = D * e == 256 && (B == 16 || B == 32) && !p.generic_only;
+  if (p.warps_per_head) {
+    c.warps_per_head = p.warps_per_head;
+  } else if (fast_rows) {
+    c.warps_per_head = static_cast<int>(B / 16);
+  } else {
+    c.warps_per_head = 8 / c.heads_per_cta;
+  }
+  c.fast = fast_rows && B == 16 * c.warps_per_head;
   if (!combo_built(c.heads_per_cta, c.warps_per_head)) return PA_ERR_INVALID;
   const int64_t stage_bytes = 2 * B * c.heads_per_cta * D * e;
   c.stages = 1;
@@ -395,6 +409,7 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
   // ---- partitioning and workspace --------------------------------------------------------
   const int64_t Lcap = max_blocks * B;
   int64_t items_max = 0;
+  if (p.items_per_cta < 0 || p.generic_only < 0) return PA_ERR_INVALID;
   if (p.partition_tokens == -1 || Lcap == 0) {
     a.fixed_part = static_cast<int32_t>(std::max<int64_t>(Lcap, B));
   } else if (p.partition_tokens > 0) {
@@ -402,28 +417,31 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
     if (a.fixed_part < Lcap) items_max = S * a.G * ((Lcap + a.fixed_part - 1) / a.fixed_part);
   } else if (p.partition_tokens == 0) {
     a.fixed_part = 0;
-    a.target_items = 4 * c.grid;
+    a.target_items = (p.items_per_cta ? p.items_per_cta : 4) * c.grid;
     a.min_part = round_up(256, B);
     if (a.min_part < Lcap)
       items_max = std::min<int64_t>(S * a.G * ((Lcap + a.min_part - 1) / a.min_part), a.target_items + S * a.G);
   } else {
     return PA_ERR_INVALID;
   }
-  if (items_max > 0) {
+  {
+    const size_t off_bytes = (static_cast<size_t>(2 * S + 4) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
     const size_t ml_bytes = static_cast<size_t>(items_max) * c.heads_per_cta * 2 * sizeof(float);
     const size_t o_bytes = static_cast<size_t>(items_max) * c.heads_per_cta * D * sizeof(float);
-    const size_t off_bytes = static_cast<size_t>(S + 2) * sizeof(int32_t);
     void* ws = nullptr;
-    PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), o_bytes + ml_bytes + off_bytes + 256, &ws));
+    PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), kSchedBytes + off_bytes + o_bytes + ml_bytes, &ws));
     unsigned char* w = static_cast<unsigned char*>(ws);
-    a.ws_o = reinterpret_cast<float*>(w);
-    a.ws_ml = reinterpret_cast<float*>(w + o_bytes);
-    a.ws_off = reinterpret_cast<int32_t*>(w + o_bytes + ml_bytes);
+    a.sched = reinterpret_cast<int32_t*>(w);
+    a.ws_off = reinterpret_cast<int32_t*>(w + kSchedBytes);
+    if (items_max > 0) {
+      a.ws_o = reinterpret_cast<float*>(w + kSchedBytes + off_bytes);
+      a.ws_ml = reinterpret_cast<float*>(w + kSchedBytes + off_bytes + o_bytes);
+    }
   }
 
   if (dispatch_decode(a, c, tk, tv, static_cast<cudaStream_t>(stream), false, nullptr) != cudaSuccess)
     return PA_ERR_CUDA;
-  g_launches.fetch_add(a.ws_off ? 2 : 1);
+  g_launches.fetch_add(a.ws_o ? 2 : 1);
   return PA_OK;
 }
 

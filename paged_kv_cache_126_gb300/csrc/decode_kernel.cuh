@@ -10,29 +10,36 @@
 //
 // Design (GB300):
 //   * Work item = (sequence, head group of HG heads, context partition).  A
-//     persistent grid of thread blocks walks the item list round-robin; the
-//     partition length is chosen on the device from the actual context lengths
-//     so that there are a few items per thread block.  Items of one sequence are
-//     adjacent, so the K/V rows a thread block streams sit next to those of the
-//     blocks working beside it.
-//   * One producer warp: reads the item's block-table slice (one coalesced load
-//     per 32 frames), bounds-checks every frame id, and for each frame issues two
-//     3-D TMA tile loads (K and V: box {D, HG, B} of the [num_blocks*B, H, D] view)
-//     into a ring of `stages` shared-memory buffers, completing on an mbarrier.
-//   * HG*WPH consumer warps: warp (h, w) owns head h and every WPH-th group of
-//     rows of each staged frame.  A row (one token, one head) is read as 16-byte
-//     chunks by LPR = D*elem/16 lanes, so a warp covers TPI = 32/LPR tokens per
-//     step with conflict-free shared-memory reads.  Dot products are reduced with
-//     xor shuffles inside each row group; the softmax is online (running max m and
-//     sum l in log2 units, ex2.approx) and the value accumulation is fp32.
-//   * Epilogue: row groups, then warps of a head, are combined with the same
-//     log-sum-exp rule.  A sequence that fits in one partition is normalised and
-//     written directly; otherwise the (m, l, o) partial goes to the workspace and
-//     merge_kernel combines the partitions.
+//     persistent grid of thread blocks takes items from a global atomic counter
+//     (dynamic scheduling), longest items first: every full partition of every
+//     sequence, then the shorter last partitions.  The partition length is chosen
+//     on the device from the actual context lengths so there are a few items per
+//     thread block.  The counter resets itself: the last thread block to retire
+//     zeroes it for the next launch on the stream.
+//   * One producer warp: takes the next item, hands its id to the consumers
+//     through a two-slot mbarrier ring, reads the item's block-table slice (one
+//     coalesced load per 32 frames), bounds-checks every frame id, and for each
+//     frame issues two 3-D TMA tile loads (K and V: box {D, HG, B} of the
+//     [num_blocks*B, H, D] view) into a ring of `stages` shared-memory buffers.
+//   * HG*WPH consumer warps: warp (h, w) owns head h and a share of the rows of
+//     each staged frame.  A row (one token, one head) is read as 16-byte chunks by
+//     LPR = D*elem/16 lanes (conflict-free shared-memory reads).  For 256-byte rows
+//     and B = 16*WPH a fully unrolled path handles a whole frame: eight row steps
+//     per warp, one transposed shuffle reduction for the eight dot products, one
+//     block max, a rescale only when the max grows, and one shuffle per row step
+//     to hand each lane its softmax weight.  Other shapes, and the partly filled
+//     last frame of a sequence, take the generic path (xor reductions per step,
+//     online update per chunk of steps).  Softmax runs in log2 units with
+//     ex2.approx; all products and sums are fp32.
+//   * Epilogue: row groups, then warps of a head (through shared memory, handed
+//     over with mbarriers), are combined by the log-sum-exp rule.  A sequence that
+//     fits in one partition is normalised and written directly; otherwise the
+//     (m, l, o) partial goes to the workspace and merge_kernel combines them.
 //   * Bad frame ids / context lengths: the affected output rows become zeros and a
-//     sticky status bit is set.  Every mbarrier wait is bounded; a wait that gives
-//     up sets PA_DEV_TIMEOUT, turns all later waits of the block into no-ops and
-//     the producer waits (again bounded) for its copies in flight before exiting.
+//     sticky status bit is set.  Every wait is an mbarrier wait with a bound; a
+//     wait that gives up sets PA_DEV_TIMEOUT, turns all later waits of the block
+//     into no-ops, and the producer waits (again bounded) for its copies in
+//     flight before the block retires.
 #pragma once
 
 #include <cuda.h>
@@ -195,19 +202,18 @@ struct Chunk<__nv_bfloat16> {
 
 // ---- shared-memory layout (host and device agree) -------------------------------------------
 struct Layout {
-  uint32_t stage_pitch, bars, flags, offs, comb, total;
+  uint32_t stage_pitch, bars, flags, offa, offb, comb, total;
   __host__ __device__ Layout(int stages, uint32_t stage_bytes, int S, int ncw, int D) {
     stage_pitch = (stage_bytes + 127u) & ~127u;
-    bars = stages * stage_pitch;                    // full[stages], empty[stages]
-    flags = bars + 16u * stages;                    // poison[stages], abort
-    offs = (flags + 4u * (stages + 1) + 15u) & ~15u;  // item offsets [S + 1]
-    comb = (offs + 4u * (S + 1) + 15u) & ~15u;      // combine scratch [ncw][D + 2]
-    total = comb + 4u * ncw * (D + 2) + 128u;       // + slack for 128-byte base alignment
+    // mbarriers: full[stages], empty[stages], item_full[2], item_empty[2], comb_full[4], comb_empty[4]
+    bars = stages * stage_pitch;
+    flags = bars + 16u * stages + 32u + 64u;          // poison[stages], abort, item_slot[2]
+    offa = (flags + 4u * (stages + 3) + 15u) & ~15u;  // full-partition item offsets [S + 1]
+    offb = (offa + 4u * (S + 1) + 15u) & ~15u;        // last-partition item offsets [S + 1]
+    comb = (offb + 4u * (S + 1) + 15u) & ~15u;        // combine scratch [ncw][D + 2]
+    total = comb + 4u * ncw * (D + 2) + 128u;         // + slack for 128-byte base alignment
   }
 };
-
-// Partition count of one sequence (1 for an empty or invalid length).
-__device__ __forceinline__ int parts_of(int L, int P) { return L <= P ? 1 : (L + P - 1) / P; }
 
 // Validated context length, or -1.
 __device__ __forceinline__ int valid_len(const DecodeArgs& a, int s) {
@@ -215,47 +221,244 @@ __device__ __forceinline__ int valid_len(const DecodeArgs& a, int s) {
   return (L < 0 || static_cast<int64_t>(L) > static_cast<int64_t>(a.max_blocks) * a.B) ? -1 : L;
 }
 
+// Number of partitions of a sequence: full ones, plus one shorter last partition
+// when the length is not a multiple of P (an empty or invalid sequence has exactly
+// one, empty, last partition).
+__device__ __forceinline__ int full_parts(int Lv, int P) { return Lv / P; }
+__device__ __forceinline__ int last_part(int Lv, int P) { return (Lv % P != 0 || Lv == 0) ? 1 : 0; }
+
+// Largest s in [0, S) with off[s] <= x (off non-decreasing, off[0] = 0).
+__device__ __forceinline__ int upper_seq(const int32_t* off, int S, int x) {
+  int lo = 0, hi = S - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct Item {
+  int s, g, L;        // sequence, head group, validated length (-1 = invalid)
+  int tok1, blk0, nblk;
+  bool single;        // the sequence has one partition: write the output directly
+};
+
+__device__ __forceinline__ Item locate(const DecodeArgs& a, const int32_t* offa, const int32_t* offb,
+                                       int a_total, int P, int item) {
+  Item it;
+  int p;
+  if (item < a_total) {
+    it.s = upper_seq(offa, a.S, item);
+    const int local = item - offa[it.s];
+    p = local / a.G;
+    it.g = local - p * a.G;
+  } else {
+    const int b = item - a_total;
+    it.s = upper_seq(offb, a.S, b);
+    it.g = b - offb[it.s];
+    p = -1;  // the last partition
+  }
+  it.L = valid_len(a, it.s);
+  const int Lv = it.L < 0 ? 0 : it.L;
+  const int nf = full_parts(Lv, P);
+  if (p < 0) p = nf;
+  it.single = nf + last_part(Lv, P) == 1;
+  const int tok0 = p * P;
+  it.tok1 = min(Lv, tok0 + P);
+  it.blk0 = tok0 / a.B;
+  it.nblk = it.tok1 > tok0 ? (it.tok1 + a.B - 1) / a.B - it.blk0 : 0;
+  return it;
+}
+
+// Online-softmax state of one consumer warp for one head: running max m (log2
+// units, warp-uniform), l = sum of weights of this lane's row group, lf = weights
+// gathered by the unrolled path (one row step per lane, folded into l at the end),
+// o = weighted values of this lane's 16-byte chunk over its row group's tokens.
+template <int VEC>
+struct SoftState {
+  float m, l, lf;
+  float o[VEC];
+  __device__ __forceinline__ void reset() {
+    m = -INFINITY;
+    l = 0.f;
+    lf = 0.f;
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) o[v] = 0.f;
+  }
+  __device__ __forceinline__ void rescale(float m_new) {
+    const float alpha = ex2(m - m_new);
+    l *= alpha;
+    lf *= alpha;
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) o[v] *= alpha;
+    m = m_new;
+  }
+};
+
+// Generic frame: any B, any valid-row count.  Rows are dealt to the WPH warps of a
+// head in turn; online update once per CH row steps.
 template <typename T, int D, int HG, int WPH>
-__global__ void __launch_bounds__(32 * (HG * WPH + 1), 2)
+__device__ __forceinline__ void frame_generic(SoftState<16 / sizeof(T)>& st, const float (&qv)[16 / sizeof(T)],
+                                              const unsigned char* kst, const unsigned char* vst, int B,
+                                              int n_valid, int w, int r) {
+  constexpr int E = sizeof(T);
+  constexpr int VEC = 16 / E;
+  constexpr int LPR = D / VEC;
+  constexpr int TPI = 32 / LPR;
+  constexpr int CH = 8;
+  constexpr uint32_t row_bytes = HG * D * E;
+  const int NIT = (B + TPI - 1) / TPI;
+  for (int it0 = w; it0 < NIT; it0 += WPH * CH) {
+    float x[CH];
+#pragma unroll
+    for (int u = 0; u < CH; ++u) {
+      const int it = it0 + u * WPH;
+      const int t = it * TPI + r;
+      float acc = 0.f;
+      if (it < NIT) {
+        if (t < n_valid) {
+          float kv[VEC];
+          Chunk<T>::load(kst + t * row_bytes, kv);
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) acc = fmaf(qv[v], kv[v], acc);
+        }
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
+      }
+      x[u] = (it < NIT && t < n_valid) ? acc : -INFINITY;
+    }
+    float cm = x[0];
+#pragma unroll
+    for (int u = 1; u < CH; ++u) cm = fmaxf(cm, x[u]);
+#pragma unroll
+    for (int off = LPR; off < 32; off <<= 1) cm = fmaxf(cm, __shfl_xor_sync(kFull, cm, off));
+    if (cm > st.m) st.rescale(cm);   // warp-uniform
+    if (st.m == -INFINITY) continue;  // nothing valid yet
+#pragma unroll
+    for (int u = 0; u < CH; ++u) {
+      const int it = it0 + u * WPH;
+      const int t = it * TPI + r;
+      if (it < NIT && t < n_valid) {
+        const float pw = ex2(x[u] - st.m);
+        st.l += pw;
+        float vv[VEC];
+        Chunk<T>::load(vst + t * row_bytes, vv);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) st.o[v] = fmaf(pw, vv[v], st.o[v]);
+      }
+    }
+  }
+}
+
+// Full frame of B = 16*WPH rows with 256-byte rows (16 lanes per row, 2 rows per
+// warp step): warp w takes row steps 8w .. 8w+7, i.e. tokens 16w .. 16w+15.
+template <typename T, int D, int HG>
+__device__ __forceinline__ void frame_fast(SoftState<16 / sizeof(T)>& st, const float (&qv)[16 / sizeof(T)],
+                                           const unsigned char* kst, const unsigned char* vst, int w, int r,
+                                           int c) {
+  constexpr int E = sizeof(T);
+  constexpr int VEC = 16 / E;
+  static_assert(D * E == 256, "fast path needs 256-byte rows");
+  constexpr uint32_t row_bytes = HG * D * E;
+  const unsigned char* kb = kst + (16 * w + r) * row_bytes;
+  const unsigned char* vb = vst + (16 * w + r) * row_bytes;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float kv[VEC];
+    Chunk<T>::load(kb + 2 * i * row_bytes, kv);
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int v = 0; v < VEC; v += 2) {
+      s0 = fmaf(qv[v], kv[v], s0);
+      s1 = fmaf(qv[v + 1], kv[v + 1], s1);
+    }
+    acc[i] = s0 + s1;
+  }
+  // transposed reduction over the 16 lanes of the row group: afterwards lane c
+  // holds the full dot product of row step (c >> 1) & 7.
+  const bool b3 = (c & 8) != 0, b2 = (c & 4) != 0, b1 = (c & 2) != 0;
+  float b[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float send = b3 ? acc[j] : acc[j + 4];
+    const float keep = b3 ? acc[j + 4] : acc[j];
+    b[j] = keep + __shfl_xor_sync(kFull, send, 8);
+  }
+  float d[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float send = b2 ? b[j] : b[j + 2];
+    const float keep = b2 ? b[j + 2] : b[j];
+    d[j] = keep + __shfl_xor_sync(kFull, send, 4);
+  }
+  float sc;
+  {
+    const float send = b1 ? d[0] : d[1];
+    const float keep = b1 ? d[1] : d[0];
+    sc = keep + __shfl_xor_sync(kFull, send, 2);
+  }
+  sc += __shfl_xor_sync(kFull, sc, 1);
+  float bm = sc;
+#pragma unroll
+  for (int off = 2; off < 32; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, off));
+  if (bm > st.m) st.rescale(bm);  // warp-uniform; rare once the running max settles
+  const float p = ex2(sc - st.m);
+  st.lf += p;
+  const int src = (r << 4);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float pt = __shfl_sync(kFull, p, src | (2 * i));
+    float vv[VEC];
+    Chunk<T>::load(vb + 2 * i * row_bytes, vv);
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) st.o[v] = fmaf(pt, vv[v], st.o[v]);
+  }
+}
+
+template <typename T, int D, int HG, int WPH, int BFAST>
+__global__ void __launch_bounds__(32 * (HG * WPH + 1), (HG * WPH <= 4 ? 3 : 2))
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const DecodeArgs a, const int stages) {
   constexpr int E = sizeof(T);
   constexpr int VEC = 16 / E;   // elements per 16-byte chunk
   constexpr int LPR = D / VEC;  // lanes per (token, head) row
   static_assert(LPR >= 1 && LPR <= 32 && (32 % LPR) == 0, "unsupported head_dim");
-  constexpr int TPI = 32 / LPR;  // rows per warp step
   constexpr int NCW = HG * WPH;  // consumer warps
-  constexpr int CH = 8;          // row steps per online-softmax update
+  static_assert(BFAST == 0 || (BFAST == 16 * WPH && D * E == 256), "fast path shape");
 
   const int B = a.B;
   const uint32_t tile_bytes = static_cast<uint32_t>(B) * HG * D * E;
   const uint32_t stage_bytes = 2u * tile_bytes;
-  const uint32_t row_bytes = HG * D * E;  // one token's HG heads inside a staged tile
 
   extern __shared__ unsigned char smem_raw[];
   const Layout lay(stages, stage_bytes, a.S, NCW, D);
-  unsigned char* smem =
-      smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);  // 128-byte aligned base
+  unsigned char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);  // 128-byte aligned
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + lay.bars;
   const uint32_t bar_empty = bar_full + 8u * stages;
+  const uint32_t bar_ifull = bar_empty + 8u * stages;
+  const uint32_t bar_iempty = bar_ifull + 16u;
+  const uint32_t bar_cfull = bar_iempty + 16u;   // per head: warps 1.. of the head have written
+  const uint32_t bar_cempty = bar_cfull + 32u;   // per head: warp 0 has read
   volatile int32_t* poison = reinterpret_cast<volatile int32_t*>(smem + lay.flags);
   volatile int32_t* abort_flag = poison + stages;
-  int32_t* item_off = reinterpret_cast<int32_t*>(smem + lay.offs);
+  volatile int32_t* item_slot = abort_flag + 1;
+  int32_t* offa = reinterpret_cast<int32_t*>(smem + lay.offa);
+  int32_t* offb = reinterpret_cast<int32_t*>(smem + lay.offb);
   float* comb = reinterpret_cast<float*>(smem + lay.comb);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  // ---- 1. per-sequence item counts, partition length, prefix offsets ------------------------
+  // ---- 1. partition length, per-sequence item counts, prefix offsets ----------------------
   int P;
   {
     const int Lcap = a.max_blocks * B;
     if (a.fixed_part > 0) {
       P = a.fixed_part;
     } else {
-      // total valid tokens (block-wide reduction through the combine scratch)
       long long local = 0;
       for (int s = tid; s < a.S; s += blockDim.x) {
         const int L = valid_len(a, s);
@@ -280,14 +483,25 @@ __global__ void __launch_bounds__(32 * (HG * WPH + 1), 2)
   for (int s = tid; s < a.S; s += blockDim.x) {
     const int L = valid_len(a, s);
     if (L < 0 && blockIdx.x == 0) atomicOr(a.status, kDevBadLen);
-    item_off[s + 1] = parts_of(L < 0 ? 0 : L, P) * a.G;
+    const int Lv = L < 0 ? 0 : L;
+    offa[s + 1] = full_parts(Lv, P) * a.G;
+    offb[s + 1] = last_part(Lv, P) * a.G;
   }
   if (tid == 0) {
-    item_off[0] = 0;
+    offa[0] = 0;
+    offb[0] = 0;
     for (int i = 0; i < stages; ++i) {
       mbar_init(bar_full + 8u * i, 1);
       mbar_init(bar_empty + 8u * i, NCW);
       poison[i] = 0;
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_ifull + 8u * i, 1);
+      mbar_init(bar_iempty + 8u * i, NCW);
+    }
+    for (int h = 0; h < HG; ++h) {
+      mbar_init(bar_cfull + 8u * h, WPH > 1 ? WPH - 1 : 1);
+      mbar_init(bar_cempty + 8u * h, 1);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -298,64 +512,63 @@ __global__ void __launch_bounds__(32 * (HG * WPH + 1), 2)
     prefetch_tmap(&tmap_v);
   }
   __syncthreads();
-  if (warp == 0) {  // inclusive scan of item counts
+  if (warp < 2) {  // warp 0 scans the full-partition counts, warp 1 the last-partition counts
+    int32_t* off = warp == 0 ? offa : offb;
     int carry = 0;
     for (int base = 0; base < a.S; base += 32) {
       const int i = base + lane;
-      int v = i < a.S ? item_off[i + 1] : 0;
+      int v = i < a.S ? off[i + 1] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int n = __shfl_up_sync(kFull, v, o);
         if (lane >= o) v += n;
       }
       v += carry;
-      if (i < a.S) item_off[i + 1] = v;
+      if (i < a.S) off[i + 1] = v;
       carry = __shfl_sync(kFull, v, 31);
     }
   }
   __syncthreads();
-  const int total_items = item_off[a.S];
-  if (blockIdx.x == 0 && a.ws_off != nullptr) {
-    for (int i = tid; i <= a.S; i += blockDim.x) a.ws_off[i] = item_off[i];
-    if (tid == 0) a.ws_off[a.S + 1] = P;
-  }
-
-  // item -> (s, p, g), token range and frame range
-  auto locate = [&](int item, int& s, int& p, int& g, int& L, int& tok1, int& blk0, int& nblk, bool& single) {
-    int lo = 0, hi = a.S - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (item_off[mid] <= item) lo = mid; else hi = mid - 1;
+  const int a_total = offa[a.S];
+  const int total_items = a_total + offb[a.S];
+  if (blockIdx.x == 0) {
+    for (int i = tid; i <= a.S; i += blockDim.x) {
+      a.ws_off[i] = offa[i];
+      a.ws_off[a.S + 1 + i] = offb[i];
     }
-    s = lo;
-    const int local = item - item_off[s];
-    p = local / a.G;
-    g = local - p * a.G;
-    L = valid_len(a, s);
-    const int Le = L < 0 ? 0 : L;
-    single = parts_of(Le, P) == 1;
-    const int tok0 = p * P;
-    tok1 = min(Le, tok0 + P);
-    blk0 = tok0 / B;
-    nblk = tok1 > tok0 ? (tok1 + B - 1) / B - blk0 : 0;
-  };
+    if (tid == 0) {
+      a.ws_off[2 * a.S + 2] = a_total;
+      a.ws_off[2 * a.S + 3] = P;
+    }
+  }
 
   if (warp == NCW) {
     // ============================== producer warp ==============================
-    int k = 0;
+    int k = 0, ni = 0;
     uint32_t issued = 0;  // bit i: stage i holds copies not yet known complete
-    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-      int s, p, g, L, tok1, blk0, nblk;
-      bool single;
-      locate(item, s, p, g, L, tok1, blk0, nblk, single);
-      const int32_t* row = a.block_tables + static_cast<int64_t>(s) * a.bt_row + blk0;
-      for (int j0 = 0; j0 < nblk; j0 += 32) {
+    while (true) {
+      int item = 0;
+      if (lane == 0) item = *abort_flag ? total_items : atomicAdd(a.sched, 1);
+      item = __shfl_sync(kFull, item, 0);
+      const bool done = item >= total_items;
+      if (lane == 0) {
+        const int sl = ni & 1;
+        if (mbar_wait(bar_iempty + 8u * sl, static_cast<uint32_t>((ni >> 1) & 1) ^ 1u, abort_flag, a.status)) {
+          item_slot[sl] = done ? -1 : item;
+          mbar_arrive(bar_ifull + 8u * sl);
+        }
+      }
+      ++ni;
+      if (done) break;
+      const Item it = locate(a, offa, offb, a_total, P, item);
+      const int32_t* row = a.block_tables + static_cast<int64_t>(it.s) * a.bt_row + it.blk0;
+      for (int j0 = 0; j0 < it.nblk; j0 += 32) {
         const int jj = j0 + lane;
         int frame = -1;
-        if (jj < nblk) frame = row[jj];
-        const bool bad = (jj < nblk) && (frame < 0 || frame >= a.num_blocks);
+        if (jj < it.nblk) frame = row[jj];
+        const bool bad = (jj < it.nblk) && (frame < 0 || frame >= a.num_blocks);
         if (__ballot_sync(kFull, bad) != 0u && lane == 0) atomicOr(a.status, kDevBadBlock);
-        const int cnt = min(32, nblk - j0);
+        const int cnt = min(32, it.nblk - j0);
         for (int j = 0; j < cnt; ++j, ++k) {
           const int fr = __shfl_sync(kFull, frame, j);
           if (lane == 0) {
@@ -370,8 +583,8 @@ __global__ void __launch_bounds__(32 * (HG * WPH + 1), 2)
                 poison[st] = 0;
                 const uint32_t dst = sbase + st * lay.stage_pitch;
                 mbar_arrive_expect_tx(bar_full + 8u * st, stage_bytes);
-                tma_load_3d(dst, &tmap_k, 0, g * HG, fr * B, bar_full + 8u * st);
-                tma_load_3d(dst + tile_bytes, &tmap_v, 0, g * HG, fr * B, bar_full + 8u * st);
+                tma_load_3d(dst, &tmap_k, 0, it.g * HG, fr * B, bar_full + 8u * st);
+                tma_load_3d(dst + tile_bytes, &tmap_v, 0, it.g * HG, fr * B, bar_full + 8u * st);
                 issued |= 1u << st;
               }
             } else {
@@ -381,16 +594,25 @@ __global__ void __launch_bounds__(32 * (HG * WPH + 1), 2)
         }
       }
     }
-    // If the block is aborting, copies may still be landing in shared memory:
-    // wait for them (bounded) before the block retires.
-    if (lane == 0 && *abort_flag) {
-      for (int kk = (k > stages ? k - stages : 0); kk < k; ++kk) {
-        const int st = kk % stages;
-        if (!(issued & (1u << st))) continue;
-        const uint32_t ph = static_cast<uint32_t>(kk / stages) & 1u;
-        const long long t0 = clock64();
-        while (!mbar_try_wait(bar_full + 8u * st, ph) && clock64() - t0 < kDrainCycles) {
+    if (lane == 0) {
+      // An aborting block may still have copies landing in shared memory: wait for
+      // them (bounded) before the block retires.
+      if (*abort_flag) {
+        for (int kk = (k > stages ? k - stages : 0); kk < k; ++kk) {
+          const int st = kk % stages;
+          if (!(issued & (1u << st))) continue;
+          const uint32_t ph = static_cast<uint32_t>(kk / stages) & 1u;
+          const long long t0 = clock64();
+          while (!mbar_try_wait(bar_full + 8u * st, ph) && clock64() - t0 < kDrainCycles) {
+          }
         }
+      }
+      // Retire: the last block to finish taking items resets the counters.
+      __threadfence();
+      if (atomicAdd(a.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+        a.sched[0] = 0;
+        a.sched[1] = 0;
+        __threadfence();
       }
     }
     return;
@@ -398,94 +620,70 @@ __global__ void __launch_bounds__(32 * (HG * WPH + 1), 2)
 
   // ============================== consumer warps ==============================
   const int h = warp / WPH;  // head within the group
-  const int w = warp % WPH;  // row-step slot within the head
+  const int w = warp % WPH;  // share of rows within the head
   const int r = lane / LPR;  // row group within the warp
   const int c = lane % LPR;  // 16-byte chunk within the row
-  const int NIT = (B + TPI - 1) / TPI;
   const unsigned char* const stage0 = smem;
-  int k = 0;
+  int k = 0, ni = 0, nc = 0;
+  SoftState<VEC> st;
 
-  for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-    int s, p, g, L, tok1, blk0, nblk;
-    bool single;
-    locate(item, s, p, g, L, tok1, blk0, nblk, single);
-    const int head = g * HG + h;
+  while (true) {
+    const int sl = ni & 1;
+    const bool got =
+        __all_sync(kFull, mbar_wait(bar_ifull + 8u * sl, static_cast<uint32_t>((ni >> 1) & 1), abort_flag, a.status));
+    const int item = got ? item_slot[sl] : -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_iempty + 8u * sl);
+    ++ni;
+    if (item < 0) break;
+    const Item it = locate(a, offa, offb, a_total, P, item);
+    const int head = it.g * HG + h;
 
     float qv[VEC];
     {
-      const T* qp = reinterpret_cast<const T*>(a.q) + static_cast<int64_t>(s) * a.q_row +
+      const T* qp = reinterpret_cast<const T*>(a.q) + static_cast<int64_t>(it.s) * a.q_row +
                     static_cast<int64_t>(head) * D + c * VEC;
       Chunk<T>::load(qp, qv);
 #pragma unroll
       for (int v = 0; v < VEC; ++v) qv[v] *= a.qk_scale_log2;
     }
-    float m = -INFINITY, l = 0.f;
-    float o[VEC];
-#pragma unroll
-    for (int v = 0; v < VEC; ++v) o[v] = 0.f;
-    bool poisoned = (L < 0);
+    st.reset();
+    bool poisoned = it.L < 0;
 
-    for (int j = 0; j < nblk; ++j, ++k) {
-      const int st = k % stages;
+    for (int j = 0; j < it.nblk; ++j, ++k) {
+      const int s_ = k % stages;
       const uint32_t ph = static_cast<uint32_t>(k / stages) & 1u;
-      const bool got = __all_sync(kFull, mbar_wait(bar_full + 8u * st, ph, abort_flag, a.status));
-      if (!got) poisoned = true;
-      if (got && poison[st]) poisoned = true;
-      if (got && !poisoned) {
-        const int n_valid = min(B, tok1 - (blk0 + j) * B);
-        const unsigned char* kst = stage0 + st * lay.stage_pitch + (h * D + c * VEC) * E;
+      const bool ok = __all_sync(kFull, mbar_wait(bar_full + 8u * s_, ph, abort_flag, a.status));
+      if (!ok || poison[s_]) poisoned = true;
+      if (!poisoned) {
+        const int n_valid = min(B, it.tok1 - (it.blk0 + j) * B);
+        const unsigned char* kst = stage0 + s_ * lay.stage_pitch + (h * D + c * VEC) * E;
         const unsigned char* vst = kst + tile_bytes;
-        for (int it0 = w; it0 < NIT; it0 += WPH * CH) {
-          float x[CH];
-#pragma unroll
-          for (int u = 0; u < CH; ++u) {
-            const int it = it0 + u * WPH;
-            const int t = it * TPI + r;
-            float acc = 0.f;
-            if (it < NIT) {
-              if (t < n_valid) {
-                float kv[VEC];
-                Chunk<T>::load(kst + t * row_bytes, kv);
-#pragma unroll
-                for (int v = 0; v < VEC; ++v) acc = fmaf(qv[v], kv[v], acc);
-              }
-#pragma unroll
-              for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
-            }
-            x[u] = (it < NIT && t < n_valid) ? acc : -INFINITY;
+        if constexpr (BFAST > 0) {
+          if (n_valid == BFAST) {
+            frame_fast<T, D, HG>(st, qv, kst, vst, w, r, c);
+          } else {
+            frame_generic<T, D, HG, WPH>(st, qv, kst, vst, B, n_valid, w, r);
           }
-          float cm = x[0];
-#pragma unroll
-          for (int u = 1; u < CH; ++u) cm = fmaxf(cm, x[u]);
-#pragma unroll
-          for (int off = LPR; off < 32; off <<= 1) cm = fmaxf(cm, __shfl_xor_sync(kFull, cm, off));
-          const float m_new = fmaxf(m, cm);
-          if (m_new == -INFINITY) continue;  // nothing valid yet (warp-uniform)
-          const float alpha = ex2(m - m_new);
-          l *= alpha;
-#pragma unroll
-          for (int v = 0; v < VEC; ++v) o[v] *= alpha;
-          m = m_new;
-#pragma unroll
-          for (int u = 0; u < CH; ++u) {
-            const int it = it0 + u * WPH;
-            const int t = it * TPI + r;
-            const float pw = ex2(x[u] - m);
-            if (it < NIT && t < n_valid) {
-              l += pw;
-              float vv[VEC];
-              Chunk<T>::load(vst + t * row_bytes, vv);
-#pragma unroll
-              for (int v = 0; v < VEC; ++v) o[v] = fmaf(pw, vv[v], o[v]);
-            }
-          }
+        } else {
+          frame_generic<T, D, HG, WPH>(st, qv, kst, vst, B, n_valid, w, r);
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8u * st);
+      if (lane == 0) mbar_arrive(bar_empty + 8u * s_);
     }
 
-    // ---- epilogue: combine row groups, then warps of the head -------------------------------
+    // ---- epilogue: fold the unrolled path's weights, combine row groups, then warps ----
+    if constexpr (BFAST > 0) {
+      float lf = st.lf;
+#pragma unroll
+      for (int off = 2; off < LPR; off <<= 1) lf += __shfl_xor_sync(kFull, lf, off);
+      st.l += lf;
+    }
+    float l = st.l, m = st.m;
+    float o[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) o[v] = st.o[v];
 #pragma unroll
     for (int off = LPR; off < 32; off <<= 1) {
       l += __shfl_xor_sync(kFull, l, off);
@@ -493,53 +691,63 @@ __global__ void __launch_bounds__(32 * (HG * WPH + 1), 2)
       for (int v = 0; v < VEC; ++v) o[v] += __shfl_xor_sync(kFull, o[v], off);
     }
     if constexpr (WPH > 1) {
-      named_bar(1, NCW * 32);  // previous item's readers are done with the scratch
+      const uint32_t cph = static_cast<uint32_t>(nc & 1);
       float* mine = comb + (h * WPH + w) * (D + 2);
-      if (lane < LPR) {
+      if (w > 0) {
+        // wait until warp 0 has read the previous item's states, then publish ours
+        const bool free_ok =
+            __all_sync(kFull, mbar_wait(bar_cempty + 8u * h, cph ^ 1u, abort_flag, a.status));
+        if (free_ok && lane < LPR) {
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) mine[c * VEC + v] = o[v];
-        if (c == 0) {
-          mine[D] = m;
-          mine[D + 1] = l;
+          for (int v = 0; v < VEC; ++v) mine[c * VEC + v] = o[v];
+          if (c == 0) {
+            mine[D] = m;
+            mine[D + 1] = l;
+          }
         }
-      }
-      named_bar(1, NCW * 32);
-      if (w == 0) {
-        float M = -INFINITY;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_cfull + 8u * h);
+      } else {
+        const bool have = __all_sync(kFull, mbar_wait(bar_cfull + 8u * h, cph, abort_flag, a.status));
+        if (!have) poisoned = true;
+        float M = m;
 #pragma unroll
-        for (int ww = 0; ww < WPH; ++ww) M = fmaxf(M, comb[(h * WPH + ww) * (D + 2) + D]);
-        l = 0.f;
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) o[v] = 0.f;
+        for (int ww = 1; ww < WPH; ++ww) M = fmaxf(M, comb[(h * WPH + ww) * (D + 2) + D]);
         if (M != -INFINITY) {
+          const float s0 = ex2(m - M);
+          l *= s0;
 #pragma unroll
-          for (int ww = 0; ww < WPH; ++ww) {
+          for (int v = 0; v < VEC; ++v) o[v] *= s0;
+#pragma unroll
+          for (int ww = 1; ww < WPH; ++ww) {
             const float* src = comb + (h * WPH + ww) * (D + 2);
             const float sc = ex2(src[D] - M);
             l = fmaf(sc, src[D + 1], l);
-            if (lane < LPR) {
 #pragma unroll
-              for (int v = 0; v < VEC; ++v) o[v] = fmaf(sc, src[c * VEC + v], o[v]);
-            }
+            for (int v = 0; v < VEC; ++v) o[v] = fmaf(sc, src[c * VEC + v], o[v]);
           }
         }
         m = M;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_cempty + 8u * h);
       }
+      ++nc;
     }
     if (w == 0 && lane < LPR) {
-      if (single) {
+      if (it.single) {
         float res[VEC];
         const bool zero = poisoned || !(l > 0.f);
         const float inv = zero ? 0.f : 1.f / l;
 #pragma unroll
         for (int v = 0; v < VEC; ++v) res[v] = zero ? 0.f : o[v] * inv;
-        T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(s) * a.out_row +
+        T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(it.s) * a.out_row +
                 static_cast<int64_t>(head) * D + c * VEC;
         Chunk<T>::store(op, res);
       } else {
         float* wo = a.ws_o + (static_cast<int64_t>(item) * HG + h) * D + c * VEC;
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) wo[v] = o[v];
+        for (int v = 0; v < VEC; v += 4)
+          *reinterpret_cast<float4*>(wo + v) = make_float4(o[v], o[v + 1], o[v + 2], o[v + 3]);
         if (c == 0) {
           float* wml = a.ws_ml + (static_cast<int64_t>(item) * HG + h) * 2;
           wml[0] = m;
@@ -550,8 +758,10 @@ __global__ void __launch_bounds__(32 * (HG * WPH + 1), 2)
   }
 }
 
-// Log-sum-exp merge of the partitions of every split (sequence, head).
-// out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p, M = max_p m_p (log2 units).
+// Log-sum-exp merge of the partitions of every split (sequence, head):
+// out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p with M = max_p m_p (log2 units).
+// The item ids of a sequence's partitions come from the offsets the decode kernel
+// stored: full partitions at offa[s] + p*G + g, the last one at a_total + offb[s] + g.
 template <typename T, int D>
 __global__ void __launch_bounds__(D) merge_kernel(const DecodeArgs a, const int HG) {
   const int s = blockIdx.x / a.H;
@@ -559,23 +769,27 @@ __global__ void __launch_bounds__(D) merge_kernel(const DecodeArgs a, const int 
   const int d = threadIdx.x;
   const int L = valid_len(a, s);
   if (L < 0) return;
-  const int P = a.ws_off[a.S + 1];
-  const int np = parts_of(L, P);
+  const int32_t* offa = a.ws_off;
+  const int32_t* offb = a.ws_off + a.S + 1;
+  const int a_total = a.ws_off[2 * a.S + 2];
+  const int P = a.ws_off[2 * a.S + 3];
+  const int nf = full_parts(L, P);
+  const int np = nf + last_part(L, P);
   if (np <= 1) return;
   const int g = head / HG;
   const int h = head - g * HG;
-  const int base = a.ws_off[s] + g;
+  auto item_of = [&](int p) { return p < nf ? offa[s] + p * a.G + g : a_total + offb[s] + g; };
   float M = -INFINITY;
   bool bad = false;
   for (int p = 0; p < np; ++p) {
-    const float* ml = a.ws_ml + (static_cast<int64_t>(base + p * a.G) * HG + h) * 2;
+    const float* ml = a.ws_ml + (static_cast<int64_t>(item_of(p)) * HG + h) * 2;
     M = fmaxf(M, ml[0]);
     bad |= ml[1] < 0.f;
   }
   float num = 0.f, den = 0.f;
   if (!bad && M != -INFINITY) {
     for (int p = 0; p < np; ++p) {
-      const int64_t it = static_cast<int64_t>(base + p * a.G) * HG + h;
+      const int64_t it = static_cast<int64_t>(item_of(p)) * HG + h;
       const float sc = ex2(a.ws_ml[it * 2] - M);
       den = fmaf(sc, a.ws_ml[it * 2 + 1], den);
       num = fmaf(sc, a.ws_o[it * D + d], num);
@@ -587,14 +801,14 @@ __global__ void __launch_bounds__(D) merge_kernel(const DecodeArgs a, const int 
 }
 
 // ---- host-side launcher for one element type ----------------------------------------------
-template <typename T, int D, int HG, int WPH>
+template <typename T, int D, int HG, int WPH, int BFAST>
 cudaError_t launch_one(const DecodeArgs& a, const DecodeCfg& c, const CUtensorMap& tk, const CUtensorMap& tv,
                        cudaStream_t stream, bool query_only, int* max_ctas) {
   constexpr int NCW = HG * WPH;
   const uint32_t stage_bytes = 2u * static_cast<uint32_t>(a.B) * HG * D * sizeof(T);
   const Layout lay(c.stages, stage_bytes, a.S, NCW, D);
   const size_t smem = lay.total;
-  auto kern = decode_kernel<T, D, HG, WPH>;
+  auto kern = decode_kernel<T, D, HG, WPH, BFAST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (query_only) {
@@ -605,7 +819,7 @@ cudaError_t launch_one(const DecodeArgs& a, const DecodeCfg& c, const CUtensorMa
   }
   kern<<<c.grid, 32 * (NCW + 1), smem, stream>>>(tk, tv, a, c.stages);
   e = cudaGetLastError();
-  if (e != cudaSuccess || a.ws_off == nullptr) return e;
+  if (e != cudaSuccess || a.ws_o == nullptr) return e;
   merge_kernel<T, D><<<a.S * a.H, D, 0, stream>>>(a, HG);
   return cudaGetLastError();
 }
@@ -613,11 +827,16 @@ cudaError_t launch_one(const DecodeArgs& a, const DecodeCfg& c, const CUtensorMa
 template <typename T, int D>
 cudaError_t launch_d(const DecodeArgs& a, const DecodeCfg& c, const CUtensorMap& tk, const CUtensorMap& tv,
                      cudaStream_t stream, bool query_only, int* max_ctas) {
-#define PA_DK_CASE(hg, wph)                                                          \
-  if (c.heads_per_cta == hg && c.warps_per_head == wph)                              \
-    return launch_one<T, D, hg, wph>(a, c, tk, tv, stream, query_only, max_ctas);
-  PA_DK_CASE(1, 4) PA_DK_CASE(1, 8)
-  PA_DK_CASE(2, 2) PA_DK_CASE(2, 4)
+  constexpr bool kFastRows = D * sizeof(T) == 256;
+  const bool fast = kFastRows && c.fast && (a.B == 16 * c.warps_per_head);
+#define PA_DK_CASE(hg, wph)                                                                         \
+  if (c.heads_per_cta == hg && c.warps_per_head == wph) {                                           \
+    if constexpr (kFastRows && (wph == 1 || wph == 2))                                              \
+      if (fast) return launch_one<T, D, hg, wph, 16 * wph>(a, c, tk, tv, stream, query_only, max_ctas); \
+    return launch_one<T, D, hg, wph, 0>(a, c, tk, tv, stream, query_only, max_ctas);                \
+  }
+  PA_DK_CASE(1, 1) PA_DK_CASE(1, 2) PA_DK_CASE(1, 4) PA_DK_CASE(1, 8)
+  PA_DK_CASE(2, 1) PA_DK_CASE(2, 2) PA_DK_CASE(2, 4)
   PA_DK_CASE(4, 1) PA_DK_CASE(4, 2)
 #undef PA_DK_CASE
   return cudaErrorInvalidValue;

@@ -51,10 +51,12 @@ struct DecodeArgs {
   int32_t fixed_part;
   int32_t target_items;
   int32_t min_part;
-  // split workspace (null when no sequence can be split)
-  float* ws_ml;                 // [items][HG][2] = (running max in log2 units, sum)
-  float* ws_o;                  // [items][HG][D] unnormalised partial outputs
-  int32_t* ws_off;              // [S + 2]: item offset per sequence, then the partition length
+  // workspace
+  int32_t* sched;               // [2]: next item, retired blocks (zero between launches)
+  int32_t* ws_off;              // [2S + 4]: full-partition offsets [S+1], last-partition
+                                // offsets [S+1], number of full-partition items, partition length
+  float* ws_ml;                 // [items][HG][2] = (running max in log2 units, sum); null if no split
+  float* ws_o;                  // [items][HG][D] unnormalised partial outputs; null if no split
   int32_t* status;
 };
 
@@ -65,6 +67,7 @@ struct DecodeCfg {
   int warps_per_head;
   int stages;
   int grid;          // persistent thread blocks
+  bool fast;         // allow the unrolled full-frame path (256-byte rows, B = 16 * warps_per_head)
 };
 
 // per-dtype launchers (one translation unit each).  query_only: set the kernel's

@@ -147,8 +147,13 @@ class PagedKVEngine:
                   dev[:n], scale, out, stream=self._stream(), params=params)
         return out
 
-    def decode_step(self, seqs, k_rows, v_rows, q, scale: float, out=None, params=None):
-        """append + attend with one staged upload: the whole hot path of one step."""
+    def decode_step(self, seqs, k_rows, v_rows, q, scale: float, out=None, params=None, events=None):
+        """append + attend with one staged upload: the whole hot path of one step.
+
+        ``events`` (start, end): CUDA events recorded on the engine stream around
+        the pa_decode call (decode kernel + merge), for timing.
+        Returns (out, number of copy-on-write pairs, staged context lengths view).
+        """
         ids = self._ids_for(seqs)
         n = len(ids)
         mb = self.max_blocks
@@ -166,9 +171,13 @@ class PagedKVEngine:
         pa_cache_append(k_rows, v_rows, dev[:n], self.k_cache, self.v_cache, stream=st)
         if out is None:
             out = torch.empty_like(q)
+        if events is not None:
+            events[0].record(st)
         pa_decode(q, self.k_cache, self.v_cache, dev[4 * n:4 * n + n * mb].view(n, mb), dev[3 * n:4 * n],
                   scale, out, stream=st, params=params)
-        return out, nc
+        if events is not None:
+            events[1].record(st)
+        return out, nc, lens
 
 
 def run_workload_ops(engine: PagedKVEngine, w, attend_params=None):

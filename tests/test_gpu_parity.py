@@ -35,13 +35,45 @@ def test_split_modes_agree_with_oracle(pa, cfg, mode):
     check_outputs(w, outs, ref)
 
 
-@pytest.mark.parametrize("hg,wph", [(1, 4), (1, 8), (2, 2), (2, 4), (4, 1), (4, 2)])
-@pytest.mark.parametrize("stages", [2, 5])
-def test_launch_shapes(pa, hg, wph, stages):
-    w = workloads.custom([1, 15, 16, 17, 200, 333, 700], H=8, D=128, B=16, dtype="f16", seed=11)
-    params = {"heads_per_cta": hg, "warps_per_head": wph, "stages": stages, "partition_tokens": 64}
+@pytest.mark.parametrize("hg,wph", [(1, 1), (1, 2), (1, 4), (1, 8), (2, 1), (2, 2), (2, 4), (4, 1), (4, 2)])
+@pytest.mark.parametrize("stages", [2, 3])
+@pytest.mark.parametrize("B,dtype", [(16, "f16"), (32, "bf16")])
+def test_launch_shapes(pa, hg, wph, stages, B, dtype):
+    """Every built (heads per block, warps per head) pair; B = 16 * warps per head takes
+    the unrolled full-frame path, the rest (and every partly filled frame) the generic one."""
+    w = workloads.custom([1, 15, 16, 17, 33, 200, 333, 700], H=8, D=128, B=B, dtype=dtype, seed=11)
+    params = {"heads_per_cta": hg, "warps_per_head": wph, "stages": stages, "partition_tokens": 4 * B}
     eng, outs, ref = run_both(pa, w, params=params)
     check_outputs(w, outs, ref)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 4])
+def test_generic_path_on_fast_shapes(pa, cfg):
+    w = workloads.build(cfg, small=True)
+    eng, outs, ref = run_both(pa, w, params={"generic_only": 1})
+    check_outputs(w, outs, ref)
+
+
+def test_repeated_launches_identical(pa):
+    """The work counter resets itself: back-to-back launches, on one stream and on two
+    streams, give the same bits."""
+    w = workloads.custom([300, 1000, 17, 4000, 2048], H=8, D=128, B=16, dtype="f16", seed=21)
+    eng, outs, ref = run_both(pa, w)
+    (op,) = [i for i, o in enumerate(w.ops) if o[0] == "attend"]
+    q = pa.to_device_rows(w.query(op), w.dtype, eng.device)
+    first = outs[op].clone()
+    for _ in range(5):
+        again = eng.attend(w.ops[op][1], q, w.scale)
+        assert torch.equal(again, first)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        again = eng.attend(w.ops[op][1], q, w.scale)
+    side.synchronize()
+    assert torch.equal(again, first)
+    for items in (1, 2, 16):
+        o = eng.attend(w.ops[op][1], q, w.scale, params={"items_per_cta": items})
+        assert_attention_close(o, ref.outputs[op], w.dtype)
+    assert pa.pa_get_device_status() == 0
 
 
 EDGE = [
