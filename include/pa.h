@@ -54,6 +54,7 @@ enum pa_dtype { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_I32 = 3 };
 #define PA_ERR_CUDA          -9   /* a CUDA runtime call or launch failed */
 #define PA_ERR_UNSUPPORTED  -10   /* head_dim / dtype / size outside the built kernels */
 #define PA_ERR_CAPACITY     -11   /* caller-provided output buffer too small */
+#define PA_ERR_SCRATCH_LIMIT -12  /* pa_decode_static: scratch need exceeds its fixed array */
 
 /* ---- sticky device status bits (pa_get_device_status) ------------------------------ */
 #define PA_DEV_BAD_SLOT   0x1   /* append: slot >= num_blocks*block_size */
@@ -161,6 +162,36 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
                  const pa_tensor* block_tables, const pa_tensor* context_lens,
                  float scale, const pa_tensor* out, const pa_decode_params* params,
                  pa_stream stream);
+
+/*
+ * pa_decode_static -- pa_decode that allocates nothing.  (No counterpart in the
+ * pages: an addition for callers that cannot allocate device memory.)
+ *
+ * Who needs it: a process whose device memory is entirely owned by its own pool
+ * allocator (a cudaMalloc from this library could fail or fragment that pool), or
+ * a latency-bound loop that cannot take the device-wide synchronisation of a
+ * first cudaMalloc.  pa_decode would allocate its workspace on first use; this
+ * entry point instead uses a fixed 16 MiB scratch array compiled into the library
+ * (a file-scope __device__ array that every GPU which loads the library keeps
+ * until the process exits).
+ *
+ * Arguments, results and error checks are those of pa_decode with automatic
+ * launch options; the caller still provides every input and output.
+ *   - Returns PA_ERR_SCRATCH_LIMIT, launching nothing, when the problem needs more
+ *     than 16 MiB of scratch: 256 B of counters, (2*S + 4) int32 offsets, and for
+ *     contexts that get split about (4 * resident thread blocks + S*H/heads_per_cta)
+ *     items of heads_per_cta*(head_dim + 2) floats (about 3.6 MiB for 64 sequences
+ *     of up to 2048 tokens with 32 heads of 128).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call before
+ *     any stream capture.
+ *   - Every call shares the one array and each call zeroes its counters with
+ *     cudaMemsetAsync on `stream` before the kernels: calls whose kernels overlap on
+ *     the GPU (different streams, or other threads) race on it.  Serialise them.
+ */
+int pa_decode_static(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                     const pa_tensor* block_tables, const pa_tensor* context_lens,
+                     float scale, const pa_tensor* out, pa_stream stream);
 
 /* Synchronises `stream`, returns the current device's sticky PA_DEV_* bits in
  * *status_out and clears them. */

@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     PA_DEV_BAD_SLOT,
     PA_DEV_TIMEOUT,
     PA_ERR_OUT_OF_BLOCKS,
+    PA_ERR_SCRATCH_LIMIT,
     PA_ERR_SEQ_EXISTS,
     PA_ERR_UNKNOWN_SEQ,
     PA_WARN_DOUBLE_FREE,
@@ -25,6 +26,7 @@ from ._binding import (  # noqa: F401
     pa_copy_blocks,
     pa_decode,
     pa_decode_ex,
+    pa_decode_static,
     pa_get_device_status,
     pa_launch_count,
     pa_shutdown,

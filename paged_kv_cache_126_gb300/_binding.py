@@ -21,6 +21,7 @@ PA_WARN_DOUBLE_FREE = 1
 PA_ERR_OUT_OF_BLOCKS = -6
 PA_ERR_UNKNOWN_SEQ = -7
 PA_ERR_SEQ_EXISTS = -8
+PA_ERR_SCRATCH_LIMIT = -12
 
 PA_DEV_BAD_SLOT = 0x1
 PA_DEV_BAD_BLOCK = 0x2
@@ -61,6 +62,7 @@ def _load():
         "pa_copy_blocks": ([P, P, P, vp], C.c_int),
         "pa_decode": ([P, P, P, P, P, C.c_float, P, vp], C.c_int),
         "pa_decode_ex": ([P, P, P, P, P, C.c_float, P, C.POINTER(PaDecodeParams), vp], C.c_int),
+        "pa_decode_static": ([P, P, P, P, P, C.c_float, P, vp], C.c_int),
         "pa_get_device_status": ([vp, i32p], C.c_int),
         "pa_strerror": ([C.c_int], C.c_char_p),
         "pa_launch_count": ([], C.c_int64),
@@ -90,7 +92,7 @@ def _load():
 
 LIB = _load()
 EXPORTED = (
-    "pa_cache_append", "pa_copy_blocks", "pa_decode", "pa_decode_ex", "pa_get_device_status",
+    "pa_cache_append", "pa_copy_blocks", "pa_decode", "pa_decode_ex", "pa_decode_static", "pa_get_device_status",
     "pa_strerror", "pa_launch_count", "pa_shutdown", "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq",
     "pa_bm_append", "pa_bm_step", "pa_bm_fork", "pa_bm_free", "pa_bm_block_tables", "pa_bm_seq_info",
     "pa_bm_table", "pa_bm_slot", "pa_bm_num_free", "pa_bm_free_list", "pa_bm_ref_counts",
@@ -176,6 +178,17 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, strea
 def pa_decode_ex(q, k_cache, v_cache, block_tables, context_lens, scale, out, params=None, stream=None):
     return pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, stream=stream,
                      params=params or {})
+
+
+def pa_decode_static(q, k_cache, v_cache, block_tables, context_lens, scale, out, stream=None):
+    """pa_decode without any device allocation: scratch comes from a fixed 16 MiB array
+    inside libpa (for callers whose device memory belongs to their own allocator).
+    Calls must not overlap on the GPU; see include/pa.h."""
+    st = _stream_of(q, stream)
+    ds = [tensor_desc(t) for t in (q, k_cache, v_cache, block_tables, context_lens)]
+    o = tensor_desc(out)
+    _check(LIB.pa_decode_static(*map(_ref, ds), C.c_float(scale), C.byref(o), st), "pa_decode_static")
+    return out
 
 
 def pa_get_device_status(stream=None) -> int:

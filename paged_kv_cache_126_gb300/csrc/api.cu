@@ -205,6 +205,7 @@ const char* pa_strerror(int code) {
     case PA_ERR_CUDA: return "CUDA runtime error";
     case PA_ERR_UNSUPPORTED: return "size or dtype outside the built kernels";
     case PA_ERR_CAPACITY: return "output buffer too small";
+    case PA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the fixed 16 MiB array of pa_decode_static";
     default: return "unknown code";
   }
 }
@@ -451,3 +452,145 @@ int pa_decode(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_c
 }
 
 }  // extern "C"
+
+// ---- decode without any allocation ---------------------------------------------------------
+// Some callers may not allocate device memory at all: a serving process that has
+// handed the whole device to its own pool allocator (a cudaMalloc behind its back
+// can fail or fragment the pool), or a latency-bound loop that cannot afford the
+// device-wide synchronisation a first cudaMalloc brings.  For them
+// pa_decode_static runs the same kernels with the scratch memory taken from this
+// fixed array, which every device that loads the library holds until the process
+// exits.  Host code must not use the array's name as a device address: it is a
+// host-side stand-in.  The address is looked up once per device with
+// cudaGetSymbolAddress, with that device current.
+constexpr size_t kFixedScratchBytes = static_cast<size_t>(16) << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_pa_fixed_scratch[kFixedScratchBytes];
+
+namespace {
+struct FixedScratch {
+  std::once_flag once;
+  unsigned char* ptr = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+FixedScratch g_fixed[kMaxDevices];
+
+int fixed_scratch(int dev, unsigned char** out) {
+  FixedScratch& f = g_fixed[dev];
+  std::call_once(f.once, [&] { f.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&f.ptr), g_pa_fixed_scratch); });
+  if (f.err != cudaSuccess || f.ptr == nullptr) return PA_ERR_CUDA;
+  *out = f.ptr;
+  return PA_OK;
+}
+}  // namespace
+
+extern "C" int pa_decode_static(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                                const pa_tensor* block_tables, const pa_tensor* context_lens, float scale,
+                                const pa_tensor* out, pa_stream stream) {
+  // Same checks and automatic launch choices as pa_decode.
+  PA_TRY(check_cache(k_cache, v_cache));
+  const int dt = k_cache->dtype;
+  const int64_t nb = k_cache->shape[0], B = k_cache->shape[1], H = k_cache->shape[2], D = k_cache->shape[3];
+  PA_TRY(check_rows(q, dt, H, D));
+  PA_TRY(check_rows(out, dt, H, D));
+  if (!block_tables || !context_lens) return PA_ERR_INVALID;
+  PA_TRY(check_i32(block_tables, 2));
+  PA_TRY(check_i32(context_lens, 1));
+  const int64_t S = q->shape[0];
+  if (out->shape[0] != S || block_tables->shape[0] != S || context_lens->shape[0] != S) return PA_ERR_SHAPE;
+  const int64_t max_blocks = block_tables->shape[1];
+  if (max_blocks < 0 || (S > 1 && block_tables->stride[0] < max_blocks)) return PA_ERR_STRIDE;
+  if (B > 256) return PA_ERR_UNSUPPORTED;
+  if (!(D == 64 || D == 128 || (D == 256 && dt != PA_F32))) return PA_ERR_UNSUPPORTED;
+  if (max_blocks * B > INT32_MAX || S > 65536) return PA_ERR_UNSUPPORTED;
+  if (S == 0) return PA_OK;
+  if (max_blocks > 0 && !block_tables->data) return PA_ERR_INVALID;
+
+  int dev;
+  PA_TRY(current_device(&dev));
+  unsigned char* scratch = nullptr;
+  PA_TRY(fixed_scratch(dev, &scratch));
+  const int e = elem_bytes(dt);
+
+  pa::DecodeCfg c;
+  c.dtype = dt;
+  c.D = static_cast<int>(D);
+  c.heads_per_cta = 1;
+  for (int hg : {4, 2}) {
+    if (H % hg == 0 && 2 * B * hg * D * e <= 32768) {
+      c.heads_per_cta = hg;
+      break;
+    }
+  }
+  const bool fast_rows = D * e == 256 && (B == 16 || B == 32);
+  c.warps_per_head = fast_rows ? static_cast<int>(B / 16) : 8 / c.heads_per_cta;
+  c.fast = fast_rows;
+  const size_t smem_cap = 227 * 1024;
+  c.stages = 0;
+  for (int st = 8; st >= 3; --st) {
+    c.stages = st;
+    if (pa::decode_smem_bytes(c, e, static_cast<int>(B), static_cast<int>(S)) <= smem_cap / 2 - 1024) break;
+    c.stages = 0;
+  }
+  if (c.stages == 0) {
+    for (int st = 8; st >= 2; --st) {
+      c.stages = st;
+      if (pa::decode_smem_bytes(c, e, static_cast<int>(B), static_cast<int>(S)) <= smem_cap) break;
+      c.stages = 0;
+    }
+  }
+  if (c.stages == 0) return PA_ERR_UNSUPPORTED;
+
+  pa::DecodeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = q->data;
+  a.out = out->data;
+  a.q_row = q->stride[0];
+  a.out_row = out->stride[0];
+  a.block_tables = static_cast<const int32_t*>(block_tables->data);
+  a.bt_row = block_tables->stride[0];
+  a.context_lens = static_cast<const int32_t*>(context_lens->data);
+  a.S = static_cast<int32_t>(S);
+  a.H = static_cast<int32_t>(H);
+  a.B = static_cast<int32_t>(B);
+  a.num_blocks = static_cast<int32_t>(nb);
+  a.max_blocks = static_cast<int32_t>(max_blocks);
+  a.G = static_cast<int32_t>(H / c.heads_per_cta);
+  a.qk_scale_log2 = scale * 1.4426950408889634f;
+  a.status = g_dev[dev].status;
+
+  CUtensorMap tk, tv;
+  PA_TRY(make_cache_map(&tk, k_cache->data, dt, nb, B, H, D, c.heads_per_cta));
+  PA_TRY(make_cache_map(&tv, v_cache->data, dt, nb, B, H, D, c.heads_per_cta));
+  int occ = 0;
+  if (dispatch_decode(a, c, tk, tv, nullptr, true, &occ) != cudaSuccess || occ <= 0) return PA_ERR_CUDA;
+  c.grid = g_dev[dev].num_sms * occ;
+
+  // Scratch layout: counters | offsets | split partials, all inside the fixed array.
+  const int64_t Lcap = max_blocks * B;
+  int64_t items_max = 0;
+  if (Lcap == 0) {
+    a.fixed_part = static_cast<int32_t>(B);
+  } else {
+    a.fixed_part = 0;
+    a.target_items = 4 * c.grid;
+    a.min_part = round_up(256, B);
+    if (a.min_part < Lcap)
+      items_max = std::min<int64_t>(S * a.G * ((Lcap + a.min_part - 1) / a.min_part), a.target_items + S * a.G);
+  }
+  const size_t off_bytes = (static_cast<size_t>(2 * S + 4) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
+  const size_t ml_bytes = static_cast<size_t>(items_max) * c.heads_per_cta * 2 * sizeof(float);
+  const size_t o_bytes = static_cast<size_t>(items_max) * c.heads_per_cta * D * sizeof(float);
+  if (kSchedBytes + off_bytes + o_bytes + ml_bytes > kFixedScratchBytes) return PA_ERR_SCRATCH_LIMIT;
+  a.sched = reinterpret_cast<int32_t*>(scratch);
+  a.ws_off = reinterpret_cast<int32_t*>(scratch + kSchedBytes);
+  if (items_max > 0) {
+    a.ws_o = reinterpret_cast<float*>(scratch + kSchedBytes + off_bytes);
+    a.ws_ml = reinterpret_cast<float*>(scratch + kSchedBytes + off_bytes + o_bytes);
+  }
+  // The work counters must start at zero; the array keeps whatever the last call left.
+  if (cudaMemsetAsync(scratch, 0, kSchedBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
+  if (dispatch_decode(a, c, tk, tv, static_cast<cudaStream_t>(stream), false, nullptr) != cudaSuccess)
+    return PA_ERR_CUDA;
+  g_launches.fetch_add(a.ws_o ? 2 : 1);
+  return PA_OK;
+}

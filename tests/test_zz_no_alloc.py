@@ -1,0 +1,70 @@
+"""pa_decode_static: decode attention that allocates no device memory (GPU).
+
+Some callers cannot let a library call cudaMalloc: a serving process whose
+device memory is owned by its own pool allocator, or a latency-bound loop that
+cannot take the device-wide synchronisation of a first allocation.  For them
+pa_decode_static takes its scratch from a fixed 16 MiB array compiled into
+libpa.  These tests call it through the C ABI and compare it with pa_decode on
+the same inputs, on two calls in a row (the array keeps the previous call's
+contents), and check that a problem needing more scratch than the array holds is
+refused without launching anything.
+
+This file is collected last on purpose: it should pass alone in a fresh process
+and after every other test.
+"""
+
+import pytest
+import torch
+
+import workloads
+from tests._gpu_common import assert_attention_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _engine_batch(pa, w):
+    eng = pa.PagedKVEngine(w.num_blocks, w.block_size, w.num_heads, w.head_dim, w.dtype,
+                           free_order=w.free_order, max_seqs=max(64, len(w.final_lens)),
+                           max_blocks_per_seq=max(1, max(-(-L // w.block_size) for L in w.final_lens.values())))
+    pa.run_workload_ops(eng, w)
+    (op,) = w.attend_ops
+    seqs = w.ops[op][1]
+    tables, lens = eng.bm.block_tables(seqs, eng.max_blocks)
+    q = pa.to_device_rows(w.query(op), w.dtype, eng.device)
+    return eng, q, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda()
+
+
+@pytest.mark.parametrize("lengths,H,B,dtype", [
+    ([300, 1000, 17, 4000, 2048, 0, 1, 16], 8, 16, "f16"),   # split contexts + merge, unrolled path
+    ([2500, 5, 700, 33], 4, 32, "bf16"),                     # two warps per head
+    ([9, 130, 41], 3, 10, "f32"),                            # generic path, B not a power of two
+])
+def test_static_scratch_matches_pa_decode(pa, lengths, H, B, dtype):
+    w = workloads.custom(lengths, H=H, D=128 if dtype != "f32" else 64, B=B, dtype=dtype, seed=77)
+    eng, q, tables, lens = _engine_batch(pa, w)
+    ref = torch.empty_like(q)
+    pa.pa_decode(q, eng.k_cache, eng.v_cache, tables, lens, w.scale, ref)
+    torch.cuda.synchronize()
+    ref64 = ref.double().cpu().numpy()
+    for _ in range(2):  # the second call starts from the first call's leftovers
+        out = torch.full_like(q, float("nan"))
+        pa.pa_decode_static(q, eng.k_cache, eng.v_cache, tables, lens, w.scale, out)
+        torch.cuda.synchronize()
+        assert_attention_close(out, ref64, dtype)
+    assert pa.pa_get_device_status() == 0
+
+
+def test_static_scratch_refuses_oversized_problem(pa):
+    S, H, D, B, nb, mb = 4096, 32, 128, 16, 64, 20   # needs ~70 MB of split partials
+    kc = torch.zeros(nb, B, H, D, dtype=torch.float16, device="cuda")
+    q = torch.zeros(S, H, D, dtype=torch.float16, device="cuda")
+    out = torch.full_like(q, 3.0)
+    tables = torch.zeros(S, mb, dtype=torch.int32, device="cuda")
+    lens = torch.zeros(S, dtype=torch.int32, device="cuda")
+    n0 = pa.pa_launch_count()
+    with pytest.raises(pa.PAError) as ei:
+        pa.pa_decode_static(q, kc, kc, tables, lens, 0.1, out)
+    assert ei.value.code == pa.PA_ERR_SCRATCH_LIMIT
+    assert pa.pa_launch_count() == n0
+    torch.cuda.synchronize()
+    assert torch.all(out == 3.0)
