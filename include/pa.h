@@ -151,8 +151,10 @@ typedef struct pa_decode_params {
   int32_t warps_per_head;    /* 1, 2, 4 or 8 */
   int32_t stages;            /* K/V staging buffers per thread block, 2..8 */
   int32_t ctas_per_sm;       /* persistent grid = SMs x this (clamped to occupancy) */
-  int32_t items_per_cta;     /* automatic partition length aims at this many work items per
-                                thread block (default 4) */
+  int32_t items_per_cta;     /* 0 (default): keep whole sequences when they already give
+                                every thread block work and the longest is at most the
+                                average load per block, else aim at 1.5 work items per
+                                thread block; >0: always aim at this many */
   int32_t generic_only;      /* 1: never take the unrolled full-frame path (testing) */
   int32_t reserved;
 } pa_decode_params;
@@ -178,10 +180,11 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
  * Arguments, results and error checks are those of pa_decode with automatic
  * launch options; the caller still provides every input and output.
  *   - Returns PA_ERR_SCRATCH_LIMIT, launching nothing, when the problem needs more
- *     than 16 MiB of scratch: 256 B of counters, (2*S + 4) int32 offsets, and for
- *     contexts that get split about (4 * resident thread blocks + S*H/heads_per_cta)
- *     items of heads_per_cta*(head_dim + 2) floats (about 3.6 MiB for 64 sequences
- *     of up to 2048 tokens with 32 heads of 128).
+ *     than 16 MiB of scratch: 256 B of work counters and, when a context may be
+ *     split, S*H int32 arrival counters plus room for up to
+ *     (3 * resident thread blocks + S*H/heads_per_cta) partial results of
+ *     heads_per_cta*(head_dim + 2) floats each (about 6 MiB for 64 sequences of up
+ *     to 2048 tokens with 32 heads of 128).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call before
  *     any stream capture.

@@ -82,20 +82,28 @@ int make_cache_map(CUtensorMap* map, void* base, int dtype, int64_t nb, int64_t 
 }
 
 // ---- library-owned workspace, one per (device, stream) -------------------------------------
-// Layout: [0, 256) scheduler counters (zeroed at allocation; each decode launch
-// leaves them zero), then the per-launch offsets and split partials.
+// Layout: [0, 256) scheduler counters | arrival counters, one per (sequence, head) |
+// per-launch offsets and split partials.  Both counter regions must hold zeros
+// when a launch starts; every decode launch leaves them zero.  They are zeroed when
+// first allocated and whenever the arrival-counter region grows.
 constexpr size_t kSchedBytes = 256;
 
 struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
+  size_t cnt_bytes = 0;  // arrival-counter region known to hold zeros
 };
 std::mutex g_ws_mu;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 
-int workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Returns the workspace base and the size of its arrival-counter region (>= cnt_need).
+int workspace(int dev, cudaStream_t stream, size_t cnt_need, size_t rest_bytes, void** out, size_t* cnt_bytes) {
   std::lock_guard<std::mutex> lk(g_ws_mu);
   Workspace& w = g_ws[{dev, stream}];
+  const size_t cnt = std::max(round256(cnt_need), w.cnt_bytes);
+  const size_t bytes = kSchedBytes + cnt + rest_bytes;
   if (w.bytes < bytes) {
     if (w.ptr) {
       // the old buffer may still be used by earlier launches on this stream
@@ -103,13 +111,24 @@ int workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
       cudaFree(w.ptr);
       w.ptr = nullptr;
       w.bytes = 0;
+      w.cnt_bytes = 0;
     }
     const size_t grow = std::max(bytes, static_cast<size_t>(1) << 20);
     if (cudaMalloc(&w.ptr, grow) != cudaSuccess) return PA_ERR_CUDA;
-    if (cudaMemsetAsync(w.ptr, 0, kSchedBytes, stream) != cudaSuccess) return PA_ERR_CUDA;
     w.bytes = grow;
   }
+  if (w.cnt_bytes < cnt || w.cnt_bytes == 0) {
+    // zero the scheduler counters and any counter bytes not known to be zero
+    if (w.cnt_bytes == 0) {
+      if (cudaMemsetAsync(w.ptr, 0, kSchedBytes + cnt, stream) != cudaSuccess) return PA_ERR_CUDA;
+    } else {
+      unsigned char* base = static_cast<unsigned char*>(w.ptr) + kSchedBytes + w.cnt_bytes;
+      if (cudaMemsetAsync(base, 0, cnt - w.cnt_bytes, stream) != cudaSuccess) return PA_ERR_CUDA;
+    }
+    w.cnt_bytes = cnt;
+  }
   *out = w.ptr;
+  *cnt_bytes = cnt;
   return PA_OK;
 }
 
@@ -418,31 +437,35 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
     if (a.fixed_part < Lcap) items_max = S * a.G * ((Lcap + a.fixed_part - 1) / a.fixed_part);
   } else if (p.partition_tokens == 0) {
     a.fixed_part = 0;
-    a.target_items = (p.items_per_cta ? p.items_per_cta : 4) * c.grid;
+    a.whole_first = p.items_per_cta == 0;
+    a.target_items = p.items_per_cta ? p.items_per_cta * c.grid : (3 * c.grid) / 2;
     a.min_part = round_up(256, B);
-    if (a.min_part < Lcap)
-      items_max = std::min<int64_t>(S * a.G * ((Lcap + a.min_part - 1) / a.min_part), a.target_items + S * a.G);
+    if (a.min_part < Lcap)  // the kernel may shorten its partitions down to half its first choice
+      items_max = std::min<int64_t>(S * a.G * ((Lcap + a.min_part - 1) / a.min_part), 2 * a.target_items + S * a.G);
   } else {
     return PA_ERR_INVALID;
   }
   {
-    const size_t off_bytes = (static_cast<size_t>(2 * S + 4) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
     const size_t ml_bytes = static_cast<size_t>(items_max) * c.heads_per_cta * 2 * sizeof(float);
     const size_t o_bytes = static_cast<size_t>(items_max) * c.heads_per_cta * D * sizeof(float);
+    const size_t cnt_need = items_max > 0 ? static_cast<size_t>(S * H) * sizeof(int32_t) : 0;
     void* ws = nullptr;
-    PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), kSchedBytes + off_bytes + o_bytes + ml_bytes, &ws));
+    size_t cnt_bytes = 0;
+    PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), cnt_need, o_bytes + ml_bytes, &ws,
+                     &cnt_bytes));
     unsigned char* w = static_cast<unsigned char*>(ws);
+    unsigned char* rest = w + kSchedBytes + cnt_bytes;
     a.sched = reinterpret_cast<int32_t*>(w);
-    a.ws_off = reinterpret_cast<int32_t*>(w + kSchedBytes);
+    a.ws_cnt = reinterpret_cast<int32_t*>(w + kSchedBytes);
     if (items_max > 0) {
-      a.ws_o = reinterpret_cast<float*>(w + kSchedBytes + off_bytes);
-      a.ws_ml = reinterpret_cast<float*>(w + kSchedBytes + off_bytes + o_bytes);
+      a.ws_o = reinterpret_cast<float*>(rest);
+      a.ws_ml = reinterpret_cast<float*>(rest + o_bytes);
     }
   }
 
   if (dispatch_decode(a, c, tk, tv, static_cast<cudaStream_t>(stream), false, nullptr) != cudaSuccess)
     return PA_ERR_CUDA;
-  g_launches.fetch_add(a.ws_o ? 2 : 1);
+  g_launches.fetch_add(1);
   return PA_OK;
 }
 
@@ -572,25 +595,28 @@ extern "C" int pa_decode_static(const pa_tensor* q, const pa_tensor* k_cache, co
     a.fixed_part = static_cast<int32_t>(B);
   } else {
     a.fixed_part = 0;
-    a.target_items = 4 * c.grid;
+    a.whole_first = 1;
+    a.target_items = (3 * c.grid) / 2;
     a.min_part = round_up(256, B);
     if (a.min_part < Lcap)
-      items_max = std::min<int64_t>(S * a.G * ((Lcap + a.min_part - 1) / a.min_part), a.target_items + S * a.G);
+      items_max = std::min<int64_t>(S * a.G * ((Lcap + a.min_part - 1) / a.min_part), 2 * a.target_items + S * a.G);
   }
-  const size_t off_bytes = (static_cast<size_t>(2 * S + 4) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
   const size_t ml_bytes = static_cast<size_t>(items_max) * c.heads_per_cta * 2 * sizeof(float);
   const size_t o_bytes = static_cast<size_t>(items_max) * c.heads_per_cta * D * sizeof(float);
-  if (kSchedBytes + off_bytes + o_bytes + ml_bytes > kFixedScratchBytes) return PA_ERR_SCRATCH_LIMIT;
+  const size_t cnt_bytes = items_max > 0 ? round256(static_cast<size_t>(S * H) * sizeof(int32_t)) : 0;
+  if (kSchedBytes + cnt_bytes + o_bytes + ml_bytes > kFixedScratchBytes) return PA_ERR_SCRATCH_LIMIT;
+  unsigned char* rest = scratch + kSchedBytes + cnt_bytes;
   a.sched = reinterpret_cast<int32_t*>(scratch);
-  a.ws_off = reinterpret_cast<int32_t*>(scratch + kSchedBytes);
+  a.ws_cnt = reinterpret_cast<int32_t*>(scratch + kSchedBytes);
   if (items_max > 0) {
-    a.ws_o = reinterpret_cast<float*>(scratch + kSchedBytes + off_bytes);
-    a.ws_ml = reinterpret_cast<float*>(scratch + kSchedBytes + off_bytes + o_bytes);
+    a.ws_o = reinterpret_cast<float*>(rest);
+    a.ws_ml = reinterpret_cast<float*>(rest + o_bytes);
   }
-  // The work counters must start at zero; the array keeps whatever the last call left.
-  if (cudaMemsetAsync(scratch, 0, kSchedBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
+  // The counters must start at zero; the array keeps whatever the last call left.
+  if (cudaMemsetAsync(scratch, 0, kSchedBytes + cnt_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
   if (dispatch_decode(a, c, tk, tv, static_cast<cudaStream_t>(stream), false, nullptr) != cudaSuccess)
     return PA_ERR_CUDA;
-  g_launches.fetch_add(a.ws_o ? 2 : 1);
+  g_launches.fetch_add(1);
   return PA_OK;
 }

@@ -20,6 +20,10 @@ namespace pa {
 namespace {
 
 __global__ void __launch_bounds__(256) cache_append_kernel(const AppendArgs a) {
+  // Launched with programmatic stream serialisation: let the next kernel start its
+  // set-up now, and wait for the previous kernel's writes before reading inputs.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t nvec = a.row_bytes >> 4;
   for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
     const int32_t slot = __ldg(a.slots + t);
@@ -67,8 +71,16 @@ cudaError_t launch_cache_append(const AppendArgs& a, int num_sms, cudaStream_t s
   const int threads = nvec >= 256 ? 256 : static_cast<int>(((nvec + 31) / 32) * 32);
   const int max_grid = num_sms * 16;
   const int grid = a.T < max_grid ? a.T : max_grid;
-  cache_append_kernel<<<grid, threads, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, cache_append_kernel, a);
 }
 
 cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream) {

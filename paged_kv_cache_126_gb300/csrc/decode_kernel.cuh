@@ -34,7 +34,11 @@
 //   * Epilogue: row groups, then warps of a head (through shared memory, handed
 //     over with mbarriers), are combined by the log-sum-exp rule.  A sequence that
 //     fits in one partition is normalised and written directly; otherwise the
-//     (m, l, o) partial goes to the workspace and merge_kernel combines them.
+//     (m, l, o) partial goes to the workspace, an arrival counter per (sequence,
+//     head) is bumped, and the warp that brings it to the partition count merges
+//     all partials of that head and zeroes the counter -- no second kernel.
+//   * Launched with programmatic stream serialisation: barrier set-up overlaps the
+//     tail of the previous kernel; griddepcontrol.wait precedes every input read.
 //   * Bad frame ids / context lengths: the affected output rows become zeros and a
 //     sticky status bit is set.  Every wait is an mbarrier wait with a bound; a
 //     wait that gives up sets PA_DEV_TIMEOUT, turns all later waits of the block
@@ -202,15 +206,17 @@ struct Chunk<__nv_bfloat16> {
 
 // ---- shared-memory layout (host and device agree) -------------------------------------------
 struct Layout {
-  uint32_t stage_pitch, bars, flags, offa, offb, comb, total;
+  uint32_t stage_pitch, bars, flags, offa, order, invpos, hist, comb, total;
   __host__ __device__ Layout(int stages, uint32_t stage_bytes, int S, int ncw, int D) {
     stage_pitch = (stage_bytes + 127u) & ~127u;
     // mbarriers: full[stages], empty[stages], item_full[2], item_empty[2], comb_full[4], comb_empty[4]
     bars = stages * stage_pitch;
     flags = bars + 16u * stages + 32u + 64u;          // poison[stages], abort, item_slot[2]
     offa = (flags + 4u * (stages + 3) + 15u) & ~15u;  // full-partition item offsets [S + 1]
-    offb = (offa + 4u * (S + 1) + 15u) & ~15u;        // last-partition item offsets [S + 1]
-    comb = (offb + 4u * (S + 1) + 15u) & ~15u;        // combine scratch [ncw][D + 2]
+    order = (offa + 4u * (S + 1) + 15u) & ~15u;       // sequences with a last partition, longest first [S]
+    invpos = (order + 4u * S + 15u) & ~15u;           // position of a sequence in `order` [S]
+    hist = (invpos + 4u * S + 15u) & ~15u;            // remainder buckets [32] + cursors [32]
+    comb = hist + 256u;                               // combine scratch [ncw][D + 2]
     total = comb + 4u * ncw * (D + 2) + 128u;         // + slack for 128-byte base alignment
   }
 };
@@ -243,7 +249,7 @@ struct Item {
   bool single;        // the sequence has one partition: write the output directly
 };
 
-__device__ __forceinline__ Item locate(const DecodeArgs& a, const int32_t* offa, const int32_t* offb,
+__device__ __forceinline__ Item locate(const DecodeArgs& a, const int32_t* offa, const int32_t* order,
                                        int a_total, int P, int item) {
   Item it;
   int p;
@@ -254,8 +260,9 @@ __device__ __forceinline__ Item locate(const DecodeArgs& a, const int32_t* offa,
     it.g = local - p * a.G;
   } else {
     const int b = item - a_total;
-    it.s = upper_seq(offb, a.S, b);
-    it.g = b - offb[it.s];
+    const int j = b / a.G;
+    it.s = order[j];
+    it.g = b - j * a.G;
     p = -1;  // the last partition
   }
   it.L = valid_len(a, it.s);
@@ -416,6 +423,74 @@ __device__ __forceinline__ void frame_fast(SoftState<16 / sizeof(T)>& st, const 
   }
 }
 
+// Log-sum-exp merge of the partitions of one (sequence, head), by one warp:
+// out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p with M = max_p m_p (log2 units).
+// Partition p of the sequence is item offa[s] + p*G + g (full partitions) or
+// a_total + invpos[s]*G + g (the shorter last one).  Partials written by other
+// thread blocks are read past L1.
+template <typename T, int D, int HG>
+__device__ __forceinline__ void merge_head(const DecodeArgs& a, const int32_t* offa, const int32_t* invpos,
+                                           int a_total, int s, int g, int h, int head, int nf, int np, int lane,
+                                           int c) {
+  constexpr int VEC = 16 / sizeof(T);
+  constexpr int LPR = D / VEC;
+  auto item_of = [&](int p) { return p < nf ? offa[s] + p * a.G + g : a_total + invpos[s] * a.G + g; };
+  // pass 1, lanes across partitions: M, bad flag
+  float M = -INFINITY;
+  bool bad = false;
+  for (int p = lane; p < np; p += 32) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + (static_cast<int64_t>(item_of(p)) * HG + h) * 2));
+    M = fmaxf(M, ml.x);
+    bad |= ml.y < 0.f;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+  bad = __any_sync(kFull, bad);
+  float num[VEC];
+#pragma unroll
+  for (int v = 0; v < VEC; ++v) num[v] = 0.f;
+  float den = 0.f;
+  if (!bad && M != -INFINITY) {
+    // pass 2: weights computed lane-parallel, values accumulated by the chunk owners
+    for (int p0 = 0; p0 < np; p0 += 32) {
+      float wgt = 0.f, wl = 0.f;
+      const int p = p0 + lane;
+      if (p < np) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + (static_cast<int64_t>(item_of(p)) * HG + h) * 2));
+        wgt = ex2(ml.x - M);
+        wl = wgt * ml.y;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) wl += __shfl_xor_sync(kFull, wl, off);
+      den += wl;
+      const int n = min(32, np - p0);
+      for (int j = 0; j < n; ++j) {
+        const float sc = __shfl_sync(kFull, wgt, j);
+        if (lane < LPR) {
+          const float* src = a.ws_o + (static_cast<int64_t>(item_of(p0 + j)) * HG + h) * D + c * VEC;
+#pragma unroll
+          for (int v = 0; v < VEC; v += 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(src + v));
+            num[v] = fmaf(sc, x.x, num[v]);
+            num[v + 1] = fmaf(sc, x.y, num[v + 1]);
+            num[v + 2] = fmaf(sc, x.z, num[v + 2]);
+            num[v + 3] = fmaf(sc, x.w, num[v + 3]);
+          }
+        }
+      }
+    }
+  }
+  if (lane < LPR) {
+    const bool zero = bad || !(den > 0.f);
+    const float inv = zero ? 0.f : 1.f / den;
+    float res[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) res[v] = zero ? 0.f : num[v] * inv;
+    T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(s) * a.out_row + static_cast<int64_t>(head) * D + c * VEC;
+    Chunk<T>::store(op, res);
+  }
+}
+
 template <typename T, int D, int HG, int WPH, int BFAST>
 __global__ void __launch_bounds__(32 * (HG * WPH + 1), (HG * WPH <= 4 ? 3 : 2))
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
@@ -445,51 +520,17 @@ __global__ void __launch_bounds__(32 * (HG * WPH + 1), (HG * WPH <= 4 ? 3 : 2))
   volatile int32_t* abort_flag = poison + stages;
   volatile int32_t* item_slot = abort_flag + 1;
   int32_t* offa = reinterpret_cast<int32_t*>(smem + lay.offa);
-  int32_t* offb = reinterpret_cast<int32_t*>(smem + lay.offb);
+  int32_t* order = reinterpret_cast<int32_t*>(smem + lay.order);
+  int32_t* invpos = reinterpret_cast<int32_t*>(smem + lay.invpos);
+  int32_t* hist = reinterpret_cast<int32_t*>(smem + lay.hist);
   float* comb = reinterpret_cast<float*>(smem + lay.comb);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  // ---- 1. partition length, per-sequence item counts, prefix offsets ----------------------
-  int P;
-  {
-    const int Lcap = a.max_blocks * B;
-    if (a.fixed_part > 0) {
-      P = a.fixed_part;
-    } else {
-      long long local = 0;
-      for (int s = tid; s < a.S; s += blockDim.x) {
-        const int L = valid_len(a, s);
-        local += L > 0 ? L : 0;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(kFull, local, o);
-      long long* red = reinterpret_cast<long long*>(comb);
-      if (lane == 0) red[warp] = local;
-      __syncthreads();
-      long long total = 0;
-      for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) total += red[w];
-      __syncthreads();
-      long long p = (total * a.G + a.target_items - 1) / (a.target_items > 0 ? a.target_items : 1);
-      p = ((p + B - 1) / B) * B;
-      if (p < a.min_part) p = a.min_part;
-      if (p > Lcap) p = Lcap;
-      if (p < B) p = B;
-      P = static_cast<int>(p);
-    }
-  }
-  for (int s = tid; s < a.S; s += blockDim.x) {
-    const int L = valid_len(a, s);
-    if (L < 0 && blockIdx.x == 0) atomicOr(a.status, kDevBadLen);
-    const int Lv = L < 0 ? 0 : L;
-    offa[s + 1] = full_parts(Lv, P) * a.G;
-    offb[s + 1] = last_part(Lv, P) * a.G;
-  }
+  // ---- 0. shared-memory barriers, then wait for the previous kernel's writes -----------------
   if (tid == 0) {
-    offa[0] = 0;
-    offb[0] = 0;
     for (int i = 0; i < stages; ++i) {
       mbar_init(bar_full + 8u * i, 1);
       mbar_init(bar_empty + 8u * i, NCW);
@@ -499,9 +540,9 @@ __global__ void __launch_bounds__(32 * (HG * WPH + 1), (HG * WPH <= 4 ? 3 : 2))
       mbar_init(bar_ifull + 8u * i, 1);
       mbar_init(bar_iempty + 8u * i, NCW);
     }
-    for (int h = 0; h < HG; ++h) {
-      mbar_init(bar_cfull + 8u * h, WPH > 1 ? WPH - 1 : 1);
-      mbar_init(bar_cempty + 8u * h, 1);
+    for (int hh = 0; hh < HG; ++hh) {
+      mbar_init(bar_cfull + 8u * hh, WPH > 1 ? WPH - 1 : 1);
+      mbar_init(bar_cempty + 8u * hh, 1);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -511,42 +552,145 @@ __global__ void __launch_bounds__(32 * (HG * WPH + 1), (HG * WPH <= 4 ? 3 : 2))
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // ---- 1. partition length ------------------------------------------------------------------
+  // Automatic: whole sequences when they already give every thread block work and
+  // the longest is no longer than the average load per block (longest-first
+  // scheduling then balances them); otherwise about target_items items of at least
+  // min_part tokens, shortened so the longest sequence splits into equal parts.
+  int P;
+  {
+    const int Lcap = a.max_blocks * B;
+    if (a.fixed_part > 0) {
+      P = a.fixed_part;
+    } else {
+      long long local = 0;
+      int lmax = 0;
+      for (int s = tid; s < a.S; s += blockDim.x) {
+        const int L = valid_len(a, s);
+        local += L > 0 ? L : 0;
+        lmax = max(lmax, L);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        local += __shfl_xor_sync(kFull, local, o);
+        lmax = max(lmax, __shfl_xor_sync(kFull, lmax, o));
+      }
+      long long* red = reinterpret_cast<long long*>(comb);
+      int* redmax = reinterpret_cast<int*>(red + (blockDim.x >> 5));
+      if (lane == 0) {
+        red[warp] = local;
+        redmax[warp] = lmax;
+      }
+      __syncthreads();
+      long long total = 0;
+      for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
+        total += red[w];
+        lmax = max(lmax, redmax[w]);
+      }
+      __syncthreads();
+      const long long grid = gridDim.x;
+      long long p;
+      if (a.whole_first && static_cast<long long>(a.S) * a.G >= grid && lmax * grid <= total * a.G) {
+        p = Lcap;
+      } else {
+        p = (total * a.G + a.target_items - 1) / (a.target_items > 0 ? a.target_items : 1);
+        p = ((p + B - 1) / B) * B;
+        if (p < a.min_part) p = a.min_part;
+        if (p > Lcap) p = Lcap;
+        if (lmax > p) {  // equal parts for the longest sequence
+          const long long n = (lmax + p - 1) / p;
+          const long long q = (((lmax + n - 1) / n + B - 1) / B) * B;
+          if (q >= a.min_part) p = q;
+        }
+      }
+      if (p < B) p = B;
+      P = static_cast<int>(p);
+    }
+  }
+
+  // ---- 2. work items: full partitions in sequence order, then the shorter last
+  //      partitions ordered longest first (stable 32-bucket counting sort by length,
+  //      identical in every thread block) ---------------------------------------------------
+  for (int s = tid; s < a.S; s += blockDim.x) {
+    const int L = valid_len(a, s);
+    if (L < 0 && blockIdx.x == 0) atomicOr(a.status, kDevBadLen);
+    const int Lv = L < 0 ? 0 : L;
+    offa[s + 1] = full_parts(Lv, P) * a.G;
+  }
+  if (tid < 64) hist[tid] = 0;
+  if (tid == 0) offa[0] = 0;
   __syncthreads();
-  if (warp < 2) {  // warp 0 scans the full-partition counts, warp 1 the last-partition counts
-    int32_t* off = warp == 0 ? offa : offb;
+  if (warp == 0) {  // prefix sum of the full-partition item counts
     int carry = 0;
     for (int base = 0; base < a.S; base += 32) {
       const int i = base + lane;
-      int v = i < a.S ? off[i + 1] : 0;
+      int v = i < a.S ? offa[i + 1] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int n = __shfl_up_sync(kFull, v, o);
         if (lane >= o) v += n;
       }
       v += carry;
-      if (i < a.S) off[i + 1] = v;
+      if (i < a.S) offa[i + 1] = v;
       carry = __shfl_sync(kFull, v, 31);
     }
+  } else if (warp == 1) {  // order of the last partitions
+    auto bucket_of = [&](int s) {
+      const int L = valid_len(a, s);
+      const int Lv = L < 0 ? 0 : L;
+      if (!last_part(Lv, P)) return -1;
+      return min(31, static_cast<int>((static_cast<long long>(Lv % P) * 32) / P));
+    };
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = 0; base < a.S; base += 32) {
+      const int s = base + lane;
+      const int b = s < a.S ? bucket_of(s) : -1;
+      const unsigned same = __match_any_sync(kFull, b);
+      if (b >= 0 && (same & lt) == 0) hist[b] += __popc(same);
+      __syncwarp();
+    }
+    // cursor[b] = number of entries in buckets above b (longest first)
+    const int cnt = hist[31 - lane];
+    int v = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(kFull, v, o);
+      if (lane >= o) v += n;
+    }
+    hist[32 + (31 - lane)] = v - cnt;
+    if (lane == 31) hist[31] = v;  // bucket 31's count is no longer needed: total entries
+    __syncwarp();
+    const int n_last = hist[31];
+    __syncwarp();
+    for (int base = 0; base < a.S; base += 32) {
+      const int s = base + lane;
+      const int b = s < a.S ? bucket_of(s) : -1;
+      const unsigned same = __match_any_sync(kFull, b);
+      if (b >= 0) {
+        const int pos = hist[32 + b] + __popc(same & lt);
+        order[pos] = s;
+        invpos[s] = pos;
+      }
+      __syncwarp();
+      if (b >= 0 && (same & lt) == 0) hist[32 + b] += __popc(same);
+      __syncwarp();
+    }
+    if (lane == 0) hist[0] = n_last;
   }
   __syncthreads();
   const int a_total = offa[a.S];
-  const int total_items = a_total + offb[a.S];
-  if (blockIdx.x == 0) {
-    for (int i = tid; i <= a.S; i += blockDim.x) {
-      a.ws_off[i] = offa[i];
-      a.ws_off[a.S + 1 + i] = offb[i];
-    }
-    if (tid == 0) {
-      a.ws_off[2 * a.S + 2] = a_total;
-      a.ws_off[2 * a.S + 3] = P;
-    }
-  }
+  const int total_items = a_total + hist[0] * a.G;
 
   if (warp == NCW) {
     // ============================== producer warp ==============================
     int k = 0, ni = 0;
     uint32_t issued = 0;  // bit i: stage i holds copies not yet known complete
     while (true) {
+      // An item is claimed only when the previous one is fully issued, so the
+      // longest-first order is kept (claiming ahead would pin items to busy blocks).
       int item = 0;
       if (lane == 0) item = *abort_flag ? total_items : atomicAdd(a.sched, 1);
       item = __shfl_sync(kFull, item, 0);
@@ -560,7 +704,7 @@ __global__ void __launch_bounds__(32 * (HG * WPH + 1), (HG * WPH <= 4 ? 3 : 2))
       }
       ++ni;
       if (done) break;
-      const Item it = locate(a, offa, offb, a_total, P, item);
+      const Item it = locate(a, offa, order, a_total, P, item);
       const int32_t* row = a.block_tables + static_cast<int64_t>(it.s) * a.bt_row + it.blk0;
       for (int j0 = 0; j0 < it.nblk; j0 += 32) {
         const int jj = j0 + lane;
@@ -636,7 +780,7 @@ __global__ void __launch_bounds__(32 * (HG * WPH + 1), (HG * WPH <= 4 ? 3 : 2))
     if (lane == 0) mbar_arrive(bar_iempty + 8u * sl);
     ++ni;
     if (item < 0) break;
-    const Item it = locate(a, offa, offb, a_total, P, item);
+    const Item it = locate(a, offa, order, a_total, P, item);
     const int head = it.g * HG + h;
 
     float qv[VEC];
@@ -733,71 +877,46 @@ __global__ void __launch_bounds__(32 * (HG * WPH + 1), (HG * WPH <= 4 ? 3 : 2))
       }
       ++nc;
     }
-    if (w == 0 && lane < LPR) {
+    if (w == 0) {
       if (it.single) {
-        float res[VEC];
-        const bool zero = poisoned || !(l > 0.f);
-        const float inv = zero ? 0.f : 1.f / l;
+        if (lane < LPR) {
+          float res[VEC];
+          const bool zero = poisoned || !(l > 0.f);
+          const float inv = zero ? 0.f : 1.f / l;
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) res[v] = zero ? 0.f : o[v] * inv;
-        T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(it.s) * a.out_row +
-                static_cast<int64_t>(head) * D + c * VEC;
-        Chunk<T>::store(op, res);
+          for (int v = 0; v < VEC; ++v) res[v] = zero ? 0.f : o[v] * inv;
+          T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(it.s) * a.out_row +
+                  static_cast<int64_t>(head) * D + c * VEC;
+          Chunk<T>::store(op, res);
+        }
       } else {
-        float* wo = a.ws_o + (static_cast<int64_t>(item) * HG + h) * D + c * VEC;
+        if (lane < LPR) {
+          float* wo = a.ws_o + (static_cast<int64_t>(item) * HG + h) * D + c * VEC;
 #pragma unroll
-        for (int v = 0; v < VEC; v += 4)
-          *reinterpret_cast<float4*>(wo + v) = make_float4(o[v], o[v + 1], o[v + 2], o[v + 3]);
-        if (c == 0) {
-          float* wml = a.ws_ml + (static_cast<int64_t>(item) * HG + h) * 2;
-          wml[0] = m;
-          wml[1] = poisoned ? -1.f : l;
+          for (int v = 0; v < VEC; v += 4)
+            *reinterpret_cast<float4*>(wo + v) = make_float4(o[v], o[v + 1], o[v + 2], o[v + 3]);
+          if (c == 0)
+            *reinterpret_cast<float2*>(a.ws_ml + (static_cast<int64_t>(item) * HG + h) * 2) =
+                make_float2(m, poisoned ? -1.f : l);
+        }
+        // Publish the partial, count it; the last partition of (sequence, head) to
+        // arrive merges all of them and resets the counter for the next launch.
+        __threadfence();
+        __syncwarp();
+        const int Lv = it.L < 0 ? 0 : it.L;
+        const int nf = full_parts(Lv, P);
+        const int np = nf + last_part(Lv, P);
+        int32_t* cnt = a.ws_cnt + static_cast<int64_t>(it.s) * a.H + head;
+        int last = 0;
+        if (lane == 0) last = atomicAdd(cnt, 1) == np - 1;
+        if (__shfl_sync(kFull, last, 0)) {
+          __threadfence();
+          merge_head<T, D, HG>(a, offa, invpos, a_total, it.s, it.g, h, head, nf, np, lane, c);
+          if (lane == 0) *cnt = 0;
         }
       }
     }
   }
-}
-
-// Log-sum-exp merge of the partitions of every split (sequence, head):
-// out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p with M = max_p m_p (log2 units).
-// The item ids of a sequence's partitions come from the offsets the decode kernel
-// stored: full partitions at offa[s] + p*G + g, the last one at a_total + offb[s] + g.
-template <typename T, int D>
-__global__ void __launch_bounds__(D) merge_kernel(const DecodeArgs a, const int HG) {
-  const int s = blockIdx.x / a.H;
-  const int head = blockIdx.x - s * a.H;
-  const int d = threadIdx.x;
-  const int L = valid_len(a, s);
-  if (L < 0) return;
-  const int32_t* offa = a.ws_off;
-  const int32_t* offb = a.ws_off + a.S + 1;
-  const int a_total = a.ws_off[2 * a.S + 2];
-  const int P = a.ws_off[2 * a.S + 3];
-  const int nf = full_parts(L, P);
-  const int np = nf + last_part(L, P);
-  if (np <= 1) return;
-  const int g = head / HG;
-  const int h = head - g * HG;
-  auto item_of = [&](int p) { return p < nf ? offa[s] + p * a.G + g : a_total + offb[s] + g; };
-  float M = -INFINITY;
-  bool bad = false;
-  for (int p = 0; p < np; ++p) {
-    const float* ml = a.ws_ml + (static_cast<int64_t>(item_of(p)) * HG + h) * 2;
-    M = fmaxf(M, ml[0]);
-    bad |= ml[1] < 0.f;
-  }
-  float num = 0.f, den = 0.f;
-  if (!bad && M != -INFINITY) {
-    for (int p = 0; p < np; ++p) {
-      const int64_t it = static_cast<int64_t>(item_of(p)) * HG + h;
-      const float sc = ex2(a.ws_ml[it * 2] - M);
-      den = fmaf(sc, a.ws_ml[it * 2 + 1], den);
-      num = fmaf(sc, a.ws_o[it * D + d], num);
-    }
-  }
-  const float res = (bad || !(den > 0.f)) ? 0.f : num / den;
-  T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(s) * a.out_row + static_cast<int64_t>(head) * D + d;
-  Chunk<T>::store1(op, res);
 }
 
 // ---- host-side launcher for one element type ----------------------------------------------
@@ -817,11 +936,19 @@ cudaError_t launch_one(const DecodeArgs& a, const DecodeCfg& c, const CUtensorMa
     if (max_ctas) *max_ctas = n;
     return e;
   }
-  kern<<<c.grid, 32 * (NCW + 1), smem, stream>>>(tk, tv, a, c.stages);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || a.ws_o == nullptr) return e;
-  merge_kernel<T, D><<<a.S * a.H, D, 0, stream>>>(a, HG);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the grid may start while the previous kernel on
+  // the stream drains; it waits (griddepcontrol.wait) before reading any input.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(c.grid);
+  cfg.blockDim = dim3(32 * (NCW + 1));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, a, c.stages);
 }
 
 template <typename T, int D>

@@ -46,15 +46,16 @@ struct DecodeArgs {
   int32_t G;                    // head groups per sequence = H / heads_per_cta
   float qk_scale_log2;          // scale * log2(e)
   // partitioning: fixed_part > 0 forces that many tokens per partition (multiple of
-  // B); otherwise partition length is chosen on the device from the lengths so that
-  // the work splits into about target_items items, never shorter than min_part.
+  // B); otherwise the partition length is chosen on the device from the lengths
+  // (whole sequences if whole_first and they balance, else about target_items
+  // items, never shorter than min_part).
   int32_t fixed_part;
   int32_t target_items;
   int32_t min_part;
+  int32_t whole_first;          // automatic mode: keep whole sequences when they balance
   // workspace
   int32_t* sched;               // [2]: next item, retired blocks (zero between launches)
-  int32_t* ws_off;              // [2S + 4]: full-partition offsets [S+1], last-partition
-                                // offsets [S+1], number of full-partition items, partition length
+  int32_t* ws_cnt;              // [S * H]: partitions finished per (sequence, head) (zero between launches)
   float* ws_ml;                 // [items][HG][2] = (running max in log2 units, sum); null if no split
   float* ws_o;                  // [items][HG][D] unnormalised partial outputs; null if no split
   int32_t* status;
