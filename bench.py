@@ -460,6 +460,69 @@ def fixed_variant(args, device):
     return res
 
 
+# ----------------------------------------------------------------------------- per-workload sweep
+SWEEP_KEYS = ("0", "1", "1x", "2", "3", "3c", "4")
+
+
+def sweep(keys, reps=20):
+    """pa_decode on the final state of each workload's replay (host-generated data,
+    automatic launch options): one JSON line per workload.  "3c" is the unshared
+    control of the parallel-sampling workload: the same final lengths, every branch
+    with private frames."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_126_gb300 as pa
+    import workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    st = torch.cuda.current_stream(dev)
+    for key in keys:
+        cfg = {"0": 0, "1": 1, "1x": "1x", "2": 2, "3": 3, "3c": 3, "4": 4}[key]
+        w = workloads.build(cfg)
+        if key == "3c":
+            L = [w.final_lens[s] for s in range(len(w.final_lens))]
+            w = workloads.custom(L, H=w.num_heads, D=w.head_dim, B=w.block_size, dtype=w.dtype, seed=w.seed,
+                                 name="parallel-sampling control: same lengths, no shared frames")
+        eng = pa.PagedKVEngine(w.num_blocks, w.block_size, w.num_heads, w.head_dim, w.dtype,
+                               free_order=w.free_order, device=dev, max_seqs=max(64, len(w.final_lens)),
+                               max_blocks_per_seq=max(1, max(-(-L // w.block_size) for L in w.final_lens.values())))
+        outs, trace = pa.run_workload_ops(eng, w)
+        op = w.attend_ops[-1]
+        seqs = w.ops[op][1]
+        tables, lens = eng.bm.block_tables(seqs, eng.max_blocks)
+        tt, ll = torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev)
+        q = pa.to_device_rows(w.query(op), w.dtype, dev)
+        out = torch.empty_like(q)
+        n = reps if key != "4" else max(5, reps // 2)
+        for _ in range(3):
+            pa.pa_decode(q, eng.k_cache, eng.v_cache, tt, ll, w.scale, out)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(n):
+            pa.pa_decode(q, eng.k_cache, eng.v_cache, tt, ll, w.scale, out)
+        e1.record(st)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / n * 1e3
+        logical = algorithmic_bytes(lens, w.num_heads, w.head_dim, w.block_size, w.elem_bytes)
+        frames = set()
+        for t, L in zip(tables, lens):
+            frames.update(t[: -(-int(L) // w.block_size)].tolist())
+        unique = len(frames) * w.block_size * w.num_heads * w.head_dim * w.elem_bytes * 2
+        peak, _ = _peaks()
+        print(json.dumps({
+            "workload": key, "name": w.name, "seqs": len(seqs), "sum_len": int(np.sum(lens)),
+            "decode_us": round(us, 2), "algorithmic_bytes": logical, "gbps": round(logical / (us * 1e-6) / 1e9, 1),
+            "pct_of_peak": round(100 * logical / (us * 1e-6) / 1e9 / peak, 1),
+            "unique_frame_bytes": unique, "gbps_unique_frames": round(unique / (us * 1e-6) / 1e9, 1),
+            "seqs_per_sec": round(len(seqs) / (us * 1e-6), 1),
+            "cow_copies": sum(len(t["copies"]) for t in trace.values())}), flush=True)
+        del eng, outs, tt, ll, q, out
+        torch.cuda.empty_cache()
+
+
 # ----------------------------------------------------------------------------- reference arm
 def reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
@@ -507,7 +570,13 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--config", default="1")
     ap.add_argument("--cpu-worker", default=None)
+    ap.add_argument("--sweep", default=None, metavar="KEYS",
+                    help="time pa_decode on each listed workload instead (comma list of 0,1,1x,2,3,3c,4 or 'all')")
     args = ap.parse_args()
+    if args.sweep is not None:
+        keys = SWEEP_KEYS if args.sweep == "all" else tuple(args.sweep.split(","))
+        sweep(keys)
+        return
     if args.config not in ("1", "1x"):
         raise SystemExit("the bench times the decode batch workload (1) or its fixed 64x2048 form (1x)")
     args.config = 1 if args.config == "1" else "1x"
