@@ -249,6 +249,13 @@ int pa_bm_append(pa_bm* bm, int64_t seq_id, int32_t* slot_out,
 int pa_bm_step(pa_bm* bm, const int64_t* seq_ids, int32_t n, int32_t* slots_out,
                int32_t* copies_out, int32_t* n_copies_out);
 
+/* A prompt chunk: num_tokens new tokens for one sequence, each following the
+ * pa_bm_append rule in turn, all-or-nothing.  slots_out [num_tokens]; copies_out
+ * (nullable) [num_tokens][2] receives copy-on-write pairs (at most one, for the
+ * first token), *n_copies_out their count (nullable). */
+int pa_bm_extend(pa_bm* bm, int64_t seq_id, int32_t num_tokens, int32_t* slots_out,
+                 int32_t* copies_out, int32_t* n_copies_out);
+
 /* Zero-copy fork: child shares every frame of parent (each gains a reference)
  * and inherits its length [VM "2. Zero-Copy Branching"]. */
 int pa_bm_fork(pa_bm* bm, int64_t parent_id, int64_t child_id);

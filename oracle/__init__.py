@@ -35,6 +35,8 @@ from .cache import OracleKVCache, decode_storage  # noqa: F401
 from .attention import (  # noqa: F401
     attention_fp64,
     paged_decode,
+    paged_prefill,
+    prefill_weight_bound,
     partial_state,
     lse_merge,
     round_to_storage,

@@ -10,6 +10,11 @@ to [n_frames*B, H, D] and trimmed to the context length ("Implementation",
 PagedAttention.forward).  Reading: the newest token (appended this step) is part of
 the attended set, i.e. the causal j <= i form with i the new token.
 
+Several queries per sequence (prefill / chunked prefill): the general causal form
+of the same equation, o_i = sum_{j <= i} softmax(a_ij) v_j -- query i attends the
+keys at positions 0..i.  A chunk of n queries is the last n positions of the
+sequence (its keys already written to the cache).
+
 The split-context merge (partial softmax states combined with log-sum-exp) is
 not on the pages; its definition is stated here so the merge kernel has an oracle:
 for a token subset P, m_P = max a_j, l_P = sum e^{a_j - m_P},
@@ -56,6 +61,42 @@ def paged_decode(q: np.ndarray, cache, tables, lens, scale: float) -> np.ndarray
         K, V = gather(cache, tables[s], int(lens[s]))
         out[s] = attention_fp64(qd[s], K, V, scale)
     return out
+
+
+def paged_prefill(q: np.ndarray, cache, tables, lens, query_start, scale: float) -> np.ndarray:
+    """Causal attention for chunks of queries.
+
+    q [T, H, D] (storage dtype): rows query_start[s] .. query_start[s+1]-1 are the
+    last n_s = query_start[s+1] - query_start[s] positions of sequence s (length
+    lens[s]); row r at position p attends keys 0..p.  Returns float64 [T, H, D].
+    """
+    qd = decode_storage(q, cache.dtype)
+    out = np.zeros(qd.shape, np.float64)
+    for s in range(len(lens)):
+        a, b = int(query_start[s]), int(query_start[s + 1])
+        L = int(lens[s])
+        K, V = gather(cache, tables[s], L)
+        for r in range(a, b):
+            pos = L - (b - a) + (r - a)
+            out[r] = attention_fp64(qd[r], K[: pos + 1], V[: pos + 1], scale)
+    return out
+
+
+def prefill_weight_bound(q: np.ndarray, cache, tables, lens, query_start, scale: float) -> np.ndarray:
+    """Per output element, sum_j w_j |v_j| (softmax weights times value magnitudes).
+
+    A kernel that rounds the softmax weights to a u-precision type before the
+    value product can be off by at most u * this (plus its own fp32 error)."""
+    qd = decode_storage(q, cache.dtype)
+    bound = np.zeros(qd.shape, np.float64)
+    for s in range(len(lens)):
+        a, b = int(query_start[s]), int(query_start[s + 1])
+        L = int(lens[s])
+        K, V = gather(cache, tables[s], L)
+        for r in range(a, b):
+            pos = L - (b - a) + (r - a)
+            bound[r] = attention_fp64(qd[r], K[: pos + 1], np.abs(V[: pos + 1]), scale)
+    return bound
 
 
 def partial_state(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float):

@@ -137,6 +137,14 @@ class OracleBlockManager:
             raise
         return slots, copies
 
+    def extend(self, seq: int, n: int):
+        """n new tokens for one sequence (a prompt chunk), all-or-nothing.
+
+        Each token follows the single-token rule in turn.  Returns (slots, copies)."""
+        if seq not in self.tables:
+            raise UnknownSequence(seq)
+        return self.step([seq] * int(n))
+
     def fork(self, parent: int, child: int) -> None:
         if parent not in self.tables:
             raise UnknownSequence(parent)

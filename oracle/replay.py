@@ -11,7 +11,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from .attention import paged_decode
+from .attention import paged_decode, paged_prefill
 from .block_manager import OracleBlockManager
 from .cache import OracleKVCache
 
@@ -44,6 +44,13 @@ def _kept_frames(w, keep_seqs):
         elif kind == "step":
             _, copies = bm.step(op[1])
             edges.extend(copies)
+        elif kind == "extend":
+            _, copies = bm.extend(op[1], op[2])
+            edges.extend(copies)
+        elif kind == "prefill":
+            for s in op[1]:
+                if s in keep_seqs:
+                    seen.update(bm.tables[s])
         elif kind == "free":
             bm.free(op[1])
         elif kind == "attend":
@@ -91,6 +98,29 @@ def replay(w, keep_seqs=None, with_cache: bool = True, snapshots: bool = False) 
                 if frames is None or any(s // B in frames for s in slots):
                     k, v = w.rows(i)
                     cache.write(slots, k, v)
+        elif kind == "extend":
+            slots, copies = bm.extend(op[1], op[2])
+            res.trace[i] = {"slots": slots, "copies": copies}
+            if cache is not None:
+                for src, dst in copies:
+                    cache.copy_block(src, dst)
+                if frames is None or any(s // B in frames for s in slots):
+                    k, v = w.rows(i)
+                    cache.write(slots, k, v)
+        elif kind == "prefill":
+            seqs, counts = op[1], op[2]
+            tables = [list(bm.tables[s]) for s in seqs]
+            lens = [bm.lens[s] for s in seqs]
+            res.attend_meta[i] = (tables, lens)
+            if cache is not None:
+                q = w.query(i)
+                qs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+                out = np.full(q.shape, np.nan)
+                for j, s in enumerate(seqs):
+                    if keep is None or s in keep:
+                        a, b = qs[j], qs[j + 1]
+                        out[a:b] = paged_prefill(q[a:b], cache, [tables[j]], [lens[j]], [0, b - a], w.scale)
+                res.outputs[i] = out
         elif kind == "free":
             bm.free(op[1])
         elif kind == "attend":

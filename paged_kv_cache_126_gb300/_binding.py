@@ -72,6 +72,7 @@ def _load():
         "pa_bm_add_seq": ([vp, C.c_int64, C.c_int32, i32p], C.c_int),
         "pa_bm_append": ([vp, C.c_int64, i32p, i32p, i32p], C.c_int),
         "pa_bm_step": ([vp, i64p, C.c_int32, i32p, i32p, i32p], C.c_int),
+        "pa_bm_extend": ([vp, C.c_int64, C.c_int32, i32p, i32p, i32p], C.c_int),
         "pa_bm_fork": ([vp, C.c_int64, C.c_int64], C.c_int),
         "pa_bm_free": ([vp, C.c_int64], C.c_int),
         "pa_bm_block_tables": ([vp, i64p, C.c_int32, C.c_int32, i32p, i32p], C.c_int),
@@ -94,7 +95,7 @@ LIB = _load()
 EXPORTED = (
     "pa_cache_append", "pa_copy_blocks", "pa_decode", "pa_decode_ex", "pa_decode_static", "pa_get_device_status",
     "pa_strerror", "pa_launch_count", "pa_shutdown", "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq",
-    "pa_bm_append", "pa_bm_step", "pa_bm_fork", "pa_bm_free", "pa_bm_block_tables", "pa_bm_seq_info",
+    "pa_bm_append", "pa_bm_step", "pa_bm_extend", "pa_bm_fork", "pa_bm_free", "pa_bm_block_tables", "pa_bm_seq_info",
     "pa_bm_table", "pa_bm_slot", "pa_bm_num_free", "pa_bm_free_list", "pa_bm_ref_counts",
     "pa_bm_num_seqs",
 )
@@ -267,6 +268,15 @@ class BlockManager:
         copies = np.empty((max(len(ids), 1), 2), np.int32)
         n = self.step_into(ids, slots, copies)
         return slots[: len(ids)], copies[:n]
+
+    def extend(self, seq: int, n: int):
+        """n new tokens for one sequence (a prompt chunk). Returns (slots, copies)."""
+        n = int(n)
+        slots = np.empty(max(n, 1), np.int32)
+        copies = np.empty((max(n, 1), 2), np.int32)
+        nc = C.c_int32(0)
+        _check(LIB.pa_bm_extend(self._h, int(seq), n, _i32(slots), _i32(copies), C.byref(nc)), "pa_bm_extend")
+        return slots[:n], copies[: nc.value]
 
     def fork(self, parent: int, child: int) -> None:
         _check(LIB.pa_bm_fork(self._h, int(parent), int(child)), "pa_bm_fork")

@@ -230,6 +230,32 @@ int pa_bm_step(pa_bm* bm, const int64_t* seq_ids, int32_t n, int32_t* slots_out,
   return PA_OK;
 }
 
+int pa_bm_extend(pa_bm* bm, int64_t seq_id, int32_t num_tokens, int32_t* slots_out, int32_t* copies_out,
+                 int32_t* n_copies_out) {
+  if (!bm || num_tokens < 0 || (num_tokens > 0 && !slots_out)) return PA_ERR_INVALID;
+  if (!bm->seqs.count(seq_id)) return PA_ERR_UNKNOWN_SEQ;
+  std::vector<Undo> log;
+  log.reserve(num_tokens);
+  int32_t n_copies = 0;
+  for (int32_t i = 0; i < num_tokens; ++i) {
+    int32_t src, dst;
+    int rc = bm->append_one(seq_id, &slots_out[i], &src, &dst, &log);
+    if (rc != PA_OK) {
+      for (auto u = log.rbegin(); u != log.rend(); ++u) bm->undo(*u);
+      return rc;
+    }
+    if (src >= 0) {
+      if (copies_out) {
+        copies_out[2 * n_copies] = src;
+        copies_out[2 * n_copies + 1] = dst;
+      }
+      ++n_copies;
+    }
+  }
+  if (n_copies_out) *n_copies_out = n_copies;
+  return PA_OK;
+}
+
 int pa_bm_fork(pa_bm* bm, int64_t parent_id, int64_t child_id) {
   if (!bm) return PA_ERR_INVALID;
   auto p = bm->seqs.find(parent_id);

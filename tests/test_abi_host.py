@@ -120,6 +120,18 @@ def test_random_ops_bit_exact(pa, seed):
             want = ob.free(s)
             got = bm.free(s)
             assert (got == pa.PA_WARN_DOUBLE_FREE) == (want == DOUBLE_FREE)
+        elif r < 0.55:
+            s, n_new = rnd.choice(live), rnd.randint(0, 2 * B + 3)
+            try:
+                want = ob.extend(s, n_new)
+            except OutOfBlocks:
+                with pytest.raises(pa.PAError) as ei:
+                    bm.extend(s, n_new)
+                assert ei.value.code == pa.PA_ERR_OUT_OF_BLOCKS
+            else:
+                slots, copies = bm.extend(s, n_new)
+                assert slots.tolist() == want[0]
+                assert [tuple(c) for c in copies.tolist()] == want[1]
         else:
             seqs = [rnd.choice(live) for _ in range(rnd.randint(1, 5))]  # repeats allowed
             try:

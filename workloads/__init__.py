@@ -10,7 +10,9 @@ from .gen import (  # noqa: F401
     DTYPES,
     Workload,
     build,
+    chunked_prefill,
     custom,
+    prefill_batch,
     CONFIG_IDS,
     storage_numpy_dtype,
 )

@@ -11,6 +11,11 @@ each operation carries:
 * ``("attend", seqs)``    -- single-query decode attention for each listed
                              sequence; payload: one query per sequence.
 * ``("free", seq)``       -- the sequence finishes.
+* ``("extend", seq, n)``  -- a prompt chunk: n new tokens for one sequence; payload:
+                             n K rows and n V rows.
+* ``("prefill", seqs, counts)`` -- causal attention for the last counts[i] positions
+                             of seqs[i]; payload: sum(counts) queries, grouped by
+                             sequence in list order.
 
 Payloads are drawn from a PCG64 stream keyed by ``(seed, op_index, kind)`` so any
 op's rows can be regenerated alone.  Values are drawn as float32 N(0, sigma^2)
@@ -90,20 +95,27 @@ class Workload:
         return _to_storage(x, self.dtype).reshape(n, self.num_heads, self.head_dim)
 
     def rows(self, op_index: int):
-        """(k, v) rows carried by an ``add`` or ``step`` op, storage dtype."""
+        """(k, v) rows carried by an ``add``, ``extend`` or ``step`` op, storage dtype."""
         op = self.ops[op_index]
-        n = op[2] if op[0] == "add" else len(op[1])
+        n = op[2] if op[0] in ("add", "extend") else len(op[1])
         return self._draw(op_index, "k", n), self._draw(op_index, "v", n)
 
     def query(self, op_index: int) -> np.ndarray:
-        """Queries ``[len(seqs), H, D]`` carried by an ``attend`` op, storage dtype."""
+        """Queries carried by an ``attend`` op ``[len(seqs), H, D]`` or a ``prefill`` op
+        ``[sum(counts), H, D]``, storage dtype."""
         op = self.ops[op_index]
-        assert op[0] == "attend"
-        return self._draw(op_index, "q", len(op[1]))
+        if op[0] == "attend":
+            return self._draw(op_index, "q", len(op[1]))
+        assert op[0] == "prefill"
+        return self._draw(op_index, "q", int(sum(op[2])))
 
     @property
     def attend_ops(self):
         return [i for i, op in enumerate(self.ops) if op[0] == "attend"]
+
+    @property
+    def prefill_ops(self):
+        return [i for i, op in enumerate(self.ops) if op[0] == "prefill"]
 
     @property
     def elem_bytes(self) -> int:
@@ -224,6 +236,41 @@ def build(cfg, small: bool = False) -> Workload:
         return _decode_batch("serving mix: 256 seqs, L~logU[16,8192], H=40, D=128, B=16, bf16",
                              L, 40, 128, 16, "bf16", 0.5, seed)
     raise ValueError(f"unknown workload {cfg!r}")
+
+
+def chunked_prefill(prefix_lens, chunk_lens, *, H=2, D=128, B=16, dtype="f16", sigma=1.0, seed=11,
+                    shuffle=True, name=None) -> Workload:
+    """Each sequence has a cached prefix, then one prompt chunk is appended and its
+    queries attend causally (a prefill when the prefix is empty)."""
+    prefix_lens = [int(x) for x in prefix_lens]
+    chunk_lens = [int(x) for x in chunk_lens]
+    final = [a + b for a, b in zip(prefix_lens, chunk_lens)]
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0])))
+    nb = _pool_size(final, B)
+    free_order = rng.permutation(nb).astype(np.int32) if shuffle else np.arange(nb, dtype=np.int32)
+    ops = [("add", s, L) for s, L in enumerate(prefix_lens)]
+    ops += [("extend", s, n) for s, n in enumerate(chunk_lens) if n > 0]
+    seqs = tuple(range(len(final)))
+    ops.append(("prefill", seqs, tuple(chunk_lens)))
+    return Workload(name=name or f"chunked prefill: {len(final)} seqs, chunks {chunk_lens[:4]}..., H={H}, D={D}, "
+                                 f"B={B}, {dtype}",
+                    num_heads=H, head_dim=D, block_size=B, dtype=dtype, sigma=sigma, num_blocks=nb,
+                    free_order=free_order, ops=ops, seed=seed, final_lens={s: L for s, L in enumerate(final)})
+
+
+def prefill_batch(small: bool = False) -> Workload:
+    """Chunked-prefill batch: 16 sequences, cached prefix ~U{0..3072}, a 512-token
+    chunk each (4 sequences, prefix ~U{0..400}, chunks ~U{1..300} when small)."""
+    seed = 1010 + (500 if small else 0)
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 1])))
+    if small:
+        pre = rng.integers(0, 401, size=4)
+        ch = rng.integers(1, 301, size=4)
+        return chunked_prefill(pre, ch, H=2, D=128, B=16, dtype="f16", seed=seed,
+                               name="chunked prefill (small): 4 seqs, prefix~U[0,400], chunk~U[1,300], H=2, f16")
+    pre = rng.integers(0, 3073, size=16)
+    return chunked_prefill(pre, [512] * 16, H=32, D=128, B=16, dtype="f16", seed=seed,
+                           name="chunked prefill: 16 seqs, prefix~U[0,3072], chunk 512, H=32, D=128, B=16, f16")
 
 
 def custom(lengths, *, H=2, D=128, B=16, dtype="f16", sigma=1.0, seed=7, shuffle=True,
