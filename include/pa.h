@@ -143,6 +143,35 @@ int pa_decode(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_c
               const pa_tensor* block_tables, const pa_tensor* context_lens,
               float scale, const pa_tensor* out, pa_stream stream);
 
+/*
+ * pa_prefill -- causal attention for chunks of queries (prefill / chunked
+ * prefill) over the paged cache, on the tensor cores.
+ * [MW "1. The Mathematical Foundation", the causal form o_i = sum_{j<=i}
+ *  softmax(a_ij) v_j; "2. The Algorithmic Steps" (prompt tokens are written to the
+ *  cache, then attention runs over the sequence's frames).]
+ *
+ *   q             [T, H, 128] fp16/bf16, row stride free (16-byte multiple).  Rows
+ *                 query_start[s] .. query_start[s+1]-1 are the last
+ *                 n_s = query_start[s+1] - query_start[s] positions of sequence s;
+ *                 their K/V rows must already be in the cache (pa_cache_append).
+ *   k_cache, v_cache  [num_blocks, B, H, 128], same dtype as q; B in {8, 16, 32, 64, 128}.
+ *   block_tables  int32 [S, max_blocks]; context_lens int32 [S] = L_s (chunk included);
+ *   query_start   int32 [S + 1], non-decreasing, query_start[S] <= T.
+ *   out           [T, H, 128], same dtype; row r at position p = L_s - n_s + (r -
+ *                 query_start[s]) gets sum_{j<=p} softmax(q_r . k_j * scale) v_j.
+ * Arithmetic: q.k products accumulated in fp32 by the tensor cores, softmax in fp32,
+ * the weights rounded to the cache dtype before the value product (fp32 accumulate),
+ * normalisation in fp32.  Cache slots of a frame beyond L_s are read and must hold
+ * finite values (the weights there are zero).  A sequence with n_s > L_s or
+ * L_s > max_blocks*B sets PA_DEV_BAD_LEN and its rows are left untouched; frame ids
+ * outside [0, num_blocks) set PA_DEV_BAD_BLOCK and read as zeros.  Uses the
+ * (device, stream) workspace's work counter; one thread block per SM.
+ */
+int pa_prefill(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+               const pa_tensor* block_tables, const pa_tensor* context_lens,
+               const pa_tensor* query_start, float scale, const pa_tensor* out,
+               pa_stream stream);
+
 /* Launch options for pa_decode_ex; 0 in any field = automatic choice. */
 typedef struct pa_decode_params {
   int32_t partition_tokens;  /* >0: split context into partitions of this many tokens

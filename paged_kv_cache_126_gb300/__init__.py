@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     pa_decode,
     pa_decode_ex,
     pa_decode_static,
+    pa_prefill,
     pa_get_device_status,
     pa_launch_count,
     pa_shutdown,

@@ -63,6 +63,7 @@ def _load():
         "pa_decode": ([P, P, P, P, P, C.c_float, P, vp], C.c_int),
         "pa_decode_ex": ([P, P, P, P, P, C.c_float, P, C.POINTER(PaDecodeParams), vp], C.c_int),
         "pa_decode_static": ([P, P, P, P, P, C.c_float, P, vp], C.c_int),
+        "pa_prefill": ([P, P, P, P, P, P, C.c_float, P, vp], C.c_int),
         "pa_get_device_status": ([vp, i32p], C.c_int),
         "pa_strerror": ([C.c_int], C.c_char_p),
         "pa_launch_count": ([], C.c_int64),
@@ -93,7 +94,8 @@ def _load():
 
 LIB = _load()
 EXPORTED = (
-    "pa_cache_append", "pa_copy_blocks", "pa_decode", "pa_decode_ex", "pa_decode_static", "pa_get_device_status",
+    "pa_cache_append", "pa_copy_blocks", "pa_decode", "pa_decode_ex", "pa_decode_static", "pa_prefill",
+    "pa_get_device_status",
     "pa_strerror", "pa_launch_count", "pa_shutdown", "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq",
     "pa_bm_append", "pa_bm_step", "pa_bm_extend", "pa_bm_fork", "pa_bm_free", "pa_bm_block_tables", "pa_bm_seq_info",
     "pa_bm_table", "pa_bm_slot", "pa_bm_num_free", "pa_bm_free_list", "pa_bm_ref_counts",
@@ -189,6 +191,15 @@ def pa_decode_static(q, k_cache, v_cache, block_tables, context_lens, scale, out
     ds = [tensor_desc(t) for t in (q, k_cache, v_cache, block_tables, context_lens)]
     o = tensor_desc(out)
     _check(LIB.pa_decode_static(*map(_ref, ds), C.c_float(scale), C.byref(o), st), "pa_decode_static")
+    return out
+
+
+def pa_prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale, out, stream=None):
+    """Causal attention for query chunks (see include/pa.h)."""
+    st = _stream_of(q, stream)
+    ds = [tensor_desc(t) for t in (q, k_cache, v_cache, block_tables, context_lens, query_start)]
+    o = tensor_desc(out)
+    _check(LIB.pa_prefill(*map(_ref, ds), C.c_float(scale), C.byref(o), st), "pa_prefill")
     return out
 
 

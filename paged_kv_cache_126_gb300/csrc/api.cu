@@ -81,6 +81,22 @@ int make_cache_map(CUtensorMap* map, void* base, int dtype, int64_t nb, int64_t 
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
 }
 
+// 3-D view [rows, H, D] of a 16-bit tensor whose rows are `row_elems` apart, box {64, 1, box_rows},
+// 128-byte swizzle (the layout tcgen05 reads as K-major or MN-major operands).
+int make_sw128_map(CUtensorMap* map, void* base, int dtype, int64_t rows, int64_t H, int64_t D, int64_t row_elems,
+                   int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return PA_ERR_CUDA;
+  CUtensorMapDataType t = dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * 2), static_cast<cuuint64_t>(row_elems * 2)};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, t, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
+}
+
 // ---- library-owned workspace, one per (device, stream) -------------------------------------
 // Layout: [0, 256) scheduler counters | arrival counters, one per (sequence, head) |
 // per-launch offsets and split partials.  Both counter regions must hold zeros
@@ -472,6 +488,65 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
 int pa_decode(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_tensor* block_tables,
               const pa_tensor* context_lens, float scale, const pa_tensor* out, pa_stream stream) {
   return pa_decode_ex(q, k_cache, v_cache, block_tables, context_lens, scale, out, nullptr, stream);
+}
+
+int pa_prefill(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_tensor* block_tables,
+               const pa_tensor* context_lens, const pa_tensor* query_start, float scale, const pa_tensor* out,
+               pa_stream stream) {
+  PA_TRY(check_cache(k_cache, v_cache));
+  const int dt = k_cache->dtype;
+  if (dt != PA_F16 && dt != PA_BF16) return PA_ERR_UNSUPPORTED;
+  const int64_t nb = k_cache->shape[0], B = k_cache->shape[1], H = k_cache->shape[2], D = k_cache->shape[3];
+  if (D != 128 || !(B == 8 || B == 16 || B == 32 || B == 64 || B == 128)) return PA_ERR_UNSUPPORTED;
+  PA_TRY(check_rows(q, dt, H, D));
+  PA_TRY(check_rows(out, dt, H, D));
+  if (!block_tables || !context_lens || !query_start) return PA_ERR_INVALID;
+  PA_TRY(check_i32(block_tables, 2));
+  PA_TRY(check_i32(context_lens, 1));
+  PA_TRY(check_i32(query_start, 1));
+  const int64_t T = q->shape[0], S = context_lens->shape[0];
+  if (out->shape[0] != T || block_tables->shape[0] != S || query_start->shape[0] != S + 1) return PA_ERR_SHAPE;
+  const int64_t max_blocks = block_tables->shape[1];
+  if (max_blocks < 0 || (S > 1 && block_tables->stride[0] < max_blocks)) return PA_ERR_STRIDE;
+  if (max_blocks * B > INT32_MAX || T > INT32_MAX || nb * B > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (S == 0 || T == 0) return PA_OK;
+  if (pa::prefill_smem_bytes(static_cast<int>(S)) > 227 * 1024) return PA_ERR_UNSUPPORTED;
+  int dev;
+  PA_TRY(current_device(&dev));
+
+  pa::PrefillArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = q->data;
+  a.out = out->data;
+  a.q_row = q->stride[0];
+  a.out_row = out->stride[0];
+  a.block_tables = static_cast<const int32_t*>(block_tables->data);
+  a.bt_row = block_tables->stride[0];
+  a.context_lens = static_cast<const int32_t*>(context_lens->data);
+  a.query_start = static_cast<const int32_t*>(query_start->data);
+  a.S = static_cast<int32_t>(S);
+  a.H = static_cast<int32_t>(H);
+  a.B = static_cast<int32_t>(B);
+  a.num_blocks = static_cast<int32_t>(nb);
+  a.max_blocks = static_cast<int32_t>(max_blocks);
+  a.T = static_cast<int32_t>(T);
+  a.qk_scale_log2 = scale * 1.4426950408889634f;
+  a.status = g_dev[dev].status;
+
+  CUtensorMap tq, tk, tv;
+  PA_TRY(make_sw128_map(&tq, q->data, dt, T, H, D, q->stride[0], 128));
+  PA_TRY(make_sw128_map(&tk, k_cache->data, dt, nb * B, H, D, H * D, static_cast<int>(B)));
+  PA_TRY(make_sw128_map(&tv, v_cache->data, dt, nb * B, H, D, H * D, static_cast<int>(B)));
+  void* ws = nullptr;
+  size_t cnt_bytes = 0;
+  PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), 0, 0, &ws, &cnt_bytes));
+  a.sched = static_cast<int32_t*>(ws);
+  const int grid = g_dev[dev].num_sms;
+  const cudaError_t e = dt == PA_F16 ? pa::launch_prefill_f16(a, tq, tk, tv, grid, static_cast<cudaStream_t>(stream))
+                                     : pa::launch_prefill_bf16(a, tq, tk, tv, grid, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return PA_OK;
 }
 
 }  // extern "C"

@@ -83,6 +83,26 @@ cudaError_t launch_decode_bf16(const DecodeArgs&, const DecodeCfg&, const CUtens
 // Dynamic shared memory of one decode thread block (mirrors the kernel's layout).
 size_t decode_smem_bytes(const DecodeCfg& c, int elem_bytes, int B, int S);
 
+// ---- chunked prefill (tensor cores) ------------------------------------------------------------
+struct PrefillArgs {
+  const void* q;                // [T, H, 128], row stride q_row elements
+  void* out;                    // [T, H, 128], row stride out_row elements
+  int64_t q_row, out_row;
+  const int32_t* block_tables;  // [S, max_blocks]
+  int64_t bt_row;
+  const int32_t* context_lens;  // [S] tokens in the cache, chunk included
+  const int32_t* query_start;   // [S + 1] q rows of sequence s: query_start[s] .. query_start[s+1]-1
+  int32_t S, H, B, num_blocks, max_blocks, T;
+  float qk_scale_log2;
+  int32_t* sched;               // [2] work counter, retired blocks (zero between launches)
+  int32_t* status;
+};
+cudaError_t launch_prefill_f16(const PrefillArgs&, const CUtensorMap& tq, const CUtensorMap& tk,
+                               const CUtensorMap& tv, int grid, cudaStream_t);
+cudaError_t launch_prefill_bf16(const PrefillArgs&, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, int grid, cudaStream_t);
+size_t prefill_smem_bytes(int S);
+
 // status bits (mirror pa.h)
 constexpr int32_t kDevBadSlot = 0x1;
 constexpr int32_t kDevBadBlock = 0x2;

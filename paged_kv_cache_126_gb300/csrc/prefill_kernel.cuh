@@ -1,0 +1,586 @@
+// Causal multi-query attention over the paged cache (prefill / chunked prefill)
+// on the 5th-generation tensor cores of sm_103a.
+//
+// What it computes ("Solving the LLM Memory Wall", "1. The Mathematical
+// Foundation", general causal form): for a chunk of n_s queries that are the last
+// n_s positions of sequence s (its keys already appended to the cache), query i
+// at position p attends keys 0..p:  o_i = sum_{j<=p} softmax(q_i.k_j * scale) v_j.
+// Keys and values are read through the block table from the caches
+// [num_blocks, B, H, D] ("PagedAttention: Virtual Memory Guide for LLM
+// Inference", "The Mathematics of Block Translation").
+//
+// Design (one thread block per SM, persistent, dynamic work counter):
+//   * Work item = (sequence, head, tile of 128 queries); later (longer) query
+//     tiles of a sequence first.  K/V are walked in tiles of 128 keys, each
+//     assembled from 128/B frames by 3-D TMA loads (box {64, 1, B}, 128-byte
+//     swizzle, two 64-column halves); frames past the sequence end are loaded from
+//     an out-of-range row, i.e. zero-filled.
+//   * warp 0 (one lane): TMA producer -- Q tile, then K and V tiles into two-stage
+//     rings.  warp 1 (one lane): tcgen05.mma issuer -- S = Q K^T into one of two
+//     128-column TMEM buffers, then O_j = P_j V_j into one of two more (fp32
+//     accumulators, M = N = 128, K = 16 per instruction); Q K^T of tile j+1 is
+//     issued before P V of tile j so the tensor cores work while the softmax runs.
+//     warps 4..7 (128 threads, thread = query row, TMEM lane = row): load S,
+//     apply the causal mask, online softmax in log2 units (ex2.approx, fp32), write
+//     P (operand type) to shared memory in the 128-byte-swizzled K-major layout the
+//     MMA reads, and fold each O_j into an fp32 row accumulator in registers with
+//     the usual rescaling.  Normalised rows are written to `out`.
+//   * Every wait is a bounded mbarrier wait; one that gives up sets PA_DEV_TIMEOUT
+//     and makes the block's later waits no-ops; before the TMEM is freed the MMA
+//     lane waits (bounded) for its own MMAs and the producer for its copies.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <type_traits>
+
+#include "pa_internal.h"
+
+namespace pa {
+namespace pk {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr long long kWaitCycles = 4000000000LL;
+constexpr long long kDrainCycles = 200000000LL;
+constexpr int kD = 128;           // head_dim
+constexpr int kBM = 128;          // queries per tile
+constexpr int kBN = 128;          // keys per tile
+constexpr int kThreads = 256;     // 8 warps
+constexpr uint32_t kTile = 32768; // bytes of one 128 x 128 16-bit tile
+constexpr uint32_t kHalf = 16384; // one 64-column half of a tile
+
+// shared-memory map (offsets from a 1024-byte aligned base)
+constexpr uint32_t kSmQ = 0;
+constexpr uint32_t kSmK = kSmQ + kTile;           // 2 stages
+constexpr uint32_t kSmV = kSmK + 2 * kTile;       // 2 stages
+constexpr uint32_t kSmP = kSmV + 2 * kTile;
+constexpr uint32_t kSmBar = kSmP + kTile;         // mbarriers
+constexpr uint32_t kSmMisc = kSmBar + 32 * 8;     // flags, TMEM address, item ring
+constexpr uint32_t kSmOff = kSmMisc + 64;         // per-sequence item offsets [S + 1]
+__host__ __device__ constexpr uint32_t smem_bytes(int S) { return kSmOff + 4u * (S + 1) + 1024u; }
+
+// mbarrier indices
+enum : int {
+  BQ_FULL = 0, BQ_EMPTY = 1,
+  BK_FULL = 2, BK_EMPTY = 4, BV_FULL = 6, BV_EMPTY = 8,   // [2] each
+  BS_FULL = 10, BS_EMPTY = 12, BO_FULL = 14, BO_EMPTY = 16,  // [2] each
+  BP_FULL = 18, BP_EMPTY = 19,
+  BI_FULL = 20, BI_EMPTY = 22,                             // item ring [2]
+  BDRAIN = 24,
+  NBARS = 25
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag,
+                                          int32_t* status) {
+  if (mbar_try(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (*abort_flag) return false;
+    if (mbar_try(bar, parity)) return true;
+    if (clock64() - t0 > kWaitCycles) {
+      atomicOr(status, kDevTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// tcgen05 shared-memory matrix descriptor: 128-byte swizzle, SM100 version field.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+// kind::f16 instruction descriptor, fp32 accumulate, M = N = 128, A K-major.
+template <typename T>
+__host__ __device__ constexpr uint32_t idesc(bool b_mn_major) {
+  constexpr uint32_t fmt = sizeof(T) == 2 && !std::is_same<T, __half>::value ? 1u : 0u;  // bf16 = 1
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(b_mn_major) << 16) | ((128u >> 3) << 17) |
+         ((128u >> 4) << 24);
+}
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ int upper_seq(const int32_t* off, int S, int x) {
+  int lo = 0, hi = S - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct PItem {
+  int s, h;
+  int qrow0;    // first q row of the tile (global row index)
+  int nrows;    // valid rows in the tile
+  int pos0;     // position of the tile's first row
+  int nkv;      // key tiles to visit
+  bool bad;
+};
+
+__device__ __forceinline__ PItem locate(const PrefillArgs& a, const int32_t* off, int item) {
+  PItem it;
+  it.s = upper_seq(off, a.S, item);
+  const int local = item - off[it.s];
+  const int qt_rev = local / a.H;
+  it.h = local - qt_rev * a.H;
+  const int qs = a.query_start[it.s], qe = a.query_start[it.s + 1];
+  const int n = qe - qs;
+  const int L = a.context_lens[it.s];
+  it.bad = n < 0 || L < n || static_cast<int64_t>(L) > static_cast<int64_t>(a.max_blocks) * a.B;
+  const int ntiles = n > 0 ? (n + kBM - 1) / kBM : 0;
+  const int qt = ntiles - 1 - qt_rev;  // later tiles first
+  it.qrow0 = qs + qt * kBM;
+  it.nrows = it.bad ? 0 : min(kBM, n - qt * kBM);
+  it.pos0 = L - n + qt * kBM;
+  const int pos_last = it.pos0 + it.nrows - 1;
+  it.nkv = it.nrows > 0 ? (pos_last + kBN) / kBN : 0;
+  return it;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bars = sb + kSmBar;
+  auto BAR = [&](int i) { return bars + 8u * i; };
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kSmMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmMisc + 4);
+  volatile int32_t* item_slot = reinterpret_cast<volatile int32_t*>(smem + kSmMisc + 8);  // [2]
+  int32_t* off = reinterpret_cast<int32_t*>(smem + kSmOff);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = a.B;
+  const int fpt = kBN / B;  // frames per key tile
+
+  if (tid == 0) {
+    for (int i = 0; i < NBARS; ++i) {
+      uint32_t cnt = 1;
+      if (i == BS_EMPTY || i == BS_EMPTY + 1 || i == BO_EMPTY || i == BO_EMPTY + 1 || i == BP_FULL) cnt = 4;
+      if (i == BI_EMPTY || i == BI_EMPTY + 1) cnt = 5;  // MMA warp + 4 softmax warps
+      mbar_init(BAR(i), cnt);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 2) {  // TMEM: S0 S1 O0 O1, 128 columns each
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_q)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
+  }
+  // per-sequence item counts and their prefix
+  for (int s = tid; s < a.S; s += blockDim.x) {
+    const int n = a.query_start[s + 1] - a.query_start[s];
+    const int L = a.context_lens[s];
+    const bool bad = n < 0 || L < n || static_cast<int64_t>(L) > static_cast<int64_t>(a.max_blocks) * B;
+    if (bad && blockIdx.x == 0) atomicOr(a.status, kDevBadLen);
+    off[s + 1] = bad || n <= 0 ? 0 : ((n + kBM - 1) / kBM) * a.H;
+  }
+  if (tid == 0) off[0] = 0;
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < a.S; base += 32) {
+      const int i = base + lane;
+      int v = i < a.S ? off[i + 1] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += n;
+      }
+      v += carry;
+      if (i < a.S) off[i + 1] = v;
+      carry = __shfl_sync(kFull, v, 31);
+    }
+  }
+  __syncthreads();
+  const int total = off[a.S];
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ====================================== producer ======================================
+    if (lane == 0) {
+      int ni = 0, kt = 0, qi = 0;
+      uint32_t pend = 0;  // bit 0: Q, bits 1-2: K stages, bits 3-4: V stages with copies in flight
+      while (true) {
+        const int item = *abort_flag ? total : atomicAdd(a.sched, 1);
+        const bool done = item >= total;
+        const int sl = ni & 1;
+        if (mbar_wait(BAR(BI_EMPTY + sl), ((ni >> 1) & 1) ^ 1, abort_flag, a.status)) {
+          item_slot[sl] = done ? -1 : item;
+          mbar_arrive(BAR(BI_FULL + sl));
+        }
+        ++ni;
+        if (done) break;
+        const PItem it = locate(a, off, item);
+        if (it.nkv == 0) continue;
+        // Q tile (two 64-column halves)
+        if (!mbar_wait(BAR(BQ_EMPTY), (qi & 1) ^ 1, abort_flag, a.status)) break;
+        mbar_expect_tx(BAR(BQ_FULL), kTile);
+        tma_load_3d(sb + kSmQ, &tmap_q, 0, it.h, it.qrow0, BAR(BQ_FULL));
+        tma_load_3d(sb + kSmQ + kHalf, &tmap_q, 64, it.h, it.qrow0, BAR(BQ_FULL));
+        pend |= 1u;
+        ++qi;
+        const int32_t* table = a.block_tables + static_cast<int64_t>(it.s) * a.bt_row;
+        const int Lv = a.context_lens[it.s];
+        const int oob_row = a.num_blocks * B;  // any row past the cache: zero fill
+        for (int j = 0; j < it.nkv; ++j, ++kt) {
+          const int st = kt & 1;
+          const uint32_t ph = (kt >> 1) & 1;
+          const int frame0 = j * fpt;
+          // K
+          if (!mbar_wait(BAR(BK_EMPTY + st), ph ^ 1, abort_flag, a.status)) break;
+          mbar_expect_tx(BAR(BK_FULL + st), kTile);
+          for (int f = 0; f < fpt; ++f) {
+            const int lb = frame0 + f;
+            int row = oob_row;
+            if (lb * B < Lv) {
+              const int fr = table[lb];
+              if (fr >= 0 && fr < a.num_blocks) row = fr * B;
+              else atomicOr(a.status, kDevBadBlock);
+            }
+            const uint32_t dst = sb + kSmK + st * kTile + f * B * 128;
+            tma_load_3d(dst, &tmap_k, 0, it.h, row, BAR(BK_FULL + st));
+            tma_load_3d(dst + kHalf, &tmap_k, 64, it.h, row, BAR(BK_FULL + st));
+          }
+          pend |= 2u << st;
+          // V
+          if (!mbar_wait(BAR(BV_EMPTY + st), ph ^ 1, abort_flag, a.status)) break;
+          mbar_expect_tx(BAR(BV_FULL + st), kTile);
+          for (int f = 0; f < fpt; ++f) {
+            const int lb = frame0 + f;
+            int row = oob_row;
+            if (lb * B < Lv) {
+              const int fr = table[lb];
+              if (fr >= 0 && fr < a.num_blocks) row = fr * B;
+            }
+            const uint32_t dst = sb + kSmV + st * kTile + f * B * 128;
+            tma_load_3d(dst, &tmap_v, 0, it.h, row, BAR(BV_FULL + st));
+            tma_load_3d(dst + kHalf, &tmap_v, 64, it.h, row, BAR(BV_FULL + st));
+          }
+          pend |= 8u << st;
+        }
+      }
+      if (*abort_flag) {  // copies still landing must finish before the block retires
+        const long long t0 = clock64();
+        while (clock64() - t0 < kDrainCycles) {
+        }
+      }
+      __threadfence();
+      if (atomicAdd(a.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+        a.sched[0] = 0;
+        a.sched[1] = 0;
+        __threadfence();
+      }
+      (void)pend;
+    }
+  } else if (warp == 1) {
+    // ====================================== MMA issuer ======================================
+    int ni = 0, kt = 0, qi = 0, pt = 0;
+    const uint32_t id_qk = idesc<T>(false);
+    const uint32_t id_pv = idesc<T>(true);
+    auto pv = [&](int t) -> bool {
+      const int st = t & 1;
+      const uint32_t ph = (t >> 1) & 1;
+      if (!mbar_wait(BAR(BP_FULL), pt & 1, abort_flag, a.status)) return false;
+      if (!mbar_wait(BAR(BV_FULL + st), ph, abort_flag, a.status)) return false;
+      if (!mbar_wait(BAR(BO_EMPTY + st), ph ^ 1, abort_flag, a.status)) return false;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t d = tmem + 256 + st * 128;
+#pragma unroll
+      for (int ks = 0; ks < kBN / 16; ++ks) {
+        const uint64_t ad = sdesc(sb + kSmP + (ks >> 2) * kHalf + (ks & 3) * 32, 0, 1024);
+        const uint64_t bd = sdesc(sb + kSmV + st * kTile + ks * 16 * 128, kHalf, 1024);
+        mma(d, ad, bd, id_pv, ks > 0);
+      }
+      commit(BAR(BO_FULL + st));
+      commit(BAR(BV_EMPTY + st));
+      commit(BAR(BP_EMPTY));
+      ++pt;
+      return true;
+    };
+    if (lane == 0) {
+      while (true) {
+        const int sl = ni & 1;
+        int item = -1;
+        if (mbar_wait(BAR(BI_FULL + sl), (ni >> 1) & 1, abort_flag, a.status)) item = item_slot[sl];
+        mbar_arrive(BAR(BI_EMPTY + sl));
+        ++ni;
+        if (item < 0) break;
+        const PItem it = locate(a, off, item);
+        if (it.nkv == 0) continue;
+        if (!mbar_wait(BAR(BQ_FULL), qi & 1, abort_flag, a.status)) break;
+        ++qi;
+        bool ok = true;
+        for (int j = 0; j < it.nkv && ok; ++j) {
+          const int t = kt + j;
+          const int st = t & 1;
+          const uint32_t ph = (t >> 1) & 1;
+          if (!mbar_wait(BAR(BK_FULL + st), ph, abort_flag, a.status)) { ok = false; break; }
+          if (!mbar_wait(BAR(BS_EMPTY + st), ph ^ 1, abort_flag, a.status)) { ok = false; break; }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t d = tmem + st * 128;
+#pragma unroll
+          for (int ks = 0; ks < kD / 16; ++ks) {
+            const uint64_t ad = sdesc(sb + kSmQ + (ks >> 2) * kHalf + (ks & 3) * 32, 0, 1024);
+            const uint64_t bd = sdesc(sb + kSmK + st * kTile + (ks >> 2) * kHalf + (ks & 3) * 32, 0, 1024);
+            mma(d, ad, bd, id_qk, ks > 0);
+          }
+          commit(BAR(BS_FULL + st));
+          commit(BAR(BK_EMPTY + st));
+          if (j == it.nkv - 1) commit(BAR(BQ_EMPTY));
+          if (j >= 1) ok = pv(t - 1);
+        }
+        if (ok) ok = pv(kt + it.nkv - 1);
+        kt += it.nkv;
+        if (!ok) break;
+      }
+      // all MMAs of this lane complete before the TMEM can be freed
+      commit(BAR(BDRAIN));
+      const long long t0 = clock64();
+      while (!mbar_try(BAR(BDRAIN), 0) && clock64() - t0 < kDrainCycles) {
+      }
+    }
+  } else if (warp >= 4) {
+    // ====================================== softmax / epilogue ======================================
+    const int q4 = warp - 4;          // TMEM lane quadrant
+    const int row = q4 * 32 + lane;   // query row in the tile
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    int ni = 0, kt = 0, pt = 0;
+    while (true) {
+      const int sl = ni & 1;
+      int item = -1;
+      if (__all_sync(kFull, mbar_wait(BAR(BI_FULL + sl), (ni >> 1) & 1, abort_flag, a.status)))
+        item = item_slot[sl];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(BI_EMPTY + sl));
+      ++ni;
+      if (item < 0) break;
+      const PItem it = locate(a, off, item);
+      const bool valid = row < it.nrows;
+      // rows past the chunk end attend everything they are shown (not stored)
+      const int pos = valid ? it.pos0 + row : 0x3fffffff;
+      float m = -INFINITY, l = 0.f, m_acc = -INFINITY, m_tile = -INFINITY;
+      float o[kD];
+#pragma unroll
+      for (int i = 0; i < kD; ++i) o[i] = 0.f;
+      bool ok = true;
+      auto fold = [&](int t, float mt) -> bool {
+        const int st = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        if (!__all_sync(kFull, mbar_wait(BAR(BO_FULL + st), ph, abort_flag, a.status))) return false;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const float alpha = ex2(m_acc - mt);
+        m_acc = mt;
+#pragma unroll
+        for (int c = 0; c < kD / 16; ++c) {
+          float v[16];
+          tmem_ld16(tmem + lane_base + 256 + st * 128 + c * 16, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[c * 16 + i] = fmaf(o[c * 16 + i], alpha, v[i]);
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(BO_EMPTY + st));
+        return true;
+      };
+      for (int j = 0; j < it.nkv && ok; ++j) {
+        const int t = kt + j;
+        const int st = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        if (!__all_sync(kFull, mbar_wait(BAR(BS_FULL + st), ph, abort_flag, a.status))) { ok = false; break; }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t s_addr = tmem + lane_base + st * 128;
+        const int key0 = j * kBN;
+        const bool masked = key0 + kBN - 1 > it.pos0;  // the tile reaches past some row's position
+        // pass 1: row max
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kBN / 16; ++c) {
+          float v[16];
+          tmem_ld16(s_addr + c * 16, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float x = v[i] * a.qk_scale_log2;
+            if (masked && key0 + c * 16 + i > pos) x = -INFINITY;
+            mx = fmaxf(mx, x);
+          }
+        }
+        const float m_new = fmaxf(m, mx);
+        // P buffer must be free (previous P V done reading it)
+        if (!__all_sync(kFull, mbar_wait(BAR(BP_EMPTY), (pt & 1) ^ 1, abort_flag, a.status))) { ok = false; break; }
+        // pass 2: weights, row sum, P row to shared memory (K-major, 128-byte swizzle)
+        float sum = 0.f;
+        unsigned char* prow = smem + kSmP;
+#pragma unroll
+        for (int c = 0; c < kBN / 16; ++c) {
+          float v[16];
+          tmem_ld16(s_addr + c * 16, v);
+          // keys c*16 .. c*16+15 -> half (c >> 2), 16-byte chunks 2*(c&3), 2*(c&3)+1
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+              const int kk = c * 16 + q * 8 + i;
+              float x0 = v[q * 8 + i] * a.qk_scale_log2, x1 = v[q * 8 + i + 1] * a.qk_scale_log2;
+              if (masked && key0 + kk > pos) x0 = -INFINITY;
+              if (masked && key0 + kk + 1 > pos) x1 = -INFINITY;
+              const float p0 = ex2(x0 - m_new), p1 = ex2(x1 - m_new);
+              sum += p0 + p1;
+              w[i >> 1] = pack2<T>(p0, p1);
+            }
+            const int chunk = ((c & 3) * 2 + q) ^ (row & 7);
+            *reinterpret_cast<uint4*>(prow + (c >> 2) * kHalf + row * 128 + chunk * 16) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(BS_EMPTY + st));
+        l = l * ex2(m - m_new) + sum;
+        m = m_new;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(BP_FULL));
+        ++pt;
+        if (j >= 1 && !fold(t - 1, m_tile)) { ok = false; break; }
+        m_tile = m_new;
+      }
+      if (ok && it.nkv > 0) ok = fold(kt + it.nkv - 1, m_tile);
+      kt += it.nkv;
+      if (valid) {
+        const bool zero = !ok || it.bad || !(l > 0.f);
+        const float inv = zero ? 0.f : 1.f / l;
+        T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(it.qrow0 + row) * a.out_row +
+                static_cast<int64_t>(it.h) * kD;
+#pragma unroll
+        for (int c = 0; c < kD; c += 8) {
+          uint4 w4;
+          w4.x = pack2<T>(zero ? 0.f : o[c] * inv, zero ? 0.f : o[c + 1] * inv);
+          w4.y = pack2<T>(zero ? 0.f : o[c + 2] * inv, zero ? 0.f : o[c + 3] * inv);
+          w4.z = pack2<T>(zero ? 0.f : o[c + 4] * inv, zero ? 0.f : o[c + 5] * inv);
+          w4.w = pack2<T>(zero ? 0.f : o[c + 6] * inv, zero ? 0.f : o[c + 7] * inv);
+          *reinterpret_cast<uint4*>(op + c) = w4;
+        }
+      }
+      if (!ok) break;
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+}
+
+template <typename T>
+cudaError_t launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                   int grid, cudaStream_t stream) {
+  const size_t smem = smem_bytes(a.S);
+  auto kern = prefill_kernel<T>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace pk
+}  // namespace pa

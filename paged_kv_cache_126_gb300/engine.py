@@ -24,6 +24,7 @@ from ._binding import (
     pa_cache_append,
     pa_copy_blocks,
     pa_decode,
+    pa_prefill,
 )
 
 TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
@@ -131,6 +132,39 @@ class PagedKVEngine:
         pa_cache_append(k, v, dev[:n], self.k_cache, self.v_cache, stream=st)
         return out_slots, out_copies
 
+    def extend(self, seq: int, k_rows, v_rows):
+        """A prompt chunk for one sequence: its K/V rows go to the new slots."""
+        k = to_device_rows(k_rows, self.dtype, self.device)
+        v = to_device_rows(v_rows, self.dtype, self.device)
+        slots, copies = self.bm.extend(seq, k.shape[0])
+        st = self._stream()
+        if len(copies):
+            pa_copy_blocks(self.k_cache, self.v_cache, torch.from_numpy(np.ascontiguousarray(copies)).to(self.device),
+                           stream=st)
+        if len(slots):
+            pa_cache_append(k, v, torch.from_numpy(slots).to(self.device), self.k_cache, self.v_cache, stream=st)
+        return slots, copies
+
+    def prefill(self, seqs, counts, q, scale: float, out=None) -> torch.Tensor:
+        """Causal attention for the last counts[i] positions of seqs[i]; q rows grouped
+        by sequence in order."""
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        n = len(ids)
+        mb = self.max_blocks
+        q = to_device_rows(q, self.dtype, self.device)
+        if out is None:
+            out = torch.empty_like(q)
+        tables = np.empty((max(n, 1), mb), np.int32)
+        lens = np.empty(max(n, 1), np.int32)
+        self.bm.block_tables_into(ids, mb, tables, lens)
+        qs = np.zeros(n + 1, np.int32)
+        qs[1:] = np.cumsum(np.asarray(counts, np.int64))
+        dev = self.device
+        pa_prefill(q, self.k_cache, self.v_cache, torch.from_numpy(tables[:n]).to(dev),
+                   torch.from_numpy(lens[:n]).to(dev), torch.from_numpy(qs).to(dev), scale, out,
+                   stream=self._stream())
+        return out
+
     def attend(self, seqs, q, scale: float, out=None, params=None) -> torch.Tensor:
         """Decode attention for seqs with queries q [n, H, D]."""
         ids = self._ids_for(seqs)
@@ -197,6 +231,12 @@ def run_workload_ops(engine: PagedKVEngine, w, attend_params=None):
             trace[i] = {"slots": slots.tolist(), "copies": [tuple(c) for c in copies.tolist()]}
         elif kind == "free":
             engine.free(op[1])
+        elif kind == "extend":
+            k, v = w.rows(i)
+            slots, copies = engine.extend(op[1], k, v)
+            trace[i] = {"slots": slots.tolist(), "copies": [tuple(c) for c in copies.tolist()]}
+        elif kind == "prefill":
+            outs[i] = engine.prefill(op[1], op[2], w.query(i), w.scale)
         elif kind == "attend":
             outs[i] = engine.attend(op[1], w.query(i), w.scale, params=attend_params)
         else:

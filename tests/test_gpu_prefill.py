@@ -1,0 +1,86 @@
+"""GPU parity of pa_prefill (causal attention for query chunks, tensor cores).
+
+The kernel rounds the softmax weights to the cache dtype before the value product
+(the tensor cores take both operands in one 16-bit type).  Its error against the
+fp64 oracle is therefore bounded by u * sum_j w_j |v_j| (u = 2^-11 for fp16, 2^-8
+for bf16) plus fp32 accumulation error and the final rounding of the result; the
+test allows 2e-3 for the fp32 part on top of the other two, element-wise.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import prefill_weight_bound, round_to_storage
+from tests._gpu_common import run_both
+
+pytestmark = pytest.mark.gpu
+
+U = {"f16": 2.0 ** -11, "bf16": 2.0 ** -8}
+
+
+def check_prefill(w, outs, ref, tol=2e-3):
+    (op,) = w.prefill_ops
+    got = outs[op].double().cpu().numpy()
+    r = ref.outputs[op]
+    tables, lens = ref.attend_meta[op]
+    counts = w.ops[op][2]
+    qs = np.concatenate([[0], np.cumsum(counts)])
+    bound = prefill_weight_bound(w.query(op), ref.cache, tables, lens, qs, w.scale)
+    assert np.isfinite(got).all()
+    excess = np.abs(got - r) - np.abs(round_to_storage(r, w.dtype) - r) - U[w.dtype] * bound
+    worst = np.unravel_index(np.argmax(excess), excess.shape)
+    assert excess.max() <= tol, f"excess {excess.max():.3e} at {worst}: {got[worst]} vs {r[worst]}"
+    return float(np.abs(got - r).max())
+
+
+def test_small_prefill_batch(pa):
+    w = workloads.prefill_batch(small=True)
+    eng, outs, ref = run_both(pa, w)
+    check_prefill(w, outs, ref)
+
+
+@pytest.mark.parametrize("prefix,chunk", [
+    ([0], [1]), ([0], [127]), ([0], [128]), ([0], [129]), ([0], [300]),
+    ([5], [1]), ([100], [1]), ([127], [1]), ([128], [1]), ([1000], [64]),
+    ([0, 17, 256, 900], [513, 1, 128, 77]),
+])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_chunks_and_prefixes(pa, prefix, chunk, dtype):
+    w = workloads.chunked_prefill(prefix, chunk, H=2, D=128, B=16, dtype=dtype, seed=sum(prefix) + sum(chunk))
+    eng, outs, ref = run_both(pa, w)
+    check_prefill(w, outs, ref)
+
+
+@pytest.mark.parametrize("B", [8, 16, 32, 64, 128])
+def test_block_sizes(pa, B):
+    w = workloads.chunked_prefill([0, 300, 77], [200, 150, 260], H=3, D=128, B=B, dtype="f16", seed=B)
+    eng, outs, ref = run_both(pa, w)
+    check_prefill(w, outs, ref)
+
+
+def test_many_items_per_block(pa):
+    """More work items than SMs: several items per persistent block, ring reuse."""
+    rng = np.random.default_rng(5)
+    pre = rng.integers(0, 700, size=10).tolist()
+    ch = rng.integers(100, 400, size=10).tolist()
+    w = workloads.chunked_prefill(pre, ch, H=8, D=128, B=16, dtype="bf16", seed=5)
+    eng, outs, ref = run_both(pa, w)
+    check_prefill(w, outs, ref)
+    # the work counter resets itself: a second launch gives the same bits
+    (op,) = w.prefill_ops
+    again = eng.prefill(w.ops[op][1], w.ops[op][2], w.query(op), w.scale)
+    assert torch.equal(again, outs[op])
+    assert pa.pa_get_device_status() == 0
+
+
+def test_prefill_one_query_matches_decode(pa):
+    """A chunk of one query is a decode step: both kernels agree within tolerance."""
+    L = [37, 300, 811, 1]
+    w = workloads.chunked_prefill([x - 1 for x in L], [1] * len(L), H=4, D=128, B=16, dtype="f16", seed=9)
+    eng, outs, ref = run_both(pa, w)
+    check_prefill(w, outs, ref)
+    (op,) = w.prefill_ops
+    dec = eng.attend(w.ops[op][1], w.query(op), w.scale)
+    assert (dec.float() - outs[op].float()).abs().max().item() < 2e-3
