@@ -523,6 +523,69 @@ def sweep(keys, reps=20):
         torch.cuda.empty_cache()
 
 
+# ----------------------------------------------------------------------------- chunked prefill
+def prefill_flops(prefix_lens, chunk_lens, H, D) -> int:
+    """Causal attention FLOPs: query at position p does 2*D*(p+1) for Q K^T and the
+    same for P V, per head."""
+    total = 0
+    for L0, n in zip(prefix_lens, chunk_lens):
+        # sum over positions L0 .. L0+n-1 of (p + 1)
+        total += n * (2 * L0 + n + 1) // 2
+    return 4 * D * H * total
+
+
+def prefill_bench(reps=20):
+    """pa_prefill on the chunked-prefill batch; one JSON line (TFLOP/s)."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_126_gb300 as pa
+    import workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    st = torch.cuda.current_stream(dev)
+    w = workloads.prefill_batch()
+    eng = pa.PagedKVEngine(w.num_blocks, w.block_size, w.num_heads, w.head_dim, w.dtype, free_order=w.free_order,
+                           device=dev, max_seqs=64,
+                           max_blocks_per_seq=max(-(-L // w.block_size) for L in w.final_lens.values()))
+    (op,) = w.prefill_ops
+    for i, o in enumerate(w.ops[:op]):
+        if o[0] == "add":
+            eng.add_seq(o[1], *w.rows(i))
+        elif o[0] == "extend":
+            eng.extend(o[1], *w.rows(i))
+    seqs, counts = w.ops[op][1], w.ops[op][2]
+    tables, lens = eng.bm.block_tables(seqs, eng.max_blocks)
+    qs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    tt, ll, qq = (torch.from_numpy(x).to(dev) for x in (tables, lens, qs))
+    q = pa.to_device_rows(w.query(op), w.dtype, dev)
+    out = torch.empty_like(q)
+    for _ in range(3):
+        pa.pa_prefill(q, eng.k_cache, eng.v_cache, tt, ll, qq, w.scale, out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        pa.pa_prefill(q, eng.k_cache, eng.v_cache, tt, ll, qq, w.scale, out)
+    e1.record(st)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / reps * 1e3
+    prefix = [int(L) - int(n) for L, n in zip(lens, counts)]
+    flops = prefill_flops(prefix, counts, w.num_heads, w.head_dim)
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, src = float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except Exception:
+        peak, src = 1900.0, "fallback (1.9 PFLOP/s)"
+    tf = flops / (us * 1e-6) / 1e12
+    print(json.dumps({"metric": "chunked prefill attention TFLOP/s (causal FLOPs)", "workload": w.name,
+                      "prefill_us": round(us, 2), "flops": flops, "tflops": round(tf, 1),
+                      "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                                   "frac": round(tf / peak, 4), "peak_source": src},
+                      "query_rows": int(qs[-1]), "dtype": w.dtype}), flush=True)
+
+
 # ----------------------------------------------------------------------------- reference arm
 def reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
@@ -570,9 +633,13 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--config", default="1")
     ap.add_argument("--cpu-worker", default=None)
+    ap.add_argument("--prefill", action="store_true", help="time pa_prefill on the chunked-prefill batch instead")
     ap.add_argument("--sweep", default=None, metavar="KEYS",
                     help="time pa_decode on each listed workload instead (comma list of 0,1,1x,2,3,3c,4 or 'all')")
     args = ap.parse_args()
+    if args.prefill:
+        prefill_bench()
+        return
     if args.sweep is not None:
         keys = SWEEP_KEYS if args.sweep == "all" else tuple(args.sweep.split(","))
         sweep(keys)
