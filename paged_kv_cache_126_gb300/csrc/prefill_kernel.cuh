@@ -57,8 +57,8 @@ constexpr uint32_t kHalf = 16384; // one 64-column half of a tile
 constexpr uint32_t kSmQ = 0;
 constexpr uint32_t kSmK = kSmQ + kTile;           // 2 stages
 constexpr uint32_t kSmV = kSmK + 2 * kTile;       // 2 stages
-constexpr uint32_t kSmP = kSmV + 2 * kTile;
-constexpr uint32_t kSmBar = kSmP + kTile;         // mbarriers
+constexpr uint32_t kSmP = kSmV + 2 * kTile;       // 2 buffers
+constexpr uint32_t kSmBar = kSmP + 2 * kTile;     // mbarriers
 constexpr uint32_t kSmMisc = kSmBar + 32 * 8;     // flags, TMEM address, item ring
 constexpr uint32_t kSmOff = kSmMisc + 64;         // per-sequence item offsets [S + 1]
 __host__ __device__ constexpr uint32_t smem_bytes(int S) { return kSmOff + 4u * (S + 1) + 1024u; }
@@ -68,10 +68,10 @@ enum : int {
   BQ_FULL = 0, BQ_EMPTY = 1,
   BK_FULL = 2, BK_EMPTY = 4, BV_FULL = 6, BV_EMPTY = 8,   // [2] each
   BS_FULL = 10, BS_EMPTY = 12, BO_FULL = 14, BO_EMPTY = 16,  // [2] each
-  BP_FULL = 18, BP_EMPTY = 19,
-  BI_FULL = 20, BI_EMPTY = 22,                             // item ring [2]
-  BDRAIN = 24,
-  NBARS = 25
+  BP_FULL = 18, BP_EMPTY = 20,                             // [2] each
+  BI_FULL = 22, BI_EMPTY = 24,                             // item ring [2]
+  BDRAIN = 26,
+  NBARS = 27
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -175,6 +175,40 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// tcgen05.ld of 32 columns without waiting; pair with tmem_wait_ld() and tie32().
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Empty statement that claims to rewrite the registers: every later use depends on it,
+// and it is ordered after the (volatile) wait that precedes it.
+__device__ __forceinline__ void tie32(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]),
+      "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float a, float b);
 template <>
@@ -247,7 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < NBARS; ++i) {
       uint32_t cnt = 1;
-      if (i == BS_EMPTY || i == BS_EMPTY + 1 || i == BO_EMPTY || i == BO_EMPTY + 1 || i == BP_FULL) cnt = 4;
+      if (i == BS_EMPTY || i == BS_EMPTY + 1 || i == BO_EMPTY || i == BO_EMPTY + 1 || i == BP_FULL ||
+          i == BP_FULL + 1)
+        cnt = 4;
       if (i == BI_EMPTY || i == BI_EMPTY + 1) cnt = 5;  // MMA warp + 4 softmax warps
       mbar_init(BAR(i), cnt);
     }
@@ -374,27 +410,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ====================================== MMA issuer ======================================
-    int ni = 0, kt = 0, qi = 0, pt = 0;
+    // S_t = Q K_t^T into TMEM buffer t%2; O (+)= P_t V_t into one O buffer that
+    // accumulates over the item's key tiles (the first tile overwrites it).
+    int ni = 0, kt = 0, qi = 0, oi = 0;
     const uint32_t id_qk = idesc<T>(false);
     const uint32_t id_pv = idesc<T>(true);
-    auto pv = [&](int t) -> bool {
+    const uint32_t o_tmem = tmem + 256;
+    auto pv = [&](int t, bool first) -> bool {
       const int st = t & 1;
       const uint32_t ph = (t >> 1) & 1;
-      if (!mbar_wait(BAR(BP_FULL), pt & 1, abort_flag, a.status)) return false;
+      if (!mbar_wait(BAR(BP_FULL + st), ph, abort_flag, a.status)) return false;
       if (!mbar_wait(BAR(BV_FULL + st), ph, abort_flag, a.status)) return false;
-      if (!mbar_wait(BAR(BO_EMPTY + st), ph ^ 1, abort_flag, a.status)) return false;
+      if (first && !mbar_wait(BAR(BO_EMPTY), (oi & 1) ^ 1, abort_flag, a.status)) return false;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t d = tmem + 256 + st * 128;
 #pragma unroll
       for (int ks = 0; ks < kBN / 16; ++ks) {
-        const uint64_t ad = sdesc(sb + kSmP + (ks >> 2) * kHalf + (ks & 3) * 32, 0, 1024);
+        const uint64_t ad = sdesc(sb + kSmP + st * kTile + (ks >> 2) * kHalf + (ks & 3) * 32, 0, 1024);
         const uint64_t bd = sdesc(sb + kSmV + st * kTile + ks * 16 * 128, kHalf, 1024);
-        mma(d, ad, bd, id_pv, ks > 0);
+        mma(o_tmem, ad, bd, id_pv, (!first || ks > 0) ? 1u : 0u);
       }
-      commit(BAR(BO_FULL + st));
       commit(BAR(BV_EMPTY + st));
-      commit(BAR(BP_EMPTY));
-      ++pt;
+      commit(BAR(BP_EMPTY + st));  // P buffer free again; O holds the tiles so far
       return true;
     };
     if (lane == 0) {
@@ -422,14 +458,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ks = 0; ks < kD / 16; ++ks) {
             const uint64_t ad = sdesc(sb + kSmQ + (ks >> 2) * kHalf + (ks & 3) * 32, 0, 1024);
             const uint64_t bd = sdesc(sb + kSmK + st * kTile + (ks >> 2) * kHalf + (ks & 3) * 32, 0, 1024);
-            mma(d, ad, bd, id_qk, ks > 0);
+            mma(d, ad, bd, id_qk, ks > 0 ? 1u : 0u);
           }
           commit(BAR(BS_FULL + st));
           commit(BAR(BK_EMPTY + st));
           if (j == it.nkv - 1) commit(BAR(BQ_EMPTY));
-          if (j >= 1) ok = pv(t - 1);
+          if (j >= 1) ok = pv(t - 1, j == 1);
         }
-        if (ok) ok = pv(kt + it.nkv - 1);
+        if (ok) ok = pv(kt + it.nkv - 1, it.nkv == 1);
+        if (ok) commit(BAR(BO_FULL));  // O final for this item
+        ++oi;
         kt += it.nkv;
         if (!ok) break;
       }
@@ -441,10 +479,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ====================================== softmax / epilogue ======================================
+    // Thread = query row = TMEM lane.  The whole S row lives in registers; weights
+    // use a reference max m_ref that is raised (and O, l rescaled) only when the
+    // row max exceeds it by more than 8 (log2 units), so weights stay <= 2^8.
     const int q4 = warp - 4;          // TMEM lane quadrant
     const int row = q4 * 32 + lane;   // query row in the tile
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
-    int ni = 0, kt = 0, pt = 0;
+    const uint32_t o_tmem = tmem + lane_base + 256;
+    const float sl2 = a.qk_scale_log2;
+    int ni = 0, kt = 0, oi = 0;
     while (true) {
       const int sl = ni & 1;
       int item = -1;
@@ -458,110 +501,126 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = row < it.nrows;
       // rows past the chunk end attend everything they are shown (not stored)
       const int pos = valid ? it.pos0 + row : 0x3fffffff;
-      float m = -INFINITY, l = 0.f, m_acc = -INFINITY, m_tile = -INFINITY;
-      float o[kD];
-#pragma unroll
-      for (int i = 0; i < kD; ++i) o[i] = 0.f;
+      float m_ref = -INFINITY, l = 0.f;
       bool ok = true;
-      auto fold = [&](int t, float mt) -> bool {
-        const int st = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
-        if (!__all_sync(kFull, mbar_wait(BAR(BO_FULL + st), ph, abort_flag, a.status))) return false;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const float alpha = ex2(m_acc - mt);
-        m_acc = mt;
-#pragma unroll
-        for (int c = 0; c < kD / 16; ++c) {
-          float v[16];
-          tmem_ld16(tmem + lane_base + 256 + st * 128 + c * 16, v);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) o[c * 16 + i] = fmaf(o[c * 16 + i], alpha, v[i]);
-        }
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(BO_EMPTY + st));
-        return true;
-      };
       for (int j = 0; j < it.nkv && ok; ++j) {
         const int t = kt + j;
         const int st = t & 1;
         const uint32_t ph = (t >> 1) & 1;
         if (!__all_sync(kFull, mbar_wait(BAR(BS_FULL + st), ph, abort_flag, a.status))) { ok = false; break; }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        uint32_t sr[4][32];
         const uint32_t s_addr = tmem + lane_base + st * 128;
-        const int key0 = j * kBN;
-        const bool masked = key0 + kBN - 1 > it.pos0;  // the tile reaches past some row's position
-        // pass 1: row max
-        float mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kBN / 16; ++c) {
-          float v[16];
-          tmem_ld16(s_addr + c * 16, v);
+        for (int c = 0; c < 4; ++c) tmem_ld32_async(s_addr + c * 32, sr[c]);
+        tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float x = v[i] * a.qk_scale_log2;
-            if (masked && key0 + c * 16 + i > pos) x = -INFINITY;
-            mx = fmaxf(mx, x);
-          }
-        }
-        const float m_new = fmaxf(m, mx);
-        // P buffer must be free (previous P V done reading it)
-        if (!__all_sync(kFull, mbar_wait(BAR(BP_EMPTY), (pt & 1) ^ 1, abort_flag, a.status))) { ok = false; break; }
-        // pass 2: weights, row sum, P row to shared memory (K-major, 128-byte swizzle)
-        float sum = 0.f;
-        unsigned char* prow = smem + kSmP;
-#pragma unroll
-        for (int c = 0; c < kBN / 16; ++c) {
-          float v[16];
-          tmem_ld16(s_addr + c * 16, v);
-          // keys c*16 .. c*16+15 -> half (c >> 2), 16-byte chunks 2*(c&3), 2*(c&3)+1
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-              const int kk = c * 16 + q * 8 + i;
-              float x0 = v[q * 8 + i] * a.qk_scale_log2, x1 = v[q * 8 + i + 1] * a.qk_scale_log2;
-              if (masked && key0 + kk > pos) x0 = -INFINITY;
-              if (masked && key0 + kk + 1 > pos) x1 = -INFINITY;
-              const float p0 = ex2(x0 - m_new), p1 = ex2(x1 - m_new);
-              sum += p0 + p1;
-              w[i >> 1] = pack2<T>(p0, p1);
-            }
-            const int chunk = ((c & 3) * 2 + q) ^ (row & 7);
-            *reinterpret_cast<uint4*>(prow + (c >> 2) * kHalf + row * 128 + chunk * 16) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-          }
-        }
+        for (int c = 0; c < 4; ++c) tie32(sr[c]);
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(BS_EMPTY + st));
-        l = l * ex2(m - m_new) + sum;
-        m = m_new;
+        const int key0 = j * kBN;
+        if (key0 + kBN - 1 > it.pos0) {  // the tile reaches past some row's position
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (key0 + c * 32 + i > pos) sr[c][i] = __float_as_uint(-INFINITY);
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+        const float m_new = fmaxf(m_ref, mx * sl2);
+        const bool raise = m_new > m_ref + 8.f;
+        const float alpha = raise ? ex2(m_ref - m_new) : 1.f;
+        if (raise) {
+          l *= alpha;
+          m_ref = m_new;
+        }
+        if (j > 0 && __any_sync(kFull, raise)) {
+          // rescale this warp's rows of O in TMEM (lanes that did not raise scale by 1)
+          // once the previous tile's P V has landed in O
+          const int tp = t - 1;
+          if (!__all_sync(kFull, mbar_wait(BAR(BP_EMPTY + (tp & 1)), (tp >> 1) & 1, abort_flag, a.status))) {
+            ok = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld32_async(o_tmem + c * 32, r);
+            tmem_wait_ld();
+            tie32(r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(o_tmem + c * 32, r);
+          }
+          tmem_wait_st();
+        }
+        // this P buffer was last read by the P V of tile t-2
+        if (!__all_sync(kFull, mbar_wait(BAR(BP_EMPTY + st), ph ^ 1, abort_flag, a.status))) { ok = false; break; }
+        // weights, row sum, P row into shared memory (K-major, 128-byte swizzle)
+        float sum = 0.f;
+        unsigned char* prow = smem + kSmP + st * kTile;
+        const float nm = -m_ref;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+              const float p0 = ex2(fmaf(__uint_as_float(sr[c][q * 8 + i]), sl2, nm));
+              const float p1 = ex2(fmaf(__uint_as_float(sr[c][q * 8 + i + 1]), sl2, nm));
+              sum += p0 + p1;
+              w[i >> 1] = pack2<T>(p0, p1);
+            }
+            // keys c*32 + 8q .. +7 -> half (c >> 1), 16-byte chunk (c & 1) * 4 + q
+            const int chunk = ((c & 1) * 4 + q) ^ (row & 7);
+            *reinterpret_cast<uint4*>(prow + (c >> 1) * kHalf + row * 128 + chunk * 16) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        l += sum;
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(BP_FULL));
-        ++pt;
-        if (j >= 1 && !fold(t - 1, m_tile)) { ok = false; break; }
-        m_tile = m_new;
+        if (lane == 0) mbar_arrive(BAR(BP_FULL + st));
       }
-      if (ok && it.nkv > 0) ok = fold(kt + it.nkv - 1, m_tile);
       kt += it.nkv;
-      if (valid) {
-        const bool zero = !ok || it.bad || !(l > 0.f);
-        const float inv = zero ? 0.f : 1.f / l;
-        T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(it.qrow0 + row) * a.out_row +
-                static_cast<int64_t>(it.h) * kD;
+      // epilogue: wait for the item's last P V, normalise, store
+      if (ok && it.nkv > 0 && !__all_sync(kFull, mbar_wait(BAR(BO_FULL), oi & 1, abort_flag, a.status))) ok = false;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const bool zero = !ok || it.bad || !(l > 0.f);
+      const float inv = zero ? 0.f : 1.f / l;
+      T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(it.qrow0 + row) * a.out_row +
+              static_cast<int64_t>(it.h) * kD;
 #pragma unroll
-        for (int c = 0; c < kD; c += 8) {
-          uint4 w4;
-          w4.x = pack2<T>(zero ? 0.f : o[c] * inv, zero ? 0.f : o[c + 1] * inv);
-          w4.y = pack2<T>(zero ? 0.f : o[c + 2] * inv, zero ? 0.f : o[c + 3] * inv);
-          w4.z = pack2<T>(zero ? 0.f : o[c + 4] * inv, zero ? 0.f : o[c + 5] * inv);
-          w4.w = pack2<T>(zero ? 0.f : o[c + 6] * inv, zero ? 0.f : o[c + 7] * inv);
-          *reinterpret_cast<uint4*>(op + c) = w4;
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32_async(o_tmem + c * 32, r);
+        tmem_wait_ld();
+        tie32(r);
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w4;
+            w4.x = pack2<T>(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv);
+            w4.y = pack2<T>(__uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv);
+            w4.z = pack2<T>(__uint_as_float(r[i + 4]) * inv, __uint_as_float(r[i + 5]) * inv);
+            w4.w = pack2<T>(__uint_as_float(r[i + 6]) * inv, __uint_as_float(r[i + 7]) * inv);
+            if (zero) w4 = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(op + c * 32 + i) = w4;
+          }
         }
       }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(BO_EMPTY));
+      ++oi;
       if (!ok) break;
     }
   }
