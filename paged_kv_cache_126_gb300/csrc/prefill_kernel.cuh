@@ -15,8 +15,8 @@
 //     assembled from 128/B frames by 3-D TMA loads (box {64, 1, B}, 128-byte
 //     swizzle, two 64-column halves); frames past the sequence end are loaded from
 //     an out-of-range row, i.e. zero-filled.
-//   * warp 0 (one lane): TMA producer -- Q tile, then K and V tiles into two-stage
-//     rings.  warp 1 (one lane): tcgen05.mma issuer -- S = Q K^T into one of two
+//   * warp 0: TMA producer -- Q tile, then K and V tiles into two-stage rings; the
+//     frame copies of a tile are issued by the warp's lanes in parallel.  warp 1 (one lane): tcgen05.mma issuer -- S = Q K^T into one of two
 //     128-column TMEM buffers, then O_j = P_j V_j into one of two more (fp32
 //     accumulators, M = N = 128, K = 16 per instruction); Q K^T of tile j+1 is
 //     issued before P V of tile j so the tensor cores work while the softmax runs.
@@ -333,68 +333,87 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ====================================== producer ======================================
-    if (lane == 0) {
-      int ni = 0, kt = 0, qi = 0;
-      uint32_t pend = 0;  // bit 0: Q, bits 1-2: K stages, bits 3-4: V stages with copies in flight
-      while (true) {
-        const int item = *abort_flag ? total : atomicAdd(a.sched, 1);
-        const bool done = item >= total;
-        const int sl = ni & 1;
-        if (mbar_wait(BAR(BI_EMPTY + sl), ((ni >> 1) & 1) ^ 1, abort_flag, a.status)) {
-          item_slot[sl] = done ? -1 : item;
-          mbar_arrive(BAR(BI_FULL + sl));
-        }
-        ++ni;
-        if (done) break;
-        const PItem it = locate(a, off, item);
-        if (it.nkv == 0) continue;
-        // Q tile (two 64-column halves)
-        if (!mbar_wait(BAR(BQ_EMPTY), (qi & 1) ^ 1, abort_flag, a.status)) break;
-        mbar_expect_tx(BAR(BQ_FULL), kTile);
-        tma_load_3d(sb + kSmQ, &tmap_q, 0, it.h, it.qrow0, BAR(BQ_FULL));
-        tma_load_3d(sb + kSmQ + kHalf, &tmap_q, 64, it.h, it.qrow0, BAR(BQ_FULL));
-        pend |= 1u;
-        ++qi;
-        const int32_t* table = a.block_tables + static_cast<int64_t>(it.s) * a.bt_row;
-        const int Lv = a.context_lens[it.s];
-        const int oob_row = a.num_blocks * B;  // any row past the cache: zero fill
-        for (int j = 0; j < it.nkv; ++j, ++kt) {
-          const int st = kt & 1;
-          const uint32_t ph = (kt >> 1) & 1;
-          const int frame0 = j * fpt;
-          // K
-          if (!mbar_wait(BAR(BK_EMPTY + st), ph ^ 1, abort_flag, a.status)) break;
-          mbar_expect_tx(BAR(BK_FULL + st), kTile);
-          for (int f = 0; f < fpt; ++f) {
-            const int lb = frame0 + f;
-            int row = oob_row;
-            if (lb * B < Lv) {
-              const int fr = table[lb];
-              if (fr >= 0 && fr < a.num_blocks) row = fr * B;
-              else atomicOr(a.status, kDevBadBlock);
-            }
-            const uint32_t dst = sb + kSmK + st * kTile + f * B * 128;
-            tma_load_3d(dst, &tmap_k, 0, it.h, row, BAR(BK_FULL + st));
-            tma_load_3d(dst + kHalf, &tmap_k, 64, it.h, row, BAR(BK_FULL + st));
-          }
-          pend |= 2u << st;
-          // V
-          if (!mbar_wait(BAR(BV_EMPTY + st), ph ^ 1, abort_flag, a.status)) break;
-          mbar_expect_tx(BAR(BV_FULL + st), kTile);
-          for (int f = 0; f < fpt; ++f) {
-            const int lb = frame0 + f;
-            int row = oob_row;
-            if (lb * B < Lv) {
-              const int fr = table[lb];
-              if (fr >= 0 && fr < a.num_blocks) row = fr * B;
-            }
-            const uint32_t dst = sb + kSmV + st * kTile + f * B * 128;
-            tma_load_3d(dst, &tmap_v, 0, it.h, row, BAR(BV_FULL + st));
-            tma_load_3d(dst + kHalf, &tmap_v, 64, it.h, row, BAR(BV_FULL + st));
-          }
-          pend |= 8u << st;
+    // Lane 0 takes work items and arms the barriers; the frame copies of a key tile
+    // are spread over the warp (one 64-column half of one frame per lane), each lane
+    // reading its own block-table entry, so a tile costs one table-load latency
+    // instead of one per frame.  The entries of the next tile are read before the
+    // wait for its ring slot.
+    int ni = 0, kt = 0, qi = 0;
+    const int ncopy = 2 * fpt;  // TMA copies per K (or V) tile
+    while (true) {
+      int item = 0;
+      if (lane == 0) item = *abort_flag ? total : atomicAdd(a.sched, 1);
+      item = __shfl_sync(kFull, item, 0);
+      const bool done = item >= total;
+      const int sl = ni & 1;
+      if (lane == 0 && mbar_wait(BAR(BI_EMPTY + sl), ((ni >> 1) & 1) ^ 1, abort_flag, a.status)) {
+        item_slot[sl] = done ? -1 : item;
+        mbar_arrive(BAR(BI_FULL + sl));
+      }
+      ++ni;
+      if (done) break;
+      const PItem it = locate(a, off, item);
+      if (it.nkv == 0) continue;
+      // Q tile (two 64-column halves)
+      int ok = 1;
+      if (lane == 0) {
+        ok = mbar_wait(BAR(BQ_EMPTY), (qi & 1) ^ 1, abort_flag, a.status);
+        if (ok) {
+          mbar_expect_tx(BAR(BQ_FULL), kTile);
+          tma_load_3d(sb + kSmQ, &tmap_q, 0, it.h, it.qrow0, BAR(BQ_FULL));
+          tma_load_3d(sb + kSmQ + kHalf, &tmap_q, 64, it.h, it.qrow0, BAR(BQ_FULL));
         }
       }
+      ok = __shfl_sync(kFull, ok, 0);
+      if (!ok) break;
+      ++qi;
+      const int32_t* table = a.block_tables + static_cast<int64_t>(it.s) * a.bt_row;
+      const int Lv = a.context_lens[it.s];
+      const int oob_row = a.num_blocks * B;  // any row past the cache: zero fill
+      // cache row of the frame a lane copies in tile j (copy c: frame c >> 1, half c & 1)
+      auto frame_row = [&](int j, int c) -> int {
+        const int lb = j * fpt + (c >> 1);
+        int row = oob_row;
+        if (c < ncopy && lb * B < Lv) {
+          const int fr = __ldg(table + lb);
+          if (fr >= 0 && fr < a.num_blocks) row = fr * B;
+          else if ((c & 1) == 0) atomicOr(a.status, kDevBadBlock);
+        }
+        return row;
+      };
+      int row = frame_row(0, lane);
+      for (int j = 0; j < it.nkv; ++j, ++kt) {
+        const int st = kt & 1;
+        const uint32_t ph = (kt >> 1) & 1;
+        // K
+        if (lane == 0) {
+          ok = mbar_wait(BAR(BK_EMPTY + st), ph ^ 1, abort_flag, a.status);
+          if (ok) mbar_expect_tx(BAR(BK_FULL + st), kTile);
+        }
+        ok = __shfl_sync(kFull, ok, 0);
+        if (!ok) break;
+        for (int c = lane; c < ncopy; c += 32) {
+          const int r = c < 32 ? row : frame_row(j, c);
+          tma_load_3d(sb + kSmK + st * kTile + (c >> 1) * B * 128 + (c & 1) * kHalf, &tmap_k, (c & 1) * 64, it.h,
+                      r, BAR(BK_FULL + st));
+        }
+        // V
+        if (lane == 0) {
+          ok = mbar_wait(BAR(BV_EMPTY + st), ph ^ 1, abort_flag, a.status);
+          if (ok) mbar_expect_tx(BAR(BV_FULL + st), kTile);
+        }
+        ok = __shfl_sync(kFull, ok, 0);
+        if (!ok) break;
+        for (int c = lane; c < ncopy; c += 32) {
+          const int r = c < 32 ? row : frame_row(j, c);
+          tma_load_3d(sb + kSmV + st * kTile + (c >> 1) * B * 128 + (c & 1) * kHalf, &tmap_v, (c & 1) * 64, it.h,
+                      r, BAR(BV_FULL + st));
+        }
+        if (j + 1 < it.nkv) row = frame_row(j + 1, lane);
+      }
+      if (!ok) break;
+    }
+    if (lane == 0) {
       if (*abort_flag) {  // copies still landing must finish before the block retires
         const long long t0 = clock64();
         while (clock64() - t0 < kDrainCycles) {
@@ -406,7 +425,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         a.sched[1] = 0;
         __threadfence();
       }
-      (void)pend;
     }
   } else if (warp == 1) {
     // ====================================== MMA issuer ======================================
