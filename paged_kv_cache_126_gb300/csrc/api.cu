@@ -97,6 +97,27 @@ int make_sw128_map(CUtensorMap* map, void* base, int dtype, int64_t rows, int64_
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
 }
 
+// A whole cache frame of one head in one copy, laid out in shared memory as
+// [B/8 groups][2 column halves][8 rows][64 elements] with the 128-byte swizzle: the
+// 5-D view splits the row index into (row mod 8, row / 8) and the head dimension
+// into two 64-element halves, ordered so that the box lands half-major inside each
+// 8-row group.  rows must be a multiple of 8; every coordinate of the view stays
+// inside the cache, so the last frame's box never leaves the allocation.
+int make_frame_map(CUtensorMap* map, void* base, int dtype, int64_t rows, int64_t H, int64_t D, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return PA_ERR_CUDA;
+  if (rows % 8 != 0 || box_rows % 8 != 0 || D != 128) return PA_ERR_UNSUPPORTED;
+  CUtensorMapDataType t = dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(H * D * 2);
+  cuuint64_t dims[5] = {64, 8, 2, static_cast<cuuint64_t>(rows / 8), static_cast<cuuint64_t>(H)};
+  cuuint64_t strides[4] = {row_bytes, 128, 8 * row_bytes, static_cast<cuuint64_t>(D * 2)};
+  cuuint32_t box[5] = {64, 8, 2, static_cast<cuuint32_t>(box_rows / 8), 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(map, t, 5, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
+}
+
 // ---- library-owned workspace, one per (device, stream) -------------------------------------
 // Layout: [0, 256) scheduler counters | arrival counters, one per (sequence, head) |
 // per-launch offsets and split partials.  Both counter regions must hold zeros
@@ -535,8 +556,8 @@ int pa_prefill(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_
 
   CUtensorMap tq, tk, tv;
   PA_TRY(make_sw128_map(&tq, q->data, dt, T, H, D, q->stride[0], 128));
-  PA_TRY(make_sw128_map(&tk, k_cache->data, dt, nb * B, H, D, H * D, static_cast<int>(B)));
-  PA_TRY(make_sw128_map(&tv, v_cache->data, dt, nb * B, H, D, H * D, static_cast<int>(B)));
+  PA_TRY(make_frame_map(&tk, k_cache->data, dt, nb * B, H, D, static_cast<int>(B)));
+  PA_TRY(make_frame_map(&tv, v_cache->data, dt, nb * B, H, D, static_cast<int>(B)));
   void* ws = nullptr;
   size_t cnt_bytes = 0;
   PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), 0, 0, &ws, &cnt_bytes));

@@ -12,9 +12,11 @@
 // Design (one thread block per SM, persistent, dynamic work counter):
 //   * Work item = (sequence, head, tile of 128 queries); later (longer) query
 //     tiles of a sequence first.  K/V are walked in tiles of 128 keys, each
-//     assembled from 128/B frames by 3-D TMA loads (box {64, 1, B}, 128-byte
-//     swizzle, two 64-column halves); frames past the sequence end are loaded from
-//     an out-of-range row, i.e. zero-filled.
+//     assembled from 128/B frames, one TMA copy per frame through a 5-D view of the
+//     cache that lands the frame as [B/8 row groups][2 column halves][8 rows][64]
+//     (128-byte swizzle; the MMA descriptors stride 2048 bytes per 8 keys); frames
+//     past the sequence end are read at an out-of-range group, i.e. zero-filled.
+//     The Q tile is [2 halves][128 rows][64] (two 3-D copies).
 //   * warp 0: TMA producer -- Q tile, then K and V tiles into two-stage rings; the
 //     frame copies of a tile are issued by the warp's lanes in parallel.  warp 1 (one lane): tcgen05.mma issuer -- S = Q K^T into one of two
 //     128-column TMEM buffers, then O_j = P_j V_j into one of two more (fp32
@@ -117,6 +119,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+// Whole frame of one head: coordinates (0, 0, 0, first 8-row group, head) of the 5-D
+// frame view of a cache.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, int group, int head,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %2, %2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(group), "r"(head), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ float ex2(float x) {
@@ -333,13 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ====================================== producer ======================================
-    // Lane 0 takes work items and arms the barriers; the frame copies of a key tile
-    // are spread over the warp (one 64-column half of one frame per lane), each lane
-    // reading its own block-table entry, so a tile costs one table-load latency
-    // instead of one per frame.  The entries of the next tile are read before the
-    // wait for its ring slot.
+    // Lane 0 takes work items and arms the barriers; lane f issues the copy of frame
+    // f of a key tile (one 5-D box holds a whole frame of one head, both column
+    // halves), after reading its own block-table entry: a tile costs one table-load
+    // latency, and the entries of the next tile are read before its ring slot is
+    // waited for.  Copies go out in the order the MMA lane consumes them:
+    // K0 K1 V0 K2 V1 ... K(n-1) V(n-2) V(n-1).
     int ni = 0, kt = 0, qi = 0;
-    const int ncopy = 2 * fpt;  // TMA copies per K (or V) tile
     while (true) {
       int item = 0;
       if (lane == 0) item = *abort_flag ? total : atomicAdd(a.sched, 1);
@@ -369,48 +381,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++qi;
       const int32_t* table = a.block_tables + static_cast<int64_t>(it.s) * a.bt_row;
       const int Lv = a.context_lens[it.s];
-      const int oob_row = a.num_blocks * B;  // any row past the cache: zero fill
-      // cache row of the frame a lane copies in tile j (copy c: frame c >> 1, half c & 1)
-      auto frame_row = [&](int j, int c) -> int {
-        const int lb = j * fpt + (c >> 1);
-        int row = oob_row;
-        if (c < ncopy && lb * B < Lv) {
+      const int oob_group = a.num_blocks * (B / 8);  // any frame past the cache: zero fill
+      // first 8-row group (in the frame map) of the frame lane f copies in tile j
+      auto frame_group = [&](int j) -> int {
+        const int lb = j * fpt + lane;
+        int g = oob_group;
+        if (lane < fpt && lb * B < Lv) {
           const int fr = __ldg(table + lb);
-          if (fr >= 0 && fr < a.num_blocks) row = fr * B;
-          else if ((c & 1) == 0) atomicOr(a.status, kDevBadBlock);
+          if (fr >= 0 && fr < a.num_blocks) g = fr * (B / 8);
+          else atomicOr(a.status, kDevBadBlock);
         }
-        return row;
+        return g;
       };
-      int row = frame_row(0, lane);
-      for (int j = 0; j < it.nkv; ++j, ++kt) {
-        const int st = kt & 1;
-        const uint32_t ph = (kt >> 1) & 1;
-        // K
+      auto issue = [&](const CUtensorMap* map, uint32_t ring, int empty_bar, int full_bar, int t, int g) -> bool {
+        const int st = t & 1;
+        int w = 1;
         if (lane == 0) {
-          ok = mbar_wait(BAR(BK_EMPTY + st), ph ^ 1, abort_flag, a.status);
-          if (ok) mbar_expect_tx(BAR(BK_FULL + st), kTile);
+          w = mbar_wait(BAR(empty_bar + st), ((t >> 1) & 1) ^ 1, abort_flag, a.status);
+          if (w) mbar_expect_tx(BAR(full_bar + st), kTile);
         }
-        ok = __shfl_sync(kFull, ok, 0);
-        if (!ok) break;
-        for (int c = lane; c < ncopy; c += 32) {
-          const int r = c < 32 ? row : frame_row(j, c);
-          tma_load_3d(sb + kSmK + st * kTile + (c >> 1) * B * 128 + (c & 1) * kHalf, &tmap_k, (c & 1) * 64, it.h,
-                      r, BAR(BK_FULL + st));
-        }
-        // V
-        if (lane == 0) {
-          ok = mbar_wait(BAR(BV_EMPTY + st), ph ^ 1, abort_flag, a.status);
-          if (ok) mbar_expect_tx(BAR(BV_FULL + st), kTile);
-        }
-        ok = __shfl_sync(kFull, ok, 0);
-        if (!ok) break;
-        for (int c = lane; c < ncopy; c += 32) {
-          const int r = c < 32 ? row : frame_row(j, c);
-          tma_load_3d(sb + kSmV + st * kTile + (c >> 1) * B * 128 + (c & 1) * kHalf, &tmap_v, (c & 1) * 64, it.h,
-                      r, BAR(BV_FULL + st));
-        }
-        if (j + 1 < it.nkv) row = frame_row(j + 1, lane);
+        w = __shfl_sync(kFull, w, 0);
+        if (!w) return false;
+        if (lane < fpt) tma_load_5d(sb + ring + st * kTile + lane * B * 256, map, g, it.h, BAR(full_bar + st));
+        return true;
+      };
+      int gk = frame_group(0), gv = 0;
+      for (int j = 0; j <= it.nkv && ok; ++j) {
+        if (j < it.nkv) ok = issue(&tmap_k, kSmK, BK_EMPTY, BK_FULL, kt + j, gk);
+        if (ok && j >= 1) ok = issue(&tmap_v, kSmV, BV_EMPTY, BV_FULL, kt + j - 1, gv);
+        gv = gk;
+        if (j + 1 < it.nkv) gk = frame_group(j + 1);
       }
+      kt += it.nkv;
       if (!ok) break;
     }
     if (lane == 0) {
@@ -444,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int ks = 0; ks < kBN / 16; ++ks) {
         const uint64_t ad = sdesc(sb + kSmP + st * kTile + (ks >> 2) * kHalf + (ks & 3) * 32, 0, 1024);
-        const uint64_t bd = sdesc(sb + kSmV + st * kTile + ks * 16 * 128, kHalf, 1024);
+        const uint64_t bd = sdesc(sb + kSmV + st * kTile + ks * 2 * 2048, 1024, 2048);
         mma(o_tmem, ad, bd, id_pv, (!first || ks > 0) ? 1u : 0u);
       }
       commit(BAR(BV_EMPTY + st));
@@ -475,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < kD / 16; ++ks) {
             const uint64_t ad = sdesc(sb + kSmQ + (ks >> 2) * kHalf + (ks & 3) * 32, 0, 1024);
-            const uint64_t bd = sdesc(sb + kSmK + st * kTile + (ks >> 2) * kHalf + (ks & 3) * 32, 0, 1024);
+            const uint64_t bd = sdesc(sb + kSmK + st * kTile + (ks >> 2) * 1024 + (ks & 3) * 32, 0, 2048);
             mma(d, ad, bd, id_qk, ks > 0 ? 1u : 0u);
           }
           commit(BAR(BS_FULL + st));
