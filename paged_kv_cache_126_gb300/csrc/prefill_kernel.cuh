@@ -10,23 +10,23 @@
 // Inference", "The Mathematics of Block Translation").
 //
 // Design (one thread block per SM, persistent, dynamic work counter):
-//   * Work item = (sequence, head, tile of 128 queries); later (longer) query
-//     tiles of a sequence first.  K/V are walked in tiles of 128 keys, each
-//     assembled from 128/B frames, one TMA copy per frame through a 5-D view of the
-//     cache that lands the frame as [B/8 row groups][2 column halves][8 rows][64]
-//     (128-byte swizzle; the MMA descriptors stride 2048 bytes per 8 keys); frames
-//     past the sequence end are read at an out-of-range group, i.e. zero-filled.
-//     The Q tile is [2 halves][128 rows][64] (two 3-D copies).
-//   * warp 0: TMA producer -- Q tile, then K and V tiles into two-stage rings; the
-//     frame copies of a tile are issued by the warp's lanes in parallel.  warp 1 (one lane): tcgen05.mma issuer -- S = Q K^T into one of two
-//     128-column TMEM buffers, then O_j = P_j V_j into one of two more (fp32
-//     accumulators, M = N = 128, K = 16 per instruction); Q K^T of tile j+1 is
-//     issued before P V of tile j so the tensor cores work while the softmax runs.
-//     warps 4..7 (128 threads, thread = query row, TMEM lane = row): load S,
-//     apply the causal mask, online softmax in log2 units (ex2.approx, fp32), write
-//     P (operand type) to shared memory in the 128-byte-swizzled K-major layout the
-//     MMA reads, and fold each O_j into an fp32 row accumulator in registers with
-//     the usual rescaling.  Normalised rows are written to `out`.
+//   * Work item = (sequence, head, pair of consecutive 128-query tiles); later
+//     (longer) pairs of a sequence first.  Both tiles of a pair share every K/V
+//     tile, which halves the copies and the L2 traffic per FLOP.  K/V are walked in
+//     tiles of 128 keys, each assembled from 128/B frames, one TMA copy per frame
+//     through a 5-D view of the cache that lands the frame as [B/8 row groups]
+//     [2 column halves][8 rows][64] (128-byte swizzle; the MMA descriptors stride
+//     2048 bytes per 8 keys); frames past the sequence end are read at an
+//     out-of-range group, i.e. zero-filled.  Q tiles are [2 halves][128 rows][64].
+//   * warp 0: TMA producer (Q tiles, then K_t, V_t into two-stage rings; the frame
+//     copies of a tile are issued by the warp's lanes).  warp 1 (one lane):
+//     tcgen05.mma issuer, fp32 accumulators in TMEM (512 columns: S_0 S_1 O_0 O_1).
+//     S_q = Q_q K_t^T from shared memory; O_q (+)= P_q V_t with P_q read from TMEM,
+//     where the softmax left it over the first 64 columns of S_q.
+//     warps 2-5 / 6-9: softmax of slot 0 / 1 (thread = query row = TMEM lane):
+//     causal mask, online softmax in log2 units (ex2.approx, fp32) with a lazily
+//     raised reference max, P (operand type) back to TMEM, O rescaled in TMEM when
+//     the reference max moves; normalised rows are written to `out`.
 //   * Every wait is a bounded mbarrier wait; one that gives up sets PA_DEV_TIMEOUT
 //     and makes the block's later waits no-ops; before the TMEM is freed the MMA
 //     lane waits (bounded) for its own MMAs and the producer for its copies.
@@ -51,29 +51,32 @@ constexpr long long kDrainCycles = 200000000LL;
 constexpr int kD = 128;           // head_dim
 constexpr int kBM = 128;          // queries per tile
 constexpr int kBN = 128;          // keys per tile
-constexpr int kThreads = 256;     // 8 warps
+constexpr int kThreads = 320;     // 10 warps
+constexpr int kSmxWarp0 = 2;      // softmax group q: warps 2 + 4q .. 5 + 4q
 constexpr uint32_t kTile = 32768; // bytes of one 128 x 128 16-bit tile
-constexpr uint32_t kHalf = 16384; // one 64-column half of a tile
+constexpr uint32_t kHalf = 16384; // one 64-column half of a Q tile
 
 // shared-memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t kSmQ = 0;
-constexpr uint32_t kSmK = kSmQ + kTile;           // 2 stages
-constexpr uint32_t kSmV = kSmK + 2 * kTile;       // 2 stages
-constexpr uint32_t kSmP = kSmV + 2 * kTile;       // 2 buffers
-constexpr uint32_t kSmBar = kSmP + 2 * kTile;     // mbarriers
-constexpr uint32_t kSmMisc = kSmBar + 32 * 8;     // flags, TMEM address, item ring
-constexpr uint32_t kSmOff = kSmMisc + 64;         // per-sequence item offsets [S + 1]
+constexpr uint32_t kSmQ = 0;                  // [2 slots] Q tiles: [2 halves][128 rows][64]
+constexpr uint32_t kSmK = kSmQ + 2 * kTile;   // [2 stages] K tiles: [16 groups][2 halves][8 rows][64]
+constexpr uint32_t kSmV = kSmK + 2 * kTile;   // [2 stages] V tiles, same layout
+constexpr uint32_t kSmBar = kSmV + 2 * kTile; // mbarriers
+constexpr uint32_t kSmMisc = kSmBar + 32 * 8; // flags, TMEM address, item ring
+constexpr uint32_t kSmOff = kSmMisc + 64;     // per-sequence item offsets [S + 1]
 __host__ __device__ constexpr uint32_t smem_bytes(int S) { return kSmOff + 4u * (S + 1) + 1024u; }
+
+// TMEM (512 columns): S_q at column 128 q, O_q at 256 + 128 q (fp32, lane = query row);
+// P_q (16-bit, two per column) overwrites the first 64 columns of S_q.
+constexpr uint32_t kTmemS = 0, kTmemO = 256;
 
 // mbarrier indices
 enum : int {
   BQ_FULL = 0, BQ_EMPTY = 1,
-  BK_FULL = 2, BK_EMPTY = 4, BV_FULL = 6, BV_EMPTY = 8,   // [2] each
-  BS_FULL = 10, BS_EMPTY = 12, BO_FULL = 14, BO_EMPTY = 16,  // [2] each
-  BP_FULL = 18, BP_EMPTY = 20,                             // [2] each
-  BI_FULL = 22, BI_EMPTY = 24,                             // item ring [2]
-  BDRAIN = 26,
-  NBARS = 27
+  BK_FULL = 2, BK_EMPTY = 4, BV_FULL = 6, BV_EMPTY = 8,  // [2 stages] each
+  BS_FULL = 10, BP_FULL = 12, BO_FULL = 14,              // [2 slots] each
+  BI_FULL = 16, BI_EMPTY = 18,                           // item ring [2]
+  BDRAIN = 20,
+  NBARS = 21
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -156,37 +159,25 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uin
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(id), "r"(acc));
 }
+// A operand from TMEM (M = 128 lanes, 16-bit elements two per column), B from shared memory.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
 __device__ __forceinline__ void commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
 }
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // tcgen05.ld of 32 columns without waiting; pair with tmem_wait_ld() and tie32().
 __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -243,32 +234,49 @@ __device__ __forceinline__ int upper_seq(const int32_t* off, int S, int x) {
   return lo;
 }
 
+// A work item is a pair of consecutive 128-query tiles of one (sequence, head):
+// slot 1 holds the later tile, slot 0 the one before it (absent when the chunk has
+// an odd tile count and this is its first pair).  Both share every K/V tile.
 struct PItem {
   int s, h;
-  int qrow0;    // first q row of the tile (global row index)
-  int nrows;    // valid rows in the tile
-  int pos0;     // position of the tile's first row
-  int nkv;      // key tiles to visit
-  bool bad;
+  int nkv;       // key tiles the item walks (those of slot 1)
+  int qrow0[2];  // first q row of the slot's tile (global row index)
+  int nrows[2];  // valid rows of the slot's tile, 0 when the slot is unused
+  int pos0[2];   // position of the slot's first row
+  int nkv_q[2];  // key tiles the slot visits, 0 when unused
 };
+
+__device__ __forceinline__ bool seq_bad(int n, int L, const PrefillArgs& a) {
+  return n < 0 || L < n || static_cast<int64_t>(L) > static_cast<int64_t>(a.max_blocks) * a.B;
+}
 
 __device__ __forceinline__ PItem locate(const PrefillArgs& a, const int32_t* off, int item) {
   PItem it;
   it.s = upper_seq(off, a.S, item);
   const int local = item - off[it.s];
-  const int qt_rev = local / a.H;
-  it.h = local - qt_rev * a.H;
+  const int pr = local / a.H;  // pair index, counted from the end of the chunk
+  it.h = local - pr * a.H;
   const int qs = a.query_start[it.s], qe = a.query_start[it.s + 1];
   const int n = qe - qs;
   const int L = a.context_lens[it.s];
-  it.bad = n < 0 || L < n || static_cast<int64_t>(L) > static_cast<int64_t>(a.max_blocks) * a.B;
+  const bool bad = seq_bad(n, L, a);
   const int ntiles = n > 0 ? (n + kBM - 1) / kBM : 0;
-  const int qt = ntiles - 1 - qt_rev;  // later tiles first
-  it.qrow0 = qs + qt * kBM;
-  it.nrows = it.bad ? 0 : min(kBM, n - qt * kBM);
-  it.pos0 = L - n + qt * kBM;
-  const int pos_last = it.pos0 + it.nrows - 1;
-  it.nkv = it.nrows > 0 ? (pos_last + kBN) / kBN : 0;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int qt = ntiles - 1 - 2 * pr - (1 - q);
+    if (bad || qt < 0) {
+      it.qrow0[q] = qs;
+      it.nrows[q] = 0;
+      it.pos0[q] = 0;
+      it.nkv_q[q] = 0;
+    } else {
+      it.qrow0[q] = qs + qt * kBM;
+      it.nrows[q] = min(kBM, n - qt * kBM);
+      it.pos0[q] = L - n + qt * kBM;
+      it.nkv_q[q] = (it.pos0[q] + it.nrows[q] - 1 + kBN) / kBN;
+    }
+  }
+  it.nkv = it.nkv_q[1];
   return it;
 }
 
@@ -293,17 +301,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < NBARS; ++i) {
       uint32_t cnt = 1;
-      if (i == BS_EMPTY || i == BS_EMPTY + 1 || i == BO_EMPTY || i == BO_EMPTY + 1 || i == BP_FULL ||
-          i == BP_FULL + 1)
-        cnt = 4;
-      if (i == BI_EMPTY || i == BI_EMPTY + 1) cnt = 5;  // MMA warp + 4 softmax warps
+      if (i == BP_FULL || i == BP_FULL + 1) cnt = 4;        // the slot's four softmax warps
+      if (i == BI_EMPTY || i == BI_EMPTY + 1) cnt = 9;      // MMA warp + eight softmax warps
       mbar_init(BAR(i), cnt);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == 2) {  // TMEM: S0 S1 O0 O1, 128 columns each
+  if (warp == 1) {  // TMEM: S0 S1 O0 O1, 128 columns each
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
@@ -312,13 +318,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
   }
-  // per-sequence item counts and their prefix
+  // per-sequence item counts (tile pairs x heads) and their prefix
   for (int s = tid; s < a.S; s += blockDim.x) {
     const int n = a.query_start[s + 1] - a.query_start[s];
     const int L = a.context_lens[s];
-    const bool bad = n < 0 || L < n || static_cast<int64_t>(L) > static_cast<int64_t>(a.max_blocks) * B;
+    const bool bad = seq_bad(n, L, a);
     if (bad && blockIdx.x == 0) atomicOr(a.status, kDevBadLen);
-    off[s + 1] = bad || n <= 0 ? 0 : ((n + kBM - 1) / kBM) * a.H;
+    const int ntiles = n > 0 ? (n + kBM - 1) / kBM : 0;
+    off[s + 1] = bad ? 0 : ((ntiles + 1) / 2) * a.H;
   }
   if (tid == 0) off[0] = 0;
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -349,8 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // f of a key tile (one 5-D box holds a whole frame of one head, both column
     // halves), after reading its own block-table entry: a tile costs one table-load
     // latency, and the entries of the next tile are read before its ring slot is
-    // waited for.  Copies go out in the order the MMA lane consumes them:
-    // K0 K1 V0 K2 V1 ... K(n-1) V(n-2) V(n-1).
+    // waited for.
     int ni = 0, kt = 0, qi = 0;
     while (true) {
       int item = 0;
@@ -366,14 +372,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (done) break;
       const PItem it = locate(a, off, item);
       if (it.nkv == 0) continue;
-      // Q tile (two 64-column halves)
+      // Q tiles of the used slots (two 64-column halves each)
       int ok = 1;
       if (lane == 0) {
         ok = mbar_wait(BAR(BQ_EMPTY), (qi & 1) ^ 1, abort_flag, a.status);
         if (ok) {
-          mbar_expect_tx(BAR(BQ_FULL), kTile);
-          tma_load_3d(sb + kSmQ, &tmap_q, 0, it.h, it.qrow0, BAR(BQ_FULL));
-          tma_load_3d(sb + kSmQ + kHalf, &tmap_q, 64, it.h, it.qrow0, BAR(BQ_FULL));
+          mbar_expect_tx(BAR(BQ_FULL), kTile * ((it.nrows[0] > 0) + (it.nrows[1] > 0)));
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            if (it.nrows[q] > 0) {
+              tma_load_3d(sb + kSmQ + q * kTile, &tmap_q, 0, it.h, it.qrow0[q], BAR(BQ_FULL));
+              tma_load_3d(sb + kSmQ + q * kTile + kHalf, &tmap_q, 64, it.h, it.qrow0[q], BAR(BQ_FULL));
+            }
+          }
         }
       }
       ok = __shfl_sync(kFull, ok, 0);
@@ -382,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t* table = a.block_tables + static_cast<int64_t>(it.s) * a.bt_row;
       const int Lv = a.context_lens[it.s];
       const int oob_group = a.num_blocks * (B / 8);  // any frame past the cache: zero fill
-      // first 8-row group (in the frame map) of the frame lane f copies in tile j
+      // first 8-row group (in the frame view) of the frame lane f copies in tile j
       auto frame_group = [&](int j) -> int {
         const int lb = j * fpt + lane;
         int g = oob_group;
@@ -405,12 +416,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < fpt) tma_load_5d(sb + ring + st * kTile + lane * B * 256, map, g, it.h, BAR(full_bar + st));
         return true;
       };
-      int gk = frame_group(0), gv = 0;
-      for (int j = 0; j <= it.nkv && ok; ++j) {
-        if (j < it.nkv) ok = issue(&tmap_k, kSmK, BK_EMPTY, BK_FULL, kt + j, gk);
-        if (ok && j >= 1) ok = issue(&tmap_v, kSmV, BV_EMPTY, BV_FULL, kt + j - 1, gv);
-        gv = gk;
-        if (j + 1 < it.nkv) gk = frame_group(j + 1);
+      int g = frame_group(0);
+      for (int j = 0; j < it.nkv && ok; ++j) {
+        ok = issue(&tmap_k, kSmK, BK_EMPTY, BK_FULL, kt + j, g);
+        if (ok) ok = issue(&tmap_v, kSmV, BV_EMPTY, BV_FULL, kt + j, g);
+        if (j + 1 < it.nkv) g = frame_group(j + 1);
       }
       kt += it.nkv;
       if (!ok) break;
@@ -430,28 +440,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ====================================== MMA issuer ======================================
-    // S_t = Q K_t^T into TMEM buffer t%2; O (+)= P_t V_t into one O buffer that
-    // accumulates over the item's key tiles (the first tile overwrites it).
-    int ni = 0, kt = 0, qi = 0, oi = 0;
+    // Per key tile t of an item:  S_0 = Q_0 K_t^T, S_1 = Q_1 K_t^T, then for each slot
+    // in turn O_q (+)= P_q V_t followed by S_q = Q_q K_{t+1}^T, so that one slot's
+    // products run while the other slot's softmax works.  P_q lives in S_q's columns:
+    // the next S_q is issued after the P V that reads it (the tensor core keeps issue
+    // order), and the commit that publishes S_q also covers that P V, so the softmax
+    // may rescale O_q once it sees S_q.
+    int ni = 0, kt = 0, qi = 0;
+    uint32_t pc0 = 0, pc1 = 0;  // P V products issued per slot (P_FULL phases)
     const uint32_t id_qk = idesc<T>(false);
     const uint32_t id_pv = idesc<T>(true);
-    const uint32_t o_tmem = tmem + 256;
-    auto pv = [&](int t, bool first) -> bool {
+    auto qk = [&](int q, int t) {
       const int st = t & 1;
-      const uint32_t ph = (t >> 1) & 1;
-      if (!mbar_wait(BAR(BP_FULL + st), ph, abort_flag, a.status)) return false;
-      if (!mbar_wait(BAR(BV_FULL + st), ph, abort_flag, a.status)) return false;
-      if (first && !mbar_wait(BAR(BO_EMPTY), (oi & 1) ^ 1, abort_flag, a.status)) return false;
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+      for (int ks = 0; ks < kD / 16; ++ks) {
+        const uint64_t ad = sdesc(sb + kSmQ + q * kTile + (ks >> 2) * kHalf + (ks & 3) * 32, 0, 1024);
+        const uint64_t bd = sdesc(sb + kSmK + st * kTile + (ks >> 2) * 1024 + (ks & 3) * 32, 0, 2048);
+        mma(tmem + kTmemS + q * 128, ad, bd, id_qk, ks > 0 ? 1u : 0u);
+      }
+      commit(BAR(BS_FULL + q));
+    };
+    auto pv = [&](int q, int t, bool first) {
+      const int st = t & 1;
 #pragma unroll
       for (int ks = 0; ks < kBN / 16; ++ks) {
-        const uint64_t ad = sdesc(sb + kSmP + st * kTile + (ks >> 2) * kHalf + (ks & 3) * 32, 0, 1024);
         const uint64_t bd = sdesc(sb + kSmV + st * kTile + ks * 2 * 2048, 1024, 2048);
-        mma(o_tmem, ad, bd, id_pv, (!first || ks > 0) ? 1u : 0u);
+        mma_ts(tmem + kTmemO + q * 128, tmem + kTmemS + q * 128 + ks * 8, bd, id_pv, (!first || ks > 0) ? 1u : 0u);
       }
-      commit(BAR(BV_EMPTY + st));
-      commit(BAR(BP_EMPTY + st));  // P buffer free again; O holds the tiles so far
-      return true;
+    };
+    auto wait = [&](int bar, uint32_t parity) -> bool {
+      const bool w = mbar_wait(BAR(bar), parity, abort_flag, a.status);
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      return w;
     };
     if (lane == 0) {
       while (true) {
@@ -463,32 +483,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (item < 0) break;
         const PItem it = locate(a, off, item);
         if (it.nkv == 0) continue;
-        if (!mbar_wait(BAR(BQ_FULL), qi & 1, abort_flag, a.status)) break;
+        const int n0 = it.nkv_q[0], n1 = it.nkv_q[1];
+        bool ok = wait(BQ_FULL, qi & 1);
         ++qi;
-        bool ok = true;
-        for (int j = 0; j < it.nkv && ok; ++j) {
-          const int t = kt + j;
-          const int st = t & 1;
-          const uint32_t ph = (t >> 1) & 1;
-          if (!mbar_wait(BAR(BK_FULL + st), ph, abort_flag, a.status)) { ok = false; break; }
-          if (!mbar_wait(BAR(BS_EMPTY + st), ph ^ 1, abort_flag, a.status)) { ok = false; break; }
-          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          const uint32_t d = tmem + st * 128;
-#pragma unroll
-          for (int ks = 0; ks < kD / 16; ++ks) {
-            const uint64_t ad = sdesc(sb + kSmQ + (ks >> 2) * kHalf + (ks & 3) * 32, 0, 1024);
-            const uint64_t bd = sdesc(sb + kSmK + st * kTile + (ks >> 2) * 1024 + (ks & 3) * 32, 0, 2048);
-            mma(d, ad, bd, id_qk, ks > 0 ? 1u : 0u);
-          }
-          commit(BAR(BS_FULL + st));
-          commit(BAR(BK_EMPTY + st));
-          if (j == it.nkv - 1) commit(BAR(BQ_EMPTY));
-          if (j >= 1) ok = pv(t - 1, j == 1);
+        ok = ok && wait(BK_FULL + (kt & 1), (kt >> 1) & 1);
+        if (ok) {
+          if (n0 > 0) qk(0, kt);
+          qk(1, kt);
+          commit(BAR(BK_EMPTY + (kt & 1)));
+          if (n1 == 1) commit(BAR(BQ_EMPTY));
         }
-        if (ok) ok = pv(kt + it.nkv - 1, it.nkv == 1);
-        if (ok) commit(BAR(BO_FULL));  // O final for this item
-        ++oi;
-        kt += it.nkv;
+        for (int j = 0; j < n1 && ok; ++j) {
+          const int t = kt + j;
+          bool have_v = false, have_k = false;
+          if (j < n0) {
+            ok = wait(BP_FULL + 0, pc0 & 1) && wait(BV_FULL + (t & 1), (t >> 1) & 1);
+            if (!ok) break;
+            have_v = true;
+            pv(0, t, j == 0);
+            ++pc0;
+            if (j == n0 - 1) commit(BAR(BO_FULL + 0));
+            if (j + 1 < n0) {
+              ok = wait(BK_FULL + ((t + 1) & 1), ((t + 1) >> 1) & 1);
+              if (!ok) break;
+              have_k = true;
+              qk(0, t + 1);
+            }
+          }
+          ok = wait(BP_FULL + 1, pc1 & 1) && (have_v || wait(BV_FULL + (t & 1), (t >> 1) & 1));
+          if (!ok) break;
+          pv(1, t, j == 0);
+          ++pc1;
+          commit(BAR(BV_EMPTY + (t & 1)));
+          if (j == n1 - 1) commit(BAR(BO_FULL + 1));
+          if (j + 1 < n1) {
+            ok = have_k || wait(BK_FULL + ((t + 1) & 1), ((t + 1) >> 1) & 1);
+            if (!ok) break;
+            qk(1, t + 1);
+            commit(BAR(BK_EMPTY + ((t + 1) & 1)));
+            if (j + 1 == n1 - 1) commit(BAR(BQ_EMPTY));
+          }
+        }
+        kt += n1;
         if (!ok) break;
       }
       // all MMAs of this lane complete before the TMEM can be freed
@@ -497,17 +533,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (!mbar_try(BAR(BDRAIN), 0) && clock64() - t0 < kDrainCycles) {
       }
     }
-  } else if (warp >= 4) {
+  } else {
     // ====================================== softmax / epilogue ======================================
-    // Thread = query row = TMEM lane.  The whole S row lives in registers; weights
-    // use a reference max m_ref that is raised (and O, l rescaled) only when the
-    // row max exceeds it by more than 8 (log2 units), so weights stay <= 2^8.
-    const int q4 = warp - 4;          // TMEM lane quadrant
-    const int row = q4 * 32 + lane;   // query row in the tile
-    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t o_tmem = tmem + lane_base + 256;
+    // Group q (four warps) owns slot q.  Thread = query row = TMEM lane.  The S row
+    // is held in registers; weights use a reference max m_ref that is raised (and
+    // O, l rescaled) only when the row max exceeds it by more than 8 (log2 units),
+    // so weights stay <= 2^8.  P goes back to TMEM over the S columns.
+    const int q = (warp - kSmxWarp0) >> 2;
+    const int quad = warp & 3;        // TMEM lane quadrant a warp may access
+    const int row = quad * 32 + lane; // query row in the tile
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t s_tmem = tmem + lane_base + kTmemS + q * 128;
+    const uint32_t o_tmem = tmem + lane_base + kTmemO + q * 128;
     const float sl2 = a.qk_scale_log2;
-    int ni = 0, kt = 0, oi = 0;
+    int ni = 0;
+    uint32_t sc = 0, oc = 0;  // S_FULL and O_FULL phases of this slot
+    auto wait_all = [&](int bar, uint32_t parity) -> bool {
+      const bool w = __all_sync(kFull, mbar_wait(BAR(bar), parity, abort_flag, a.status));
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      return w;
+    };
     while (true) {
       const int sl = ni & 1;
       int item = -1;
@@ -518,40 +563,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++ni;
       if (item < 0) break;
       const PItem it = locate(a, off, item);
-      const bool valid = row < it.nrows;
+      const int nk = q ? it.nkv_q[1] : it.nkv_q[0];
+      if (nk == 0) continue;
+      const int pos0 = q ? it.pos0[1] : it.pos0[0];
+      const int qrow0 = q ? it.qrow0[1] : it.qrow0[0];
+      const bool valid = row < (q ? it.nrows[1] : it.nrows[0]);
       // rows past the chunk end attend everything they are shown (not stored)
-      const int pos = valid ? it.pos0 + row : 0x3fffffff;
+      const int pos = valid ? pos0 + row : 0x3fffffff;
       float m_ref = -INFINITY, l = 0.f;
       bool ok = true;
-      for (int j = 0; j < it.nkv && ok; ++j) {
-        const int t = kt + j;
-        const int st = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
-        if (!__all_sync(kFull, mbar_wait(BAR(BS_FULL + st), ph, abort_flag, a.status))) { ok = false; break; }
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        uint32_t sr[4][32];
-        const uint32_t s_addr = tmem + lane_base + st * 128;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32_async(s_addr + c * 32, sr[c]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tie32(sr[c]);
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(BS_EMPTY + st));
+      for (int j = 0; j < nk; ++j) {
+        if (!wait_all(BS_FULL + q, sc & 1)) { ok = false; break; }
+        ++sc;
+        // two passes over S in TMEM (row max, then weights), 64 columns in flight
         const int key0 = j * kBN;
-        if (key0 + kBN - 1 > it.pos0) {  // the tile reaches past some row's position
+        const bool diag = key0 + kBN - 1 > pos0;  // the tile reaches past some row's position
+        auto load_half = [&](int hf, uint32_t (&sr)[2][32]) {
+          tmem_ld32_async(s_tmem + hf * 64, sr[0]);
+          tmem_ld32_async(s_tmem + hf * 64 + 32, sr[1]);
+          tmem_wait_ld();
+          tie32(sr[0]);
+          tie32(sr[1]);
+          if (diag) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 2; ++c)
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (key0 + c * 32 + i > pos) sr[c][i] = __float_as_uint(-INFINITY);
+              for (int i = 0; i < 32; ++i)
+                if (key0 + hf * 64 + c * 32 + i > pos) sr[c][i] = __float_as_uint(-INFINITY);
+          }
+        };
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t sr[2][32];
+          load_half(hf, sr);
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sr[c][i]));
         }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         const float m_new = fmaxf(m_ref, mx * sl2);
         const bool raise = m_new > m_ref + 8.f;
         const float alpha = raise ? ex2(m_ref - m_new) : 1.f;
@@ -560,14 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = m_new;
         }
         if (j > 0 && __any_sync(kFull, raise)) {
-          // rescale this warp's rows of O in TMEM (lanes that did not raise scale by 1)
-          // once the previous tile's P V has landed in O
-          const int tp = t - 1;
-          if (!__all_sync(kFull, mbar_wait(BAR(BP_EMPTY + (tp & 1)), (tp >> 1) & 1, abort_flag, a.status))) {
-            ok = false;
-            break;
-          }
-          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          // O_q already holds the previous tiles (the S commit covered their P V);
+          // lanes that did not raise scale by 1
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t r[32];
@@ -578,45 +623,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
             tmem_st32(o_tmem + c * 32, r);
           }
-          tmem_wait_st();
         }
-        // this P buffer was last read by the P V of tile t-2
-        if (!__all_sync(kFull, mbar_wait(BAR(BP_EMPTY + st), ph ^ 1, abort_flag, a.status))) { ok = false; break; }
-        // weights, row sum, P row into shared memory (K-major, 128-byte swizzle)
-        float sum = 0.f;
-        unsigned char* prow = smem + kSmP + st * kTile;
+        // weights, row sum, P row (16-bit, keys 2i and 2i+1 in column i) over S: the
+        // P of keys 64h .. 64h+63 lands in columns 32h .. 32h+31, which pass h has read
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
         const float nm = -m_ref;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t sr[2][32];
+          load_half(hf, sr);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t w[4];
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pw[16];
 #pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-              const float p0 = ex2(fmaf(__uint_as_float(sr[c][q * 8 + i]), sl2, nm));
-              const float p1 = ex2(fmaf(__uint_as_float(sr[c][q * 8 + i + 1]), sl2, nm));
-              sum += p0 + p1;
-              w[i >> 1] = pack2<T>(p0, p1);
+            for (int i = 0; i < 32; i += 2) {
+              const float p0 = ex2(fmaf(__uint_as_float(sr[c][i]), sl2, nm));
+              const float p1 = ex2(fmaf(__uint_as_float(sr[c][i + 1]), sl2, nm));
+              sum4[(i >> 1) & 3] += p0 + p1;
+              pw[i >> 1] = pack2<T>(p0, p1);
             }
-            // keys c*32 + 8q .. +7 -> half (c >> 1), 16-byte chunk (c & 1) * 4 + q
-            const int chunk = ((c & 1) * 4 + q) ^ (row & 7);
-            *reinterpret_cast<uint4*>(prow + (c >> 1) * kHalf + row * 128 + chunk * 16) =
-                make_uint4(w[0], w[1], w[2], w[3]);
+            tmem_st16(s_tmem + hf * 32 + c * 16, pw);
           }
         }
-        l += sum;
+        l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+        tmem_wait_st();
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(BP_FULL + st));
+        if (lane == 0) mbar_arrive(BAR(BP_FULL + q));
       }
-      kt += it.nkv;
-      // epilogue: wait for the item's last P V, normalise, store
-      if (ok && it.nkv > 0 && !__all_sync(kFull, mbar_wait(BAR(BO_FULL), oi & 1, abort_flag, a.status))) ok = false;
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const bool zero = !ok || it.bad || !(l > 0.f);
+      // epilogue: wait for the slot's last P V, normalise, store
+      if (ok && !wait_all(BO_FULL + q, oc & 1)) ok = false;
+      ++oc;
+      const bool zero = !ok || !(l > 0.f);
       const float inv = zero ? 0.f : 1.f / l;
-      T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(it.qrow0 + row) * a.out_row +
+      T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(qrow0 + row) * a.out_row +
               static_cast<int64_t>(it.h) * kD;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -638,16 +678,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(BO_EMPTY));
-      ++oi;
       if (!ok) break;
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
 }
 
 template <typename T>

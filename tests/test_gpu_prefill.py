@@ -45,6 +45,8 @@ def test_small_prefill_batch(pa):
     ([0], [1]), ([0], [127]), ([0], [128]), ([0], [129]), ([0], [300]),
     ([5], [1]), ([100], [1]), ([127], [1]), ([128], [1]), ([1000], [64]),
     ([0, 17, 256, 900], [513, 1, 128, 77]),
+    # tile pairs: both tiles ending in the same key tile, odd tile counts, ragged tails
+    ([5], [129]), ([0], [384]), ([60], [640]), ([200], [255]),
 ])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_chunks_and_prefixes(pa, prefix, chunk, dtype):
