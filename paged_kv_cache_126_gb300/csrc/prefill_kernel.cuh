@@ -189,6 +189,19 @@ __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tie16(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]));
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 // Empty statement that claims to rewrite the registers: every later use depends on it,
 // and it is ordered after the (volatile) wait that precedes it.
@@ -223,6 +236,20 @@ template <>
 __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Two packed 16-bit weights times a factor, rounded back to the operand type.
+template <typename T>
+__device__ __forceinline__ uint32_t scale2(uint32_t packed, float f);
+template <>
+__device__ __forceinline__ uint32_t scale2<__half>(uint32_t packed, float f) {
+  const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&packed));
+  return pack2<__half>(v.x * f, v.y * f);
+}
+template <>
+__device__ __forceinline__ uint32_t scale2<__nv_bfloat16>(uint32_t packed, float f) {
+  const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&packed));
+  return pack2<__nv_bfloat16>(v.x * f, v.y * f);
 }
 
 __device__ __forceinline__ int upper_seq(const int32_t* off, int S, int x) {
@@ -575,44 +602,82 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nk; ++j) {
         if (!wait_all(BS_FULL + q, sc & 1)) { ok = false; break; }
         ++sc;
-        // two passes over S in TMEM (row max, then weights), 64 columns in flight
+        // Keys of this tile a row may see: 0 .. nvalid-1.  Rows of a warp are
+        // consecutive positions, so a 32-key chunk is (warp-uniformly) fully visible,
+        // fully masked (weight 0, not loaded) or split by the diagonal (masked per
+        // key); masked chunks only follow unmasked ones.
         const int key0 = j * kBN;
-        const bool diag = key0 + kBN - 1 > pos0;  // the tile reaches past some row's position
-        auto load_half = [&](int hf, uint32_t (&sr)[2][32]) {
-          tmem_ld32_async(s_tmem + hf * 64, sr[0]);
-          tmem_ld32_async(s_tmem + hf * 64 + 32, sr[1]);
-          tmem_wait_ld();
-          tie32(sr[0]);
-          tie32(sr[1]);
-          if (diag) {
+        const int nvalid = max(0, min(kBN, pos - key0 + 1));
+        const int wmin = __reduce_min_sync(kFull, nvalid), wmax = __reduce_max_sync(kFull, nvalid);
+        // One pass over the chunks of S, the next chunk's load in flight while one is
+        // processed.  A chunk's weights use the current reference max; when a chunk
+        // raises it (row max above the reference by more than 8), the weights already
+        // stored for this tile, the row sum and (at the end) O are scaled down.  The P
+        // of chunk c lands in columns 16c .. 16c+15, i.e. over S of chunk c/2, which
+        // has been read by then.
+        float o_scale = 1.f;
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t sr[2][32];
+        if (wmax > 0) tmem_ld32_async(s_tmem, sr[0]);
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 4; ++c) {
+          uint32_t(&cur)[32] = sr[c & 1];
+          if (wmax <= c * 32) {  // this and every later chunk are masked for the whole warp
+            uint32_t z[16];
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (key0 + hf * 64 + c * 32 + i > pos) sr[c][i] = __float_as_uint(-INFINITY);
+            for (int k = 0; k < 16; ++k) z[k] = 0u;
+            tmem_st16(s_tmem + c * 16, z);
+            continue;
           }
-        };
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          tmem_wait_ld();
+          tie32(cur);
+          if (c < 3 && wmax > (c + 1) * 32) tmem_ld32_async(s_tmem + (c + 1) * 32, sr[(c + 1) & 1]);
+          if (wmin < (c + 1) * 32) {
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t sr[2][32];
-          load_half(hf, sr);
+            for (int i = 0; i < 32; ++i)
+              if (c * 32 + i >= nvalid) cur[i] = __float_as_uint(-INFINITY);
+          }
+          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
+          for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(cur[i]));
+          const float m_new = fmaxf(m_ref, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2);
+          const bool raise = m_new > m_ref + 8.f;
+          if (__any_sync(kFull, raise)) {
+            const float alpha = raise ? ex2(m_ref - m_new) : 1.f;
+            l = (l + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]))) * alpha;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sr[c][i]));
+            for (int k = 0; k < 4; ++k) sum4[k] = 0.f;
+            if (raise) m_ref = m_new;
+            o_scale *= alpha;
+            if (c > 0) {  // rescale the weights this tile has stored so far
+              tmem_wait_st();
+#pragma unroll
+              for (int cp = 0; cp < c; ++cp) {
+                uint32_t pr[16];
+                tmem_ld16_async(s_tmem + cp * 16, pr);
+                tmem_wait_ld();
+                tie16(pr);
+                uint32_t w[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) w[k] = scale2<T>(pr[k], alpha);
+                tmem_st16(s_tmem + cp * 16, w);
+              }
+            }
+          }
+          const float nm = -m_ref;
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float p0 = ex2(fmaf(__uint_as_float(cur[i]), sl2, nm));
+            const float p1 = ex2(fmaf(__uint_as_float(cur[i + 1]), sl2, nm));
+            sum4[(i >> 1) & 3] += p0 + p1;
+            w[i >> 1] = pack2<T>(p0, p1);
+          }
+          tmem_st16(s_tmem + c * 16, w);
         }
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        const float m_new = fmaxf(m_ref, mx * sl2);
-        const bool raise = m_new > m_ref + 8.f;
-        const float alpha = raise ? ex2(m_ref - m_new) : 1.f;
-        if (raise) {
-          l *= alpha;
-          m_ref = m_new;
-        }
-        if (j > 0 && __any_sync(kFull, raise)) {
+        if (j > 0 && __any_sync(kFull, o_scale != 1.f)) {
           // O_q already holds the previous tiles (the S commit covered their P V);
-          // lanes that did not raise scale by 1
+          // rows that did not raise scale by 1
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t r[32];
@@ -620,29 +685,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
             tie32(r);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * o_scale);
             tmem_st32(o_tmem + c * 32, r);
-          }
-        }
-        // weights, row sum, P row (16-bit, keys 2i and 2i+1 in column i) over S: the
-        // P of keys 64h .. 64h+63 lands in columns 32h .. 32h+31, which pass h has read
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-        const float nm = -m_ref;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t sr[2][32];
-          load_half(hf, sr);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t pw[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float p0 = ex2(fmaf(__uint_as_float(sr[c][i]), sl2, nm));
-              const float p1 = ex2(fmaf(__uint_as_float(sr[c][i + 1]), sl2, nm));
-              sum4[(i >> 1) & 3] += p0 + p1;
-              pw[i >> 1] = pack2<T>(p0, p1);
-            }
-            tmem_st16(s_tmem + hf * 32 + c * 16, pw);
           }
         }
         l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);

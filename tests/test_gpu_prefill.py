@@ -86,3 +86,14 @@ def test_prefill_one_query_matches_decode(pa):
     (op,) = w.prefill_ops
     dec = eng.attend(w.ops[op][1], w.query(op), w.scale)
     assert (dec.float() - outs[op].float()).abs().max().item() < 2e-3
+
+
+@pytest.mark.parametrize("sigma,dtype", [(3.0, "f16"), (4.0, "bf16")])
+def test_wide_score_range(pa, sigma, dtype):
+    """Scores with a spread of many log2 units: the running reference max is raised
+    inside tiles (weights already stored for the tile are scaled down) and across
+    tiles (O and the row sum are scaled)."""
+    w = workloads.chunked_prefill([0, 700, 1500], [640, 300, 129], H=2, D=128, B=16, dtype=dtype, sigma=sigma,
+                                  seed=int(sigma * 10))
+    eng, outs, ref = run_both(pa, w)
+    check_prefill(w, outs, ref)
