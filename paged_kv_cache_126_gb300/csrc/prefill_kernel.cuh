@@ -238,6 +238,11 @@ __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// Excess (log2 units) of a row max over the reference at which weights would no
+// longer fit the operand type: fp16 tops out just below 2^16, bf16 near 2^128.
+template <typename T>
+constexpr float kRaiseNow = std::is_same<T, __half>::value ? 15.f : 120.f;
+
 // Two packed 16-bit weights times a factor, rounded back to the operand type.
 template <typename T>
 __device__ __forceinline__ uint32_t scale2(uint32_t packed, float f);
@@ -597,7 +602,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = row < (q ? it.nrows[1] : it.nrows[0]);
       // rows past the chunk end attend everything they are shown (not stored)
       const int pos = valid ? pos0 + row : 0x3fffffff;
-      float m_ref = -INFINITY, l = 0.f;
+      // m_ref: reference max the weights are taken against (O and l are relative to
+      // it); m_run: running row max (log2 units); o_pending: factor O still owes for
+      // a reference raise at the end of the previous tile (applied once that tile's
+      // P V has landed in O).
+      float m_ref = -INFINITY, m_run = -INFINITY, l = 0.f, o_pending = 1.f;
       bool ok = true;
       for (int j = 0; j < nk; ++j) {
         if (!wait_all(BS_FULL + q, sc & 1)) { ok = false; break; }
@@ -610,12 +619,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nvalid = max(0, min(kBN, pos - key0 + 1));
         const int wmin = __reduce_min_sync(kFull, nvalid), wmax = __reduce_max_sync(kFull, nvalid);
         // One pass over the chunks of S, the next chunk's load in flight while one is
-        // processed.  A chunk's weights use the current reference max; when a chunk
-        // raises it (row max above the reference by more than 8), the weights already
-        // stored for this tile, the row sum and (at the end) O are scaled down.  The P
-        // of chunk c lands in columns 16c .. 16c+15, i.e. over S of chunk c/2, which
-        // has been read by then.
-        float o_scale = 1.f;
+        // processed; the P of chunk c lands in columns 16c .. 16c+15, i.e. over S of
+        // chunk c/2, which has been read by then.  Weights are taken against m_ref,
+        // held for the whole tile, so they are rounded to the operand type once.  Only
+        // if a row's max passes m_ref by more than kRaiseNow (the weights would
+        // overflow the operand type) is m_ref raised inside the tile, scaling down the
+        // weights already stored (rounded a second time).
+        float o_scale = o_pending;
         float sum4[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t sr[2][32];
         if (wmax > 0) tmem_ld32_async(s_tmem, sr[0]);
@@ -640,14 +650,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(cur[i]));
-          const float m_new = fmaxf(m_ref, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2);
-          const bool raise = m_new > m_ref + 8.f;
+          m_run = fmaxf(m_run, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2);
+          const bool raise = m_run > m_ref + kRaiseNow<T>;  // also the first chunk of an item
           if (__any_sync(kFull, raise)) {
-            const float alpha = raise ? ex2(m_ref - m_new) : 1.f;
+            const float alpha = raise ? ex2(m_ref - m_run) : 1.f;
             l = (l + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]))) * alpha;
 #pragma unroll
             for (int k = 0; k < 4; ++k) sum4[k] = 0.f;
-            if (raise) m_ref = m_new;
+            if (raise) m_ref = m_run;
             o_scale *= alpha;
             if (c > 0) {  // rescale the weights this tile has stored so far
               tmem_wait_st();
@@ -676,8 +686,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st16(s_tmem + c * 16, w);
         }
         if (j > 0 && __any_sync(kFull, o_scale != 1.f)) {
-          // O_q already holds the previous tiles (the S commit covered their P V);
-          // rows that did not raise scale by 1
+          // O_q holds the previous tiles (the S commit covered their P V); rows with
+          // nothing owed scale by 1
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t r[32];
@@ -690,6 +700,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+        // raise the reference for the next tile once the row max has moved by more
+        // than 8, so weights stay near or below 2^8; O pays the factor next tile
+        o_pending = 1.f;
+        if (m_run > m_ref + 8.f) {
+          o_pending = ex2(m_ref - m_run);
+          l *= o_pending;
+          m_ref = m_run;
+        }
         tmem_wait_st();
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         __syncwarp();
@@ -699,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && !wait_all(BO_FULL + q, oc & 1)) ok = false;
       ++oc;
       const bool zero = !ok || !(l > 0.f);
-      const float inv = zero ? 0.f : 1.f / l;
+      const float inv = zero ? 0.f : o_pending / l;  // O still owes the last tile's raise
       T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(qrow0 + row) * a.out_row +
               static_cast<int64_t>(it.h) * kD;
 #pragma unroll
