@@ -162,10 +162,15 @@ int pa_decode(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_c
  * Arithmetic: q.k products accumulated in fp32 by the tensor cores, softmax in fp32,
  * the weights rounded to the cache dtype before the value product (fp32 accumulate),
  * normalisation in fp32.  Cache slots of a frame beyond L_s are read and must hold
- * finite values (the weights there are zero).  A sequence with n_s > L_s or
- * L_s > max_blocks*B sets PA_DEV_BAD_LEN and its rows are left untouched; frame ids
- * outside [0, num_blocks) set PA_DEV_BAD_BLOCK and read as zeros.  Uses the
- * (device, stream) workspace's work counter; one thread block per SM.
+ * finite values (the weights there are zero).  A sequence whose query range is not
+ * inside [0, T] (query_start[s] < 0, query_start[s+1] < query_start[s] or > T), with
+ * n_s > L_s or with L_s > max_blocks*B sets PA_DEV_BAD_LEN and its rows are left
+ * untouched; ranges that overlap so much that they hold more 256-row tile pairs than
+ * T rows allow set PA_DEV_BAD_LEN and nothing is computed.  Frame ids outside
+ * [0, num_blocks) set PA_DEV_BAD_BLOCK and read as zeros.  Uses the (device, stream)
+ * workspace's work counter; one thread block per SM; tile pairs are taken longest
+ * first.  PA_ERR_UNSUPPORTED when S + T/256 is too large for the block's shared memory
+ * (about 8000).
  */
 int pa_prefill(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
                const pa_tensor* block_tables, const pa_tensor* context_lens,

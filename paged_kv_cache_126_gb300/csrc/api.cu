@@ -531,7 +531,11 @@ int pa_prefill(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_
   if (max_blocks < 0 || (S > 1 && block_tables->stride[0] < max_blocks)) return PA_ERR_STRIDE;
   if (max_blocks * B > INT32_MAX || T > INT32_MAX || nb * B > INT32_MAX) return PA_ERR_UNSUPPORTED;
   if (S == 0 || T == 0) return PA_OK;
-  if (pa::prefill_smem_bytes(static_cast<int>(S)) > 227 * 1024) return PA_ERR_UNSUPPORTED;
+  // a sequence with n query rows forms ceil(ceil(n / 128) / 2) <= n / 256 + 1 units
+  const int64_t unit_cap = S + (T + 255) / 256 + 1;
+  if (unit_cap > INT32_MAX ||
+      pa::prefill_smem_bytes(static_cast<int>(S), static_cast<int>(unit_cap)) > 227 * 1024)
+    return PA_ERR_UNSUPPORTED;
   int dev;
   PA_TRY(current_device(&dev));
 
@@ -551,6 +555,7 @@ int pa_prefill(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_
   a.num_blocks = static_cast<int32_t>(nb);
   a.max_blocks = static_cast<int32_t>(max_blocks);
   a.T = static_cast<int32_t>(T);
+  a.unit_cap = static_cast<int32_t>(unit_cap);
   a.qk_scale_log2 = scale * 1.4426950408889634f;
   a.status = g_dev[dev].status;
 

@@ -93,6 +93,7 @@ struct PrefillArgs {
   const int32_t* context_lens;  // [S] tokens in the cache, chunk included
   const int32_t* query_start;   // [S + 1] q rows of sequence s: query_start[s] .. query_start[s+1]-1
   int32_t S, H, B, num_blocks, max_blocks, T;
+  int32_t unit_cap;             // room for (sequence, tile pair) units in shared memory
   float qk_scale_log2;
   int32_t* sched;               // [2] work counter, retired blocks (zero between launches)
   int32_t* status;
@@ -101,7 +102,7 @@ cudaError_t launch_prefill_f16(const PrefillArgs&, const CUtensorMap& tq, const 
                                const CUtensorMap& tv, int grid, cudaStream_t);
 cudaError_t launch_prefill_bf16(const PrefillArgs&, const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, int grid, cudaStream_t);
-size_t prefill_smem_bytes(int S);
+size_t prefill_smem_bytes(int S, int unit_cap);
 
 // status bits (mirror pa.h)
 constexpr int32_t kDevBadSlot = 0x1;

@@ -15,6 +15,6 @@ cudaError_t launch_prefill_bf16(const PrefillArgs& a, const CUtensorMap& tq, con
   return pk::launch<__nv_bfloat16>(a, tq, tk, tv, grid, stream);
 }
 
-size_t prefill_smem_bytes(int S) { return pk::smem_bytes(S); }
+size_t prefill_smem_bytes(int S, int unit_cap) { return pk::smem_bytes(S, unit_cap); }
 
 }  // namespace pa

@@ -10,8 +10,8 @@
 // Inference", "The Mathematics of Block Translation").
 //
 // Design (one thread block per SM, persistent, dynamic work counter):
-//   * Work item = (sequence, head, pair of consecutive 128-query tiles); later
-//     (longer) pairs of a sequence first.  Both tiles of a pair share every K/V
+//   * Work item = (sequence, head, pair of consecutive 128-query tiles); pairs are
+//     taken longest first (stable 32-bucket counting sort on their key-tile count).  Both tiles of a pair share every K/V
 //     tile, which halves the copies and the L2 traffic per FLOP.  K/V are walked in
 //     tiles of 128 keys, each assembled from 128/B frames, one TMA copy per frame
 //     through a 5-D view of the cache that lands the frame as [B/8 row groups]
@@ -62,8 +62,10 @@ constexpr uint32_t kSmK = kSmQ + 2 * kTile;   // [2 stages] K tiles: [16 groups]
 constexpr uint32_t kSmV = kSmK + 2 * kTile;   // [2 stages] V tiles, same layout
 constexpr uint32_t kSmBar = kSmV + 2 * kTile; // mbarriers
 constexpr uint32_t kSmMisc = kSmBar + 32 * 8; // flags, TMEM address, item ring
-constexpr uint32_t kSmOff = kSmMisc + 64;     // per-sequence item offsets [S + 1]
-__host__ __device__ constexpr uint32_t smem_bytes(int S) { return kSmOff + 4u * (S + 1) + 1024u; }
+constexpr uint32_t kSmOff = kSmMisc + 64;     // unit offsets [S + 1] | histogram [64] | unit order [unit_cap]
+__host__ __device__ constexpr uint32_t smem_bytes(int S, int unit_cap) {
+  return kSmOff + 4u * (S + 1) + 4u * 64u + 4u * unit_cap + 1024u;
+}
 
 // TMEM (512 columns): S_q at column 128 q, O_q at 256 + 128 q (fp32, lane = query row);
 // P_q (16-bit, two per column) overwrites the first 64 columns of S_q.
@@ -266,9 +268,10 @@ __device__ __forceinline__ int upper_seq(const int32_t* off, int S, int x) {
   return lo;
 }
 
-// A work item is a pair of consecutive 128-query tiles of one (sequence, head):
-// slot 1 holds the later tile, slot 0 the one before it (absent when the chunk has
-// an odd tile count and this is its first pair).  Both share every K/V tile.
+// A unit is a pair of consecutive 128-query tiles of one sequence: slot 1 holds the
+// later tile, slot 0 the one before it (absent when the chunk has an odd tile count
+// and this is its first pair).  A work item is (unit, head); both tiles share every
+// K/V tile.
 struct PItem {
   int s, h;
   int nkv;       // key tiles the item walks (those of slot 1)
@@ -278,24 +281,23 @@ struct PItem {
   int nkv_q[2];  // key tiles the slot visits, 0 when unused
 };
 
-__device__ __forceinline__ bool seq_bad(int n, int L, const PrefillArgs& a) {
-  return n < 0 || L < n || static_cast<int64_t>(L) > static_cast<int64_t>(a.max_blocks) * a.B;
+// A sequence is skipped (and flagged) unless 0 <= qs <= qe <= T, n = qe - qs <= L and
+// L fits its block table.
+__device__ __forceinline__ bool seq_bad(int qs, int qe, int L, const PrefillArgs& a) {
+  return qs < 0 || qe < qs || qe > a.T || L < qe - qs ||
+         static_cast<int64_t>(L) > static_cast<int64_t>(a.max_blocks) * a.B;
 }
 
-__device__ __forceinline__ PItem locate(const PrefillArgs& a, const int32_t* off, int item) {
-  PItem it;
-  it.s = upper_seq(off, a.S, item);
-  const int local = item - off[it.s];
-  const int pr = local / a.H;  // pair index, counted from the end of the chunk
-  it.h = local - pr * a.H;
-  const int qs = a.query_start[it.s], qe = a.query_start[it.s + 1];
+// Tiles of pair p (counted from the end of the chunk) of a sequence.
+__device__ __forceinline__ void pair_tiles(const PrefillArgs& a, int s, int p, PItem& it) {
+  const int qs = a.query_start[s], qe = a.query_start[s + 1];
   const int n = qe - qs;
-  const int L = a.context_lens[it.s];
-  const bool bad = seq_bad(n, L, a);
+  const int L = a.context_lens[s];
+  const bool bad = seq_bad(qs, qe, L, a);
   const int ntiles = n > 0 ? (n + kBM - 1) / kBM : 0;
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
-    const int qt = ntiles - 1 - 2 * pr - (1 - q);
+    const int qt = ntiles - 1 - 2 * p - (1 - q);
     if (bad || qt < 0) {
       it.qrow0[q] = qs;
       it.nrows[q] = 0;
@@ -309,6 +311,17 @@ __device__ __forceinline__ PItem locate(const PrefillArgs& a, const int32_t* off
     }
   }
   it.nkv = it.nkv_q[1];
+}
+
+// Item -> (unit of rank item / H in the longest-first order, head item % H).
+__device__ __forceinline__ PItem locate(const PrefillArgs& a, const int32_t* offu, const int32_t* order,
+                                        int item) {
+  PItem it;
+  const int r = item / a.H;
+  it.h = item - r * a.H;
+  const int u = order[r];
+  it.s = upper_seq(offu, a.S, u);
+  pair_tiles(a, it.s, u - offu[it.s], it);
   return it;
 }
 
@@ -324,7 +337,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kSmMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmMisc + 4);
   volatile int32_t* item_slot = reinterpret_cast<volatile int32_t*>(smem + kSmMisc + 8);  // [2]
-  int32_t* off = reinterpret_cast<int32_t*>(smem + kSmOff);
+  int32_t* offu = reinterpret_cast<int32_t*>(smem + kSmOff);  // [S + 1] units per sequence, prefix
+  int32_t* hist = offu + (a.S + 1);                            // [64] bucket counts, cursors
+  int32_t* order = hist + 64;                                  // [unit_cap] units, longest first
+  int32_t* max_nkv = reinterpret_cast<int32_t*>(smem + kSmMisc + 16);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = a.B;
@@ -350,16 +366,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
   }
-  // per-sequence item counts (tile pairs x heads) and their prefix
+  // ---- work list: units (sequence, tile pair) ordered longest first by a stable
+  //      32-bucket counting sort on their key-tile count (identical in every block);
+  //      item = (unit rank, head) -------------------------------------------------------
+  if (tid == 0) *max_nkv = 0;
+  if (tid < 64) hist[tid] = 0;
+  if (tid == 0) offu[0] = 0;
+  __syncthreads();
   for (int s = tid; s < a.S; s += blockDim.x) {
-    const int n = a.query_start[s + 1] - a.query_start[s];
+    const int qs = a.query_start[s], qe = a.query_start[s + 1];
     const int L = a.context_lens[s];
-    const bool bad = seq_bad(n, L, a);
+    const bool bad = seq_bad(qs, qe, L, a);
     if (bad && blockIdx.x == 0) atomicOr(a.status, kDevBadLen);
-    const int ntiles = n > 0 ? (n + kBM - 1) / kBM : 0;
-    off[s + 1] = bad ? 0 : ((ntiles + 1) / 2) * a.H;
+    const int n = bad ? 0 : qe - qs;
+    const int ntiles = (n + kBM - 1) / kBM;
+    offu[s + 1] = (ntiles + 1) / 2;
+    if (n > 0) atomicMax(max_nkv, (L + kBN - 1) / kBN);  // the last tile sees the whole context
   }
-  if (tid == 0) off[0] = 0;
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -367,19 +390,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     int carry = 0;
     for (int base = 0; base < a.S; base += 32) {
       const int i = base + lane;
-      int v = i < a.S ? off[i + 1] : 0;
+      int v = i < a.S ? offu[i + 1] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int n = __shfl_up_sync(kFull, v, o);
         if (lane >= o) v += n;
       }
       v += carry;
-      if (i < a.S) off[i + 1] = v;
+      if (i < a.S) offu[i + 1] = v;
       carry = __shfl_sync(kFull, v, 31);
     }
   }
   __syncthreads();
-  const int total = off[a.S];
+  const int n_units = offu[a.S];
+  if (n_units > a.unit_cap) {  // query ranges overlap beyond the rows given: no work
+    if (tid == 0 && blockIdx.x == 0) atomicOr(a.status, kDevBadLen);
+  } else if (warp == 1) {
+    const int mx = *max_nkv;
+    auto bucket_of = [&](int u) {
+      if (u >= n_units) return -1;
+      PItem t;
+      const int s = upper_seq(offu, a.S, u);
+      pair_tiles(a, s, u - offu[s], t);
+      return min(31, static_cast<int>((static_cast<long long>(t.nkv) * 32) / (mx + 1)));
+    };
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = 0; base < n_units; base += 32) {
+      const int b = bucket_of(base + lane);
+      const unsigned same = __match_any_sync(kFull, b);
+      if (b >= 0 && (same & lt) == 0) hist[b] += __popc(same);
+      __syncwarp();
+    }
+    // cursor[b] = units in buckets above b (longest first)
+    const int cnt = hist[31 - lane];
+    int v = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(kFull, v, o);
+      if (lane >= o) v += n;
+    }
+    hist[32 + (31 - lane)] = v - cnt;
+    __syncwarp();
+    for (int base = 0; base < n_units; base += 32) {
+      const int u = base + lane;
+      const int b = bucket_of(u);
+      const unsigned same = __match_any_sync(kFull, b);
+      if (b >= 0) order[hist[32 + b] + __popc(same & lt)] = u;
+      __syncwarp();
+      if (b >= 0 && (same & lt) == 0) hist[32 + b] += __popc(same);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  const int total = n_units > a.unit_cap ? 0 : n_units * a.H;
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
@@ -402,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++ni;
       if (done) break;
-      const PItem it = locate(a, off, item);
+      const PItem it = locate(a, offu, order, item);
       if (it.nkv == 0) continue;
       // Q tiles of the used slots (two 64-column halves each)
       int ok = 1;
@@ -513,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(BAR(BI_EMPTY + sl));
         ++ni;
         if (item < 0) break;
-        const PItem it = locate(a, off, item);
+        const PItem it = locate(a, offu, order, item);
         if (it.nkv == 0) continue;
         const int n0 = it.nkv_q[0], n1 = it.nkv_q[1];
         bool ok = wait(BQ_FULL, qi & 1);
@@ -594,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(BAR(BI_EMPTY + sl));
       ++ni;
       if (item < 0) break;
-      const PItem it = locate(a, off, item);
+      const PItem it = locate(a, offu, order, item);
       const int nk = q ? it.nkv_q[1] : it.nkv_q[0];
       if (nk == 0) continue;
       const int pos0 = q ? it.pos0[1] : it.pos0[0];
@@ -752,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <typename T>
 cudaError_t launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                    int grid, cudaStream_t stream) {
-  const size_t smem = smem_bytes(a.S);
+  const size_t smem = smem_bytes(a.S, a.unit_cap);
   auto kern = prefill_kernel<T>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;

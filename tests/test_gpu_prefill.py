@@ -110,3 +110,32 @@ def test_wide_score_range(pa, sigma, dtype):
                                   seed=int(sigma * 10))
     eng, outs, ref = run_both(pa, w)
     check_prefill(w, outs, ref, weight_roundings=2)
+
+
+@pytest.mark.parametrize("qs_kind", ["past_end", "negative_start", "decreasing"])
+def test_bad_query_ranges_flagged_and_skipped(pa, qs_kind):
+    """A sequence whose query range leaves [0, T] (or runs backwards) is flagged with
+    PA_DEV_BAD_LEN and its rows stay untouched; the other sequence is computed as in
+    a clean launch."""
+    w = workloads.chunked_prefill([40, 300], [200, 150], H=2, D=128, B=16, dtype="f16", seed=3)
+    eng, outs, ref = run_both(pa, w)
+    (op,) = w.prefill_ops
+    seqs, counts = w.ops[op][1], w.ops[op][2]
+    T = sum(counts)
+    good = outs[op]
+    dev = good.device
+    assert pa.pa_get_device_status() == 0
+    if qs_kind == "past_end":
+        qs, bad_rows, ok_rows = [0, 200, T + 64], slice(200, T), slice(0, 200)
+    elif qs_kind == "negative_start":
+        qs, bad_rows, ok_rows = [-5, 200, T], slice(0, 200), slice(200, T)
+    else:
+        qs, bad_rows, ok_rows = [0, 200, 150], slice(200, T), slice(0, 200)
+    tables, lens = eng.bm.block_tables(list(seqs), eng.max_blocks)
+    q = pa.to_device_rows(w.query(op), w.dtype, dev)
+    out = torch.full_like(good, 7.0)
+    pa.pa_prefill(q, eng.k_cache, eng.v_cache, torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev),
+                  torch.tensor(qs, dtype=torch.int32, device=dev), w.scale, out)
+    assert pa.pa_get_device_status() & pa.PA_DEV_BAD_LEN
+    assert torch.all(out[bad_rows] == 7.0)
+    assert torch.equal(out[ok_rows], good[ok_rows])
