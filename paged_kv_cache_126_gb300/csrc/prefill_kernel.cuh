@@ -142,6 +142,36 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Three-input max and packed two-lane fp32 arithmetic (one instruction per pair).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unf2(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // tcgen05 shared-memory matrix descriptor: 128-byte swizzle, SM100 version field.
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
@@ -641,6 +671,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_tmem = tmem + lane_base + kTmemS + q * 128;
     const uint32_t o_tmem = tmem + lane_base + kTmemO + q * 128;
     const float sl2 = a.qk_scale_log2;
+    const uint64_t sl2x2 = f2(sl2, sl2);
+    auto row_sum = [](const uint64_t (&v)[2]) {
+      float a0, a1, b0, b1;
+      unf2(v[0], a0, a1);
+      unf2(v[1], b0, b1);
+      return (a0 + a1) + (b0 + b1);
+    };
     int ni = 0;
     uint32_t sc = 0, oc = 0;  // S_FULL and O_FULL phases of this slot
     auto wait_all = [&](int bar, uint32_t parity) -> bool {
@@ -689,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // overflow the operand type) is m_ref raised inside the tile, scaling down the
         // weights already stored (rounded a second time).
         float o_scale = o_pending;
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint64_t sum2[2] = {0ull, 0ull};  // packed fp32 pairs of partial row sums
         uint32_t sr[2][32];
         if (wmax > 0) tmem_ld32_async(s_tmem, sr[0]);
 #pragma unroll
@@ -712,14 +749,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(cur[i]));
+          for (int i = 0; i < 32; i += 2)
+            mx4[(i >> 1) & 3] = fmax3(mx4[(i >> 1) & 3], __uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
           m_run = fmaxf(m_run, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2);
           const bool raise = m_run > m_ref + kRaiseNow<T>;  // also the first chunk of an item
           if (__any_sync(kFull, raise)) {
             const float alpha = raise ? ex2(m_ref - m_run) : 1.f;
-            l = (l + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]))) * alpha;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) sum4[k] = 0.f;
+            l = (l + row_sum(sum2)) * alpha;
+            sum2[0] = sum2[1] = 0ull;
             if (raise) m_ref = m_run;
             o_scale *= alpha;
             if (c > 0) {  // rescale the weights this tile has stored so far
@@ -737,13 +774,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
-          const float nm = -m_ref;
+          const uint64_t nm2 = f2(-m_ref, -m_ref);
           uint32_t w[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const float p0 = ex2(fmaf(__uint_as_float(cur[i]), sl2, nm));
-            const float p1 = ex2(fmaf(__uint_as_float(cur[i + 1]), sl2, nm));
-            sum4[(i >> 1) & 3] += p0 + p1;
+            float x0, x1;
+            unf2(ffma2(f2(__uint_as_float(cur[i]), __uint_as_float(cur[i + 1])), sl2x2, nm2), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            sum2[(i >> 1) & 1] = fadd2(sum2[(i >> 1) & 1], f2(p0, p1));
             w[i >> 1] = pack2<T>(p0, p1);
           }
           tmem_st16(s_tmem + c * 16, w);
@@ -762,7 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(o_tmem + c * 32, r);
           }
         }
-        l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+        l += row_sum(sum2);
         // raise the reference for the next tile once the row max has moved by more
         // than 8, so weights stay near or below 2^8; O pays the factor next tile
         o_pending = 1.f;
