@@ -290,6 +290,42 @@ int pa_bm_step(pa_bm* bm, const int64_t* seq_ids, int32_t n, int32_t* slots_out,
 int pa_bm_extend(pa_bm* bm, int64_t seq_id, int32_t num_tokens, int32_t* slots_out,
                  int32_t* copies_out, int32_t* n_copies_out);
 
+/* ---- prefix caching ["PagedAttention: Virtual Memory Guide for LLM Inference",
+ * "2. Native Synergy with RadixAttention and Prompt Caching": filled blocks are
+ * immutable, so a prompt whose token prefix is already in the cache maps those
+ * blocks onto the frames holding them, with no recomputation].
+ *
+ * A filled block of a sequence admitted with token ids is registered under the key
+ * (node of the block before it, its B token ids); nodes form a trie and their ids
+ * are never reused.  A freed frame keeps its block registered and goes to the back
+ * of the free list as usual; the registration is dropped (evicted) only when the
+ * free list hands the frame out again.  Sequences admitted without token ids, and
+ * their forks, never register blocks; an append without a token id leaves its
+ * block (and every later block of that sequence) unregistered.
+ *
+ * pa_bm_add_seq_cached: admit a prompt of num_tokens token ids [num_tokens].  Its
+ * leading filled blocks that are registered (looked up in order, stopping at the
+ * first miss; a block holding the prompt's last token never counts) are shared:
+ * each gains a reference, leaving the free list if it was there.  The remaining
+ * blocks come from the free list (blocks filled by the prompt are registered; if
+ * the same content is registered already the existing node stands for it).
+ * *n_cached_out = tokens found in the cache (a multiple of B, < num_tokens unless
+ * num_tokens is 0); slots_out [num_tokens] receives the slots of tokens
+ * n_cached .. num_tokens-1, whose K/V rows the caller must write.  All-or-nothing:
+ * PA_ERR_OUT_OF_BLOCKS (counting cached frames about to be reused as taken) leaves
+ * every state unchanged; PA_ERR_SEQ_EXISTS for a live id.
+ * pa_bm_step_tokens / pa_bm_extend_tokens: pa_bm_step / pa_bm_extend with the id of
+ * each appended token (tokens [n]), so that blocks they fill are registered.
+ * pa_bm_cached_frames: out[f] = 1 if frame f holds a registered block (out may be
+ * NULL when cap is 0); *n_cached_out = how many do. */
+int pa_bm_add_seq_cached(pa_bm* bm, int64_t seq_id, const int32_t* tokens, int32_t num_tokens,
+                         int32_t* slots_out, int32_t* n_cached_out);
+int pa_bm_step_tokens(pa_bm* bm, const int64_t* seq_ids, const int32_t* tokens, int32_t n,
+                      int32_t* slots_out, int32_t* copies_out, int32_t* n_copies_out);
+int pa_bm_extend_tokens(pa_bm* bm, int64_t seq_id, const int32_t* tokens, int32_t num_tokens,
+                        int32_t* slots_out, int32_t* copies_out, int32_t* n_copies_out);
+int pa_bm_cached_frames(const pa_bm* bm, int32_t* out, int32_t cap, int32_t* n_cached_out);
+
 /* Zero-copy fork: child shares every frame of parent (each gains a reference)
  * and inherits its length [VM "2. Zero-Copy Branching"]. */
 int pa_bm_fork(pa_bm* bm, int64_t parent_id, int64_t child_id);

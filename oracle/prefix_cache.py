@@ -20,8 +20,9 @@ Readings taken where the page leaves the mechanics open (listed in the design doc):
     (the prompt's full blocks past the hits) and when appends with token ids fill
     a block.  If the key is already registered (the same content computed twice),
     the existing node stands for the block's content and this frame stays
-    unregistered.  Appends without token ids (and prompts admitted without token
-    ids) never register anything.
+    unregistered.  An append without a token id leaves its block unregistered
+    (and every later block of that sequence); a sequence admitted without token
+    ids (and its forks) never registers anything.
   * A freed frame keeps its contents and its registration and goes to the back of
     the free list like any other; it is evicted (its node removed) only when the
     free list hands it out again.  Frames are therefore evicted least recently
@@ -49,6 +50,7 @@ class OraclePrefixBlockManager(OracleBlockManager):
         self.next_node = 1
         self.tokens: dict[int, list] = {}            # seq -> token ids (None entries: unknown)
         self.nodes: dict[int, list] = {}             # seq -> node id per block (0: none)
+        self.tracked: set[int] = set()               # sequences admitted with token ids
 
     # -- frame pool: a frame handed out again loses its registration -----------------------
     def _take_frame(self) -> int:
@@ -81,6 +83,8 @@ class OraclePrefixBlockManager(OracleBlockManager):
         B = self.block_size
         toks = self.tokens[seq][block * B:(block + 1) * B]
         nodes = self.nodes[seq]
+        if seq not in self.tracked:
+            return
         parent = self.ROOT if block == 0 else nodes[block - 1]
         if any(t is None for t in toks) or parent == 0 and block > 0:
             nodes[block] = 0
@@ -135,6 +139,7 @@ class OraclePrefixBlockManager(OracleBlockManager):
         self.lens[seq] = L
         self.tokens[seq] = list(tokens)
         self.nodes[seq] = [n for n, _ in hits]
+        self.tracked.add(seq)
         for i in range(len(hits), n_blocks):
             table.append(self._take_frame())
             self.nodes[seq].append(0)
@@ -160,11 +165,11 @@ class OraclePrefixBlockManager(OracleBlockManager):
         return (copy.copy(self.free_list), list(self.refs), {s: list(t) for s, t in self.tables.items()},
                 dict(self.lens), dict(self.node_of_key), dict(self.node_frame), dict(self.node_key),
                 list(self.frame_node), self.next_node, {s: list(t) for s, t in self.tokens.items()},
-                {s: list(n) for s, n in self.nodes.items()})
+                {s: list(n) for s, n in self.nodes.items()}, set(self.tracked))
 
     def _restore(self, saved):
         (self.free_list, self.refs, self.tables, self.lens, self.node_of_key, self.node_frame, self.node_key,
-         self.frame_node, self.next_node, self.tokens, self.nodes) = saved
+         self.frame_node, self.next_node, self.tokens, self.nodes, self.tracked) = saved
 
     def step(self, seqs, tokens=None):
         """One decode step (tokens[i] is the id appended to seqs[i], or None)."""
@@ -190,12 +195,15 @@ class OraclePrefixBlockManager(OracleBlockManager):
         super().fork(parent, child)
         self.tokens[child] = list(self.tokens[parent])
         self.nodes[child] = list(self.nodes[parent])
+        if parent in self.tracked:
+            self.tracked.add(child)
 
     def free(self, seq: int):
         r = super().free(seq)
         if r is None:
             del self.tokens[seq]
             del self.nodes[seq]
+            self.tracked.discard(seq)
         return r
 
     # -- views --------------------------------------------------------------------------

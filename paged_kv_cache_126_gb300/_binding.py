@@ -84,6 +84,10 @@ def _load():
         "pa_bm_free_list": ([vp, i32p, C.c_int32, i32p], C.c_int),
         "pa_bm_ref_counts": ([vp, i32p, C.c_int32], C.c_int),
         "pa_bm_num_seqs": ([vp, i32p], C.c_int),
+        "pa_bm_add_seq_cached": ([vp, C.c_int64, i32p, C.c_int32, i32p, i32p], C.c_int),
+        "pa_bm_step_tokens": ([vp, i64p, i32p, C.c_int32, i32p, i32p, i32p], C.c_int),
+        "pa_bm_extend_tokens": ([vp, C.c_int64, i32p, C.c_int32, i32p, i32p, i32p], C.c_int),
+        "pa_bm_cached_frames": ([vp, i32p, C.c_int32, i32p], C.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -99,7 +103,7 @@ EXPORTED = (
     "pa_strerror", "pa_launch_count", "pa_shutdown", "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq",
     "pa_bm_append", "pa_bm_step", "pa_bm_extend", "pa_bm_fork", "pa_bm_free", "pa_bm_block_tables", "pa_bm_seq_info",
     "pa_bm_table", "pa_bm_slot", "pa_bm_num_free", "pa_bm_free_list", "pa_bm_ref_counts",
-    "pa_bm_num_seqs",
+    "pa_bm_num_seqs", "pa_bm_add_seq_cached", "pa_bm_step_tokens", "pa_bm_extend_tokens", "pa_bm_cached_frames",
 )
 
 
@@ -227,7 +231,7 @@ def _i64(a: np.ndarray):
 
 
 class BlockManager:
-    """Host block manager of libpa (free list, refcounts, fork, copy-on-write)."""
+    """Host block manager of libpa (free list, refcounts, fork, copy-on-write, prefix cache)."""
 
     def __init__(self, num_blocks: int, block_size: int, free_order=None):
         self.num_blocks, self.block_size = int(num_blocks), int(block_size)
@@ -288,6 +292,46 @@ class BlockManager:
         nc = C.c_int32(0)
         _check(LIB.pa_bm_extend(self._h, int(seq), n, _i32(slots), _i32(copies), C.byref(nc)), "pa_bm_extend")
         return slots[:n], copies[: nc.value]
+
+    # -- prefix caching -------------------------------------------------------------
+    def add_seq_cached(self, seq: int, tokens):
+        """Admit a prompt by its token ids; returns (n_cached, slots of the uncached tokens)."""
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        L = len(toks)
+        slots = np.empty(max(L, 1), np.int32)
+        nc = C.c_int32(0)
+        _check(LIB.pa_bm_add_seq_cached(self._h, int(seq), _i32(toks) if L else None, L, _i32(slots),
+                                        C.byref(nc)), "pa_bm_add_seq_cached")
+        return nc.value, slots[: L - nc.value]
+
+    def step_tokens(self, seqs, tokens):
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        n = len(ids)
+        if len(toks) != n:
+            raise ValueError("one token id per appended sequence")
+        slots = np.empty(max(n, 1), np.int32)
+        copies = np.empty((max(n, 1), 2), np.int32)
+        nc = C.c_int32(0)
+        _check(LIB.pa_bm_step_tokens(self._h, _i64(ids), _i32(toks), n, _i32(slots), _i32(copies), C.byref(nc)),
+               "pa_bm_step_tokens")
+        return slots[:n], copies[: nc.value]
+
+    def extend_tokens(self, seq: int, tokens):
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        n = len(toks)
+        slots = np.empty(max(n, 1), np.int32)
+        copies = np.empty((max(n, 1), 2), np.int32)
+        nc = C.c_int32(0)
+        _check(LIB.pa_bm_extend_tokens(self._h, int(seq), _i32(toks) if n else None, n, _i32(slots), _i32(copies),
+                                       C.byref(nc)), "pa_bm_extend_tokens")
+        return slots[:n], copies[: nc.value]
+
+    def cached_frames(self) -> list:
+        out = np.empty(self.num_blocks, np.int32)
+        n = C.c_int32()
+        _check(LIB.pa_bm_cached_frames(self._h, _i32(out), self.num_blocks, C.byref(n)), "pa_bm_cached_frames")
+        return out.tolist()
 
     def fork(self, parent: int, child: int) -> None:
         _check(LIB.pa_bm_fork(self._h, int(parent), int(child)), "pa_bm_fork")

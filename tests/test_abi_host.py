@@ -189,3 +189,136 @@ def test_errors_leave_state_unchanged(pa):
         pa.BlockManager(0, 2)
     assert bm.free(0) == 0
     assert bm.free(0) == pa.PA_WARN_DOUBLE_FREE
+
+
+# ------------------------------------------------------------------ prefix caching
+from oracle.prefix_cache import OraclePrefixBlockManager  # noqa: E402
+
+
+def _same_cache_state(bm, ob):
+    _same_state(bm, ob)
+    assert bm.cached_frames() == ob.cached_frames()
+
+
+def test_prefix_cache_trace_bit_exact(pa, golden):
+    g = golden("prefix_cache_trace.json")
+    bm = pa.BlockManager(g["num_blocks"], g["block_size"])
+    ob = OraclePrefixBlockManager(g["num_blocks"], g["block_size"])
+    for st in g["steps"]:
+        exp = st["expect"]
+        if st["op"] == "add_cached":
+            if exp.get("error") == "out_of_blocks":
+                with pytest.raises(pa.PAError) as ei:
+                    bm.add_seq_cached(st["seq"], st["tokens"])
+                assert ei.value.code == pa.PA_ERR_OUT_OF_BLOCKS
+                with pytest.raises(OutOfBlocks):
+                    ob.add_seq_cached(st["seq"], st["tokens"])
+            else:
+                n_cached, slots = bm.add_seq_cached(st["seq"], st["tokens"])
+                assert n_cached == exp["n_cached"] and slots.tolist() == exp["slots"]
+                ob.add_seq_cached(st["seq"], st["tokens"])
+        elif st["op"] == "free":
+            assert bm.free(st["seq"]) == 0
+            ob.free(st["seq"])
+        elif st["op"] == "extend":
+            slots, copies = bm.extend_tokens(st["seq"], st["tokens"])
+            assert slots.tolist() == exp["slots"] and copies.tolist() == exp["copies"]
+            ob.extend(st["seq"], len(st["tokens"]), st["tokens"])
+        if "free" in exp:
+            assert bm.free_list() == exp["free"]
+        if "cached" in exp:
+            assert bm.cached_frames() == exp["cached"]
+        _same_cache_state(bm, ob)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_prefix_cache_random_ops_bit_exact(pa, seed):
+    rnd = random.Random(7000 + seed)
+    B = rnd.choice([1, 2, 4, 8, 16])
+    n = rnd.randint(10, 70)
+    order = rnd.sample(range(n), n)
+    bm = pa.BlockManager(n, B, order)
+    ob = OraclePrefixBlockManager(n, B, order)
+    prompts = [[rnd.randint(0, 3) for _ in range(rnd.randint(0, 5 * B))] for _ in range(4)]
+    next_id, hits = 0, 0
+    for _ in range(400):
+        live = list(ob.tables)
+        r = rnd.random()
+        if r < 0.3 or not live:
+            base = rnd.choice(prompts)
+            cut = rnd.randint(0, len(base))
+            toks = base[:cut] + [rnd.randint(0, 3) for _ in range(rnd.randint(0, 3 * B))]
+            try:
+                want = ob.add_seq_cached(next_id, toks)
+            except OutOfBlocks:
+                with pytest.raises(pa.PAError) as ei:
+                    bm.add_seq_cached(next_id, toks)
+                assert ei.value.code == pa.PA_ERR_OUT_OF_BLOCKS
+            else:
+                got = bm.add_seq_cached(next_id, toks)
+                assert got[0] == want[0] and got[1].tolist() == want[1]
+                hits += want[0]
+                if rnd.random() < 0.3:
+                    prompts.append(toks)
+            next_id += 1
+        elif r < 0.35:
+            L = rnd.randint(0, 2 * B)               # a prompt without token ids
+            try:
+                want = ob.add_seq(next_id, L)
+            except OutOfBlocks:
+                with pytest.raises(pa.PAError):
+                    bm.add_seq(next_id, L)
+            else:
+                assert bm.add_seq(next_id, L).tolist() == want
+            next_id += 1
+        elif r < 0.45:
+            p = rnd.choice(live)
+            ob.fork(p, next_id)
+            bm.fork(p, next_id)
+            next_id += 1
+        elif r < 0.6:
+            s = rnd.choice(live)
+            assert (bm.free(s) == pa.PA_WARN_DOUBLE_FREE) == (ob.free(s) is not None)
+        else:
+            seqs = [rnd.choice(live) for _ in range(rnd.randint(1, 4))]
+            with_tokens = rnd.random() < 0.8
+            toks = [rnd.randint(0, 3) for _ in seqs]
+            single = rnd.random() < 0.3
+            try:
+                if single:
+                    want = ob.extend(seqs[0], len(seqs), toks if with_tokens else None)
+                else:
+                    want = ob.step(seqs, toks if with_tokens else None)
+            except OutOfBlocks:
+                with pytest.raises(pa.PAError) as ei:
+                    if single:
+                        bm.extend_tokens(seqs[0], toks) if with_tokens else bm.extend(seqs[0], len(seqs))
+                    else:
+                        bm.step_tokens(seqs, toks) if with_tokens else bm.step(seqs)
+                assert ei.value.code == pa.PA_ERR_OUT_OF_BLOCKS
+            else:
+                if single:
+                    got = bm.extend_tokens(seqs[0], toks) if with_tokens else bm.extend(seqs[0], len(seqs))
+                else:
+                    got = bm.step_tokens(seqs, toks) if with_tokens else bm.step(seqs)
+                assert got[0].tolist() == want[0]
+                assert [tuple(c) for c in got[1].tolist()] == want[1]
+        _same_cache_state(bm, ob)
+    assert hits >= 0
+
+
+def test_prefix_cache_errors(pa):
+    bm = pa.BlockManager(4, 2)
+    assert bm.add_seq_cached(0, [1, 2, 3])[0] == 0
+    with pytest.raises(pa.PAError) as ei:
+        bm.add_seq_cached(0, [1, 2])
+    assert ei.value.code == pa.PA_ERR_SEQ_EXISTS
+    before = (bm.free_list(), bm.ref_counts(), bm.cached_frames())
+    with pytest.raises(pa.PAError) as ei:
+        bm.add_seq_cached(1, [9] * 7)                      # 4 new frames, 2 free
+    assert ei.value.code == pa.PA_ERR_OUT_OF_BLOCKS
+    assert (bm.free_list(), bm.ref_counts(), bm.cached_frames()) == before
+    n_cached, slots = bm.add_seq_cached(2, [])             # empty prompt: nothing to look up
+    assert n_cached == 0 and len(slots) == 0
+    with pytest.raises(ValueError):
+        bm.step_tokens([0, 2], [5])                        # one token id per sequence
