@@ -14,6 +14,9 @@ import numpy as np
 from .attention import paged_decode, paged_prefill
 from .block_manager import OracleBlockManager
 from .cache import OracleKVCache
+from .prefix_cache import OraclePrefixBlockManager
+
+TOKEN_OPS = ("add_tokens", "extend_tokens", "step_tokens", "prefill_new")
 
 
 @dataclass
@@ -28,6 +31,8 @@ class ReplayResult:
     outputs: dict = field(default_factory=dict)
     # per attend op index: (tables, lens) the attention used, in the op's seq order
     attend_meta: dict = field(default_factory=dict)
+    # per token-driven sequence: tokens its admission found in the cache
+    n_cached: dict = field(default_factory=dict)
 
 
 def _kept_frames(w, keep_seqs):
@@ -51,6 +56,37 @@ def _kept_frames(w, keep_seqs):
             for s in op[1]:
                 if s in keep_seqs:
                     seen.update(bm.tables[s])
+        elif kind == "add_tokens":
+            n_cached, slots = bm.add_seq_cached(op[1], op[2])
+            res.n_cached[op[1]] = n_cached
+            res.trace[i] = {"slots": slots, "copies": [], "n_cached": n_cached}
+            if cache is not None and slots:
+                k, v = w.token_rows(i)
+                cache.write(slots, k[n_cached:], v[n_cached:])
+        elif kind in ("extend_tokens", "step_tokens"):
+            if kind == "extend_tokens":
+                slots, copies = bm.extend(op[1], len(op[2]), list(op[2]))
+            else:
+                slots, copies = bm.step(list(op[1]), list(op[2]))
+            res.trace[i] = {"slots": slots, "copies": copies}
+            if cache is not None:
+                for src, dst in copies:
+                    cache.copy_block(src, dst)
+                k, v = w.token_rows(i)
+                cache.write(slots, k, v)
+        elif kind == "prefill_new":
+            seqs = op[1]
+            tables = [list(bm.tables[s]) for s in seqs]
+            lens = [bm.lens[s] for s in seqs]
+            counts = [lens[j] - res.n_cached[s] for j, s in enumerate(seqs)]
+            res.attend_meta[i] = (tables, lens, counts)
+            if cache is not None:
+                qs = w.position_queries(i)
+                outs = []
+                for j, s in enumerate(seqs):
+                    q = qs[j][lens[j] - counts[j]:lens[j]]
+                    outs.append(paged_prefill(q, cache, [tables[j]], [lens[j]], [0, counts[j]], w.scale))
+                res.outputs[i] = outs
         elif kind == "free":
             bm.free(op[1])
         elif kind == "attend":
@@ -73,8 +109,11 @@ def _kept_frames(w, keep_seqs):
 def replay(w, keep_seqs=None, with_cache: bool = True, snapshots: bool = False) -> ReplayResult:
     """Run every op of ``w``; attention only for ``keep_seqs`` (all if None)."""
     keep = None if keep_seqs is None else set(int(s) for s in keep_seqs)
+    tokens = any(op[0] in TOKEN_OPS for op in w.ops)
+    if tokens and keep is not None:
+        raise ValueError("token-driven workloads replay every sequence")
     frames = None if keep is None else _kept_frames(w, keep)
-    bm = OracleBlockManager(w.num_blocks, w.block_size, w.free_order)
+    bm = (OraclePrefixBlockManager if tokens else OracleBlockManager)(w.num_blocks, w.block_size, w.free_order)
     cache = (OracleKVCache(w.num_blocks, w.block_size, w.num_heads, w.head_dim, w.dtype, keep=frames)
              if with_cache else None)
     res = ReplayResult(bm=bm, cache=cache)
@@ -121,6 +160,37 @@ def replay(w, keep_seqs=None, with_cache: bool = True, snapshots: bool = False) 
                         a, b = qs[j], qs[j + 1]
                         out[a:b] = paged_prefill(q[a:b], cache, [tables[j]], [lens[j]], [0, b - a], w.scale)
                 res.outputs[i] = out
+        elif kind == "add_tokens":
+            n_cached, slots = bm.add_seq_cached(op[1], op[2])
+            res.n_cached[op[1]] = n_cached
+            res.trace[i] = {"slots": slots, "copies": [], "n_cached": n_cached}
+            if cache is not None and slots:
+                k, v = w.token_rows(i)
+                cache.write(slots, k[n_cached:], v[n_cached:])
+        elif kind in ("extend_tokens", "step_tokens"):
+            if kind == "extend_tokens":
+                slots, copies = bm.extend(op[1], len(op[2]), list(op[2]))
+            else:
+                slots, copies = bm.step(list(op[1]), list(op[2]))
+            res.trace[i] = {"slots": slots, "copies": copies}
+            if cache is not None:
+                for src, dst in copies:
+                    cache.copy_block(src, dst)
+                k, v = w.token_rows(i)
+                cache.write(slots, k, v)
+        elif kind == "prefill_new":
+            seqs = op[1]
+            tables = [list(bm.tables[s]) for s in seqs]
+            lens = [bm.lens[s] for s in seqs]
+            counts = [lens[j] - res.n_cached[s] for j, s in enumerate(seqs)]
+            res.attend_meta[i] = (tables, lens, counts)
+            if cache is not None:
+                qs = w.position_queries(i)
+                outs = []
+                for j, s in enumerate(seqs):
+                    q = qs[j][lens[j] - counts[j]:lens[j]]
+                    outs.append(paged_prefill(q, cache, [tables[j]], [lens[j]], [0, counts[j]], w.scale))
+                res.outputs[i] = outs
         elif kind == "free":
             bm.free(op[1])
         elif kind == "attend":

@@ -250,3 +250,40 @@ def test_planted_last_token_hit_is_caught(golden):
     g = golden("prefix_cache_trace.json")
     with pytest.raises(AssertionError):
         replay_trace(LastTokenMayHit(g["num_blocks"], g["block_size"]), g)
+
+
+# ------------------------------------------------------------------ attention through reused frames
+def _logical_prefill(w, op_index, seq_pos, seq, count):
+    """Definition: causal attention over the sequence's own token rows (no cache,
+    no block table), for its last `count` positions."""
+    import numpy as np
+
+    from oracle import attention_fp64, decode_storage
+
+    toks = w.token_history(op_index)[seq]
+    L = len(toks)
+    k, v = w.prefix_rows(toks)
+    K, V = decode_storage(k, w.dtype), decode_storage(v, w.dtype)
+    q = decode_storage(w.position_queries(op_index)[seq_pos][L - count:], w.dtype)
+    return np.stack([attention_fp64(q[r], K[:L - count + r + 1], V[:L - count + r + 1], w.scale)
+                     for r in range(count)])
+
+
+@pytest.mark.parametrize("turns,free_between,B", [(1, False, 8), (2, False, 8), (3, True, 4), (2, False, 16)])
+def test_prefill_through_reused_frames_equals_definition(turns, free_between, B):
+    import numpy as np
+
+    import workloads
+    from oracle import replay
+
+    w = workloads.shared_prefix(3, 37, [11, 20, 4], B=B, turns=turns, reply_len=7, free_between=free_between,
+                                seed=30 + turns)
+    r = replay(w)
+    assert sum(r.n_cached.values()) > 0          # the workload does reuse blocks
+    for i in w.prefill_ops + [j for j, op in enumerate(w.ops) if op[0] == "prefill_new"]:
+        if w.ops[i][0] != "prefill_new":
+            continue
+        tables, lens, counts = r.attend_meta[i]
+        for j, s in enumerate(w.ops[i][1]):
+            want = _logical_prefill(w, i, j, s, counts[j])
+            np.testing.assert_allclose(r.outputs[i][j], want, rtol=0, atol=1e-12)

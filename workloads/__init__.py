@@ -13,6 +13,8 @@ from .gen import (  # noqa: F401
     chunked_prefill,
     custom,
     prefill_batch,
+    prefix_ids,
+    shared_prefix,
     CONFIG_IDS,
     storage_numpy_dtype,
 )

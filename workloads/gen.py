@@ -17,6 +17,19 @@ each operation carries:
                              of seqs[i]; payload: sum(counts) queries, grouped by
                              sequence in list order.
 
+Token-driven ops (prefix caching).  Their K/V rows are a function of the token
+prefix, as a model's would be: the row of position j is drawn from a stream keyed
+by a 64-bit identity of tokens 0..j, so two requests with the same prefix carry
+identical rows for it.
+
+* ``("add_tokens", seq, tokens)``    -- a new sequence given by its token ids.
+* ``("extend_tokens", seq, tokens)`` -- tokens appended to one sequence.
+* ``("step_tokens", seqs, tokens)``  -- one decode step, tokens[i] for seqs[i].
+* ``("prefill_new", seqs)``          -- causal attention for the positions of each
+                             sequence that its admission did not find in the cache;
+                             payload: queries for every position of each sequence
+                             (the consumer takes the ones it needs).
+
 Payloads are drawn from a PCG64 stream keyed by ``(seed, op_index, kind)`` so any
 op's rows can be regenerated alone.  Values are drawn as float32 N(0, sigma^2)
 and rounded to nearest-even into the storage type; bf16 is carried as uint16 bit
@@ -61,6 +74,44 @@ def _to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "bf16":
         return _bf16_bits(x)
     raise ValueError(dtype)
+
+
+_M64 = np.uint64(0xFFFFFFFFFFFFFFFF)
+
+
+def _mix64(z: np.ndarray) -> np.ndarray:
+    """splitmix64 output function on uint64 arrays (wrapping arithmetic)."""
+    with np.errstate(over="ignore"):
+        z = z + np.uint64(0x9E3779B97F4A7C15)
+        z = (z ^ (z >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
+        z = (z ^ (z >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
+        return z ^ (z >> np.uint64(31))
+
+
+def prefix_ids(seed: int, tokens) -> np.ndarray:
+    """uint64 identity of every token prefix: ids[j] depends on tokens[0..j] only."""
+    out = np.empty(len(tokens), np.uint64)
+    h = _mix64(np.array([seed], np.uint64))[0]
+    with np.errstate(over="ignore"):
+        for j, t in enumerate(tokens):
+            h = _mix64(np.array([h ^ (np.uint64(int(t) & 0xFFFFFFFF) * np.uint64(0x100000001B3))], np.uint64))[0]
+            out[j] = h
+    return out
+
+
+def _keyed_normals(keys: np.ndarray, count: int) -> np.ndarray:
+    """float32 [len(keys), count] standard normals, one counter-based stream per key
+    (splitmix64 of key and index, Box-Muller on pairs)."""
+    keys = np.asarray(keys, np.uint64)
+    half = (count + 1) // 2
+    idx = np.arange(2 * half, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = _mix64(keys[:, None] * np.uint64(0xD1B54A32D192ED03) + idx[None, :])
+    u = ((z >> np.uint64(11)).astype(np.float64) + 0.5) * (1.0 / 9007199254740992.0)
+    u1, u2 = u[:, 0::2], u[:, 1::2]
+    r = np.sqrt(-2.0 * np.log(u1))
+    x = np.concatenate([r * np.cos(2 * np.pi * u2), r * np.sin(2 * np.pi * u2)], axis=1)
+    return x[:, :count].astype(np.float32)
 
 
 @dataclass
@@ -108,6 +159,75 @@ class Workload:
             return self._draw(op_index, "q", len(op[1]))
         assert op[0] == "prefill"
         return self._draw(op_index, "q", int(sum(op[2])))
+
+    # -- token-driven payloads ------------------------------------------------------
+    def token_history(self, op_index: int) -> dict:
+        """Token ids of every live token-driven sequence just before op ``op_index``."""
+        hist = {}
+        for op in self.ops[:op_index]:
+            kind = op[0]
+            if kind == "add_tokens":
+                hist[op[1]] = list(op[2])
+            elif kind == "extend_tokens":
+                hist[op[1]] = hist[op[1]] + list(op[2])
+            elif kind == "step_tokens":
+                for s, t in zip(op[1], op[2]):
+                    hist[s] = hist[s] + [t]
+            elif kind == "fork" and op[1] in hist:
+                hist[op[2]] = list(hist[op[1]])
+            elif kind == "free":
+                hist.pop(op[1], None)
+        return hist
+
+    def prefix_rows(self, tokens, start: int = 0, stop=None):
+        """(k, v) rows [stop-start, H, D] of positions start..stop-1 of a sequence with
+        these token ids, storage dtype; each row depends on its token prefix only."""
+        stop = len(tokens) if stop is None else stop
+        ids = prefix_ids(self.seed, tokens[:stop])[start:stop]
+        n, HD = len(ids), self.num_heads * self.head_dim
+        x = _keyed_normals(ids, 2 * HD)
+        if self.sigma != 1.0:
+            x *= np.float32(self.sigma)
+        k = _to_storage(x[:, :HD], self.dtype).reshape(n, self.num_heads, self.head_dim)
+        v = _to_storage(x[:, HD:], self.dtype).reshape(n, self.num_heads, self.head_dim)
+        return k, v
+
+    def token_rows(self, op_index: int):
+        """(k, v) rows carried by a token-driven op: every position of an
+        ``add_tokens`` prompt, the new positions of ``extend_tokens``, one row per
+        sequence of ``step_tokens`` (in op order)."""
+        op = self.ops[op_index]
+        hist = self.token_history(op_index)
+        if op[0] == "add_tokens":
+            return self.prefix_rows(list(op[2]))
+        if op[0] == "extend_tokens":
+            toks = hist[op[1]] + list(op[2])
+            return self.prefix_rows(toks, len(hist[op[1]]))
+        assert op[0] == "step_tokens"
+        ks, vs = [], []
+        for s, t in zip(op[1], op[2]):
+            toks = hist[s] + [t]
+            hist[s] = toks
+            k, v = self.prefix_rows(toks, len(toks) - 1)
+            ks.append(k)
+            vs.append(v)
+        return np.concatenate(ks), np.concatenate(vs)
+
+    def position_queries(self, op_index: int):
+        """Queries of a ``prefill_new`` op: one array [L_i, H, D] per listed sequence
+        (every position of its current length), storage dtype."""
+        op = self.ops[op_index]
+        hist = self.token_history(op_index)
+        out = []
+        for i, s in enumerate(op[1]):
+            L = len(hist[s])
+            ss = np.random.SeedSequence([self.seed, op_index, _KIND["q"], i])
+            g = np.random.Generator(np.random.PCG64(ss))
+            x = g.standard_normal(L * self.num_heads * self.head_dim, dtype=np.float32)
+            if self.sigma != 1.0:
+                x *= np.float32(self.sigma)
+            out.append(_to_storage(x, self.dtype).reshape(L, self.num_heads, self.head_dim))
+        return out
 
     @property
     def attend_ops(self):
@@ -271,6 +391,58 @@ def prefill_batch(small: bool = False) -> Workload:
     pre = rng.integers(0, 3073, size=16)
     return chunked_prefill(pre, [512] * 16, H=32, D=128, B=16, dtype="f16", seed=seed,
                            name="chunked prefill: 16 seqs, prefix~U[0,3072], chunk 512, H=32, D=128, B=16, f16")
+
+
+def shared_prefix(n_requests: int, system_len: int, user_lens, *, H=2, D=128, B=16, dtype="f16", sigma=1.0,
+                  seed=21, turns: int = 1, reply_len: int = 0, free_between: bool = False, pool=None,
+                  name=None) -> Workload:
+    """Requests that share a system prompt, each followed by a causal prefill of the
+    tokens its admission did not find in the cache.
+
+    Request i's prompt is the shared ``system_len`` tokens plus ``user_lens[i]``
+    tokens of its own.  With ``turns > 1`` each request then appends a reply of
+    ``reply_len`` tokens and returns for another turn as a new sequence whose prompt
+    is its whole conversation plus a fresh user message (multi-turn reuse).  With
+    ``free_between`` every request of a turn is freed before the next turn is
+    admitted (cached frames then come back from the free list).
+    """
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0])))
+    vocab = 1 << 20
+    system = rng.integers(0, vocab, size=system_len).tolist()
+    user_lens = [int(u) for u in user_lens]
+    conv = [system + rng.integers(0, vocab, size=u).tolist() for u in user_lens]
+    ops = []
+    seq = 0
+    final = {}
+    live = []
+    for t in range(turns):
+        ids = []
+        for i in range(n_requests):
+            ops.append(("add_tokens", seq, tuple(conv[i])))
+            ids.append(seq)
+            seq += 1
+        ops.append(("prefill_new", tuple(ids)))
+        for i, s in enumerate(ids):
+            final[s] = len(conv[i])
+        if t + 1 < turns:
+            for i, s in enumerate(ids):
+                reply = rng.integers(0, vocab, size=reply_len).tolist()
+                if reply:
+                    ops.append(("extend_tokens", s, tuple(reply)))
+                conv[i] = conv[i] + reply + rng.integers(0, vocab, size=max(1, user_lens[i] // 2)).tolist()
+                final[s] += reply_len
+        if free_between and t + 1 < turns:
+            for s in ids:
+                ops.append(("free", s))
+        else:
+            live += ids
+    need = sum(-(-L // B) for L in final.values())
+    nb = pool if pool is not None else max(1, int(math.ceil(1.2 * need)))
+    free_order = rng.permutation(nb).astype(np.int32)
+    return Workload(name=name or f"shared prefix: {n_requests} requests x (system {system_len} + user), "
+                                 f"{turns} turn(s), H={H}, D={D}, B={B}, {dtype}",
+                    num_heads=H, head_dim=D, block_size=B, dtype=dtype, sigma=sigma, num_blocks=nb,
+                    free_order=free_order, ops=ops, seed=seed, final_lens=final)
 
 
 def custom(lengths, *, H=2, D=128, B=16, dtype="f16", sigma=1.0, seed=7, shuffle=True,
