@@ -620,6 +620,106 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+def prefix_bench(n_requests=16, system_len=2048, user_len=512, reps=10):
+    """Admission of requests that share a system prompt: host block manager, cache
+    append of the rows that must be computed, causal prefill of those tokens.
+    Three ways: no prefix cache (every prompt in full), prefix cache starting empty
+    (the first request computes the system prompt), prefix cache already holding it.
+    One JSON line per run: prompt tokens admitted per second on the GPU (the append
+    of the computed rows + the prefill, CUDA events) and end to end (host block
+    manager + launches + GPU, one synchronize per admission), with the parts."""
+    import time
+
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_126_gb300 as pa
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    st = torch.cuda.current_stream(dev)
+    H, D, B, dtype = 32, 128, 16, "f16"
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([2024, 0])))
+    system = rng.integers(0, 1 << 20, size=system_len).astype(np.int32)
+    prompts = [np.concatenate([system, rng.integers(0, 1 << 20, size=user_len).astype(np.int32)])
+               for _ in range(n_requests)]
+    warm_prompt = np.concatenate([system, np.zeros(1, np.int32)])
+    L = system_len + user_len
+    nb = int(1.2 * n_requests * -(-L // B)) + 8
+    eng = pa.PagedKVEngine(nb, B, H, D, dtype, device=dev, max_seqs=max(64, n_requests), max_blocks_per_seq=-(-L // B))
+    g = torch.Generator(device=dev).manual_seed(7)
+    k_rows = torch.randn((n_requests, L, H, D), generator=g, device=dev, dtype=torch.float32).to(torch.float16)
+    v_rows = torch.randn((n_requests, L, H, D), generator=g, device=dev, dtype=torch.float32).to(torch.float16)
+    q_rows = torch.randn((n_requests * L, H, D), generator=g, device=dev, dtype=torch.float32).to(torch.float16)
+    scale = 1.0 / float(np.sqrt(D))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def host_admit(mode):
+        """Block manager only: per request (n_cached, slots of the rows to write)."""
+        eng.bm = pa.BlockManager(nb, B)
+        if mode == "warm":  # an earlier request left the system prompt in the cache
+            eng.bm.add_seq_cached(10 ** 6, warm_prompt)
+            eng.bm.free(10 ** 6)
+        res = []
+        for i, toks in enumerate(prompts):
+            if mode == "none":
+                res.append((0, eng.bm.add_seq(i, L)))
+            else:
+                res.append(eng.bm.add_seq_cached(i, toks))
+        return res
+
+    out = {}
+    for mode in ("none", "cold", "warm"):
+        # the rows a model would produce for the tokens that must be computed, laid
+        # out contiguously per admission (built once, outside the timed region)
+        res = host_admit(mode)
+        counts = [L - n for n, _ in res]
+        krows = torch.cat([k_rows[i, n:] for i, (n, _) in enumerate(res)])
+        vrows = torch.cat([v_rows[i, n:] for i, (n, _) in enumerate(res)])
+        q = torch.cat([q_rows[i * L + n:(i + 1) * L] for i, (n, _) in enumerate(res)])
+        flops = sum(prefill_flops([n], [L - n], H, D) for n, _ in res)
+        seqs = list(range(n_requests))
+
+        def admit():
+            t = time.perf_counter()
+            r = host_admit(mode)
+            t_bm = time.perf_counter() - t
+            ev[0].record(st)
+            eng.write_rows(np.concatenate([sl for _, sl in r]), krows, vrows)
+            ev[1].record(st)
+            eng.prefill(seqs, counts, q, scale)
+            ev[2].record(st)
+            torch.cuda.synchronize()
+            return t_bm, ev[0].elapsed_time(ev[1]) / 1e3, ev[1].elapsed_time(ev[2]) / 1e3
+
+        for _ in range(3):
+            admit()
+        walls, app, pf, bm_t = [], [], [], []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            t_bm, t_ap, t_pf = admit()
+            walls.append(time.perf_counter() - t0)
+            app.append(t_ap)
+            pf.append(t_pf)
+            bm_t.append(t_bm)
+        med = lambda x: float(np.median(x))
+        wall, ap, pfm, tb = med(walls), med(app), med(pf), med(bm_t)
+        out[mode] = {"ms_e2e": round(wall * 1e3, 3), "prompt_tokens_per_s_e2e": round(n_requests * L / wall),
+                     "gpu_ms": round((ap + pfm) * 1e3, 3),
+                     "prompt_tokens_per_s_gpu": round(n_requests * L / (ap + pfm)),
+                     "tokens_computed": sum(counts), "tokens_from_cache": n_requests * L - sum(counts),
+                     "append_ms": round(ap * 1e3, 3), "prefill_ms": round(pfm * 1e3, 3),
+                     "prefill_tflops": round(flops / pfm / 1e12, 1), "host_block_manager_ms": round(tb * 1e3, 3)}
+    line = {"metric": "prompt admission tokens/s with prefix caching (host block manager + append + prefill)",
+            "workload": f"{n_requests} requests x (system {system_len} + user {user_len}), H={H}, D={D}, B={B}, "
+                        f"{dtype}", "reps": reps, "statistic": "median", **out,
+            "speedup_gpu_warm_vs_none": round(out["none"]["gpu_ms"] / out["warm"]["gpu_ms"], 2),
+            "speedup_gpu_cold_vs_none": round(out["none"]["gpu_ms"] / out["cold"]["gpu_ms"], 2),
+            "speedup_e2e_warm_vs_none": round(out["none"]["ms_e2e"] / out["warm"]["ms_e2e"], 2),
+            "speedup_e2e_cold_vs_none": round(out["none"]["ms_e2e"] / out["cold"]["ms_e2e"], 2)}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -634,9 +734,13 @@ def main():
     ap.add_argument("--config", default="1")
     ap.add_argument("--cpu-worker", default=None)
     ap.add_argument("--prefill", action="store_true", help="time pa_prefill on the chunked-prefill batch instead")
+    ap.add_argument("--prefix", action="store_true", help="time prompt admission with and without prefix caching")
     ap.add_argument("--sweep", default=None, metavar="KEYS",
                     help="time pa_decode on each listed workload instead (comma list of 0,1,1x,2,3,3c,4 or 'all')")
     args = ap.parse_args()
+    if args.prefix:
+        prefix_bench()
+        return
     if args.prefill:
         prefill_bench()
         return

@@ -108,6 +108,62 @@ class PagedKVEngine:
             pa_cache_append(k, v, sd, self.k_cache, self.v_cache, stream=self._stream())
         return slots
 
+    # -- prefix caching ----------------------------------------------------------------------
+    def add_seq_cached(self, seq: int, tokens):
+        """Admit a prompt by its token ids, reusing cached blocks of an identical prefix.
+
+        Returns (n_cached, slots): the first n_cached tokens are already in the cache;
+        the caller computes only the remaining tokens' K/V rows and writes them with
+        write_rows(slots, k, v)."""
+        return self.bm.add_seq_cached(seq, tokens)
+
+    def _upload_ints(self, *arrays) -> list:
+        """Stage int32 host arrays in one pinned buffer, one async copy; returns
+        device views in order (large uploads fall back to a plain copy)."""
+        sizes = [int(np.size(a)) for a in arrays]
+        total = sum(sizes)
+        if total > self._pin[0].numel():
+            return [torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(self.device) for a in arrays]
+        i = self._stage()
+        buf = self._pin_np[i]
+        off = 0
+        for a, n in zip(arrays, sizes):
+            buf[off:off + n] = np.ravel(a)
+            off += n
+        dev = self._upload(i, total)
+        views, off = [], 0
+        for a, n in zip(arrays, sizes):
+            views.append(dev[off:off + n].view(np.shape(a)))
+            off += n
+        return views
+
+    def write_rows(self, slots, k_rows, v_rows) -> None:
+        if len(slots) == 0:
+            return
+        k = to_device_rows(k_rows, self.dtype, self.device)
+        v = to_device_rows(v_rows, self.dtype, self.device)
+        (sd,) = self._upload_ints(np.asarray(slots, dtype=np.int32))
+        pa_cache_append(k, v, sd, self.k_cache, self.v_cache, stream=self._stream())
+
+    def _apply(self, slots, copies, k_rows, v_rows) -> None:
+        st = self._stream()
+        if len(copies):
+            pa_copy_blocks(self.k_cache, self.v_cache, torch.from_numpy(np.ascontiguousarray(copies)).to(self.device),
+                           stream=st)
+        self.write_rows(slots, k_rows, v_rows)
+
+    def extend_tokens(self, seq: int, tokens, k_rows, v_rows):
+        """extend() with the token ids, so blocks it fills become reusable."""
+        slots, copies = self.bm.extend_tokens(seq, tokens)
+        self._apply(slots, copies, k_rows, v_rows)
+        return slots, copies
+
+    def step_tokens(self, seqs, tokens, k_rows, v_rows):
+        """step() with the token id appended to each sequence."""
+        slots, copies = self.bm.step_tokens(seqs, tokens)
+        self._apply(slots, copies, k_rows, v_rows)
+        return slots, copies
+
     def fork(self, parent: int, child: int) -> None:
         self.bm.fork(parent, child)
 
@@ -159,10 +215,8 @@ class PagedKVEngine:
         self.bm.block_tables_into(ids, mb, tables, lens)
         qs = np.zeros(n + 1, np.int32)
         qs[1:] = np.cumsum(np.asarray(counts, np.int64))
-        dev = self.device
-        pa_prefill(q, self.k_cache, self.v_cache, torch.from_numpy(tables[:n]).to(dev),
-                   torch.from_numpy(lens[:n]).to(dev), torch.from_numpy(qs).to(dev), scale, out,
-                   stream=self._stream())
+        td, ld, qd = self._upload_ints(tables[:n], lens[:n], qs)
+        pa_prefill(q, self.k_cache, self.v_cache, td, ld, qd, scale, out, stream=self._stream())
         return out
 
     def attend(self, seqs, q, scale: float, out=None, params=None) -> torch.Tensor:
@@ -215,9 +269,10 @@ class PagedKVEngine:
 
 
 def run_workload_ops(engine: PagedKVEngine, w, attend_params=None):
-    """Replay a workload op list through the engine. Returns {attend op index: out}."""
+    """Replay a workload op list through the engine. Returns ({attend / prefill op
+    index: out}, trace); token-driven admissions record ``trace["n_cached"][seq]``."""
     outs = {}
-    trace = {}
+    trace = {"n_cached": {}}
     for i, op in enumerate(w.ops):
         kind = op[0]
         if kind == "add":
@@ -237,6 +292,27 @@ def run_workload_ops(engine: PagedKVEngine, w, attend_params=None):
             trace[i] = {"slots": slots.tolist(), "copies": [tuple(c) for c in copies.tolist()]}
         elif kind == "prefill":
             outs[i] = engine.prefill(op[1], op[2], w.query(i), w.scale)
+        elif kind == "add_tokens":
+            n_cached, slots = engine.add_seq_cached(op[1], op[2])
+            trace["n_cached"][op[1]] = n_cached
+            trace[i] = {"slots": slots.tolist(), "copies": [], "n_cached": n_cached}
+            if len(slots):
+                k, v = w.token_rows(i)
+                engine.write_rows(slots, k[n_cached:], v[n_cached:])
+        elif kind in ("extend_tokens", "step_tokens"):
+            k, v = w.token_rows(i)
+            if kind == "extend_tokens":
+                slots, copies = engine.extend_tokens(op[1], op[2], k, v)
+            else:
+                slots, copies = engine.step_tokens(op[1], op[2], k, v)
+            trace[i] = {"slots": slots.tolist(), "copies": [tuple(c) for c in copies.tolist()]}
+        elif kind == "prefill_new":
+            seqs = list(op[1])
+            lens = [engine.bm.seq_info(s)[0] for s in seqs]
+            counts = [lens[j] - trace["n_cached"][s] for j, s in enumerate(seqs)]
+            qs = w.position_queries(i)
+            q = np.concatenate([qs[j][lens[j] - counts[j]:lens[j]] for j in range(len(seqs))])
+            outs[i] = engine.prefill(seqs, counts, q, w.scale)
         elif kind == "attend":
             outs[i] = engine.attend(op[1], w.query(i), w.scale, params=attend_params)
         else:

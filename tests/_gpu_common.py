@@ -58,6 +58,7 @@ def run_both(pa, w, params=None, keep_seqs=None, compare_cache=True):
     assert pa.pa_get_device_status() == 0
     ref = replay(w, keep_seqs=keep_seqs)
     # host block manager: every slot and copy pair, then the final state
+    assert trace.pop("n_cached") == ref.n_cached
     for i, t in trace.items():
         assert t["slots"] == list(ref.trace[i]["slots"]), f"slots differ at op {i}"
         assert t["copies"] == [tuple(c) for c in ref.trace[i]["copies"]], f"copies differ at op {i}"
@@ -65,6 +66,8 @@ def run_both(pa, w, params=None, keep_seqs=None, compare_cache=True):
     assert eng.bm.ref_counts() == ref.bm.refs
     for s, tab in ref.bm.tables.items():
         assert eng.bm.table(s) == tab
+    if hasattr(ref.bm, "cached_frames"):
+        assert eng.bm.cached_frames() == ref.bm.cached_frames()
     if compare_cache:
         if keep_seqs is None:
             assert np.array_equal(cache_bits(eng.k_cache), oracle_bits(ref.cache.k))
