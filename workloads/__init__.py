@@ -9,9 +9,11 @@ attention computation).  Each side replays a :class:`Workload` with its own code
 from .gen import (  # noqa: F401
     DTYPES,
     Workload,
+    beam_search,
     build,
     chunked_prefill,
     custom,
+    mcts_tree,
     prefill_batch,
     prefix_ids,
     shared_prefix,

@@ -393,6 +393,109 @@ def prefill_batch(small: bool = False) -> Workload:
                            name="chunked prefill: 16 seqs, prefix~U[0,3072], chunk 512, H=32, D=128, B=16, f16")
 
 
+def beam_search(n_prompts: int, prompt_len: int, width: int, steps: int, *, H=2, D=128, B=16, dtype="f16",
+                sigma=1.0, seed=31, attend_every: int = 1, name=None) -> Workload:
+    """Beam search over forked sequences.
+
+    Each prompt is admitted, then forked into ``width`` beams.  Every step appends
+    one token to every live beam (prompts in order, beams in order) and, every
+    ``attend_every`` steps, attends all of them; then each prompt keeps ``width``
+    survivors drawn uniformly with replacement from its beams: a beam drawn c times
+    continues and forks c-1 children, a beam never drawn is freed.
+    """
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0])))
+    ops, beams, final = [], [], {}
+    nid = 0
+    for p in range(n_prompts):
+        root = nid
+        nid += 1
+        ops.append(("add", root, prompt_len))
+        final[root] = prompt_len
+        group = [root]
+        for _ in range(width - 1):
+            ops.append(("fork", root, nid))
+            final[nid] = prompt_len
+            group.append(nid)
+            nid += 1
+        beams.append(group)
+    for t in range(steps):
+        live = tuple(s for g in beams for s in g)
+        ops.append(("step", live))
+        for s in live:
+            final[s] += 1
+        if (t + 1) % attend_every == 0 or t + 1 == steps:
+            ops.append(("attend", live))
+        if t + 1 == steps:
+            break
+        for p in range(n_prompts):
+            counts = rng.multinomial(width, np.full(width, 1.0 / width))
+            new = []
+            for beam, c in zip(beams[p], counts):
+                if c == 0:
+                    ops.append(("free", beam))
+                    continue
+                new.append(beam)
+                for _ in range(int(c) - 1):
+                    ops.append(("fork", beam, nid))
+                    final[nid] = final[beam]
+                    new.append(nid)
+                    nid += 1
+            beams[p] = new
+    per_beam = -(-(steps + B) // B) + 1
+    nb = int(math.ceil(1.2 * n_prompts * (-(-prompt_len // B) + 2 * width * per_beam)))
+    free_order = rng.permutation(nb).astype(np.int32)
+    return Workload(name=name or f"beam search: {n_prompts} prompts x {prompt_len}, width {width}, {steps} steps, "
+                                 f"H={H}, D={D}, B={B}, {dtype}",
+                    num_heads=H, head_dim=D, block_size=B, dtype=dtype, sigma=sigma, num_blocks=nb,
+                    free_order=free_order, ops=ops, seed=seed, final_lens=final)
+
+
+def mcts_tree(n_roots: int, prompt_len: int, iterations: int, *, batch: int = 4, rollout_max: int = 24,
+              max_nodes: int = 48, H=2, D=128, B=16, dtype="f16", sigma=1.0, seed=41, name=None) -> Workload:
+    """Monte Carlo tree search over forked sequences.
+
+    Every iteration picks ``batch`` live nodes at random (with replacement), forks
+    each into a new child, extends the child by r ~ U{1..rollout_max} tokens (a
+    chunk: copy-on-write of a shared tail, then new frames), and attends all new
+    children; while more than ``max_nodes`` nodes live, random non-root nodes are
+    freed (their children keep the frames they share).
+    """
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0])))
+    ops, final, live, roots = [], {}, [], set()
+    nid = 0
+    for _ in range(n_roots):
+        ops.append(("add", nid, prompt_len))
+        final[nid] = prompt_len
+        live.append(nid)
+        roots.add(nid)
+        nid += 1
+    for _ in range(iterations):
+        kids = []
+        for parent in rng.choice(live, size=batch):
+            parent = int(parent)
+            ops.append(("fork", parent, nid))
+            r = int(rng.integers(1, rollout_max + 1))
+            ops.append(("extend", nid, r))
+            final[nid] = final[parent] + r
+            kids.append(nid)
+            nid += 1
+        live += kids
+        ops.append(("attend", tuple(kids)))
+        while len(live) > max_nodes:
+            cand = [s for s in live if s not in roots]
+            victim = int(rng.choice(cand))
+            ops.append(("free", victim))
+            live.remove(victim)
+    longest = max(final.values())
+    nb = int(math.ceil(1.2 * (n_roots * -(-prompt_len // B) + (max_nodes + batch) * (-(-longest // B) - 
+                                                                                    prompt_len // B + 2))))
+    free_order = rng.permutation(nb).astype(np.int32)
+    return Workload(name=name or f"MCTS: {n_roots} roots x {prompt_len}, {iterations} iterations x {batch} "
+                                 f"rollouts <= {rollout_max}, <= {max_nodes} nodes, H={H}, D={D}, B={B}, {dtype}",
+                    num_heads=H, head_dim=D, block_size=B, dtype=dtype, sigma=sigma, num_blocks=nb,
+                    free_order=free_order, ops=ops, seed=seed, final_lens=final)
+
+
 def shared_prefix(n_requests: int, system_len: int, user_lens, *, H=2, D=128, B=16, dtype="f16", sigma=1.0,
                   seed=21, turns: int = 1, reply_len: int = 0, free_between: bool = False, pool=None,
                   name=None) -> Workload:
