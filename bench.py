@@ -720,6 +720,87 @@ def prefix_bench(n_requests=16, system_len=2048, user_len=512, reps=10):
     print(json.dumps(line), flush=True)
 
 
+def fork_tree_bench(n_prompts=8, prompt_len=2048, width=8, steps=64):
+    """Beam search over forked sequences, the whole step loop on one GPU: host block
+    manager (step with copy-on-write, then the selection's forks and frees), staged
+    upload, pa_copy_blocks, pa_cache_append and pa_decode over every live beam.
+    One JSON line: step time end to end, decode time (CUDA events), decode GB/s of
+    logical bytes (what the beams attend) and of the unique frames they hold."""
+    import time
+
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_126_gb300 as pa
+    import workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    st = torch.cuda.current_stream(dev)
+    H, D, B, dtype = 32, 128, 16, "f16"
+    w = workloads.beam_search(n_prompts, prompt_len, width, steps, H=H, D=D, B=B, dtype=dtype, seed=77)
+    nbeams = n_prompts * width
+    mb = -(-(prompt_len + steps) // B)
+    g = torch.Generator(device=dev).manual_seed(9)
+    prompt_k = torch.randn((prompt_len, H, D), generator=g, device=dev).to(torch.float16)
+    prompt_v = torch.randn((prompt_len, H, D), generator=g, device=dev).to(torch.float16)
+    step_k = torch.randn((nbeams, H, D), generator=g, device=dev).to(torch.float16)
+    step_v = torch.randn((nbeams, H, D), generator=g, device=dev).to(torch.float16)
+    q = torch.randn((nbeams, H, D), generator=g, device=dev).to(torch.float16)
+    out = torch.empty_like(q)
+    scale = 1.0 / float(np.sqrt(D))
+    row = 2 * H * D * 2  # K + V bytes of one token of one sequence
+
+    def run(record):
+        eng = pa.PagedKVEngine(w.num_blocks, B, H, D, dtype, free_order=w.free_order, device=dev,
+                               max_seqs=nbeams, max_blocks_per_seq=mb)
+        ops = w.ops
+        stats = []
+        i = 0
+        while i < len(ops):
+            op = ops[i]
+            if op[0] == "add":
+                eng.add_seq(op[1], prompt_k, prompt_v)
+            elif op[0] == "fork":
+                eng.fork(op[1], op[2])
+            elif op[0] == "free":
+                eng.free(op[1])
+            elif op[0] == "step":
+                live = op[1]
+                assert ops[i + 1][0] == "attend" and ops[i + 1][1] == live
+                e = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+                _, nc, lens = eng.decode_step(live, step_k, step_v, q, scale, out=out, events=e)
+                if record:
+                    tables, ln = eng.bm.block_tables(live, mb)
+                    unique = len(set(tables[tables >= 0].tolist()))
+                    stats.append((e, int(ln.sum()) * row, unique * B * row, nc))
+                else:
+                    stats.append((e, 0, 0, nc))
+                i += 1
+            i += 1
+        torch.cuda.synchronize()
+        return stats
+
+    run(False)
+    t0 = time.perf_counter()
+    n_steps = len(run(False))
+    total = time.perf_counter() - t0
+    stats = run(True)  # decode events and byte counts (host bookkeeping kept out of the timed run)
+    dec = np.array([e[0].elapsed_time(e[1]) / 1e3 for e, *_ in stats])
+    logical = np.array([x[1] for x in stats], np.float64)
+    unique = np.array([x[2] for x in stats], np.float64)
+    copies = int(sum(x[3] for x in stats))
+    print(json.dumps({
+        "metric": "beam-search decode step over forked sequences (block manager + copy-on-write + append + decode)",
+        "workload": w.name, "beams": nbeams, "steps": len(stats),
+        "ms_per_step_e2e": round(total / n_steps * 1e3, 3),
+        "decode_us_median": round(float(np.median(dec)) * 1e6, 2),
+        "decode_gbs_logical": round(float(np.sum(logical) / np.sum(dec)) / 1e9, 1),
+        "decode_gbs_unique_frames": round(float(np.sum(unique) / np.sum(dec)) / 1e9, 1),
+        "logical_over_unique_bytes": round(float(np.sum(logical) / np.sum(unique)), 2),
+        "cow_copies": copies, "cow_copies_per_step": round(copies / len(stats), 2)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -735,11 +816,15 @@ def main():
     ap.add_argument("--cpu-worker", default=None)
     ap.add_argument("--prefill", action="store_true", help="time pa_prefill on the chunked-prefill batch instead")
     ap.add_argument("--prefix", action="store_true", help="time prompt admission with and without prefix caching")
+    ap.add_argument("--fork-trees", action="store_true", help="time the beam-search step loop over forked sequences")
     ap.add_argument("--sweep", default=None, metavar="KEYS",
                     help="time pa_decode on each listed workload instead (comma list of 0,1,1x,2,3,3c,4 or 'all')")
     args = ap.parse_args()
     if args.prefix:
         prefix_bench()
+        return
+    if args.fork_trees:
+        fork_tree_bench()
         return
     if args.prefill:
         prefill_bench()
