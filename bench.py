@@ -801,6 +801,86 @@ def fork_tree_bench(n_prompts=8, prompt_len=2048, width=8, steps=64):
         "cow_copies": copies, "cow_copies_per_step": round(copies / len(stats), 2)}), flush=True)
 
 
+def block_sweep(blocks=(8, 16, 32, 64, 128, 256), reps=20):
+    """Block size B against throughput, one JSON line per B: pa_decode on the decode
+    batch's lengths (64 sequences, L ~ U[512, 2048], H=32, D=128, fp16; GB/s of
+    algorithmic bytes) and pa_prefill on the chunked-prefill batch's shapes (16 x
+    512-token chunks after prefixes ~U[0, 3072]; TFLOP/s of causal FLOPs; B <= 128).
+    Caches are filled on the device; frames come from a shuffled free list."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_126_gb300 as pa
+    import workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    st = torch.cuda.current_stream(dev)
+    H, D = 32, 128
+    dec_lens = [w_L for w_L in workloads.build(1).final_lens.values()]
+    pw = workloads.prefill_batch()
+    (pop,) = pw.prefill_ops
+    pre_lens = [pw.final_lens[s] - n for s, n in zip(pw.ops[pop][1], pw.ops[pop][2])]
+    chunks = list(pw.ops[pop][2])
+    g = torch.Generator(device=dev).manual_seed(11)
+
+    def engine(lengths, B):
+        need = sum(-(-L // B) for L in lengths)
+        nb = int(1.2 * need) + 1
+        order = np.random.Generator(np.random.PCG64(B)).permutation(nb).astype(np.int32)
+        eng = pa.PagedKVEngine(nb, B, H, D, "f16", free_order=order, device=dev, max_seqs=len(lengths),
+                               max_blocks_per_seq=max(-(-L // B) for L in lengths))
+        for s, L in enumerate(lengths):
+            eng.bm.add_seq(s, L)
+        eng.k_cache.normal_(generator=g)
+        eng.v_cache.normal_(generator=g)
+        return eng
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            fn()
+        e1.record(st)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / reps
+
+    for B in blocks:
+        line = {"metric": "block size sweep", "B": B}
+        eng = engine(dec_lens, B)
+        S = len(dec_lens)
+        ids = list(range(S))
+        tables, lens = eng.bm.block_tables(ids, eng.max_blocks)
+        td, ld = torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev)
+        q = torch.randn((S, H, D), generator=g, device=dev).to(torch.float16)
+        out = torch.empty_like(q)
+        try:
+            t = timed(lambda: pa.pa_decode(q, eng.k_cache, eng.v_cache, td, ld, 0.0883883, out))
+        except pa.PAError as e:
+            line["decode"] = f"unsupported: {e}"
+        else:
+            byts = sum(2 * L * H * D * 2 + 4 * -(-L // B) for L in dec_lens) + 4 * S + 2 * S * H * D * 2
+            line.update({"decode_us": round(t * 1e6, 2), "decode_gbs": round(byts / t / 1e9, 1)})
+        del eng
+        if B <= 128:
+            eng = engine([a + b for a, b in zip(pre_lens, chunks)], B)
+            S = len(chunks)
+            ids = list(range(S))
+            tables, lens = eng.bm.block_tables(ids, eng.max_blocks)
+            qs = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+            td, ld, qd = (torch.from_numpy(x).to(dev) for x in (tables, lens, qs))
+            qq = torch.randn((int(qs[-1]), H, D), generator=g, device=dev).to(torch.float16)
+            oo = torch.empty_like(qq)
+            t = timed(lambda: pa.pa_prefill(qq, eng.k_cache, eng.v_cache, td, ld, qd, 0.0883883, oo))
+            fl = prefill_flops(pre_lens, chunks, H, D)
+            line.update({"prefill_us": round(t * 1e6, 2), "prefill_tflops": round(fl / t / 1e12, 1)})
+            del eng
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -817,6 +897,7 @@ def main():
     ap.add_argument("--prefill", action="store_true", help="time pa_prefill on the chunked-prefill batch instead")
     ap.add_argument("--prefix", action="store_true", help="time prompt admission with and without prefix caching")
     ap.add_argument("--fork-trees", action="store_true", help="time the beam-search step loop over forked sequences")
+    ap.add_argument("--block-sweep", action="store_true", help="decode and prefill throughput against block size")
     ap.add_argument("--sweep", default=None, metavar="KEYS",
                     help="time pa_decode on each listed workload instead (comma list of 0,1,1x,2,3,3c,4 or 'all')")
     args = ap.parse_args()
@@ -825,6 +906,9 @@ def main():
         return
     if args.fork_trees:
         fork_tree_bench()
+        return
+    if args.block_sweep:
+        block_sweep()
         return
     if args.prefill:
         prefill_bench()
