@@ -31,7 +31,7 @@ from .block_manager import (  # noqa: F401
     SequenceExists,
     DOUBLE_FREE,
 )
-from .cache import OracleKVCache, decode_storage  # noqa: F401
+from .cache import OracleKVCache, decode_storage, split_layout  # noqa: F401
 from .attention import (  # noqa: F401
     attention_fp64,
     paged_decode,

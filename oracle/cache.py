@@ -65,3 +65,16 @@ class OracleKVCache:
     def frame(self, which: str, b: int) -> np.ndarray:
         arr = self.k if which == "k" else self.v
         return arr[b]
+
+
+def split_layout(k: np.ndarray, v: np.ndarray, elem_bytes: int):
+    """The kernel-side cache layout of "PagedAttention: Virtual Memory Guide for LLM
+    Inference", "3. PagedAttention CUDA Kernel Execution" (the conceptual kernel
+    signature): K as [num_blocks, heads, head_dim/x, block_size, x] and V as
+    [num_blocks, heads, head_dim, block_size], x = elements per 16 bytes, holding the
+    same values as the [num_blocks, block_size, heads, head_dim] caches."""
+    nb, B, H, D = k.shape
+    x = 16 // elem_bytes
+    ks = k.reshape(nb, B, H, D // x, x).transpose(0, 2, 3, 1, 4)
+    vs = v.transpose(0, 2, 3, 1)
+    return np.ascontiguousarray(ks), np.ascontiguousarray(vs)

@@ -227,3 +227,31 @@ def test_round_to_f16_nearest_even():
         cands = [np.nextafter(h, np.float16(-np.inf)), h, np.nextafter(h, np.float16(np.inf))]
         best = min(cands, key=lambda c: (abs(float(c) - x), int(c.view(np.uint16)) & 1))
         assert g == float(best)
+
+
+# ------------------------------------------------------------------ split cache layout
+def test_split_layout_matches_the_printed_shapes():
+    """[VM] "3. PagedAttention CUDA Kernel Execution" prints k_cache as
+    [num_blocks, num_heads, head_dim/x, block_size, x] and v_cache as
+    [num_blocks, num_heads, head_dim, block_size].  Row-major byte offsets of those
+    shapes (closed form) locate, in the arrays split_layout returns, exactly the
+    element k[f, b, h, d] (v[f, b, h, d]) of the [nb, B, H, D] caches."""
+    import numpy as np
+
+    from oracle import split_layout
+
+    rng = np.random.default_rng(3)
+    for dtype, e in ((np.float16, 2), (np.float32, 4)):
+        nb, B, H, D = 5, 16, 3, 64
+        x = 16 // e
+        k = rng.standard_normal((nb, B, H, D)).astype(dtype)
+        v = rng.standard_normal((nb, B, H, D)).astype(dtype)
+        ks, vs = split_layout(k, v, e)
+        assert ks.shape == (nb, H, D // x, B, x) and vs.shape == (nb, H, D, B)
+        kb, vb = ks.tobytes(), vs.tobytes()
+        for _ in range(200):
+            f, b, h, d = (int(rng.integers(n)) for n in (nb, B, H, D))
+            ko = ((((f * H + h) * (D // x) + d // x) * B + b) * x + d % x) * e
+            vo = (((f * H + h) * D + d) * B + b) * e
+            assert np.frombuffer(kb[ko:ko + e], dtype)[0] == k[f, b, h, d]
+            assert np.frombuffer(vb[vo:vo + e], dtype)[0] == v[f, b, h, d]
