@@ -177,6 +177,25 @@ int pa_prefill(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_
                const pa_tensor* query_start, float scale, const pa_tensor* out,
                pa_stream stream);
 
+/* ---- the split cache layout ["PagedAttention: Virtual Memory Guide for LLM
+ * Inference", "3. PagedAttention CUDA Kernel Execution": the kernel signature stores
+ * k_cache as [num_blocks, num_heads, head_dim/x, block_size, x] and v_cache as
+ * [num_blocks, num_heads, head_dim, block_size], x = elements per 16 bytes].
+ *
+ * Same contract as pa_cache_append / pa_decode with the caches in that layout:
+ * k_cache passed as the 4-D view [num_blocks, H, D/8, B*8] (each last-dim row holds
+ * B chunks of 8 elements), v_cache as [num_blocks, H, D, B]; both contiguous, fp16 or
+ * bf16, D in {64, 128}, B in {8, 16, 32}, H a multiple of 4 (else
+ * PA_ERR_UNSUPPORTED).  pa_decode_split splits long contexts into partitions when the
+ * (sequence, 4-head group) items cannot fill the GPU and then launches a second,
+ * merging kernel; its partials use the (device, stream) workspace.  Status bits and
+ * error codes as for pa_decode. */
+int pa_cache_append_split(const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* slot_mapping,
+                          const pa_tensor* k_cache, const pa_tensor* v_cache, pa_stream stream);
+int pa_decode_split(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                    const pa_tensor* block_tables, const pa_tensor* context_lens, float scale,
+                    const pa_tensor* out, pa_stream stream);
+
 /* Launch options for pa_decode_ex; 0 in any field = automatic choice. */
 typedef struct pa_decode_params {
   int32_t partition_tokens;  /* >0: split context into partitions of this many tokens

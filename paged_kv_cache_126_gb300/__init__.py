@@ -21,11 +21,14 @@ from ._binding import (  # noqa: F401
     PA_ERR_SCRATCH_LIMIT,
     PA_ERR_SEQ_EXISTS,
     PA_ERR_UNKNOWN_SEQ,
+    PA_ERR_UNSUPPORTED,
     PA_WARN_DOUBLE_FREE,
     pa_cache_append,
+    pa_cache_append_split,
     pa_copy_blocks,
     pa_decode,
     pa_decode_ex,
+    pa_decode_split,
     pa_decode_static,
     pa_prefill,
     pa_get_device_status,

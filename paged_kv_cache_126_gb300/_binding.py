@@ -22,6 +22,7 @@ PA_ERR_OUT_OF_BLOCKS = -6
 PA_ERR_UNKNOWN_SEQ = -7
 PA_ERR_SEQ_EXISTS = -8
 PA_ERR_SCRATCH_LIMIT = -12
+PA_ERR_UNSUPPORTED = -10
 
 PA_DEV_BAD_SLOT = 0x1
 PA_DEV_BAD_BLOCK = 0x2
@@ -64,6 +65,8 @@ def _load():
         "pa_decode_ex": ([P, P, P, P, P, C.c_float, P, C.POINTER(PaDecodeParams), vp], C.c_int),
         "pa_decode_static": ([P, P, P, P, P, C.c_float, P, vp], C.c_int),
         "pa_prefill": ([P, P, P, P, P, P, C.c_float, P, vp], C.c_int),
+        "pa_cache_append_split": ([P, P, P, P, P, vp], C.c_int),
+        "pa_decode_split": ([P, P, P, P, P, C.c_float, P, vp], C.c_int),
         "pa_get_device_status": ([vp, i32p], C.c_int),
         "pa_strerror": ([C.c_int], C.c_char_p),
         "pa_launch_count": ([], C.c_int64),
@@ -99,6 +102,7 @@ def _load():
 LIB = _load()
 EXPORTED = (
     "pa_cache_append", "pa_copy_blocks", "pa_decode", "pa_decode_ex", "pa_decode_static", "pa_prefill",
+    "pa_cache_append_split", "pa_decode_split",
     "pa_get_device_status",
     "pa_strerror", "pa_launch_count", "pa_shutdown", "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq",
     "pa_bm_append", "pa_bm_step", "pa_bm_extend", "pa_bm_fork", "pa_bm_free", "pa_bm_block_tables", "pa_bm_seq_info",
@@ -204,6 +208,23 @@ def pa_prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, sca
     ds = [tensor_desc(t) for t in (q, k_cache, v_cache, block_tables, context_lens, query_start)]
     o = tensor_desc(out)
     _check(LIB.pa_prefill(*map(_ref, ds), C.c_float(scale), C.byref(o), st), "pa_prefill")
+    return out
+
+
+def pa_cache_append_split(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None):
+    """Cache append into the split layout (see include/pa.h); k_cache is the 4-D view
+    [num_blocks, H, D/8, B*8] of [num_blocks, H, D/8, B, 8]."""
+    st = _stream_of(k_new, stream)
+    ds = [tensor_desc(t) for t in (k_new, v_new, slot_mapping, k_cache, v_cache)]
+    _check(LIB.pa_cache_append_split(*map(_ref, ds), st), "pa_cache_append_split")
+
+
+def pa_decode_split(q, k_cache, v_cache, block_tables, context_lens, scale, out, stream=None):
+    """Decode attention over the split layout (see include/pa.h)."""
+    st = _stream_of(q, stream)
+    ds = [tensor_desc(t) for t in (q, k_cache, v_cache, block_tables, context_lens)]
+    o = tensor_desc(out)
+    _check(LIB.pa_decode_split(*map(_ref, ds), C.c_float(scale), C.byref(o), st), "pa_decode_split")
     return out
 
 

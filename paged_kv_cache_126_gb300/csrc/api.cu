@@ -330,6 +330,126 @@ int pa_cache_append(const pa_tensor* k_new, const pa_tensor* v_new, const pa_ten
   return PA_OK;
 }
 
+// ---- the split cache layout ---------------------------------------------------------------
+// k_cache viewed as [nb, H, D/x, B*x], v_cache as [nb, H, D, B], both contiguous, fp16/bf16.
+static int check_split_caches(const pa_tensor* k, const pa_tensor* v, int64_t* nb, int64_t* H, int64_t* D,
+                              int64_t* B) {
+  if (!k || !v || !k->data || !v->data) return PA_ERR_INVALID;
+  if (k->dtype != v->dtype || (k->dtype != PA_F16 && k->dtype != PA_BF16)) return PA_ERR_DTYPE;
+  if (k->ndim != 4 || v->ndim != 4) return PA_ERR_SHAPE;
+  const int64_t x = 8;
+  *nb = v->shape[0];
+  *H = v->shape[1];
+  *D = v->shape[2];
+  *B = v->shape[3];
+  if (k->shape[0] != *nb || k->shape[1] != *H || k->shape[2] * x != *D || k->shape[3] != *B * x) return PA_ERR_SHAPE;
+  for (const pa_tensor* t : {k, v}) {
+    int64_t want = 1;
+    for (int i = 3; i >= 0; --i) {
+      if (t->shape[i] > 1 && t->stride[i] != want) return PA_ERR_STRIDE;
+      want *= t->shape[i];
+    }
+    if (!aligned16(t->data)) return PA_ERR_ALIGN;
+  }
+  if (*nb <= 0 || *H <= 0) return PA_ERR_SHAPE;
+  if (!(*D == 64 || *D == 128) || !(*B == 8 || *B == 16 || *B == 32) || *H % 4 != 0) return PA_ERR_UNSUPPORTED;
+  if (*nb * *B > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+int pa_cache_append_split(const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* slot_mapping,
+                          const pa_tensor* k_cache, const pa_tensor* v_cache, pa_stream stream) {
+  int64_t nb, H, D, B;
+  PA_TRY(check_split_caches(k_cache, v_cache, &nb, &H, &D, &B));
+  const int dt = k_cache->dtype;
+  PA_TRY(check_rows(k_new, dt, H, D));
+  PA_TRY(check_rows(v_new, dt, H, D));
+  if (!slot_mapping) return PA_ERR_INVALID;
+  PA_TRY(check_i32(slot_mapping, 1));
+  const int64_t T = k_new->shape[0];
+  if (v_new->shape[0] != T || slot_mapping->shape[0] != T) return PA_ERR_SHAPE;
+  if (T > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (T == 0) return PA_OK;
+  int dev;
+  PA_TRY(current_device(&dev));
+  const int64_t units = T * H * (D / 8);
+  const int grid = static_cast<int>(std::min<int64_t>((units + 255) / 256, 16LL * g_dev[dev].num_sms));
+  if (pa::launch_append_split(dt, k_new->data, v_new->data, k_new->stride[0], v_new->stride[0],
+                              static_cast<const int32_t*>(slot_mapping->data), static_cast<int32_t>(T),
+                              static_cast<int32_t>(H), static_cast<int32_t>(D), static_cast<int32_t>(B),
+                              static_cast<int32_t>(nb), k_cache->data, v_cache->data, g_dev[dev].status, grid,
+                              static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return PA_OK;
+}
+
+int pa_decode_split(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                    const pa_tensor* block_tables, const pa_tensor* context_lens, float scale, const pa_tensor* out,
+                    pa_stream stream) {
+  int64_t nb, H, D, B;
+  PA_TRY(check_split_caches(k_cache, v_cache, &nb, &H, &D, &B));
+  const int dt = k_cache->dtype;
+  PA_TRY(check_rows(q, dt, H, D));
+  PA_TRY(check_rows(out, dt, H, D));
+  if (!block_tables || !context_lens) return PA_ERR_INVALID;
+  PA_TRY(check_i32(block_tables, 2));
+  PA_TRY(check_i32(context_lens, 1));
+  const int64_t S = q->shape[0];
+  if (out->shape[0] != S || block_tables->shape[0] != S || context_lens->shape[0] != S) return PA_ERR_SHAPE;
+  const int64_t max_blocks = block_tables->shape[1];
+  if (max_blocks < 0 || (S > 1 && block_tables->stride[0] < max_blocks)) return PA_ERR_STRIDE;
+  if (max_blocks * B > INT32_MAX || S * H > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (S == 0) return PA_OK;
+  int dev;
+  PA_TRY(current_device(&dev));
+  const int sms = g_dev[dev].num_sms;
+  // context partitions only when (sequence, head group) items cannot fill the GPU
+  const int64_t groups = H / 4, cap = std::max<int64_t>(max_blocks * B, B);
+  int64_t P = cap, NP = 1;
+  if (S * groups < 2LL * sms) {
+    const int64_t want = (2LL * sms + S * groups - 1) / (S * groups);
+    P = std::max<int64_t>(256, ((cap + want - 1) / want + B - 1) / B * B);
+    NP = (cap + P - 1) / P;
+  }
+  if (S * groups * NP > INT32_MAX / 4) return PA_ERR_UNSUPPORTED;
+  pa::SplitArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = q->data;
+  a.out = out->data;
+  a.q_row = q->stride[0];
+  a.out_row = out->stride[0];
+  a.k_cache = k_cache->data;
+  a.v_cache = v_cache->data;
+  a.block_tables = static_cast<const int32_t*>(block_tables->data);
+  a.bt_row = block_tables->stride[0];
+  a.context_lens = static_cast<const int32_t*>(context_lens->data);
+  a.S = static_cast<int32_t>(S);
+  a.H = static_cast<int32_t>(H);
+  a.num_blocks = static_cast<int32_t>(nb);
+  a.max_blocks = static_cast<int32_t>(max_blocks);
+  a.P = static_cast<int32_t>(P);
+  a.NP = static_cast<int32_t>(NP);
+  a.qk_scale_log2 = scale * 1.4426950408889634f;
+  a.status = g_dev[dev].status;
+  const size_t items = static_cast<size_t>(S * groups * NP);
+  const size_t rest = NP > 1 ? items * 4 * (2 + static_cast<size_t>(D)) * sizeof(float) : 0;
+  void* ws = nullptr;
+  size_t cnt_bytes = 0;
+  PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), 0, rest, &ws, &cnt_bytes));
+  a.sched = static_cast<int32_t*>(ws);
+  if (NP > 1) {
+    float* base = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kSchedBytes + cnt_bytes);
+    a.ws_ml = base;
+    a.ws_o = base + items * 4 * 2;
+  }
+  if (pa::launch_decode_split(dt, static_cast<int>(D), static_cast<int>(B), a, sms,
+                              static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  g_launches.fetch_add(NP > 1 ? 2 : 1);
+  return PA_OK;
+}
+
 int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_tensor* pairs, pa_stream stream) {
   PA_TRY(check_cache(k_cache, v_cache));
   if (!pairs) return PA_ERR_INVALID;

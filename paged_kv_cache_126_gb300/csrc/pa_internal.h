@@ -104,6 +104,30 @@ cudaError_t launch_prefill_bf16(const PrefillArgs&, const CUtensorMap& tq, const
                                 const CUtensorMap& tv, int grid, cudaStream_t);
 size_t prefill_smem_bytes(int S, int unit_cap);
 
+// Decode over the split cache layout (k [nb, H, D/x, B, x], v [nb, H, D, B]).
+struct SplitArgs {
+  const void* q;                // [S, H, D], row stride q_row elements
+  void* out;                    // [S, H, D], row stride out_row elements
+  int64_t q_row, out_row;
+  const void* k_cache;          // [num_blocks, H, D/x, B, x]
+  const void* v_cache;          // [num_blocks, H, D, B]
+  const int32_t* block_tables;  // [S, max_blocks]
+  int64_t bt_row;
+  const int32_t* context_lens;  // [S]
+  int32_t S, H, num_blocks, max_blocks;
+  int32_t P, NP;                // tokens per partition (multiple of B), partitions per sequence
+  float qk_scale_log2;
+  int32_t* sched;               // [2] work counter, retired blocks (zero between launches)
+  float* ws_ml;                 // [S * H/4 * NP][4][2] partial (max, sum) when NP > 1
+  float* ws_o;                  // [S * H/4 * NP][4][D] partial unnormalised outputs
+  int32_t* status;
+};
+cudaError_t launch_decode_split(int dtype, int D, int B, const SplitArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_append_split(int dtype, const void* k_new, const void* v_new, int64_t k_row, int64_t v_row,
+                                const int32_t* slots, int32_t T, int32_t H, int32_t D, int32_t B,
+                                int32_t num_blocks, void* k_cache, void* v_cache, int32_t* status,
+                                int grid, cudaStream_t stream);
+
 // status bits (mirror pa.h)
 constexpr int32_t kDevBadSlot = 0x1;
 constexpr int32_t kDevBadBlock = 0x2;
