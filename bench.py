@@ -881,6 +881,67 @@ def block_sweep(blocks=(8, 16, 32, 64, 128, 256), reps=20):
         print(json.dumps(line), flush=True)
 
 
+def split_layout_bench(reps=20):
+    """The two cache layouts head to head, one JSON line per (workload, B): pa_decode
+    on [num_blocks, B, H, D] caches and pa_decode_split on the layout of the pages'
+    kernel signature (k [num_blocks, H, D/x, B, x], v [num_blocks, H, D, B]); same
+    lengths, same frames, caches filled on the device; GB/s of algorithmic bytes."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_126_gb300 as pa
+    import workloads
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    st = torch.cuda.current_stream(dev)
+    H, D = 32, 128
+    g = torch.Generator(device=dev).manual_seed(13)
+    cases = [("decode batch: 64 seqs, L~U[512,2048]", list(workloads.build(1).final_lens.values())),
+             ("long context: 4 x 16384", [16384] * 4)]
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            fn()
+        e1.record(st)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / reps
+
+    for name, lens in cases:
+        for B in (8, 16, 32):
+            S = len(lens)
+            need = sum(-(-L // B) for L in lens)
+            nb = int(1.2 * need) + 1
+            order = np.random.Generator(np.random.PCG64(B)).permutation(nb).astype(np.int32)
+            bm = pa.BlockManager(nb, B, order)
+            for s, L in enumerate(lens):
+                bm.add_seq(s, L)
+            mb = max(-(-L // B) for L in lens)
+            tables, ln = bm.block_tables(list(range(S)), mb)
+            td, ld = torch.from_numpy(tables).to(dev), torch.from_numpy(ln).to(dev)
+            q = torch.randn((S, H, D), generator=g, device=dev).to(torch.float16)
+            out = torch.empty_like(q)
+            byts = sum(2 * L * H * D * 2 + 4 * -(-L // B) for L in lens) + 4 * S + 2 * S * H * D * 2
+            line = {"metric": "cache layout: row [nb,B,H,D] vs split [nb,H,D/x,B,x]/[nb,H,D,B] decode",
+                    "workload": name, "B": B}
+            kc = torch.empty((nb, B, H, D), dtype=torch.float16, device=dev).normal_(generator=g)
+            vc = torch.empty((nb, B, H, D), dtype=torch.float16, device=dev).normal_(generator=g)
+            t = timed(lambda: pa.pa_decode(q, kc, vc, td, ld, 0.0883883, out))
+            line["row_gbs"] = round(byts / t / 1e9, 1)
+            del kc, vc
+            ks = torch.empty((nb, H, D // 8, B * 8), dtype=torch.float16, device=dev).normal_(generator=g)
+            vs = torch.empty((nb, H, D, B), dtype=torch.float16, device=dev).normal_(generator=g)
+            t = timed(lambda: pa.pa_decode_split(q, ks, vs, td, ld, 0.0883883, out))
+            line["split_gbs"] = round(byts / t / 1e9, 1)
+            del ks, vs
+            print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -898,6 +959,7 @@ def main():
     ap.add_argument("--prefix", action="store_true", help="time prompt admission with and without prefix caching")
     ap.add_argument("--fork-trees", action="store_true", help="time the beam-search step loop over forked sequences")
     ap.add_argument("--block-sweep", action="store_true", help="decode and prefill throughput against block size")
+    ap.add_argument("--split-layout", action="store_true", help="decode throughput of the two cache layouts")
     ap.add_argument("--sweep", default=None, metavar="KEYS",
                     help="time pa_decode on each listed workload instead (comma list of 0,1,1x,2,3,3c,4 or 'all')")
     args = ap.parse_args()
@@ -909,6 +971,9 @@ def main():
         return
     if args.block_sweep:
         block_sweep()
+        return
+    if args.split_layout:
+        split_layout_bench()
         return
     if args.prefill:
         prefill_bench()
