@@ -63,8 +63,10 @@ EncodeTiledFn encode_fn() {
   return g_encode;
 }
 
-// 3-D view [num_blocks*B, H, D] of a cache, box {D, hg, B}: one frame of hg heads.
-int make_cache_map(CUtensorMap* map, void* base, int dtype, int64_t nb, int64_t B, int64_t H, int64_t D, int hg) {
+// 3-D view [num_blocks*B, H, D] of a cache, box {D, hg, box_rows}: box_rows rows (a
+// frame, or a slice of one) of hg heads.
+int make_cache_map(CUtensorMap* map, void* base, int dtype, int64_t nb, int64_t B, int64_t H, int64_t D, int hg,
+                   int64_t box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return PA_ERR_CUDA;
   CUtensorMapDataType t = dtype == PA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -73,7 +75,7 @@ int make_cache_map(CUtensorMap* map, void* base, int dtype, int64_t nb, int64_t 
   const int64_t e = dtype == PA_F32 ? 4 : 2;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(nb * B)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * e), static_cast<cuuint64_t>(H * D * e)};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(hg), static_cast<cuuint32_t>(B)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(hg), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, t, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -236,10 +238,20 @@ bool combo_built(int hg, int wph) {
          (hg == 1 && (wph == 1 || wph == 2 || wph == 4 || wph == 8));
 }
 
+// Tokens per staged unit.  With 256-byte rows and B a power of two, the unrolled path
+// takes units of R = 16 * warps_per_head tokens (1 or 2 warps per head): R/B frames
+// share a stage when B < R, a frame is staged as B/R slices when B > R.  Otherwise a
+// unit is one frame.
+int64_t unit_rows(int64_t B, int wph, bool fast_rows) {
+  const int64_t R = 16 * wph;
+  if (fast_rows && (wph == 1 || wph == 2) && (R % B == 0 || B % R == 0)) return R;
+  return B;
+}
+
 }  // namespace
 
-size_t pa::decode_smem_bytes(const DecodeCfg& c, int elem, int B, int S) {
-  const uint32_t stage_bytes = 2u * static_cast<uint32_t>(B) * c.heads_per_cta * c.D * elem;
+size_t pa::decode_smem_bytes(const DecodeCfg& c, int elem, int R, int S) {
+  const uint32_t stage_bytes = 2u * static_cast<uint32_t>(R) * c.heads_per_cta * c.D * elem;
   const dk::Layout lay(c.stages, stage_bytes, S, c.heads_per_cta * c.warps_per_head, c.D);
   return lay.total;
 }
@@ -506,6 +518,11 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
   pa::DecodeCfg c;
   c.dtype = dt;
   c.D = static_cast<int>(D);
+  // Unrolled full-frame path: 256-byte rows, units of 16 * warps_per_head tokens.
+  const bool fast_rows = D * e == 256 && (B & (B - 1)) == 0 && !p.generic_only;
+  int wph = p.warps_per_head;
+  if (!wph && fast_rows) wph = B >= 32 ? 2 : 1;
+  const int64_t R = wph ? unit_rows(B, wph, fast_rows) : B;
   if (p.heads_per_cta) {
     if (!(p.heads_per_cta == 1 || p.heads_per_cta == 2 || p.heads_per_cta == 4) || H % p.heads_per_cta != 0)
       return PA_ERR_INVALID;
@@ -513,24 +530,16 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
   } else {
     c.heads_per_cta = 1;
     for (int hg : {4, 2}) {
-      if (H % hg == 0 && 2 * B * hg * D * e <= 32768) {
+      if (H % hg == 0 && 2 * R * hg * D * e <= 32768) {
         c.heads_per_cta = hg;
         break;
       }
     }
   }
-  // Unrolled full-frame path: 256-byte rows and B = 16 * warps_per_head.
-  const bool fast_rows = D * e == 256 && (B == 16 || B == 32) && !p.generic_only;
-  if (p.warps_per_head) {
-    c.warps_per_head = p.warps_per_head;
-  } else if (fast_rows) {
-    c.warps_per_head = static_cast<int>(B / 16);
-  } else {
-    c.warps_per_head = 8 / c.heads_per_cta;
-  }
-  c.fast = fast_rows && B == 16 * c.warps_per_head;
+  c.warps_per_head = wph ? wph : 8 / c.heads_per_cta;
+  c.fast = fast_rows && R == 16 * c.warps_per_head;
   if (!combo_built(c.heads_per_cta, c.warps_per_head)) return PA_ERR_INVALID;
-  const int64_t stage_bytes = 2 * B * c.heads_per_cta * D * e;
+  const int64_t stage_bytes = 2 * R * c.heads_per_cta * D * e;
   c.stages = 1;
   const size_t smem_cap = 227 * 1024;
   if (p.stages) {
@@ -540,20 +549,20 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
     // two resident blocks per SM when the staging ring still holds >= 3 frames
     for (int st = 8; st >= 2; --st) {
       c.stages = st;
-      if (pa::decode_smem_bytes(c, e, static_cast<int>(B), static_cast<int>(S)) <= smem_cap / 2 - 1024 && st >= 3)
+      if (pa::decode_smem_bytes(c, e, static_cast<int>(R), static_cast<int>(S)) <= smem_cap / 2 - 1024 && st >= 3)
         break;
       c.stages = 0;
     }
     if (c.stages == 0) {
       for (int st = 8; st >= 2; --st) {
         c.stages = st;
-        if (pa::decode_smem_bytes(c, e, static_cast<int>(B), static_cast<int>(S)) <= smem_cap) break;
+        if (pa::decode_smem_bytes(c, e, static_cast<int>(R), static_cast<int>(S)) <= smem_cap) break;
         c.stages = 0;
       }
     }
     if (c.stages == 0) return PA_ERR_UNSUPPORTED;
   }
-  if (pa::decode_smem_bytes(c, e, static_cast<int>(B), static_cast<int>(S)) > smem_cap) return PA_ERR_UNSUPPORTED;
+  if (pa::decode_smem_bytes(c, e, static_cast<int>(R), static_cast<int>(S)) > smem_cap) return PA_ERR_UNSUPPORTED;
   (void)stage_bytes;
 
   pa::DecodeArgs a;
@@ -568,6 +577,7 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
   a.S = static_cast<int32_t>(S);
   a.H = static_cast<int32_t>(H);
   a.B = static_cast<int32_t>(B);
+  a.R = static_cast<int32_t>(R);
   a.num_blocks = static_cast<int32_t>(nb);
   a.max_blocks = static_cast<int32_t>(max_blocks);
   a.G = static_cast<int32_t>(H / c.heads_per_cta);
@@ -575,8 +585,8 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
   a.status = g_dev[dev].status;
 
   CUtensorMap tk, tv;
-  PA_TRY(make_cache_map(&tk, k_cache->data, dt, nb, B, H, D, c.heads_per_cta));
-  PA_TRY(make_cache_map(&tv, v_cache->data, dt, nb, B, H, D, c.heads_per_cta));
+  PA_TRY(make_cache_map(&tk, k_cache->data, dt, nb, B, H, D, c.heads_per_cta, std::min(B, R)));
+  PA_TRY(make_cache_map(&tv, v_cache->data, dt, nb, B, H, D, c.heads_per_cta, std::min(B, R)));
 
   int occ = 0;
   if (dispatch_decode(a, c, tk, tv, nullptr, true, &occ) != cudaSuccess || occ <= 0) return PA_ERR_CUDA;
@@ -758,27 +768,29 @@ extern "C" int pa_decode_static(const pa_tensor* q, const pa_tensor* k_cache, co
   pa::DecodeCfg c;
   c.dtype = dt;
   c.D = static_cast<int>(D);
+  const bool fast_rows = D * e == 256 && (B & (B - 1)) == 0;
+  const int wph = fast_rows ? (B >= 32 ? 2 : 1) : 0;
+  const int64_t R = wph ? unit_rows(B, wph, fast_rows) : B;
   c.heads_per_cta = 1;
   for (int hg : {4, 2}) {
-    if (H % hg == 0 && 2 * B * hg * D * e <= 32768) {
+    if (H % hg == 0 && 2 * R * hg * D * e <= 32768) {
       c.heads_per_cta = hg;
       break;
     }
   }
-  const bool fast_rows = D * e == 256 && (B == 16 || B == 32);
-  c.warps_per_head = fast_rows ? static_cast<int>(B / 16) : 8 / c.heads_per_cta;
-  c.fast = fast_rows;
+  c.warps_per_head = wph ? wph : 8 / c.heads_per_cta;
+  c.fast = fast_rows && R == 16 * c.warps_per_head;
   const size_t smem_cap = 227 * 1024;
   c.stages = 0;
   for (int st = 8; st >= 3; --st) {
     c.stages = st;
-    if (pa::decode_smem_bytes(c, e, static_cast<int>(B), static_cast<int>(S)) <= smem_cap / 2 - 1024) break;
+    if (pa::decode_smem_bytes(c, e, static_cast<int>(R), static_cast<int>(S)) <= smem_cap / 2 - 1024) break;
     c.stages = 0;
   }
   if (c.stages == 0) {
     for (int st = 8; st >= 2; --st) {
       c.stages = st;
-      if (pa::decode_smem_bytes(c, e, static_cast<int>(B), static_cast<int>(S)) <= smem_cap) break;
+      if (pa::decode_smem_bytes(c, e, static_cast<int>(R), static_cast<int>(S)) <= smem_cap) break;
       c.stages = 0;
     }
   }
@@ -796,6 +808,7 @@ extern "C" int pa_decode_static(const pa_tensor* q, const pa_tensor* k_cache, co
   a.S = static_cast<int32_t>(S);
   a.H = static_cast<int32_t>(H);
   a.B = static_cast<int32_t>(B);
+  a.R = static_cast<int32_t>(R);
   a.num_blocks = static_cast<int32_t>(nb);
   a.max_blocks = static_cast<int32_t>(max_blocks);
   a.G = static_cast<int32_t>(H / c.heads_per_cta);
@@ -803,8 +816,8 @@ extern "C" int pa_decode_static(const pa_tensor* q, const pa_tensor* k_cache, co
   a.status = g_dev[dev].status;
 
   CUtensorMap tk, tv;
-  PA_TRY(make_cache_map(&tk, k_cache->data, dt, nb, B, H, D, c.heads_per_cta));
-  PA_TRY(make_cache_map(&tv, v_cache->data, dt, nb, B, H, D, c.heads_per_cta));
+  PA_TRY(make_cache_map(&tk, k_cache->data, dt, nb, B, H, D, c.heads_per_cta, std::min(B, R)));
+  PA_TRY(make_cache_map(&tv, v_cache->data, dt, nb, B, H, D, c.heads_per_cta, std::min(B, R)));
   int occ = 0;
   if (dispatch_decode(a, c, tk, tv, nullptr, true, &occ) != cudaSuccess || occ <= 0) return PA_ERR_CUDA;
   c.grid = g_dev[dev].num_sms * occ;

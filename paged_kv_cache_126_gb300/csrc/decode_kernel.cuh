@@ -503,8 +503,12 @@ __global__ void __launch_bounds__(32 * (HG * WPH + 1), (HG * WPH <= 4 ? 3 : 2))
   static_assert(BFAST == 0 || (BFAST == 16 * WPH && D * E == 256), "fast path shape");
 
   const int B = a.B;
-  const uint32_t tile_bytes = static_cast<uint32_t>(B) * HG * D * E;
+  const int R = a.R;                          // tokens per stage
+  const int FPS = R > B ? R / B : 1;          // frames per stage
+  const int SPF = B > R ? B / R : 1;          // stages per frame
+  const uint32_t tile_bytes = static_cast<uint32_t>(R) * HG * D * E;
   const uint32_t stage_bytes = 2u * tile_bytes;
+  const uint32_t box_bytes = static_cast<uint32_t>(R > B ? B : R) * HG * D * E;  // one copy (K or V)
 
   extern __shared__ unsigned char smem_raw[];
   const Layout lay(stages, stage_bytes, a.S, NCW, D);
@@ -706,35 +710,47 @@ __global__ void __launch_bounds__(32 * (HG * WPH + 1), (HG * WPH <= 4 ? 3 : 2))
       if (done) break;
       const Item it = locate(a, offa, order, a_total, P, item);
       const int32_t* row = a.block_tables + static_cast<int64_t>(it.s) * a.bt_row + it.blk0;
-      for (int j0 = 0; j0 < it.nblk; j0 += 32) {
-        const int jj = j0 + lane;
-        int frame = -1;
-        if (jj < it.nblk) frame = row[jj];
-        const bool bad = (jj < it.nblk) && (frame < 0 || frame >= a.num_blocks);
-        if (__ballot_sync(kFull, bad) != 0u && lane == 0) atomicOr(a.status, kDevBadBlock);
-        const int cnt = min(32, it.nblk - j0);
-        for (int j = 0; j < cnt; ++j, ++k) {
-          const int fr = __shfl_sync(kFull, frame, j);
-          if (lane == 0) {
-            const int st = k % stages;
-            const uint32_t ph = static_cast<uint32_t>(k / stages) & 1u;
-            if (mbar_wait(bar_empty + 8u * st, ph ^ 1u, abort_flag, a.status)) {
-              if (fr < 0 || fr >= a.num_blocks) {
-                poison[st] = 1;
-                mbar_arrive(bar_full + 8u * st);
-                issued &= ~(1u << st);
-              } else {
-                poison[st] = 0;
-                const uint32_t dst = sbase + st * lay.stage_pitch;
-                mbar_arrive_expect_tx(bar_full + 8u * st, stage_bytes);
-                tma_load_3d(dst, &tmap_k, 0, it.g * HG, fr * B, bar_full + 8u * st);
-                tma_load_3d(dst + tile_bytes, &tmap_v, 0, it.g * HG, fr * B, bar_full + 8u * st);
-                issued |= 1u << st;
-              }
-            } else {
+      // staged units of this item: R tokens each (FPS frames, or one slice of a frame)
+      const int ntok = it.tok1 - it.blk0 * B;
+      const int nvf = ntok > 0 ? (ntok + R - 1) / R : 0;
+      int chunk = -1, frame = -1;  // lane-distributed block-table slice, 32 frames
+      for (int vf = 0; vf < nvf; ++vf, ++k) {
+        const int f0 = FPS > 1 ? vf * FPS : vf / SPF;  // first frame of the unit (item-relative)
+        const int nf = FPS > 1 ? min(FPS, it.nblk - f0) : 1;
+        if ((f0 >> 5) != chunk) {  // FPS divides 32: a unit never straddles two slices
+          chunk = f0 >> 5;
+          const int jj = chunk * 32 + lane;
+          frame = jj < it.nblk ? row[jj] : 0;
+          const bool bad = (jj < it.nblk) && (frame < 0 || frame >= a.num_blocks);
+          if (__ballot_sync(kFull, bad) != 0u && lane == 0) atomicOr(a.status, kDevBadBlock);
+        }
+        const int fr = __shfl_sync(kFull, frame, (f0 & 31) + (lane < nf ? lane : 0));
+        const bool poisoned = __ballot_sync(kFull, lane < nf && (fr < 0 || fr >= a.num_blocks)) != 0u;
+        const int st = k % stages;
+        const uint32_t ph = static_cast<uint32_t>(k / stages) & 1u;
+        int go = 0;
+        if (lane == 0) {
+          if (mbar_wait(bar_empty + 8u * st, ph ^ 1u, abort_flag, a.status)) {
+            if (poisoned) {
+              poison[st] = 1;
+              mbar_arrive(bar_full + 8u * st);
               issued &= ~(1u << st);
+            } else {
+              poison[st] = 0;
+              mbar_arrive_expect_tx(bar_full + 8u * st, 2u * box_bytes * nf);
+              issued |= 1u << st;
+              go = 1;
             }
+          } else {
+            issued &= ~(1u << st);
           }
+        }
+        go = __shfl_sync(kFull, go, 0);
+        if (go && lane < nf) {
+          const uint32_t dst = sbase + st * lay.stage_pitch + lane * box_bytes;
+          const int r0 = fr * B + (SPF > 1 ? (vf % SPF) * R : 0);
+          tma_load_3d(dst, &tmap_k, 0, it.g * HG, r0, bar_full + 8u * st);
+          tma_load_3d(dst + tile_bytes, &tmap_v, 0, it.g * HG, r0, bar_full + 8u * st);
         }
       }
     }
@@ -794,23 +810,25 @@ __global__ void __launch_bounds__(32 * (HG * WPH + 1), (HG * WPH <= 4 ? 3 : 2))
     st.reset();
     bool poisoned = it.L < 0;
 
-    for (int j = 0; j < it.nblk; ++j, ++k) {
+    const int ntok = it.tok1 - it.blk0 * B;
+    const int nvf = ntok > 0 ? (ntok + R - 1) / R : 0;
+    for (int j = 0; j < nvf; ++j, ++k) {
       const int s_ = k % stages;
       const uint32_t ph = static_cast<uint32_t>(k / stages) & 1u;
       const bool ok = __all_sync(kFull, mbar_wait(bar_full + 8u * s_, ph, abort_flag, a.status));
       if (!ok || poison[s_]) poisoned = true;
       if (!poisoned) {
-        const int n_valid = min(B, it.tok1 - (it.blk0 + j) * B);
+        const int n_valid = min(R, ntok - j * R);
         const unsigned char* kst = stage0 + s_ * lay.stage_pitch + (h * D + c * VEC) * E;
         const unsigned char* vst = kst + tile_bytes;
         if constexpr (BFAST > 0) {
           if (n_valid == BFAST) {
             frame_fast<T, D, HG>(st, qv, kst, vst, w, r, c);
           } else {
-            frame_generic<T, D, HG, WPH>(st, qv, kst, vst, B, n_valid, w, r);
+            frame_generic<T, D, HG, WPH>(st, qv, kst, vst, R, n_valid, w, r);
           }
         } else {
-          frame_generic<T, D, HG, WPH>(st, qv, kst, vst, B, n_valid, w, r);
+          frame_generic<T, D, HG, WPH>(st, qv, kst, vst, R, n_valid, w, r);
         }
       }
       __syncwarp();
@@ -924,7 +942,7 @@ template <typename T, int D, int HG, int WPH, int BFAST>
 cudaError_t launch_one(const DecodeArgs& a, const DecodeCfg& c, const CUtensorMap& tk, const CUtensorMap& tv,
                        cudaStream_t stream, bool query_only, int* max_ctas) {
   constexpr int NCW = HG * WPH;
-  const uint32_t stage_bytes = 2u * static_cast<uint32_t>(a.B) * HG * D * sizeof(T);
+  const uint32_t stage_bytes = 2u * static_cast<uint32_t>(a.R) * HG * D * sizeof(T);
   const Layout lay(c.stages, stage_bytes, a.S, NCW, D);
   const size_t smem = lay.total;
   auto kern = decode_kernel<T, D, HG, WPH, BFAST>;
@@ -955,7 +973,7 @@ template <typename T, int D>
 cudaError_t launch_d(const DecodeArgs& a, const DecodeCfg& c, const CUtensorMap& tk, const CUtensorMap& tv,
                      cudaStream_t stream, bool query_only, int* max_ctas) {
   constexpr bool kFastRows = D * sizeof(T) == 256;
-  const bool fast = kFastRows && c.fast && (a.B == 16 * c.warps_per_head);
+  const bool fast = kFastRows && c.fast && (a.R == 16 * c.warps_per_head);
 #define PA_DK_CASE(hg, wph)                                                                         \
   if (c.heads_per_cta == hg && c.warps_per_head == wph) {                                           \
     if constexpr (kFastRows && (wph == 1 || wph == 2))                                              \

@@ -43,6 +43,9 @@ struct DecodeArgs {
   int64_t bt_row;
   const int32_t* context_lens;  // [S]
   int32_t S, H, B, num_blocks, max_blocks;
+  // tokens per staged unit: B, or R = 16 * warps_per_head when B divides R (R/B frames
+  // share a stage) or R divides B (a frame is staged as B/R slices)
+  int32_t R;
   int32_t G;                    // head groups per sequence = H / heads_per_cta
   float qk_scale_log2;          // scale * log2(e)
   // partitioning: fixed_part > 0 forces that many tokens per partition (multiple of
@@ -81,7 +84,7 @@ cudaError_t launch_decode_f16(const DecodeArgs&, const DecodeCfg&, const CUtenso
 cudaError_t launch_decode_bf16(const DecodeArgs&, const DecodeCfg&, const CUtensorMap&, const CUtensorMap&,
                                cudaStream_t, bool query_only, int* max_ctas);
 // Dynamic shared memory of one decode thread block (mirrors the kernel's layout).
-size_t decode_smem_bytes(const DecodeCfg& c, int elem_bytes, int B, int S);
+size_t decode_smem_bytes(const DecodeCfg& c, int elem_bytes, int R, int S);  // R: tokens per staged unit
 
 // ---- chunked prefill (tensor cores) ------------------------------------------------------------
 struct PrefillArgs {
