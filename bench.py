@@ -66,8 +66,10 @@ def _peaks():
 
 
 def _kernel_source_hash() -> str:
+    """Hash of the decode kernel's source: DRAM bytes per launch are the algorithm's,
+    not the launch options', so the host code is left out."""
     h = hashlib.sha256()
-    for f in ("decode_kernel.cuh", "api.cu"):
+    for f in ("decode_kernel.cuh",):
         with open(os.path.join(ROOT, "paged_kv_cache_126_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:12]
