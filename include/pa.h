@@ -209,10 +209,34 @@ typedef struct pa_decode_params {
                                 average load per block, else aim at 1.5 work items per
                                 thread block; >0: always aim at this many */
   int32_t generic_only;      /* 1: never take the unrolled full-frame path (testing) */
-  int32_t reserved;
+  int32_t share_prefix;      /* >0: read frames that consecutive sequences share once for
+                                all of them (see below); 1 = runs of at least 256 shared
+                                tokens, >1 = runs of at least this many tokens */
 } pa_decode_params;
 
-/* pa_decode with explicit launch options (tests, tuning).  params may be NULL. */
+/* pa_decode with explicit launch options (tests, tuning).  params may be NULL.
+ *
+ * share_prefix > 0 -- shared-prefix decode.  The result is pa_decode's; only the
+ * number of reads of shared frames changes.  Forks copy block tables and raise
+ * reference counts ("PagedAttention: Virtual Memory Guide for LLM Inference", "Key
+ * Architectural Mechanics"), so siblings' tables begin with the same frame ids, and
+ * for the tokens in those frames their keys and values are the same bytes.  A first
+ * kernel finds, for every sequence s >= 1, how many leading tokens it reads through
+ * the same frame ids as sequence s-1 (equal leading table entries, capped by both
+ * context lengths).  Runs of consecutive sequences whose count reaches the
+ * threshold (share_prefix == 1: 256 tokens; > 1: that many; never below B) are cut
+ * into chunks of up to 16; each chunk's smallest count, rounded down to whole
+ * frames, is its shared prefix, attended once with all members' queries (one read of
+ * each shared frame, the queries as the rows of a tensor-core tile), while each
+ * member's remaining tokens are attended alone; the parts are merged by the
+ * log-sum-exp rule.  Put sibling sequences next to each other in the batch to
+ * benefit.  Arithmetic: q.k products and the weighted sums of values on the tensor
+ * cores with fp32 accumulation, the weights carried as two 16-bit parts (fp32
+ * accurate), softmax in fp32.  Applies to fp16 / bf16 caches with D = 128, B a power
+ * of two >= 8 and 2 <= S <= 4096 (other shapes run the plain decode, with the same
+ * result).  heads_per_cta, when given, must be 1, 2 or 4 and warps_per_head 0 or 1,
+ * else PA_ERR_INVALID.  Uses workspace partials for every sequence that has more than
+ * one part, and launches two kernels. */
 int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
                  const pa_tensor* block_tables, const pa_tensor* context_lens,
                  float scale, const pa_tensor* out, const pa_decode_params* params,

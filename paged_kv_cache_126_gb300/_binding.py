@@ -41,7 +41,7 @@ class PaTensor(C.Structure):
 class PaDecodeParams(C.Structure):
     _fields_ = [("partition_tokens", C.c_int32), ("heads_per_cta", C.c_int32),
                 ("warps_per_head", C.c_int32), ("stages", C.c_int32), ("ctas_per_sm", C.c_int32),
-                ("items_per_cta", C.c_int32), ("generic_only", C.c_int32), ("reserved", C.c_int32)]
+                ("items_per_cta", C.c_int32), ("generic_only", C.c_int32), ("share_prefix", C.c_int32)]
 
 
 class PAError(RuntimeError):
@@ -168,7 +168,10 @@ def make_params(params) -> PaDecodeParams | None:
     if isinstance(params, PaDecodeParams):
         return params
     p = PaDecodeParams()
+    names = {f[0] for f in PaDecodeParams._fields_}
     for k, v in dict(params).items():
+        if k not in names:
+            raise ValueError(f"unknown decode option {k!r}")
         setattr(p, k, int(v))
     return p
 

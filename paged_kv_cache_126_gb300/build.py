@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpa.so")
 
 SOURCES = ["block_manager.cpp", "api.cu", "append.cu", "decode_f16.cu", "decode_bf16.cu", "decode_f32.cu",
-           "prefill.cu", "decode_split.cu"]
+           "prefill.cu", "decode_split.cu", "decode_shared.cu"]
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
 
 

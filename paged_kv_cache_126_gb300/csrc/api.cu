@@ -120,6 +120,23 @@ int make_frame_map(CUtensorMap* map, void* base, int dtype, int64_t rows, int64_
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
 }
 
+// 4-D view {64 elements, rows, 2 column halves, H} of a 16-bit cache with D = 128, box
+// {64, box_rows, 2, hg}, 128-byte swizzle: a box lands in shared memory as
+// [hg][2][box_rows][64] with every 128-byte line swizzled (the layout ldmatrix reads
+// without bank conflicts).
+int make_half_rows_map(CUtensorMap* map, void* base, int dtype, int64_t rows, int64_t H, int hg, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return PA_ERR_CUDA;
+  CUtensorMapDataType t = dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), 2, static_cast<cuuint64_t>(H)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(H * 256), 128, 256};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 2, static_cast<cuuint32_t>(hg)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, t, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
+}
+
 // ---- library-owned workspace, one per (device, stream) -------------------------------------
 // Layout: [0, 256) scheduler counters | arrival counters, one per (sequence, head) |
 // per-launch offsets and split partials.  Both counter regions must hold zeros
@@ -485,6 +502,127 @@ int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_
   return PA_OK;
 }
 
+}  // extern "C"
+
+namespace {
+// Shared-prefix decode (pa_decode_params.share_prefix).  Returns PA_OK after launching
+// the plan kernel and the decode, kNotApplicable when the shapes fall outside what the
+// shared-prefix kernel handles (the caller then runs the plain decode: same result),
+// or an error code.
+constexpr int kNotApplicable = 1;
+
+int decode_shared(int dev, const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                  const pa_tensor* block_tables, const pa_tensor* context_lens, float scale, const pa_tensor* out,
+                  const pa_decode_params& p, pa_stream stream) {
+  const int dt = k_cache->dtype;
+  const int64_t nb = k_cache->shape[0], B = k_cache->shape[1], H = k_cache->shape[2], D = k_cache->shape[3];
+  const int64_t S = q->shape[0];
+  const int64_t max_blocks = block_tables->shape[1];
+  if (!(dt == PA_F16 || dt == PA_BF16) || D != 128 || (B & (B - 1)) != 0 || B < 8 || S < 2 || S > 4096)
+    return kNotApplicable;
+  pa::DecodeCfg c;
+  c.dtype = dt;
+  c.D = 128;
+  c.fast = true;
+  c.heads_per_cta = p.heads_per_cta ? p.heads_per_cta : (H % 4 == 0 ? 4 : H % 2 == 0 ? 2 : 1);
+  c.warps_per_head = p.warps_per_head ? p.warps_per_head : 1;
+  if (!pa::decode_shared_combo(c.heads_per_cta, c.warps_per_head) || H % c.heads_per_cta != 0)
+    return PA_ERR_INVALID;
+  const int64_t R = 16;  // tokens per staged unit: one 16-key tensor-core tile
+  const size_t smem_cap = 227 * 1024;
+  auto smem_of = [&](int st) {
+    pa::DecodeCfg t = c;
+    t.stages = st;
+    return pa::decode_shared_smem_bytes(t, static_cast<int>(R), static_cast<int>(S));
+  };
+  c.stages = 0;
+  if (p.stages) {
+    if (p.stages < 2 || p.stages > 8) return PA_ERR_INVALID;
+    c.stages = p.stages;
+  } else {
+    for (int st = 8; st >= 3 && !c.stages; --st)
+      if (smem_of(st) <= smem_cap / 2 - 1024) c.stages = st;
+    for (int st = 8; st >= 2 && !c.stages; --st)
+      if (smem_of(st) <= smem_cap) c.stages = st;
+  }
+  if (!c.stages || smem_of(c.stages) > smem_cap) return kNotApplicable;
+
+  pa::DecodeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = q->data;
+  a.out = out->data;
+  a.q_row = q->stride[0];
+  a.out_row = out->stride[0];
+  a.block_tables = static_cast<const int32_t*>(block_tables->data);
+  a.bt_row = block_tables->stride[0];
+  a.context_lens = static_cast<const int32_t*>(context_lens->data);
+  a.S = static_cast<int32_t>(S);
+  a.H = static_cast<int32_t>(H);
+  a.B = static_cast<int32_t>(B);
+  a.R = static_cast<int32_t>(R);
+  a.num_blocks = static_cast<int32_t>(nb);
+  a.max_blocks = static_cast<int32_t>(max_blocks);
+  a.G = static_cast<int32_t>(H / c.heads_per_cta);
+  a.qk_scale_log2 = scale * 1.4426950408889634f;
+  a.status = g_dev[dev].status;
+  a.min_shared = static_cast<int32_t>(std::max<int64_t>(p.share_prefix == 1 ? 256 : p.share_prefix, B));
+
+  CUtensorMap tk, tv;
+  PA_TRY(make_half_rows_map(&tk, k_cache->data, dt, nb * B, H, c.heads_per_cta, static_cast<int>(std::min(B, R))));
+  PA_TRY(make_half_rows_map(&tv, v_cache->data, dt, nb * B, H, c.heads_per_cta, static_cast<int>(std::min(B, R))));
+  int occ = 0;
+  if (pa::launch_decode_shared(a, c, tk, tv, nullptr, true, &occ) != cudaSuccess || occ <= 0) return PA_ERR_CUDA;
+  c.grid = g_dev[dev].num_sms * (p.ctas_per_sm ? std::min(p.ctas_per_sm, occ) : occ);
+
+  // partition length and the number of partial slots the workspace holds (the kernel
+  // falls back to whole segments, at most 2 per sequence, if its parts would not fit)
+  const int64_t Lcap = max_blocks * B;
+  int64_t part_cap;
+  if (p.items_per_cta < 0) return PA_ERR_INVALID;
+  if (p.partition_tokens == -1 || Lcap == 0) {
+    a.fixed_part = static_cast<int32_t>(std::max<int64_t>(Lcap, B));
+    part_cap = 2 * S;
+  } else if (p.partition_tokens > 0) {
+    a.fixed_part = round_up(p.partition_tokens, B);
+    part_cap = S * ((Lcap + a.fixed_part - 1) / a.fixed_part + 2);
+  } else if (p.partition_tokens == 0) {
+    a.whole_first = p.items_per_cta == 0;
+    a.target_items = p.items_per_cta ? p.items_per_cta * c.grid : (3 * c.grid) / 2;
+    a.min_part = round_up(256, B);
+    // parts of the automatic choice: every member of a chunk holds its own partial of
+    // each shared part, so up to 16 per shared part, plus the private parts
+    part_cap = 3 * S + 2 * (16 + 1) * ((a.target_items + a.G - 1) / a.G) + 8;
+  } else {
+    return PA_ERR_INVALID;
+  }
+  const int64_t slot_bytes = H * (D + 2) * static_cast<int64_t>(sizeof(float));
+  part_cap = std::max<int64_t>(2 * S, std::min<int64_t>(part_cap, (static_cast<int64_t>(1) << 32) / slot_bytes));
+  a.part_cap = static_cast<int32_t>(part_cap);
+  {
+    const size_t o_bytes = static_cast<size_t>(part_cap * H * D) * sizeof(float);
+    const size_t ml_bytes = static_cast<size_t>(part_cap * H * 2) * sizeof(float);
+    const size_t lcp_bytes = static_cast<size_t>(S) * sizeof(int32_t);
+    void* ws = nullptr;
+    size_t cnt_bytes = 0;
+    PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), static_cast<size_t>(S * H) * sizeof(int32_t),
+                     o_bytes + ml_bytes + lcp_bytes, &ws, &cnt_bytes));
+    unsigned char* w = static_cast<unsigned char*>(ws);
+    unsigned char* rest = w + kSchedBytes + cnt_bytes;
+    a.sched = reinterpret_cast<int32_t*>(w);
+    a.ws_cnt = reinterpret_cast<int32_t*>(w + kSchedBytes);
+    a.ws_o = reinterpret_cast<float*>(rest);
+    a.ws_ml = reinterpret_cast<float*>(rest + o_bytes);
+    a.lcp = reinterpret_cast<int32_t*>(rest + o_bytes + ml_bytes);
+  }
+  if (pa::launch_decode_shared(a, c, tk, tv, static_cast<cudaStream_t>(stream), false, nullptr) != cudaSuccess)
+    return PA_ERR_CUDA;
+  g_launches.fetch_add(2);
+  return PA_OK;
+}
+}  // namespace
+
+extern "C" {
+
 int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
                  const pa_tensor* block_tables, const pa_tensor* context_lens, float scale, const pa_tensor* out,
                  const pa_decode_params* params, pa_stream stream) {
@@ -508,11 +646,16 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
   pa_decode_params p;
   std::memset(&p, 0, sizeof(p));
   if (params) p = *params;
-  if (p.heads_per_cta < 0 || p.warps_per_head < 0 || p.stages < 0 || p.ctas_per_sm < 0) return PA_ERR_INVALID;
+  if (p.heads_per_cta < 0 || p.warps_per_head < 0 || p.stages < 0 || p.ctas_per_sm < 0 || p.share_prefix < 0)
+    return PA_ERR_INVALID;
 
   int dev;
   PA_TRY(current_device(&dev));
   const int e = elem_bytes(dt);
+  if (p.share_prefix > 0) {
+    const int rc = decode_shared(dev, q, k_cache, v_cache, block_tables, context_lens, scale, out, p, stream);
+    if (rc != kNotApplicable) return rc;
+  }
 
   // ---- launch configuration -------------------------------------------------------------
   pa::DecodeCfg c;

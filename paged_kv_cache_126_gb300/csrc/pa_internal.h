@@ -62,6 +62,12 @@ struct DecodeArgs {
   float* ws_ml;                 // [items][HG][2] = (running max in log2 units, sum); null if no split
   float* ws_o;                  // [items][HG][D] unnormalised partial outputs; null if no split
   int32_t* status;
+  // shared-prefix decode only: lcp[s] = leading tokens s reads through the same frames as
+  // s - 1 (written by its plan kernel); runs with lcp >= min_shared form chunks; the
+  // workspace holds part_cap partial slots of [H][D] (ws_o) and [H][2] (ws_ml)
+  int32_t* lcp;
+  int32_t min_shared;
+  int32_t part_cap;
 };
 
 struct DecodeCfg {
@@ -85,6 +91,13 @@ cudaError_t launch_decode_bf16(const DecodeArgs&, const DecodeCfg&, const CUtens
                                cudaStream_t, bool query_only, int* max_ctas);
 // Dynamic shared memory of one decode thread block (mirrors the kernel's layout).
 size_t decode_smem_bytes(const DecodeCfg& c, int elem_bytes, int R, int S);  // R: tokens per staged unit
+
+// Shared-prefix decode (16-bit caches, D = 128): the plan kernel, then the decode over
+// shared and private parts.  query_only as for the launchers above.
+cudaError_t launch_decode_shared(const DecodeArgs&, const DecodeCfg&, const CUtensorMap&, const CUtensorMap&,
+                                 cudaStream_t, bool query_only, int* max_ctas);
+size_t decode_shared_smem_bytes(const DecodeCfg& c, int R, int S);
+bool decode_shared_combo(int heads_per_cta, int warps_per_head);
 
 // ---- chunked prefill (tensor cores) ------------------------------------------------------------
 struct PrefillArgs {

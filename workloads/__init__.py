@@ -16,6 +16,7 @@ from .gen import (  # noqa: F401
     mcts_tree,
     prefill_batch,
     prefix_ids,
+    random_storage,
     shared_prefix,
     CONFIG_IDS,
     storage_numpy_dtype,

@@ -76,6 +76,13 @@ def _to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(dtype)
 
 
+def random_storage(seed: int, shape, dtype: str, sigma: float = 1.0) -> np.ndarray:
+    """N(0, sigma) values of the given shape, rounded to the storage dtype (bf16 as
+    uint16 bit patterns)."""
+    x = np.random.default_rng(seed).standard_normal(shape, dtype=np.float32) * np.float32(sigma)
+    return _to_storage(x, dtype)
+
+
 _M64 = np.uint64(0xFFFFFFFFFFFFFFFF)
 
 
