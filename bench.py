@@ -463,14 +463,15 @@ def fixed_variant(args, device):
 
 
 # ----------------------------------------------------------------------------- per-workload sweep
-SWEEP_KEYS = ("0", "1", "1x", "2", "3", "3c", "4")
+SWEEP_KEYS = ("0", "1", "1x", "2", "3", "3c", "3s", "4")
 
 
 def sweep(keys, reps=20):
     """pa_decode on the final state of each workload's replay (host-generated data,
     automatic launch options): one JSON line per workload.  "3c" is the unshared
     control of the parallel-sampling workload: the same final lengths, every branch
-    with private frames."""
+    with private frames; "3s" is the parallel-sampling workload through the
+    shared-prefix decode (each shared prompt frame read once for its branches)."""
     import numpy as np
     import torch
 
@@ -481,7 +482,8 @@ def sweep(keys, reps=20):
     torch.cuda.set_device(dev)
     st = torch.cuda.current_stream(dev)
     for key in keys:
-        cfg = {"0": 0, "1": 1, "1x": "1x", "2": 2, "3": 3, "3c": 3, "4": 4}[key]
+        cfg = {"0": 0, "1": 1, "1x": "1x", "2": 2, "3": 3, "3c": 3, "3s": 3, "4": 4}[key]
+        params = {"share_prefix": 1} if key == "3s" else None
         w = workloads.build(cfg)
         if key == "3c":
             L = [w.final_lens[s] for s in range(len(w.final_lens))]
@@ -499,12 +501,12 @@ def sweep(keys, reps=20):
         out = torch.empty_like(q)
         n = reps if key != "4" else max(5, reps // 2)
         for _ in range(3):
-            pa.pa_decode(q, eng.k_cache, eng.v_cache, tt, ll, w.scale, out)
+            pa.pa_decode(q, eng.k_cache, eng.v_cache, tt, ll, w.scale, out, params=params)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(st)
         for _ in range(n):
-            pa.pa_decode(q, eng.k_cache, eng.v_cache, tt, ll, w.scale, out)
+            pa.pa_decode(q, eng.k_cache, eng.v_cache, tt, ll, w.scale, out, params=params)
         e1.record(st)
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) / n * 1e3
@@ -515,12 +517,12 @@ def sweep(keys, reps=20):
         unique = len(frames) * w.block_size * w.num_heads * w.head_dim * w.elem_bytes * 2
         peak, _ = _peaks()
         print(json.dumps({
-            "workload": key, "name": w.name, "seqs": len(seqs), "sum_len": int(np.sum(lens)),
+            "workload": key, "name": w.name, "params": params, "seqs": len(seqs), "sum_len": int(np.sum(lens)),
             "decode_us": round(us, 2), "algorithmic_bytes": logical, "gbps": round(logical / (us * 1e-6) / 1e9, 1),
             "pct_of_peak": round(100 * logical / (us * 1e-6) / 1e9 / peak, 1),
             "unique_frame_bytes": unique, "gbps_unique_frames": round(unique / (us * 1e-6) / 1e9, 1),
             "seqs_per_sec": round(len(seqs) / (us * 1e-6), 1),
-            "cow_copies": sum(len(t["copies"]) for t in trace.values())}), flush=True)
+            "cow_copies": sum(len(t["copies"]) for t in trace.values() if isinstance(t, dict) and "copies" in t)}), flush=True)
         del eng, outs, tt, ll, q, out
         torch.cuda.empty_cache()
 
@@ -722,7 +724,7 @@ def prefix_bench(n_requests=16, system_len=2048, user_len=512, reps=10):
     print(json.dumps(line), flush=True)
 
 
-def fork_tree_bench(n_prompts=8, prompt_len=2048, width=8, steps=64):
+def fork_tree_bench(n_prompts=8, prompt_len=2048, width=8, steps=64, share=False):
     """Beam search over forked sequences, the whole step loop on one GPU: host block
     manager (step with copy-on-write, then the selection's forks and frees), staged
     upload, pa_copy_blocks, pa_cache_append and pa_decode over every live beam.
@@ -771,7 +773,8 @@ def fork_tree_bench(n_prompts=8, prompt_len=2048, width=8, steps=64):
                 live = op[1]
                 assert ops[i + 1][0] == "attend" and ops[i + 1][1] == live
                 e = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-                _, nc, lens = eng.decode_step(live, step_k, step_v, q, scale, out=out, events=e)
+                _, nc, lens = eng.decode_step(live, step_k, step_v, q, scale, out=out, events=e,
+                                              params={"share_prefix": 1} if share else None)
                 if record:
                     tables, ln = eng.bm.block_tables(live, mb)
                     unique = len(set(tables[tables >= 0].tolist()))
@@ -794,7 +797,7 @@ def fork_tree_bench(n_prompts=8, prompt_len=2048, width=8, steps=64):
     copies = int(sum(x[3] for x in stats))
     print(json.dumps({
         "metric": "beam-search decode step over forked sequences (block manager + copy-on-write + append + decode)",
-        "workload": w.name, "beams": nbeams, "steps": len(stats),
+        "workload": w.name, "share_prefix": int(share), "beams": nbeams, "steps": len(stats),
         "ms_per_step_e2e": round(total / n_steps * 1e3, 3),
         "decode_us_median": round(float(np.median(dec)) * 1e6, 2),
         "decode_gbs_logical": round(float(np.sum(logical) / np.sum(dec)) / 1e9, 1),
@@ -963,13 +966,14 @@ def main():
     ap.add_argument("--block-sweep", action="store_true", help="decode and prefill throughput against block size")
     ap.add_argument("--split-layout", action="store_true", help="decode throughput of the two cache layouts")
     ap.add_argument("--sweep", default=None, metavar="KEYS",
-                    help="time pa_decode on each listed workload instead (comma list of 0,1,1x,2,3,3c,4 or 'all')")
+                    help="time pa_decode on each listed workload instead (comma list of 0,1,1x,2,3,3c,3s,4 or 'all')")
     args = ap.parse_args()
     if args.prefix:
         prefix_bench()
         return
     if args.fork_trees:
         fork_tree_bench()
+        fork_tree_bench(share=True)
         return
     if args.block_sweep:
         block_sweep()

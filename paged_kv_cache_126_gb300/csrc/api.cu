@@ -588,7 +588,9 @@ int decode_shared(int dev, const pa_tensor* q, const pa_tensor* k_cache, const p
   } else if (p.partition_tokens == 0) {
     a.whole_first = p.items_per_cta == 0;
     a.target_items = p.items_per_cta ? p.items_per_cta * c.grid : (3 * c.grid) / 2;
-    a.min_part = round_up(256, B);
+    // parts of at least 512 tokens: an item carries up to 16 queries and pays their loads
+    // and its epilogue once, so longer parts than the plain decode's amortise better
+    a.min_part = round_up(512, B);
     // parts of the automatic choice: every member of a chunk holds its own partial of
     // each shared part, so up to 16 per shared part, plus the private parts
     part_cap = 3 * S + 2 * (16 + 1) * ((a.target_items + a.G - 1) / a.G) + 8;
@@ -601,11 +603,10 @@ int decode_shared(int dev, const pa_tensor* q, const pa_tensor* k_cache, const p
   {
     const size_t o_bytes = static_cast<size_t>(part_cap * H * D) * sizeof(float);
     const size_t ml_bytes = static_cast<size_t>(part_cap * H * 2) * sizeof(float);
-    const size_t lcp_bytes = static_cast<size_t>(S) * sizeof(int32_t);
+    const size_t lcp_bytes = static_cast<size_t>(2 * S + 1) * sizeof(int32_t);  // lcp [S], slot offsets [S + 1]
     void* ws = nullptr;
     size_t cnt_bytes = 0;
-    PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), static_cast<size_t>(S * H) * sizeof(int32_t),
-                     o_bytes + ml_bytes + lcp_bytes, &ws, &cnt_bytes));
+    PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), 0, o_bytes + ml_bytes + lcp_bytes, &ws, &cnt_bytes));
     unsigned char* w = static_cast<unsigned char*>(ws);
     unsigned char* rest = w + kSchedBytes + cnt_bytes;
     a.sched = reinterpret_cast<int32_t*>(w);
@@ -613,10 +614,11 @@ int decode_shared(int dev, const pa_tensor* q, const pa_tensor* k_cache, const p
     a.ws_o = reinterpret_cast<float*>(rest);
     a.ws_ml = reinterpret_cast<float*>(rest + o_bytes);
     a.lcp = reinterpret_cast<int32_t*>(rest + o_bytes + ml_bytes);
+    a.pbase_out = a.lcp + S;
   }
   if (pa::launch_decode_shared(a, c, tk, tv, static_cast<cudaStream_t>(stream), false, nullptr) != cudaSuccess)
     return PA_ERR_CUDA;
-  g_launches.fetch_add(2);
+  g_launches.fetch_add(3);
   return PA_OK;
 }
 }  // namespace

@@ -946,11 +946,10 @@ cudaError_t launch_one(const DecodeArgs& a, const DecodeCfg& c, const CUtensorMa
   const Layout lay(c.stages, stage_bytes, a.S, NCW, D);
   const size_t smem = lay.total;
   auto kern = decode_kernel<T, D, HG, WPH, BFAST>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  int n = 0;
+  cudaError_t e = kernel_prep(reinterpret_cast<const void*>(kern), 32 * (NCW + 1), smem, &n);
   if (e != cudaSuccess) return e;
   if (query_only) {
-    int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32 * (NCW + 1), smem);
     if (max_ctas) *max_ctas = n;
     return e;
   }

@@ -36,9 +36,12 @@
 //       of a shared frame serves all members; K/V rows reach the tensor cores
 //       through conflict-free ldmatrix loads from a 128-byte-swizzled layout.
 //     - Every part's (m, l, o) goes to slot pbase[s] + part of the workspace, or
-//       straight to the output when the sequence has one part; the last part of a
-//       (sequence, head) to arrive merges the slots (log-sum-exp) and zeroes its
-//       counter.
+//       straight to the output when the sequence has one part.
+//   * merge kernel (one warp per (sequence, head), programmatic dependent launch):
+//     log-sum-exp merge of the slots of every sequence with more than one part.  A
+//     separate launch keeps the decode warps streaming: merging inside them (fence,
+//     arrival counter, then up to 16 members' merges by one warp) stalled the
+//     staging ring of the whole thread block.
 //   * Bad frame ids / lengths: as in decode_kernel (rows of the affected sequences
 //     become zeros, sticky status bits).  A bad length ends a run (its lcp is 0).
 #include <climits>
@@ -496,31 +499,7 @@ __device__ __forceinline__ void run_item(const DecodeArgs& a, const Plan& pl, co
       need_merge |= 1u << ri;
     }
   }
-  // publish the partials, then count them: lane (g, 0) counts member rows g and g + 8;
-  // the arrival that completes a (sequence, head) merges it (the whole warp, one at a time)
-  __threadfence();
-  __syncwarp();
-  unsigned last = 0;
-  if (t == 0) {
-#pragma unroll
-    for (int ri = 0; ri < 2; ++ri) {
-      if (!(need_merge & (1u << ri))) continue;
-      const int sj = it.s + g + 8 * ri;
-      const int np = pl.pbase[sj + 1] - pl.pbase[sj];
-      if (atomicAdd(a.ws_cnt + static_cast<int64_t>(sj) * a.H + head, 1) == np - 1) last |= 1u << ri;
-    }
-  }
-  for (int ri = 0; ri < 2; ++ri) {
-    unsigned todo = __ballot_sync(kFull, (last >> ri) & 1u);
-    while (todo) {
-      const int src = __ffs(todo) - 1;
-      todo &= todo - 1;
-      const int sj = it.s + (src >> 2) + 8 * ri;
-      __threadfence();
-      merge_slots<T, D>(a, sj, head, pl.pbase[sj], pl.pbase[sj + 1] - pl.pbase[sj], lane, lane & 15);
-      if (lane == 0) a.ws_cnt[static_cast<int64_t>(sj) * a.H + head] = 0;
-    }
-  }
+  (void)need_merge;  // split (sequence, head) pairs are merged by merge_shared_kernel
 }
 
 // Inclusive scan of arr[1 .. n] in place by one warp (arr[0] = 0 is left alone).
@@ -818,6 +797,9 @@ __global__ void __launch_bounds__(32 * (HG + 1), 2)
   __syncthreads();
   // `order` held the run starts until the sort above overwrote it; nothing reads them after
   // the chunk pass.
+  // block 0 publishes the partial-slot offsets for the merge kernel
+  if (blockIdx.x == 0)
+    for (int s = tid; s <= a.S; s += blockDim.x) a.pbase_out[s] = pbase[s];
   Plan pl;
   pl.lv = lv;
   pl.cinfo = cinfo;
@@ -936,6 +918,23 @@ __global__ void __launch_bounds__(32 * (HG + 1), 2)
   }
 }
 
+// Log-sum-exp merge of every split (sequence, head), one warp each, after the decode
+// kernel has finished (programmatic dependent launch: the wait returns once every
+// partial is written and visible).
+template <typename T>
+__global__ void __launch_bounds__(256) merge_shared_kernel(const DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int64_t wi = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (wi >= static_cast<int64_t>(a.S) * a.H) return;
+  const int s = static_cast<int>(wi / a.H), head = static_cast<int>(wi % a.H);
+  const int base = a.pbase_out[s];
+  const int np = a.pbase_out[s + 1] - base;
+  if (np <= 1) return;  // written directly by the decode kernel
+  merge_slots<T, 128>(a, s, head, base, np, lane, lane & 15);
+}
+
 // lcp[s]: leading tokens sequence s reads through the same frame ids as s - 1.
 __global__ void __launch_bounds__(256) share_plan_kernel(const DecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -976,11 +975,10 @@ cudaError_t launch_one(const DecodeArgs& a, const DecodeCfg& c, const CUtensorMa
   const SLayout lay(c.stages, stage_bytes, a.S);
   const size_t smem = lay.total;
   auto kern = decode_shared_kernel<T, HG>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  int n = 0;
+  cudaError_t e = kernel_prep(reinterpret_cast<const void*>(kern), 32 * (NCW + 1), smem, &n);
   if (e != cudaSuccess) return e;
   if (query_only) {
-    int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32 * (NCW + 1), smem);
     if (max_ctas) *max_ctas = n;
     return e;
   }
@@ -1004,7 +1002,15 @@ cudaError_t launch_one(const DecodeArgs& a, const DecodeCfg& c, const CUtensorMa
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tk, tv, a, c.stages);
+  e = cudaLaunchKernelEx(&cfg, kern, tk, tv, a, c.stages);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t mcfg = {};
+  mcfg.gridDim = dim3(static_cast<unsigned>((static_cast<int64_t>(a.S) * a.H + 7) / 8));
+  mcfg.blockDim = dim3(256);
+  mcfg.stream = stream;
+  mcfg.attrs = attr;
+  mcfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&mcfg, merge_shared_kernel<T>, a);
 }
 
 template <typename T>

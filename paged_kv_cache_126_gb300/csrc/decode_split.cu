@@ -382,10 +382,8 @@ template <typename T, int D, int B>
 cudaError_t launch(const SplitArgs& a, int num_sms, cudaStream_t stream) {
   using G = Geo<T, D, B>;
   auto kern = decode_split_kernel<T, D, B>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(G::SMEM));
-  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, G::SMEM);
+  cudaError_t e = kernel_prep(reinterpret_cast<const void*>(kern), kThreads, G::SMEM, &per_sm);
   if (e != cudaSuccess) return e;
   const int total = a.S * (a.H / kHG) * a.NP;
   const int grid = std::max(1, std::min(total, num_sms * std::max(per_sm, 1)));

@@ -4,9 +4,46 @@
 
 #include <cuda.h>  // CUtensorMap
 #include <cuda_runtime.h>
+
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 namespace pa {
+
+// Launch preparation of a kernel with dynamic shared memory, cached per (device,
+// kernel, threads, bytes): raises the kernel's dynamic shared-memory limit to the
+// largest size asked for so far and returns the resident blocks per SM.  Both CUDA
+// calls cost microseconds of host time, which a decode step of tens of microseconds
+// cannot afford on every launch.
+inline cudaError_t kernel_prep(const void* fn, int threads, size_t smem, int* blocks_per_sm) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, int, size_t>, int> occ;
+  static std::map<std::pair<int, const void*>, size_t> limit;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_tuple(dev, fn, threads, smem);
+  auto it = occ.find(key);
+  if (it != occ.end()) {
+    if (blocks_per_sm) *blocks_per_sm = it->second;
+    return cudaSuccess;
+  }
+  size_t& lim = limit[{dev, fn}];
+  if (smem > lim) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    lim = smem;
+  }
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);
+  if (e != cudaSuccess) return e;
+  occ[key] = n;
+  if (blocks_per_sm) *blocks_per_sm = n;
+  return cudaSuccess;
+}
 
 // ---- cache append / frame copy ---------------------------------------------------------
 struct AppendArgs {
@@ -66,6 +103,7 @@ struct DecodeArgs {
   // s - 1 (written by its plan kernel); runs with lcp >= min_shared form chunks; the
   // workspace holds part_cap partial slots of [H][D] (ws_o) and [H][2] (ws_ml)
   int32_t* lcp;
+  int32_t* pbase_out;           // [S + 1] first partial slot of each sequence, for the merge kernel
   int32_t min_shared;
   int32_t part_cap;
 };

@@ -855,7 +855,7 @@ cudaError_t launch(const PrefillArgs& a, const CUtensorMap& tq, const CUtensorMa
                    int grid, cudaStream_t stream) {
   const size_t smem = smem_bytes(a.S, a.unit_cap);
   auto kern = prefill_kernel<T>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = kernel_prep(reinterpret_cast<const void*>(kern), kThreads, smem, nullptr);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();
