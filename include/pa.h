@@ -378,6 +378,15 @@ int pa_bm_fork(pa_bm* bm, int64_t parent_id, int64_t child_id);
  * live is a no-op returning PA_WARN_DOUBLE_FREE. */
 int pa_bm_free(pa_bm* bm, int64_t seq_id);
 
+/* Batched forms for a search step (beam search keeps the survivors' forks and drops
+ * the rest in one call each).  pa_bm_fork_many performs n forks in order, all or
+ * nothing: the whole batch is checked first (a child forked earlier in the batch may
+ * be a later parent); PA_ERR_UNKNOWN_SEQ / PA_ERR_SEQ_EXISTS leave the manager
+ * unchanged.  pa_bm_free_many frees in order exactly as n pa_bm_free calls would and
+ * returns PA_WARN_DOUBLE_FREE if any id was not live (the others are still freed). */
+int pa_bm_fork_many(pa_bm* bm, const int64_t* parent_ids, const int64_t* child_ids, int32_t n);
+int pa_bm_free_many(pa_bm* bm, const int64_t* seq_ids, int32_t n);
+
 /* Block tables [n, max_blocks] (row-major, unused entries -1) and lengths [n] of
  * the listed sequences, ready to upload for pa_decode.  PA_ERR_CAPACITY if a
  * table is longer than max_blocks. lens_out may be NULL. */

@@ -78,6 +78,8 @@ def _load():
         "pa_bm_step": ([vp, i64p, C.c_int32, i32p, i32p, i32p], C.c_int),
         "pa_bm_extend": ([vp, C.c_int64, C.c_int32, i32p, i32p, i32p], C.c_int),
         "pa_bm_fork": ([vp, C.c_int64, C.c_int64], C.c_int),
+        "pa_bm_fork_many": ([vp, i64p, i64p, C.c_int32], C.c_int),
+        "pa_bm_free_many": ([vp, i64p, C.c_int32], C.c_int),
         "pa_bm_free": ([vp, C.c_int64], C.c_int),
         "pa_bm_block_tables": ([vp, i64p, C.c_int32, C.c_int32, i32p, i32p], C.c_int),
         "pa_bm_seq_info": ([vp, C.c_int64, i32p, i32p], C.c_int),
@@ -108,6 +110,7 @@ EXPORTED = (
     "pa_bm_append", "pa_bm_step", "pa_bm_extend", "pa_bm_fork", "pa_bm_free", "pa_bm_block_tables", "pa_bm_seq_info",
     "pa_bm_table", "pa_bm_slot", "pa_bm_num_free", "pa_bm_free_list", "pa_bm_ref_counts",
     "pa_bm_num_seqs", "pa_bm_add_seq_cached", "pa_bm_step_tokens", "pa_bm_extend_tokens", "pa_bm_cached_frames",
+    "pa_bm_fork_many", "pa_bm_free_many",
 )
 
 
@@ -362,6 +365,17 @@ class BlockManager:
 
     def free(self, seq: int) -> int:
         return _check(LIB.pa_bm_free(self._h, int(seq)), "pa_bm_free")
+
+    def fork_many(self, parents, children) -> None:
+        p = np.ascontiguousarray(parents, dtype=np.int64)
+        c = np.ascontiguousarray(children, dtype=np.int64)
+        if p.shape != c.shape or p.ndim != 1:
+            raise ValueError("parents and children must be 1-D and of equal length")
+        _check(LIB.pa_bm_fork_many(self._h, _i64(p), _i64(c), len(p)), "pa_bm_fork_many")
+
+    def free_many(self, seqs) -> int:
+        s = np.ascontiguousarray(seqs, dtype=np.int64)
+        return _check(LIB.pa_bm_free_many(self._h, _i64(s), len(s)), "pa_bm_free_many")
 
     def block_tables_into(self, ids: np.ndarray, max_blocks: int, tables_out: np.ndarray, lens_out: np.ndarray):
         _check(LIB.pa_bm_block_tables(self._h, _i64(ids), len(ids), int(max_blocks), _i32(tables_out),

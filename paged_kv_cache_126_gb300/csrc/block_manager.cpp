@@ -22,6 +22,7 @@
 #include <cstring>
 #include <new>
 #include <unordered_map>
+#include <unordered_set>
 #include <vector>
 
 #include "pa.h"
@@ -460,6 +461,28 @@ int pa_bm_free(pa_bm* bm, int64_t seq_id) {
   for (int32_t f : it->second.frames) bm->drop_ref(f);
   bm->seqs.erase(it);
   return PA_OK;
+}
+
+int pa_bm_fork_many(pa_bm* bm, const int64_t* parent_ids, const int64_t* child_ids, int32_t n) {
+  if (!bm || n < 0 || (n > 0 && (!parent_ids || !child_ids))) return PA_ERR_INVALID;
+  // all-or-nothing: check the whole batch in order (a child forked earlier in the batch may
+  // be a later parent) before changing anything
+  std::unordered_set<int64_t> born;
+  for (int32_t i = 0; i < n; ++i) {
+    if (!bm->seqs.count(parent_ids[i]) && !born.count(parent_ids[i])) return PA_ERR_UNKNOWN_SEQ;
+    if (bm->seqs.count(child_ids[i]) || born.count(child_ids[i])) return PA_ERR_SEQ_EXISTS;
+    born.insert(child_ids[i]);
+  }
+  for (int32_t i = 0; i < n; ++i) pa_bm_fork(bm, parent_ids[i], child_ids[i]);
+  return PA_OK;
+}
+
+int pa_bm_free_many(pa_bm* bm, const int64_t* seq_ids, int32_t n) {
+  if (!bm || n < 0 || (n > 0 && !seq_ids)) return PA_ERR_INVALID;
+  int rc = PA_OK;
+  for (int32_t i = 0; i < n; ++i)
+    if (pa_bm_free(bm, seq_ids[i]) == PA_WARN_DOUBLE_FREE) rc = PA_WARN_DOUBLE_FREE;
+  return rc;
 }
 
 int pa_bm_block_tables(const pa_bm* bm, const int64_t* seq_ids, int32_t n, int32_t max_blocks,

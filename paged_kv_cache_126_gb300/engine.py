@@ -170,6 +170,14 @@ class PagedKVEngine:
     def free(self, seq: int) -> int:
         return self.bm.free(seq)
 
+    def fork_many(self, parents, children) -> None:
+        """Forks in order, all or nothing (one block-manager call)."""
+        self.bm.fork_many(parents, children)
+
+    def free_many(self, seqs) -> int:
+        """Frees in order (one block-manager call)."""
+        return self.bm.free_many(seqs)
+
     def step(self, seqs, k_rows, v_rows):
         """Append one token to each of seqs (batch order). Returns (slots, copies)."""
         ids = self._ids_for(seqs)

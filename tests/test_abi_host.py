@@ -191,6 +191,56 @@ def test_errors_leave_state_unchanged(pa):
     assert bm.free(0) == pa.PA_WARN_DOUBLE_FREE
 
 
+@pytest.mark.parametrize("seed", range(4))
+def test_batched_fork_and_free_match_the_oracle(pa, seed):
+    """fork_many / free_many = the same forks / frees one at a time (oracle), including
+    chained forks inside one batch; a bad batch changes nothing."""
+    rnd = random.Random(seed)
+    n, B = 64, 4
+    order = rnd.sample(range(n), n)
+    bm = pa.BlockManager(n, B, order)
+    ob = OracleBlockManager(n, B, order)
+    for s in range(4):
+        L = rnd.randint(1, 9)
+        assert bm.add_seq(s, L).tolist() == ob.add_seq(s, L)
+    nid = 100
+    for _ in range(12):
+        live = sorted(ob.tables)
+        parents, children = [], []
+        for _ in range(rnd.randint(1, 5)):
+            parents.append(rnd.choice(live + children))
+            children.append(nid)
+            nid += 1
+        bm.fork_many(parents, children)
+        for p_, c_ in zip(parents, children):
+            ob.fork(p_, c_)
+        step = rnd.sample(sorted(ob.tables), min(3, len(ob.tables)))
+        slots, copies = bm.step(step)
+        oslots, ocopies = ob.step(step)
+        assert slots.tolist() == list(oslots) and [tuple(c) for c in copies] == [tuple(c) for c in ocopies]
+        dead = rnd.sample(sorted(ob.tables), max(0, len(ob.tables) - 6))
+        assert bm.free_many(dead) == 0
+        for d in dead:
+            ob.free(d)
+        assert bm.free_list() == list(ob.free_list) and bm.ref_counts() == ob.refs
+        for s_, t in ob.tables.items():
+            assert bm.table(s_) == t
+    live = sorted(ob.tables)
+    before = (bm.free_list(), bm.ref_counts(), [bm.table(s_) for s_ in live])
+    with pytest.raises(pa.PAError) as ei:
+        bm.fork_many([live[0], 999999], [nid, nid + 1])        # second parent unknown
+    assert ei.value.code == pa.PA_ERR_UNKNOWN_SEQ
+    with pytest.raises(pa.PAError) as ei:
+        bm.fork_many([live[0], live[0]], [nid, nid])           # child twice
+    assert ei.value.code == pa.PA_ERR_SEQ_EXISTS
+    with pytest.raises(pa.PAError) as ei:
+        bm.fork_many([live[0]], [live[1]])                     # child already live
+    assert ei.value.code == pa.PA_ERR_SEQ_EXISTS
+    assert (bm.free_list(), bm.ref_counts(), [bm.table(s_) for s_ in live]) == before
+    assert bm.free_many([live[0], live[0]]) == pa.PA_WARN_DOUBLE_FREE  # second is not live
+    assert bm.free_many([]) == 0
+
+
 # ------------------------------------------------------------------ prefix caching
 from oracle.prefix_cache import OraclePrefixBlockManager  # noqa: E402
 

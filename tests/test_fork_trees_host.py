@@ -75,3 +75,46 @@ def test_beam_search_keeps_width():
     for op in w.ops:
         if op[0] == "attend":
             assert len(op[1]) == 3 * 5
+
+
+@pytest.mark.parametrize("kind,kw", [c for c in CASES if c[0] == "beam"])
+def test_grouped_selection_equals_interleaved(pa, kind, kw):
+    """A beam-search selection (the forks and frees between two steps) applied as one
+    batched fork call and then one batched free call leaves the manager exactly as the
+    interleaved single calls do: a fork copies a live beam's table and never touches
+    the free list, and a freed beam is never forked from, so a free cannot release a
+    frame a later fork copies.  Checked against the oracle's op-by-op replay."""
+    w = build(kind, kw)
+    ob = OracleBlockManager(w.num_blocks, w.block_size, list(w.free_order))
+    bm = pa.BlockManager(w.num_blocks, w.block_size, w.free_order)
+    ops = w.ops
+    i = 0
+    while i < len(ops):
+        op = ops[i]
+        if op[0] in ("fork", "free"):
+            j = i
+            while j < len(ops) and ops[j][0] in ("fork", "free"):
+                j += 1
+            for o in ops[i:j]:  # oracle: interleaved, one at a time
+                if o[0] == "fork":
+                    ob.fork(o[1], o[2])
+                else:
+                    ob.free(o[1])
+            forks = [o for o in ops[i:j] if o[0] == "fork"]
+            bm.fork_many([o[1] for o in forks], [o[2] for o in forks])
+            bm.free_many([o[1] for o in ops[i:j] if o[0] == "free"])
+            assert bm.free_list() == list(ob.free_list) and bm.ref_counts() == ob.refs
+            for s_, t in ob.tables.items():
+                assert bm.table(s_) == t
+            i = j
+            continue
+        if op[0] == "add":
+            assert bm.add_seq(op[1], op[2]).tolist() == ob.add_seq(op[1], op[2])
+        elif op[0] == "step":
+            slots, copies = bm.step(op[1])
+            oslots, ocopies = ob.step(op[1])
+            assert slots.tolist() == list(oslots)
+            assert [tuple(c) for c in copies] == [tuple(c) for c in ocopies]
+        i += 1
+    invariants(ob)
+
