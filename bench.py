@@ -789,7 +789,7 @@ def fork_tree_bench(n_prompts=8, prompt_len=2048, width=8, steps=64, share=False
                 assert ops[i + 1][0] == "attend" and ops[i + 1][1] == live
                 e = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
                 _, nc, lens = eng.decode_step(live, step_k, step_v, q, scale, out=out, events=e,
-                                              params={"share_prefix": 1} if share else None)
+                                              params={"share_prefix": 1} if share else {})
                 if record:
                     tables, ln = eng.bm.block_tables(live, mb)
                     unique = len(set(tables[tables >= 0].tolist()))

@@ -46,7 +46,10 @@ def to_device_rows(rows, dtype: str, device) -> torch.Tensor:
 class PagedKVEngine:
     def __init__(self, num_blocks: int, block_size: int, num_heads: int, head_dim: int, dtype: str = "f16", *,
                  free_order=None, device=None, max_seqs: int = 256, max_blocks_per_seq: int | None = None,
-                 ring: int = 4, stream: torch.cuda.Stream | None = None):
+                 ring: int = 4, stream: torch.cuda.Stream | None = None, auto_share: bool = True):
+        # auto_share: decode a batch through the shared-prefix path (pa_decode_ex with
+        # share_prefix) when two neighbouring sequences of it start on the same frame
+        self.auto_share = bool(auto_share)
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
         self.num_blocks, self.B, self.H, self.D = int(num_blocks), int(block_size), int(num_heads), int(head_dim)
         self.dtype = dtype
@@ -227,6 +230,17 @@ class PagedKVEngine:
         pa_prefill(q, self.k_cache, self.v_cache, td, ld, qd, scale, out, stream=self._stream())
         return out
 
+    def _decode_params(self, tables: np.ndarray, params):
+        """Launch options of one decode: the caller's, else the shared-prefix path when two
+        neighbouring sequences of the batch start on the same frame (forks of one parent,
+        prompts admitted through the prefix cache), else the defaults."""
+        if params is not None or not self.auto_share or tables.shape[0] < 2 or tables.shape[1] == 0:
+            return params
+        first = tables[:, 0]
+        if np.any((first[1:] == first[:-1]) & (first[1:] >= 0)):
+            return {"share_prefix": 1}
+        return None
+
     def attend(self, seqs, q, scale: float, out=None, params=None) -> torch.Tensor:
         """Decode attention for seqs with queries q [n, H, D]."""
         ids = self._ids_for(seqs)
@@ -240,7 +254,7 @@ class PagedKVEngine:
         self.bm.block_tables_into(ids, self.max_blocks, tables, lens)
         dev = self._upload(i, n + n * self.max_blocks)
         pa_decode(q, self.k_cache, self.v_cache, dev[n:n + n * self.max_blocks].view(n, self.max_blocks),
-                  dev[:n], scale, out, stream=self._stream(), params=params)
+                  dev[:n], scale, out, stream=self._stream(), params=self._decode_params(tables, params))
         return out
 
     def decode_step(self, seqs, k_rows, v_rows, q, scale: float, out=None, params=None, events=None):
@@ -270,7 +284,7 @@ class PagedKVEngine:
         if events is not None:
             events[0].record(st)
         pa_decode(q, self.k_cache, self.v_cache, dev[4 * n:4 * n + n * mb].view(n, mb), dev[3 * n:4 * n],
-                  scale, out, stream=st, params=params)
+                  scale, out, stream=st, params=self._decode_params(tables, params))
         if events is not None:
             events[1].record(st)
         return out, nc, lens

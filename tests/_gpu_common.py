@@ -45,14 +45,17 @@ def assert_attention_close(got: torch.Tensor, ref: np.ndarray, dtype: str, tol: 
     return float(err.max())
 
 
-def run_both(pa, w, params=None, keep_seqs=None, compare_cache=True):
+def run_both(pa, w, params=None, keep_seqs=None, compare_cache=True, auto_share=True):
     """Replay w on the GPU (libpa) and on the oracle; compare traces, BM state, caches.
 
+    auto_share: the engine's automatic choice of the shared-prefix decode for batches
+    whose neighbouring sequences start on the same frame (off: always pa_decode's path).
     Returns (gpu outputs {op: tensor}, oracle result).
     """
     eng = pa.PagedKVEngine(w.num_blocks, w.block_size, w.num_heads, w.head_dim, w.dtype,
                            free_order=w.free_order, max_seqs=max(64, len(w.final_lens)),
-                           max_blocks_per_seq=max(1, max(-(-L // w.block_size) for L in w.final_lens.values())))
+                           max_blocks_per_seq=max(1, max(-(-L // w.block_size) for L in w.final_lens.values())),
+                           auto_share=auto_share)
     outs, trace = pa.run_workload_ops(eng, w, attend_params=params)
     torch.cuda.synchronize()
     assert pa.pa_get_device_status() == 0

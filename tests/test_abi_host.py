@@ -241,6 +241,25 @@ def test_batched_fork_and_free_match_the_oracle(pa, seed):
     assert bm.free_many([]) == 0
 
 
+def test_engine_picks_the_shared_prefix_path(pa):
+    """The engine decodes through the shared-prefix path exactly when two neighbouring
+    sequences of the batch start on the same frame (and never overrides the caller)."""
+    import types
+
+    pick = pa.PagedKVEngine._decode_params
+    on, off = types.SimpleNamespace(auto_share=True), types.SimpleNamespace(auto_share=False)
+    forked = np.array([[5, 9, 2], [5, 9, 7], [1, 3, -1]], np.int32)
+    apart = np.array([[5, 9, 2], [6, 9, 7], [5, 3, -1]], np.int32)   # equal first frames, not neighbours
+    empty = np.array([[-1, -1], [-1, -1]], np.int32)
+    assert pick(on, forked, None) == {"share_prefix": 1}
+    assert pick(on, apart, None) is None
+    assert pick(on, empty, None) is None
+    assert pick(on, forked[:1], None) is None
+    assert pick(off, forked, None) is None
+    assert pick(on, forked, {}) == {}
+    assert pick(on, forked, {"partition_tokens": -1}) == {"partition_tokens": -1}
+
+
 # ------------------------------------------------------------------ prefix caching
 from oracle.prefix_cache import OraclePrefixBlockManager  # noqa: E402
 
