@@ -221,71 +221,6 @@ __device__ __forceinline__ SItem locate(const DecodeArgs& a, const Plan& pl, int
   return it;
 }
 
-// Log-sum-exp merge of the np partial slots base .. base+np-1 of one (sequence, head),
-// by one warp (16 lanes own the 16-byte output chunks).  Partials written by other
-// thread blocks are read past L1.
-template <typename T, int D>
-__device__ __forceinline__ void merge_slots(const DecodeArgs& a, int s, int head, int base, int np, int lane,
-                                            int c) {
-  constexpr int VEC = 16 / sizeof(T);
-  constexpr int LPR = D / VEC;
-  auto ml_at = [&](int p) {
-    return __ldcg(reinterpret_cast<const float2*>(a.ws_ml + (static_cast<int64_t>(base + p) * a.H + head) * 2));
-  };
-  float M = -INFINITY;
-  bool bad = false;
-  for (int p = lane; p < np; p += 32) {
-    const float2 ml = ml_at(p);
-    M = fmaxf(M, ml.x);
-    bad |= ml.y < 0.f;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-  bad = __any_sync(kFull, bad);
-  float num[VEC];
-#pragma unroll
-  for (int v = 0; v < VEC; ++v) num[v] = 0.f;
-  float den = 0.f;
-  if (!bad && M != -INFINITY) {
-    for (int p0 = 0; p0 < np; p0 += 32) {
-      float wgt = 0.f, wl = 0.f;
-      const int p = p0 + lane;
-      if (p < np) {
-        const float2 ml = ml_at(p);
-        wgt = ex2(ml.x - M);
-        wl = wgt * ml.y;
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) wl += __shfl_xor_sync(kFull, wl, off);
-      den += wl;
-      const int n = min(32, np - p0);
-      for (int j = 0; j < n; ++j) {
-        const float sc = __shfl_sync(kFull, wgt, j);
-        if (lane < LPR) {
-          const float* src = a.ws_o + (static_cast<int64_t>(base + p0 + j) * a.H + head) * D + c * VEC;
-#pragma unroll
-          for (int v = 0; v < VEC; v += 4) {
-            const float4 x = __ldcg(reinterpret_cast<const float4*>(src + v));
-            num[v] = fmaf(sc, x.x, num[v]);
-            num[v + 1] = fmaf(sc, x.y, num[v + 1]);
-            num[v + 2] = fmaf(sc, x.z, num[v + 2]);
-            num[v + 3] = fmaf(sc, x.w, num[v + 3]);
-          }
-        }
-      }
-    }
-  }
-  if (lane < LPR) {
-    const bool zero = bad || !(den > 0.f);
-    const float inv = zero ? 0.f : 1.f / den;
-    float res[VEC];
-#pragma unroll
-    for (int v = 0; v < VEC; ++v) res[v] = zero ? 0.f : num[v] * inv;
-    T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(s) * a.out_row + static_cast<int64_t>(head) * D + c * VEC;
-    Chunk<T>::store(op, res);
-  }
-}
-
 // One work item of a consumer warp (head h of the item's head group): the n <= 16
 // queries of sequences s .. s+n-1 as the rows of a 16-row tensor-core tile (rows >= n
 // zero), every staged unit of 16 keys as
@@ -920,11 +855,14 @@ __global__ void __launch_bounds__(32 * (HG + 1), 2)
 
 // Log-sum-exp merge of every split (sequence, head), one warp each, after the decode
 // kernel has finished (programmatic dependent launch: the wait returns once every
-// partial is written and visible).
+// partial is written and visible).  Lane p holds part p's (max, sum) -- parts in chunks
+// of 32 -- and lane l accumulates output dimensions 4l .. 4l+3 over the parts, with the
+// loads of four parts in flight at a time.
 template <typename T>
 __global__ void __launch_bounds__(256) merge_shared_kernel(const DecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  constexpr int D = 128;
   const int lane = threadIdx.x & 31;
   const int64_t wi = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (wi >= static_cast<int64_t>(a.S) * a.H) return;
@@ -932,7 +870,73 @@ __global__ void __launch_bounds__(256) merge_shared_kernel(const DecodeArgs a) {
   const int base = a.pbase_out[s];
   const int np = a.pbase_out[s + 1] - base;
   if (np <= 1) return;  // written directly by the decode kernel
-  merge_slots<T, 128>(a, s, head, base, np, lane, lane & 15);
+  auto ml_at = [&](int p) {
+    return __ldcg(reinterpret_cast<const float2*>(a.ws_ml + (static_cast<int64_t>(base + p) * a.H + head) * 2));
+  };
+  // 1. the largest running max, and whether any part was poisoned
+  float M = -INFINITY;
+  bool bad = false;
+  float2 first = make_float2(-INFINITY, 0.f);
+  for (int p0 = 0; p0 < np; p0 += 32) {
+    const float2 ml = p0 + lane < np ? ml_at(p0 + lane) : make_float2(-INFINITY, 0.f);
+    if (p0 == 0) first = ml;
+    M = fmaxf(M, ml.x);
+    bad |= p0 + lane < np && ml.y < 0.f;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+  bad = __any_sync(kFull, bad);
+  // 2. weights 2^(m_p - M), the denominator, and the weighted sum of the partial outputs
+  float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+  if (!bad && M != -INFINITY) {
+    const float* ob = a.ws_o + (static_cast<int64_t>(base) * a.H + head) * D + 4 * lane;
+    const int64_t pstride = static_cast<int64_t>(a.H) * D;
+    for (int p0 = 0; p0 < np; p0 += 32) {
+      const float2 ml = p0 == 0 ? first : (p0 + lane < np ? ml_at(p0 + lane) : make_float2(-INFINITY, 0.f));
+      const float wgt = p0 + lane < np ? ex2(ml.x - M) : 0.f;
+      float wl = wgt * ml.y;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) wl += __shfl_xor_sync(kFull, wl, off);
+      den += wl;
+      const int n = min(32, np - p0);
+      for (int j = 0; j < n; j += 4) {
+        float4 x[4];
+        float w4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          w4[u] = __shfl_sync(kFull, wgt, (j + u) & 31);
+          x[u] = j + u < n ? __ldcg(reinterpret_cast<const float4*>(ob + (p0 + j + u) * pstride))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (j + u >= n) break;
+          num.x = fmaf(w4[u], x[u].x, num.x);
+          num.y = fmaf(w4[u], x[u].y, num.y);
+          num.z = fmaf(w4[u], x[u].z, num.z);
+          num.w = fmaf(w4[u], x[u].w, num.w);
+        }
+      }
+    }
+  }
+  const bool zero = bad || !(den > 0.f);
+  const float inv = zero ? 0.f : 1.f / den;
+  T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(s) * a.out_row + static_cast<int64_t>(head) * D + 4 * lane;
+  if constexpr (std::is_same<T, __half>::value) {
+    const __half2 lo = __floats2half2_rn(num.x * inv, num.y * inv), hi = __floats2half2_rn(num.z * inv, num.w * inv);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&lo);
+    u.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(op) = u;
+  } else {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(num.x * inv, num.y * inv);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(num.z * inv, num.w * inv);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&lo);
+    u.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(op) = u;
+  }
 }
 
 // lcp[s]: leading tokens sequence s reads through the same frame ids as s - 1.
