@@ -64,7 +64,8 @@ class PagedKVEngine:
         self._pin = [torch.empty(cap, dtype=torch.int32, pin_memory=True) for _ in range(ring)]
         self._pin_np = [p.numpy() for p in self._pin]
         self._dev = torch.empty(cap, dtype=torch.int32, device=self.device)
-        self._events = [None] * ring
+        self._events = [torch.cuda.Event() for _ in range(ring)]  # the copy that last read each buffer
+        self._recorded = [False] * ring
         self._k = 0
         self._ids_key = None
         self._ids = None
@@ -86,18 +87,19 @@ class PagedKVEngine:
         """Next pinned staging buffer, once the copy that last read it has run."""
         i = self._k % len(self._pin)
         self._k += 1
-        ev = self._events[i]
-        if ev is not None:
-            ev.synchronize()
+        if self._recorded[i]:
+            self._events[i].synchronize()
         return i
 
     def _upload(self, i: int, n: int) -> torch.Tensor:
-        st = self._stream()
-        with torch.cuda.stream(st):
+        if self.stream is None:  # the current stream: no stream switch needed
             self._dev[:n].copy_(self._pin[i][:n], non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record(st)
-        self._events[i] = ev
+            self._events[i].record()
+        else:
+            with torch.cuda.stream(self.stream):
+                self._dev[:n].copy_(self._pin[i][:n], non_blocking=True)
+                self._events[i].record(self.stream)
+        self._recorded[i] = True
         return self._dev
 
     # -- sequence operations -------------------------------------------------------------------
