@@ -53,7 +53,6 @@
 namespace pa {
 namespace ds {
 
-using dk::Chunk;
 using dk::kFull;
 using dk::mbar_arrive;
 using dk::mbar_arrive_expect_tx;
@@ -403,7 +402,6 @@ __device__ __forceinline__ void run_item(const DecodeArgs& a, const Plan& pl, co
     l[ri] += __shfl_xor_sync(kFull, l[ri], 1);
     l[ri] += __shfl_xor_sync(kFull, l[ri], 2);
   }
-  unsigned need_merge = 0;  // bit r: this lane's member row r finished a split (sequence, head)
 #pragma unroll
   for (int ri = 0; ri < 2; ++ri) {
     const int row = g + 8 * ri;
@@ -431,10 +429,9 @@ __device__ __forceinline__ void run_item(const DecodeArgs& a, const Plan& pl, co
       for (int jj = 0; jj < 16; ++jj)
         *reinterpret_cast<float2*>(wo + jj * 8 + 2 * t) = make_float2(o[jj][2 * ri], o[jj][2 * ri + 1]);
       if (t == 0) *reinterpret_cast<float2*>(a.ws_ml + slot * 2) = make_float2(m[ri], poisoned ? -1.f : l[ri]);
-      need_merge |= 1u << ri;
     }
   }
-  (void)need_merge;  // split (sequence, head) pairs are merged by merge_shared_kernel
+  // sequences with more than one part are merged by merge_shared_kernel
 }
 
 // Inclusive scan of arr[1 .. n] in place by one warp (arr[0] = 0 is left alone).
@@ -491,7 +488,7 @@ __global__ void __launch_bounds__(32 * (HG + 1), 2)
   int32_t* offa = reinterpret_cast<int32_t*>(smem + lay.offa);
   int32_t* order = reinterpret_cast<int32_t*>(smem + lay.order);
   int32_t* hist = reinterpret_cast<int32_t*>(smem + lay.hist);
-  float* comb = reinterpret_cast<float*>(smem + lay.comb);
+  float* comb = reinterpret_cast<float*>(smem + lay.comb);  // setup reductions
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
