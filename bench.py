@@ -728,8 +728,10 @@ def fork_tree_bench(n_prompts=8, prompt_len=2048, width=8, steps=64, share=False
     manager (step with copy-on-write, then the selection's forks and frees in one
     batched call each), staged
     upload, pa_copy_blocks, pa_cache_append and pa_decode over every live beam.
-    One JSON line: step time end to end, decode time (CUDA events), decode GB/s of
-    logical bytes (what the beams attend) and of the unique frames they hold."""
+    One JSON line: step time end to end, decode time (CUDA events around a repeat of
+    each step's decode queued behind a short GPU sleep, so host enqueue gaps are not
+    counted), decode GB/s of logical bytes (what the beams attend) and of the unique
+    frames they hold."""
     import time
 
     import numpy as np
@@ -752,6 +754,7 @@ def fork_tree_bench(n_prompts=8, prompt_len=2048, width=8, steps=64, share=False
     step_v = torch.randn((nbeams, H, D), generator=g, device=dev).to(torch.float16)
     q = torch.randn((nbeams, H, D), generator=g, device=dev).to(torch.float16)
     out = torch.empty_like(q)
+    out2 = torch.empty_like(q)
     scale = 1.0 / float(np.sqrt(D))
     row = 2 * H * D * 2  # K + V bytes of one token of one sequence
 
@@ -787,15 +790,20 @@ def fork_tree_bench(n_prompts=8, prompt_len=2048, width=8, steps=64, share=False
             elif op[0] == "step":
                 live = op[1]
                 assert ops[i + 1][0] == "attend" and ops[i + 1][1] == live
-                e = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-                _, nc, lens = eng.decode_step(live, step_k, step_v, q, scale, out=out, events=e,
-                                              params={"share_prefix": 1} if share else {})
+                prm = {"share_prefix": 1} if share else {}
+                _, nc, lens = eng.decode_step(live, step_k, step_v, q, scale, out=out, params=prm)
                 if record:
+                    # decode time: the same decode again behind a short GPU sleep, so the host
+                    # has enqueued it before the start event runs and the events bracket GPU
+                    # work only (the host side of a step takes longer than a shared decode)
+                    e = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+                    torch.cuda._sleep(400_000)
+                    eng.attend(live, q, scale, out=out2, params=prm, events=e)
                     tables, ln = eng.bm.block_tables(live, mb)
                     unique = len(set(tables[tables >= 0].tolist()))
                     stats.append((e, int(ln.sum()) * row, unique * B * row, nc))
                 else:
-                    stats.append((e, 0, 0, nc))
+                    stats.append((None, 0, 0, nc))
                 i += 1
             i += 1
         torch.cuda.synchronize()

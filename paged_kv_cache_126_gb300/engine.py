@@ -243,8 +243,9 @@ class PagedKVEngine:
             return {"share_prefix": 1}
         return None
 
-    def attend(self, seqs, q, scale: float, out=None, params=None) -> torch.Tensor:
-        """Decode attention for seqs with queries q [n, H, D]."""
+    def attend(self, seqs, q, scale: float, out=None, params=None, events=None) -> torch.Tensor:
+        """Decode attention for seqs with queries q [n, H, D].  ``events`` (start, end):
+        CUDA events recorded on the engine stream around the pa_decode call."""
         ids = self._ids_for(seqs)
         n = len(ids)
         q = to_device_rows(q, self.dtype, self.device)
@@ -255,8 +256,13 @@ class PagedKVEngine:
         lens, tables = buf[:n], buf[n:n + n * self.max_blocks].reshape(n, self.max_blocks)
         self.bm.block_tables_into(ids, self.max_blocks, tables, lens)
         dev = self._upload(i, n + n * self.max_blocks)
+        p = self._decode_params(tables, params)
+        if events is not None:
+            events[0].record(self._stream())
         pa_decode(q, self.k_cache, self.v_cache, dev[n:n + n * self.max_blocks].view(n, self.max_blocks),
-                  dev[:n], scale, out, stream=self._stream(), params=self._decode_params(tables, params))
+                  dev[:n], scale, out, stream=self._stream(), params=p)
+        if events is not None:
+            events[1].record(self._stream())
         return out
 
     def decode_step(self, seqs, k_rows, v_rows, q, scale: float, out=None, params=None, events=None):
