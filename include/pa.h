@@ -387,6 +387,25 @@ int pa_bm_free(pa_bm* bm, int64_t seq_id);
 int pa_bm_fork_many(pa_bm* bm, const int64_t* parent_ids, const int64_t* child_ids, int32_t n);
 int pa_bm_free_many(pa_bm* bm, const int64_t* seq_ids, int32_t n);
 
+/* One decode step of a batch with the host side done natively: pa_bm_step for
+ * seq_ids[0..n) (one token each, copy-on-write as pa_bm_append), the batch's block
+ * tables [n, max_blocks] and lengths, one asynchronous upload from a library-owned
+ * pinned staging ring (per device and stream, four slots, each reused only after the
+ * copy that last read it has run), then pa_copy_blocks (when a shared tail was
+ * written), pa_cache_append of k_new / v_new [n, H, D] (device) at the step's slots,
+ * and pa_decode_ex of q [n, H, D] into out, all on `stream`.  params may be NULL:
+ * automatic launch options, with share_prefix = 1 when auto_share is set and two
+ * neighbouring sequences of the batch start on the same frame.  *n_copies_out (may
+ * be NULL) receives the number of frame copies; lens_out (host, n entries, may be
+ * NULL) the context lengths attended.  Errors: those of pa_bm_step leave everything
+ * unchanged and launch nothing; PA_ERR_CAPACITY (a table longer than max_blocks) and
+ * errors of the device calls come after the block-manager step, which stands. */
+int pa_step_decode(pa_bm* bm, const int64_t* seq_ids, int32_t n, int32_t max_blocks,
+                   const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* q,
+                   const pa_tensor* k_cache, const pa_tensor* v_cache, float scale,
+                   const pa_tensor* out, const pa_decode_params* params, int32_t auto_share,
+                   pa_stream stream, int32_t* n_copies_out, int32_t* lens_out);
+
 /* Block tables [n, max_blocks] (row-major, unused entries -1) and lengths [n] of
  * the listed sequences, ready to upload for pa_decode.  PA_ERR_CAPACITY if a
  * table is longer than max_blocks. lens_out may be NULL. */

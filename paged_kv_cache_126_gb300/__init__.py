@@ -31,6 +31,7 @@ from ._binding import (  # noqa: F401
     pa_decode_split,
     pa_decode_static,
     pa_prefill,
+    pa_step_decode,
     pa_get_device_status,
     pa_launch_count,
     pa_shutdown,

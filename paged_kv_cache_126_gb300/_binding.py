@@ -78,6 +78,8 @@ def _load():
         "pa_bm_step": ([vp, i64p, C.c_int32, i32p, i32p, i32p], C.c_int),
         "pa_bm_extend": ([vp, C.c_int64, C.c_int32, i32p, i32p, i32p], C.c_int),
         "pa_bm_fork": ([vp, C.c_int64, C.c_int64], C.c_int),
+        "pa_step_decode": ([vp, i64p, C.c_int32, C.c_int32, P, P, P, P, P, C.c_float, P,
+                            C.POINTER(PaDecodeParams), C.c_int32, vp, i32p, i32p], C.c_int),
         "pa_bm_fork_many": ([vp, i64p, i64p, C.c_int32], C.c_int),
         "pa_bm_free_many": ([vp, i64p, C.c_int32], C.c_int),
         "pa_bm_free": ([vp, C.c_int64], C.c_int),
@@ -110,7 +112,7 @@ EXPORTED = (
     "pa_bm_append", "pa_bm_step", "pa_bm_extend", "pa_bm_fork", "pa_bm_free", "pa_bm_block_tables", "pa_bm_seq_info",
     "pa_bm_table", "pa_bm_slot", "pa_bm_num_free", "pa_bm_free_list", "pa_bm_ref_counts",
     "pa_bm_num_seqs", "pa_bm_add_seq_cached", "pa_bm_step_tokens", "pa_bm_extend_tokens", "pa_bm_cached_frames",
-    "pa_bm_fork_many", "pa_bm_free_many",
+    "pa_bm_fork_many", "pa_bm_free_many", "pa_step_decode",
 )
 
 
@@ -214,6 +216,25 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, strea
 def pa_decode_ex(q, k_cache, v_cache, block_tables, context_lens, scale, out, params=None, stream=None):
     return pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, stream=stream,
                      params=params or {})
+
+
+def pa_step_decode(bm, seq_ids, max_blocks, k_new, v_new, q, k_cache, v_cache, scale, out, params=None,
+                   auto_share=True, stream=None, lens_out=None) -> int:
+    """One decode step with the host side in libpa (see include/pa.h): block-manager step,
+    tables, one staged upload, copy-on-write copies, append and decode.  seq_ids: int64
+    host array; lens_out: optional int32 host array of len(seq_ids) for the context
+    lengths.  Returns the number of copy-on-write frame copies."""
+    st = _stream_of(q, stream)
+    ids = seq_ids if isinstance(seq_ids, np.ndarray) and seq_ids.dtype == np.int64 else \
+        np.ascontiguousarray(seq_ids, dtype=np.int64)
+    ds = [tensor_desc(t) for t in (k_new, v_new, q, k_cache, v_cache)]
+    o = tensor_desc(out)
+    p = make_params(params)
+    nc = C.c_int32()
+    _check(LIB.pa_step_decode(bm._h, _i64(ids), len(ids), int(max_blocks), *map(_ref, ds), C.c_float(scale),
+                              C.byref(o), C.byref(p) if p is not None else None, int(bool(auto_share)), st,
+                              C.byref(nc), _i32(lens_out) if lens_out is not None else None), "pa_step_decode")
+    return nc.value
 
 
 def pa_decode_static(q, k_cache, v_cache, block_tables, context_lens, scale, out, stream=None):

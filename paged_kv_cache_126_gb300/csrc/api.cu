@@ -265,6 +265,9 @@ int64_t unit_rows(int64_t B, int wph, bool fast_rows) {
   return B;
 }
 
+// pinned staging of pa_step_decode (defined with it, below)
+void release_step_stages();
+
 }  // namespace
 
 size_t pa::decode_smem_bytes(const DecodeCfg& c, int elem, int R, int S) {
@@ -311,6 +314,7 @@ int pa_get_device_status(pa_stream stream, int32_t* status_out) {
 }
 
 int pa_shutdown(void) {
+  release_step_stages();
   std::lock_guard<std::mutex> lk(g_ws_mu);
   int prev = -1;
   cudaGetDevice(&prev);
@@ -998,4 +1002,146 @@ extern "C" int pa_decode_static(const pa_tensor* q, const pa_tensor* k_cache, co
     return PA_ERR_CUDA;
   g_launches.fetch_add(1);
   return PA_OK;
+}
+
+// ---- one decode step in one call ------------------------------------------------------------
+// The host side of a step (block-manager step, table export, one upload, three launches)
+// costs tens of microseconds per call through a binding; a shared-prefix decode of a
+// beam-search batch takes about as long on the GPU.  pa_step_decode does the whole host
+// side natively.  Its staging buffers form a ring per (device, stream): pinned host
+// memory the step writes, device memory one asynchronous copy fills, and an event per
+// slot marking when the copy that last read it has run.
+namespace {
+constexpr int kStepRing = 4;
+
+struct StepStage {
+  int32_t* host[kStepRing] = {};
+  int32_t* dev[kStepRing] = {};
+  cudaEvent_t done[kStepRing] = {};
+  bool recorded[kStepRing] = {};
+  size_t cap = 0;  // int32 elements per slot
+  int next = 0;
+};
+std::mutex g_step_mu;
+std::map<std::pair<int, cudaStream_t>, StepStage> g_step;
+
+void free_stage(StepStage& s) {
+  for (int i = 0; i < kStepRing; ++i) {
+    if (s.host[i]) cudaFreeHost(s.host[i]);
+    if (s.dev[i]) cudaFree(s.dev[i]);
+    if (s.done[i]) cudaEventDestroy(s.done[i]);
+    s.host[i] = nullptr;
+    s.dev[i] = nullptr;
+    s.done[i] = nullptr;
+    s.recorded[i] = false;
+  }
+  s.cap = 0;
+}
+
+// A ring slot with room for `need` int32 values, free to overwrite; -1 on a CUDA error.
+int stage_slot(int dev, cudaStream_t stream, size_t need, StepStage** out) {
+  std::lock_guard<std::mutex> lk(g_step_mu);
+  StepStage& s = g_step[{dev, stream}];
+  if (s.cap < need) {
+    if (s.cap && cudaStreamSynchronize(stream) != cudaSuccess) return -1;
+    free_stage(s);
+    const size_t cap = std::max(need, static_cast<size_t>(1) << 14);
+    for (int i = 0; i < kStepRing; ++i) {
+      if (cudaHostAlloc(reinterpret_cast<void**>(&s.host[i]), cap * sizeof(int32_t), cudaHostAllocDefault) !=
+              cudaSuccess ||
+          cudaMalloc(reinterpret_cast<void**>(&s.dev[i]), cap * sizeof(int32_t)) != cudaSuccess ||
+          cudaEventCreateWithFlags(&s.done[i], cudaEventDisableTiming) != cudaSuccess) {
+        free_stage(s);
+        return -1;
+      }
+    }
+    s.cap = cap;
+  }
+  const int i = s.next;
+  s.next = (s.next + 1) % kStepRing;
+  if (s.recorded[i] && cudaEventSynchronize(s.done[i]) != cudaSuccess) return -1;
+  *out = &s;
+  return i;
+}
+
+void release_step_stages() {
+  std::lock_guard<std::mutex> lk(g_step_mu);
+  int prev = -1;
+  cudaGetDevice(&prev);
+  for (auto& kv : g_step) {
+    cudaSetDevice(kv.first.first);
+    free_stage(kv.second);
+  }
+  g_step.clear();
+  if (prev >= 0) cudaSetDevice(prev);
+}
+
+pa_tensor i32_view(int32_t* p, int64_t d0, int64_t d1) {
+  pa_tensor t;
+  std::memset(&t, 0, sizeof(t));
+  t.data = p;
+  t.dtype = PA_I32;
+  t.ndim = d1 > 0 ? 2 : 1;
+  t.shape[0] = d0;
+  t.stride[0] = d1 > 0 ? d1 : 1;
+  if (d1 > 0) {
+    t.shape[1] = d1;
+    t.stride[1] = 1;
+  }
+  return t;
+}
+}  // namespace
+
+extern "C" int pa_step_decode(pa_bm* bm, const int64_t* seq_ids, int32_t n, int32_t max_blocks,
+                              const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* q,
+                              const pa_tensor* k_cache, const pa_tensor* v_cache, float scale, const pa_tensor* out,
+                              const pa_decode_params* params, int32_t auto_share, pa_stream stream,
+                              int32_t* n_copies_out, int32_t* lens_out) {
+  if (!bm || n < 0 || max_blocks <= 0 || (n > 0 && !seq_ids)) return PA_ERR_INVALID;
+  if (n_copies_out) *n_copies_out = 0;
+  if (n == 0) return PA_OK;
+  int dev;
+  PA_TRY(current_device(&dev));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // staging: slots [n] | copies [n][2] | lengths [n] | tables [n][max_blocks]
+  const size_t need = static_cast<size_t>(n) * (4 + static_cast<size_t>(max_blocks));
+  StepStage* s = nullptr;
+  const int i = stage_slot(dev, st, need, &s);
+  if (i < 0) return PA_ERR_CUDA;
+  int32_t* h = s->host[i];
+  int32_t* d = s->dev[i];
+  int32_t nc = 0;
+  PA_TRY(pa_bm_step(bm, seq_ids, n, h, h + n, &nc));
+  PA_TRY(pa_bm_block_tables(bm, seq_ids, n, max_blocks, h + 4 * n, h + 3 * n));
+  if (cudaMemcpyAsync(d, h, need * sizeof(int32_t), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaEventRecord(s->done[i], st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  s->recorded[i] = true;
+  if (n_copies_out) *n_copies_out = nc;
+  if (lens_out) std::memcpy(lens_out, h + 3 * n, sizeof(int32_t) * n);
+  // copy-on-write frame copies, the new rows, then the decode
+  if (nc) {
+    const pa_tensor pairs = i32_view(d + n, nc, 2);
+    PA_TRY(pa_copy_blocks(k_cache, v_cache, &pairs, stream));
+  }
+  const pa_tensor slots = i32_view(d, n, 0);
+  PA_TRY(pa_cache_append(k_new, v_new, &slots, k_cache, v_cache, stream));
+  pa_decode_params p;
+  const pa_decode_params* pp = params;
+  if (!params && auto_share) {
+    // the shared-prefix decode when two neighbouring sequences start on the same frame
+    const int32_t* tb = h + 4 * n;
+    for (int32_t j = 1; j < n; ++j) {
+      if (tb[static_cast<int64_t>(j) * max_blocks] >= 0 &&
+          tb[static_cast<int64_t>(j) * max_blocks] == tb[static_cast<int64_t>(j - 1) * max_blocks]) {
+        std::memset(&p, 0, sizeof(p));
+        p.share_prefix = 1;
+        pp = &p;
+        break;
+      }
+    }
+  }
+  const pa_tensor tables = i32_view(d + 4 * n, n, max_blocks);
+  const pa_tensor lens = i32_view(d + 3 * n, n, 0);
+  return pa_decode_ex(q, k_cache, v_cache, &tables, &lens, scale, out, pp, stream);
 }

@@ -25,6 +25,7 @@ from ._binding import (
     pa_copy_blocks,
     pa_decode,
     pa_prefill,
+    pa_step_decode,
 )
 
 TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
@@ -64,6 +65,7 @@ class PagedKVEngine:
         self._pin = [torch.empty(cap, dtype=torch.int32, pin_memory=True) for _ in range(ring)]
         self._pin_np = [p.numpy() for p in self._pin]
         self._dev = torch.empty(cap, dtype=torch.int32, device=self.device)
+        self._step_lens = [np.empty(self.max_seqs, np.int32) for _ in range(ring)]  # lengths per native step
         self._events = [torch.cuda.Event() for _ in range(ring)]  # the copy that last read each buffer
         self._recorded = [False] * ring
         self._k = 0
@@ -268,12 +270,23 @@ class PagedKVEngine:
     def decode_step(self, seqs, k_rows, v_rows, q, scale: float, out=None, params=None, events=None):
         """append + attend with one staged upload: the whole hot path of one step.
 
-        ``events`` (start, end): CUDA events recorded on the engine stream around
-        the pa_decode call (decode kernel + merge), for timing.
-        Returns (out, number of copy-on-write pairs, staged context lengths view).
+        Without ``events`` the whole host side runs in libpa (pa_step_decode: block-manager
+        step, tables, one staged upload, copies, append, decode).  ``events`` (start, end):
+        CUDA events recorded on the engine stream around the pa_decode call (decode kernel +
+        merge), for timing; the step then runs through the separate calls.
+        Returns (out, number of copy-on-write pairs, context lengths).
         """
         ids = self._ids_for(seqs)
         n = len(ids)
+        if events is None:
+            if out is None:
+                out = torch.empty_like(q)
+            ring = self._step_lens[self._k % len(self._step_lens)]
+            self._k += 1
+            lens = ring[:n] if n <= ring.shape[0] else np.empty(n, np.int32)
+            nc = pa_step_decode(self.bm, ids, self.max_blocks, k_rows, v_rows, q, self.k_cache, self.v_cache, scale,
+                                out, params=params, auto_share=self.auto_share, stream=self._stream(), lens_out=lens)
+            return out, nc, lens
         mb = self.max_blocks
         i = self._stage()
         buf = self._pin_np[i]
