@@ -18,6 +18,7 @@
 // until the free list hands it out again.  A decode step is made all-or-nothing
 // with an undo log replayed in reverse on failure, which restores the free-list
 // order, evicted nodes and registrations exactly.
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -138,6 +139,19 @@ struct pa_bm {
 
   int32_t slot_of(const Seq& s, int32_t pos) const {
     return s.frames[pos / block_size] * block_size + pos % block_size;
+  }
+
+  // slots of positions [from, to) of s into out[0 .. to-from), frame by frame (no
+  // division per token: a prompt's slots are most of its admission's host time)
+  void slots_of(const Seq& s, int32_t from, int32_t to, int32_t* out) const {
+    int32_t pos = from;
+    while (pos < to) {
+      const int32_t b = pos / block_size;
+      const int32_t off = pos - b * block_size;
+      const int32_t end = std::min(to, (b + 1) * block_size);
+      const int32_t base = s.frames[b] * block_size;
+      for (int32_t o = off; pos < end; ++pos, ++o) *out++ = base + o;
+    }
   }
 
   // Pops the front frame; a frame still holding a cached block loses its node.
@@ -308,6 +322,9 @@ int pa_bm_create(int32_t num_blocks, int32_t block_size, const int32_t* free_ord
   bm->block_size = block_size;
   bm->refs.assign(num_blocks, 0);
   bm->frame_node.assign(num_blocks, 0);
+  // at most one registered block per frame: the prefix-cache maps never rehash
+  bm->node_of_key.reserve(static_cast<size_t>(num_blocks));
+  bm->nodes.reserve(static_cast<size_t>(num_blocks));
   bm->free_list.reset(num_blocks);
   if (free_order) {
     std::vector<uint8_t> seen(num_blocks, 0);
@@ -339,7 +356,7 @@ int pa_bm_add_seq(pa_bm* bm, int64_t seq_id, int32_t num_tokens, int32_t* slots_
   for (int32_t j = 0; j < need; ++j) s.frames.push_back(bm->take_frame(nullptr));
   s.len = num_tokens;
   if (slots_out)
-    for (int32_t i = 0; i < num_tokens; ++i) slots_out[i] = bm->slot_of(s, i);
+    bm->slots_of(s, 0, num_tokens, slots_out);
   bm->seqs.emplace(seq_id, std::move(s));
   return PA_OK;
 }
@@ -424,7 +441,7 @@ int pa_bm_add_seq_cached(pa_bm* bm, int64_t seq_id, const int32_t* tokens, int32
     if (static_cast<int64_t>(i + 1) * B <= L) bm->register_block(s, i, &mapped);
   }
   const int32_t n_cached = n_hits * B;
-  for (int32_t i = n_cached; i < L; ++i) slots_out[i - n_cached] = bm->slot_of(s, i);
+  bm->slots_of(s, n_cached, L, slots_out);
   if (n_cached_out) *n_cached_out = n_cached;
   bm->seqs.emplace(seq_id, std::move(s));
   return PA_OK;
