@@ -659,7 +659,9 @@ def prefix_bench(n_requests=16, system_len=2048, user_len=512, reps=10):
     (the first request computes the system prompt), prefix cache already holding it.
     One JSON line per run: prompt tokens admitted per second on the GPU (the append
     of the computed rows + the prefill, CUDA events) and end to end (host block
-    manager + launches + GPU, one synchronize per admission), with the parts."""
+    manager + launches + GPU, one synchronize per admission; the block manager is
+    reset to its starting state before each timed admission, outside the timing),
+    with the parts."""
     import time
 
     import numpy as np
@@ -686,12 +688,15 @@ def prefix_bench(n_requests=16, system_len=2048, user_len=512, reps=10):
     scale = 1.0 / float(np.sqrt(D))
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
 
-    def host_admit(mode):
-        """Block manager only: per request (n_cached, slots of the rows to write)."""
+    def reset(mode):
+        """A fresh block manager (not timed): empty, or holding the system prompt."""
         eng.bm = pa.BlockManager(nb, B)
         if mode == "warm":  # an earlier request left the system prompt in the cache
             eng.bm.add_seq_cached(10 ** 6, warm_prompt)
             eng.bm.free(10 ** 6)
+
+    def host_admit(mode):
+        """Block manager only: per request (n_cached, slots of the rows to write)."""
         res = []
         for i, toks in enumerate(prompts):
             if mode == "none":
@@ -704,6 +709,7 @@ def prefix_bench(n_requests=16, system_len=2048, user_len=512, reps=10):
     for mode in ("none", "cold", "warm"):
         # the rows a model would produce for the tokens that must be computed, laid
         # out contiguously per admission (built once, outside the timed region)
+        reset(mode)
         res = host_admit(mode)
         counts = [L - n for n, _ in res]
         krows = torch.cat([k_rows[i, n:] for i, (n, _) in enumerate(res)])
@@ -725,9 +731,12 @@ def prefix_bench(n_requests=16, system_len=2048, user_len=512, reps=10):
             return t_bm, ev[0].elapsed_time(ev[1]) / 1e3, ev[1].elapsed_time(ev[2]) / 1e3
 
         for _ in range(3):
+            reset(mode)
             admit()
         walls, app, pf, bm_t = [], [], [], []
         for _ in range(reps):
+            reset(mode)
+            torch.cuda.synchronize()
             t0 = time.perf_counter()
             t_bm, t_ap, t_pf = admit()
             walls.append(time.perf_counter() - t0)
