@@ -201,3 +201,31 @@ def test_mcts(pa, batch, B, dtype):
                             seed=60 + batch)
     eng, outs, ref = run_both(pa, w, params={"share_prefix": B})
     check_outputs(w, outs, ref)
+
+
+def test_many_sequences(pa):
+    """2000 sequences: runs of 1..16 siblings of short prompts, the plan's scans over many
+    32-sequence rounds, thousands of parts."""
+    B = 16
+    rng = np.random.default_rng(21)
+    specs = []
+    while len(specs) < 2000:
+        n = int(rng.integers(1, 17))
+        root = len(specs)
+        base = int(rng.integers(20, 200))
+        specs.append((None, 0, base))
+        for _ in range(n - 1):
+            specs.append((root, base // B, base + int(rng.integers(0, 40))))
+    specs = specs[:2000]
+    _run(pa, specs, B=B, H=2, params={"share_prefix": B}, seed=22)
+    _run(pa, specs, B=B, H=2, params={"share_prefix": B, "partition_tokens": B}, seed=23)
+    assert pa.pa_get_device_status() == 0
+
+
+def test_long_shared_prefix(pa):
+    """Four siblings over a 65536-token prompt: many shared parts per chunk."""
+    B = 64
+    specs = [(None, 0, 65536 + 5)] + [(0, 65536 // B, 65536 + t) for t in (0, 100, 3)]
+    for part in (0, 1024):
+        _run(pa, specs, B=B, H=2, params={"share_prefix": 1, "partition_tokens": part}, seed=24)
+    assert pa.pa_get_device_status() == 0
