@@ -16,7 +16,19 @@
 #include "pa.h"
 #include "pa_internal.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 namespace {
+
+// NVTX range around a host entry point (phases show up in Nsight timelines; a push
+// and a pop cost nanoseconds when no tool is attached).
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+  Range(const Range&) = delete;
+  Range& operator=(const Range&) = delete;
+};
+
 
 // Sticky status word, one per device (each device holds its own copy of this
 // module's globals).  Kernels in other translation units receive its address.
@@ -331,6 +343,7 @@ int pa_shutdown(void) {
 
 int pa_cache_append(const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* slot_mapping,
                     const pa_tensor* k_cache, const pa_tensor* v_cache, pa_stream stream) {
+  const Range range("pa_cache_append");
   PA_TRY(check_cache(k_cache, v_cache));
   const int dt = k_cache->dtype;
   const int64_t H = k_cache->shape[2], D = k_cache->shape[3];
@@ -632,6 +645,7 @@ extern "C" {
 int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
                  const pa_tensor* block_tables, const pa_tensor* context_lens, float scale, const pa_tensor* out,
                  const pa_decode_params* params, pa_stream stream) {
+  const Range range("pa_decode");
   PA_TRY(check_cache(k_cache, v_cache));
   const int dt = k_cache->dtype;
   const int64_t nb = k_cache->shape[0], B = k_cache->shape[1], H = k_cache->shape[2], D = k_cache->shape[3];
@@ -793,6 +807,7 @@ int pa_decode(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_c
 int pa_prefill(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_tensor* block_tables,
                const pa_tensor* context_lens, const pa_tensor* query_start, float scale, const pa_tensor* out,
                pa_stream stream) {
+  const Range range("pa_prefill");
   PA_TRY(check_cache(k_cache, v_cache));
   const int dt = k_cache->dtype;
   if (dt != PA_F16 && dt != PA_BF16) return PA_ERR_UNSUPPORTED;
@@ -1097,6 +1112,7 @@ extern "C" int pa_step_decode(pa_bm* bm, const int64_t* seq_ids, int32_t n, int3
                               const pa_tensor* k_cache, const pa_tensor* v_cache, float scale, const pa_tensor* out,
                               const pa_decode_params* params, int32_t auto_share, pa_stream stream,
                               int32_t* n_copies_out, int32_t* lens_out) {
+  const Range range("pa_step_decode");
   if (!bm || n < 0 || max_blocks <= 0 || (n > 0 && !seq_ids)) return PA_ERR_INVALID;
   if (n_copies_out) *n_copies_out = 0;
   if (n == 0) return PA_OK;
@@ -1111,8 +1127,11 @@ extern "C" int pa_step_decode(pa_bm* bm, const int64_t* seq_ids, int32_t n, int3
   int32_t* h = s->host[i];
   int32_t* d = s->dev[i];
   int32_t nc = 0;
-  PA_TRY(pa_bm_step(bm, seq_ids, n, h, h + n, &nc));
-  PA_TRY(pa_bm_block_tables(bm, seq_ids, n, max_blocks, h + 4 * n, h + 3 * n));
+  {
+    const Range bm_range("block manager step + tables");
+    PA_TRY(pa_bm_step(bm, seq_ids, n, h, h + n, &nc));
+    PA_TRY(pa_bm_block_tables(bm, seq_ids, n, max_blocks, h + 4 * n, h + 3 * n));
+  }
   if (cudaMemcpyAsync(d, h, need * sizeof(int32_t), cudaMemcpyHostToDevice, st) != cudaSuccess ||
       cudaEventRecord(s->done[i], st) != cudaSuccess)
     return PA_ERR_CUDA;
