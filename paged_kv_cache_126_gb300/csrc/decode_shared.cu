@@ -303,27 +303,17 @@ __device__ __forceinline__ void run_item(const DecodeArgs& a, const Plan& pl, co
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
       }
-      // ---- S = Q K^T (two accumulator chains per block of keys, summed) ----
-      float sc[2][4], sd[2][4];
+      // ---- S = Q K^T ----
+      float sc[2][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) sc[0][e] = sc[1][e] = sd[0][e] = sd[1][e] = 0.f;
+      for (int e = 0; e < 4; ++e) sc[0][e] = sc[1][e] = 0.f;
       const uint32_t kaddr = kb + krow;
 #pragma unroll
       for (int kd = 0; kd < 8; ++kd) {
         uint32_t b[4];
         ldsm_x4(kaddr + (kd >> 2) * half_bytes + ((static_cast<uint32_t>((2 * kd) & 7) << 4) ^ kx), b);
-        if (kd & 1) {
-          mma16816<T>(sd[0], qa[kd], b[0], b[1]);
-          mma16816<T>(sd[1], qa[kd], b[2], b[3]);
-        } else {
-          mma16816<T>(sc[0], qa[kd], b[0], b[1]);
-          mma16816<T>(sc[1], qa[kd], b[2], b[3]);
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        sc[0][e] += sd[0][e];
-        sc[1][e] += sd[1][e];
+        mma16816<T>(sc[0], qa[kd], b[0], b[1]);
+        mma16816<T>(sc[1], qa[kd], b[2], b[3]);
       }
       // ---- online softmax (log2 units) ----
       float x[2][4];
