@@ -1008,6 +1008,72 @@ def split_layout_bench(reps=20):
             print(json.dumps(line), flush=True)
 
 
+def _bm_replay(pa, w):
+    """Run a workload's block-manager ops through libpa's native manager (host only)."""
+    bm = pa.BlockManager(w.num_blocks, w.block_size, w.free_order)
+    for op in w.ops:
+        kind = op[0]
+        if kind == "add":
+            bm.add_seq(op[1], op[2])
+        elif kind == "fork":
+            bm.fork(op[1], op[2])
+        elif kind == "step":
+            bm.step(op[1])
+        elif kind == "extend":
+            bm.extend(op[1], op[2])
+        elif kind == "free":
+            bm.free(op[1])
+        elif kind == "add_tokens":
+            bm.add_seq_cached(op[1], op[2])
+        elif kind == "extend_tokens":
+            bm.extend_tokens(op[1], op[2])
+        elif kind == "step_tokens":
+            bm.step_tokens(op[1], op[2])
+    return bm
+
+
+def memory_report(l_max=8192):
+    """Memory held by the paged cache at each workload's final state (host only).
+
+    Paged: frames in use x B slots against the token slots they hold (waste is
+    confined to each sequence's last frame, under B slots); frames shared by forked
+    sequences are held once.  Contiguous counterfactual: every live sequence reserves
+    max(l_max, its workload's longest sequence) slots.
+    """
+    import workloads
+    import paged_kv_cache_126_gb300 as pa
+
+    cases = [(str(k), workloads.build(k)) for k in (0, 1, "1x", 2, 3, 4)]
+    cases.append(("beam", workloads.beam_search(8, 2048, 8, 64, H=32, D=128, B=16, dtype="f16", seed=31)))
+    cases.append(("prefix", workloads.shared_prefix(16, 2048, [512] * 16, H=32, D=128, B=16, dtype="f16",
+                                                    seed=21)))
+    for key, w in cases:
+        t0 = time.perf_counter()
+        bm = _bm_replay(pa, w)
+        u = bm.usage()
+        host_ms = (time.perf_counter() - t0) * 1e3
+        B = w.block_size
+        row_bytes = 2 * w.num_heads * w.head_dim * w.elem_bytes  # K and V of one token
+        slots = u["frames_in_use"] * B
+        lmax = max([l_max] + [int(x) for x in w.final_lens.values()])
+        reserve = u["num_seqs"] * lmax
+        print(json.dumps({
+            "memory": w.name, "key": key, "block_size": B, "seqs": u["num_seqs"],
+            "frames_in_use": u["frames_in_use"], "frames_total": u["frames_total"],
+            "frames_cached": u["frames_cached"], "slots_allocated": slots, "slots_filled": u["slots_filled"],
+            "tokens_logical": u["tokens_logical"], "table_entries": u["table_entries"],
+            "paged_waste_pct": round(100.0 * (1 - u["slots_filled"] / slots), 3) if slots else 0.0,
+            "max_seq_waste_slots": u["max_seq_waste"], "waste_bound_slots": B - 1,
+            "shared_frames_saving_pct": (round(100.0 * (1 - u["frames_in_use"] / u["table_entries"]), 2)
+                                         if u["table_entries"] else 0.0),
+            "contiguous_l_max": lmax,
+            "contiguous_waste_pct": round(100.0 * (1 - u["tokens_logical"] / reserve), 2) if reserve else 0.0,
+            "kv_gb_paged": round(slots * row_bytes / 1e9, 4),
+            "kv_gb_contiguous": round(reserve * row_bytes / 1e9, 4),
+            "replay_host_ms": round(host_ms, 1)}), flush=True)
+        bm.close()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1028,7 +1094,12 @@ def main():
     ap.add_argument("--split-layout", action="store_true", help="decode throughput of the two cache layouts")
     ap.add_argument("--sweep", default=None, metavar="KEYS",
                     help="time pa_decode on each listed workload instead (comma list of 0,1,1x,2,3,3c,3s,4 or 'all')")
+    ap.add_argument("--memory", action="store_true",
+                    help="memory held by the paged cache vs a contiguous reservation, per workload (host only)")
     args = ap.parse_args()
+    if args.memory:
+        memory_report()
+        return
     if args.prefix:
         prefix_bench()
         return

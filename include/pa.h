@@ -421,6 +421,41 @@ int pa_bm_free_list(const pa_bm* bm, int32_t* out, int32_t cap, int32_t* n_out);
 int pa_bm_ref_counts(const pa_bm* bm, int32_t* out, int32_t cap);               /* [num_blocks] */
 int pa_bm_num_seqs(const pa_bm* bm, int32_t* n_out);
 
+/* Memory accounting of the pool as it stands.  Pages: "PagedAttention: Virtual
+ * Memory Guide for LLM Inference", "The Solution" (frames are granted on demand, so
+ * a sequence wastes only the unfilled slots of its last frame: fewer than B) and
+ * "2. Zero-Copy Branching via Copy-on-Write" (forked sequences hold shared frames
+ * once); "Solving the LLM Memory Wall", "Performance Analysis" (slots allocated
+ * against tokens held).  Fields, all counts:
+ *   num_seqs        live sequences
+ *   frames_total    frames in the pool (num_blocks)
+ *   frames_in_use   frames with a reference count above zero
+ *   frames_cached   free frames that still hold a registered block of the prefix
+ *                   cache (reusable by a prompt with the same token prefix)
+ *   table_entries   sum of the live sequences' table lengths: the frames they would
+ *                   hold without sharing
+ *   tokens_logical  sum of the live sequences' lengths
+ *   slots_filled    token slots of frames in use that hold a token of a live
+ *                   sequence; a frame counts the largest fill any of its sharers
+ *                   gives it (sequence length minus the frame's first position,
+ *                   clamped to [0, B])
+ *   max_seq_waste   largest (table length * B - length) over live sequences, 0 when
+ *                   there are none; always < B
+ * Derived: paged waste = 1 - slots_filled / (frames_in_use * B); saving from shared
+ * frames = 1 - frames_in_use / table_entries.  Read only; O(num_blocks + total table
+ * length) time.  Errors: PA_ERR_INVALID for a NULL argument. */
+typedef struct {
+  int64_t num_seqs;
+  int64_t frames_total;
+  int64_t frames_in_use;
+  int64_t frames_cached;
+  int64_t table_entries;
+  int64_t tokens_logical;
+  int64_t slots_filled;
+  int64_t max_seq_waste;
+} pa_bm_usage_t;
+int pa_bm_usage(const pa_bm* bm, pa_bm_usage_t* out);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

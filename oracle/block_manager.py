@@ -175,6 +175,41 @@ class OracleBlockManager:
         L, B = self.lens[seq], self.block_size
         return [min(B, L - j * B) for j in range(len(self.tables[seq]))]
 
+    def _cached_free_frames(self) -> int:
+        return 0  # no prefix cache in the plain manager
+
+    def usage(self) -> dict:
+        """Memory accounting of the pool.
+
+        "PagedAttention: Virtual Memory Guide for LLM Inference", "The Solution": frames
+        come on demand, so only the unfilled slots of a sequence's last frame are wasted
+        (fewer than B per sequence); "2. Zero-Copy Branching via Copy-on-Write": forked
+        sequences hold their shared frames once.  "Solving the LLM Memory Wall",
+        "Performance Analysis": slots allocated against tokens held.
+        """
+        B = self.block_size
+        filled = {}  # frame -> the most slots any sequence holding it has filled
+        entries = tokens = worst = 0
+        for s, table in self.tables.items():
+            L = self.lens[s]
+            entries += len(table)
+            tokens += L
+            worst = max(worst, len(table) * B - L)
+            for j, frame in enumerate(table):
+                held = min(B, max(0, L - j * B))
+                filled[frame] = max(filled.get(frame, 0), held)
+        in_use = [f for f in range(self.num_blocks) if self.refs[f] > 0]
+        return {
+            "num_seqs": len(self.tables),
+            "frames_total": self.num_blocks,
+            "frames_in_use": len(in_use),
+            "frames_cached": self._cached_free_frames(),
+            "table_entries": entries,
+            "tokens_logical": tokens,
+            "slots_filled": sum(filled.get(f, 0) for f in in_use),
+            "max_seq_waste": worst,
+        }
+
     def snapshot(self):
         return {
             "tables": {s: list(t) for s, t in self.tables.items()},

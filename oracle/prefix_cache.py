@@ -207,6 +207,10 @@ class OraclePrefixBlockManager(OracleBlockManager):
         return r
 
     # -- views --------------------------------------------------------------------------
+    def _cached_free_frames(self) -> int:
+        free = set(self.free_list)
+        return sum(1 for f, n in enumerate(self.frame_node) if n and f in free)
+
     def cached_frames(self) -> list[int]:
         """1 for each frame that holds a registered block, else 0."""
         return [1 if n else 0 for n in self.frame_node]

@@ -44,6 +44,12 @@ class PaDecodeParams(C.Structure):
                 ("items_per_cta", C.c_int32), ("generic_only", C.c_int32), ("share_prefix", C.c_int32)]
 
 
+class PaBmUsage(C.Structure):
+    _fields_ = [(name, C.c_int64) for name in (
+        "num_seqs", "frames_total", "frames_in_use", "frames_cached", "table_entries", "tokens_logical",
+        "slots_filled", "max_seq_waste")]
+
+
 class PAError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
@@ -95,6 +101,7 @@ def _load():
         "pa_bm_step_tokens": ([vp, i64p, i32p, C.c_int32, i32p, i32p, i32p], C.c_int),
         "pa_bm_extend_tokens": ([vp, C.c_int64, i32p, C.c_int32, i32p, i32p, i32p], C.c_int),
         "pa_bm_cached_frames": ([vp, i32p, C.c_int32, i32p], C.c_int),
+        "pa_bm_usage": ([vp, C.POINTER(PaBmUsage)], C.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -112,7 +119,7 @@ EXPORTED = (
     "pa_bm_append", "pa_bm_step", "pa_bm_extend", "pa_bm_fork", "pa_bm_free", "pa_bm_block_tables", "pa_bm_seq_info",
     "pa_bm_table", "pa_bm_slot", "pa_bm_num_free", "pa_bm_free_list", "pa_bm_ref_counts",
     "pa_bm_num_seqs", "pa_bm_add_seq_cached", "pa_bm_step_tokens", "pa_bm_extend_tokens", "pa_bm_cached_frames",
-    "pa_bm_fork_many", "pa_bm_free_many", "pa_step_decode",
+    "pa_bm_fork_many", "pa_bm_free_many", "pa_step_decode", "pa_bm_usage",
 )
 
 
@@ -467,3 +474,9 @@ class BlockManager:
         n = C.c_int32()
         _check(LIB.pa_bm_num_seqs(self._h, C.byref(n)), "pa_bm_num_seqs")
         return n.value
+
+    def usage(self) -> dict:
+        """Memory accounting of the pool (``pa_bm_usage``): field name -> count."""
+        u = PaBmUsage()
+        _check(LIB.pa_bm_usage(self._h, C.byref(u)), "pa_bm_usage")
+        return {name: int(getattr(u, name)) for name, _ in PaBmUsage._fields_}

@@ -580,4 +580,35 @@ int pa_bm_num_seqs(const pa_bm* bm, int32_t* n_out) {
   return PA_OK;
 }
 
+int pa_bm_usage(const pa_bm* bm, pa_bm_usage_t* out) {
+  if (!bm || !out) return PA_ERR_INVALID;
+  const int64_t B = bm->block_size;
+  pa_bm_usage_t u{};
+  u.num_seqs = static_cast<int64_t>(bm->seqs.size());
+  u.frames_total = bm->num_blocks;
+  std::vector<int32_t> fill(bm->num_blocks, 0);  // largest fill any sharer gives a frame
+  for (const auto& kv : bm->seqs) {
+    const Seq& s = kv.second;
+    const int64_t nf = static_cast<int64_t>(s.frames.size());
+    u.table_entries += nf;
+    u.tokens_logical += s.len;
+    u.max_seq_waste = std::max(u.max_seq_waste, nf * B - s.len);
+    for (int64_t i = 0; i < nf; ++i) {
+      const int32_t f = static_cast<int32_t>(std::min(B, std::max<int64_t>(0, s.len - i * B)));
+      int32_t& slot = fill[s.frames[i]];
+      slot = std::max(slot, f);
+    }
+  }
+  for (int32_t f = 0; f < bm->num_blocks; ++f) {
+    if (bm->refs[f] > 0) {
+      ++u.frames_in_use;
+      u.slots_filled += fill[f];
+    } else if (bm->frame_node[f] != 0 && bm->free_list.contains(f)) {
+      ++u.frames_cached;
+    }
+  }
+  *out = u;
+  return PA_OK;
+}
+
 }  // extern "C"

@@ -8,6 +8,7 @@
   double free, bad arguments.
 """
 
+import json
 import os
 import random
 import re
@@ -54,6 +55,7 @@ def _same_state(bm, ob):
     for s, t in ob.tables.items():
         assert bm.table(s) == t
         assert bm.seq_info(s) == (ob.lens[s], len(t))
+    assert bm.usage() == ob.usage()
 
 
 def test_worked_trace_bit_exact(pa, golden):
@@ -391,3 +393,20 @@ def test_prefix_cache_errors(pa):
     assert n_cached == 0 and len(slots) == 0
     with pytest.raises(ValueError):
         bm.step_tokens([0, 2], [5])                        # one token id per sequence
+
+
+def test_memory_report_lines(pa, capsys):
+    # bench.py --memory: one line per workload from the native manager's accounting;
+    # every sequence wastes fewer than B slots, and at B = 16 the paged waste stays
+    # under the pages' 4 % on every realistic workload.
+    import bench
+    bench.memory_report()
+    lines = [json.loads(x) for x in capsys.readouterr().out.splitlines() if x.startswith("{")]
+    assert [x["key"] for x in lines] == ["0", "1", "1x", "2", "3", "4", "beam", "prefix"]
+    for x in lines:
+        assert 0 <= x["max_seq_waste_slots"] <= x["waste_bound_slots"] == x["block_size"] - 1
+        assert x["slots_filled"] <= x["slots_allocated"] == x["frames_in_use"] * x["block_size"]
+        if x["block_size"] == 16:
+            assert x["paged_waste_pct"] < 4.0
+    shared = {x["key"]: x["shared_frames_saving_pct"] for x in lines}
+    assert shared["3"] > 50 and shared["beam"] > 50 and shared["prefix"] > 50 and shared["1"] == 0

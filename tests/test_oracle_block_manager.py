@@ -211,3 +211,100 @@ def test_random_ops_keep_invariants(seed):
         except OutOfBlocks:
             pass
         _check_invariants(bm)
+
+
+# -- memory accounting (usage) ---------------------------------------------------------------
+
+def test_usage_worked_trace(golden):
+    # Final state of the printed trace: the fill levels it prints give the filled slots,
+    # the frames and each request's waste ("max wastage per block is block_size minus 1").
+    g = golden("worked_allocation_trace.json")
+    bm = OracleBlockManager(g["num_blocks"], g["block_size"])
+    seq = {name: i for i, name in enumerate(g["order"])}
+    for name in g["order"]:
+        bm.add_seq(seq[name], g["prefill"][name])
+    for _ in g["steps"]:
+        bm.step([seq[n] for n in g["order"]])
+    fill = g["steps"][-1]["fill"]
+    u = bm.usage()
+    assert u["num_seqs"] == len(g["order"])
+    assert u["frames_total"] == g["num_blocks"]
+    assert u["frames_in_use"] == sum(len(v) for v in fill.values()) == u["table_entries"]
+    assert u["slots_filled"] == sum(n for v in fill.values() for _, n in v) == u["tokens_logical"]
+    assert u["max_seq_waste"] == max(len(v) * g["block_size"] - sum(n for _, n in v) for v in fill.values())
+    assert u["max_seq_waste"] <= g["block_size"] - 1
+    assert u["frames_cached"] == 0
+
+
+def test_usage_slot_efficiency_example(golden):
+    # "Performance Analysis": 7 tokens at B = 4 fill 7 of 8 slots (87.5 %), against 7 of a
+    # 2048-slot contiguous reservation (0.3 %).
+    g = golden("slot_efficiency.json")
+    bm = OracleBlockManager(16, g["block_size"])
+    bm.add_seq(0, g["seq_len"])
+    u = bm.usage()
+    assert u["frames_in_use"] * g["block_size"] == g["slots"]
+    assert u["frames_in_use"] * g["block_size"] - u["slots_filled"] == g["wasted_slots"] == u["max_seq_waste"]
+    assert round(100 * u["slots_filled"] / (u["frames_in_use"] * g["block_size"]), 1) == g["efficiency_pct_approx"]
+    assert round(100 * u["tokens_logical"] / g["contiguous_prealloc_slots"], 1) == g["contiguous_efficiency_pct_approx"]
+
+
+def test_usage_copy_on_write_trace(golden):
+    # The hand-derived copy-on-write trace: after the fork both sequences hold frames 0, 1
+    # once (2 frames for 4 table entries); alpha's write moves it to frame 2 (slot 36 =
+    # frame 2, offset 4, so frame 2 holds 5 tokens) while beta keeps 4 tokens in frame 1;
+    # beta's two in-place writes (slots 20, 21) bring frame 1 to 6.
+    g = golden("cow_trace.json")
+    B = g["block_size"]
+    bm = OracleBlockManager(g["num_blocks"], B)
+    bm.add_seq(0, g["prompt"])
+    bm.fork(0, 1)
+    u = bm.usage()
+    assert (u["frames_in_use"], u["table_entries"]) == (2, 4)
+    assert (u["slots_filled"], u["tokens_logical"]) == (g["prompt"], 2 * g["prompt"])
+    slot, _ = bm.append(0)
+    assert slot == g["expect"]["append_alpha"]["slot"]
+    u = bm.usage()
+    assert (u["frames_in_use"], u["table_entries"]) == (3, 4)
+    assert u["slots_filled"] == B + (g["prompt"] - B) + (slot % B + 1)
+    bm.append(1)
+    bm.append(1)
+    u = bm.usage()
+    assert u["slots_filled"] == B + (g["prompt"] - B + 2) + (slot % B + 1)
+    assert u["tokens_logical"] == 3 * g["prompt"] + 3 - g["prompt"]
+    assert u["max_seq_waste"] == max(2 * B - (g["prompt"] + 1), 2 * B - (g["prompt"] + 2))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_usage_brute_force(seed):
+    # Filled slots = the distinct flat slots of every live (sequence, position); frames in
+    # use = the distinct frames of the live tables; waste per sequence stays below B.
+    rnd = random.Random(300 + seed)
+    B = rnd.choice([1, 3, 8, 16])
+    bm = OracleBlockManager(rnd.randint(20, 60), B)
+    nxt = 0
+    for _ in range(200):
+        live = list(bm.tables)
+        r = rnd.random()
+        try:
+            if r < 0.25 or not live:
+                bm.add_seq(nxt, rnd.randint(0, 3 * B))
+                nxt += 1
+            elif r < 0.45:
+                bm.fork(rnd.choice(live), nxt)
+                nxt += 1
+            elif r < 0.55:
+                bm.free(rnd.choice(live))
+            else:
+                bm.step([rnd.choice(live) for _ in range(rnd.randint(1, 4))])
+        except OutOfBlocks:
+            pass
+        u = bm.usage()
+        slots = {bm.slot(s, i) for s in bm.tables for i in range(bm.lens[s])}
+        frames = {f for t in bm.tables.values() for f in t}
+        assert u["slots_filled"] == len(slots)
+        assert u["frames_in_use"] == len(frames) == sum(1 for c in bm.refs if c > 0)
+        assert u["table_entries"] == sum(len(t) for t in bm.tables.values())
+        assert u["tokens_logical"] == sum(bm.lens.values())
+        assert 0 <= u["max_seq_waste"] < B
+        assert u["frames_in_use"] + bm.free_count == bm.num_blocks

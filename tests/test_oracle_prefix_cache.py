@@ -287,3 +287,22 @@ def test_prefill_through_reused_frames_equals_definition(turns, free_between, B)
         for j, s in enumerate(w.ops[i][1]):
             want = _logical_prefill(w, i, j, s, counts[j])
             np.testing.assert_allclose(r.outputs[i][j], want, rtol=0, atol=1e-12)
+
+
+def test_usage_counts_cached_free_frames():
+    # A freed prompt's filled blocks stay registered while free; a prompt that reuses
+    # one takes it off the free list (no longer counted as cached-and-free), the
+    # partial block was never registered.
+    B = 4
+    bm = OraclePrefixBlockManager(10, B)
+    first = list(range(100, 110))  # 10 tokens: blocks 0, 1 filled, block 2 partial
+    bm.add_seq_cached(0, first)
+    u = bm.usage()
+    assert (u["frames_in_use"], u["frames_cached"], u["slots_filled"]) == (3, 0, 10)
+    bm.free(0)
+    u = bm.usage()
+    assert (u["frames_in_use"], u["frames_cached"], u["num_seqs"]) == (0, 2, 0)
+    n_cached, _ = bm.add_seq_cached(1, first[:4] + [7, 7])  # block 0 hits, block 1 is new
+    assert n_cached == 4
+    u = bm.usage()
+    assert (u["frames_in_use"], u["frames_cached"], u["slots_filled"]) == (2, 1, 6)
