@@ -494,12 +494,19 @@ def fixed_variant(args, device):
 SWEEP_KEYS = ("0", "1", "1x", "2", "3", "3c", "3s", "4")
 
 
-def sweep(keys, reps=20):
+def sweep(keys, reps=20, flushed_reps=50):
     """pa_decode on the final state of each workload's replay (host-generated data,
     automatic launch options): one JSON line per workload.  "3c" is the unshared
     control of the parallel-sampling workload: the same final lengths, every branch
     with private frames; "3s" is the parallel-sampling workload through the
-    shared-prefix decode (each shared prompt frame read once for its branches)."""
+    shared-prefix decode (each shared prompt frame read once for its branches).
+
+    Two timings: the mean over ``reps`` back-to-back launches (``decode_us``), and the
+    median over ``flushed_reps`` launches each timed alone with CUDA events after a
+    read of twice the L2 size (``flushed``: no K/V byte is served from L2 left warm by
+    the previous launch).  A read leaves clean lines; a memset flush (also reported,
+    ``flushed_memset``) leaves the L2 full of dirty lines, and their write-back
+    (~the L2 size) then lands inside the timed launch."""
     import numpy as np
     import torch
 
@@ -538,6 +545,45 @@ def sweep(keys, reps=20):
         e1.record(st)
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) / n * 1e3
+        l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or 132 * 2 ** 20
+        flush = torch.ones(2 * l2 // 4, dtype=torch.int32, device=dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(flushed_reps)]
+
+        def isolated(fn, clear):
+            for a, b in ev:
+                clear()
+                a.record(st)
+                fn()
+                b.record(st)
+            torch.cuda.synchronize()
+            return float(np.median([a.elapsed_time(b) for a, b in ev])) * 1e3
+
+        def decode():
+            pa.pa_decode(q, eng.k_cache, eng.v_cache, tt, ll, w.scale, out, params=params)
+
+        us_flushed = isolated(decode, lambda: flush.sum())
+        us_memset = isolated(decode, lambda: flush.zero_())
+        # pa_cache_append of one new row per sequence at its last token's slot (the
+        # rows already there, so the cache is unchanged): read k_new, v_new and the
+        # slots, write the two cache rows
+        slots = torch.tensor([eng.bm.slot(s, int(L) - 1) for s, L in zip(seqs, lens) if L > 0],
+                             dtype=torch.int32, device=dev)
+        kn = eng.k_cache.view(-1, w.num_heads, w.head_dim)[slots.long()].contiguous()
+        vn = eng.v_cache.view(-1, w.num_heads, w.head_dim)[slots.long()].contiguous()
+        for _ in range(3):
+            pa.pa_cache_append(kn, vn, slots, eng.k_cache, eng.v_cache)
+        torch.cuda.synchronize()
+        e0.record(st)
+        for _ in range(reps):
+            pa.pa_cache_append(kn, vn, slots, eng.k_cache, eng.v_cache)
+        e1.record(st)
+        torch.cuda.synchronize()
+        ap_us = e0.elapsed_time(e1) / reps * 1e3
+        ap_us_flushed = isolated(lambda: pa.pa_cache_append(kn, vn, slots, eng.k_cache, eng.v_cache),
+                                 lambda: flush.sum())
+        ap_bytes = 4 * kn.numel() * kn.element_size() + 4 * slots.numel()
+        del flush
         logical = algorithmic_bytes(lens, w.num_heads, w.head_dim, w.block_size, w.elem_bytes)
         frames = set()
         for t, L in zip(tables, lens):
@@ -550,8 +596,18 @@ def sweep(keys, reps=20):
             "pct_of_peak": round(100 * logical / (us * 1e-6) / 1e9 / peak, 1),
             "unique_frame_bytes": unique, "gbps_unique_frames": round(unique / (us * 1e-6) / 1e9, 1),
             "seqs_per_sec": round(len(seqs) / (us * 1e-6), 1),
+            "flushed": {"decode_us_median": round(us_flushed, 2), "launches": flushed_reps,
+                        "gbps": round(logical / (us_flushed * 1e-6) / 1e9, 1),
+                        "pct_of_peak": round(100 * logical / (us_flushed * 1e-6) / 1e9 / peak, 1),
+                        "gbps_unique_frames": round(unique / (us_flushed * 1e-6) / 1e9, 1),
+                        "seqs_per_sec": round(len(seqs) / (us_flushed * 1e-6), 1)},
+            "flushed_memset": {"decode_us_median": round(us_memset, 2),
+                               "gbps": round(logical / (us_memset * 1e-6) / 1e9, 1)},
+            "append": {"rows": int(slots.numel()), "bytes": int(ap_bytes), "us": round(ap_us, 2),
+                       "gbps": round(ap_bytes / (ap_us * 1e-6) / 1e9, 1), "us_flushed_median": round(ap_us_flushed, 2),
+                       "gbps_flushed": round(ap_bytes / (ap_us_flushed * 1e-6) / 1e9, 1)},
             "cow_copies": sum(len(t["copies"]) for t in trace.values() if isinstance(t, dict) and "copies" in t)}), flush=True)
-        del eng, outs, tt, ll, q, out
+        del eng, outs, tt, ll, q, out, kn, vn, slots
         torch.cuda.empty_cache()
 
 

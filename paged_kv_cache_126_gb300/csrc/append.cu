@@ -9,7 +9,10 @@
 // duplicated.
 //
 // Both are pure data movement: 16-byte vector loads and stores, one thread block
-// per token row (append) or per slice of a frame (copy), 64-bit byte offsets.
+// per token row (append) or per slice of a frame (copy), 64-bit byte offsets.  An
+// append is a few KB per row, so its time is latency: every thread issues all of
+// its loads (K and V, up to kVecs each) before its first store, one DRAM round trip
+// per row instead of one per vector.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -19,12 +22,15 @@
 namespace pa {
 namespace {
 
+constexpr int kVecs = 4;  // 16-byte vectors per thread and cache held before storing
+
 __global__ void __launch_bounds__(256) cache_append_kernel(const AppendArgs a) {
   // Launched with programmatic stream serialisation: let the next kernel start its
   // set-up now, and wait for the previous kernel's writes before reading inputs.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t nvec = a.row_bytes >> 4;
+  const int64_t stride = static_cast<int64_t>(blockDim.x);
   for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
     const int32_t slot = __ldg(a.slots + t);
     if (slot < 0) continue;  // padding
@@ -36,11 +42,24 @@ __global__ void __launch_bounds__(256) cache_append_kernel(const AppendArgs a) {
     const uint4* vs = reinterpret_cast<const uint4*>(a.v_new + static_cast<int64_t>(t) * a.v_pitch);
     uint4* kd = reinterpret_cast<uint4*>(a.k_cache + static_cast<int64_t>(slot) * a.row_bytes);
     uint4* vd = reinterpret_cast<uint4*>(a.v_cache + static_cast<int64_t>(slot) * a.row_bytes);
-    for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
-      const uint4 kv = __ldg(ks + i);
-      const uint4 vv = __ldg(vs + i);
-      kd[i] = kv;
-      vd[i] = vv;
+    for (int64_t base = threadIdx.x; base < nvec; base += kVecs * stride) {
+      uint4 kr[kVecs], vr[kVecs];
+#pragma unroll
+      for (int u = 0; u < kVecs; ++u) {
+        const int64_t i = base + u * stride;
+        if (i < nvec) {
+          kr[u] = __ldg(ks + i);
+          vr[u] = __ldg(vs + i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kVecs; ++u) {
+        const int64_t i = base + u * stride;
+        if (i < nvec) {
+          kd[i] = kr[u];
+          vd[i] = vr[u];
+        }
+      }
     }
   }
 }
