@@ -149,11 +149,13 @@ def _oracle_sample(cfg, n_seqs, seed_shift=0):
     return w, ref, keep, q[keep], [tables[j] for j in keep], [lens[j] for j in keep]
 
 
-def cpu_baseline_worker(cfg, budget_s: float, per_step: bool = False, steps: int = 0):
+def cpu_baseline_worker(cfg, budget_s: float, per_step: bool = False, steps: int = 0, seed_shift: int = 0):
     """Time the oracle's paged decode (gather + fp64 softmax attention) on host cores."""
     from oracle import paged_decode
 
-    w, ref, keep, q, tables, lens = _oracle_sample(cfg, 4 if not per_step else 8)
+    # the toy has 4 sequences; a long-context sequence (16384 tokens) is a sample by itself
+    n = 1 if cfg == 2 else (4 if (not per_step or cfg == 0) else 8)
+    w, ref, keep, q, tables, lens = _oracle_sample(cfg, n, seed_shift)
     bytes_per_seq = [algorithmic_bytes([L], w.num_heads, w.head_dim, w.block_size, w.elem_bytes) for L in lens]
     if per_step:
         times, byts = [], []
@@ -179,14 +181,50 @@ def cpu_baseline_worker(cfg, budget_s: float, per_step: bool = False, steps: int
             "seqs_per_sec": done / elapsed}
 
 
+_CPU_ENV = dict(OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+
+
+def _cpu_cmd(cfg, budget_s, seed_shift=0):
+    return [sys.executable, os.path.abspath(__file__), "--cpu-worker", str(cfg), "--cpu-budget", str(budget_s),
+            "--cpu-seed-shift", str(seed_shift)]
+
+
 def run_cpu_baseline(cfg, budget_s: float):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", str(cfg), "--cpu-budget", str(budget_s)]
-    res = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=max(600, 20 * budget_s))
+    env = dict(os.environ, **_CPU_ENV)
+    res = subprocess.run(_cpu_cmd(cfg, budget_s), capture_output=True, text=True, env=env,
+                         timeout=max(600, 20 * budget_s))
     if res.returncode != 0:
         return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "error": res.stderr[-400:]}
     return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def cpu_sweep(keys=("0", "1", "2", "3", "4"), budget_s: float = 8.0):
+    """The oracle's decode timed on the host per workload: one thread, then one
+    single-threaded worker per affine core at once (each on its own sampled sequences);
+    one JSON line per workload."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    env = dict(os.environ, **_CPU_ENV)
+    for key in keys:
+        single = run_cpu_baseline(key, budget_s)
+        procs = [subprocess.Popen(_cpu_cmd(key, budget_s, 1 + i), stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                                  text=True, env=env) for i in range(cores)]
+        outs = []
+        for p in procs:
+            o, e = p.communicate(timeout=max(900, 30 * budget_s))
+            if p.returncode != 0:
+                raise SystemExit(f"cpu worker failed: {e[-400:]}")
+            outs.append(json.loads(o.strip().splitlines()[-1]))
+        sps = sum(o["seqs_per_sec"] for o in outs)
+        print(json.dumps({
+            "cpu_baseline": key, "kind": "oracle", "unit": UNIT,
+            "single": {"cores": 1, "gbps": round(single["value"], 3), "seqs_per_sec": round(single["seqs_per_sec"], 2),
+                       "s_per_call": round(1.0 / single["seqs_per_sec"], 5), "sample": single["sample"]},
+            "all_cores": {"cores": cores, "gbps": round(sum(o["value"] for o in outs), 3),
+                          "seqs_per_sec": round(sps, 2), "s_per_call": round(1.0 / sps, 6),
+                          "sample": f"{cores} single-threaded workers at once, each cycling over its own sampled "
+                                    f"sequences for {budget_s:.0f} s of decode time"},
+            "call": "one single-sequence decode (all heads): gather of the sequence's frames, fp64 attention"}),
+            flush=True)
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -453,7 +491,7 @@ def gpu_arm(args):
     if not args.no_extra:
         line["extra"] = {"fixed_64x2048": fixed_variant(args, device)}
     if not args.no_cpu:
-        line["cpu_baseline"] = run_cpu_baseline(args.config, args.cpu_budget)
+        line["cpu_baseline"] = run_cpu_baseline(args.config, args.cpu_budget or 12.0)
     print(json.dumps(line), flush=True)
 
 
@@ -1138,7 +1176,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--batches", type=int, default=16, help="resident copies of the batch decoded in rotation")
     ap.add_argument("--e2e-steps", type=int, default=400)
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--cpu-budget", type=float, default=None,
+                    help="seconds of oracle decode time per CPU measurement (12 in the bench line, 8 per worker in --cpu-sweep)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--config", default="1")
@@ -1150,11 +1189,17 @@ def main():
     ap.add_argument("--split-layout", action="store_true", help="decode throughput of the two cache layouts")
     ap.add_argument("--sweep", default=None, metavar="KEYS",
                     help="time pa_decode on each listed workload instead (comma list of 0,1,1x,2,3,3c,3s,4 or 'all')")
+    ap.add_argument("--cpu-seed-shift", type=int, default=0)
+    ap.add_argument("--cpu-sweep", action="store_true",
+                    help="time the oracle's decode on the host per workload, one thread and all affine cores")
     ap.add_argument("--memory", action="store_true",
                     help="memory held by the paged cache vs a contiguous reservation, per workload (host only)")
     args = ap.parse_args()
     if args.memory:
         memory_report()
+        return
+    if args.cpu_sweep:
+        cpu_sweep(budget_s=args.cpu_budget or 8.0)
         return
     if args.prefix:
         prefix_bench()
@@ -1180,8 +1225,8 @@ def main():
         raise SystemExit("the bench times the decode batch workload (1) or its fixed 64x2048 form (1x)")
     args.config = 1 if args.config == "1" else "1x"
     if args.cpu_worker is not None:
-        cfg = 1 if args.cpu_worker == "1" else "1x"
-        print(json.dumps(cpu_baseline_worker(cfg, args.cpu_budget)), flush=True)
+        cfg = args.cpu_worker if args.cpu_worker == "1x" else int(args.cpu_worker)
+        print(json.dumps(cpu_baseline_worker(cfg, args.cpu_budget or 12.0, seed_shift=args.cpu_seed_shift)), flush=True)
         return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

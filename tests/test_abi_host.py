@@ -410,3 +410,11 @@ def test_memory_report_lines(pa, capsys):
             assert x["paged_waste_pct"] < 4.0
     shared = {x["key"]: x["shared_frames_saving_pct"] for x in lines}
     assert shared["3"] > 50 and shared["beam"] > 50 and shared["prefix"] > 50 and shared["1"] == 0
+
+
+def test_cpu_baseline_worker_runs():
+    # The oracle timing behind bench.py's cpu_baseline and --cpu-sweep (toy workload).
+    import bench
+    r = bench.cpu_baseline_worker(0, 0.2, seed_shift=3)
+    assert r["kind"] == "oracle" and r["cores"] == 1
+    assert r["value"] > 0 and r["seqs_per_sec"] > 0
