@@ -697,6 +697,52 @@ def prefill_bench(reps=20):
     e1.record(st)
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) / reps * 1e3
+    # the same launch timed alone after a read of twice the L2 size (median of 50)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or 132 * 2 ** 20
+    flush = torch.ones(2 * l2 // 4, dtype=torch.int32, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+    for a, b in ev:
+        flush.sum()
+        a.record(st)
+        pa.pa_prefill(q, eng.k_cache, eng.v_cache, tt, ll, qq, w.scale, out)
+        b.record(st)
+    torch.cuda.synchronize()
+    us_flushed = float(np.median([a.elapsed_time(b) for a, b in ev])) * 1e3
+    del flush
+    # End to end through host buffers: every step copies the chunk's queries and its new
+    # K/V rows from pinned host memory, appends the rows at their slots (the values
+    # already there: the cache is unchanged), prefills, and copies the output back.
+    slot_list = []
+    for s_, L_, n_ in zip(seqs, lens, counts):
+        slot_list += [eng.bm.slot(s_, p_) for p_ in range(int(L_) - int(n_), int(L_))]
+    slots = torch.tensor(slot_list, dtype=torch.int32, device=dev)
+    kn = eng.k_cache.view(-1, w.num_heads, w.head_dim)[slots.long()]
+    vn = eng.v_cache.view(-1, w.num_heads, w.head_dim)[slots.long()]
+    hq, hk, hv = (x.cpu().pin_memory() for x in (q, kn, vn))
+    hout = torch.empty_like(out, device="cpu").pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+    k_e2e = 10
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        pa.pa_cache_append(dk, dv, slots, eng.k_cache, eng.v_cache)
+        pa.pa_prefill(dq, eng.k_cache, eng.v_cache, tt, ll, qq, w.scale, out)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0.record(st)
+    for _ in range(k_e2e):
+        e2e_step()
+    e1.record(st)
+    torch.cuda.synchronize()
+    e2e_us = e0.elapsed_time(e1) / k_e2e * 1e3
+    assert torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16))
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+    d2h = hout.numel() * hout.element_size()
     prefix = [int(L) - int(n) for L, n in zip(lens, counts)]
     flops = prefill_flops(prefix, counts, w.num_heads, w.head_dim)
     try:
@@ -709,6 +755,12 @@ def prefill_bench(reps=20):
                       "prefill_us": round(us, 2), "flops": flops, "tflops": round(tf, 1),
                       "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
                                    "frac": round(tf / peak, 4), "peak_source": src},
+                      "flushed": {"prefill_us_median": round(us_flushed, 2), "launches": 50,
+                                  "tflops": round(flops / (us_flushed * 1e-6) / 1e12, 1)},
+                      "e2e": {"us_per_step": round(e2e_us, 2), "tflops": round(flops / (e2e_us * 1e-6) / 1e12, 1),
+                              "steps": k_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                              "step": "queries and the chunk's K/V rows copied from pinned host memory, "
+                                      "pa_cache_append of the chunk, pa_prefill, output copied back"},
                       "query_rows": int(qs[-1]), "dtype": w.dtype}), flush=True)
 
 
