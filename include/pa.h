@@ -421,6 +421,18 @@ int pa_bm_free_list(const pa_bm* bm, int32_t* out, int32_t cap, int32_t* n_out);
 int pa_bm_ref_counts(const pa_bm* bm, int32_t* out, int32_t cap);               /* [num_blocks] */
 int pa_bm_num_seqs(const pa_bm* bm, int32_t* n_out);
 
+/* Self-test of the failure path of every kernel's bounded waits (each mbarrier wait
+ * gives up after ~2 s at the maximum SM clock, raises PA_DEV_TIMEOUT in the status
+ * word and makes the thread block's later waits return at once, so a stuck copy ends
+ * the kernel with an error instead of hanging the GPU).  Launches one small kernel on
+ * `stream` whose first warp waits on an mbarrier that nothing arrives on, then whose
+ * second warp waits on the same barrier; synchronises the stream and writes
+ * result_out[4] (host): the two waits' results (1 = completed, 0 = gave up) and the SM
+ * cycles each took.  Expected: {0, 0, > 4e9, small}, and PA_DEV_TIMEOUT set for the
+ * next pa_get_device_status.  Takes about two seconds; the context stays usable.
+ * Errors: PA_ERR_INVALID (result_out NULL), PA_ERR_CUDA. */
+int pa_selftest_wait_timeout(int64_t* result_out, pa_stream stream);
+
 /* Memory accounting of the pool as it stands.  Pages: "PagedAttention: Virtual
  * Memory Guide for LLM Inference", "The Solution" (frames are granted on demand, so
  * a sequence wastes only the unfilled slots of its last frame: fewer than B) and

@@ -33,6 +33,7 @@ from ._binding import (  # noqa: F401
     pa_prefill,
     pa_step_decode,
     pa_get_device_status,
+    pa_selftest_wait_timeout,
     pa_launch_count,
     pa_shutdown,
     strerror as pa_strerror,

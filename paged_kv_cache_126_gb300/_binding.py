@@ -102,6 +102,7 @@ def _load():
         "pa_bm_extend_tokens": ([vp, C.c_int64, i32p, C.c_int32, i32p, i32p, i32p], C.c_int),
         "pa_bm_cached_frames": ([vp, i32p, C.c_int32, i32p], C.c_int),
         "pa_bm_usage": ([vp, C.POINTER(PaBmUsage)], C.c_int),
+        "pa_selftest_wait_timeout": ([i64p, vp], C.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -119,7 +120,7 @@ EXPORTED = (
     "pa_bm_append", "pa_bm_step", "pa_bm_extend", "pa_bm_fork", "pa_bm_free", "pa_bm_block_tables", "pa_bm_seq_info",
     "pa_bm_table", "pa_bm_slot", "pa_bm_num_free", "pa_bm_free_list", "pa_bm_ref_counts",
     "pa_bm_num_seqs", "pa_bm_add_seq_cached", "pa_bm_step_tokens", "pa_bm_extend_tokens", "pa_bm_cached_frames",
-    "pa_bm_fork_many", "pa_bm_free_many", "pa_step_decode", "pa_bm_usage",
+    "pa_bm_fork_many", "pa_bm_free_many", "pa_step_decode", "pa_bm_usage", "pa_selftest_wait_timeout",
 )
 
 
@@ -286,6 +287,16 @@ def pa_get_device_status(stream=None) -> int:
     v = C.c_int32(0)
     _check(LIB.pa_get_device_status(C.c_void_p(s.cuda_stream), C.byref(v)), "pa_get_device_status")
     return v.value
+
+
+def pa_selftest_wait_timeout(stream=None) -> list:
+    """Run the bounded-wait self-test (about 2 s): [first wait ok, second wait ok,
+    cycles of the first, cycles of the second]."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    res = np.zeros(4, np.int64)
+    _check(LIB.pa_selftest_wait_timeout(res.ctypes.data_as(C.POINTER(C.c_int64)), C.c_void_p(s.cuda_stream)),
+           "pa_selftest_wait_timeout")
+    return res.tolist()
 
 
 def pa_launch_count() -> int:

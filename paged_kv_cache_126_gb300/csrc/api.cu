@@ -36,6 +36,43 @@ __device__ int32_t g_pa_status;
 
 constexpr int kMaxDevices = 64;
 
+// Self-test of the bounded wait that every kernel's mbarrier waits go through
+// (dk::mbar_wait, budget kWaitCycles): warp 0 waits on an mbarrier that nothing ever
+// arrives on, gives up when the budget runs out, raises PA_DEV_TIMEOUT and marks the
+// block aborting; warp 1 then waits on the same barrier and must return at once.
+// res[0], res[1]: the two waits' results (1 = completed, 0 = gave up); res[2], res[3]:
+// the SM cycles each took.
+__global__ void __launch_bounds__(64) selftest_wait_kernel(int32_t* status, long long* res) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int32_t abort_flag;
+  const uint32_t b = pa::dk::smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    pa::dk::mbar_init(b, 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int32_t* ab = &abort_flag;
+  if (warp == 0) {
+    const long long t0 = clock64();
+    const bool ok = __all_sync(pa::dk::kFull, pa::dk::mbar_wait(b, 0, ab, status));
+    if (lane == 0) {
+      res[0] = ok;
+      res[2] = clock64() - t0;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    const long long t0 = clock64();
+    const bool ok = __all_sync(pa::dk::kFull, pa::dk::mbar_wait(b, 0, ab, status));
+    if (lane == 0) {
+      res[1] = ok;
+      res[3] = clock64() - t0;
+    }
+  }
+}
+
 std::atomic<int64_t> g_launches{0};
 
 struct DeviceState {
@@ -322,6 +359,30 @@ int pa_get_device_status(pa_stream stream, int32_t* status_out) {
   if (cudaMemset(g_dev[dev].status, 0, sizeof(v)) != cudaSuccess) return PA_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
   *status_out = v;
+  return PA_OK;
+}
+
+int pa_selftest_wait_timeout(int64_t* result_out, pa_stream stream) {
+  if (!result_out) return PA_ERR_INVALID;
+  int dev;
+  PA_TRY(current_device(&dev));
+  long long* d_res = nullptr;
+  if (cudaMalloc(&d_res, 4 * sizeof(long long)) != cudaSuccess) return PA_ERR_CUDA;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc = PA_OK;
+  if (cudaMemsetAsync(d_res, 0xff, 4 * sizeof(long long), st) != cudaSuccess) rc = PA_ERR_CUDA;
+  if (rc == PA_OK) {
+    selftest_wait_kernel<<<1, 64, 0, st>>>(g_dev[dev].status, d_res);
+    if (cudaGetLastError() != cudaSuccess) rc = PA_ERR_CUDA;
+  }
+  long long h[4] = {-1, -1, -1, -1};
+  if (rc == PA_OK && (cudaMemcpyAsync(h, d_res, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+                      cudaStreamSynchronize(st) != cudaSuccess))
+    rc = PA_ERR_CUDA;
+  cudaFree(d_res);
+  if (rc != PA_OK) return rc;
+  for (int i = 0; i < 4; ++i) result_out[i] = h[i];
+  g_launches.fetch_add(1);
   return PA_OK;
 }
 
