@@ -60,3 +60,22 @@ def test_worked_trace_from_c(trace_output, golden):
     assert u == [sum(len(v) for v in fill.values()), sum(n for v in fill.values() for _, n in v),
                  sum(lens0) + 12, sum(len(v) for v in fill.values()),
                  max(10 * len(v) - sum(n for _, n in v) for v in fill.values())]
+
+
+@pytest.mark.gpu
+def test_device_path_from_c(pa, tmp_path):
+    # pa_cache_append + pa_decode from a C program (CUDA runtime only, descriptors filled by
+    # hand): a one-token context returns its value row, equal keys return the mean of the
+    # value rows, bit for bit in fp16 (tests/c/decode_from_c.c).
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    exe = str(tmp_path / "decode_from_c")
+    cmd = [cc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+           "-I", os.path.join(cuda, "include"), os.path.join(ROOT, "tests", "c", "decode_from_c.c"), "-o", exe,
+           "-L", LIBDIR, "-lpa", "-L", os.path.join(cuda, "lib64"), "-lcudart", f"-Wl,-rpath,{LIBDIR}"]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    res = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert res.returncode == 0, res.stdout + res.stderr
+    assert "mismatches 0 status 0" in res.stdout
