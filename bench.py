@@ -529,7 +529,7 @@ def fixed_variant(args, device):
 
 
 # ----------------------------------------------------------------------------- per-workload sweep
-SWEEP_KEYS = ("0", "1", "1x", "2", "3", "3c", "3s", "4")
+SWEEP_KEYS = ("0", "1", "1x", "2", "2n", "3", "3c", "3s", "4")
 
 
 def sweep(keys, reps=20, flushed_reps=50):
@@ -537,7 +537,9 @@ def sweep(keys, reps=20, flushed_reps=50):
     automatic launch options): one JSON line per workload.  "3c" is the unshared
     control of the parallel-sampling workload: the same final lengths, every branch
     with private frames; "3s" is the parallel-sampling workload through the
-    shared-prefix decode (each shared prompt frame read once for its branches).
+    shared-prefix decode (each shared prompt frame read once for its branches); "2n"
+    is the long-context workload without split-context partitions (one item per
+    sequence and head group), the baseline of the split's speedup.
 
     Two timings: the mean over ``reps`` back-to-back launches (``decode_us``), and the
     median over ``flushed_reps`` launches each timed alone with CUDA events after a
@@ -555,8 +557,8 @@ def sweep(keys, reps=20, flushed_reps=50):
     torch.cuda.set_device(dev)
     st = torch.cuda.current_stream(dev)
     for key in keys:
-        cfg = {"0": 0, "1": 1, "1x": "1x", "2": 2, "3": 3, "3c": 3, "3s": 3, "4": 4}[key]
-        params = {"share_prefix": 1} if key == "3s" else None
+        cfg = {"0": 0, "1": 1, "1x": "1x", "2": 2, "2n": 2, "3": 3, "3c": 3, "3s": 3, "4": 4}[key]
+        params = {"share_prefix": 1} if key == "3s" else ({"partition_tokens": -1} if key == "2n" else None)
         w = workloads.build(cfg)
         if key == "3c":
             L = [w.final_lens[s] for s in range(len(w.final_lens))]
@@ -1240,7 +1242,7 @@ def main():
     ap.add_argument("--block-sweep", action="store_true", help="decode and prefill throughput against block size")
     ap.add_argument("--split-layout", action="store_true", help="decode throughput of the two cache layouts")
     ap.add_argument("--sweep", default=None, metavar="KEYS",
-                    help="time pa_decode on each listed workload instead (comma list of 0,1,1x,2,3,3c,3s,4 or 'all')")
+                    help="time pa_decode on each listed workload instead (comma list of 0,1,1x,2,2n,3,3c,3s,4 or 'all')")
     ap.add_argument("--cpu-seed-shift", type=int, default=0)
     ap.add_argument("--cpu-sweep", action="store_true",
                     help="time the oracle's decode on the host per workload, one thread and all affine cores")

@@ -236,7 +236,7 @@ typedef struct pa_decode_params {
  * of two >= 8 and 2 <= S <= 4096 (other shapes run the plain decode, with the same
  * result).  heads_per_cta, when given, must be 1, 2 or 4 and warps_per_head 0 or 1,
  * else PA_ERR_INVALID.  Uses workspace partials for every sequence that has more than
- * one part, and launches two kernels. */
+ * one part, and launches three kernels (the plan, the decode, the log-sum-exp merge). */
 int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
                  const pa_tensor* block_tables, const pa_tensor* context_lens,
                  float scale, const pa_tensor* out, const pa_decode_params* params,
