@@ -23,10 +23,12 @@
 //     tcgen05.mma issuer, fp32 accumulators in TMEM (512 columns: S_0 S_1 O_0 O_1).
 //     S_q = Q_q K_t^T from shared memory; O_q (+)= P_q V_t with P_q read from TMEM,
 //     where the softmax left it over the first 64 columns of S_q.
-//     warps 2-5 / 6-9: softmax of slot 0 / 1 (thread = query row = TMEM lane):
-//     causal mask, online softmax in log2 units (ex2.approx, fp32) with a lazily
-//     raised reference max, P (operand type) back to TMEM, O rescaled in TMEM when
-//     the reference max moves; normalised rows are written to `out`.
+//     warps 2-9: softmax of both slots, tile by tile (thread = query row = TMEM
+//     lane; warps w and w + 4 share a lane quadrant and split each tile's keys and
+//     the output dimensions in halves, exchanging row maxima and sums through shared
+//     memory): causal mask, online softmax in log2 units (ex2.approx, fp32) with a
+//     lazily raised reference max, P (operand type) back to TMEM, O rescaled in TMEM
+//     when the reference max moves; normalised rows are written to `out`.
 //   * Every wait is a bounded mbarrier wait; one that gives up sets PA_DEV_TIMEOUT
 //     and makes the block's later waits no-ops; before the TMEM is freed the MMA
 //     lane waits (bounded) for its own MMAs and the producer for its copies.
@@ -52,7 +54,7 @@ constexpr int kD = 128;           // head_dim
 constexpr int kBM = 128;          // queries per tile
 constexpr int kBN = 128;          // keys per tile
 constexpr int kThreads = 320;     // 10 warps
-constexpr int kSmxWarp0 = 2;      // softmax group q: warps 2 + 4q .. 5 + 4q
+constexpr int kSmxWarp0 = 2;      // softmax warps 2 .. 9; half h: warps 2 + 4h .. 5 + 4h
 constexpr uint32_t kTile = 32768; // bytes of one 128 x 128 16-bit tile
 constexpr uint32_t kHalf = 16384; // one 64-column half of a Q tile
 
@@ -62,7 +64,8 @@ constexpr uint32_t kSmK = kSmQ + 2 * kTile;   // [2 stages] K tiles: [16 groups]
 constexpr uint32_t kSmV = kSmK + 2 * kTile;   // [2 stages] V tiles, same layout
 constexpr uint32_t kSmBar = kSmV + 2 * kTile; // mbarriers
 constexpr uint32_t kSmMisc = kSmBar + 32 * 8; // flags, TMEM address, item ring
-constexpr uint32_t kSmOff = kSmMisc + 64;     // unit offsets [S + 1] | histogram [64] | unit order [unit_cap]
+constexpr uint32_t kSmX = kSmMisc + 64;       // row-max / row-sum exchange [2 phases][2 halves][128 rows] fp32
+constexpr uint32_t kSmOff = kSmX + 2048;      // unit offsets [S + 1] | histogram [64] | unit order [unit_cap]
 __host__ __device__ constexpr uint32_t smem_bytes(int S, int unit_cap) {
   return kSmOff + 4u * (S + 1) + 4u * 64u + 4u * unit_cap + 1024u;
 }
@@ -78,7 +81,8 @@ enum : int {
   BS_FULL = 10, BP_FULL = 12, BO_FULL = 14,              // [2 slots] each
   BI_FULL = 16, BI_EMPTY = 18,                           // item ring [2]
   BDRAIN = 20,
-  NBARS = 21
+  BX = 21,                                               // [4 TMEM lane quadrants] half exchange
+  NBARS = 25
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -270,25 +274,6 @@ __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Excess (log2 units) of a row max over the reference at which weights would no
-// longer fit the operand type: fp16 tops out just below 2^16, bf16 near 2^128.
-template <typename T>
-constexpr float kRaiseNow = std::is_same<T, __half>::value ? 15.f : 120.f;
-
-// Two packed 16-bit weights times a factor, rounded back to the operand type.
-template <typename T>
-__device__ __forceinline__ uint32_t scale2(uint32_t packed, float f);
-template <>
-__device__ __forceinline__ uint32_t scale2<__half>(uint32_t packed, float f) {
-  const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&packed));
-  return pack2<__half>(v.x * f, v.y * f);
-}
-template <>
-__device__ __forceinline__ uint32_t scale2<__nv_bfloat16>(uint32_t packed, float f) {
-  const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&packed));
-  return pack2<__nv_bfloat16>(v.x * f, v.y * f);
-}
-
 __device__ __forceinline__ int upper_seq(const int32_t* off, int S, int x) {
   int lo = 0, hi = S - 1;
   while (lo < hi) {
@@ -379,8 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < NBARS; ++i) {
       uint32_t cnt = 1;
-      if (i == BP_FULL || i == BP_FULL + 1) cnt = 4;        // the slot's four softmax warps
+      if (i == BP_FULL || i == BP_FULL + 1) cnt = 8;        // all eight softmax warps
       if (i == BI_EMPTY || i == BI_EMPTY + 1) cnt = 9;      // MMA warp + eight softmax warps
+      if (i >= BX && i < BX + 4) cnt = 2;                   // the two warps of a lane quadrant
       mbar_init(BAR(i), cnt);
     }
     *abort_flag = 0;
@@ -660,30 +646,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ====================================== softmax / epilogue ======================================
-    // Group q (four warps) owns slot q.  Thread = query row = TMEM lane.  The S row
-    // is held in registers; weights use a reference max m_ref that is raised (and
-    // O, l rescaled) only when the row max exceeds it by more than 8 (log2 units),
-    // so weights stay <= 2^8.  P goes back to TMEM over the S columns.
-    const int q = (warp - kSmxWarp0) >> 2;
+    // All eight warps work on every tile of both slots, in the order the MMA warp
+    // publishes them (slot 0 tile j, then slot 1 tile j).  Warps w and w + 4 share TMEM
+    // lane quadrant w mod 4 (query rows 32 (w mod 4) ..): the first takes keys 0-63 of
+    // a tile and output dimensions 0-63, the second keys 64-127 and dimensions 64-127.
+    // Thread = query row = TMEM lane.  Per tile each half finds its row max, the two
+    // halves exchange it through shared memory (one mbarrier per quadrant, bounded
+    // wait), and both take the same decision: the reference max m_ref the weights are
+    // taken against moves only when the tile's row max passed it by more than 8 (log2
+    // units), so weights stay <= 2^8 and O is rescaled rarely.  Each half keeps a partial
+    // row sum; the halves add them at the epilogue.  P goes back to TMEM over the first
+    // 64 columns of S (keys 32c .. 32c+31 in columns 16c .. 16c+15): the second half's
+    // weights land over the first half's scores, which the exchange orders after the
+    // first half has read them.
+    const int half = (warp - kSmxWarp0) >> 2;
     const int quad = warp & 3;        // TMEM lane quadrant a warp may access
     const int row = quad * 32 + lane; // query row in the tile
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t s_tmem = tmem + lane_base + kTmemS + q * 128;
-    const uint32_t o_tmem = tmem + lane_base + kTmemO + q * 128;
+    float* xbuf = reinterpret_cast<float*>(smem + kSmX);  // [2 phases][2 halves][128 rows]
+    const uint32_t xbar = BAR(BX + quad);
     const float sl2 = a.qk_scale_log2;
     const uint64_t sl2x2 = f2(sl2, sl2);
+    int ni = 0;
+    uint32_t sc[2] = {0u, 0u}, oc[2] = {0u, 0u};  // S_FULL and O_FULL phases per slot
+    uint32_t xk = 0;                              // exchanges done (phase of xbar)
+    auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+      const bool w = __all_sync(kFull, mbar_wait(bar, parity, abort_flag, a.status));
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      return w;
+    };
+    // Give the partner half this row's value and take its one (false: the block aborts).
+    auto exchange = [&](float mine, float& theirs) -> bool {
+      float* xb = xbuf + (xk & 1u) * 256;
+      xb[half * 128 + row] = mine;
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xbar);
+      const bool w = wait_all(xbar, xk & 1u);
+      ++xk;
+      theirs = xb[(half ^ 1) * 128 + row];
+      return w;
+    };
     auto row_sum = [](const uint64_t (&v)[2]) {
       float a0, a1, b0, b1;
       unf2(v[0], a0, a1);
       unf2(v[1], b0, b1);
       return (a0 + a1) + (b0 + b1);
-    };
-    int ni = 0;
-    uint32_t sc = 0, oc = 0;  // S_FULL and O_FULL phases of this slot
-    auto wait_all = [&](int bar, uint32_t parity) -> bool {
-      const bool w = __all_sync(kFull, mbar_wait(BAR(bar), parity, abort_flag, a.status));
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      return w;
     };
     while (true) {
       const int sl = ni & 1;
@@ -695,148 +703,137 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++ni;
       if (item < 0) break;
       const PItem it = locate(a, offu, order, item);
-      const int nk = q ? it.nkv_q[1] : it.nkv_q[0];
-      if (nk == 0) continue;
-      const int pos0 = q ? it.pos0[1] : it.pos0[0];
-      const int qrow0 = q ? it.qrow0[1] : it.qrow0[0];
-      const bool valid = row < (q ? it.nrows[1] : it.nrows[0]);
+      const int n0 = it.nkv_q[0], n1 = it.nkv_q[1];
+      if (n1 == 0) continue;
       // rows past the chunk end attend everything they are shown (not stored)
-      const int pos = valid ? pos0 + row : 0x3fffffff;
-      // m_ref: reference max the weights are taken against (O and l are relative to
-      // it); m_run: running row max (log2 units); o_pending: factor O still owes for
-      // a reference raise at the end of the previous tile (applied once that tile's
-      // P V has landed in O).
-      float m_ref = -INFINITY, m_run = -INFINITY, l = 0.f, o_pending = 1.f;
+      int pos[2];
+      float m_ref[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < 2; ++q) pos[q] = row < it.nrows[q] ? it.pos0[q] + row : 0x3fffffff;
       bool ok = true;
-      for (int j = 0; j < nk; ++j) {
-        if (!wait_all(BS_FULL + q, sc & 1)) { ok = false; break; }
-        ++sc;
-        // Keys of this tile a row may see: 0 .. nvalid-1.  Rows of a warp are
+      // per tile of slot q (slot 0 tile j, then slot 1 tile j): scores of this half's 64
+      // keys -> weights, O rescaled if the reference moved
+      for (int j = 0; j < n1 && ok; ++j) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        if ((q == 0 && j >= n0) || !ok) continue;
+        if (!wait_all(BAR(BS_FULL + q), sc[q] & 1u)) { ok = false; continue; }
+        ++sc[q];
+        const uint32_t s_tmem = tmem + lane_base + kTmemS + q * 128;
+        // keys of this half a row may see: 64 half + (0 .. nv-1).  Rows of a warp are
         // consecutive positions, so a 32-key chunk is (warp-uniformly) fully visible,
-        // fully masked (weight 0, not loaded) or split by the diagonal (masked per
-        // key); masked chunks only follow unmasked ones.
-        const int key0 = j * kBN;
-        const int nvalid = max(0, min(kBN, pos - key0 + 1));
-        const int wmin = __reduce_min_sync(kFull, nvalid), wmax = __reduce_max_sync(kFull, nvalid);
-        // One pass over the chunks of S, the next chunk's load in flight while one is
-        // processed; the P of chunk c lands in columns 16c .. 16c+15, i.e. over S of
-        // chunk c/2, which has been read by then.  Weights are taken against m_ref,
-        // held for the whole tile, so they are rounded to the operand type once.  Only
-        // if a row's max passes m_ref by more than kRaiseNow (the weights would
-        // overflow the operand type) is m_ref raised inside the tile, scaling down the
-        // weights already stored (rounded a second time).
-        float o_scale = o_pending;
-        uint64_t sum2[2] = {0ull, 0ull};  // packed fp32 pairs of partial row sums
+        // fully masked (weight 0, not loaded) or split by the diagonal.
+        const int nvalid = max(0, min(kBN, pos[q] - j * kBN + 1));
+        const int nv = max(0, min(64, nvalid - 64 * half));
+        const int wmin = __reduce_min_sync(kFull, nv), wmax = __reduce_max_sync(kFull, nv);
         uint32_t sr[2][32];
-        if (wmax > 0) tmem_ld32_async(s_tmem, sr[0]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t(&cur)[32] = sr[c & 1];
-          if (wmax <= c * 32) {  // this and every later chunk are masked for the whole warp
-            uint32_t z[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) z[k] = 0u;
-            tmem_st16(s_tmem + c * 16, z);
-            continue;
-          }
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (wmax > 0) {
+          tmem_ld32_async(s_tmem + 64 * half, sr[0]);
+          if (wmax > 32) tmem_ld32_async(s_tmem + 64 * half + 32, sr[1]);
           tmem_wait_ld();
-          tie32(cur);
-          if (c < 3 && wmax > (c + 1) * 32) tmem_ld32_async(s_tmem + (c + 1) * 32, sr[(c + 1) & 1]);
-          if (wmin < (c + 1) * 32) {
+          tie32(sr[0]);
+          if (wmax > 32) tie32(sr[1]);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (c * 32 + i >= nvalid) cur[i] = __float_as_uint(-INFINITY);
+          for (int cc = 0; cc < 2; ++cc) {
+            if (wmax <= cc * 32) break;
+            uint32_t(&cur)[32] = sr[cc];
+            if (wmin < (cc + 1) * 32) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (cc * 32 + i >= nv) cur[i] = __float_as_uint(-INFINITY);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; i += 2)
+              mx4[(i >> 1) & 3] = fmax3(mx4[(i >> 1) & 3], __uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
           }
-          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        }
+        float other;
+        if (!exchange(fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])), other)) { ok = false; continue; }
+        const float m_t = fmaxf(fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])), other) * sl2;
+        // one decision per tile, the same in both halves (always on a row's first tile)
+        float alpha = 1.f;
+        if (m_t > m_ref[q] + 8.f) {
+          alpha = ex2(m_ref[q] - m_t);
+          m_ref[q] = m_t;
+        }
+        const uint64_t nm2 = f2(-m_ref[q], -m_ref[q]);
+        uint64_t sum2[2] = {0ull, 0ull};  // packed fp32 pairs of partial row sums
 #pragma unroll
-          for (int i = 0; i < 32; i += 2)
-            mx4[(i >> 1) & 3] = fmax3(mx4[(i >> 1) & 3], __uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
-          m_run = fmaxf(m_run, fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2);
-          const bool raise = m_run > m_ref + kRaiseNow<T>;  // also the first chunk of an item
-          if (__any_sync(kFull, raise)) {
-            const float alpha = raise ? ex2(m_ref - m_run) : 1.f;
-            l = (l + row_sum(sum2)) * alpha;
-            sum2[0] = sum2[1] = 0ull;
-            if (raise) m_ref = m_run;
-            o_scale *= alpha;
-            if (c > 0) {  // rescale the weights this tile has stored so far
-              tmem_wait_st();
+        for (int cc = 0; cc < 2; ++cc) {
+          const uint32_t pcol = s_tmem + 32 * half + 16 * cc;
+          uint32_t w[16];
+          if (wmax <= cc * 32) {
 #pragma unroll
-              for (int cp = 0; cp < c; ++cp) {
-                uint32_t pr[16];
-                tmem_ld16_async(s_tmem + cp * 16, pr);
-                tmem_wait_ld();
-                tie16(pr);
-                uint32_t w[16];
+            for (int k = 0; k < 16; ++k) w[k] = 0u;
+          } else {
+            const uint32_t(&cur)[32] = sr[cc];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) w[k] = scale2<T>(pr[k], alpha);
-                tmem_st16(s_tmem + cp * 16, w);
-              }
+            for (int i = 0; i < 32; i += 2) {
+              float x0, x1;
+              unf2(ffma2(f2(__uint_as_float(cur[i]), __uint_as_float(cur[i + 1])), sl2x2, nm2), x0, x1);
+              const float p0 = ex2(x0), p1 = ex2(x1);
+              sum2[(i >> 1) & 1] = fadd2(sum2[(i >> 1) & 1], f2(p0, p1));
+              w[i >> 1] = pack2<T>(p0, p1);
             }
           }
-          const uint64_t nm2 = f2(-m_ref, -m_ref);
-          uint32_t w[16];
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float x0, x1;
-            unf2(ffma2(f2(__uint_as_float(cur[i]), __uint_as_float(cur[i + 1])), sl2x2, nm2), x0, x1);
-            const float p0 = ex2(x0), p1 = ex2(x1);
-            sum2[(i >> 1) & 1] = fadd2(sum2[(i >> 1) & 1], f2(p0, p1));
-            w[i >> 1] = pack2<T>(p0, p1);
-          }
-          tmem_st16(s_tmem + c * 16, w);
+          tmem_st16(pcol, w);
         }
-        if (j > 0 && __any_sync(kFull, o_scale != 1.f)) {
-          // O_q holds the previous tiles (the S commit covered their P V); rows with
-          // nothing owed scale by 1
+        if (j > 0 && __any_sync(kFull, alpha != 1.f)) {
+          // O_q holds the previous tiles (the S commit covered their P V); this half's
+          // dimensions, rows whose reference did not move scale by 1
+          const uint32_t o_tmem = tmem + lane_base + kTmemO + q * 128 + 64 * half;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t r[32];
             tmem_ld32_async(o_tmem + c * 32, r);
             tmem_wait_ld();
             tie32(r);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * o_scale);
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
             tmem_st32(o_tmem + c * 32, r);
           }
         }
-        l += row_sum(sum2);
-        // raise the reference for the next tile once the row max has moved by more
-        // than 8, so weights stay near or below 2^8; O pays the factor next tile
-        o_pending = 1.f;
-        if (m_run > m_ref + 8.f) {
-          o_pending = ex2(m_ref - m_run);
-          l *= o_pending;
-          m_ref = m_run;
-        }
+        l[q] = l[q] * alpha + row_sum(sum2);
         tmem_wait_st();
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(BP_FULL + q));
       }
-      // epilogue: wait for the slot's last P V, normalise, store
-      if (ok && !wait_all(BO_FULL + q, oc & 1)) ok = false;
-      ++oc;
-      const bool zero = !ok || !(l > 0.f);
-      const float inv = zero ? 0.f : o_pending / l;  // O still owes the last tile's raise
-      T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(qrow0 + row) * a.out_row +
-              static_cast<int64_t>(it.h) * kD;
+      }
+      // epilogues, slot 0 then slot 1: wait for the slot's last P V, add the halves'
+      // row sums, normalise this half's 64 dimensions, store
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32_async(o_tmem + c * 32, r);
-        tmem_wait_ld();
-        tie32(r);
-        if (valid) {
+      for (int q = 0; q < 2; ++q) {
+        if ((q ? n1 : n0) == 0) continue;
+        if (ok && !wait_all(BAR(BO_FULL + q), oc[q] & 1u)) ok = false;
+        ++oc[q];
+        float other = 0.f;
+        if (ok && !exchange(l[q], other)) ok = false;
+        const float lt = l[q] + other;
+        const bool zero = !ok || !(lt > 0.f);
+        const float inv = zero ? 0.f : 1.f / lt;
+        const bool valid = row < it.nrows[q];
+        const uint32_t o_tmem = tmem + lane_base + kTmemO + q * 128 + 64 * half;
+        T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(it.qrow0[q] + row) * a.out_row +
+                static_cast<int64_t>(it.h) * kD + 64 * half;
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            uint4 w4;
-            w4.x = pack2<T>(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv);
-            w4.y = pack2<T>(__uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv);
-            w4.z = pack2<T>(__uint_as_float(r[i + 4]) * inv, __uint_as_float(r[i + 5]) * inv);
-            w4.w = pack2<T>(__uint_as_float(r[i + 6]) * inv, __uint_as_float(r[i + 7]) * inv);
-            if (zero) w4 = make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(op + c * 32 + i) = w4;
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[32];
+          tmem_ld32_async(o_tmem + c * 32, r);
+          tmem_wait_ld();
+          tie32(r);
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint4 w4;
+              w4.x = pack2<T>(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv);
+              w4.y = pack2<T>(__uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv);
+              w4.z = pack2<T>(__uint_as_float(r[i + 4]) * inv, __uint_as_float(r[i + 5]) * inv);
+              w4.w = pack2<T>(__uint_as_float(r[i + 6]) * inv, __uint_as_float(r[i + 7]) * inv);
+              if (zero) w4 = make_uint4(0u, 0u, 0u, 0u);
+              *reinterpret_cast<uint4*>(op + c * 32 + i) = w4;
+            }
           }
         }
       }
