@@ -511,11 +511,14 @@ int pa_decode_split(const pa_tensor* q, const pa_tensor* k_cache, const pa_tenso
   int dev;
   PA_TRY(current_device(&dev));
   const int sms = g_dev[dev].num_sms;
-  // context partitions only when (sequence, head group) items cannot fill the GPU
+  // context partitions only when (sequence, head group) items cannot fill the GPU; then
+  // about four per thread-block slot (two blocks per SM), so that the dynamic scheduler
+  // ends the launch with short items on every block instead of a second wave of long
+  // ones on a few
   const int64_t groups = H / 4, cap = std::max<int64_t>(max_blocks * B, B);
   int64_t P = cap, NP = 1;
   if (S * groups < 2LL * sms) {
-    const int64_t want = (2LL * sms + S * groups - 1) / (S * groups);
+    const int64_t want = (8LL * sms + S * groups - 1) / (S * groups);
     P = std::max<int64_t>(256, ((cap + want - 1) / want + B - 1) / B * B);
     NP = (cap + P - 1) / P;
   }

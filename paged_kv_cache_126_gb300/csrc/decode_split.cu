@@ -50,7 +50,10 @@ struct Geo {
   static constexpr int NC = D / X;                       // chunks per head row
   static constexpr int PH = 32 / B;                      // lanes per token
   static constexpr int STEPS = NC / PH;                  // chunks per lane
-  static constexpr int ND = D / 32;                      // output elements per lane
+  static constexpr int ND = D / 32;                      // output elements per lane (final rows)
+  static constexpr int C = B / X;                        // 16-byte chunks per V row [D][B]
+  static constexpr int RPI = 32 / C;                     // V rows one warp-wide read covers
+  static constexpr int NR = D / RPI;                     // V rows each lane accumulates (part of)
   static constexpr uint32_t HEAD = D * B * E;            // one head of one frame (K or V)
   static constexpr uint32_t STAGE = 2 * kHG * HEAD;      // K of 4 heads, then V of 4 heads
   static constexpr int NST = (96 * 1024 / STAGE) < 2 ? 2 : ((96 * 1024 / STAGE) > 6 ? 6 : 96 * 1024 / STAGE);
@@ -58,6 +61,7 @@ struct Geo {
   static constexpr uint32_t MISC_OFF = BAR_OFF + 8 * (2 * NST + 4);
   static constexpr uint32_t SMEM = MISC_OFF + 4 * (4 + NST) + 128;
   static_assert(PH * B == 32 && STEPS * PH == NC, "B must divide 32 and the chunk count");
+  static_assert(C * RPI == 32 && NR * RPI == D, "V rows must tile the warp");
 };
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -246,8 +250,15 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
   }
 
   // ------------------------------------------------------------------ consumers
+  // Scores: lane (tok, ph) = (lane mod B, lane / B) dots token tok's chunks ph, ph + PH,
+  // ... (one warp step reads 32 consecutive 16-byte chunks).  Values: V is [D][B] per
+  // head; lane (r0, c) = (lane / C, lane mod C) reads chunk c (tokens cX .. cX+X-1) of
+  // rows r0, r0 + RPI, ... -- again 32 consecutive chunks per warp step, conflict-free --
+  // and keeps a partial sum per row over its chunk's tokens; the C lanes of a row add
+  // their parts once per item.
   const int hh = warp - 1;
   const int tok = lane % B, ph = lane / B;
+  const int vr0 = lane / G::C, vc = lane % G::C;
   int ni = 0, kt = 0;
   while (true) {
     const int sl = ni & 1;
@@ -273,9 +284,9 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
         for (int i = 0; i < 8; ++i) qv[k][i] = v[i] * a.qk_scale_log2;
       }
     }
-    float m = -INFINITY, lsum = 0.f, o[G::ND];
+    float m = -INFINITY, lsum = 0.f, o[G::NR];
 #pragma unroll
-    for (int j = 0; j < G::ND; ++j) o[j] = 0.f;
+    for (int j = 0; j < G::NR; ++j) o[j] = 0.f;
     bool ok = true;
     for (int t = it.t0; t < t1; t += B, ++kt) {
       const int st = kt % G::NST;
@@ -304,24 +315,21 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
         const float alpha = ex2(m - fm);
         lsum *= alpha;
 #pragma unroll
-        for (int j = 0; j < G::ND; ++j) o[j] *= alpha;
+        for (int j = 0; j < G::NR; ++j) o[j] *= alpha;
         m = fm;
       }
       const float pw = tok < nv ? ex2(x - m) : 0.f;
       if (ph == 0) lsum += pw;
-      float pt[B];
+      // the weights of this lane's value chunk: tokens vc X .. vc X + X - 1
+      float pt[G::X];
 #pragma unroll
-      for (int u = 0; u < B; ++u) pt[u] = __shfl_sync(kFull, pw, u);
+      for (int u = 0; u < G::X; ++u) pt[u] = __shfl_sync(kFull, pw, vc * G::X + u);
 #pragma unroll
-      for (int j = 0; j < G::ND; ++j) {
-        const T* vr = vh + (lane + 32 * j) * B;
+      for (int j = 0; j < G::NR; ++j) {
+        float vv[8];
+        load8<T>(vh + (vr0 + G::RPI * j) * B + vc * G::X, vv);
 #pragma unroll
-        for (int c = 0; c < B / G::X; ++c) {
-          float vv[8];
-          load8<T>(vr + c * G::X, vv);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) o[j] = fmaf(pt[c * G::X + i], vv[i], o[j]);
-        }
+        for (int i = 0; i < 8; ++i) o[j] = fmaf(pt[i], vv[i], o[j]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(EMPTY(st));
@@ -329,15 +337,24 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
     float l = lsum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) l += __shfl_xor_sync(kFull, l, off);
+    // add the C lanes' parts of every row: lane (r0, 0) then holds rows r0 + RPI j
+#pragma unroll
+    for (int j = 0; j < G::NR; ++j)
+#pragma unroll
+      for (int off = 1; off < G::C; off <<= 1) o[j] += __shfl_xor_sync(kFull, o[j], off);
     if (a.NP == 1) {
       const float inv = (ok && l > 0.f) ? 1.f / l : 0.f;
       T* orow = static_cast<T*>(a.out) + static_cast<int64_t>(it.s) * a.out_row + static_cast<int64_t>(h) * D;
+      if (vc == 0) {
 #pragma unroll
-      for (int j = 0; j < G::ND; ++j) orow[lane + 32 * j] = from_float<T>(o[j] * inv);
+        for (int j = 0; j < G::NR; ++j) orow[vr0 + G::RPI * j] = from_float<T>(o[j] * inv);
+      }
     } else {
       const int64_t slot = static_cast<int64_t>(item) * kHG + hh;
+      if (vc == 0) {
 #pragma unroll
-      for (int j = 0; j < G::ND; ++j) a.ws_o[slot * D + lane + 32 * j] = ok ? o[j] : 0.f;
+        for (int j = 0; j < G::NR; ++j) a.ws_o[slot * D + vr0 + G::RPI * j] = ok ? o[j] : 0.f;
+      }
       if (lane == 0) {
         a.ws_ml[slot * 2] = ok ? m : -INFINITY;
         a.ws_ml[slot * 2 + 1] = ok ? l : 0.f;
@@ -357,19 +374,41 @@ __global__ void __launch_bounds__(128) merge_split_kernel(const SplitArgs a) {
   const int g = h / kHG, hh = h % kHG;
   const int groups = a.H / kHG;
   auto slot = [&](int p) { return (static_cast<int64_t>((s * groups + g) * a.NP + p)) * kHG + hh; };
+  // 1. lane p holds part p's (max, sum), parts in chunks of 32: the largest max
   float M = -INFINITY;
-  for (int p = 0; p < a.NP; ++p) M = fmaxf(M, a.ws_ml[slot(p) * 2]);
+  for (int p0 = 0; p0 < a.NP; p0 += 32)
+    if (p0 + lane < a.NP) M = fmaxf(M, a.ws_ml[slot(p0 + lane) * 2]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+  // 2. weights 2^(m_p - M) (lane-parallel), the denominator, and the weighted sum of the
+  //    partial outputs with four parts' loads in flight
   float num[ND], den = 0.f;
 #pragma unroll
   for (int j = 0; j < ND; ++j) num[j] = 0.f;
   if (M != -INFINITY) {
-    for (int p = 0; p < a.NP; ++p) {
-      const float mp = a.ws_ml[slot(p) * 2];
-      if (mp == -INFINITY) continue;
-      const float w = ex2(mp - M);
-      den += w * a.ws_ml[slot(p) * 2 + 1];
+    for (int p0 = 0; p0 < a.NP; p0 += 32) {
+      const bool have = p0 + lane < a.NP;
+      const float mp = have ? a.ws_ml[slot(p0 + lane) * 2] : -INFINITY;
+      const float w = mp == -INFINITY ? 0.f : ex2(mp - M);
+      float wl = have ? w * a.ws_ml[slot(p0 + lane) * 2 + 1] : 0.f;
 #pragma unroll
-      for (int j = 0; j < ND; ++j) num[j] = fmaf(w, a.ws_o[slot(p) * D + lane + 32 * j], num[j]);
+      for (int off = 16; off > 0; off >>= 1) wl += __shfl_xor_sync(kFull, wl, off);
+      den += wl;
+      const int n = min(32, a.NP - p0);
+      for (int j0 = 0; j0 < n; j0 += 4) {
+        float wj[4], x[4][ND];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          wj[u] = __shfl_sync(kFull, w, (j0 + u) & 31);
+#pragma unroll
+          for (int j = 0; j < ND; ++j)
+            x[u][j] = j0 + u < n ? a.ws_o[slot(p0 + j0 + u) * D + lane + 32 * j] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int j = 0; j < ND; ++j) num[j] = fmaf(wj[u], x[u][j], num[j]);
+      }
     }
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
