@@ -189,7 +189,8 @@ int pa_prefill(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_
  * PA_ERR_UNSUPPORTED).  pa_decode_split splits long contexts into partitions when the
  * (sequence, 4-head group) items cannot fill the GPU and then launches a second,
  * merging kernel; its partials use the (device, stream) workspace.  Status bits and
- * error codes as for pa_decode. */
+ * error codes as for pa_decode; as there, cache slots that hold no token of a sequence
+ * may hold any bits (they never reach the result). */
 int pa_cache_append_split(const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* slot_mapping,
                           const pa_tensor* k_cache, const pa_tensor* v_cache, pa_stream stream);
 int pa_decode_split(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,

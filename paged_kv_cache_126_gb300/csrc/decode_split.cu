@@ -324,10 +324,18 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
       float pt[G::X];
 #pragma unroll
       for (int u = 0; u < G::X; ++u) pt[u] = __shfl_sync(kFull, pw, vc * G::X + u);
+      // on a partly filled frame the slots past the context may hold anything (0 times a
+      // non-finite value would poison the sum): take only the valid tokens' values
+      const bool partial = nv < B;  // warp-uniform
 #pragma unroll
       for (int j = 0; j < G::NR; ++j) {
         float vv[8];
         load8<T>(vh + (vr0 + G::RPI * j) * B + vc * G::X, vv);
+        if (partial) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (vc * G::X + i >= nv) vv[i] = 0.f;
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) o[j] = fmaf(pt[i], vv[i], o[j]);
       }
