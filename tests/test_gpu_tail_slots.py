@@ -7,7 +7,9 @@ is not 0).  Here every such slot holds NaN, the written slots random finite valu
 and each decode path must match the oracle, which reads only the sequence's own tokens
 (pa_decode whole, split into partitions with the merge, automatic; the shared-prefix
 decode; pa_decode_static; pa_decode_split on the same caches permuted into the pages'
-split layout).
+split layout).  pa_prefill's value product runs on the tensor cores, where a zero
+weight times a non-finite value would not vanish: its contract asks those slots to hold
+finite values, and its test fills them with the largest finite values instead.
 """
 
 import numpy as np
@@ -15,8 +17,10 @@ import pytest
 import torch
 
 import workloads
-from oracle import OracleKVCache, paged_decode, split_layout
+from oracle import OracleKVCache, paged_decode, paged_prefill, split_layout
 from tests._gpu_common import assert_attention_close
+from tests.test_gpu_prefill import U, half_ulp
+from oracle import prefill_weight_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -24,7 +28,10 @@ TD = {"f16": torch.float16, "bf16": torch.bfloat16}
 NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0}
 
 
-def _case(dtype, seed):
+MAX_BITS = {"f16": 0x7BFF, "bf16": 0x7F7F}  # largest finite value of the type
+
+
+def _case(dtype, seed, filler=None):
     B, H, D = 16, 4, 128
     L = [1, 15, 17, 300, 300, 777, 0, 33, 64, 65]
     need = sum(-(-x // B) for x in L) + 4
@@ -45,7 +52,7 @@ def _case(dtype, seed):
         for t, x in zip(tables, L):
             for j in range(-(-x // B)):
                 live[t[j], : min(B, x - j * B)] = True
-        full[~live] = NAN_BITS[dtype]
+        full[~live] = NAN_BITS[dtype] if filler is None else filler[dtype]
         bits[kind] = full
     q = workloads.random_storage(seed + 3, (len(L), H, D), dtype)
     return B, H, D, L, tables, bits, q
@@ -88,3 +95,34 @@ def test_unwritten_slots_never_reach_the_output(pa, dtype):
     torch.cuda.synchronize()
     assert pa.pa_get_device_status() == 0
     assert_attention_close(out, ref, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_prefill_ignores_unwritten_slots(pa, dtype):
+    B, H, D, L, tables, bits, q = _case(dtype, seed=41, filler=MAX_BITS)
+    scale = float(np.float32(1.0) / np.sqrt(np.float32(D)))
+    # the last n_s positions of every non-empty sequence are the chunk's queries
+    counts = [min(x, c) for x, c in zip(L, [1, 15, 17, 130, 129, 300, 0, 33, 64, 65])]
+    qs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    qrows = workloads.random_storage(51, (int(qs[-1]), H, D), dtype)
+    need = bits["k"].shape[0]
+    c = OracleKVCache(need, B, H, D, dtype)
+    c.k = bits["k"].view(np.float16) if dtype == "f16" else bits["k"]
+    c.v = bits["v"].view(np.float16) if dtype == "f16" else bits["v"]
+    ref = paged_prefill(qrows, c, tables, L, qs, scale)
+    dev = torch.device("cuda")
+    kc = torch.from_numpy(bits["k"].view(np.int16)).to(dev).view(TD[dtype])
+    vc = torch.from_numpy(bits["v"].view(np.int16)).to(dev).view(TD[dtype])
+    qd = torch.from_numpy(qrows.view(np.int16)).to(dev).view(TD[dtype])
+    td = torch.tensor(np.array(tables, np.int32), device=dev)
+    ld = torch.tensor(L, dtype=torch.int32, device=dev)
+    qq = torch.tensor(qs, device=dev)
+    out = torch.empty_like(qd)
+    pa.pa_prefill(qd, kc, vc, td, ld, qq, scale, out)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_status() == 0
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    bound = prefill_weight_bound(qrows, c, tables, L, qs, scale)
+    excess = np.abs(got - ref) - half_ulp(np.maximum(np.abs(got), np.abs(ref)), dtype) - U[dtype] * bound
+    assert excess.max() <= 2e-3
