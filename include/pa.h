@@ -55,6 +55,7 @@ enum pa_dtype { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_I32 = 3 };
 #define PA_ERR_UNSUPPORTED  -10   /* head_dim / dtype / size outside the built kernels */
 #define PA_ERR_CAPACITY     -11   /* caller-provided output buffer too small */
 #define PA_ERR_SCRATCH_LIMIT -12  /* pa_decode_static: scratch need exceeds its fixed array */
+#define PA_ERR_HOST_MEMORY  -13   /* a host allocation failed (no exception crosses this ABI) */
 
 /* ---- sticky device status bits (pa_get_device_status) ------------------------------ */
 #define PA_DEV_BAD_SLOT   0x1   /* append: slot >= num_blocks*block_size */

@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     PA_DEV_TIMEOUT,
     PA_ERR_OUT_OF_BLOCKS,
     PA_ERR_SCRATCH_LIMIT,
+    PA_ERR_HOST_MEMORY,
     PA_ERR_SEQ_EXISTS,
     PA_ERR_UNKNOWN_SEQ,
     PA_ERR_UNSUPPORTED,

@@ -22,6 +22,7 @@ PA_ERR_OUT_OF_BLOCKS = -6
 PA_ERR_UNKNOWN_SEQ = -7
 PA_ERR_SEQ_EXISTS = -8
 PA_ERR_SCRATCH_LIMIT = -12
+PA_ERR_HOST_MEMORY = -13
 PA_ERR_UNSUPPORTED = -10
 
 PA_DEV_BAD_SLOT = 0x1

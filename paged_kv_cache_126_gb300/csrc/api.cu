@@ -206,7 +206,13 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // Returns the workspace base and the size of its arrival-counter region (>= cnt_need).
 int workspace(int dev, cudaStream_t stream, size_t cnt_need, size_t rest_bytes, void** out, size_t* cnt_bytes) {
   std::lock_guard<std::mutex> lk(g_ws_mu);
-  Workspace& w = g_ws[{dev, stream}];
+  Workspace* wp = nullptr;
+  try {  // no C++ exception crosses the C ABI
+    wp = &g_ws[{dev, stream}];
+  } catch (...) {
+    return PA_ERR_HOST_MEMORY;
+  }
+  Workspace& w = *wp;
   const size_t cnt = std::max(round256(cnt_need), w.cnt_bytes);
   const size_t bytes = kSchedBytes + cnt + rest_bytes;
   if (w.bytes < bytes) {
@@ -341,6 +347,7 @@ const char* pa_strerror(int code) {
     case PA_ERR_SEQ_EXISTS: return "sequence id already live";
     case PA_ERR_CUDA: return "CUDA runtime error";
     case PA_ERR_UNSUPPORTED: return "size or dtype outside the built kernels";
+    case PA_ERR_HOST_MEMORY: return "host memory allocation failed";
     case PA_ERR_CAPACITY: return "output buffer too small";
     case PA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the fixed 16 MiB array of pa_decode_static";
     default: return "unknown code";
@@ -1117,10 +1124,17 @@ void free_stage(StepStage& s) {
   s.cap = 0;
 }
 
-// A ring slot with room for `need` int32 values, free to overwrite; -1 on a CUDA error.
+// A ring slot with room for `need` int32 values, free to overwrite; -1 on a CUDA error,
+// -2 when host memory for the ring's bookkeeping cannot be had.
 int stage_slot(int dev, cudaStream_t stream, size_t need, StepStage** out) {
   std::lock_guard<std::mutex> lk(g_step_mu);
-  StepStage& s = g_step[{dev, stream}];
+  StepStage* sp = nullptr;
+  try {  // no C++ exception crosses the C ABI
+    sp = &g_step[{dev, stream}];
+  } catch (...) {
+    return -2;
+  }
+  StepStage& s = *sp;
   if (s.cap < need) {
     if (s.cap && cudaStreamSynchronize(stream) != cudaSuccess) return -1;
     free_stage(s);
@@ -1187,7 +1201,7 @@ extern "C" int pa_step_decode(pa_bm* bm, const int64_t* seq_ids, int32_t n, int3
   const size_t need = static_cast<size_t>(n) * (4 + static_cast<size_t>(max_blocks));
   StepStage* s = nullptr;
   const int i = stage_slot(dev, st, need, &s);
-  if (i < 0) return PA_ERR_CUDA;
+  if (i < 0) return i == -2 ? PA_ERR_HOST_MEMORY : PA_ERR_CUDA;
   int32_t* h = s->host[i];
   int32_t* d = s->dev[i];
   int32_t nc = 0;

@@ -311,304 +311,363 @@ struct pa_bm {
   }
 };
 
+// Every entry point runs inside guarded(): no C++ exception crosses the C ABI.  A failed
+// host allocation returns PA_ERR_HOST_MEMORY (the manager's state may then be partly
+// changed: operations are all-or-nothing for lack of frames, not for lack of host memory).
+template <typename F>
+int guarded(F&& f) noexcept {
+  try {
+    return f();
+  } catch (const std::bad_alloc&) {
+    return PA_ERR_HOST_MEMORY;
+  } catch (...) {
+    return PA_ERR_INVALID;
+  }
+}
+
 extern "C" {
 
 int pa_bm_create(int32_t num_blocks, int32_t block_size, const int32_t* free_order, pa_bm** bm_out) {
-  if (!bm_out || num_blocks <= 0 || block_size <= 0) return PA_ERR_INVALID;
-  if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX) return PA_ERR_INVALID;
-  pa_bm* bm = new (std::nothrow) pa_bm();
-  if (!bm) return PA_ERR_INVALID;
-  bm->num_blocks = num_blocks;
-  bm->block_size = block_size;
-  bm->refs.assign(num_blocks, 0);
-  bm->frame_node.assign(num_blocks, 0);
-  // at most one registered block per frame: the prefix-cache maps never rehash
-  bm->node_of_key.reserve(static_cast<size_t>(num_blocks));
-  bm->nodes.reserve(static_cast<size_t>(num_blocks));
-  bm->free_list.reset(num_blocks);
-  if (free_order) {
-    std::vector<uint8_t> seen(num_blocks, 0);
-    for (int32_t i = 0; i < num_blocks; ++i) {
-      int32_t f = free_order[i];
-      if (f < 0 || f >= num_blocks || seen[f]) {
-        delete bm;
-        return PA_ERR_INVALID;
+  return guarded([&]() -> int {
+    if (!bm_out || num_blocks <= 0 || block_size <= 0) return PA_ERR_INVALID;
+    if (static_cast<int64_t>(num_blocks) * block_size > INT32_MAX) return PA_ERR_INVALID;
+    pa_bm* bm = new (std::nothrow) pa_bm();
+    if (!bm) return PA_ERR_INVALID;
+    bm->num_blocks = num_blocks;
+    bm->block_size = block_size;
+    bm->refs.assign(num_blocks, 0);
+    bm->frame_node.assign(num_blocks, 0);
+    // at most one registered block per frame: the prefix-cache maps never rehash
+    bm->node_of_key.reserve(static_cast<size_t>(num_blocks));
+    bm->nodes.reserve(static_cast<size_t>(num_blocks));
+    bm->free_list.reset(num_blocks);
+    if (free_order) {
+      std::vector<uint8_t> seen(num_blocks, 0);
+      for (int32_t i = 0; i < num_blocks; ++i) {
+        int32_t f = free_order[i];
+        if (f < 0 || f >= num_blocks || seen[f]) {
+          delete bm;
+          return PA_ERR_INVALID;
+        }
+        seen[f] = 1;
+        bm->free_list.push_back(f);
       }
-      seen[f] = 1;
-      bm->free_list.push_back(f);
+    } else {
+      for (int32_t i = 0; i < num_blocks; ++i) bm->free_list.push_back(i);
     }
-  } else {
-    for (int32_t i = 0; i < num_blocks; ++i) bm->free_list.push_back(i);
-  }
-  *bm_out = bm;
-  return PA_OK;
+    *bm_out = bm;
+    return PA_OK;
+  });
 }
 
 void pa_bm_destroy(pa_bm* bm) { delete bm; }
 
 int pa_bm_add_seq(pa_bm* bm, int64_t seq_id, int32_t num_tokens, int32_t* slots_out) {
-  if (!bm || num_tokens < 0) return PA_ERR_INVALID;
-  if (bm->seqs.count(seq_id)) return PA_ERR_SEQ_EXISTS;
-  const int32_t need = num_tokens / bm->block_size + (num_tokens % bm->block_size != 0);
-  if (need > bm->free_list.size()) return PA_ERR_OUT_OF_BLOCKS;
-  Seq s;
-  s.frames.reserve(need + 1);
-  for (int32_t j = 0; j < need; ++j) s.frames.push_back(bm->take_frame(nullptr));
-  s.len = num_tokens;
-  if (slots_out)
-    bm->slots_of(s, 0, num_tokens, slots_out);
-  bm->seqs.emplace(seq_id, std::move(s));
-  return PA_OK;
+  return guarded([&]() -> int {
+    if (!bm || num_tokens < 0) return PA_ERR_INVALID;
+    if (bm->seqs.count(seq_id)) return PA_ERR_SEQ_EXISTS;
+    const int32_t need = num_tokens / bm->block_size + (num_tokens % bm->block_size != 0);
+    if (need > bm->free_list.size()) return PA_ERR_OUT_OF_BLOCKS;
+    Seq s;
+    s.frames.reserve(need + 1);
+    for (int32_t j = 0; j < need; ++j) s.frames.push_back(bm->take_frame(nullptr));
+    s.len = num_tokens;
+    if (slots_out)
+      bm->slots_of(s, 0, num_tokens, slots_out);
+    bm->seqs.emplace(seq_id, std::move(s));
+    return PA_OK;
+  });
 }
 
 int pa_bm_append(pa_bm* bm, int64_t seq_id, int32_t* slot_out, int32_t* cow_src, int32_t* cow_dst) {
-  if (!bm || !slot_out) return PA_ERR_INVALID;
-  int32_t src, dst;
-  int rc = bm->append_one(seq_id, kUnknownToken, slot_out, &src, &dst, nullptr);
-  if (rc != PA_OK) return rc;
-  if (cow_src) *cow_src = src;
-  if (cow_dst) *cow_dst = dst;
-  return PA_OK;
+  return guarded([&]() -> int {
+    if (!bm || !slot_out) return PA_ERR_INVALID;
+    int32_t src, dst;
+    int rc = bm->append_one(seq_id, kUnknownToken, slot_out, &src, &dst, nullptr);
+    if (rc != PA_OK) return rc;
+    if (cow_src) *cow_src = src;
+    if (cow_dst) *cow_dst = dst;
+    return PA_OK;
+  });
 }
 
 int pa_bm_step(pa_bm* bm, const int64_t* seq_ids, int32_t n, int32_t* slots_out,
                int32_t* copies_out, int32_t* n_copies_out) {
-  if (!bm || n < 0 || (n > 0 && (!seq_ids || !slots_out))) return PA_ERR_INVALID;
-  return bm->run_appends(seq_ids, 0, nullptr, n, slots_out, copies_out, n_copies_out);
+  return guarded([&]() -> int {
+    if (!bm || n < 0 || (n > 0 && (!seq_ids || !slots_out))) return PA_ERR_INVALID;
+    return bm->run_appends(seq_ids, 0, nullptr, n, slots_out, copies_out, n_copies_out);
+  });
 }
 
 int pa_bm_step_tokens(pa_bm* bm, const int64_t* seq_ids, const int32_t* tokens, int32_t n, int32_t* slots_out,
                       int32_t* copies_out, int32_t* n_copies_out) {
-  if (!bm || n < 0 || (n > 0 && (!seq_ids || !tokens || !slots_out))) return PA_ERR_INVALID;
-  return bm->run_appends(seq_ids, 0, tokens, n, slots_out, copies_out, n_copies_out);
+  return guarded([&]() -> int {
+    if (!bm || n < 0 || (n > 0 && (!seq_ids || !tokens || !slots_out))) return PA_ERR_INVALID;
+    return bm->run_appends(seq_ids, 0, tokens, n, slots_out, copies_out, n_copies_out);
+  });
 }
 
 int pa_bm_extend(pa_bm* bm, int64_t seq_id, int32_t num_tokens, int32_t* slots_out, int32_t* copies_out,
                  int32_t* n_copies_out) {
-  if (!bm || num_tokens < 0 || (num_tokens > 0 && !slots_out)) return PA_ERR_INVALID;
-  if (!bm->seqs.count(seq_id)) return PA_ERR_UNKNOWN_SEQ;
-  return bm->run_appends(nullptr, seq_id, nullptr, num_tokens, slots_out, copies_out, n_copies_out);
+  return guarded([&]() -> int {
+    if (!bm || num_tokens < 0 || (num_tokens > 0 && !slots_out)) return PA_ERR_INVALID;
+    if (!bm->seqs.count(seq_id)) return PA_ERR_UNKNOWN_SEQ;
+    return bm->run_appends(nullptr, seq_id, nullptr, num_tokens, slots_out, copies_out, n_copies_out);
+  });
 }
 
 int pa_bm_extend_tokens(pa_bm* bm, int64_t seq_id, const int32_t* tokens, int32_t num_tokens, int32_t* slots_out,
                         int32_t* copies_out, int32_t* n_copies_out) {
-  if (!bm || num_tokens < 0 || (num_tokens > 0 && (!slots_out || !tokens))) return PA_ERR_INVALID;
-  if (!bm->seqs.count(seq_id)) return PA_ERR_UNKNOWN_SEQ;
-  return bm->run_appends(nullptr, seq_id, tokens, num_tokens, slots_out, copies_out, n_copies_out);
+  return guarded([&]() -> int {
+    if (!bm || num_tokens < 0 || (num_tokens > 0 && (!slots_out || !tokens))) return PA_ERR_INVALID;
+    if (!bm->seqs.count(seq_id)) return PA_ERR_UNKNOWN_SEQ;
+    return bm->run_appends(nullptr, seq_id, tokens, num_tokens, slots_out, copies_out, n_copies_out);
+  });
 }
 
 int pa_bm_add_seq_cached(pa_bm* bm, int64_t seq_id, const int32_t* tokens, int32_t num_tokens,
                          int32_t* slots_out, int32_t* n_cached_out) {
-  if (!bm || num_tokens < 0 || (num_tokens > 0 && (!tokens || !slots_out))) return PA_ERR_INVALID;
-  if (bm->seqs.count(seq_id)) return PA_ERR_SEQ_EXISTS;
-  const int32_t B = bm->block_size, L = num_tokens;
-  // leading filled blocks already cached; the last token is never among them
-  std::vector<int64_t> hit_nodes;
-  std::vector<int32_t> hit_frames;
-  int64_t parent = 0;
-  BlockKey key{0, std::vector<int32_t>(B)};
-  while (static_cast<int64_t>(hit_nodes.size() + 1) * B <= static_cast<int64_t>(L) - 1) {
-    const size_t i = hit_nodes.size();
-    key.parent = parent;
-    std::memcpy(key.tokens.data(), tokens + i * B, sizeof(int32_t) * B);
-    auto it = bm->node_of_key.find(key);
-    if (it == bm->node_of_key.end()) break;
-    hit_nodes.push_back(it->second);
-    hit_frames.push_back(bm->nodes.find(it->second)->second.frame);
-    parent = it->second;
-  }
-  const int32_t n_hits = static_cast<int32_t>(hit_nodes.size());
-  const int32_t n_blocks = L / B + (L % B != 0);
-  int32_t available = bm->free_list.size();
-  for (int32_t f : hit_frames)
-    if (bm->refs[f] == 0) --available;
-  if (n_blocks - n_hits > available) return PA_ERR_OUT_OF_BLOCKS;
-  for (int32_t f : hit_frames) {  // reuse: a freed cached frame leaves the free list
-    if (bm->refs[f] == 0) bm->free_list.remove(f);
-    bm->refs[f] += 1;
-  }
-  Seq s;
-  s.tracked = true;
-  s.len = L;
-  s.frames = hit_frames;
-  s.nodes = hit_nodes;
-  s.tokens.assign(tokens, tokens + L);
-  s.frames.reserve(n_blocks + 1);
-  for (int32_t i = n_hits; i < n_blocks; ++i) {
-    s.frames.push_back(bm->take_frame(nullptr));
-    s.nodes.push_back(0);
-    bool mapped;
-    if (static_cast<int64_t>(i + 1) * B <= L) bm->register_block(s, i, &mapped);
-  }
-  const int32_t n_cached = n_hits * B;
-  bm->slots_of(s, n_cached, L, slots_out);
-  if (n_cached_out) *n_cached_out = n_cached;
-  bm->seqs.emplace(seq_id, std::move(s));
-  return PA_OK;
+  return guarded([&]() -> int {
+    if (!bm || num_tokens < 0 || (num_tokens > 0 && (!tokens || !slots_out))) return PA_ERR_INVALID;
+    if (bm->seqs.count(seq_id)) return PA_ERR_SEQ_EXISTS;
+    const int32_t B = bm->block_size, L = num_tokens;
+    // leading filled blocks already cached; the last token is never among them
+    std::vector<int64_t> hit_nodes;
+    std::vector<int32_t> hit_frames;
+    int64_t parent = 0;
+    BlockKey key{0, std::vector<int32_t>(B)};
+    while (static_cast<int64_t>(hit_nodes.size() + 1) * B <= static_cast<int64_t>(L) - 1) {
+      const size_t i = hit_nodes.size();
+      key.parent = parent;
+      std::memcpy(key.tokens.data(), tokens + i * B, sizeof(int32_t) * B);
+      auto it = bm->node_of_key.find(key);
+      if (it == bm->node_of_key.end()) break;
+      hit_nodes.push_back(it->second);
+      hit_frames.push_back(bm->nodes.find(it->second)->second.frame);
+      parent = it->second;
+    }
+    const int32_t n_hits = static_cast<int32_t>(hit_nodes.size());
+    const int32_t n_blocks = L / B + (L % B != 0);
+    int32_t available = bm->free_list.size();
+    for (int32_t f : hit_frames)
+      if (bm->refs[f] == 0) --available;
+    if (n_blocks - n_hits > available) return PA_ERR_OUT_OF_BLOCKS;
+    for (int32_t f : hit_frames) {  // reuse: a freed cached frame leaves the free list
+      if (bm->refs[f] == 0) bm->free_list.remove(f);
+      bm->refs[f] += 1;
+    }
+    Seq s;
+    s.tracked = true;
+    s.len = L;
+    s.frames = hit_frames;
+    s.nodes = hit_nodes;
+    s.tokens.assign(tokens, tokens + L);
+    s.frames.reserve(n_blocks + 1);
+    for (int32_t i = n_hits; i < n_blocks; ++i) {
+      s.frames.push_back(bm->take_frame(nullptr));
+      s.nodes.push_back(0);
+      bool mapped;
+      if (static_cast<int64_t>(i + 1) * B <= L) bm->register_block(s, i, &mapped);
+    }
+    const int32_t n_cached = n_hits * B;
+    bm->slots_of(s, n_cached, L, slots_out);
+    if (n_cached_out) *n_cached_out = n_cached;
+    bm->seqs.emplace(seq_id, std::move(s));
+    return PA_OK;
+  });
 }
 
 int pa_bm_cached_frames(const pa_bm* bm, int32_t* out, int32_t cap, int32_t* n_cached_out) {
-  if (!bm || cap < 0 || (cap > 0 && !out)) return PA_ERR_INVALID;
-  if (out && cap < bm->num_blocks) return PA_ERR_CAPACITY;
-  int32_t n = 0;
-  for (int32_t f = 0; f < bm->num_blocks; ++f) {
-    const int32_t c = bm->frame_node[f] != 0;
-    if (out) out[f] = c;
-    n += c;
-  }
-  if (n_cached_out) *n_cached_out = n;
-  return PA_OK;
+  return guarded([&]() -> int {
+    if (!bm || cap < 0 || (cap > 0 && !out)) return PA_ERR_INVALID;
+    if (out && cap < bm->num_blocks) return PA_ERR_CAPACITY;
+    int32_t n = 0;
+    for (int32_t f = 0; f < bm->num_blocks; ++f) {
+      const int32_t c = bm->frame_node[f] != 0;
+      if (out) out[f] = c;
+      n += c;
+    }
+    if (n_cached_out) *n_cached_out = n;
+    return PA_OK;
+  });
 }
 
 int pa_bm_fork(pa_bm* bm, int64_t parent_id, int64_t child_id) {
-  if (!bm) return PA_ERR_INVALID;
-  auto p = bm->seqs.find(parent_id);
-  if (p == bm->seqs.end()) return PA_ERR_UNKNOWN_SEQ;
-  if (bm->seqs.count(child_id)) return PA_ERR_SEQ_EXISTS;
-  Seq child = p->second;  // copy of the table and the length
-  for (int32_t f : child.frames) bm->refs[f] += 1;
-  bm->seqs.emplace(child_id, std::move(child));
-  return PA_OK;
+  return guarded([&]() -> int {
+    if (!bm) return PA_ERR_INVALID;
+    auto p = bm->seqs.find(parent_id);
+    if (p == bm->seqs.end()) return PA_ERR_UNKNOWN_SEQ;
+    if (bm->seqs.count(child_id)) return PA_ERR_SEQ_EXISTS;
+    Seq child = p->second;  // copy of the table and the length
+    // insert first: if that allocation fails, no reference count has moved
+    const auto ins = bm->seqs.emplace(child_id, std::move(child));
+    for (int32_t f : ins.first->second.frames) bm->refs[f] += 1;
+    return PA_OK;
+  });
 }
 
 int pa_bm_free(pa_bm* bm, int64_t seq_id) {
-  if (!bm) return PA_ERR_INVALID;
-  auto it = bm->seqs.find(seq_id);
-  if (it == bm->seqs.end()) return PA_WARN_DOUBLE_FREE;
-  for (int32_t f : it->second.frames) bm->drop_ref(f);
-  bm->seqs.erase(it);
-  return PA_OK;
+  return guarded([&]() -> int {
+    if (!bm) return PA_ERR_INVALID;
+    auto it = bm->seqs.find(seq_id);
+    if (it == bm->seqs.end()) return PA_WARN_DOUBLE_FREE;
+    for (int32_t f : it->second.frames) bm->drop_ref(f);
+    bm->seqs.erase(it);
+    return PA_OK;
+  });
 }
 
 int pa_bm_fork_many(pa_bm* bm, const int64_t* parent_ids, const int64_t* child_ids, int32_t n) {
-  if (!bm || n < 0 || (n > 0 && (!parent_ids || !child_ids))) return PA_ERR_INVALID;
-  // all-or-nothing: check the whole batch in order (a child forked earlier in the batch may
-  // be a later parent) before changing anything
-  std::unordered_set<int64_t> born;
-  for (int32_t i = 0; i < n; ++i) {
-    if (!bm->seqs.count(parent_ids[i]) && !born.count(parent_ids[i])) return PA_ERR_UNKNOWN_SEQ;
-    if (bm->seqs.count(child_ids[i]) || born.count(child_ids[i])) return PA_ERR_SEQ_EXISTS;
-    born.insert(child_ids[i]);
-  }
-  for (int32_t i = 0; i < n; ++i) pa_bm_fork(bm, parent_ids[i], child_ids[i]);
-  return PA_OK;
+  return guarded([&]() -> int {
+    if (!bm || n < 0 || (n > 0 && (!parent_ids || !child_ids))) return PA_ERR_INVALID;
+    // all-or-nothing: check the whole batch in order (a child forked earlier in the batch may
+    // be a later parent) before changing anything
+    std::unordered_set<int64_t> born;
+    for (int32_t i = 0; i < n; ++i) {
+      if (!bm->seqs.count(parent_ids[i]) && !born.count(parent_ids[i])) return PA_ERR_UNKNOWN_SEQ;
+      if (bm->seqs.count(child_ids[i]) || born.count(child_ids[i])) return PA_ERR_SEQ_EXISTS;
+      born.insert(child_ids[i]);
+    }
+    for (int32_t i = 0; i < n; ++i) pa_bm_fork(bm, parent_ids[i], child_ids[i]);
+    return PA_OK;
+  });
 }
 
 int pa_bm_free_many(pa_bm* bm, const int64_t* seq_ids, int32_t n) {
-  if (!bm || n < 0 || (n > 0 && !seq_ids)) return PA_ERR_INVALID;
-  int rc = PA_OK;
-  for (int32_t i = 0; i < n; ++i)
-    if (pa_bm_free(bm, seq_ids[i]) == PA_WARN_DOUBLE_FREE) rc = PA_WARN_DOUBLE_FREE;
-  return rc;
+  return guarded([&]() -> int {
+    if (!bm || n < 0 || (n > 0 && !seq_ids)) return PA_ERR_INVALID;
+    int rc = PA_OK;
+    for (int32_t i = 0; i < n; ++i)
+      if (pa_bm_free(bm, seq_ids[i]) == PA_WARN_DOUBLE_FREE) rc = PA_WARN_DOUBLE_FREE;
+    return rc;
+  });
 }
 
 int pa_bm_block_tables(const pa_bm* bm, const int64_t* seq_ids, int32_t n, int32_t max_blocks,
                        int32_t* tables_out, int32_t* lens_out) {
-  if (!bm || n < 0 || max_blocks < 0 || (n > 0 && (!seq_ids || (!tables_out && max_blocks > 0))))
-    return PA_ERR_INVALID;
-  for (int32_t i = 0; i < n; ++i) {
-    auto it = bm->seqs.find(seq_ids[i]);
-    if (it == bm->seqs.end()) return PA_ERR_UNKNOWN_SEQ;
-    if (static_cast<int32_t>(it->second.frames.size()) > max_blocks) return PA_ERR_CAPACITY;
-  }
-  for (int32_t i = 0; i < n; ++i) {
-    const Seq& s = bm->seqs.find(seq_ids[i])->second;
-    int32_t* row = tables_out + static_cast<int64_t>(i) * max_blocks;
-    const int32_t nf = static_cast<int32_t>(s.frames.size());
-    if (nf) std::memcpy(row, s.frames.data(), sizeof(int32_t) * nf);
-    for (int32_t j = nf; j < max_blocks; ++j) row[j] = -1;
-    if (lens_out) lens_out[i] = s.len;
-  }
-  return PA_OK;
+  return guarded([&]() -> int {
+    if (!bm || n < 0 || max_blocks < 0 || (n > 0 && (!seq_ids || (!tables_out && max_blocks > 0))))
+      return PA_ERR_INVALID;
+    for (int32_t i = 0; i < n; ++i) {
+      auto it = bm->seqs.find(seq_ids[i]);
+      if (it == bm->seqs.end()) return PA_ERR_UNKNOWN_SEQ;
+      if (static_cast<int32_t>(it->second.frames.size()) > max_blocks) return PA_ERR_CAPACITY;
+    }
+    for (int32_t i = 0; i < n; ++i) {
+      const Seq& s = bm->seqs.find(seq_ids[i])->second;
+      int32_t* row = tables_out + static_cast<int64_t>(i) * max_blocks;
+      const int32_t nf = static_cast<int32_t>(s.frames.size());
+      if (nf) std::memcpy(row, s.frames.data(), sizeof(int32_t) * nf);
+      for (int32_t j = nf; j < max_blocks; ++j) row[j] = -1;
+      if (lens_out) lens_out[i] = s.len;
+    }
+    return PA_OK;
+  });
 }
 
 int pa_bm_seq_info(const pa_bm* bm, int64_t seq_id, int32_t* len_out, int32_t* n_blocks_out) {
-  if (!bm) return PA_ERR_INVALID;
-  auto it = bm->seqs.find(seq_id);
-  if (it == bm->seqs.end()) return PA_ERR_UNKNOWN_SEQ;
-  if (len_out) *len_out = it->second.len;
-  if (n_blocks_out) *n_blocks_out = static_cast<int32_t>(it->second.frames.size());
-  return PA_OK;
+  return guarded([&]() -> int {
+    if (!bm) return PA_ERR_INVALID;
+    auto it = bm->seqs.find(seq_id);
+    if (it == bm->seqs.end()) return PA_ERR_UNKNOWN_SEQ;
+    if (len_out) *len_out = it->second.len;
+    if (n_blocks_out) *n_blocks_out = static_cast<int32_t>(it->second.frames.size());
+    return PA_OK;
+  });
 }
 
 int pa_bm_table(const pa_bm* bm, int64_t seq_id, int32_t* out, int32_t cap, int32_t* n_out) {
-  if (!bm || cap < 0 || (cap > 0 && !out)) return PA_ERR_INVALID;
-  auto it = bm->seqs.find(seq_id);
-  if (it == bm->seqs.end()) return PA_ERR_UNKNOWN_SEQ;
-  const auto& fr = it->second.frames;
-  if (n_out) *n_out = static_cast<int32_t>(fr.size());
-  if (static_cast<int32_t>(fr.size()) > cap) return PA_ERR_CAPACITY;
-  if (!fr.empty()) std::memcpy(out, fr.data(), sizeof(int32_t) * fr.size());
-  return PA_OK;
+  return guarded([&]() -> int {
+    if (!bm || cap < 0 || (cap > 0 && !out)) return PA_ERR_INVALID;
+    auto it = bm->seqs.find(seq_id);
+    if (it == bm->seqs.end()) return PA_ERR_UNKNOWN_SEQ;
+    const auto& fr = it->second.frames;
+    if (n_out) *n_out = static_cast<int32_t>(fr.size());
+    if (static_cast<int32_t>(fr.size()) > cap) return PA_ERR_CAPACITY;
+    if (!fr.empty()) std::memcpy(out, fr.data(), sizeof(int32_t) * fr.size());
+    return PA_OK;
+  });
 }
 
 int pa_bm_slot(const pa_bm* bm, int64_t seq_id, int32_t pos, int32_t* slot_out) {
-  if (!bm || !slot_out) return PA_ERR_INVALID;
-  auto it = bm->seqs.find(seq_id);
-  if (it == bm->seqs.end()) return PA_ERR_UNKNOWN_SEQ;
-  if (pos < 0 || pos >= it->second.len) return PA_ERR_INVALID;
-  *slot_out = bm->slot_of(it->second, pos);
-  return PA_OK;
+  return guarded([&]() -> int {
+    if (!bm || !slot_out) return PA_ERR_INVALID;
+    auto it = bm->seqs.find(seq_id);
+    if (it == bm->seqs.end()) return PA_ERR_UNKNOWN_SEQ;
+    if (pos < 0 || pos >= it->second.len) return PA_ERR_INVALID;
+    *slot_out = bm->slot_of(it->second, pos);
+    return PA_OK;
+  });
 }
 
 int pa_bm_num_free(const pa_bm* bm, int32_t* n_out) {
-  if (!bm || !n_out) return PA_ERR_INVALID;
-  *n_out = bm->free_list.size();
-  return PA_OK;
+  return guarded([&]() -> int {
+    if (!bm || !n_out) return PA_ERR_INVALID;
+    *n_out = bm->free_list.size();
+    return PA_OK;
+  });
 }
 
 int pa_bm_free_list(const pa_bm* bm, int32_t* out, int32_t cap, int32_t* n_out) {
-  if (!bm || cap < 0 || (cap > 0 && !out)) return PA_ERR_INVALID;
-  const int32_t n = bm->free_list.size();
-  if (n_out) *n_out = n;
-  if (n > cap) return PA_ERR_CAPACITY;
-  int32_t i = 0;
-  for (int32_t f = bm->free_list.front(); f >= 0; f = bm->free_list.next(f)) out[i++] = f;
-  return PA_OK;
+  return guarded([&]() -> int {
+    if (!bm || cap < 0 || (cap > 0 && !out)) return PA_ERR_INVALID;
+    const int32_t n = bm->free_list.size();
+    if (n_out) *n_out = n;
+    if (n > cap) return PA_ERR_CAPACITY;
+    int32_t i = 0;
+    for (int32_t f = bm->free_list.front(); f >= 0; f = bm->free_list.next(f)) out[i++] = f;
+    return PA_OK;
+  });
 }
 
 int pa_bm_ref_counts(const pa_bm* bm, int32_t* out, int32_t cap) {
-  if (!bm || !out) return PA_ERR_INVALID;
-  if (cap < bm->num_blocks) return PA_ERR_CAPACITY;
-  std::memcpy(out, bm->refs.data(), sizeof(int32_t) * bm->num_blocks);
-  return PA_OK;
+  return guarded([&]() -> int {
+    if (!bm || !out) return PA_ERR_INVALID;
+    if (cap < bm->num_blocks) return PA_ERR_CAPACITY;
+    std::memcpy(out, bm->refs.data(), sizeof(int32_t) * bm->num_blocks);
+    return PA_OK;
+  });
 }
 
 int pa_bm_num_seqs(const pa_bm* bm, int32_t* n_out) {
-  if (!bm || !n_out) return PA_ERR_INVALID;
-  *n_out = static_cast<int32_t>(bm->seqs.size());
-  return PA_OK;
+  return guarded([&]() -> int {
+    if (!bm || !n_out) return PA_ERR_INVALID;
+    *n_out = static_cast<int32_t>(bm->seqs.size());
+    return PA_OK;
+  });
 }
 
 int pa_bm_usage(const pa_bm* bm, pa_bm_usage_t* out) {
-  if (!bm || !out) return PA_ERR_INVALID;
-  const int64_t B = bm->block_size;
-  pa_bm_usage_t u{};
-  u.num_seqs = static_cast<int64_t>(bm->seqs.size());
-  u.frames_total = bm->num_blocks;
-  std::vector<int32_t> fill(bm->num_blocks, 0);  // largest fill any sharer gives a frame
-  for (const auto& kv : bm->seqs) {
-    const Seq& s = kv.second;
-    const int64_t nf = static_cast<int64_t>(s.frames.size());
-    u.table_entries += nf;
-    u.tokens_logical += s.len;
-    u.max_seq_waste = std::max(u.max_seq_waste, nf * B - s.len);
-    for (int64_t i = 0; i < nf; ++i) {
-      const int32_t f = static_cast<int32_t>(std::min(B, std::max<int64_t>(0, s.len - i * B)));
-      int32_t& slot = fill[s.frames[i]];
-      slot = std::max(slot, f);
+  return guarded([&]() -> int {
+    if (!bm || !out) return PA_ERR_INVALID;
+    const int64_t B = bm->block_size;
+    pa_bm_usage_t u{};
+    u.num_seqs = static_cast<int64_t>(bm->seqs.size());
+    u.frames_total = bm->num_blocks;
+    std::vector<int32_t> fill(bm->num_blocks, 0);  // largest fill any sharer gives a frame
+    for (const auto& kv : bm->seqs) {
+      const Seq& s = kv.second;
+      const int64_t nf = static_cast<int64_t>(s.frames.size());
+      u.table_entries += nf;
+      u.tokens_logical += s.len;
+      u.max_seq_waste = std::max(u.max_seq_waste, nf * B - s.len);
+      for (int64_t i = 0; i < nf; ++i) {
+        const int32_t f = static_cast<int32_t>(std::min(B, std::max<int64_t>(0, s.len - i * B)));
+        int32_t& slot = fill[s.frames[i]];
+        slot = std::max(slot, f);
+      }
     }
-  }
-  for (int32_t f = 0; f < bm->num_blocks; ++f) {
-    if (bm->refs[f] > 0) {
-      ++u.frames_in_use;
-      u.slots_filled += fill[f];
-    } else if (bm->frame_node[f] != 0 && bm->free_list.contains(f)) {
-      ++u.frames_cached;
+    for (int32_t f = 0; f < bm->num_blocks; ++f) {
+      if (bm->refs[f] > 0) {
+        ++u.frames_in_use;
+        u.slots_filled += fill[f];
+      } else if (bm->frame_node[f] != 0 && bm->free_list.contains(f)) {
+        ++u.frames_cached;
+      }
     }
-  }
-  *out = u;
-  return PA_OK;
+    *out = u;
+    return PA_OK;
+  });
 }
 
 }  // extern "C"

@@ -25,24 +25,28 @@ inline cudaError_t kernel_prep(const void* fn, int threads, size_t smem, int* bl
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(mu);
-  const auto key = std::make_tuple(dev, fn, threads, smem);
-  auto it = occ.find(key);
-  if (it != occ.end()) {
-    if (blocks_per_sm) *blocks_per_sm = it->second;
-    return cudaSuccess;
-  }
-  size_t& lim = limit[{dev, fn}];
-  if (smem > lim) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  try {  // the caches allocate; no C++ exception crosses the C ABI
+    const auto key = std::make_tuple(dev, fn, threads, smem);
+    auto it = occ.find(key);
+    if (it != occ.end()) {
+      if (blocks_per_sm) *blocks_per_sm = it->second;
+      return cudaSuccess;
+    }
+    size_t& lim = limit[{dev, fn}];
+    if (smem > lim) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      lim = smem;
+    }
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);
     if (e != cudaSuccess) return e;
-    lim = smem;
+    occ[key] = n;
+    if (blocks_per_sm) *blocks_per_sm = n;
+    return cudaSuccess;
+  } catch (...) {
+    return cudaErrorMemoryAllocation;
   }
-  int n = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);
-  if (e != cudaSuccess) return e;
-  occ[key] = n;
-  if (blocks_per_sm) *blocks_per_sm = n;
-  return cudaSuccess;
 }
 
 // ---- cache append / frame copy ---------------------------------------------------------

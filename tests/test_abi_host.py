@@ -418,3 +418,15 @@ def test_cpu_baseline_worker_runs():
     r = bench.cpu_baseline_worker(0, 0.2, seed_shift=3)
     assert r["kind"] == "oracle" and r["cores"] == 1
     assert r["value"] > 0 and r["seqs_per_sec"] > 0
+
+
+def test_every_error_code_has_a_message(pa):
+    # each PA_ERR_* / PA_WARN_* code the header defines has its own message
+    text = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pa.h")).read()
+    codes = {name: int(v) for name, v in re.findall(r"#define (PA_(?:ERR|WARN)_\w+)\s+(-?\d+)", text)}
+    assert "PA_ERR_HOST_MEMORY" in codes
+    unknown = pa.pa_strerror(-999)
+    msgs = {name: pa.pa_strerror(v) for name, v in codes.items()}
+    assert all(m and m != unknown for m in msgs.values()), msgs
+    assert len(set(msgs.values())) == len(msgs)
+    assert getattr(pa, "PA_ERR_HOST_MEMORY") == codes["PA_ERR_HOST_MEMORY"]
