@@ -435,6 +435,22 @@ int pa_bm_num_seqs(const pa_bm* bm, int32_t* n_out);
  * Errors: PA_ERR_INVALID (result_out NULL), PA_ERR_CUDA. */
 int pa_selftest_wait_timeout(int64_t* result_out, pa_stream stream);
 
+/* Snapshot of the whole manager into caller buffers (parity checks against a reference
+ * manager, debugging, inspection), the state the "Reference Implementation" of
+ * "PagedAttention: Virtual Memory Guide for LLM Inference" keeps: the live sequences in
+ * ascending id order -- ids_out[n_seqs], lens_out[n_seqs], table_offsets_out[n_seqs + 1]
+ * (table of sequence i = tables_out[table_offsets_out[i] .. table_offsets_out[i+1])) --,
+ * the free list front first (free_out[n_free]) and every frame's reference count
+ * (refs_out[num_blocks]).  cap_seqs bounds ids_out / lens_out (table_offsets_out holds
+ * cap_seqs + 1), cap_entries bounds tables_out; free_out and refs_out must hold
+ * num_blocks entries.  The sizes needed are written to *n_seqs_out, *n_entries_out and
+ * *n_free_out (each may be NULL) even when a buffer is too small, which returns
+ * PA_ERR_CAPACITY and writes nothing else.  Read only.  PA_ERR_INVALID for a NULL
+ * manager or output buffer, or negative capacities. */
+int pa_bm_export(const pa_bm* bm, int64_t* ids_out, int32_t* lens_out, int64_t* table_offsets_out,
+                 int32_t* tables_out, int32_t* free_out, int32_t* refs_out, int32_t cap_seqs,
+                 int64_t cap_entries, int32_t* n_seqs_out, int64_t* n_entries_out, int32_t* n_free_out);
+
 /* Memory accounting of the pool as it stands.  Pages: "PagedAttention: Virtual
  * Memory Guide for LLM Inference", "The Solution" (frames are granted on demand, so
  * a sequence wastes only the unfilled slots of its last frame: fewer than B) and

@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     PA_ERR_OUT_OF_BLOCKS,
     PA_ERR_SCRATCH_LIMIT,
     PA_ERR_HOST_MEMORY,
+    PA_ERR_CAPACITY,
     PA_ERR_SEQ_EXISTS,
     PA_ERR_UNKNOWN_SEQ,
     PA_ERR_UNSUPPORTED,

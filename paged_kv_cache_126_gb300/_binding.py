@@ -18,12 +18,14 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpa.so")
 PA_F32, PA_F16, PA_BF16, PA_I32 = 0, 1, 2, 3
 PA_OK = 0
 PA_WARN_DOUBLE_FREE = 1
+PA_ERR_INVALID = -1
 PA_ERR_OUT_OF_BLOCKS = -6
 PA_ERR_UNKNOWN_SEQ = -7
 PA_ERR_SEQ_EXISTS = -8
 PA_ERR_SCRATCH_LIMIT = -12
 PA_ERR_HOST_MEMORY = -13
 PA_ERR_UNSUPPORTED = -10
+PA_ERR_CAPACITY = -11
 
 PA_DEV_BAD_SLOT = 0x1
 PA_DEV_BAD_BLOCK = 0x2
@@ -103,6 +105,7 @@ def _load():
         "pa_bm_extend_tokens": ([vp, C.c_int64, i32p, C.c_int32, i32p, i32p, i32p], C.c_int),
         "pa_bm_cached_frames": ([vp, i32p, C.c_int32, i32p], C.c_int),
         "pa_bm_usage": ([vp, C.POINTER(PaBmUsage)], C.c_int),
+        "pa_bm_export": ([vp, i64p, i32p, i64p, i32p, i32p, i32p, C.c_int32, C.c_int64, i32p, i64p, i32p], C.c_int),
         "pa_selftest_wait_timeout": ([i64p, vp], C.c_int),
     }
     for name, (args, res) in sig.items():
@@ -122,6 +125,7 @@ EXPORTED = (
     "pa_bm_table", "pa_bm_slot", "pa_bm_num_free", "pa_bm_free_list", "pa_bm_ref_counts",
     "pa_bm_num_seqs", "pa_bm_add_seq_cached", "pa_bm_step_tokens", "pa_bm_extend_tokens", "pa_bm_cached_frames",
     "pa_bm_fork_many", "pa_bm_free_many", "pa_step_decode", "pa_bm_usage", "pa_selftest_wait_timeout",
+    "pa_bm_export",
 )
 
 
@@ -486,6 +490,28 @@ class BlockManager:
         n = C.c_int32()
         _check(LIB.pa_bm_num_seqs(self._h, C.byref(n)), "pa_bm_num_seqs")
         return n.value
+
+    def export(self) -> dict:
+        """Whole state (``pa_bm_export``): {"tables": {seq: [frames]}, "lens": {seq: len},
+        "free": [front first], "refs": [per frame]}."""
+        ns, ne, nf = C.c_int32(), C.c_int64(), C.c_int32()
+        dummy64, dummy32 = np.zeros(1, np.int64), np.zeros(1, np.int32)
+        free = np.empty(self.num_blocks, np.int32)
+        refs = np.empty(self.num_blocks, np.int32)
+        rc = LIB.pa_bm_export(self._h, _i64(dummy64), _i32(dummy32),
+                              _i64(dummy64), None, _i32(free), _i32(refs), 0, 0,
+                              C.byref(ns), C.byref(ne), C.byref(nf))
+        if rc not in (PA_OK, PA_ERR_CAPACITY):
+            _check(rc, "pa_bm_export")
+        n, e = ns.value, ne.value
+        ids, lens = np.empty(max(n, 1), np.int64), np.empty(max(n, 1), np.int32)
+        offs, tabs = np.empty(n + 1, np.int64), np.empty(max(e, 1), np.int32)
+        _check(LIB.pa_bm_export(self._h, _i64(ids), _i32(lens), _i64(offs),
+                                _i32(tabs), _i32(free), _i32(refs), n, e, C.byref(ns), C.byref(ne), C.byref(nf)),
+               "pa_bm_export")
+        return {"tables": {int(ids[i]): tabs[offs[i]:offs[i + 1]].tolist() for i in range(n)},
+                "lens": {int(ids[i]): int(lens[i]) for i in range(n)},
+                "free": free[: nf.value].tolist(), "refs": refs.tolist()}
 
     def usage(self) -> dict:
         """Memory accounting of the pool (``pa_bm_usage``): field name -> count."""

@@ -637,6 +637,43 @@ int pa_bm_num_seqs(const pa_bm* bm, int32_t* n_out) {
   });
 }
 
+int pa_bm_export(const pa_bm* bm, int64_t* ids_out, int32_t* lens_out, int64_t* table_offsets_out,
+                 int32_t* tables_out, int32_t* free_out, int32_t* refs_out, int32_t cap_seqs,
+                 int64_t cap_entries, int32_t* n_seqs_out, int64_t* n_entries_out, int32_t* n_free_out) {
+  return guarded([&]() -> int {
+    if (!bm || cap_seqs < 0 || cap_entries < 0 || !ids_out || !lens_out || !table_offsets_out ||
+        (cap_entries > 0 && !tables_out) || !free_out || !refs_out)
+      return PA_ERR_INVALID;
+    std::vector<int64_t> ids;
+    ids.reserve(bm->seqs.size());
+    int64_t entries = 0;
+    for (const auto& kv : bm->seqs) {
+      ids.push_back(kv.first);
+      entries += static_cast<int64_t>(kv.second.frames.size());
+    }
+    std::sort(ids.begin(), ids.end());
+    const int64_t n = static_cast<int64_t>(ids.size());
+    if (n_seqs_out) *n_seqs_out = static_cast<int32_t>(n);
+    if (n_entries_out) *n_entries_out = entries;
+    if (n_free_out) *n_free_out = bm->free_list.size();
+    if (n > cap_seqs || entries > cap_entries) return PA_ERR_CAPACITY;
+    int64_t off = 0;
+    for (int64_t i = 0; i < n; ++i) {
+      const Seq& s = bm->seqs.find(ids[i])->second;
+      ids_out[i] = ids[i];
+      lens_out[i] = s.len;
+      table_offsets_out[i] = off;
+      if (!s.frames.empty()) std::memcpy(tables_out + off, s.frames.data(), sizeof(int32_t) * s.frames.size());
+      off += static_cast<int64_t>(s.frames.size());
+    }
+    table_offsets_out[n] = off;
+    int32_t k = 0;
+    for (int32_t f = bm->free_list.front(); f >= 0; f = bm->free_list.next(f)) free_out[k++] = f;
+    std::memcpy(refs_out, bm->refs.data(), sizeof(int32_t) * bm->num_blocks);
+    return PA_OK;
+  });
+}
+
 int pa_bm_usage(const pa_bm* bm, pa_bm_usage_t* out) {
   return guarded([&]() -> int {
     if (!bm || !out) return PA_ERR_INVALID;

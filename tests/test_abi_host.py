@@ -56,6 +56,9 @@ def _same_state(bm, ob):
         assert bm.table(s) == t
         assert bm.seq_info(s) == (ob.lens[s], len(t))
     assert bm.usage() == ob.usage()
+    ex = bm.export()
+    assert ex["tables"] == ob.tables and ex["lens"] == ob.lens
+    assert ex["free"] == list(ob.free_list) and ex["refs"] == ob.refs
 
 
 def test_worked_trace_bit_exact(pa, golden):
@@ -430,3 +433,28 @@ def test_every_error_code_has_a_message(pa):
     assert all(m and m != unknown for m in msgs.values()), msgs
     assert len(set(msgs.values())) == len(msgs)
     assert getattr(pa, "PA_ERR_HOST_MEMORY") == codes["PA_ERR_HOST_MEMORY"]
+
+
+def test_export_capacity_and_arguments(pa):
+    import ctypes as C
+    import numpy as np
+    bm = pa.BlockManager(10, 4)
+    bm.add_seq(7, 9)
+    bm.add_seq(3, 2)
+    assert bm.export() == {"tables": {3: [3], 7: [0, 1, 2]}, "lens": {3: 2, 7: 9},
+                           "free": [4, 5, 6, 7, 8, 9], "refs": [1, 1, 1, 1] + [0] * 6}
+    lib = pa._binding.LIB
+    ids, lens, offs = np.zeros(2, np.int64), np.zeros(2, np.int32), np.zeros(3, np.int64)
+    tabs, free, refs = np.zeros(4, np.int32), np.zeros(10, np.int32), np.zeros(10, np.int32)
+    ns, ne, nf = C.c_int32(), C.c_int64(), C.c_int32()
+    i64 = lambda a: a.ctypes.data_as(C.POINTER(C.c_int64))
+    i32 = lambda a: a.ctypes.data_as(C.POINTER(C.c_int32))
+    args = lambda cs, ce: (bm.handle, i64(ids), i32(lens), i64(offs), i32(tabs), i32(free), i32(refs), cs, ce,
+                           C.byref(ns), C.byref(ne), C.byref(nf))
+    assert lib.pa_bm_export(*args(1, 4)) == pa.PA_ERR_CAPACITY            # two sequences live
+    assert (ns.value, ne.value, nf.value) == (2, 4, 6)
+    assert lib.pa_bm_export(*args(2, 3)) == pa.PA_ERR_CAPACITY            # four table entries
+    assert lib.pa_bm_export(*args(2, 4)) == 0
+    assert ids.tolist() == [3, 7] and offs.tolist() == [0, 1, 4] and tabs.tolist() == [3, 0, 1, 2]
+    assert lib.pa_bm_export(*args(-1, 4)) == pa._binding.PA_ERR_INVALID
+    bm.close()
