@@ -23,7 +23,6 @@
 #include <cstring>
 #include <new>
 #include <unordered_map>
-#include <unordered_set>
 #include <vector>
 
 #include "pa.h"
@@ -521,12 +520,18 @@ int pa_bm_fork_many(pa_bm* bm, const int64_t* parent_ids, const int64_t* child_i
   return guarded([&]() -> int {
     if (!bm || n < 0 || (n > 0 && (!parent_ids || !child_ids))) return PA_ERR_INVALID;
     // all-or-nothing: check the whole batch in order (a child forked earlier in the batch may
-    // be a later parent) before changing anything
-    std::unordered_set<int64_t> born;
+    // be a later parent) before changing anything.  born = (child id, position) sorted, so
+    // "x is a child of an earlier fork" is one binary search: the first position of x < i.
+    std::vector<std::pair<int64_t, int32_t>> born(static_cast<size_t>(n));
+    for (int32_t i = 0; i < n; ++i) born[i] = {child_ids[i], i};
+    std::sort(born.begin(), born.end());
+    auto born_before = [&](int64_t x, int32_t i) {
+      const auto it = std::lower_bound(born.begin(), born.end(), std::make_pair(x, INT32_MIN));
+      return it != born.end() && it->first == x && it->second < i;
+    };
     for (int32_t i = 0; i < n; ++i) {
-      if (!bm->seqs.count(parent_ids[i]) && !born.count(parent_ids[i])) return PA_ERR_UNKNOWN_SEQ;
-      if (bm->seqs.count(child_ids[i]) || born.count(child_ids[i])) return PA_ERR_SEQ_EXISTS;
-      born.insert(child_ids[i]);
+      if (!bm->seqs.count(parent_ids[i]) && !born_before(parent_ids[i], i)) return PA_ERR_UNKNOWN_SEQ;
+      if (bm->seqs.count(child_ids[i]) || born_before(child_ids[i], i)) return PA_ERR_SEQ_EXISTS;
     }
     for (int32_t i = 0; i < n; ++i) pa_bm_fork(bm, parent_ids[i], child_ids[i]);
     return PA_OK;
