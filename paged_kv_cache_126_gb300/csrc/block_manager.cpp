@@ -171,6 +171,15 @@ struct pa_bm {
     return f;
   }
 
+  // Fork of a live parent into a child id known not to be live: the child shares every
+  // frame (each gains a reference) and inherits the length.  The child is inserted before
+  // any reference count moves, so a failed allocation leaves the manager as it was.
+  void fork_checked(const Seq& parent, int64_t child_id) {
+    Seq child = parent;  // copy of the table and the length (the insert may rehash: copy first)
+    const auto ins = seqs.emplace(child_id, std::move(child));
+    for (int32_t f : ins.first->second.frames) refs[f] += 1;
+  }
+
   void drop_ref(int32_t f) {
     if (refs[f] <= 0) return;  // already free: releasing again does nothing
     if (--refs[f] == 0) free_list.push_back(f);
@@ -497,10 +506,7 @@ int pa_bm_fork(pa_bm* bm, int64_t parent_id, int64_t child_id) {
     auto p = bm->seqs.find(parent_id);
     if (p == bm->seqs.end()) return PA_ERR_UNKNOWN_SEQ;
     if (bm->seqs.count(child_id)) return PA_ERR_SEQ_EXISTS;
-    Seq child = p->second;  // copy of the table and the length
-    // insert first: if that allocation fails, no reference count has moved
-    const auto ins = bm->seqs.emplace(child_id, std::move(child));
-    for (int32_t f : ins.first->second.frames) bm->refs[f] += 1;
+    bm->fork_checked(p->second, child_id);
     return PA_OK;
   });
 }
@@ -533,7 +539,7 @@ int pa_bm_fork_many(pa_bm* bm, const int64_t* parent_ids, const int64_t* child_i
       if (!bm->seqs.count(parent_ids[i]) && !born_before(parent_ids[i], i)) return PA_ERR_UNKNOWN_SEQ;
       if (bm->seqs.count(child_ids[i]) || born_before(child_ids[i], i)) return PA_ERR_SEQ_EXISTS;
     }
-    for (int32_t i = 0; i < n; ++i) pa_bm_fork(bm, parent_ids[i], child_ids[i]);
+    for (int32_t i = 0; i < n; ++i) bm->fork_checked(bm->seqs.find(parent_ids[i])->second, child_ids[i]);
     return PA_OK;
   });
 }
