@@ -241,6 +241,9 @@ def test_batched_fork_and_free_match_the_oracle(pa, seed):
     with pytest.raises(pa.PAError) as ei:
         bm.fork_many([live[0]], [live[1]])                     # child already live
     assert ei.value.code == pa.PA_ERR_SEQ_EXISTS
+    with pytest.raises(pa.PAError) as ei:
+        bm.fork_many([nid + 1, live[0]], [nid, nid + 1])       # parent born only later in the batch
+    assert ei.value.code == pa.PA_ERR_UNKNOWN_SEQ
     assert (bm.free_list(), bm.ref_counts(), [bm.table(s_) for s_ in live]) == before
     assert bm.free_many([live[0], live[0]]) == pa.PA_WARN_DOUBLE_FREE  # second is not live
     assert bm.free_many([]) == 0
