@@ -18,7 +18,7 @@ and "Solving the LLM Memory Wall" ("Implementation", BlockManager.allocate): a
 prompt's blocks are granted all-or-nothing -- the free count is checked before any
 frame leaves the list.
 
-Readings where the pages leave a step open (listed in the design doc):
+Readings where the pages leave a step open:
   * the block boundary test comes before looking at the tail frame, so an empty
     prompt (no frames yet) takes its first frame on the first append;
   * copy-on-write allocates the private frame first, then drops one reference from

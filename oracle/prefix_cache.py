@@ -6,7 +6,7 @@ later request whose token prefix is identical maps that part of its block table
 onto the same physical frames instead of recomputing it (the comparison table
 calls it chunk-level prefix reuse).
 
-Readings taken where the page leaves the mechanics open (listed in the design doc):
+Readings taken where the page leaves the mechanics open:
   * Only full blocks are shared.  A full block is identified exactly by its
     content prefix: the node of the block before it plus its own B token ids, a
     trie of blocks (no hashing, so no false matches).  Each registered block is a
