@@ -130,6 +130,7 @@ EXPORTED = (
 
 
 def strerror(code: int) -> str:
+    """Message of a libpa return code (``pa_strerror``)."""
     return LIB.pa_strerror(int(code)).decode()
 
 
@@ -188,18 +189,21 @@ def _ref(d: PaTensor):
 
 
 def pa_cache_append(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None) -> None:
+    """``pa_cache_append``: k_new / v_new rows [T, H, D] into the caches at slot_mapping [T] (int32; < 0 skipped)."""
     st = _stream_of(k_cache, stream)
     ds = [tensor_desc(t) for t in (k_new, v_new, slot_mapping, k_cache, v_cache)]
     _check(LIB.pa_cache_append(*map(_ref, ds), st), "pa_cache_append")
 
 
 def pa_copy_blocks(k_cache, v_cache, pairs, stream=None) -> None:
+    """``pa_copy_blocks``: whole-frame copies (src, dst) for copy-on-write, K and V caches."""
     st = _stream_of(k_cache, stream)
     ds = [tensor_desc(t) for t in (k_cache, v_cache, pairs)]
     _check(LIB.pa_copy_blocks(*map(_ref, ds), st), "pa_copy_blocks")
 
 
 def make_params(params) -> PaDecodeParams | None:
+    """A ``pa_decode_params`` from a dict of launch options (unknown keys raise ValueError; 0 = automatic)."""
     if params is None:
         return None
     if isinstance(params, PaDecodeParams):
@@ -214,6 +218,7 @@ def make_params(params) -> PaDecodeParams | None:
 
 
 def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, stream=None, params=None):
+    """``pa_decode`` (or ``pa_decode_ex`` when ``params`` is given): decode attention into ``out`` [S, H, D]."""
     st = _stream_of(q, stream)
     ds = [tensor_desc(t) for t in (q, k_cache, v_cache, block_tables, context_lens)]
     o = tensor_desc(out)
@@ -227,6 +232,7 @@ def pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, strea
 
 
 def pa_decode_ex(q, k_cache, v_cache, block_tables, context_lens, scale, out, params=None, stream=None):
+    """``pa_decode_ex``: ``pa_decode`` with explicit launch options (a dict, see ``make_params``)."""
     return pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale, out, stream=stream,
                      params=params or {})
 
@@ -288,6 +294,7 @@ def pa_decode_split(q, k_cache, v_cache, block_tables, context_lens, scale, out,
 
 
 def pa_get_device_status(stream=None) -> int:
+    """``pa_get_device_status``: synchronise the stream, return and clear the sticky PA_DEV_* bits."""
     s = stream if stream is not None else torch.cuda.current_stream()
     v = C.c_int32(0)
     _check(LIB.pa_get_device_status(C.c_void_p(s.cuda_stream), C.byref(v)), "pa_get_device_status")
@@ -305,10 +312,12 @@ def pa_selftest_wait_timeout(stream=None) -> list:
 
 
 def pa_launch_count() -> int:
+    """Kernels libpa has launched in this process (``pa_launch_count``)."""
     return int(LIB.pa_launch_count())
 
 
 def pa_shutdown() -> None:
+    """``pa_shutdown``: free the library-owned workspaces and staging rings."""
     _check(LIB.pa_shutdown(), "pa_shutdown")
 
 
@@ -336,6 +345,7 @@ class BlockManager:
         self._h = h
 
     def close(self) -> None:
+        """Destroy the native manager (``pa_bm_destroy``); later calls are invalid."""
         if self._h:
             LIB.pa_bm_destroy(self._h)
             self._h = C.c_void_p()
@@ -348,14 +358,17 @@ class BlockManager:
 
     @property
     def handle(self):
+        """The opaque ``pa_bm*`` for direct C calls."""
         return self._h
 
     def add_seq(self, seq: int, num_tokens: int) -> np.ndarray:
+        """``pa_bm_add_seq``: frames for a prompt of num_tokens (all-or-nothing); returns its slots."""
         slots = np.empty(max(int(num_tokens), 1), np.int32)
         _check(LIB.pa_bm_add_seq(self._h, int(seq), int(num_tokens), _i32(slots)), "pa_bm_add_seq")
         return slots[: int(num_tokens)]
 
     def append(self, seq: int):
+        """``pa_bm_append``: one token; returns (slot, (src, dst) copy or None)."""
         slot, src, dst = C.c_int32(), C.c_int32(), C.c_int32()
         _check(LIB.pa_bm_append(self._h, int(seq), C.byref(slot), C.byref(src), C.byref(dst)), "pa_bm_append")
         return slot.value, (None if src.value < 0 else (src.value, dst.value))
@@ -368,6 +381,7 @@ class BlockManager:
         return nc.value
 
     def step(self, seqs):
+        """``pa_bm_step``: one token for each listed sequence in order (all-or-nothing); returns (slots, copies [k, 2])."""
         ids = np.ascontiguousarray(seqs, dtype=np.int64)
         slots = np.empty(max(len(ids), 1), np.int32)
         copies = np.empty((max(len(ids), 1), 2), np.int32)
@@ -395,6 +409,7 @@ class BlockManager:
         return nc.value, slots[: L - nc.value]
 
     def step_tokens(self, seqs, tokens):
+        """``pa_bm_step_tokens``: ``step`` with the new tokens' ids (prefix-cache registration)."""
         ids = np.ascontiguousarray(seqs, dtype=np.int64)
         toks = np.ascontiguousarray(tokens, dtype=np.int32)
         n = len(ids)
@@ -408,6 +423,7 @@ class BlockManager:
         return slots[:n], copies[: nc.value]
 
     def extend_tokens(self, seq: int, tokens):
+        """``pa_bm_extend_tokens``: a chunk of tokens with their ids; returns (slots, copies)."""
         toks = np.ascontiguousarray(tokens, dtype=np.int32)
         n = len(toks)
         slots = np.empty(max(n, 1), np.int32)
@@ -418,18 +434,22 @@ class BlockManager:
         return slots[:n], copies[: nc.value]
 
     def cached_frames(self) -> list:
+        """``pa_bm_cached_frames``: 1 for each frame holding a registered block, else 0."""
         out = np.empty(self.num_blocks, np.int32)
         n = C.c_int32()
         _check(LIB.pa_bm_cached_frames(self._h, _i32(out), self.num_blocks, C.byref(n)), "pa_bm_cached_frames")
         return out.tolist()
 
     def fork(self, parent: int, child: int) -> None:
+        """``pa_bm_fork``: child shares every frame of parent (zero-copy)."""
         _check(LIB.pa_bm_fork(self._h, int(parent), int(child)), "pa_bm_fork")
 
     def free(self, seq: int) -> int:
+        """``pa_bm_free``: release a sequence; returns PA_WARN_DOUBLE_FREE if it was not live."""
         return _check(LIB.pa_bm_free(self._h, int(seq)), "pa_bm_free")
 
     def fork_many(self, parents, children) -> None:
+        """``pa_bm_fork_many``: forks in order, all-or-nothing (a child may be a later parent)."""
         p = np.ascontiguousarray(parents, dtype=np.int64)
         c = np.ascontiguousarray(children, dtype=np.int64)
         if p.shape != c.shape or p.ndim != 1:
@@ -437,14 +457,17 @@ class BlockManager:
         _check(LIB.pa_bm_fork_many(self._h, _i64(p), _i64(c), len(p)), "pa_bm_fork_many")
 
     def free_many(self, seqs) -> int:
+        """``pa_bm_free_many``: frees in order; PA_WARN_DOUBLE_FREE if any id was not live."""
         s = np.ascontiguousarray(seqs, dtype=np.int64)
         return _check(LIB.pa_bm_free_many(self._h, _i64(s), len(s)), "pa_bm_free_many")
 
     def block_tables_into(self, ids: np.ndarray, max_blocks: int, tables_out: np.ndarray, lens_out: np.ndarray):
+        """``pa_bm_block_tables`` into caller arrays: tables [n, max_blocks] (-1 padded), lens [n]."""
         _check(LIB.pa_bm_block_tables(self._h, _i64(ids), len(ids), int(max_blocks), _i32(tables_out),
                                       _i32(lens_out)), "pa_bm_block_tables")
 
     def block_tables(self, seqs, max_blocks: int):
+        """``pa_bm_block_tables``: (tables [n, max_blocks] int32, lens [n] int32) for the listed sequences."""
         ids = np.ascontiguousarray(seqs, dtype=np.int64)
         tables = np.empty((max(len(ids), 1), max(int(max_blocks), 1)), np.int32)
         lens = np.empty(max(len(ids), 1), np.int32)
@@ -452,11 +475,13 @@ class BlockManager:
         return tables[: len(ids), : int(max_blocks)], lens[: len(ids)]
 
     def seq_info(self, seq: int):
+        """``pa_bm_seq_info``: (length, number of frames) of a live sequence."""
         L, nb = C.c_int32(), C.c_int32()
         _check(LIB.pa_bm_seq_info(self._h, int(seq), C.byref(L), C.byref(nb)), "pa_bm_seq_info")
         return L.value, nb.value
 
     def table(self, seq: int) -> list:
+        """``pa_bm_table``: the frame ids of a live sequence, in order."""
         _, nb = self.seq_info(seq)
         out = np.empty(max(nb, 1), np.int32)
         n = C.c_int32()
@@ -464,29 +489,34 @@ class BlockManager:
         return out[: n.value].tolist()
 
     def slot(self, seq: int, pos: int) -> int:
+        """``pa_bm_slot``: flat slot (frame * B + offset) of token ``pos`` of a live sequence."""
         s = C.c_int32()
         _check(LIB.pa_bm_slot(self._h, int(seq), int(pos), C.byref(s)), "pa_bm_slot")
         return s.value
 
     @property
     def num_free(self) -> int:
+        """``pa_bm_num_free``: frames on the free list."""
         n = C.c_int32()
         _check(LIB.pa_bm_num_free(self._h, C.byref(n)), "pa_bm_num_free")
         return n.value
 
     def free_list(self) -> list:
+        """``pa_bm_free_list``: the free list, front (next to be handed out) first."""
         out = np.empty(self.num_blocks, np.int32)
         n = C.c_int32()
         _check(LIB.pa_bm_free_list(self._h, _i32(out), self.num_blocks, C.byref(n)), "pa_bm_free_list")
         return out[: n.value].tolist()
 
     def ref_counts(self) -> list:
+        """``pa_bm_ref_counts``: reference count of every frame."""
         out = np.empty(self.num_blocks, np.int32)
         _check(LIB.pa_bm_ref_counts(self._h, _i32(out), self.num_blocks), "pa_bm_ref_counts")
         return out.tolist()
 
     @property
     def num_seqs(self) -> int:
+        """``pa_bm_num_seqs``: live sequences."""
         n = C.c_int32()
         _check(LIB.pa_bm_num_seqs(self._h, C.byref(n)), "pa_bm_num_seqs")
         return n.value

@@ -145,6 +145,7 @@ class PagedKVEngine:
         return views
 
     def write_rows(self, slots, k_rows, v_rows) -> None:
+        """K/V rows [T, H, D] into the caches at the given slots (``pa_cache_append``)."""
         if len(slots) == 0:
             return
         k = to_device_rows(k_rows, self.dtype, self.device)
@@ -172,9 +173,11 @@ class PagedKVEngine:
         return slots, copies
 
     def fork(self, parent: int, child: int) -> None:
+        """Zero-copy fork in the block manager (frames shared, reference counts raised)."""
         self.bm.fork(parent, child)
 
     def free(self, seq: int) -> int:
+        """Release a sequence; returns PA_WARN_DOUBLE_FREE if it was not live."""
         return self.bm.free(seq)
 
     def fork_many(self, parents, children) -> None:
