@@ -36,7 +36,10 @@ class ReplayResult:
 
 
 def _kept_frames(w, keep_seqs):
-    """Frames whose contents reach the kept sequences: final tables + copy sources."""
+    """Frames whose contents reach the kept sequences: the frames their tables name
+    when they attend (and at the end), plus every frame a copy-on-write copy into one
+    of those read from, transitively.  Only the index-driven ops occur here: replay()
+    refuses ``keep_seqs`` for token-driven workloads."""
     bm = OracleBlockManager(w.num_blocks, w.block_size, w.free_order)
     edges = []
     seen = set()
@@ -52,47 +55,14 @@ def _kept_frames(w, keep_seqs):
         elif kind == "extend":
             _, copies = bm.extend(op[1], op[2])
             edges.extend(copies)
-        elif kind == "prefill":
-            for s in op[1]:
-                if s in keep_seqs:
-                    seen.update(bm.tables[s])
-        elif kind == "add_tokens":
-            n_cached, slots = bm.add_seq_cached(op[1], op[2])
-            res.n_cached[op[1]] = n_cached
-            res.trace[i] = {"slots": slots, "copies": [], "n_cached": n_cached}
-            if cache is not None and slots:
-                k, v = w.token_rows(i)
-                cache.write(slots, k[n_cached:], v[n_cached:])
-        elif kind in ("extend_tokens", "step_tokens"):
-            if kind == "extend_tokens":
-                slots, copies = bm.extend(op[1], len(op[2]), list(op[2]))
-            else:
-                slots, copies = bm.step(list(op[1]), list(op[2]))
-            res.trace[i] = {"slots": slots, "copies": copies}
-            if cache is not None:
-                for src, dst in copies:
-                    cache.copy_block(src, dst)
-                k, v = w.token_rows(i)
-                cache.write(slots, k, v)
-        elif kind == "prefill_new":
-            seqs = op[1]
-            tables = [list(bm.tables[s]) for s in seqs]
-            lens = [bm.lens[s] for s in seqs]
-            counts = [lens[j] - res.n_cached[s] for j, s in enumerate(seqs)]
-            res.attend_meta[i] = (tables, lens, counts)
-            if cache is not None:
-                qs = w.position_queries(i)
-                outs = []
-                for j, s in enumerate(seqs):
-                    q = qs[j][lens[j] - counts[j]:lens[j]]
-                    outs.append(paged_prefill(q, cache, [tables[j]], [lens[j]], [0, counts[j]], w.scale))
-                res.outputs[i] = outs
         elif kind == "free":
             bm.free(op[1])
-        elif kind == "attend":
+        elif kind in ("prefill", "attend"):
             for s in op[1]:
                 if s in keep_seqs:
                     seen.update(bm.tables[s])
+        else:
+            raise ValueError(f"op {op[0]!r} cannot be replayed for a subset of sequences")
     for s in keep_seqs:
         if s in bm.tables:
             seen.update(bm.tables[s])
