@@ -14,10 +14,14 @@ L2: no flush needed) and each batch's lengths drift only K/R tokens over the run
 prefill lengths are centred so that the mean attended length over the timed
 steps equals the sampled length.
 
-Printed: one JSON line (rank 0) with the throughput of the whole step (value),
-the decode op's roofline figure, the end-to-end figure through host buffers,
-the oracle's CPU baseline, launch count and SM clocks sampled during the timed
-region.  ``--impl reference`` times the CPU oracle instead.
+Printed: one JSON line (rank 0) with the throughput of the whole step (value:
+the K timed steps, nothing else on the stream), the decode kernel's roofline
+figure (pa_decode alone, timed in a separate phase after the steps: back-to-back
+launches over the resident batches), the end-to-end figure through host buffers,
+the other serving shapes and the chunked prefill under ``extra``, the oracle's
+CPU baseline (one thread, and one worker per affine core), launch count and SM
+clocks sampled while the GPU works.  ``--impl reference`` times the CPU oracle
+instead.
 """
 
 from __future__ import annotations
@@ -198,31 +202,42 @@ def run_cpu_baseline(cfg, budget_s: float):
     return json.loads(res.stdout.strip().splitlines()[-1])
 
 
+def run_cpu_all_cores(cfg, budget_s: float):
+    """One single-threaded oracle worker per affine core, all at once, each on its own
+    sampled sequences for ``budget_s`` seconds of decode time; the rates add up."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    env = dict(os.environ, **_CPU_ENV)
+    procs = [subprocess.Popen(_cpu_cmd(cfg, budget_s, 1 + i), stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                              text=True, env=env) for i in range(cores)]
+    outs = []
+    for p in procs:
+        o, e = p.communicate(timeout=max(900, 30 * budget_s))
+        if p.returncode != 0:
+            return {"value": None, "cores": cores, "error": e[-400:]}
+        outs.append(json.loads(o.strip().splitlines()[-1]))
+    sps = sum(o["seqs_per_sec"] for o in outs)
+    return {"value": sum(o["value"] for o in outs), "unit": UNIT, "cores": cores, "seqs_per_sec": sps,
+            "s_per_call": 1.0 / sps,
+            "sample": f"{cores} single-threaded workers at once, each cycling over its own sampled "
+                      f"sequences for {budget_s:.0f} s of decode time"}
+
+
 def cpu_sweep(keys=("0", "1", "2", "3", "4"), budget_s: float = 8.0):
     """The oracle's decode timed on the host per workload: one thread, then one
     single-threaded worker per affine core at once (each on its own sampled sequences);
     one JSON line per workload."""
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
-    env = dict(os.environ, **_CPU_ENV)
     for key in keys:
         single = run_cpu_baseline(key, budget_s)
-        procs = [subprocess.Popen(_cpu_cmd(key, budget_s, 1 + i), stdout=subprocess.PIPE, stderr=subprocess.PIPE,
-                                  text=True, env=env) for i in range(cores)]
-        outs = []
-        for p in procs:
-            o, e = p.communicate(timeout=max(900, 30 * budget_s))
-            if p.returncode != 0:
-                raise SystemExit(f"cpu worker failed: {e[-400:]}")
-            outs.append(json.loads(o.strip().splitlines()[-1]))
-        sps = sum(o["seqs_per_sec"] for o in outs)
+        allc = run_cpu_all_cores(key, budget_s)
+        if allc["value"] is None:
+            raise SystemExit(f"cpu worker failed: {allc['error']}")
         print(json.dumps({
             "cpu_baseline": key, "kind": "oracle", "unit": UNIT,
             "single": {"cores": 1, "gbps": round(single["value"], 3), "seqs_per_sec": round(single["seqs_per_sec"], 2),
                        "s_per_call": round(1.0 / single["seqs_per_sec"], 5), "sample": single["sample"]},
-            "all_cores": {"cores": cores, "gbps": round(sum(o["value"] for o in outs), 3),
-                          "seqs_per_sec": round(sps, 2), "s_per_call": round(1.0 / sps, 6),
-                          "sample": f"{cores} single-threaded workers at once, each cycling over its own sampled "
-                                    f"sequences for {budget_s:.0f} s of decode time"},
+            "all_cores": {"cores": allc["cores"], "gbps": round(allc["value"], 3),
+                          "seqs_per_sec": round(allc["seqs_per_sec"], 2), "s_per_call": round(allc["s_per_call"], 6),
+                          "sample": allc["sample"]},
             "call": "one single-sequence decode (all heads): gather of the sequence's frames, fp64 attention"}),
             flush=True)
 
@@ -315,11 +330,44 @@ class DecodeBench:
         self.scale = w.scale
         torch.cuda.synchronize()
 
-    def step(self, k, events=None):
+    def step(self, k):
         kn, vn, q = self.inputs[k % 4]
-        out, nc, lens = self.eng.decode_step(self.batches[k % self.R], kn, vn, q, self.scale, self.out,
-                                             events=events)
+        out, nc, lens = self.eng.decode_step(self.batches[k % self.R], kn, vn, q, self.scale, self.out)
         return algorithmic_bytes(lens, self.H, self.D, self.B, self.e), lens
+
+    def decode_only(self, n):
+        """pa_decode alone: n back-to-back launches over the resident batches in rotation
+        (every launch reads a different batch, far beyond L2), each batch at its current
+        length.  The launches are queued behind a ~1 ms GPU sleep, so the start event
+        fires with launches already waiting and no host enqueue time falls inside the
+        bracket.  Returns (mean us per launch, mean algorithmic bytes per launch, n)."""
+        torch = self.torch
+        st = torch.cuda.current_stream(self.eng.device)
+        metas = []
+        for ids in self.batches:
+            tables, lens = self.eng.bm.block_tables(ids, self.eng.max_blocks)
+            metas.append((torch.from_numpy(tables).to(self.eng.device), torch.from_numpy(lens).to(self.eng.device),
+                          algorithmic_bytes(lens, self.H, self.D, self.B, self.e)))
+        q = self.inputs[0][2]
+        out = torch.empty_like(self.out)
+        kc, vc = self.eng.k_cache, self.eng.v_cache
+
+        def launch(i):
+            t, ln, _ = metas[i % self.R]
+            self.pa.pa_decode(q, kc, vc, t, ln, self.scale, out)
+
+        for i in range(3):
+            launch(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(2_000_000)
+        e0.record(st)
+        for i in range(n):
+            launch(i)
+        e1.record(st)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / n
+        return us, sum(metas[i % self.R][2] for i in range(n)) / n, n
 
 
 def gpu_arm(args):
@@ -339,41 +387,40 @@ def gpu_arm(args):
     bench = DecodeBench(args.config, R, per_batch, centre, rank_seed(1234, rank), device)
     st = torch.cuda.current_stream(device)
 
+    # The clock sampler starts before the warm-up: its start-up must not leave the GPU
+    # idle between the warm-up and the timed steps.
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    barrier()
     for k in range(W):
         bench.step(k)
     torch.cuda.synchronize()
 
-    # ---- timed region: K steps, inputs resident in HBM --------------------------------------
-    # pa_decode is bracketed by CUDA events on every EVERY-th step only: an event
-    # between the append and decode kernels stops the decode kernel from starting
-    # while the append drains (programmatic dependent launch), so timing every step
-    # would slow every step.  EVERY is coprime with the batch rotation.
-    EVERY = 7
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) if k % EVERY == 0 else None
-          for k in range(K)]
+    # ---- timed region: K whole steps (pa_step_decode), inputs resident in HBM ----------------
+    # Nothing but the steps runs on the stream between the two events.
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local)
-    if rank == 0:
-        clocks.start()
     barrier()
     torch.cuda.synchronize()
     n_launch0 = pa.pa_launch_count()
     step_bytes, all_lens = [], []
     t_start.record(st)
     for k in range(K):
-        b, lens = bench.step(W + k, events=ev[k])
+        b, lens = bench.step(W + k)
         step_bytes.append(b)
         all_lens.append(float(np.mean(lens)))
     t_end.record(st)
     torch.cuda.synchronize()
     barrier()
     launches = pa.pa_launch_count() - n_launch0
-    clk = clocks.stop() if rank == 0 else None
     ms = t_start.elapsed_time(t_end)
-    dec_ms = [e[0].elapsed_time(e[1]) for e in ev if e is not None]
-    dec_bytes = [b for b, e in zip(step_bytes, ev) if e is not None]
     my_bytes = float(sum(step_bytes))
     max_ms, tot_bytes = reduce_max_sum(ms, my_bytes, device)
+
+    # ---- the decode kernel alone (roofline), after the timed region --------------------------
+    n_dec = max(32, 2 * R)
+    dec_us, dec_bytes, _ = bench.decode_only(n_dec)
+    clk = clocks.stop() if rank == 0 else None
 
     # ---- end to end: host buffers, copies inside the timed region ---------------------------
     dt = bench.inputs[0][0].dtype
@@ -435,8 +482,7 @@ def gpu_arm(args):
     if rank != 0:
         return
     peak, peak_src = _peaks()
-    dec_avg_ms = sum(dec_ms) / len(dec_ms)
-    achieved = (sum(dec_bytes) / len(dec_bytes)) / (dec_avg_ms * 1e-3) / 1e9
+    achieved = dec_bytes / (dec_us * 1e-6) / 1e9
     traffic = _profile_traffic("decode batch 64 x U[512,2048]")
     value = tot_bytes / (max_ms * 1e-3) / 1e9
     line = {
@@ -466,15 +512,19 @@ def gpu_arm(args):
         "roofline": {
             "bound": "hbm",
             "kernel": "decode_kernel (pa_decode; the log-sum-exp merge runs inside it)",
-            "timing": f"CUDA events around pa_decode on every {EVERY}th timed step ({len(dec_ms)} launches)",
+            "timing": f"CUDA events around {n_dec} back-to-back pa_decode launches over the {R} resident "
+                      f"batches in rotation (each launch reads a different batch, > L2), queued behind a GPU sleep; "
+                      f"run after the timed steps",
             "achieved": round(achieved, 1),
             "peak": peak,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "traffic": traffic,
             "peak_source": peak_src,
-            "decode_us_per_launch": round(1000 * dec_avg_ms, 2),
-            "algorithmic_bytes_per_launch": round(sum(dec_bytes) / len(dec_bytes)),
+            "decode_us_per_launch": round(dec_us, 2),
+            "algorithmic_bytes_per_launch": round(dec_bytes),
+            "launches": n_dec,
+            "decode_within_step": bool(dec_us <= 1000 * max_ms / K),
         },
         "e2e": {
             "value": round(e2e_tot / (e2e_max_ms * 1e-3) / 1e9, 1),
@@ -489,15 +539,22 @@ def gpu_arm(args):
         "clocks": clk,
     }
     if not args.no_extra:
-        line["extra"] = {"fixed_64x2048": fixed_variant(args, device)}
+        del bench
+        torch.cuda.empty_cache()
+        line["extra"] = {"fixed_64x2048": fixed_variant(args, device), **bench_extras(device)}
     if not args.no_cpu:
-        line["cpu_baseline"] = run_cpu_baseline(args.config, args.cpu_budget or 12.0)
+        cpu = run_cpu_baseline(args.config, args.cpu_budget or 8.0)
+        allc = run_cpu_all_cores(args.config, args.cpu_budget or 8.0)
+        if allc.get("value") is not None:
+            allc["value"] = round(allc["value"], 3)
+        cpu["all_cores"] = allc
+        line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
 
 
 def fixed_variant(args, device):
-    """The same step on 64 sequences of exactly 2048 tokens (the '64x2k' figure)."""
-    import numpy as np
+    """The same step on 64 sequences of exactly 2048 tokens (the '64x2k' figure), then
+    the decode kernel alone as in the main line."""
     import torch
 
     R, K = 4, max(40, args.steps // 8)
@@ -507,22 +564,22 @@ def fixed_variant(args, device):
         bench.step(k)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) if k % 7 == 0 else None
-          for k in range(K)]
-    tot, sampled = 0, []
+    tot = 0
     e0.record(st)
     for k in range(K):
-        b, _ = bench.step(8 + k, events=ev[k])
+        b, _ = bench.step(8 + k)
         tot += b
-        if ev[k] is not None:
-            sampled.append(b)
     e1.record(st)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    dec = float(np.mean([e[0].elapsed_time(e[1]) for e in ev if e is not None]))
+    dec_us, dec_bytes, n_dec = bench.decode_only(32)
+    peak, _ = _peaks()
     res = {"steps": K, "gbps": round(tot / (ms * 1e-3) / 1e9, 1), "seqs_per_sec": round(64 * K / (ms * 1e-3), 1),
-           "decode_us_per_launch": round(1000 * dec, 2),
-           "decode_gbps": round(float(np.mean(sampled)) / (dec * 1e-3) / 1e9, 1)}
+           "ms_per_step": round(ms / K, 5),
+           "decode_us_per_launch": round(dec_us, 2), "decode_launches": n_dec,
+           "decode_gbps": round(dec_bytes / (dec_us * 1e-6) / 1e9, 1),
+           "decode_frac": round(dec_bytes / (dec_us * 1e-6) / 1e9 / peak, 4),
+           "decode_seqs_per_sec": round(64 / (dec_us * 1e-6), 1)}
     del bench
     torch.cuda.empty_cache()
     return res
@@ -532,123 +589,203 @@ def fixed_variant(args, device):
 SWEEP_KEYS = ("0", "1", "1x", "2", "2n", "3", "3c", "3s", "4")
 
 
-def sweep(keys, reps=20, flushed_reps=50):
-    """pa_decode on the final state of each workload's replay (host-generated data,
-    automatic launch options): one JSON line per workload.  "3c" is the unshared
-    control of the parallel-sampling workload: the same final lengths, every branch
-    with private frames; "3s" is the parallel-sampling workload through the
-    shared-prefix decode (each shared prompt frame read once for its branches); "2n"
-    is the long-context workload without split-context partitions (one item per
-    sequence and head group), the baseline of the split's speedup.
+def replay_device_rows(eng, w, seed):
+    """Run a workload's operations through the engine with the K/V rows drawn on the
+    device: the workload's lengths, forks, copy-on-write copies, frees and frame order,
+    values N(0, sigma^2) rounded to the storage dtype.  For timing only (the values do
+    not change the work); drawing multi-GB caches on the host would dominate the run.
+    Returns the number of copy-on-write frame copies."""
+    import torch
 
-    Two timings: the mean over ``reps`` back-to-back launches (``decode_us``), and the
-    median over ``flushed_reps`` launches each timed alone with CUDA events after a
-    read of twice the L2 size (``flushed``: no K/V byte is served from L2 left warm by
-    the previous launch).  A read leaves clean lines; a memset flush (also reported,
-    ``flushed_memset``) leaves the L2 full of dirty lines, and their write-back
-    (~the L2 size) then lands inside the timed launch."""
+    import paged_kv_cache_126_gb300 as pa
+
+    g = torch.Generator(device=eng.device)
+    g.manual_seed(seed)
+    dt = pa.engine.TORCH_DTYPES[w.dtype]
+    H, D = w.num_heads, w.head_dim
+
+    def rows(n):
+        mk = lambda: (torch.randn(n, H, D, generator=g, device=eng.device) * w.sigma).to(dt)  # noqa: E731
+        return mk(), mk()
+
+    copies = 0
+    for op in w.ops:
+        kind = op[0]
+        if kind == "add":
+            eng.add_seq(op[1], *rows(op[2]))
+        elif kind == "fork":
+            eng.fork(op[1], op[2])
+        elif kind == "step":
+            copies += len(eng.step(op[1], *rows(len(op[1])))[1])
+        elif kind == "extend":
+            copies += len(eng.extend(op[1], *rows(op[2]))[1])
+        elif kind == "free":
+            eng.free(op[1])
+        elif kind not in ("attend", "prefill"):
+            raise ValueError(f"op {kind!r} has no device-row replay")
+    return copies
+
+
+def _workload_engine(key, dev, device_rows):
+    """Engine holding workload `key` at its final state (host-drawn rows through the
+    workload generator, or device-drawn rows), plus the copy-on-write copy count."""
+    import paged_kv_cache_126_gb300 as pa
+    import workloads
+
+    cfg = {"0": 0, "1": 1, "1x": "1x", "2": 2, "2n": 2, "3": 3, "3c": 3, "3s": 3, "4": 4}[key]
+    w = workloads.build(cfg)
+    if key == "3c":
+        L = [w.final_lens[s] for s in range(len(w.final_lens))]
+        w = workloads.custom(L, H=w.num_heads, D=w.head_dim, B=w.block_size, dtype=w.dtype, seed=w.seed,
+                             name="parallel-sampling control: same lengths, no shared frames")
+    eng = pa.PagedKVEngine(w.num_blocks, w.block_size, w.num_heads, w.head_dim, w.dtype,
+                           free_order=w.free_order, device=dev, max_seqs=max(64, len(w.final_lens)),
+                           max_blocks_per_seq=max(1, max(-(-L // w.block_size) for L in w.final_lens.values())))
+    if device_rows:
+        copies = replay_device_rows(eng, w, 4000 + w.seed)
+    else:
+        _, trace = pa.run_workload_ops(eng, w)
+        copies = sum(len(t["copies"]) for t in trace.values() if isinstance(t, dict) and "copies" in t)
+    return w, eng, copies
+
+
+def decode_figures(key, reps=20, flushed_reps=50, device_rows=False, memset=True, append=True,
+                   sample_clocks=False):
+    """pa_decode on the final state of one workload's replay (automatic launch options;
+    "3s": the engine's automatic choice, the shared-prefix decode; "2n": no
+    split-context partitions), timed two ways.
+
+    ``decode_us``: mean over ``reps`` back-to-back launches queued behind a GPU sleep.
+    ``flushed``: median over ``flushed_reps`` launches each timed alone with CUDA events
+    after a read of twice the L2 size (no K/V byte served from L2 left warm by the
+    previous launch).  A read leaves clean lines; a memset flush (``flushed_memset``)
+    leaves the L2 full of dirty lines whose write-back (~the L2 size) then lands inside
+    the timed launch.  Bytes: algorithmic (logical: every sequence's attended tokens)
+    and unique frames (each frame that some sequence reads, once)."""
     import numpy as np
     import torch
 
     import paged_kv_cache_126_gb300 as pa
-    import workloads
 
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
+    dev = torch.device("cuda", torch.cuda.current_device())
     st = torch.cuda.current_stream(dev)
-    for key in keys:
-        cfg = {"0": 0, "1": 1, "1x": "1x", "2": 2, "2n": 2, "3": 3, "3c": 3, "3s": 3, "4": 4}[key]
-        params = {"share_prefix": 1} if key == "3s" else ({"partition_tokens": -1} if key == "2n" else None)
-        w = workloads.build(cfg)
-        if key == "3c":
-            L = [w.final_lens[s] for s in range(len(w.final_lens))]
-            w = workloads.custom(L, H=w.num_heads, D=w.head_dim, B=w.block_size, dtype=w.dtype, seed=w.seed,
-                                 name="parallel-sampling control: same lengths, no shared frames")
-        eng = pa.PagedKVEngine(w.num_blocks, w.block_size, w.num_heads, w.head_dim, w.dtype,
-                               free_order=w.free_order, device=dev, max_seqs=max(64, len(w.final_lens)),
-                               max_blocks_per_seq=max(1, max(-(-L // w.block_size) for L in w.final_lens.values())))
-        outs, trace = pa.run_workload_ops(eng, w)
-        op = w.attend_ops[-1]
-        seqs = w.ops[op][1]
-        tables, lens = eng.bm.block_tables(seqs, eng.max_blocks)
-        tt, ll = torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev)
-        q = pa.to_device_rows(w.query(op), w.dtype, dev)
-        out = torch.empty_like(q)
-        n = reps if key != "4" else max(5, reps // 2)
-        for _ in range(3):
-            pa.pa_decode(q, eng.k_cache, eng.v_cache, tt, ll, w.scale, out, params=params)
+    w, eng, copies = _workload_engine(key, dev, device_rows)
+    op = w.attend_ops[-1]
+    seqs = w.ops[op][1]
+    tables, lens = eng.bm.block_tables(seqs, eng.max_blocks)
+    if key == "3s":
+        params = eng._decode_params(tables, None)
+        assert params is not None, "the parallel-sampling batch should take the shared-prefix decode"
+    else:
+        params = {"partition_tokens": -1} if key == "2n" else None
+    tt, ll = torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev)
+    q = pa.to_device_rows(w.query(op), w.dtype, dev)
+    out = torch.empty_like(q)
+
+    def decode():
+        pa.pa_decode(q, eng.k_cache, eng.v_cache, tt, ll, w.scale, out, params=params)
+
+    clocks = ClockSampler(dev.index, interval_ms=20) if sample_clocks else None
+    if clocks:
+        clocks.start()
+    for _ in range(3):
+        decode()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(2_000_000)
+    e0.record(st)
+    for _ in range(reps):
+        decode()
+    e1.record(st)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / reps * 1e3
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or 132 * 2 ** 20
+    flush = torch.ones(2 * l2 // 4, dtype=torch.int32, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(flushed_reps)]
+
+    def isolated(fn, clear):
+        for a, b in ev:
+            clear()
+            a.record(st)
+            fn()
+            b.record(st)
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(st)
-        for _ in range(n):
-            pa.pa_decode(q, eng.k_cache, eng.v_cache, tt, ll, w.scale, out, params=params)
-        e1.record(st)
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) / n * 1e3
-        l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or 132 * 2 ** 20
-        flush = torch.ones(2 * l2 // 4, dtype=torch.int32, device=dev)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(flushed_reps)]
+        return float(np.median([a.elapsed_time(b) for a, b in ev])) * 1e3
 
-        def isolated(fn, clear):
-            for a, b in ev:
-                clear()
-                a.record(st)
-                fn()
-                b.record(st)
-            torch.cuda.synchronize()
-            return float(np.median([a.elapsed_time(b) for a, b in ev])) * 1e3
-
-        def decode():
-            pa.pa_decode(q, eng.k_cache, eng.v_cache, tt, ll, w.scale, out, params=params)
-
-        us_flushed = isolated(decode, lambda: flush.sum())
-        us_memset = isolated(decode, lambda: flush.zero_())
-        # pa_cache_append of one new row per sequence at its last token's slot (the
-        # rows already there, so the cache is unchanged): read k_new, v_new and the
-        # slots, write the two cache rows
+    us_flushed = isolated(decode, lambda: flush.sum())
+    clk = clocks.stop() if clocks else None
+    us_memset = isolated(decode, lambda: flush.zero_()) if memset else None
+    logical = algorithmic_bytes(lens, w.num_heads, w.head_dim, w.block_size, w.elem_bytes)
+    frames = set()
+    for t, L in zip(tables, lens):
+        frames.update(t[: -(-int(L) // w.block_size)].tolist())
+    unique = len(frames) * w.block_size * w.num_heads * w.head_dim * w.elem_bytes * 2
+    peak, _ = _peaks()
+    gb = lambda b, t: round(b / (t * 1e-6) / 1e9, 1)  # noqa: E731
+    res = {
+        "workload": key, "name": w.name, "params": params, "seqs": len(seqs), "sum_len": int(np.sum(lens)),
+        "data": "device-drawn rows (timing only)" if device_rows else "host-drawn rows (the workload generator)",
+        "decode_us": round(us, 2), "algorithmic_bytes": logical, "gbps": gb(logical, us),
+        "pct_of_peak": round(100 * logical / (us * 1e-6) / 1e9 / peak, 1),
+        "unique_frame_bytes": unique, "gbps_unique_frames": gb(unique, us),
+        "seqs_per_sec": round(len(seqs) / (us * 1e-6), 1),
+        "flushed": {"decode_us_median": round(us_flushed, 2), "launches": flushed_reps,
+                    "gbps": gb(logical, us_flushed),
+                    "pct_of_peak": round(100 * logical / (us_flushed * 1e-6) / 1e9 / peak, 1),
+                    "gbps_unique_frames": gb(unique, us_flushed),
+                    "frac_unique_frames": round(unique / (us_flushed * 1e-6) / 1e9 / peak, 4),
+                    "seqs_per_sec": round(len(seqs) / (us_flushed * 1e-6), 1)},
+        "cow_copies": copies,
+    }
+    if us_memset is not None:
+        res["flushed_memset"] = {"decode_us_median": round(us_memset, 2), "gbps": gb(logical, us_memset)}
+    if clk is not None:
+        res["clocks"] = clk
+    if append:
+        # pa_cache_append of one new row per sequence at its last token's slot (the rows
+        # already there, so the cache is unchanged): read k_new, v_new and the slots,
+        # write the two cache rows
         slots = torch.tensor([eng.bm.slot(s, int(L) - 1) for s, L in zip(seqs, lens) if L > 0],
                              dtype=torch.int32, device=dev)
         kn = eng.k_cache.view(-1, w.num_heads, w.head_dim)[slots.long()].contiguous()
         vn = eng.v_cache.view(-1, w.num_heads, w.head_dim)[slots.long()].contiguous()
-        for _ in range(3):
+
+        def app():
             pa.pa_cache_append(kn, vn, slots, eng.k_cache, eng.v_cache)
+
+        for _ in range(3):
+            app()
         torch.cuda.synchronize()
         e0.record(st)
         for _ in range(reps):
-            pa.pa_cache_append(kn, vn, slots, eng.k_cache, eng.v_cache)
+            app()
         e1.record(st)
         torch.cuda.synchronize()
         ap_us = e0.elapsed_time(e1) / reps * 1e3
-        ap_us_flushed = isolated(lambda: pa.pa_cache_append(kn, vn, slots, eng.k_cache, eng.v_cache),
-                                 lambda: flush.sum())
+        ap_us_flushed = isolated(app, lambda: flush.sum())
         ap_bytes = 4 * kn.numel() * kn.element_size() + 4 * slots.numel()
-        del flush
-        logical = algorithmic_bytes(lens, w.num_heads, w.head_dim, w.block_size, w.elem_bytes)
-        frames = set()
-        for t, L in zip(tables, lens):
-            frames.update(t[: -(-int(L) // w.block_size)].tolist())
-        unique = len(frames) * w.block_size * w.num_heads * w.head_dim * w.elem_bytes * 2
-        peak, _ = _peaks()
-        print(json.dumps({
-            "workload": key, "name": w.name, "params": params, "seqs": len(seqs), "sum_len": int(np.sum(lens)),
-            "decode_us": round(us, 2), "algorithmic_bytes": logical, "gbps": round(logical / (us * 1e-6) / 1e9, 1),
-            "pct_of_peak": round(100 * logical / (us * 1e-6) / 1e9 / peak, 1),
-            "unique_frame_bytes": unique, "gbps_unique_frames": round(unique / (us * 1e-6) / 1e9, 1),
-            "seqs_per_sec": round(len(seqs) / (us * 1e-6), 1),
-            "flushed": {"decode_us_median": round(us_flushed, 2), "launches": flushed_reps,
-                        "gbps": round(logical / (us_flushed * 1e-6) / 1e9, 1),
-                        "pct_of_peak": round(100 * logical / (us_flushed * 1e-6) / 1e9 / peak, 1),
-                        "gbps_unique_frames": round(unique / (us_flushed * 1e-6) / 1e9, 1),
-                        "seqs_per_sec": round(len(seqs) / (us_flushed * 1e-6), 1)},
-            "flushed_memset": {"decode_us_median": round(us_memset, 2),
-                               "gbps": round(logical / (us_memset * 1e-6) / 1e9, 1)},
-            "append": {"rows": int(slots.numel()), "bytes": int(ap_bytes), "us": round(ap_us, 2),
-                       "gbps": round(ap_bytes / (ap_us * 1e-6) / 1e9, 1), "us_flushed_median": round(ap_us_flushed, 2),
-                       "gbps_flushed": round(ap_bytes / (ap_us_flushed * 1e-6) / 1e9, 1)},
-            "cow_copies": sum(len(t["copies"]) for t in trace.values() if isinstance(t, dict) and "copies" in t)}), flush=True)
-        del eng, outs, tt, ll, q, out, kn, vn, slots
-        torch.cuda.empty_cache()
+        res["append"] = {"rows": int(slots.numel()), "bytes": int(ap_bytes), "us": round(ap_us, 2),
+                         "gbps": gb(ap_bytes, ap_us), "us_flushed_median": round(ap_us_flushed, 2),
+                         "gbps_flushed": gb(ap_bytes, ap_us_flushed)}
+    del flush, eng, tt, ll, q, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def sweep(keys, reps=20, flushed_reps=50):
+    """pa_decode on the final state of each workload's replay (host-drawn rows): one
+    JSON line per workload (``decode_figures``).  "3c" is the unshared control of the
+    parallel-sampling workload (the same final lengths, every branch with private
+    frames); "3s" is the parallel-sampling workload through the shared-prefix decode
+    (each shared prompt frame read once for its branches); "2n" is the long-context
+    workload without split-context partitions (one item per sequence and head group),
+    the baseline of the split's speedup."""
+    import torch
+
+    torch.cuda.set_device(0)
+    for key in keys:
+        print(json.dumps(decode_figures(key, reps, flushed_reps)), flush=True)
 
 
 # ----------------------------------------------------------------------------- chunked prefill
@@ -662,89 +799,77 @@ def prefill_flops(prefix_lens, chunk_lens, H, D) -> int:
     return 4 * D * H * total
 
 
-def prefill_bench(reps=20):
-    """pa_prefill on the chunked-prefill batch; one JSON line (TFLOP/s)."""
+def prefill_figures(reps=20, flushed_reps=50, e2e=True, device_rows=False, sample_clocks=False, dtype="f16"):
+    """pa_prefill on the chunked-prefill batch (16 sequences, prefix ~U[0, 3072], a
+    512-token chunk each, H=32, D=128, B=16, fp16): TFLOP/s of causal FLOPs, mean of
+    ``reps`` back-to-back launches queued behind a GPU sleep (the batch's K/V, ~0.9 GB,
+    exceeds L2), and the median of ``flushed_reps`` launches each timed alone after a
+    read of twice the L2 size.  ``e2e``: the chunk step through host buffers (q, k, v
+    rows in from pinned memory, pa_cache_append, pa_prefill, output back)."""
     import numpy as np
     import torch
 
     import paged_kv_cache_126_gb300 as pa
     import workloads
 
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
+    dev = torch.device("cuda", torch.cuda.current_device())
     st = torch.cuda.current_stream(dev)
-    w = workloads.prefill_batch()
+    w = workloads.prefill_batch(dtype=dtype)
     eng = pa.PagedKVEngine(w.num_blocks, w.block_size, w.num_heads, w.head_dim, w.dtype, free_order=w.free_order,
                            device=dev, max_seqs=64,
                            max_blocks_per_seq=max(-(-L // w.block_size) for L in w.final_lens.values()))
     (op,) = w.prefill_ops
-    for i, o in enumerate(w.ops[:op]):
-        if o[0] == "add":
-            eng.add_seq(o[1], *w.rows(i))
-        elif o[0] == "extend":
-            eng.extend(o[1], *w.rows(i))
+    if device_rows:
+        replay_device_rows(eng, w, 5000 + w.seed)
+    else:
+        for i, o in enumerate(w.ops[:op]):
+            if o[0] == "add":
+                eng.add_seq(o[1], *w.rows(i))
+            elif o[0] == "extend":
+                eng.extend(o[1], *w.rows(i))
     seqs, counts = w.ops[op][1], w.ops[op][2]
     tables, lens = eng.bm.block_tables(seqs, eng.max_blocks)
     qs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     tt, ll, qq = (torch.from_numpy(x).to(dev) for x in (tables, lens, qs))
-    q = pa.to_device_rows(w.query(op), w.dtype, dev)
+    if device_rows:
+        g = torch.Generator(device=dev)
+        g.manual_seed(6000 + w.seed)
+        q = torch.randn(int(qs[-1]), w.num_heads, w.head_dim, generator=g, device=dev).to(
+            pa.engine.TORCH_DTYPES[w.dtype])
+    else:
+        q = pa.to_device_rows(w.query(op), w.dtype, dev)
     out = torch.empty_like(q)
-    for _ in range(3):
+
+    def launch():
         pa.pa_prefill(q, eng.k_cache, eng.v_cache, tt, ll, qq, w.scale, out)
+
+    clocks = ClockSampler(dev.index, interval_ms=20) if sample_clocks else None
+    if clocks:
+        clocks.start()
+    for _ in range(3):
+        launch()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(2_000_000)
     e0.record(st)
     for _ in range(reps):
-        pa.pa_prefill(q, eng.k_cache, eng.v_cache, tt, ll, qq, w.scale, out)
+        launch()
     e1.record(st)
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) / reps * 1e3
-    # the same launch timed alone after a read of twice the L2 size (median of 50)
+    # the same launch timed alone after a read of twice the L2 size
     l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or 132 * 2 ** 20
     flush = torch.ones(2 * l2 // 4, dtype=torch.int32, device=dev)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(flushed_reps)]
     for a, b in ev:
         flush.sum()
         a.record(st)
-        pa.pa_prefill(q, eng.k_cache, eng.v_cache, tt, ll, qq, w.scale, out)
+        launch()
         b.record(st)
     torch.cuda.synchronize()
     us_flushed = float(np.median([a.elapsed_time(b) for a, b in ev])) * 1e3
+    clk = clocks.stop() if clocks else None
     del flush
-    # End to end through host buffers: every step copies the chunk's queries and its new
-    # K/V rows from pinned host memory, appends the rows at their slots (the values
-    # already there: the cache is unchanged), prefills, and copies the output back.
-    slot_list = []
-    for s_, L_, n_ in zip(seqs, lens, counts):
-        slot_list += [eng.bm.slot(s_, p_) for p_ in range(int(L_) - int(n_), int(L_))]
-    slots = torch.tensor(slot_list, dtype=torch.int32, device=dev)
-    kn = eng.k_cache.view(-1, w.num_heads, w.head_dim)[slots.long()]
-    vn = eng.v_cache.view(-1, w.num_heads, w.head_dim)[slots.long()]
-    hq, hk, hv = (x.cpu().pin_memory() for x in (q, kn, vn))
-    hout = torch.empty_like(out, device="cpu").pin_memory()
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
-    k_e2e = 10
-
-    def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        pa.pa_cache_append(dk, dv, slots, eng.k_cache, eng.v_cache)
-        pa.pa_prefill(dq, eng.k_cache, eng.v_cache, tt, ll, qq, w.scale, out)
-        hout.copy_(out, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0.record(st)
-    for _ in range(k_e2e):
-        e2e_step()
-    e1.record(st)
-    torch.cuda.synchronize()
-    e2e_us = e0.elapsed_time(e1) / k_e2e * 1e3
-    assert torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16))
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
-    d2h = hout.numel() * hout.element_size()
     prefix = [int(L) - int(n) for L, n in zip(lens, counts)]
     flops = prefill_flops(prefix, counts, w.num_heads, w.head_dim)
     try:
@@ -753,17 +878,100 @@ def prefill_bench(reps=20):
     except Exception:
         peak, src = 1900.0, "fallback (1.9 PFLOP/s)"
     tf = flops / (us * 1e-6) / 1e12
-    print(json.dumps({"metric": "chunked prefill attention TFLOP/s (causal FLOPs)", "workload": w.name,
-                      "prefill_us": round(us, 2), "flops": flops, "tflops": round(tf, 1),
-                      "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
-                                   "frac": round(tf / peak, 4), "peak_source": src},
-                      "flushed": {"prefill_us_median": round(us_flushed, 2), "launches": 50,
-                                  "tflops": round(flops / (us_flushed * 1e-6) / 1e12, 1)},
-                      "e2e": {"us_per_step": round(e2e_us, 2), "tflops": round(flops / (e2e_us * 1e-6) / 1e12, 1),
-                              "steps": k_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                              "step": "queries and the chunk's K/V rows copied from pinned host memory, "
-                                      "pa_cache_append of the chunk, pa_prefill, output copied back"},
-                      "query_rows": int(qs[-1]), "dtype": w.dtype}), flush=True)
+    res = {"metric": "chunked prefill attention TFLOP/s (causal FLOPs)", "workload": w.name,
+           "prefill_us": round(us, 2), "flops": flops, "tflops": round(tf, 1),
+           "timing": f"mean of {reps} back-to-back launches queued behind a GPU sleep",
+           "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                        "frac": round(tf / peak, 4), "peak_source": src},
+           "flushed": {"prefill_us_median": round(us_flushed, 2), "launches": flushed_reps,
+                       "tflops": round(flops / (us_flushed * 1e-6) / 1e12, 1)},
+           "query_rows": int(qs[-1]), "dtype": w.dtype,
+           "data": "device-drawn rows (timing only)" if device_rows else "host-drawn rows (the workload generator)"}
+    if clk is not None:
+        res["clocks"] = clk
+    if e2e:
+        # End to end through host buffers: every step copies the chunk's queries and its
+        # new K/V rows from pinned host memory, appends the rows at their slots (the
+        # values already there: the cache is unchanged), prefills, and copies the output
+        # back.
+        slot_list = []
+        for s_, L_, n_ in zip(seqs, lens, counts):
+            slot_list += [eng.bm.slot(s_, p_) for p_ in range(int(L_) - int(n_), int(L_))]
+        slots = torch.tensor(slot_list, dtype=torch.int32, device=dev)
+        kn = eng.k_cache.view(-1, w.num_heads, w.head_dim)[slots.long()]
+        vn = eng.v_cache.view(-1, w.num_heads, w.head_dim)[slots.long()]
+        hq, hk, hv = (x.cpu().pin_memory() for x in (q, kn, vn))
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+        k_e2e = 10
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            pa.pa_cache_append(dk, dv, slots, eng.k_cache, eng.v_cache)
+            pa.pa_prefill(dq, eng.k_cache, eng.v_cache, tt, ll, qq, w.scale, out)
+            hout.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0.record(st)
+        for _ in range(k_e2e):
+            e2e_step()
+        e1.record(st)
+        torch.cuda.synchronize()
+        e2e_us = e0.elapsed_time(e1) / k_e2e * 1e3
+        assert torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16))
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+        d2h = hout.numel() * hout.element_size()
+        res["e2e"] = {"us_per_step": round(e2e_us, 2), "tflops": round(flops / (e2e_us * 1e-6) / 1e12, 1),
+                      "steps": k_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "step": "queries and the chunk's K/V rows copied from pinned host memory, "
+                              "pa_cache_append of the chunk, pa_prefill, output copied back"}
+    del eng
+    torch.cuda.empty_cache()
+    return res
+
+
+def prefill_bench(reps=20, dtype="f16"):
+    """pa_prefill on the chunked-prefill batch; one JSON line (TFLOP/s)."""
+    import torch
+
+    torch.cuda.set_device(0)
+    print(json.dumps(prefill_figures(reps, dtype=dtype)), flush=True)
+
+
+def bench_extras(device, reps=10, flushed_reps=10):
+    """The other serving shapes, each on the decode kernel path the engine picks, with
+    device-drawn rows: long context 4 x 16384 (split contexts + merge), parallel
+    sampling with copy-on-write (plain and through the shared-prefix decode), the
+    256-sequence serving mix (with its append), and the chunked prefill."""
+    peak, src = _peaks()
+    out = {}
+    for key, name in (("2", "cfg2"), ("3", "cfg3"), ("3s", "cfg3_shared"), ("4", "cfg4")):
+        f = decode_figures(key, reps, flushed_reps, device_rows=True, memset=False, append=(key == "4"),
+                           sample_clocks=True)
+        fl = f["flushed"]
+        ent = {"workload": f["name"], "params": f["params"], "seqs": f["seqs"], "sum_len": f["sum_len"],
+               "gbps": fl["gbps"], "frac": round(fl["gbps"] / peak, 4), "peak": peak, "peak_source": src,
+               "decode_us": fl["decode_us_median"],
+               "timing": f"median of {flushed_reps} launches, each timed alone with CUDA events after a read "
+                         f"of twice the L2 size",
+               "back_to_back": {"decode_us": f["decode_us"], "gbps": f["gbps"], "launches": reps},
+               "algorithmic_bytes": f["algorithmic_bytes"], "seqs_per_sec": fl["seqs_per_sec"],
+               "clocks": f.get("clocks"), "data": f["data"]}
+        if key in ("3", "3s"):
+            ent["unique_frame_bytes"] = f["unique_frame_bytes"]
+            ent["gbps_unique_frames"] = fl["gbps_unique_frames"]
+            ent["frac_unique_frames"] = fl["frac_unique_frames"]
+            ent["gbps_logical"] = fl["gbps"]
+            ent["cow_copies"] = f["cow_copies"]
+        if "append" in f:
+            ent["append"] = f["append"]
+        out[name] = ent
+    out["prefill"] = prefill_figures(reps, flushed_reps, e2e=False, device_rows=True, sample_clocks=True)
+    return out
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -1231,12 +1439,13 @@ def main():
     ap.add_argument("--batches", type=int, default=16, help="resident copies of the batch decoded in rotation")
     ap.add_argument("--e2e-steps", type=int, default=400)
     ap.add_argument("--cpu-budget", type=float, default=None,
-                    help="seconds of oracle decode time per CPU measurement (12 in the bench line, 8 per worker in --cpu-sweep)")
+                    help="seconds of oracle decode time per CPU measurement (8: one thread, then each of the all-cores workers)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--config", default="1")
     ap.add_argument("--cpu-worker", default=None)
     ap.add_argument("--prefill", action="store_true", help="time pa_prefill on the chunked-prefill batch instead")
+    ap.add_argument("--prefill-dtype", choices=["f16", "bf16"], default="f16")
     ap.add_argument("--prefix", action="store_true", help="time prompt admission with and without prefix caching")
     ap.add_argument("--fork-trees", action="store_true", help="time the beam-search step loop over forked sequences")
     ap.add_argument("--block-sweep", action="store_true", help="decode and prefill throughput against block size")
@@ -1269,7 +1478,7 @@ def main():
         split_layout_bench()
         return
     if args.prefill:
-        prefill_bench()
+        prefill_bench(dtype=args.prefill_dtype)
         return
     if args.sweep is not None:
         keys = SWEEP_KEYS if args.sweep == "all" else tuple(args.sweep.split(","))
