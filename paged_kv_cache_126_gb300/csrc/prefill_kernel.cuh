@@ -22,12 +22,14 @@
 //     copies of a tile are issued by the warp's lanes).  warp 1 (one lane):
 //     tcgen05.mma issuer, fp32 accumulators in TMEM (512 columns: S_0 S_1 O_0 O_1).
 //     S_q = Q_q K_t^T from shared memory; O_q (+)= P_q V_t with P_q read from TMEM,
-//     where the softmax left it over the first 64 columns of S_q.
+//     where the softmax left it over the first 64 columns of S_q (bf16: the weights'
+//     high parts there, their remainders over columns 64..127, two products).
 //     warps 2-9: softmax of both slots, tile by tile (thread = query row = TMEM
 //     lane; warps w and w + 4 share a lane quadrant and split each tile's keys and
 //     the output dimensions in halves, exchanging row maxima and sums through shared
 //     memory): causal mask, online softmax in log2 units (ex2.approx, fp32) with a
-//     lazily raised reference max, P (operand type) back to TMEM, O rescaled in TMEM
+//     lazily raised reference max, P (operand type; bf16 as high part + remainder)
+//     back to TMEM, O rescaled in TMEM
 //     when the reference max moves; normalised rows are written to `out`.
 //   * Every wait is a bounded mbarrier wait; one that gives up sets PA_DEV_TIMEOUT
 //     and makes the block's later waits no-ops; before the TMEM is freed the MMA
@@ -344,6 +346,10 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
+  // bf16 weights keep 8 significant bits: each weight goes to the value product as a
+  // high part and the remainder (two products into the same accumulator), which
+  // leaves 2^-16 of it; fp16 weights (11 bits) go once.
+  constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
@@ -578,6 +584,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t bd = sdesc(sb + kSmV + st * kTile + ks * 2 * 2048, 1024, 2048);
         mma_ts(tmem + kTmemO + q * 128, tmem + kTmemS + q * 128 + ks * 8, bd, id_pv, (!first || ks > 0) ? 1u : 0u);
       }
+      if constexpr (kSplitP) {  // the weights' low parts, over columns 64..127 of S_q
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          const uint64_t bd = sdesc(sb + kSmV + st * kTile + ks * 2 * 2048, 1024, 2048);
+          mma_ts(tmem + kTmemO + q * 128, tmem + kTmemS + q * 128 + 64 + ks * 8, bd, id_pv, 1u);
+        }
+      }
     };
     auto wait = [&](int bar, uint32_t parity) -> bool {
       const bool w = mbar_wait(BAR(bar), parity, abort_flag, a.status);
@@ -763,9 +776,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < 2; ++cc) {
           const uint32_t pcol = s_tmem + 32 * half + 16 * cc;
           uint32_t w[16];
+          uint32_t wl[kSplitP ? 16 : 1];  // low parts (bf16 only)
           if (wmax <= cc * 32) {
 #pragma unroll
             for (int k = 0; k < 16; ++k) w[k] = 0u;
+            if constexpr (kSplitP) {
+#pragma unroll
+              for (int k = 0; k < 16; ++k) wl[k] = 0u;
+            }
           } else {
             const uint32_t(&cur)[32] = sr[cc];
 #pragma unroll
@@ -774,10 +792,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               unf2(ffma2(f2(__uint_as_float(cur[i]), __uint_as_float(cur[i + 1])), sl2x2, nm2), x0, x1);
               const float p0 = ex2(x0), p1 = ex2(x1);
               sum2[(i >> 1) & 1] = fadd2(sum2[(i >> 1) & 1], f2(p0, p1));
-              w[i >> 1] = pack2<T>(p0, p1);
+              const uint32_t hi = pack2<T>(p0, p1);
+              w[i >> 1] = hi;
+              if constexpr (kSplitP) {
+                // p - bf16(p) is exact in fp32; its own bf16 rounding leaves 2^-16 p
+                float r0, r1;
+                unf2(ffma2(f2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u)), f2(-1.f, -1.f),
+                           f2(p0, p1)),
+                     r0, r1);
+                wl[i >> 1] = pack2<T>(r0, r1);
+              }
             }
           }
           tmem_st16(pcol, w);
+          if constexpr (kSplitP) tmem_st16(pcol + 64, wl);
         }
         if (j > 0 && __any_sync(kFull, alpha != 1.f)) {
           // O_q holds the previous tiles (the S commit covered their P V); this half's

@@ -385,19 +385,22 @@ def chunked_prefill(prefix_lens, chunk_lens, *, H=2, D=128, B=16, dtype="f16", s
                     free_order=free_order, ops=ops, seed=seed, final_lens={s: L for s, L in enumerate(final)})
 
 
-def prefill_batch(small: bool = False) -> Workload:
+def prefill_batch(small: bool = False, dtype: str = "f16") -> Workload:
     """Chunked-prefill batch: 16 sequences, cached prefix ~U{0..3072}, a 512-token
-    chunk each (4 sequences, prefix ~U{0..400}, chunks ~U{1..300} when small)."""
+    chunk each (4 sequences, prefix ~U{0..400}, chunks ~U{1..300} when small); fp16
+    unless another 16-bit dtype is asked for (same lengths and seeds)."""
     seed = 1010 + (500 if small else 0)
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 1])))
     if small:
         pre = rng.integers(0, 401, size=4)
         ch = rng.integers(1, 301, size=4)
-        return chunked_prefill(pre, ch, H=2, D=128, B=16, dtype="f16", seed=seed,
-                               name="chunked prefill (small): 4 seqs, prefix~U[0,400], chunk~U[1,300], H=2, f16")
+        return chunked_prefill(pre, ch, H=2, D=128, B=16, dtype=dtype, seed=seed,
+                               name=f"chunked prefill (small): 4 seqs, prefix~U[0,400], chunk~U[1,300], H=2, "
+                                    f"{dtype}")
     pre = rng.integers(0, 3073, size=16)
-    return chunked_prefill(pre, [512] * 16, H=32, D=128, B=16, dtype="f16", seed=seed,
-                           name="chunked prefill: 16 seqs, prefix~U[0,3072], chunk 512, H=32, D=128, B=16, f16")
+    return chunked_prefill(pre, [512] * 16, H=32, D=128, B=16, dtype=dtype, seed=seed,
+                           name=f"chunked prefill: 16 seqs, prefix~U[0,3072], chunk 512, H=32, D=128, B=16, "
+                                f"{dtype}")
 
 
 def beam_search(n_prompts: int, prompt_len: int, width: int, steps: int, *, H=2, D=128, B=16, dtype="f16",
