@@ -138,7 +138,12 @@ int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache,
  * pa_shutdown().  Calls on one stream run in order; calls on different streams
  * use different workspaces.
  * Supported: dtype f32/f16/bf16; D in {64, 128, 256} (f32: {64, 128});
- * 1 <= B <= 256.
+ * 1 <= B <= 256; S <= 65536 (each thread block keeps three int32 per sequence in
+ * shared memory) and max_blocks * B < 2^31, else PA_ERR_UNSUPPORTED.
+ * Bounded waits: every wait inside the kernels gives up after ~2 s, raising
+ * PA_DEV_TIMEOUT (the outputs of that call are then undefined).  Reading the status
+ * with pa_get_device_status marks this device's workspaces for re-zeroing, so later
+ * calls start from clean counters; pa_shutdown() frees them outright.
  */
 int pa_decode(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
               const pa_tensor* block_tables, const pa_tensor* context_lens,
@@ -275,8 +280,10 @@ int pa_decode_static(const pa_tensor* q, const pa_tensor* k_cache, const pa_tens
                      const pa_tensor* block_tables, const pa_tensor* context_lens,
                      float scale, const pa_tensor* out, pa_stream stream);
 
-/* Synchronises `stream`, returns the current device's sticky PA_DEV_* bits in
- * *status_out and clears them. */
+/* Synchronises `stream` (and then the device), returns the current device's sticky
+ * PA_DEV_* bits in *status_out and clears them.  When PA_DEV_TIMEOUT was set, the
+ * scheduler and arrival counters of every workspace of this device are re-zeroed on
+ * their next use (a block that gave up may have left them non-zero). */
 int pa_get_device_status(pa_stream stream, int32_t* status_out);
 
 /* Human-readable name of a return code (static storage). */

@@ -365,6 +365,14 @@ int pa_get_device_status(pa_stream stream, int32_t* status_out) {
   if (cudaMemcpy(&v, g_dev[dev].status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
   if (cudaMemset(g_dev[dev].status, 0, sizeof(v)) != cudaSuccess) return PA_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+  if (v & PA_DEV_TIMEOUT) {
+    // A block that gave up a wait may have left scheduler or arrival counters
+    // non-zero.  Nothing of this library runs on the device now (synchronised above):
+    // mark every workspace of this device unknown, so its next use zeroes them.
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    for (auto& kv : g_ws)
+      if (kv.first.first == dev) kv.second.cnt_bytes = 0;
+  }
   *status_out = v;
   return PA_OK;
 }
@@ -709,17 +717,14 @@ int decode_shared(int dev, const pa_tensor* q, const pa_tensor* k_cache, const p
   g_launches.fetch_add(3);
   return PA_OK;
 }
-}  // namespace
 
-extern "C" {
-
-int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
-                 const pa_tensor* block_tables, const pa_tensor* context_lens, float scale, const pa_tensor* out,
-                 const pa_decode_params* params, pa_stream stream) {
-  const Range range("pa_decode");
+// Argument checks of pa_decode and pa_decode_static; *S_out = number of sequences.
+int check_decode(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                 const pa_tensor* block_tables, const pa_tensor* context_lens, const pa_tensor* out,
+                 int64_t* S_out) {
   PA_TRY(check_cache(k_cache, v_cache));
   const int dt = k_cache->dtype;
-  const int64_t nb = k_cache->shape[0], B = k_cache->shape[1], H = k_cache->shape[2], D = k_cache->shape[3];
+  const int64_t B = k_cache->shape[1], H = k_cache->shape[2], D = k_cache->shape[3];
   PA_TRY(check_rows(q, dt, H, D));
   PA_TRY(check_rows(out, dt, H, D));
   if (!block_tables || !context_lens) return PA_ERR_INVALID;
@@ -732,24 +737,36 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
   if (B > 256) return PA_ERR_UNSUPPORTED;
   if (!(D == 64 || D == 128 || (D == 256 && dt != PA_F32))) return PA_ERR_UNSUPPORTED;
   if (max_blocks * B > INT32_MAX || S > 65536) return PA_ERR_UNSUPPORTED;
-  if (S == 0) return PA_OK;
-  if (max_blocks > 0 && !block_tables->data) return PA_ERR_INVALID;
-  pa_decode_params p;
-  std::memset(&p, 0, sizeof(p));
-  if (params) p = *params;
-  if (p.heads_per_cta < 0 || p.warps_per_head < 0 || p.stages < 0 || p.ctas_per_sm < 0 || p.share_prefix < 0)
-    return PA_ERR_INVALID;
+  if (S > 0 && max_blocks > 0 && !block_tables->data) return PA_ERR_INVALID;
+  *S_out = S;
+  return PA_OK;
+}
 
-  int dev;
-  PA_TRY(current_device(&dev));
-  const int e = elem_bytes(dt);
-  if (p.share_prefix > 0) {
-    const int rc = decode_shared(dev, q, k_cache, v_cache, block_tables, context_lens, scale, out, p, stream);
-    if (rc != kNotApplicable) return rc;
-  }
-
-  // ---- launch configuration -------------------------------------------------------------
+// One decode launch, planned: configuration, kernel arguments (all but the scratch
+// pointers), tensor maps, and the scratch it needs.  The scratch sizes follow the
+// kernel's own partition rule (at most items_max partial results), so every caller
+// that sizes its scratch from a plan gives the kernel enough.
+struct DecodePlan {
   pa::DecodeCfg c;
+  pa::DecodeArgs a;
+  CUtensorMap tk, tv;
+  int64_t items_max = 0;
+  size_t o_bytes = 0;   // split partial outputs, fp32
+  size_t ml_bytes = 0;  // split partial maxima and sums, fp32
+  size_t cnt_need = 0;  // arrival counters, one int32 per (sequence, head), when a context may split
+};
+
+// Plans a checked decode with S > 0 sequences under launch options p (0 fields =
+// automatic).
+int plan_decode(int dev, const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                const pa_tensor* block_tables, const pa_tensor* context_lens, float scale, const pa_tensor* out,
+                const pa_decode_params& p, DecodePlan* pl) {
+  const int dt = k_cache->dtype;
+  const int64_t nb = k_cache->shape[0], B = k_cache->shape[1], H = k_cache->shape[2], D = k_cache->shape[3];
+  const int64_t S = q->shape[0];
+  const int64_t max_blocks = block_tables->shape[1];
+  const int e = elem_bytes(dt);
+  pa::DecodeCfg& c = pl->c;
   c.dtype = dt;
   c.D = static_cast<int>(D);
   // Unrolled full-frame path: 256-byte rows, units of 16 * warps_per_head tokens.
@@ -773,7 +790,6 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
   c.warps_per_head = wph ? wph : 8 / c.heads_per_cta;
   c.fast = fast_rows && R == 16 * c.warps_per_head;
   if (!combo_built(c.heads_per_cta, c.warps_per_head)) return PA_ERR_INVALID;
-  const int64_t stage_bytes = 2 * R * c.heads_per_cta * D * e;
   c.stages = 1;
   const size_t smem_cap = 227 * 1024;
   if (p.stages) {
@@ -797,9 +813,8 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
     if (c.stages == 0) return PA_ERR_UNSUPPORTED;
   }
   if (pa::decode_smem_bytes(c, e, static_cast<int>(R), static_cast<int>(S)) > smem_cap) return PA_ERR_UNSUPPORTED;
-  (void)stage_bytes;
 
-  pa::DecodeArgs a;
+  pa::DecodeArgs& a = pl->a;
   std::memset(&a, 0, sizeof(a));
   a.q = q->data;
   a.out = out->data;
@@ -818,16 +833,15 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
   a.qk_scale_log2 = scale * 1.4426950408889634f;
   a.status = g_dev[dev].status;
 
-  CUtensorMap tk, tv;
-  PA_TRY(make_cache_map(&tk, k_cache->data, dt, nb, B, H, D, c.heads_per_cta, std::min(B, R)));
-  PA_TRY(make_cache_map(&tv, v_cache->data, dt, nb, B, H, D, c.heads_per_cta, std::min(B, R)));
+  PA_TRY(make_cache_map(&pl->tk, k_cache->data, dt, nb, B, H, D, c.heads_per_cta, std::min(B, R)));
+  PA_TRY(make_cache_map(&pl->tv, v_cache->data, dt, nb, B, H, D, c.heads_per_cta, std::min(B, R)));
 
   int occ = 0;
-  if (dispatch_decode(a, c, tk, tv, nullptr, true, &occ) != cudaSuccess || occ <= 0) return PA_ERR_CUDA;
+  if (dispatch_decode(a, c, pl->tk, pl->tv, nullptr, true, &occ) != cudaSuccess || occ <= 0) return PA_ERR_CUDA;
   const int cps = p.ctas_per_sm ? std::min(p.ctas_per_sm, occ) : occ;
   c.grid = g_dev[dev].num_sms * cps;
 
-  // ---- partitioning and workspace --------------------------------------------------------
+  // ---- partitioning: the most partial results the kernel can write --------------------------
   const int64_t Lcap = max_blocks * B;
   int64_t items_max = 0;
   if (p.items_per_cta < 0 || p.generic_only < 0) return PA_ERR_INVALID;
@@ -846,25 +860,54 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
   } else {
     return PA_ERR_INVALID;
   }
-  {
-    const size_t ml_bytes = static_cast<size_t>(items_max) * c.heads_per_cta * 2 * sizeof(float);
-    const size_t o_bytes = static_cast<size_t>(items_max) * c.heads_per_cta * D * sizeof(float);
-    const size_t cnt_need = items_max > 0 ? static_cast<size_t>(S * H) * sizeof(int32_t) : 0;
-    void* ws = nullptr;
-    size_t cnt_bytes = 0;
-    PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), cnt_need, o_bytes + ml_bytes, &ws,
-                     &cnt_bytes));
-    unsigned char* w = static_cast<unsigned char*>(ws);
-    unsigned char* rest = w + kSchedBytes + cnt_bytes;
-    a.sched = reinterpret_cast<int32_t*>(w);
-    a.ws_cnt = reinterpret_cast<int32_t*>(w + kSchedBytes);
-    if (items_max > 0) {
-      a.ws_o = reinterpret_cast<float*>(rest);
-      a.ws_ml = reinterpret_cast<float*>(rest + o_bytes);
-    }
-  }
+  pl->items_max = items_max;
+  pl->ml_bytes = static_cast<size_t>(items_max) * c.heads_per_cta * 2 * sizeof(float);
+  pl->o_bytes = static_cast<size_t>(items_max) * c.heads_per_cta * D * sizeof(float);
+  pl->cnt_need = items_max > 0 ? static_cast<size_t>(S * H) * sizeof(int32_t) : 0;
+  return PA_OK;
+}
 
-  if (dispatch_decode(a, c, tk, tv, static_cast<cudaStream_t>(stream), false, nullptr) != cudaSuccess)
+// Scratch pointers of a planned decode: scheduler counters at `base`, arrival counters
+// after kSchedBytes, partials after the cnt_bytes arrival-counter region.
+void place_scratch(DecodePlan* pl, unsigned char* base, size_t cnt_bytes) {
+  unsigned char* rest = base + kSchedBytes + cnt_bytes;
+  pl->a.sched = reinterpret_cast<int32_t*>(base);
+  pl->a.ws_cnt = reinterpret_cast<int32_t*>(base + kSchedBytes);
+  if (pl->items_max > 0) {
+    pl->a.ws_o = reinterpret_cast<float*>(rest);
+    pl->a.ws_ml = reinterpret_cast<float*>(rest + pl->o_bytes);
+  }
+}
+}  // namespace
+
+extern "C" {
+
+int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
+                 const pa_tensor* block_tables, const pa_tensor* context_lens, float scale, const pa_tensor* out,
+                 const pa_decode_params* params, pa_stream stream) {
+  const Range range("pa_decode");
+  int64_t S = 0;
+  PA_TRY(check_decode(q, k_cache, v_cache, block_tables, context_lens, out, &S));
+  if (S == 0) return PA_OK;
+  pa_decode_params p;
+  std::memset(&p, 0, sizeof(p));
+  if (params) p = *params;
+  if (p.heads_per_cta < 0 || p.warps_per_head < 0 || p.stages < 0 || p.ctas_per_sm < 0 || p.share_prefix < 0)
+    return PA_ERR_INVALID;
+
+  int dev;
+  PA_TRY(current_device(&dev));
+  if (p.share_prefix > 0) {
+    const int rc = decode_shared(dev, q, k_cache, v_cache, block_tables, context_lens, scale, out, p, stream);
+    if (rc != kNotApplicable) return rc;
+  }
+  DecodePlan pl;
+  PA_TRY(plan_decode(dev, q, k_cache, v_cache, block_tables, context_lens, scale, out, p, &pl));
+  void* ws = nullptr;
+  size_t cnt_bytes = 0;
+  PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), pl.cnt_need, pl.o_bytes + pl.ml_bytes, &ws, &cnt_bytes));
+  place_scratch(&pl, static_cast<unsigned char*>(ws), cnt_bytes);
+  if (dispatch_decode(pl.a, pl.c, pl.tk, pl.tv, static_cast<cudaStream_t>(stream), false, nullptr) != cudaSuccess)
     return PA_ERR_CUDA;
   g_launches.fetch_add(1);
   return PA_OK;
@@ -975,116 +1018,26 @@ int fixed_scratch(int dev, unsigned char** out) {
 extern "C" int pa_decode_static(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
                                 const pa_tensor* block_tables, const pa_tensor* context_lens, float scale,
                                 const pa_tensor* out, pa_stream stream) {
-  // Same checks and automatic launch choices as pa_decode.
-  PA_TRY(check_cache(k_cache, v_cache));
-  const int dt = k_cache->dtype;
-  const int64_t nb = k_cache->shape[0], B = k_cache->shape[1], H = k_cache->shape[2], D = k_cache->shape[3];
-  PA_TRY(check_rows(q, dt, H, D));
-  PA_TRY(check_rows(out, dt, H, D));
-  if (!block_tables || !context_lens) return PA_ERR_INVALID;
-  PA_TRY(check_i32(block_tables, 2));
-  PA_TRY(check_i32(context_lens, 1));
-  const int64_t S = q->shape[0];
-  if (out->shape[0] != S || block_tables->shape[0] != S || context_lens->shape[0] != S) return PA_ERR_SHAPE;
-  const int64_t max_blocks = block_tables->shape[1];
-  if (max_blocks < 0 || (S > 1 && block_tables->stride[0] < max_blocks)) return PA_ERR_STRIDE;
-  if (B > 256) return PA_ERR_UNSUPPORTED;
-  if (!(D == 64 || D == 128 || (D == 256 && dt != PA_F32))) return PA_ERR_UNSUPPORTED;
-  if (max_blocks * B > INT32_MAX || S > 65536) return PA_ERR_UNSUPPORTED;
+  // The checks, automatic launch choices and scratch sizing of pa_decode (one plan).
+  int64_t S = 0;
+  PA_TRY(check_decode(q, k_cache, v_cache, block_tables, context_lens, out, &S));
   if (S == 0) return PA_OK;
-  if (max_blocks > 0 && !block_tables->data) return PA_ERR_INVALID;
-
   int dev;
   PA_TRY(current_device(&dev));
   unsigned char* scratch = nullptr;
   PA_TRY(fixed_scratch(dev, &scratch));
-  const int e = elem_bytes(dt);
-
-  pa::DecodeCfg c;
-  c.dtype = dt;
-  c.D = static_cast<int>(D);
-  const bool fast_rows = D * e == 256 && (B & (B - 1)) == 0;
-  const int wph = fast_rows ? (B >= 32 ? 2 : 1) : 0;
-  const int64_t R = wph ? unit_rows(B, wph, fast_rows) : B;
-  c.heads_per_cta = 1;
-  for (int hg : {4, 2}) {
-    if (H % hg == 0 && 2 * R * hg * D * e <= 32768) {
-      c.heads_per_cta = hg;
-      break;
-    }
-  }
-  c.warps_per_head = wph ? wph : 8 / c.heads_per_cta;
-  c.fast = fast_rows && R == 16 * c.warps_per_head;
-  const size_t smem_cap = 227 * 1024;
-  c.stages = 0;
-  for (int st = 8; st >= 3; --st) {
-    c.stages = st;
-    if (pa::decode_smem_bytes(c, e, static_cast<int>(R), static_cast<int>(S)) <= smem_cap / 2 - 1024) break;
-    c.stages = 0;
-  }
-  if (c.stages == 0) {
-    for (int st = 8; st >= 2; --st) {
-      c.stages = st;
-      if (pa::decode_smem_bytes(c, e, static_cast<int>(R), static_cast<int>(S)) <= smem_cap) break;
-      c.stages = 0;
-    }
-  }
-  if (c.stages == 0) return PA_ERR_UNSUPPORTED;
-
-  pa::DecodeArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.q = q->data;
-  a.out = out->data;
-  a.q_row = q->stride[0];
-  a.out_row = out->stride[0];
-  a.block_tables = static_cast<const int32_t*>(block_tables->data);
-  a.bt_row = block_tables->stride[0];
-  a.context_lens = static_cast<const int32_t*>(context_lens->data);
-  a.S = static_cast<int32_t>(S);
-  a.H = static_cast<int32_t>(H);
-  a.B = static_cast<int32_t>(B);
-  a.R = static_cast<int32_t>(R);
-  a.num_blocks = static_cast<int32_t>(nb);
-  a.max_blocks = static_cast<int32_t>(max_blocks);
-  a.G = static_cast<int32_t>(H / c.heads_per_cta);
-  a.qk_scale_log2 = scale * 1.4426950408889634f;
-  a.status = g_dev[dev].status;
-
-  CUtensorMap tk, tv;
-  PA_TRY(make_cache_map(&tk, k_cache->data, dt, nb, B, H, D, c.heads_per_cta, std::min(B, R)));
-  PA_TRY(make_cache_map(&tv, v_cache->data, dt, nb, B, H, D, c.heads_per_cta, std::min(B, R)));
-  int occ = 0;
-  if (dispatch_decode(a, c, tk, tv, nullptr, true, &occ) != cudaSuccess || occ <= 0) return PA_ERR_CUDA;
-  c.grid = g_dev[dev].num_sms * occ;
-
-  // Scratch layout: counters | offsets | split partials, all inside the fixed array.
-  const int64_t Lcap = max_blocks * B;
-  int64_t items_max = 0;
-  if (Lcap == 0) {
-    a.fixed_part = static_cast<int32_t>(B);
-  } else {
-    a.fixed_part = 0;
-    a.whole_first = 1;
-    a.target_items = (3 * c.grid) / 2;
-    a.min_part = round_up(256, B);
-    if (a.min_part < Lcap)
-      items_max = std::min<int64_t>(S * a.G * ((Lcap + a.min_part - 1) / a.min_part), 2 * a.target_items + S * a.G);
-  }
-  const size_t ml_bytes = static_cast<size_t>(items_max) * c.heads_per_cta * 2 * sizeof(float);
-  const size_t o_bytes = static_cast<size_t>(items_max) * c.heads_per_cta * D * sizeof(float);
-  const size_t cnt_bytes = items_max > 0 ? round256(static_cast<size_t>(S * H) * sizeof(int32_t)) : 0;
-  if (kSchedBytes + cnt_bytes + o_bytes + ml_bytes > kFixedScratchBytes) return PA_ERR_SCRATCH_LIMIT;
-  unsigned char* rest = scratch + kSchedBytes + cnt_bytes;
-  a.sched = reinterpret_cast<int32_t*>(scratch);
-  a.ws_cnt = reinterpret_cast<int32_t*>(scratch + kSchedBytes);
-  if (items_max > 0) {
-    a.ws_o = reinterpret_cast<float*>(rest);
-    a.ws_ml = reinterpret_cast<float*>(rest + o_bytes);
-  }
+  pa_decode_params p;
+  std::memset(&p, 0, sizeof(p));
+  DecodePlan pl;
+  PA_TRY(plan_decode(dev, q, k_cache, v_cache, block_tables, context_lens, scale, out, p, &pl));
+  // Scratch layout inside the fixed array: counters | arrival counters | split partials.
+  const size_t cnt_bytes = round256(pl.cnt_need);
+  if (kSchedBytes + cnt_bytes + pl.o_bytes + pl.ml_bytes > kFixedScratchBytes) return PA_ERR_SCRATCH_LIMIT;
+  place_scratch(&pl, scratch, cnt_bytes);
   // The counters must start at zero; the array keeps whatever the last call left.
   if (cudaMemsetAsync(scratch, 0, kSchedBytes + cnt_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PA_ERR_CUDA;
-  if (dispatch_decode(a, c, tk, tv, static_cast<cudaStream_t>(stream), false, nullptr) != cudaSuccess)
+  if (dispatch_decode(pl.a, pl.c, pl.tk, pl.tv, static_cast<cudaStream_t>(stream), false, nullptr) != cudaSuccess)
     return PA_ERR_CUDA;
   g_launches.fetch_add(1);
   return PA_OK;
