@@ -331,6 +331,10 @@ size_t pa::decode_smem_bytes(const DecodeCfg& c, int elem, int R, int S) {
   return lay.total;
 }
 
+static int cache_append(const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* slot_mapping,
+                        const pa_tensor* k_cache, const pa_tensor* v_cache, pa_stream stream,
+                        const pa::AppendArgs* stage);
+
 extern "C" {
 
 const char* pa_strerror(int code) {
@@ -419,6 +423,16 @@ int pa_shutdown(void) {
 
 int pa_cache_append(const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* slot_mapping,
                     const pa_tensor* k_cache, const pa_tensor* v_cache, pa_stream stream) {
+  return cache_append(k_new, v_new, slot_mapping, k_cache, v_cache, stream, nullptr);
+}
+
+}  // extern "C"
+
+// pa_cache_append, optionally with its slots in mapped host memory and a staging copy
+// done by the same launch (stage != nullptr; the step path below).
+static int cache_append(const pa_tensor* k_new, const pa_tensor* v_new, const pa_tensor* slot_mapping,
+                        const pa_tensor* k_cache, const pa_tensor* v_cache, pa_stream stream,
+                        const pa::AppendArgs* stage) {
   const Range range("pa_cache_append");
   PA_TRY(check_cache(k_cache, v_cache));
   const int dt = k_cache->dtype;
@@ -445,12 +459,24 @@ int pa_cache_append(const pa_tensor* k_new, const pa_tensor* v_new, const pa_ten
   a.row_bytes = H * D * e;
   a.num_slots = k_cache->shape[0] * k_cache->shape[1];
   a.T = static_cast<int32_t>(T);
+  a.slots_host = 0;
   a.status = g_dev[dev].status;
+  a.stage_src = nullptr;
+  a.stage_dst = nullptr;
+  a.stage_vecs = 0;
+  if (stage) {
+    a.slots_host = stage->slots_host;
+    a.stage_src = stage->stage_src;
+    a.stage_dst = stage->stage_dst;
+    a.stage_vecs = stage->stage_vecs;
+  }
   if (pa::launch_cache_append(a, g_dev[dev].num_sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PA_ERR_CUDA;
   g_launches.fetch_add(1);
   return PA_OK;
 }
+
+extern "C" {
 
 // ---- the split cache layout ---------------------------------------------------------------
 // k_cache viewed as [nb, H, D/x, B*x], v_cache as [nb, H, D, B], both contiguous, fp16/bf16.
@@ -1055,6 +1081,7 @@ constexpr int kStepRing = 4;
 
 struct StepStage {
   int32_t* host[kStepRing] = {};
+  int32_t* host_dev[kStepRing] = {};  // the same pinned memory, as the device addresses it
   int32_t* dev[kStepRing] = {};
   cudaEvent_t done[kStepRing] = {};
   bool recorded[kStepRing] = {};
@@ -1070,6 +1097,7 @@ void free_stage(StepStage& s) {
     if (s.dev[i]) cudaFree(s.dev[i]);
     if (s.done[i]) cudaEventDestroy(s.done[i]);
     s.host[i] = nullptr;
+    s.host_dev[i] = nullptr;
     s.dev[i] = nullptr;
     s.done[i] = nullptr;
     s.recorded[i] = false;
@@ -1091,10 +1119,12 @@ int stage_slot(int dev, cudaStream_t stream, size_t need, StepStage** out) {
   if (s.cap < need) {
     if (s.cap && cudaStreamSynchronize(stream) != cudaSuccess) return -1;
     free_stage(s);
-    const size_t cap = std::max(need, static_cast<size_t>(1) << 14);
+    // whole 16-byte vectors: the append's staging copy moves the block in uint4 units
+    const size_t cap = (std::max(need, static_cast<size_t>(1) << 14) + 3) & ~static_cast<size_t>(3);
     for (int i = 0; i < kStepRing; ++i) {
-      if (cudaHostAlloc(reinterpret_cast<void**>(&s.host[i]), cap * sizeof(int32_t), cudaHostAllocDefault) !=
+      if (cudaHostAlloc(reinterpret_cast<void**>(&s.host[i]), cap * sizeof(int32_t), cudaHostAllocMapped) !=
               cudaSuccess ||
+          cudaHostGetDevicePointer(reinterpret_cast<void**>(&s.host_dev[i]), s.host[i], 0) != cudaSuccess ||
           cudaMalloc(reinterpret_cast<void**>(&s.dev[i]), cap * sizeof(int32_t)) != cudaSuccess ||
           cudaEventCreateWithFlags(&s.done[i], cudaEventDisableTiming) != cudaSuccess) {
         free_stage(s);
@@ -1163,19 +1193,37 @@ extern "C" int pa_step_decode(pa_bm* bm, const int64_t* seq_ids, int32_t n, int3
     PA_TRY(pa_bm_step(bm, seq_ids, n, h, h + n, &nc));
     PA_TRY(pa_bm_block_tables(bm, seq_ids, n, max_blocks, h + 4 * n, h + 3 * n));
   }
-  if (cudaMemcpyAsync(d, h, need * sizeof(int32_t), cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaEventRecord(s->done[i], st) != cudaSuccess)
-    return PA_ERR_CUDA;
-  s->recorded[i] = true;
   if (n_copies_out) *n_copies_out = nc;
   if (lens_out) std::memcpy(lens_out, h + 3 * n, sizeof(int32_t) * n);
-  // copy-on-write frame copies, the new rows, then the decode
   if (nc) {
+    // copy-on-write frame copies first: one upload of the staged block, the copies,
+    // then the new rows with their slots from device memory
+    if (cudaMemcpyAsync(d, h, need * sizeof(int32_t), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaEventRecord(s->done[i], st) != cudaSuccess)
+      return PA_ERR_CUDA;
+    s->recorded[i] = true;
     const pa_tensor pairs = i32_view(d + n, nc, 2);
     PA_TRY(pa_copy_blocks(k_cache, v_cache, &pairs, stream));
+    const pa_tensor slots = i32_view(d, n, 0);
+    PA_TRY(pa_cache_append(k_new, v_new, &slots, k_cache, v_cache, stream));
+  } else {
+    // no copies: the append reads its slots from the pinned block itself and copies the
+    // block (lengths and tables for the decode) to device memory in the same launch, so
+    // no copy-engine transfer sits between the previous step's decode and this append.
+    // The device slot it writes was last read by the decode three steps back, which has
+    // finished once any kernel of the previous step runs (each step's kernels wait for
+    // the one before them).
+    pa::AppendArgs stage;
+    std::memset(&stage, 0, sizeof(stage));
+    stage.slots_host = 1;
+    stage.stage_src = reinterpret_cast<const uint4*>(s->host_dev[i]);
+    stage.stage_dst = reinterpret_cast<uint4*>(d);
+    stage.stage_vecs = static_cast<int64_t>((need * sizeof(int32_t) + 15) / 16);
+    const pa_tensor slots = i32_view(s->host_dev[i], n, 0);
+    PA_TRY(cache_append(k_new, v_new, &slots, k_cache, v_cache, stream, &stage));
+    if (cudaEventRecord(s->done[i], st) != cudaSuccess) return PA_ERR_CUDA;
+    s->recorded[i] = true;
   }
-  const pa_tensor slots = i32_view(d, n, 0);
-  PA_TRY(pa_cache_append(k_new, v_new, &slots, k_cache, v_cache, stream));
   pa_decode_params p;
   const pa_decode_params* pp = params;
   if (!params && auto_share) {

@@ -24,15 +24,35 @@ namespace {
 
 constexpr int kVecs = 4;  // 16-byte vectors per thread and cache held before storing
 
+// Uncached loads from mapped host memory (the host rewrites it between launches).
+__device__ __forceinline__ int32_t ld_host(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.global.cv.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 ld_host(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.cv.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p)
+               : "memory");
+  return v;
+}
+
 __global__ void __launch_bounds__(256) cache_append_kernel(const AppendArgs a) {
   // Launched with programmatic stream serialisation: let the next kernel start its
   // set-up now, and wait for the previous kernel's writes before reading inputs.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // The staging copy reads host memory the host wrote before this launch and writes a
+  // buffer no running kernel reads (the caller's contract): it overlaps the wait.
+  if (a.stage_vecs > 0) {
+    const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < a.stage_vecs; i += step)
+      a.stage_dst[i] = ld_host(a.stage_src + i);
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t nvec = a.row_bytes >> 4;
   const int64_t stride = static_cast<int64_t>(blockDim.x);
   for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
-    const int32_t slot = __ldg(a.slots + t);
+    const int32_t slot = a.slots_host ? ld_host(a.slots + t) : __ldg(a.slots + t);
     if (slot < 0) continue;  // padding
     if (slot >= a.num_slots) {
       if (threadIdx.x == 0) atomicOr(a.status, kDevBadSlot);

@@ -54,13 +54,21 @@ struct AppendArgs {
   const unsigned char* k_new;   // [T, row_bytes] with row pitch k_pitch
   const unsigned char* v_new;
   int64_t k_pitch, v_pitch;     // bytes between token rows
-  const int32_t* slots;         // [T]
+  const int32_t* slots;         // [T]; device memory, or mapped pinned host memory (slots_host)
   unsigned char* k_cache;       // [num_slots, row_bytes]
   unsigned char* v_cache;
   int64_t row_bytes;            // H * D * elem (multiple of 16)
   int64_t num_slots;            // num_blocks * B
   int32_t T;
+  int32_t slots_host;           // 1: slots are read from host memory, uncached
   int32_t* status;
+  // Optional staging copy done by the same launch (stage_vecs > 0): stage_vecs 16-byte
+  // vectors from mapped pinned host memory to device memory.  It runs before the wait
+  // on the previous kernel, so stage_dst must not be read by any kernel that can still
+  // be running when this one starts.
+  const uint4* stage_src;
+  uint4* stage_dst;
+  int64_t stage_vecs;
 };
 cudaError_t launch_cache_append(const AppendArgs& a, int num_sms, cudaStream_t stream);
 
