@@ -632,8 +632,15 @@ def _workload_engine(key, dev, device_rows):
     import paged_kv_cache_126_gb300 as pa
     import workloads
 
-    cfg = {"0": 0, "1": 1, "1x": "1x", "2": 2, "2n": 2, "3": 3, "3c": 3, "3s": 3, "4": 4}[key]
+    cfg = {"0": 0, "1": 1, "1x": "1x", "2": 2, "2n": 2, "3": 3, "3c": 3, "3s": 3, "4": 4, "4d": 4}[key]
     w = workloads.build(cfg)
+    if key == "4d":
+        # the serving mix scaled down for a profiler capture: its first 48 of 256 sequences
+        # (same length law, 40 heads, bf16 N(0, 0.5), prefill L-1 + one appended token)
+        L = [w.final_lens[s] for s in range(48)]
+        w = workloads.custom(L, H=w.num_heads, D=w.head_dim, B=w.block_size, dtype=w.dtype, sigma=w.sigma,
+                             seed=w.seed, name="serving mix, first 48 of 256 seqs: L~logU[16,8192], H=40, D=128, "
+                                               "B=16, bf16")
     if key == "3c":
         L = [w.final_lens[s] for s in range(len(w.final_lens))]
         w = workloads.custom(L, H=w.num_heads, D=w.head_dim, B=w.block_size, dtype=w.dtype, seed=w.seed,
@@ -1451,7 +1458,8 @@ def main():
     ap.add_argument("--block-sweep", action="store_true", help="decode and prefill throughput against block size")
     ap.add_argument("--split-layout", action="store_true", help="decode throughput of the two cache layouts")
     ap.add_argument("--sweep", default=None, metavar="KEYS",
-                    help="time pa_decode on each listed workload instead (comma list of 0,1,1x,2,2n,3,3c,3s,4 or 'all')")
+                    help="time pa_decode on each listed workload instead (comma list of 0,1,1x,2,2n,3,3c,3s,4,4d "
+                         "or 'all'; 4d = the serving mix's first 48 sequences)")
     ap.add_argument("--cpu-seed-shift", type=int, default=0)
     ap.add_argument("--cpu-sweep", action="store_true",
                     help="time the oracle's decode on the host per workload, one thread and all affine cores")
