@@ -60,6 +60,13 @@ def replay_fused(pa, w, native=True, params=None):
 
 CASES = [
     ("decode batch", lambda: workloads.build(1, small=True)),
+    # many steps without copy-on-write: the append reads its slots from the pinned ring and
+    # carries the tables to the device itself; the ring (4 slots) wraps several times and
+    # the batch changes size every other step
+    ("decode steps", lambda: workloads.decode_steps([1, 15, 16, 17, 200, 31, 600, 2], 14, H=4, B=16,
+                                                    dtype="f16", seed=74, drop_every=3)),
+    ("decode steps bf16 B=8", lambda: workloads.decode_steps([7, 8, 9, 100, 64], 11, H=2, B=8, dtype="bf16",
+                                                             seed=75, drop_every=2)),
     ("beam search wide", lambda: workloads.beam_search(2, 150, 8, 16, H=4, B=16, dtype="f16", seed=73)),
     ("beam search", lambda: workloads.beam_search(3, 200, 4, 20, H=4, B=16, dtype="f16", seed=71)),
     ("beam search bf16 B=8", lambda: workloads.beam_search(2, 100, 8, 12, H=4, B=8, dtype="bf16", seed=72)),

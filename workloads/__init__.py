@@ -13,6 +13,7 @@ from .gen import (  # noqa: F401
     build,
     chunked_prefill,
     custom,
+    decode_steps,
     mcts_tree,
     prefill_batch,
     prefix_ids,

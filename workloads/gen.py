@@ -558,6 +558,32 @@ def shared_prefix(n_requests: int, system_len: int, user_lens, *, H=2, D=128, B=
                     free_order=free_order, ops=ops, seed=seed, final_lens=final)
 
 
+def decode_steps(prompt_lens, steps: int, *, H=2, D=128, B=16, dtype="f16", sigma=1.0, seed=9,
+                 drop_every: int = 0, name=None) -> Workload:
+    """Prompts, then ``steps`` decode steps, each followed by attention over the batch.
+    With ``drop_every`` > 0, every ``drop_every``-th sequence sits out every other step,
+    so the batch (and its size) changes from step to step."""
+    prompt_lens = [int(x) for x in prompt_lens]
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0])))
+    final = [L + steps for L in prompt_lens]
+    nb = _pool_size(final, B)
+    free_order = rng.permutation(nb).astype(np.int32)
+    ops = [("add", s, L) for s, L in enumerate(prompt_lens)]
+    counts = [0] * len(prompt_lens)
+    for k in range(steps):
+        seqs = tuple(s for s in range(len(prompt_lens))
+                     if not (drop_every and s % drop_every == 0 and k % 2 == 1))
+        for s in seqs:
+            counts[s] += 1
+        ops.append(("step", seqs))
+        ops.append(("attend", seqs))
+    return Workload(name=name or f"decode steps: {len(prompt_lens)} seqs x {steps} steps, H={H}, D={D}, B={B}, "
+                                 f"{dtype}",
+                    num_heads=H, head_dim=D, block_size=B, dtype=dtype, sigma=sigma, num_blocks=nb,
+                    free_order=free_order, ops=ops, seed=seed,
+                    final_lens={s: L + c for s, (L, c) in enumerate(zip(prompt_lens, counts))})
+
+
 def custom(lengths, *, H=2, D=128, B=16, dtype="f16", sigma=1.0, seed=7, shuffle=True,
            pool=None, free_order=None, name=None) -> Workload:
     """Decode batch with explicit final context lengths (edge cases, sweeps)."""
