@@ -397,12 +397,15 @@ int pa_bm_fork_many(pa_bm* bm, const int64_t* parent_ids, const int64_t* child_i
 int pa_bm_free_many(pa_bm* bm, const int64_t* seq_ids, int32_t n);
 
 /* One decode step of a batch with the host side done natively: pa_bm_step for
- * seq_ids[0..n) (one token each, copy-on-write as pa_bm_append), the batch's block
- * tables [n, max_blocks] and lengths, one asynchronous upload from a library-owned
- * pinned staging ring (per device and stream, four slots, each reused only after the
- * copy that last read it has run), then pa_copy_blocks (when a shared tail was
+ * seq_ids[0..n) (one token each, copy-on-write as pa_bm_append), the batch's slots,
+ * block tables [n, max_blocks] and lengths staged in a library-owned ring of mapped
+ * pinned host memory (per device and stream, four slots, each reused only after the
+ * kernel that last read it has run), then pa_copy_blocks (when a shared tail was
  * written), pa_cache_append of k_new / v_new [n, H, D] (device) at the step's slots,
- * and pa_decode_ex of q [n, H, D] into out, all on `stream`.  params may be NULL:
+ * and pa_decode_ex of q [n, H, D] into out, all on `stream`.  On a step without
+ * frame copies the append reads its slots from the ring directly and copies the
+ * tables and lengths to device memory in the same launch; a step with copies uploads
+ * the staged block with one asynchronous copy first.  params may be NULL:
  * automatic launch options, with share_prefix = 1 when auto_share is set and two
  * neighbouring sequences of the batch start on the same frame.  *n_copies_out (may
  * be NULL) receives the number of frame copies; lens_out (host, n entries, may be
