@@ -129,7 +129,13 @@ struct pa_bm {
   int32_t block_size = 0;
   FreeList free_list;
   std::vector<int32_t> refs;
-  std::unordered_map<int64_t, Seq> seqs;
+  using SeqMap = std::unordered_map<int64_t, Seq>;
+  SeqMap seqs;
+  // Map nodes of freed sequences, kept with their vectors' capacity and reused by forks:
+  // a beam-search step that forks and frees as many sequences as it keeps then
+  // allocates nothing.
+  static constexpr size_t kSpareMax = 4096;
+  std::vector<SeqMap::node_type> spare;
   // prefix cache
   std::unordered_map<BlockKey, int64_t, BlockKeyHash> node_of_key;
   std::unordered_map<int64_t, Node> nodes;
@@ -175,9 +181,37 @@ struct pa_bm {
   // frame (each gains a reference) and inherits the length.  The child is inserted before
   // any reference count moves, so a failed allocation leaves the manager as it was.
   void fork_checked(const Seq& parent, int64_t child_id) {
-    Seq child = parent;  // copy of the table and the length (the insert may rehash: copy first)
-    const auto ins = seqs.emplace(child_id, std::move(child));
-    for (int32_t f : ins.first->second.frames) refs[f] += 1;
+    SeqMap::iterator at;
+    if (!spare.empty()) {
+      // a recycled node: copying into vectors that keep their capacity allocates nothing
+      SeqMap::node_type nh = std::move(spare.back());
+      spare.pop_back();
+      nh.key() = child_id;
+      Seq& c = nh.mapped();
+      c.frames.assign(parent.frames.begin(), parent.frames.end());
+      c.len = parent.len;
+      c.tracked = parent.tracked;
+      c.tokens.assign(parent.tokens.begin(), parent.tokens.end());
+      c.nodes.assign(parent.nodes.begin(), parent.nodes.end());
+      at = seqs.insert(std::move(nh)).position;
+    } else {
+      Seq child = parent;  // copy of the table and the length (the insert may rehash: copy first)
+      at = seqs.emplace(child_id, std::move(child)).first;
+    }
+    for (int32_t f : at->second.frames) refs[f] += 1;
+  }
+
+  // Removes a live sequence's map entry, keeping its node for a later fork.
+  void erase_seq(SeqMap::iterator it) {
+    if (spare.size() >= kSpareMax) {
+      seqs.erase(it);
+      return;
+    }
+    SeqMap::node_type nh = seqs.extract(it);
+    try {
+      spare.push_back(std::move(nh));
+    } catch (...) {  // no room to keep it: the node handle frees it
+    }
   }
 
   void drop_ref(int32_t f) {
@@ -348,6 +382,7 @@ int pa_bm_create(int32_t num_blocks, int32_t block_size, const int32_t* free_ord
     // at most one registered block per frame: the prefix-cache maps never rehash
     bm->node_of_key.reserve(static_cast<size_t>(num_blocks));
     bm->nodes.reserve(static_cast<size_t>(num_blocks));
+    bm->spare.reserve(pa_bm::kSpareMax);
     bm->free_list.reset(num_blocks);
     if (free_order) {
       std::vector<uint8_t> seen(num_blocks, 0);
@@ -517,7 +552,7 @@ int pa_bm_free(pa_bm* bm, int64_t seq_id) {
     auto it = bm->seqs.find(seq_id);
     if (it == bm->seqs.end()) return PA_WARN_DOUBLE_FREE;
     for (int32_t f : it->second.frames) bm->drop_ref(f);
-    bm->seqs.erase(it);
+    bm->erase_seq(it);
     return PA_OK;
   });
 }
