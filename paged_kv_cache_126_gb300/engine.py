@@ -1,17 +1,20 @@
 """PagedKVEngine: one device's paged K/V caches driven by libpa.
 
 The engine owns the two caches [num_blocks, B, H, D] (torch device memory) and a
-libpa host block manager.  A decode step is
+libpa host block manager.  A decode step (``decode_step``, one pa_step_decode call) is
 
     host:   pa_bm_step (slots + copy-on-write pairs, in batch order)
             pa_bm_block_tables (tables + context lengths)
-            -> one pinned staging buffer -> one async host-to-device copy
-    device: pa_copy_blocks (only if a shared tail was written)
-            pa_cache_append (the step's new K/V rows)
-            pa_decode (+ its merge kernel when a context is split)
+            -> one slot of a mapped pinned staging ring
+    device: pa_copy_blocks (only if a shared tail was written; the staged block is
+            then uploaded first with one async copy)
+            pa_cache_append (the step's new K/V rows; without copies it reads its slots
+            from the ring and carries the tables to device memory itself)
+            pa_decode (split contexts merged inside the kernel)
 
-all on one stream.  Staging buffers form a ring guarded by CUDA events so the
-host can prepare step k+1 while the device still runs step k.
+all on one stream.  Staging slots form a ring guarded by CUDA events so the host can
+prepare step k+1 while the device still runs step k.  The separate operations (step,
+attend, ...) stage their small int32 arrays through the engine's own pinned ring.
 """
 
 from __future__ import annotations
@@ -271,10 +274,11 @@ class PagedKVEngine:
         return out
 
     def decode_step(self, seqs, k_rows, v_rows, q, scale: float, out=None, params=None, events=None):
-        """append + attend with one staged upload: the whole hot path of one step.
+        """append + attend: the whole hot path of one step.
 
         Without ``events`` the whole host side runs in libpa (pa_step_decode: block-manager
-        step, tables, one staged upload, copies, append, decode).  ``events`` (start, end):
+        step, tables staged in mapped pinned memory, copies, an append that also carries the
+        staged tables to the device, decode).  ``events`` (start, end):
         CUDA events recorded on the engine stream around the pa_decode call (decode kernel +
         merge), for timing; the step then runs through the separate calls.
         Returns (out, number of copy-on-write pairs, context lengths).
