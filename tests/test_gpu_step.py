@@ -67,6 +67,11 @@ CASES = [
                                                     dtype="f16", seed=74, drop_every=3)),
     ("decode steps bf16 B=8", lambda: workloads.decode_steps([7, 8, 9, 100, 64], 11, H=2, B=8, dtype="bf16",
                                                              seed=75, drop_every=2)),
+    # 4 sequences for three steps, then all 420: the staged block outgrows the ring's
+    # 16384 int32 per slot (420 x (4 + 46 table entries)) and the ring is reallocated
+    # between steps
+    ("decode steps, ring growth", lambda: workloads.decode_steps(
+        [700 + (s * 37) % 31 for s in range(420)], 6, H=2, D=64, B=16, dtype="f16", seed=76, small_first=4)),
     ("beam search wide", lambda: workloads.beam_search(2, 150, 8, 16, H=4, B=16, dtype="f16", seed=73)),
     ("beam search", lambda: workloads.beam_search(3, 200, 4, 20, H=4, B=16, dtype="f16", seed=71)),
     ("beam search bf16 B=8", lambda: workloads.beam_search(2, 100, 8, 12, H=4, B=8, dtype="bf16", seed=72)),

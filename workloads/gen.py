@@ -559,10 +559,11 @@ def shared_prefix(n_requests: int, system_len: int, user_lens, *, H=2, D=128, B=
 
 
 def decode_steps(prompt_lens, steps: int, *, H=2, D=128, B=16, dtype="f16", sigma=1.0, seed=9,
-                 drop_every: int = 0, name=None) -> Workload:
+                 drop_every: int = 0, small_first: int = 0, name=None) -> Workload:
     """Prompts, then ``steps`` decode steps, each followed by attention over the batch.
     With ``drop_every`` > 0, every ``drop_every``-th sequence sits out every other step,
-    so the batch (and its size) changes from step to step."""
+    so the batch (and its size) changes from step to step.  With ``small_first`` > 0,
+    only the first ``small_first`` sequences take part in the first half of the steps."""
     prompt_lens = [int(x) for x in prompt_lens]
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0])))
     final = [L + steps for L in prompt_lens]
@@ -572,7 +573,8 @@ def decode_steps(prompt_lens, steps: int, *, H=2, D=128, B=16, dtype="f16", sigm
     counts = [0] * len(prompt_lens)
     for k in range(steps):
         seqs = tuple(s for s in range(len(prompt_lens))
-                     if not (drop_every and s % drop_every == 0 and k % 2 == 1))
+                     if not (drop_every and s % drop_every == 0 and k % 2 == 1)
+                     and not (small_first and k < steps // 2 and s >= small_first))
         for s in seqs:
             counts[s] += 1
         ops.append(("step", seqs))
