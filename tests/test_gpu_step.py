@@ -67,6 +67,8 @@ CASES = [
                                                     dtype="f16", seed=74, drop_every=3)),
     ("decode steps bf16 B=8", lambda: workloads.decode_steps([7, 8, 9, 100, 64], 11, H=2, B=8, dtype="bf16",
                                                              seed=75, drop_every=2)),
+    ("decode steps f32 D=64 B=10", lambda: workloads.decode_steps([3, 10, 11, 95, 40], 9, H=3, D=64, B=10,
+                                                                 dtype="f32", seed=77, drop_every=2)),
     # 4 sequences for three steps, then all 420: the staged block outgrows the ring's
     # 16384 int32 per slot (420 x (4 + 46 table entries)) and the ring is reallocated
     # between steps

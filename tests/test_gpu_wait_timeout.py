@@ -25,9 +25,13 @@ def test_wait_gives_up_reports_timeout_and_context_survives(pa):
     assert second_cycles < 1_000_000          # the aborting block's later wait returns at once
     assert pa.pa_get_device_status() & pa.PA_DEV_TIMEOUT
     assert pa.pa_get_device_status() == 0     # reading clears the sticky bits
-    # the context is usable: a decode afterwards matches the oracle
+    # the context is usable: a decode afterwards matches the oracle, with the automatic
+    # launch options and with every context split into partitions (the arrival counters
+    # of the workspace, re-zeroed after a timeout was read, decide which partition merges)
     w = workloads.build(1, small=True)
     _, outs, ref = run_both(pa, w)
+    check_outputs(w, outs, ref)
+    _, outs, ref = run_both(pa, w, params={"partition_tokens": 64})
     check_outputs(w, outs, ref)
     torch.cuda.synchronize()
     assert pa.pa_get_device_status() == 0
