@@ -48,11 +48,15 @@ __global__ void __launch_bounds__(256) cache_append_kernel(const AppendArgs a) {
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < a.stage_vecs; i += step)
       a.stage_dst[i] = ld_host(a.stage_src + i);
   }
+  // Slots in host memory were written before this launch: the block's first one is read
+  // before the wait too, so its host round trip overlaps the previous kernel's tail.
+  const int32_t first_slot = a.slots_host && blockIdx.x < a.T ? ld_host(a.slots + blockIdx.x) : 0;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t nvec = a.row_bytes >> 4;
   const int64_t stride = static_cast<int64_t>(blockDim.x);
   for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
-    const int32_t slot = a.slots_host ? ld_host(a.slots + t) : __ldg(a.slots + t);
+    const int32_t slot = a.slots_host ? (t == static_cast<int>(blockIdx.x) ? first_slot : ld_host(a.slots + t))
+                                      : __ldg(a.slots + t);
     if (slot < 0) continue;  // padding
     if (slot >= a.num_slots) {
       if (threadIdx.x == 0) atomicOr(a.status, kDevBadSlot);
