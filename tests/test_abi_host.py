@@ -17,7 +17,7 @@ import subprocess
 import numpy as np
 import pytest
 
-from oracle import DOUBLE_FREE, OracleBlockManager, OutOfBlocks, SequenceExists, UnknownSequence
+from oracle import DOUBLE_FREE, OracleBlockManager, OutOfBlocks
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 

@@ -7,7 +7,6 @@ length is the max over ranks and the work is the sum over ranks.  No GPU.
 import os
 import socket
 
-import pytest
 import torch.multiprocessing as mp
 
 

@@ -6,10 +6,7 @@ reference drop) and checks that at least one pin test then fails.  The patches
 touch only the oracle, on the CPU.
 """
 
-from collections import deque
-
 import numpy as np
-import pytest
 
 import oracle.attention as att
 import oracle.block_manager as bmmod
