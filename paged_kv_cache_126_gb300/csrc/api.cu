@@ -581,6 +581,9 @@ int pa_decode_split(const pa_tensor* q, const pa_tensor* k_cache, const pa_tenso
   a.max_blocks = static_cast<int32_t>(max_blocks);
   a.P = static_cast<int32_t>(P);
   a.NP = static_cast<int32_t>(NP);
+  // whole sequences as items: hand them out longest first (the order costs 4 bytes of
+  // shared memory per sequence, kept small enough to leave two blocks per SM)
+  a.longest_first = NP == 1 && S <= 2048 ? 1 : 0;
   a.qk_scale_log2 = scale * 1.4426950408889634f;
   a.status = g_dev[dev].status;
   const size_t items = static_cast<size_t>(S * groups * NP);

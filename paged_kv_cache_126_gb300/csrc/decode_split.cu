@@ -59,7 +59,8 @@ struct Geo {
   static constexpr int NST = (96 * 1024 / STAGE) < 2 ? 2 : ((96 * 1024 / STAGE) > 6 ? 6 : 96 * 1024 / STAGE);
   static constexpr uint32_t BAR_OFF = NST * STAGE;       // [NST full][NST empty][2 item full][2 item empty]
   static constexpr uint32_t MISC_OFF = BAR_OFF + 8 * (2 * NST + 4);
-  static constexpr uint32_t SMEM = MISC_OFF + 4 * (4 + NST) + 128;
+  static constexpr uint32_t ORDER_OFF = (MISC_OFF + 4 * (4 + NST) + 15) & ~15u;  // [64] histogram, [1], [S] order
+  static constexpr uint32_t SMEM = ORDER_OFF + 128;  // + 4 * (65 + S) when the items are ordered
   static_assert(PH * B == 32 && STEPS * PH == NC, "B must divide 32 and the chunk count");
   static_assert(C * RPI == 32 && NR * RPI == D, "V rows must tile the warp");
 };
@@ -146,13 +147,14 @@ __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) { re
 struct Item {
   int s, g, p, t0, t1;  // tokens t0 .. t1-1 of sequence s, head group g, partition p
 };
-__device__ __forceinline__ Item locate(const SplitArgs& a, int item) {
+// order: sequence of each rank (longest first) when a.longest_first, else unused
+__device__ __forceinline__ Item locate(const SplitArgs& a, const int32_t* order, int item) {
   Item it;
   const int groups = a.H / kHG;
   it.p = item % a.NP;
   const int sg = item / a.NP;
   it.g = sg % groups;
-  it.s = sg / groups;
+  it.s = a.longest_first ? order[sg / groups] : sg / groups;
   const int L = a.context_lens[it.s];  // lengths past the block table are cut by the callers
   it.t0 = it.p * a.P;
   it.t1 = min(max(L, 0), it.t0 + a.P);
@@ -187,9 +189,59 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  const int64_t row_cap = static_cast<int64_t>(a.max_blocks) * B;
+  int32_t* hist = reinterpret_cast<int32_t*>(smem + G::ORDER_OFF);  // [64]: counts, then cursors
+  int32_t* longest = hist + 64;                                     // [1]
+  int32_t* order = hist + 65;                                       // [S]
+  if (a.longest_first) {
+    // Whole-sequence items in decreasing length: a stable counting sort over 32 length
+    // buckets, the same in every block, so item ids agree.  Lengths outside the table
+    // count as empty.
+    auto len_of = [&](int s) {
+      const int L = a.context_lens[s];
+      return (L < 0 || L > row_cap) ? 0 : L;
+    };
+    if (tid < 64) hist[tid] = 0;
+    if (tid == 0) *longest = 0;
+    __syncthreads();
+    for (int s = tid; s < a.S; s += blockDim.x) atomicMax(longest, len_of(s));
+    __syncthreads();
+    const int lmax = *longest;
+    if (warp == 0) {
+      auto bucket_of = [&](int s) {
+        return min(31, static_cast<int>((static_cast<long long>(len_of(s)) * 32) / (lmax + 1)));
+      };
+      const unsigned lt = (1u << lane) - 1u;
+      for (int base = 0; base < a.S; base += 32) {
+        const int s = base + lane;
+        const int b = s < a.S ? bucket_of(s) : -1;
+        const unsigned same = __match_any_sync(kFull, b);
+        if (b >= 0 && (same & lt) == 0) hist[b] += __popc(same);
+        __syncwarp();
+      }
+      // cursor of bucket b = sequences in buckets above b
+      const int cnt = hist[31 - lane];
+      int v = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += n;
+      }
+      hist[32 + (31 - lane)] = v - cnt;
+      __syncwarp();
+      for (int base = 0; base < a.S; base += 32) {
+        const int s = base + lane;
+        const int b = s < a.S ? bucket_of(s) : -1;
+        const unsigned same = __match_any_sync(kFull, b);
+        if (b >= 0) order[hist[32 + b] + __popc(same & lt)] = s;
+        __syncwarp();
+        if (b >= 0 && (same & lt) == 0) hist[32 + b] += __popc(same);
+        __syncwarp();
+      }
+    }
+  }
   __syncthreads();
   const int total = a.S * (a.H / kHG) * a.NP;
-  const int64_t row_cap = static_cast<int64_t>(a.max_blocks) * B;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -205,7 +257,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
         }
         ++ni;
         if (done) break;
-        const Item it = locate(a, item);
+        const Item it = locate(a, order, item);
         const int L = a.context_lens[it.s];
         if ((L < 0 || L > row_cap) && it.g == 0 && it.p == 0) atomicOr(a.status, kDevBadLen);
         const int t1 = (L < 0 || L > row_cap) ? 0 : it.t1;
@@ -268,7 +320,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
     if (lane == 0) mbar_arrive(IEMPTY(sl));
     ++ni;
     if (item < 0) break;
-    const Item it = locate(a, item);
+    const Item it = locate(a, order, item);
     const int L = a.context_lens[it.s];
     const int t1 = (L < 0 || L > row_cap) ? 0 : it.t1;
     const int h = it.g * kHG + hh;
@@ -358,7 +410,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
         for (int j = 0; j < G::NR; ++j) orow[vr0 + G::RPI * j] = from_float<T>(o[j] * inv);
       }
     } else {
-      const int64_t slot = static_cast<int64_t>(item) * kHG + hh;
+      // partial slots are keyed by (sequence, head group, partition), which the merge reads
+      const int64_t slot = (static_cast<int64_t>(it.s * (a.H / kHG) + it.g) * a.NP + it.p) * kHG + hh;
       if (vc == 0) {
 #pragma unroll
         for (int j = 0; j < G::NR; ++j) a.ws_o[slot * D + vr0 + G::RPI * j] = ok ? o[j] : 0.f;
@@ -430,11 +483,12 @@ cudaError_t launch(const SplitArgs& a, int num_sms, cudaStream_t stream) {
   using G = Geo<T, D, B>;
   auto kern = decode_split_kernel<T, D, B>;
   int per_sm = 0;
-  cudaError_t e = kernel_prep(reinterpret_cast<const void*>(kern), kThreads, G::SMEM, &per_sm);
+  const size_t smem = G::SMEM + (a.longest_first ? 4u * (65u + static_cast<uint32_t>(a.S)) : 0u);
+  cudaError_t e = kernel_prep(reinterpret_cast<const void*>(kern), kThreads, smem, &per_sm);
   if (e != cudaSuccess) return e;
   const int total = a.S * (a.H / kHG) * a.NP;
   const int grid = std::max(1, std::min(total, num_sms * std::max(per_sm, 1)));
-  kern<<<grid, kThreads, G::SMEM, stream>>>(a);
+  kern<<<grid, kThreads, smem, stream>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.NP == 1) return e;
   const int warps = a.S * a.H;

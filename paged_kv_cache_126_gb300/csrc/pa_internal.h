@@ -182,6 +182,8 @@ struct SplitArgs {
   const int32_t* context_lens;  // [S]
   int32_t S, H, num_blocks, max_blocks;
   int32_t P, NP;                // tokens per partition (multiple of B), partitions per sequence
+  int32_t longest_first;        // 1: items of whole sequences in decreasing length (order kept in
+                                //    shared memory after the kernel's own layout), 0: batch order
   float qk_scale_log2;
   int32_t* sched;               // [2] work counter, retired blocks (zero between launches)
   float* ws_ml;                 // [S * H/4 * NP][4][2] partial (max, sum) when NP > 1
