@@ -556,7 +556,9 @@ int pa_decode_split(const pa_tensor* q, const pa_tensor* k_cache, const pa_tenso
   // about four per thread-block slot (two blocks per SM), so that the dynamic scheduler
   // ends the launch with short items on every block instead of a second wave of long
   // ones on a few
-  const int64_t groups = H / 4, cap = std::max<int64_t>(max_blocks * B, B);
+  // heads per work item: 4, or 2 where a stage of 4 heads' frame would pass 48 KB
+  const int64_t hg = 2 * 4 * D * B * elem_bytes(dt) > 48 * 1024 ? 2 : 4;
+  const int64_t groups = H / hg, cap = std::max<int64_t>(max_blocks * B, B);
   int64_t P = cap, NP = 1;
   if (S * groups < 2LL * sms) {
     const int64_t want = (8LL * sms + S * groups - 1) / (S * groups);
@@ -581,13 +583,14 @@ int pa_decode_split(const pa_tensor* q, const pa_tensor* k_cache, const pa_tenso
   a.max_blocks = static_cast<int32_t>(max_blocks);
   a.P = static_cast<int32_t>(P);
   a.NP = static_cast<int32_t>(NP);
+  a.hg = static_cast<int32_t>(hg);
   // whole sequences as items: hand them out longest first (the order costs 4 bytes of
   // shared memory per sequence, kept small enough to leave two blocks per SM)
   a.longest_first = NP == 1 && S <= 2048 ? 1 : 0;
   a.qk_scale_log2 = scale * 1.4426950408889634f;
   a.status = g_dev[dev].status;
   const size_t items = static_cast<size_t>(S * groups * NP);
-  const size_t rest = NP > 1 ? items * 4 * (2 + static_cast<size_t>(D)) * sizeof(float) : 0;
+  const size_t rest = NP > 1 ? items * hg * (2 + static_cast<size_t>(D)) * sizeof(float) : 0;
   void* ws = nullptr;
   size_t cnt_bytes = 0;
   PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), 0, rest, &ws, &cnt_bytes));
@@ -595,7 +598,7 @@ int pa_decode_split(const pa_tensor* q, const pa_tensor* k_cache, const pa_tenso
   if (NP > 1) {
     float* base = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kSchedBytes + cnt_bytes);
     a.ws_ml = base;
-    a.ws_o = base + items * 4 * 2;
+    a.ws_o = base + items * hg * 2;
   }
   if (pa::launch_decode_split(dt, static_cast<int>(D), static_cast<int>(B), a, sms,
                               static_cast<cudaStream_t>(stream)) != cudaSuccess)

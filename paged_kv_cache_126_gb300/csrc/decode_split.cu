@@ -5,11 +5,13 @@
 // computes ("Solving the LLM Memory Wall", "1. The Mathematical Foundation"):
 // out = sum_j softmax(q . k_j * scale) v_j over the sequence's tokens.
 //
-// Design (one producer warp and kHG = 4 consumer warps per block, persistent grid,
+// Design (one producer warp and HG consumer warps per block, persistent grid,
 // dynamic work counter):
-//   * Work item = (sequence, group of 4 heads, context partition of P tokens).  In
-//     this layout the K (and the V) of one frame for 4 consecutive heads is one
-//     contiguous run of 4*D*B elements, so the producer stages a frame with two
+//   * Work item = (sequence, group of HG heads, context partition of P tokens); HG = 4,
+//     or 2 where a frame of 4 heads would make a stage larger than 48 KB (D = 128,
+//     B = 32), so that a block still holds three stages and two blocks fit an SM.  In
+//     this layout the K (and the V) of one frame for HG consecutive heads is one
+//     contiguous run of HG*D*B elements, so the producer stages a frame with two
 //     bulk copies (cp.async.bulk) into a ring of stages completing on mbarriers.
 //   * Consumer warp = one head.  Keys: lane (t, ph) = (lane mod B, lane / B) holds
 //     q chunks ph, ph + 32/B, ... (16 bytes each) and reads the same chunks of token
@@ -38,12 +40,10 @@ namespace pa {
 namespace sk {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kHG = 4;
-constexpr int kThreads = 32 * (kHG + 1);
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr long long kDrainCycles = 200000000LL;
 
-template <typename T, int D, int B>
+template <typename T, int D, int B, int HG>
 struct Geo {
   static constexpr int E = sizeof(T);
   static constexpr int X = 16 / E;                       // elements per 16-byte chunk
@@ -55,7 +55,7 @@ struct Geo {
   static constexpr int RPI = 32 / C;                     // V rows one warp-wide read covers
   static constexpr int NR = D / RPI;                     // V rows each lane accumulates (part of)
   static constexpr uint32_t HEAD = D * B * E;            // one head of one frame (K or V)
-  static constexpr uint32_t STAGE = 2 * kHG * HEAD;      // K of 4 heads, then V of 4 heads
+  static constexpr uint32_t STAGE = 2 * HG * HEAD;       // K of HG heads, then V of HG heads
   static constexpr int NST = (96 * 1024 / STAGE) < 2 ? 2 : ((96 * 1024 / STAGE) > 6 ? 6 : 96 * 1024 / STAGE);
   static constexpr uint32_t BAR_OFF = NST * STAGE;       // [NST full][NST empty][2 item full][2 item empty]
   static constexpr uint32_t MISC_OFF = BAR_OFF + 8 * (2 * NST + 4);
@@ -148,9 +148,10 @@ struct Item {
   int s, g, p, t0, t1;  // tokens t0 .. t1-1 of sequence s, head group g, partition p
 };
 // order: sequence of each rank (longest first) when a.longest_first, else unused
+template <int HG>
 __device__ __forceinline__ Item locate(const SplitArgs& a, const int32_t* order, int item) {
   Item it;
-  const int groups = a.H / kHG;
+  const int groups = a.H / HG;
   it.p = item % a.NP;
   const int sg = item / a.NP;
   it.g = sg % groups;
@@ -161,9 +162,9 @@ __device__ __forceinline__ Item locate(const SplitArgs& a, const int32_t* order,
   return it;
 }
 
-template <typename T, int D, int B>
-__global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs a) {
-  using G = Geo<T, D, B>;
+template <typename T, int D, int B, int HG>
+__global__ void __launch_bounds__(32 * (HG + 1)) decode_split_kernel(const SplitArgs a) {
+  using G = Geo<T, D, B, HG>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((128u - (su32(smem_raw) & 127u)) & 127u);
   const uint32_t sb = su32(smem);
@@ -180,11 +181,11 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
   if (tid == 0) {
     for (int i = 0; i < G::NST; ++i) {
       mbar_init(FULL(i), 1);
-      mbar_init(EMPTY(i), kHG);
+      mbar_init(EMPTY(i), HG);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(IFULL(i), 1);
-      mbar_init(IEMPTY(i), kHG);
+      mbar_init(IEMPTY(i), HG);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
     }
   }
   __syncthreads();
-  const int total = a.S * (a.H / kHG) * a.NP;
+  const int total = a.S * (a.H / HG) * a.NP;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
         }
         ++ni;
         if (done) break;
-        const Item it = locate(a, order, item);
+        const Item it = locate<HG>(a, order, item);
         const int L = a.context_lens[it.s];
         if ((L < 0 || L > row_cap) && it.g == 0 && it.p == 0) atomicOr(a.status, kDevBadLen);
         const int t1 = (L < 0 || L > row_cap) ? 0 : it.t1;
@@ -278,10 +279,10 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
           }
           n_valid[st] = nv;
           mbar_expect_tx(FULL(st), G::STAGE);
-          const int64_t head0 = static_cast<int64_t>(fr) * a.H + it.g * kHG;
+          const int64_t head0 = static_cast<int64_t>(fr) * a.H + it.g * HG;
           const uint32_t dst = sb + st * G::STAGE;
-          bulk_load(dst, static_cast<const T*>(a.k_cache) + head0 * D * B, kHG * G::HEAD, FULL(st));
-          bulk_load(dst + kHG * G::HEAD, static_cast<const T*>(a.v_cache) + head0 * D * B, kHG * G::HEAD,
+          bulk_load(dst, static_cast<const T*>(a.k_cache) + head0 * D * B, HG * G::HEAD, FULL(st));
+          bulk_load(dst + HG * G::HEAD, static_cast<const T*>(a.v_cache) + head0 * D * B, HG * G::HEAD,
                     FULL(st));
         }
         if (!ok) break;
@@ -320,10 +321,10 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
     if (lane == 0) mbar_arrive(IEMPTY(sl));
     ++ni;
     if (item < 0) break;
-    const Item it = locate(a, order, item);
+    const Item it = locate<HG>(a, order, item);
     const int L = a.context_lens[it.s];
     const int t1 = (L < 0 || L > row_cap) ? 0 : it.t1;
-    const int h = it.g * kHG + hh;
+    const int h = it.g * HG + hh;
     // q chunks of this lane, in log2 units
     float qv[G::STEPS][8];
     {
@@ -348,7 +349,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
       }
       const int nv = n_valid[st];
       const T* kh = reinterpret_cast<const T*>(smem + st * G::STAGE + hh * G::HEAD);           // [NC][B][X]
-      const T* vh = reinterpret_cast<const T*>(smem + st * G::STAGE + (kHG + hh) * G::HEAD);   // [D][B]
+      const T* vh = reinterpret_cast<const T*>(smem + st * G::STAGE + (HG + hh) * G::HEAD);    // [D][B]
       float dot = 0.f;
 #pragma unroll
       for (int k = 0; k < G::STEPS; ++k) {
@@ -411,7 +412,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const SplitArgs 
       }
     } else {
       // partial slots are keyed by (sequence, head group, partition), which the merge reads
-      const int64_t slot = (static_cast<int64_t>(it.s * (a.H / kHG) + it.g) * a.NP + it.p) * kHG + hh;
+      const int64_t slot = (static_cast<int64_t>(it.s * (a.H / HG) + it.g) * a.NP + it.p) * HG + hh;
       if (vc == 0) {
 #pragma unroll
         for (int j = 0; j < G::NR; ++j) a.ws_o[slot * D + vr0 + G::RPI * j] = ok ? o[j] : 0.f;
@@ -432,9 +433,9 @@ __global__ void __launch_bounds__(128) merge_split_kernel(const SplitArgs a) {
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= a.S * a.H) return;
   const int s = wid / a.H, h = wid % a.H;
-  const int g = h / kHG, hh = h % kHG;
-  const int groups = a.H / kHG;
-  auto slot = [&](int p) { return (static_cast<int64_t>((s * groups + g) * a.NP + p)) * kHG + hh; };
+  const int g = h / a.hg, hh = h % a.hg;
+  const int groups = a.H / a.hg;
+  auto slot = [&](int p) { return (static_cast<int64_t>((s * groups + g) * a.NP + p)) * a.hg + hh; };
   // 1. lane p holds part p's (max, sum), parts in chunks of 32: the largest max
   float M = -INFINITY;
   for (int p0 = 0; p0 < a.NP; p0 += 32)
@@ -478,15 +479,16 @@ __global__ void __launch_bounds__(128) merge_split_kernel(const SplitArgs a) {
   for (int j = 0; j < ND; ++j) orow[lane + 32 * j] = from_float<T>(num[j] * inv);
 }
 
-template <typename T, int D, int B>
+template <typename T, int D, int B, int HG>
 cudaError_t launch(const SplitArgs& a, int num_sms, cudaStream_t stream) {
-  using G = Geo<T, D, B>;
-  auto kern = decode_split_kernel<T, D, B>;
+  using G = Geo<T, D, B, HG>;
+  constexpr int kThreads = 32 * (HG + 1);
+  auto kern = decode_split_kernel<T, D, B, HG>;
   int per_sm = 0;
   const size_t smem = G::SMEM + (a.longest_first ? 4u * (65u + static_cast<uint32_t>(a.S)) : 0u);
   cudaError_t e = kernel_prep(reinterpret_cast<const void*>(kern), kThreads, smem, &per_sm);
   if (e != cudaSuccess) return e;
-  const int total = a.S * (a.H / kHG) * a.NP;
+  const int total = a.S * (a.H / HG) * a.NP;
   const int grid = std::max(1, std::min(total, num_sms * std::max(per_sm, 1)));
   kern<<<grid, kThreads, smem, stream>>>(a);
   e = cudaGetLastError();
@@ -498,14 +500,15 @@ cudaError_t launch(const SplitArgs& a, int num_sms, cudaStream_t stream) {
 
 template <typename T>
 cudaError_t launch_dt(int D, int B, const SplitArgs& a, int num_sms, cudaStream_t stream) {
+  // heads per block: a.hg, chosen by the caller (4, or 2 for D = 128 and B = 32)
   if (D == 128) {
-    if (B == 8) return launch<T, 128, 8>(a, num_sms, stream);
-    if (B == 16) return launch<T, 128, 16>(a, num_sms, stream);
-    if (B == 32) return launch<T, 128, 32>(a, num_sms, stream);
-  } else if (D == 64) {
-    if (B == 8) return launch<T, 64, 8>(a, num_sms, stream);
-    if (B == 16) return launch<T, 64, 16>(a, num_sms, stream);
-    if (B == 32) return launch<T, 64, 32>(a, num_sms, stream);
+    if (B == 8 && a.hg == 4) return launch<T, 128, 8, 4>(a, num_sms, stream);
+    if (B == 16 && a.hg == 4) return launch<T, 128, 16, 4>(a, num_sms, stream);
+    if (B == 32 && a.hg == 2) return launch<T, 128, 32, 2>(a, num_sms, stream);
+  } else if (D == 64 && a.hg == 4) {
+    if (B == 8) return launch<T, 64, 8, 4>(a, num_sms, stream);
+    if (B == 16) return launch<T, 64, 16, 4>(a, num_sms, stream);
+    if (B == 32) return launch<T, 64, 32, 4>(a, num_sms, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -182,12 +182,14 @@ struct SplitArgs {
   const int32_t* context_lens;  // [S]
   int32_t S, H, num_blocks, max_blocks;
   int32_t P, NP;                // tokens per partition (multiple of B), partitions per sequence
+  int32_t hg;                   // heads per work item and thread block: 4, or 2 when a frame of
+                                //    4 heads would make a stage larger than 48 KB
   int32_t longest_first;        // 1: items of whole sequences in decreasing length (order kept in
                                 //    shared memory after the kernel's own layout), 0: batch order
   float qk_scale_log2;
   int32_t* sched;               // [2] work counter, retired blocks (zero between launches)
-  float* ws_ml;                 // [S * H/4 * NP][4][2] partial (max, sum) when NP > 1
-  float* ws_o;                  // [S * H/4 * NP][4][D] partial unnormalised outputs
+  float* ws_ml;                 // [S * H/hg * NP][hg][2] partial (max, sum) when NP > 1
+  float* ws_o;                  // [S * H/hg * NP][hg][D] partial unnormalised outputs
   int32_t* status;
 };
 cudaError_t launch_decode_split(int dtype, int D, int B, const SplitArgs& a, int num_sms, cudaStream_t stream);

@@ -82,10 +82,12 @@ def test_head_dim_64(pa, B):
     check(pa, workloads.custom([37, 300, 512, 5], H=4, D=64, B=B, dtype="f16", seed=80 + B))
 
 
+@pytest.mark.parametrize("B", [16, 32])
 @pytest.mark.parametrize("lens", [[2500, 1700], [4096], [255, 256, 257]])
-def test_partitions_and_merge(pa, lens):
-    """Few (sequence, head group) items: the context is split and merged."""
-    check(pa, workloads.custom(lens, H=4, D=128, B=16, dtype="bf16", seed=sum(lens)))
+def test_partitions_and_merge(pa, lens, B):
+    """Few (sequence, head group) items: the context is split and merged (at B = 32 the
+    items hold two heads each, so the partial slots of both group sizes are covered)."""
+    check(pa, workloads.custom(lens, H=4, D=128, B=B, dtype="bf16", seed=sum(lens) + B))
 
 
 def test_rejects_unsupported(pa):
