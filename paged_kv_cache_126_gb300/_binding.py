@@ -163,6 +163,12 @@ def tensor_desc(t: torch.Tensor) -> PaTensor:
 
 
 def _make_desc(t: torch.Tensor) -> PaTensor:
+    # every pa_tensor argument is device memory: a host tensor would hand the kernels a
+    # host address (checked here, once per distinct tensor: descriptors are cached)
+    if not t.is_cuda:
+        raise ValueError("device operations take CUDA tensors")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"tensor on {t.device} but the current device is cuda:{torch.cuda.current_device()}")
     if t.dtype not in _TORCH_DT:
         raise TypeError(f"unsupported dtype {t.dtype}")
     if t.dim() < 1 or t.dim() > 4:

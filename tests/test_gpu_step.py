@@ -115,4 +115,8 @@ def test_native_step_errors(pa):
     eng.decode_step([0], rows, rows, q, 0.1)  # 32 tokens: still 2 frames
     with pytest.raises(pa.PAError):          # 33 tokens need a third frame: more than max_blocks
         eng.decode_step([0], rows, rows, q, 0.1)
+    before = eng.bm.seq_info(0)              # the capacity error's block-manager step stands
+    with pytest.raises(ValueError):          # host rows: refused before anything runs
+        eng.decode_step([0], rows.cpu(), rows, q, 0.1)
+    assert eng.bm.seq_info(0) == before
     torch.cuda.synchronize()
