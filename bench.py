@@ -953,7 +953,10 @@ def bench_extras(device, reps=10, flushed_reps=10):
     """The other serving shapes, each on the decode kernel path the engine picks, with
     device-drawn rows: long context 4 x 16384 (split contexts + merge), parallel
     sampling with copy-on-write (plain and through the shared-prefix decode), the
-    256-sequence serving mix (with its append), and the chunked prefill."""
+    256-sequence serving mix (with its append), and the chunked prefill.  Then the
+    beam-search step loop over forked sequences (plain and shared-prefix decode),
+    prompt admission with and without prefix caching, the two cache layouts, and
+    decode / prefill throughput against the block size."""
     peak, src = _peaks()
     out = {}
     for key, name in (("2", "cfg2"), ("3", "cfg3"), ("3s", "cfg3_shared"), ("4", "cfg4")):
@@ -978,6 +981,19 @@ def bench_extras(device, reps=10, flushed_reps=10):
             ent["append"] = f["append"]
         out[name] = ent
     out["prefill"] = prefill_figures(reps, flushed_reps, e2e=False, device_rows=True, sample_clocks=True)
+    # the remaining next-step workloads, compact: each guarded, so that a failure here
+    # leaves its error in the line instead of losing the line
+    def guarded(fn):
+        try:
+            return fn()
+        except Exception as e:  # noqa: BLE001
+            return {"error": f"{type(e).__name__}: {e}"[:300]}
+
+    out["fork_trees"] = {"pa_decode": guarded(lambda: fork_tree_bench(emit=False)),
+                         "shared_prefix": guarded(lambda: fork_tree_bench(share=True, emit=False))}
+    out["prefix_caching"] = guarded(lambda: prefix_bench(emit=False))
+    out["split_layout"] = guarded(lambda: split_layout_bench(emit=False))
+    out["block_sweep"] = guarded(lambda: block_sweep(blocks=(8, 16, 32, 64), emit=False))
     return out
 
 
@@ -1015,7 +1031,7 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
-def prefix_bench(n_requests=16, system_len=2048, user_len=512, reps=10):
+def prefix_bench(n_requests=16, system_len=2048, user_len=512, reps=10, emit=True):
     """Admission of requests that share a system prompt: host block manager, cache
     append of the rows that must be computed, causal prefill of those tokens.
     Three ways: no prefix cache (every prompt in full), prefix cache starting empty
@@ -1121,10 +1137,14 @@ def prefix_bench(n_requests=16, system_len=2048, user_len=512, reps=10):
             "speedup_gpu_cold_vs_none": round(out["none"]["gpu_ms"] / out["cold"]["gpu_ms"], 2),
             "speedup_e2e_warm_vs_none": round(out["none"]["ms_e2e"] / out["warm"]["ms_e2e"], 2),
             "speedup_e2e_cold_vs_none": round(out["none"]["ms_e2e"] / out["cold"]["ms_e2e"], 2)}
-    print(json.dumps(line), flush=True)
+    del eng, k_rows, v_rows, q_rows
+    torch.cuda.empty_cache()
+    if emit:
+        print(json.dumps(line), flush=True)
+    return line
 
 
-def fork_tree_bench(n_prompts=8, prompt_len=2048, width=8, steps=64, share=False):
+def fork_tree_bench(n_prompts=8, prompt_len=2048, width=8, steps=64, share=False, emit=True):
     """Beam search over forked sequences, the whole step loop on one GPU: host block
     manager (step with copy-on-write, then the selection's forks and frees in one
     batched call each), staged
@@ -1218,7 +1238,7 @@ def fork_tree_bench(n_prompts=8, prompt_len=2048, width=8, steps=64, share=False
     logical = np.array([x[1] for x in stats], np.float64)
     unique = np.array([x[2] for x in stats], np.float64)
     copies = int(sum(x[3] for x in stats))
-    print(json.dumps({
+    res = {
         "metric": "beam-search decode step over forked sequences (block manager + copy-on-write + append + decode)",
         "workload": w.name, "share_prefix": int(share), "beams": nbeams, "steps": len(stats),
         "ms_per_step_e2e": round(total / n_steps * 1e3, 3),
@@ -1227,10 +1247,14 @@ def fork_tree_bench(n_prompts=8, prompt_len=2048, width=8, steps=64, share=False
         "decode_gbs_logical": round(float(np.sum(logical) / np.sum(dec)) / 1e9, 1),
         "decode_gbs_unique_frames": round(float(np.sum(unique) / np.sum(dec)) / 1e9, 1),
         "logical_over_unique_bytes": round(float(np.sum(logical) / np.sum(unique)), 2),
-        "cow_copies": copies, "cow_copies_per_step": round(copies / len(stats), 2)}), flush=True)
+        "cow_copies": copies, "cow_copies_per_step": round(copies / len(stats), 2)}
+    torch.cuda.empty_cache()
+    if emit:
+        print(json.dumps(res), flush=True)
+    return res
 
 
-def block_sweep(blocks=(8, 16, 32, 64, 128, 256), reps=20):
+def block_sweep(blocks=(8, 16, 32, 64, 128, 256), reps=20, emit=True):
     """Block size B against throughput, one JSON line per B: pa_decode on the decode
     batch's lengths (64 sequences, L ~ U[512, 2048], H=32, D=128, fp16; GB/s of
     algorithmic bytes) and pa_prefill on the chunked-prefill batch's shapes (16 x
@@ -1277,6 +1301,7 @@ def block_sweep(blocks=(8, 16, 32, 64, 128, 256), reps=20):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / 1e3 / reps
 
+    lines = []
     for B in blocks:
         line = {"metric": "block size sweep", "B": B}
         eng = engine(dec_lens, B)
@@ -1307,10 +1332,14 @@ def block_sweep(blocks=(8, 16, 32, 64, 128, 256), reps=20):
             fl = prefill_flops(pre_lens, chunks, H, D)
             line.update({"prefill_us": round(t * 1e6, 2), "prefill_tflops": round(fl / t / 1e12, 1)})
             del eng
-        print(json.dumps(line), flush=True)
+        torch.cuda.empty_cache()
+        lines.append(line)
+        if emit:
+            print(json.dumps(line), flush=True)
+    return lines
 
 
-def split_layout_bench(reps=20):
+def split_layout_bench(reps=20, emit=True):
     """The two cache layouts head to head, one JSON line per (workload, B): pa_decode
     on [num_blocks, B, H, D] caches and pa_decode_split on the layout of the pages'
     kernel signature (k [num_blocks, H, D/x, B, x], v [num_blocks, H, D, B]); same
@@ -1341,6 +1370,7 @@ def split_layout_bench(reps=20):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / 1e3 / reps
 
+    lines = []
     for name, lens in cases:
         for B in (8, 16, 32):
             S = len(lens)
@@ -1368,7 +1398,11 @@ def split_layout_bench(reps=20):
             t = timed(lambda: pa.pa_decode_split(q, ks, vs, td, ld, 0.0883883, out))
             line["split_gbs"] = round(byts / t / 1e9, 1)
             del ks, vs
-            print(json.dumps(line), flush=True)
+            torch.cuda.empty_cache()
+            lines.append(line)
+            if emit:
+                print(json.dumps(line), flush=True)
+    return lines
 
 
 def _bm_replay(pa, w):
