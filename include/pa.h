@@ -402,10 +402,12 @@ int pa_bm_free_many(pa_bm* bm, const int64_t* seq_ids, int32_t n);
  * pinned host memory (per device and stream, four slots, each reused only after the
  * kernel that last read it has run), then pa_copy_blocks (when a shared tail was
  * written), pa_cache_append of k_new / v_new [n, H, D] (device) at the step's slots,
- * and pa_decode_ex of q [n, H, D] into out, all on `stream`.  On a step without
- * frame copies the append reads its slots from the ring directly and copies the
- * tables and lengths to device memory in the same launch; a step with copies uploads
- * the staged block with one asynchronous copy first.  params may be NULL:
+ * and pa_decode_ex of q [n, H, D] into out, all on `stream`.  The frame copies of a
+ * step (up to 256 of them) carry their (src, dst) pairs in the copy kernel's launch
+ * parameters; the append reads its slots from the ring directly and copies the
+ * tables and lengths to device memory in the same launch.  A step with more than 256
+ * copies uploads the staged block with one asynchronous copy first and runs
+ * pa_copy_blocks on the device pairs.  params may be NULL:
  * automatic launch options, with share_prefix = 1 when auto_share is set and two
  * neighbouring sequences of the batch start on the same frame.  *n_copies_out (may
  * be NULL) receives the number of frame copies; lens_out (host, n entries, may be

@@ -1201,9 +1201,9 @@ extern "C" int pa_step_decode(pa_bm* bm, const int64_t* seq_ids, int32_t n, int3
   }
   if (n_copies_out) *n_copies_out = nc;
   if (lens_out) std::memcpy(lens_out, h + 3 * n, sizeof(int32_t) * n);
-  if (nc) {
-    // copy-on-write frame copies first: one upload of the staged block, the copies,
-    // then the new rows with their slots from device memory
+  if (nc > pa::kInlineCopies) {
+    // more copy-on-write copies than a launch's parameters carry: one upload of the
+    // staged block, the copies, then the new rows with their slots from device memory
     if (cudaMemcpyAsync(d, h, need * sizeof(int32_t), cudaMemcpyHostToDevice, st) != cudaSuccess ||
         cudaEventRecord(s->done[i], st) != cudaSuccess)
       return PA_ERR_CUDA;
@@ -1213,12 +1213,27 @@ extern "C" int pa_step_decode(pa_bm* bm, const int64_t* seq_ids, int32_t n, int3
     const pa_tensor slots = i32_view(d, n, 0);
     PA_TRY(pa_cache_append(k_new, v_new, &slots, k_cache, v_cache, stream));
   } else {
-    // no copies: the append reads its slots from the pinned block itself and copies the
-    // block (lengths and tables for the decode) to device memory in the same launch, so
-    // no copy-engine transfer sits between the previous step's decode and this append.
-    // The device slot it writes was last read by the decode three steps back, which has
+    // Copy-on-write copies, if any, with their pairs in the kernel's parameters.  Then the
+    // append: it reads its slots from the pinned block itself and copies the block
+    // (lengths and tables for the decode) to device memory in the same launch, so no
+    // copy-engine transfer sits between the previous step's decode and this step.  The
+    // device slot it writes was last read by the decode three steps back, which has
     // finished once any kernel of the previous step runs (each step's kernels wait for
     // the one before them).
+    if (nc) {
+      PA_TRY(check_cache(k_cache, v_cache));
+      pa::InlineCopyArgs c;
+      std::memset(&c, 0, sizeof(c));
+      c.k_cache = static_cast<unsigned char*>(k_cache->data);
+      c.v_cache = static_cast<unsigned char*>(v_cache->data);
+      c.frame_bytes = k_cache->stride[0] * elem_bytes(k_cache->dtype);
+      c.n = nc;
+      c.num_blocks = static_cast<int32_t>(k_cache->shape[0]);
+      c.status = g_dev[dev].status;
+      std::memcpy(c.pairs, h + n, sizeof(int32_t) * 2 * static_cast<size_t>(nc));
+      if (pa::launch_copy_blocks_inline(c, st) != cudaSuccess) return PA_ERR_CUDA;
+      g_launches.fetch_add(1);
+    }
     pa::AppendArgs stage;
     std::memset(&stage, 0, sizeof(stage));
     stage.slots_host = 1;

@@ -106,7 +106,48 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(const CopyArgs a, cons
   for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) d[i] = s[i];
 }
 
+// The decode step's frame copies: pairs in the parameters, launched with programmatic
+// stream serialisation.  The next kernel (the step's append) may start now; its row
+// writes still wait for this kernel to finish, so a copy lands before any row is
+// written into its destination frame.
+__global__ void __launch_bounds__(256) copy_blocks_inline_kernel(const __grid_constant__ InlineCopyArgs a,
+                                                                 const int64_t slice_vecs) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int pair = blockIdx.x;
+  const int32_t src = a.pairs[2 * pair];
+  const int32_t dst = a.pairs[2 * pair + 1];
+  if (src < 0 || src >= a.num_blocks || dst < 0 || dst >= a.num_blocks) {
+    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) atomicOr(a.status, kDevBadCopy);
+    return;
+  }
+  unsigned char* base = blockIdx.z == 0 ? a.k_cache : a.v_cache;
+  const uint4* s = reinterpret_cast<const uint4*>(base + static_cast<int64_t>(src) * a.frame_bytes);
+  uint4* d = reinterpret_cast<uint4*>(base + static_cast<int64_t>(dst) * a.frame_bytes);
+  const int64_t nvec = a.frame_bytes >> 4;
+  const int64_t lo = static_cast<int64_t>(blockIdx.y) * slice_vecs;
+  const int64_t hi = lo + slice_vecs < nvec ? lo + slice_vecs : nvec;
+  for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) d[i] = s[i];
+}
+
 }  // namespace
+
+cudaError_t launch_copy_blocks_inline(const InlineCopyArgs& a, cudaStream_t stream) {
+  if (a.n <= 0 || a.n > kInlineCopies) return a.n == 0 ? cudaSuccess : cudaErrorInvalidValue;
+  const int64_t nvec = a.frame_bytes >> 4;
+  const int64_t slice_vecs = 1024;  // 16 KiB per thread block
+  const int64_t slices = (nvec + slice_vecs - 1) / slice_vecs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n, static_cast<unsigned>(slices), 2);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, copy_blocks_inline_kernel, a, slice_vecs);
+}
 
 cudaError_t launch_cache_append(const AppendArgs& a, int num_sms, cudaStream_t stream) {
   if (a.T <= 0) return cudaSuccess;

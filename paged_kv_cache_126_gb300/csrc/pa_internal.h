@@ -75,13 +75,27 @@ cudaError_t launch_cache_append(const AppendArgs& a, int num_sms, cudaStream_t s
 struct CopyArgs {
   unsigned char* k_cache;
   unsigned char* v_cache;
-  const int32_t* pairs;         // [n, 2]
+  const int32_t* pairs;         // [n, 2] in device memory
   int64_t frame_bytes;          // B * H * D * elem (multiple of 16)
   int32_t n;
   int32_t num_blocks;
   int32_t* status;
 };
 cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream);
+
+// The same copies with the pairs passed in the kernel's parameters (no device buffer):
+// the decode step's path, for up to kInlineCopies pairs.
+constexpr int kInlineCopies = 256;
+struct InlineCopyArgs {
+  unsigned char* k_cache;
+  unsigned char* v_cache;
+  int64_t frame_bytes;
+  int32_t n;
+  int32_t num_blocks;
+  int32_t* status;
+  int32_t pairs[2 * kInlineCopies];  // (src, dst) frame ids
+};
+cudaError_t launch_copy_blocks_inline(const InlineCopyArgs& a, cudaStream_t stream);
 
 // ---- decode ------------------------------------------------------------------------------
 struct DecodeArgs {

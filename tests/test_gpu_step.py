@@ -1,8 +1,8 @@
 """GPU parity of the native decode step (pa_step_decode through PagedKVEngine.decode_step).
 
 Workloads are replayed with every decode step and the attention that follows it fused
-into one decode_step call (block-manager step, tables, staged upload, copy-on-write
-copies, append, decode in libpa).  Slots, copies, tables, reference counts and every
+into one decode_step call (block-manager step, tables staged in pinned memory,
+copy-on-write copies, append, decode in libpa).  Slots, copies, tables, reference counts and every
 cache bit must equal the oracle's, attention outputs be within 2e-3 of it, and the
 native path must give the same bits as the same step through the separate calls.
 """
@@ -77,6 +77,11 @@ CASES = [
     ("beam search wide", lambda: workloads.beam_search(2, 150, 8, 16, H=4, B=16, dtype="f16", seed=73)),
     ("beam search", lambda: workloads.beam_search(3, 200, 4, 20, H=4, B=16, dtype="f16", seed=71)),
     ("beam search bf16 B=8", lambda: workloads.beam_search(2, 100, 8, 12, H=4, B=8, dtype="bf16", seed=72)),
+    # 320 beams: the first decode step copies 316 shared tail frames, more than one launch's
+    # parameters carry (256 pairs), so that step uploads its pairs; the later steps copy
+    # 109 and 123 frames with the pairs in the launch parameters
+    ("beam search, 316 copies in one step", lambda: workloads.beam_search(4, 30, 80, 4, H=2, B=16, dtype="f16",
+                                                                         seed=78)),
 ]
 
 
