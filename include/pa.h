@@ -129,8 +129,9 @@ int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache,
  *   out           [S, H, D], same dtype as q, [H, D] contiguous.
  * Arithmetic: K/V/q converted to fp32, fp32 dot products, online softmax and
  * accumulation in fp32, one rounding to the output dtype.  Long contexts are
- * split into partitions processed by separate thread blocks and combined by a
- * log-sum-exp merge kernel on the same stream.  Work is handed to a persistent
+ * split into partitions processed by separate thread blocks and combined by the
+ * log-sum-exp rule in the same kernel: the last partition of a (sequence, head) to
+ * finish merges them.  Work is handed to a persistent
  * grid through an atomic counter.  Counter and split partials live in a
  * workspace the library owns: one per (device, stream), allocated (cudaMalloc)
  * and zeroed on the first call with that pair and grown on the first call that
@@ -243,7 +244,8 @@ typedef struct pa_decode_params {
  * of two >= 8 and 2 <= S <= 4096 (other shapes run the plain decode, with the same
  * result).  heads_per_cta, when given, must be 1, 2 or 4 and warps_per_head 0 or 1,
  * else PA_ERR_INVALID.  Uses workspace partials for every sequence that has more than
- * one part, and launches three kernels (the plan, the decode, the log-sum-exp merge). */
+ * one part, and launches two kernels: the plan, then the decode, whose thread blocks
+ * merge the split sequences by the log-sum-exp rule once they have no items left. */
 int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
                  const pa_tensor* block_tables, const pa_tensor* context_lens,
                  float scale, const pa_tensor* out, const pa_decode_params* params,

@@ -634,7 +634,7 @@ int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache, const pa_
 
 namespace {
 // Shared-prefix decode (pa_decode_params.share_prefix).  Returns PA_OK after launching
-// the plan kernel and the decode, kNotApplicable when the shapes fall outside what the
+// the plan kernel and the decode (which merges split sequences itself), kNotApplicable when the shapes fall outside what the
 // shared-prefix kernel handles (the caller then runs the plain decode: same result),
 // or an error code.
 constexpr int kNotApplicable = 1;
@@ -731,10 +731,13 @@ int decode_shared(int dev, const pa_tensor* q, const pa_tensor* k_cache, const p
   {
     const size_t o_bytes = static_cast<size_t>(part_cap * H * D) * sizeof(float);
     const size_t ml_bytes = static_cast<size_t>(part_cap * H * 2) * sizeof(float);
-    const size_t lcp_bytes = static_cast<size_t>(2 * S + 1) * sizeof(int32_t);  // lcp [S], slot offsets [S + 1]
+    const size_t lcp_bytes = static_cast<size_t>(S) * sizeof(int32_t);
+    // arrival counters: parts finished per (sequence, head), for the in-kernel merges
+    const size_t cnt_need = static_cast<size_t>(S * H) * sizeof(int32_t);
     void* ws = nullptr;
     size_t cnt_bytes = 0;
-    PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), 0, o_bytes + ml_bytes + lcp_bytes, &ws, &cnt_bytes));
+    PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), cnt_need, o_bytes + ml_bytes + lcp_bytes, &ws,
+                     &cnt_bytes));
     unsigned char* w = static_cast<unsigned char*>(ws);
     unsigned char* rest = w + kSchedBytes + cnt_bytes;
     a.sched = reinterpret_cast<int32_t*>(w);
@@ -742,11 +745,10 @@ int decode_shared(int dev, const pa_tensor* q, const pa_tensor* k_cache, const p
     a.ws_o = reinterpret_cast<float*>(rest);
     a.ws_ml = reinterpret_cast<float*>(rest + o_bytes);
     a.lcp = reinterpret_cast<int32_t*>(rest + o_bytes + ml_bytes);
-    a.pbase_out = a.lcp + S;
   }
   if (pa::launch_decode_shared(a, c, tk, tv, static_cast<cudaStream_t>(stream), false, nullptr) != cudaSuccess)
     return PA_ERR_CUDA;
-  g_launches.fetch_add(3);
+  g_launches.fetch_add(2);
   return PA_OK;
 }
 

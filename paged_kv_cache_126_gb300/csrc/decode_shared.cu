@@ -37,11 +37,15 @@
 //       through conflict-free ldmatrix loads from a 128-byte-swizzled layout.
 //     - Every part's (m, l, o) goes to slot pbase[s] + part of the workspace, or
 //       straight to the output when the sequence has one part.
-//   * merge kernel (one warp per (sequence, head), programmatic dependent launch):
-//     log-sum-exp merge of the slots of every sequence with more than one part.  A
-//     separate launch keeps the decode warps streaming: merging inside them (fence,
-//     arrival counter, then up to 16 members' merges by one warp) stalled the
-//     staging ring of the whole thread block.
+//     - A part of a sequence with more than one part raises that (sequence, head)'s
+//       arrival counter once its stores are visible; a consumer warp publishes its
+//       parts in one batch when its block has no items left (a fence per item stalled
+//       the staging ring).  Warps whose block has no items left take merge tasks
+//       (sequence, head) from a second counter, in the order the sequences' parts
+//       finish, wait (bounded) for the task's parts, and merge them by the log-sum-exp
+//       rule.  This replaces a separate merge launch after the whole kernel; merging in
+//       the consumer that brings the last part (up to 16 members' merges by one warp)
+//       stalled its block's staging ring.
 //   * Bad frame ids / lengths: as in decode_kernel (rows of the affected sequences
 //     become zeros, sticky status bits).  A bad length ends a run (its lcp is 0).
 #include <climits>
@@ -141,7 +145,7 @@ struct SLayout {
     flags = bars + 16u * stages + 32u;  // poison[stages], abort, item_slot[2]
     const uint32_t arr = 4u * static_cast<uint32_t>(S + 1);
     lv = (flags + 4u * (stages + 3) + 15u) & ~15u;     // validated context lengths (-1: bad) [S]
-    lc = (lv + arr + 15u) & ~15u;                      // tokens shared with the previous sequence [S]
+    lc = (lv + arr + 15u) & ~15u;                      // tokens shared with the previous sequence, then merge order [S]
     cinfo = (lc + arr + 15u) & ~15u;                   // chunk leader | chunk size << 24 [S]
     shl = (cinfo + arr + 15u) & ~15u;                  // shared tokens of the sequence's chunk [S]
     pbase = (shl + arr + 15u) & ~15u;                  // first partial slot of each sequence [S + 1]
@@ -421,7 +425,7 @@ __device__ __forceinline__ void run_item(const DecodeArgs& a, const Plan& pl, co
       if (t == 0) *reinterpret_cast<float2*>(a.ws_ml + slot * 2) = make_float2(m[ri], poisoned ? -1.f : l[ri]);
     }
   }
-  // sequences with more than one part are merged by merge_shared_kernel
+  // partials of sequences with more than one part are published by the caller
 }
 
 // Inclusive scan of arr[1 .. n] in place by one warp (arr[0] = 0 is left alone).
@@ -438,6 +442,155 @@ __device__ __forceinline__ void warp_scan(int32_t* arr, int n, int lane) {
     v += carry;
     if (i < n) arr[i + 1] = v;
     carry = __shfl_sync(kFull, v, 31);
+  }
+}
+
+// Log-sum-exp merge of one split (sequence, head) by one warp, once its parts have
+// arrived.  Lane p holds part p's (max, sum) -- parts in chunks of 32 -- and lane l
+// accumulates output dimensions 4l .. 4l+3 over the parts, with the loads of four parts
+// in flight at a time.  ready = false (the wait gave up): the row becomes zeros.
+template <typename T>
+__device__ __forceinline__ void merge_one(const DecodeArgs& a, int s, int head, int base, int np, bool ready,
+                                          int lane) {
+  constexpr int D = 128;
+  auto ml_at = [&](int p) {
+    return __ldcg(reinterpret_cast<const float2*>(a.ws_ml + (static_cast<int64_t>(base + p) * a.H + head) * 2));
+  };
+  const float* ob = a.ws_o + (static_cast<int64_t>(base) * a.H + head) * D + 4 * lane;
+  const int64_t pstride = static_cast<int64_t>(a.H) * D;
+  // up to four parts: their outputs are loaded with their (max, sum), one round trip
+  float4 pre[4];
+  if (ready && np <= 4) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      pre[u] = u < np ? __ldcg(reinterpret_cast<const float4*>(ob + u * pstride)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // 1. the largest running max, and whether any part was poisoned
+  float M = -INFINITY;
+  bool bad = !ready;
+  float2 first = make_float2(-INFINITY, 0.f);
+  if (ready) {
+    for (int p0 = 0; p0 < np; p0 += 32) {
+      const float2 ml = p0 + lane < np ? ml_at(p0 + lane) : make_float2(-INFINITY, 0.f);
+      if (p0 == 0) first = ml;
+      M = fmaxf(M, ml.x);
+      bad |= p0 + lane < np && ml.y < 0.f;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+  bad = __any_sync(kFull, bad);
+  // 2. weights 2^(m_p - M), the denominator, and the weighted sum of the partial outputs
+  float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+  if (!bad && M != -INFINITY && np <= 4) {
+    const float wgt = lane < np ? ex2(first.x - M) : 0.f;
+    float wl = wgt * first.y;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) wl += __shfl_xor_sync(kFull, wl, off);
+    den = wl;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float w = __shfl_sync(kFull, wgt, u);
+      if (u >= np) break;
+      num.x = fmaf(w, pre[u].x, num.x);
+      num.y = fmaf(w, pre[u].y, num.y);
+      num.z = fmaf(w, pre[u].z, num.z);
+      num.w = fmaf(w, pre[u].w, num.w);
+    }
+  } else if (!bad && M != -INFINITY) {
+    for (int p0 = 0; p0 < np; p0 += 32) {
+      const float2 ml = p0 == 0 ? first : (p0 + lane < np ? ml_at(p0 + lane) : make_float2(-INFINITY, 0.f));
+      const float wgt = p0 + lane < np ? ex2(ml.x - M) : 0.f;
+      float wl = wgt * ml.y;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) wl += __shfl_xor_sync(kFull, wl, off);
+      den += wl;
+      const int n = min(32, np - p0);
+      for (int j = 0; j < n; j += 4) {
+        float4 x[4];
+        float w4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          w4[u] = __shfl_sync(kFull, wgt, (j + u) & 31);
+          x[u] = j + u < n ? __ldcg(reinterpret_cast<const float4*>(ob + (p0 + j + u) * pstride))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (j + u >= n) break;
+          num.x = fmaf(w4[u], x[u].x, num.x);
+          num.y = fmaf(w4[u], x[u].y, num.y);
+          num.z = fmaf(w4[u], x[u].z, num.z);
+          num.w = fmaf(w4[u], x[u].w, num.w);
+        }
+      }
+    }
+  }
+  const bool zero = bad || !(den > 0.f);
+  const float inv = zero ? 0.f : 1.f / den;
+  T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(s) * a.out_row + static_cast<int64_t>(head) * D + 4 * lane;
+  if constexpr (std::is_same<T, __half>::value) {
+    const __half2 lo = __floats2half2_rn(num.x * inv, num.y * inv), hi = __floats2half2_rn(num.z * inv, num.w * inv);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&lo);
+    u.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(op) = u;
+  } else {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(num.x * inv, num.y * inv);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(num.z * inv, num.w * inv);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&lo);
+    u.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(op) = u;
+  }
+}
+
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// The merges, taken from a task counter by every warp once its block has no items left:
+// task t is head t mod H of sequence morder[t / H], in the order the sequences' parts
+// finish.  Every item was claimed before any warp gets here, by a
+// block that is running and finishes it without waiting on a merge, so the waits end;
+// each is bounded all the same and gives up early once a timeout is on record.
+template <typename T>
+__device__ __forceinline__ void merge_phase(const DecodeArgs& a, const int32_t* pbase, const int32_t* morder,
+                                            int lane) {
+  const int ntask = a.S * a.H;
+  while (true) {
+    int t = 0;
+    if (lane == 0) t = atomicAdd(a.sched + 2, 1);
+    t = __shfl_sync(kFull, t, 0);
+    if (t >= ntask) break;
+    const int i = t / a.H, head = t - i * a.H;
+    const int s = morder[i];
+    const int task = s * a.H + head;
+    const int base = pbase[s];
+    const int np = pbase[s + 1] - base;
+    if (np <= 1) continue;  // written directly by its item
+    const int32_t* cnt = a.ws_cnt + task;
+    bool ready = __all_sync(kFull, ld_acquire(cnt) >= np);
+    if (!ready) {
+      const long long t0 = clock64();
+      while (true) {
+        __nanosleep(200);
+        if (__all_sync(kFull, ld_acquire(cnt) >= np)) {
+          ready = true;
+          break;
+        }
+        if (*reinterpret_cast<volatile int32_t*>(a.status) & kDevTimeout) break;
+        if (clock64() - t0 > dk::kWaitCycles) {
+          if (lane == 0) atomicOr(a.status, kDevTimeout);
+          break;
+        }
+      }
+    }
+    merge_one<T>(a, s, head, base, np, ready, lane);
+    if (lane == 0 && ready) a.ws_cnt[task] = 0;  // zero between launches
   }
 }
 
@@ -715,13 +868,23 @@ __global__ void __launch_bounds__(32 * (HG + 1), 2)
       __syncwarp();
     }
     if (lane == 0) hist[0] = n_last;
+    // merge order (over the shared-token counts, which nothing reads any more): sequences
+    // without a last private part first (their parts finish earlier), then the others in
+    // the order their last parts are scheduled
+    __syncwarp();
+    int n0 = 0;
+    for (int base = 0; base < a.S; base += 32) {
+      const int s = base + lane;
+      const bool none = s < a.S && bucket_of(s) < 0;
+      const unsigned m = __ballot_sync(kFull, none);
+      if (none) lc[n0 + __popc(m & lt)] = s;
+      n0 += __popc(m);
+    }
+    for (int i = lane; i < n_last; i += 32) lc[n0 + i] = order[i];
   }
   __syncthreads();
   // `order` held the run starts until the sort above overwrote it; nothing reads them after
   // the chunk pass.
-  // block 0 publishes the partial-slot offsets for the merge kernel
-  if (blockIdx.x == 0)
-    for (int s = tid; s <= a.S; s += blockDim.x) a.pbase_out[s] = pbase[s];
   Plan pl;
   pl.lv = lv;
   pl.cinfo = cinfo;
@@ -809,19 +972,37 @@ __global__ void __launch_bounds__(32 * (HG + 1), 2)
           }
         }
       }
-      __threadfence();
-      if (atomicAdd(a.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
-        a.sched[0] = 0;
-        a.sched[1] = 0;
-        __threadfence();
-      }
     }
-    return;
-  }
-
+  } else {
   // ============================== consumer warps ==============================
   const int h = warp;
   int k = 0, ni = 0;
+  // Partials of split sequences are published in batches, not per item: a GPU-scope
+  // fence after every item stalled the warp (and with it the staging ring).  The ids of
+  // the items whose partials await publication sit in the setup scratch (free by now).
+  constexpr int kPubCap = 64 / HG - 1;  // entry kPubCap holds the count
+  int32_t* plist = reinterpret_cast<int32_t*>(comb) + h * (kPubCap + 1);
+  volatile int32_t* npub_s = plist + kPubCap;
+  if (lane == 0) *npub_s = 0;
+  __syncwarp();
+  auto publish = [&]() {
+    // after a timeout nothing is published: the merges see the status bit and give up
+    const int npub = *abort_flag ? 0 : *npub_s;
+    if (npub == 0) return;
+    __threadfence();  // every lane's partial stores, visible at GPU scope
+    __syncwarp();
+    for (int j = 0; j < npub; ++j) {
+      const SItem pit = locate(a, pl, plist[j]);
+      if (lane < pit.n) {
+        const int sj = pit.s + lane;
+        if (pl.pbase[sj + 1] - pl.pbase[sj] > 1)
+          atomicAdd(a.ws_cnt + static_cast<int64_t>(sj) * a.H + pit.g * HG + h, 1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) *npub_s = 0;
+    __syncwarp();
+  };
   while (true) {
     const int sl = ni & 1;
     const bool got =
@@ -832,97 +1013,38 @@ __global__ void __launch_bounds__(32 * (HG + 1), 2)
     ++ni;
     if (item < 0) break;
     const SItem it = locate(a, pl, item);
+    // listed now, published after this item's stores at the next batch
+    const bool split = lane < it.n && pl.pbase[it.s + lane + 1] - pl.pbase[it.s + lane] > 1;
+    if (__any_sync(kFull, split)) {
+      if (*npub_s == kPubCap) publish();
+      if (lane == 0) {
+        const int n = *npub_s;
+        plist[n] = item;
+        *npub_s = n + 1;
+      }
+      __syncwarp();
+    }
     if (B >= 16) {
       run_item<T, HG, 16>(a, pl, it, lay, sbase_u, bar_full, bar_empty, poison, abort_flag, stages, k, h, lane);
     } else {
       run_item<T, HG, 8>(a, pl, it, lay, sbase_u, bar_full, bar_empty, poison, abort_flag, stages, k, h, lane);
     }
   }
-}
+  publish();
+  }
 
-// Log-sum-exp merge of every split (sequence, head), one warp each, after the decode
-// kernel has finished (programmatic dependent launch: the wait returns once every
-// partial is written and visible).  Lane p holds part p's (max, sum) -- parts in chunks
-// of 32 -- and lane l accumulates output dimensions 4l .. 4l+3 over the parts, with the
-// loads of four parts in flight at a time.
-template <typename T>
-__global__ void __launch_bounds__(256) merge_shared_kernel(const DecodeArgs a) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  constexpr int D = 128;
-  const int lane = threadIdx.x & 31;
-  const int64_t wi = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (wi >= static_cast<int64_t>(a.S) * a.H) return;
-  const int s = static_cast<int>(wi / a.H), head = static_cast<int>(wi % a.H);
-  const int base = a.pbase_out[s];
-  const int np = a.pbase_out[s + 1] - base;
-  if (np <= 1) return;  // written directly by the decode kernel
-  auto ml_at = [&](int p) {
-    return __ldcg(reinterpret_cast<const float2*>(a.ws_ml + (static_cast<int64_t>(base + p) * a.H + head) * 2));
-  };
-  // 1. the largest running max, and whether any part was poisoned
-  float M = -INFINITY;
-  bool bad = false;
-  float2 first = make_float2(-INFINITY, 0.f);
-  for (int p0 = 0; p0 < np; p0 += 32) {
-    const float2 ml = p0 + lane < np ? ml_at(p0 + lane) : make_float2(-INFINITY, 0.f);
-    if (p0 == 0) first = ml;
-    M = fmaxf(M, ml.x);
-    bad |= p0 + lane < np && ml.y < 0.f;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-  bad = __any_sync(kFull, bad);
-  // 2. weights 2^(m_p - M), the denominator, and the weighted sum of the partial outputs
-  float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-  float den = 0.f;
-  if (!bad && M != -INFINITY) {
-    const float* ob = a.ws_o + (static_cast<int64_t>(base) * a.H + head) * D + 4 * lane;
-    const int64_t pstride = static_cast<int64_t>(a.H) * D;
-    for (int p0 = 0; p0 < np; p0 += 32) {
-      const float2 ml = p0 == 0 ? first : (p0 + lane < np ? ml_at(p0 + lane) : make_float2(-INFINITY, 0.f));
-      const float wgt = p0 + lane < np ? ex2(ml.x - M) : 0.f;
-      float wl = wgt * ml.y;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) wl += __shfl_xor_sync(kFull, wl, off);
-      den += wl;
-      const int n = min(32, np - p0);
-      for (int j = 0; j < n; j += 4) {
-        float4 x[4];
-        float w4[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          w4[u] = __shfl_sync(kFull, wgt, (j + u) & 31);
-          x[u] = j + u < n ? __ldcg(reinterpret_cast<const float4*>(ob + (p0 + j + u) * pstride))
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (j + u >= n) break;
-          num.x = fmaf(w4[u], x[u].x, num.x);
-          num.y = fmaf(w4[u], x[u].y, num.y);
-          num.z = fmaf(w4[u], x[u].z, num.z);
-          num.w = fmaf(w4[u], x[u].w, num.w);
-        }
-      }
+  // ---- 4. merges of split sequences, then the block retires ----------------------------
+  merge_phase<T>(a, pbase, lc, lane);
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(a.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      // the last block: every item and merge task has been claimed
+      a.sched[0] = 0;
+      a.sched[1] = 0;
+      a.sched[2] = 0;
+      __threadfence();
     }
-  }
-  const bool zero = bad || !(den > 0.f);
-  const float inv = zero ? 0.f : 1.f / den;
-  T* op = reinterpret_cast<T*>(a.out) + static_cast<int64_t>(s) * a.out_row + static_cast<int64_t>(head) * D + 4 * lane;
-  if constexpr (std::is_same<T, __half>::value) {
-    const __half2 lo = __floats2half2_rn(num.x * inv, num.y * inv), hi = __floats2half2_rn(num.z * inv, num.w * inv);
-    uint2 u;
-    u.x = *reinterpret_cast<const uint32_t*>(&lo);
-    u.y = *reinterpret_cast<const uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(op) = u;
-  } else {
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(num.x * inv, num.y * inv);
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(num.z * inv, num.w * inv);
-    uint2 u;
-    u.x = *reinterpret_cast<const uint32_t*>(&lo);
-    u.y = *reinterpret_cast<const uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(op) = u;
   }
 }
 
@@ -993,15 +1115,7 @@ cudaError_t launch_one(const DecodeArgs& a, const DecodeCfg& c, const CUtensorMa
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, tk, tv, a, c.stages);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t mcfg = {};
-  mcfg.gridDim = dim3(static_cast<unsigned>((static_cast<int64_t>(a.S) * a.H + 7) / 8));
-  mcfg.blockDim = dim3(256);
-  mcfg.stream = stream;
-  mcfg.attrs = attr;
-  mcfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&mcfg, merge_shared_kernel<T>, a);
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, a, c.stages);
 }
 
 template <typename T>

@@ -120,7 +120,7 @@ struct DecodeArgs {
   int32_t min_part;
   int32_t whole_first;          // automatic mode: keep whole sequences when they balance
   // workspace
-  int32_t* sched;               // [2]: next item, retired blocks (zero between launches)
+  int32_t* sched;               // [3]: next item, retired blocks, next merge task (zero between launches)
   int32_t* ws_cnt;              // [S * H]: partitions finished per (sequence, head) (zero between launches)
   float* ws_ml;                 // [items][HG][2] = (running max in log2 units, sum); null if no split
   float* ws_o;                  // [items][HG][D] unnormalised partial outputs; null if no split
@@ -129,7 +129,6 @@ struct DecodeArgs {
   // s - 1 (written by its plan kernel); runs with lcp >= min_shared form chunks; the
   // workspace holds part_cap partial slots of [H][D] (ws_o) and [H][2] (ws_ml)
   int32_t* lcp;
-  int32_t* pbase_out;           // [S + 1] first partial slot of each sequence, for the merge kernel
   int32_t min_shared;
   int32_t part_cap;
 };
@@ -157,7 +156,7 @@ cudaError_t launch_decode_bf16(const DecodeArgs&, const DecodeCfg&, const CUtens
 size_t decode_smem_bytes(const DecodeCfg& c, int elem_bytes, int R, int S);  // R: tokens per staged unit
 
 // Shared-prefix decode (16-bit caches, D = 128): the plan kernel, then the decode over
-// shared and private parts.  query_only as for the launchers above.
+// shared and private parts, which also merges split sequences.  query_only as for the launchers above.
 cudaError_t launch_decode_shared(const DecodeArgs&, const DecodeCfg&, const CUtensorMap&, const CUtensorMap&,
                                  cudaStream_t, bool query_only, int* max_ctas);
 size_t decode_shared_smem_bytes(const DecodeCfg& c, int R, int S);
