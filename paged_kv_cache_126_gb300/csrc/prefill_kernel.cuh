@@ -22,8 +22,8 @@
 //     copies of a tile are issued by the warp's lanes).  warp 1 (one lane):
 //     tcgen05.mma issuer, fp32 accumulators in TMEM (512 columns: S_0 S_1 O_0 O_1).
 //     S_q = Q_q K_t^T from shared memory; O_q (+)= P_q V_t with P_q read from TMEM,
-//     where the softmax left it over the first 64 columns of S_q (bf16: the weights'
-//     high parts there, their remainders over columns 64..127, two products).
+//     where the softmax left it over S_q's columns (each half of the keys over its own
+//     scores; bf16: the weights' high parts and their remainders, two products).
 //     warps 2-9: softmax of both slots, tile by tile (thread = query row = TMEM
 //     lane; warps w and w + 4 share a lane quadrant and split each tile's keys and
 //     the output dimensions in halves, exchanging row maxima and sums through shared
@@ -73,7 +73,8 @@ __host__ __device__ constexpr uint32_t smem_bytes(int S, int unit_cap) {
 }
 
 // TMEM (512 columns): S_q at column 128 q, O_q at 256 + 128 q (fp32, lane = query row);
-// P_q (16-bit, two per column) overwrites the first 64 columns of S_q.
+// P_q (16-bit, two per column) overwrites S_q: keys 0-63 in columns 0-31, keys 64-127 in
+// columns 64-95 (bf16 remainders in columns 32-63 and 96-127).
 constexpr uint32_t kTmemS = 0, kTmemO = 256;
 
 // mbarrier indices
@@ -577,18 +578,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       commit(BAR(BS_FULL + q));
     };
+    // weights of keys 16 ks .. 16 ks + 15 (16-bit pairs): columns 64 (ks / 4) + 8 (ks mod 4)
+    // of S_q, over the scores of the half of the tile they belong to
+    auto pcol_of = [](int ks) { return static_cast<uint32_t>((ks >> 2) * 64 + (ks & 3) * 8); };
     auto pv = [&](int q, int t, bool first) {
       const int st = t & 1;
 #pragma unroll
       for (int ks = 0; ks < kBN / 16; ++ks) {
         const uint64_t bd = sdesc(sb + kSmV + st * kTile + ks * 2 * 2048, 1024, 2048);
-        mma_ts(tmem + kTmemO + q * 128, tmem + kTmemS + q * 128 + ks * 8, bd, id_pv, (!first || ks > 0) ? 1u : 0u);
+        mma_ts(tmem + kTmemO + q * 128, tmem + kTmemS + q * 128 + pcol_of(ks), bd, id_pv,
+               (!first || ks > 0) ? 1u : 0u);
       }
-      if constexpr (kSplitP) {  // the weights' low parts, over columns 64..127 of S_q
+      if constexpr (kSplitP) {  // the weights' low parts, 32 columns after the high parts
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks) {
           const uint64_t bd = sdesc(sb + kSmV + st * kTile + ks * 2 * 2048, 1024, 2048);
-          mma_ts(tmem + kTmemO + q * 128, tmem + kTmemS + q * 128 + 64 + ks * 8, bd, id_pv, 1u);
+          mma_ts(tmem + kTmemO + q * 128, tmem + kTmemS + q * 128 + pcol_of(ks) + 32, bd, id_pv, 1u);
         }
       }
     };
@@ -667,11 +672,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // halves exchange it through shared memory (one mbarrier per quadrant, bounded
     // wait), and both take the same decision: the reference max m_ref the weights are
     // taken against moves only when the tile's row max passed it by more than 8 (log2
-    // units), so weights stay <= 2^8 and O is rescaled rarely.  Each half keeps a partial
-    // row sum; the halves add them at the epilogue.  P goes back to TMEM over the first
-    // 64 columns of S (keys 32c .. 32c+31 in columns 16c .. 16c+15): the second half's
-    // weights land over the first half's scores, which the exchange orders after the
-    // first half has read them.
+    // units), so weights stay <= 2^8 and O is rescaled rarely.  For bf16 a half posts its
+    // max, computes and stores its weights against the current m_ref, and only then reads
+    // the partner's max; when m_ref moves (every row's first tile, rarely afterwards) the
+    // weights are computed again.  Each half keeps a partial row sum; the halves add
+    // them at the epilogue.  P goes back to TMEM over the half's own 64 score columns
+    // (keys 64h + 2k, 64h + 2k + 1 in column 64h + k; bf16 remainders 32 columns on).
     const int half = (warp - kSmxWarp0) >> 2;
     const int quad = warp & 3;        // TMEM lane quadrant a warp may access
     const int row = quad * 32 + lane; // query row in the tile
@@ -761,51 +767,74 @@ __global__ void __launch_bounds__(kThreads, 1)
               mx4[(i >> 1) & 3] = fmax3(mx4[(i >> 1) & 3], __uint_as_float(cur[i]), __uint_as_float(cur[i + 1]));
           }
         }
-        float other;
-        if (!exchange(fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])), other)) { ok = false; continue; }
-        const float m_t = fmaxf(fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])), other) * sl2;
+        // Give the partner half this row's max now.  bf16 (two 16-bit parts per weight):
+        // read the partner's max only after the weights, computed against the current
+        // reference; they are final unless the tile's max passes it by more than 8, which
+        // after a row's first tile is rare, and then computed again from the scores, still
+        // in registers (fp16, with half the weight work, measured faster without this:
+        // 991 against 939 TF/s; bf16 755 against 735).  Each half writes its weights over
+        // its own score columns only, so it may store them before the partner has read
+        // its scores.
+        const float mine = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        float* xb = xbuf + (xk & 1u) * 256;
+        xb[half * 128 + row] = mine;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xbar);
+        const bool spec = kSplitP && __all_sync(kFull, m_ref[q] > -INFINITY && mine * sl2 <= m_ref[q] + 8.f);
+        uint64_t sum2[2];  // packed fp32 pairs of partial row sums
+        auto weights = [&](float mref) {
+          const uint64_t nm2 = f2(-mref, -mref);
+          sum2[0] = sum2[1] = 0ull;
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const uint32_t pcol = s_tmem + 64 * half + 16 * cc;
+            uint32_t w[16];
+            uint32_t wl[kSplitP ? 16 : 1];  // low parts (bf16 only)
+            if (wmax <= cc * 32) {
+#pragma unroll
+              for (int k = 0; k < 16; ++k) w[k] = 0u;
+              if constexpr (kSplitP) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) wl[k] = 0u;
+              }
+            } else {
+              const uint32_t(&cur)[32] = sr[cc];
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                float x0, x1;
+                unf2(ffma2(f2(__uint_as_float(cur[i]), __uint_as_float(cur[i + 1])), sl2x2, nm2), x0, x1);
+                const float p0 = ex2(x0), p1 = ex2(x1);
+                sum2[(i >> 1) & 1] = fadd2(sum2[(i >> 1) & 1], f2(p0, p1));
+                const uint32_t hi = pack2<T>(p0, p1);
+                w[i >> 1] = hi;
+                if constexpr (kSplitP) {
+                  // p - bf16(p) is exact in fp32; its own bf16 rounding leaves 2^-16 p
+                  float r0, r1;
+                  unf2(ffma2(f2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u)), f2(-1.f, -1.f),
+                             f2(p0, p1)),
+                       r0, r1);
+                  wl[i >> 1] = pack2<T>(r0, r1);
+                }
+              }
+            }
+            tmem_st16(pcol, w);
+            if constexpr (kSplitP) tmem_st16(pcol + 32, wl);
+          }
+        };
+        if (spec) weights(m_ref[q]);
+        if (!wait_all(xbar, xk & 1u)) { ok = false; continue; }
+        ++xk;
+        const float other = xb[(half ^ 1) * 128 + row];
+        const float m_t = fmaxf(mine, other) * sl2;
         // one decision per tile, the same in both halves (always on a row's first tile)
         float alpha = 1.f;
         if (m_t > m_ref[q] + 8.f) {
           alpha = ex2(m_ref[q] - m_t);
           m_ref[q] = m_t;
         }
-        const uint64_t nm2 = f2(-m_ref[q], -m_ref[q]);
-        uint64_t sum2[2] = {0ull, 0ull};  // packed fp32 pairs of partial row sums
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const uint32_t pcol = s_tmem + 32 * half + 16 * cc;
-          uint32_t w[16];
-          uint32_t wl[kSplitP ? 16 : 1];  // low parts (bf16 only)
-          if (wmax <= cc * 32) {
-#pragma unroll
-            for (int k = 0; k < 16; ++k) w[k] = 0u;
-            if constexpr (kSplitP) {
-#pragma unroll
-              for (int k = 0; k < 16; ++k) wl[k] = 0u;
-            }
-          } else {
-            const uint32_t(&cur)[32] = sr[cc];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              float x0, x1;
-              unf2(ffma2(f2(__uint_as_float(cur[i]), __uint_as_float(cur[i + 1])), sl2x2, nm2), x0, x1);
-              const float p0 = ex2(x0), p1 = ex2(x1);
-              sum2[(i >> 1) & 1] = fadd2(sum2[(i >> 1) & 1], f2(p0, p1));
-              const uint32_t hi = pack2<T>(p0, p1);
-              w[i >> 1] = hi;
-              if constexpr (kSplitP) {
-                // p - bf16(p) is exact in fp32; its own bf16 rounding leaves 2^-16 p
-                float r0, r1;
-                unf2(ffma2(f2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u)), f2(-1.f, -1.f),
-                           f2(p0, p1)),
-                     r0, r1);
-                wl[i >> 1] = pack2<T>(r0, r1);
-              }
-            }
-          }
-          tmem_st16(pcol, w);
-          if constexpr (kSplitP) tmem_st16(pcol + 64, wl);
+        if (!spec || __any_sync(kFull, alpha != 1.f)) {
+          if (spec) tmem_wait_st();  // the stores above land before these
+          weights(m_ref[q]);
         }
         if (j > 0 && __any_sync(kFull, alpha != 1.f)) {
           // O_q holds the previous tiles (the S commit covered their P V); this half's
