@@ -139,8 +139,11 @@ int pa_copy_blocks(const pa_tensor* k_cache, const pa_tensor* v_cache,
  * pa_shutdown().  Calls on one stream run in order; calls on different streams
  * use different workspaces.
  * Supported: dtype f32/f16/bf16; D in {64, 128, 256} (f32: {64, 128});
- * 1 <= B <= 256; S <= 65536 (each thread block keeps three int32 per sequence in
- * shared memory) and max_blocks * B < 2^31, else PA_ERR_UNSUPPORTED.
+ * 1 <= B <= 256; max_blocks * B < 2^31, else PA_ERR_UNSUPPORTED.  Any S < 2^31:
+ * every thread block keeps three int32 per sequence in shared memory beside its
+ * staging ring, so a batch larger than one launch holds (about 13,000 sequences
+ * with 4 heads of 128 fp16 per block) runs as launches over consecutive ranges of
+ * sequences, one after another on the stream.
  * Bounded waits: every wait inside the kernels gives up after ~2 s, raising
  * PA_DEV_TIMEOUT (the outputs of that call are then undefined).  Reading the status
  * with pa_get_device_status marks this device's workspaces for re-zeroing, so later
@@ -265,6 +268,8 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
  *
  * Arguments, results and error checks are those of pa_decode with automatic
  * launch options; the caller still provides every input and output.
+ *   - One launch only: PA_ERR_UNSUPPORTED when S is more than one launch holds
+ *     (pa_decode would split the batch).
  *   - Returns PA_ERR_SCRATCH_LIMIT, launching nothing, when the problem needs more
  *     than 16 MiB of scratch: 256 B of work counters and, when a context may be
  *     split, S*H int32 arrival counters plus room for up to

@@ -248,6 +248,15 @@ int elem_bytes(int dtype) { return dtype == PA_F32 || dtype == PA_I32 ? 4 : (dty
 bool is_float(int dtype) { return dtype == PA_F32 || dtype == PA_F16 || dtype == PA_BF16; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Rows [s0, s0 + n) of a tensor whose first dimension is the sequence: a view with the
+// same strides.
+pa_tensor row_range(const pa_tensor* t, int64_t s0, int64_t n) {
+  pa_tensor v = *t;
+  v.data = static_cast<unsigned char*>(t->data) + s0 * t->stride[0] * elem_bytes(t->dtype);
+  v.shape[0] = n;
+  return v;
+}
+
 // [N, H, D] with the [H, D] part contiguous and a 16-byte-multiple row stride.
 int check_rows(const pa_tensor* t, int dtype, int64_t H, int64_t D) {
   if (!t) return PA_ERR_INVALID;
@@ -638,6 +647,8 @@ namespace {
 // shared-prefix kernel handles (the caller then runs the plain decode: same result),
 // or an error code.
 constexpr int kNotApplicable = 1;
+// plan_decode: the batch needs more shared memory than one launch has (split it)
+constexpr int kTooManySeqs = 2;
 
 int decode_shared(int dev, const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
                   const pa_tensor* block_tables, const pa_tensor* context_lens, float scale, const pa_tensor* out,
@@ -770,7 +781,7 @@ int check_decode(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
   if (max_blocks < 0 || (S > 1 && block_tables->stride[0] < max_blocks)) return PA_ERR_STRIDE;
   if (B > 256) return PA_ERR_UNSUPPORTED;
   if (!(D == 64 || D == 128 || (D == 256 && dt != PA_F32))) return PA_ERR_UNSUPPORTED;
-  if (max_blocks * B > INT32_MAX || S > 65536) return PA_ERR_UNSUPPORTED;
+  if (max_blocks * B > INT32_MAX || S > INT32_MAX) return PA_ERR_UNSUPPORTED;
   if (S > 0 && max_blocks > 0 && !block_tables->data) return PA_ERR_INVALID;
   *S_out = S;
   return PA_OK;
@@ -844,9 +855,14 @@ int plan_decode(int dev, const pa_tensor* q, const pa_tensor* k_cache, const pa_
         c.stages = 0;
       }
     }
-    if (c.stages == 0) return PA_ERR_UNSUPPORTED;
   }
-  if (pa::decode_smem_bytes(c, e, static_cast<int>(R), static_cast<int>(S)) > smem_cap) return PA_ERR_UNSUPPORTED;
+  if (c.stages == 0 || pa::decode_smem_bytes(c, e, static_cast<int>(R), static_cast<int>(S)) > smem_cap) {
+    // every thread block keeps three int32 per sequence in shared memory beside its
+    // staging ring: a batch too large for that is run as several launches
+    pa::DecodeCfg one = c;
+    one.stages = p.stages ? p.stages : 2;
+    return pa::decode_smem_bytes(one, e, static_cast<int>(R), 1) <= smem_cap ? kTooManySeqs : PA_ERR_UNSUPPORTED;
+  }
 
   pa::DecodeArgs& a = pl->a;
   std::memset(&a, 0, sizeof(a));
@@ -935,15 +951,31 @@ int pa_decode_ex(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* 
     const int rc = decode_shared(dev, q, k_cache, v_cache, block_tables, context_lens, scale, out, p, stream);
     if (rc != kNotApplicable) return rc;
   }
-  DecodePlan pl;
-  PA_TRY(plan_decode(dev, q, k_cache, v_cache, block_tables, context_lens, scale, out, p, &pl));
-  void* ws = nullptr;
-  size_t cnt_bytes = 0;
-  PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), pl.cnt_need, pl.o_bytes + pl.ml_bytes, &ws, &cnt_bytes));
-  place_scratch(&pl, static_cast<unsigned char*>(ws), cnt_bytes);
-  if (dispatch_decode(pl.a, pl.c, pl.tk, pl.tv, static_cast<cudaStream_t>(stream), false, nullptr) != cudaSuccess)
-    return PA_ERR_CUDA;
-  g_launches.fetch_add(1);
+  // Sequences are independent: a batch too large for one launch's shared memory runs as
+  // launches over consecutive ranges of sequences, the largest range that fits (found by
+  // halving), one after another on the stream.
+  int64_t chunk = S;
+  for (int64_t s0 = 0; s0 < S;) {
+    const int64_t n = std::min(chunk, S - s0);
+    const pa_tensor qv = row_range(q, s0, n), ov = row_range(out, s0, n);
+    const pa_tensor tv = row_range(block_tables, s0, n), lv = row_range(context_lens, s0, n);
+    DecodePlan pl;
+    const int rc = plan_decode(dev, &qv, k_cache, v_cache, &tv, &lv, scale, &ov, p, &pl);
+    if (rc == kTooManySeqs && n > 1) {
+      chunk = (n + 1) / 2;
+      continue;
+    }
+    if (rc == kTooManySeqs) return PA_ERR_UNSUPPORTED;
+    PA_TRY(rc);
+    void* ws = nullptr;
+    size_t cnt_bytes = 0;
+    PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), pl.cnt_need, pl.o_bytes + pl.ml_bytes, &ws, &cnt_bytes));
+    place_scratch(&pl, static_cast<unsigned char*>(ws), cnt_bytes);
+    if (dispatch_decode(pl.a, pl.c, pl.tk, pl.tv, static_cast<cudaStream_t>(stream), false, nullptr) != cudaSuccess)
+      return PA_ERR_CUDA;
+    g_launches.fetch_add(1);
+    s0 += n;
+  }
   return PA_OK;
 }
 
@@ -1063,7 +1095,11 @@ extern "C" int pa_decode_static(const pa_tensor* q, const pa_tensor* k_cache, co
   pa_decode_params p;
   std::memset(&p, 0, sizeof(p));
   DecodePlan pl;
-  PA_TRY(plan_decode(dev, q, k_cache, v_cache, block_tables, context_lens, scale, out, p, &pl));
+  {
+    const int rc = plan_decode(dev, q, k_cache, v_cache, block_tables, context_lens, scale, out, p, &pl);
+    if (rc == kTooManySeqs) return PA_ERR_UNSUPPORTED;  // one launch only: no split into ranges
+    PA_TRY(rc);
+  }
   // Scratch layout inside the fixed array: counters | arrival counters | split partials.
   const size_t cnt_bytes = round256(pl.cnt_need);
   if (kSchedBytes + cnt_bytes + pl.o_bytes + pl.ml_bytes > kFixedScratchBytes) return PA_ERR_SCRATCH_LIMIT;

@@ -211,3 +211,27 @@ def test_many_sequences_prefix_scan(pa):
     w = workloads.custom(L, H=2, D=64, B=16, dtype="f16", seed=3)
     eng, outs, ref = run_both(pa, w, params={"partition_tokens": 16})
     check_outputs(w, outs, ref)
+
+
+def test_batch_larger_than_one_launch(pa):
+    """24,000 sequences: more than one launch holds (every thread block keeps three
+    int32 per sequence in shared memory), so pa_decode runs consecutive ranges of
+    sequences as separate launches; every output against the oracle."""
+    rng = np.random.default_rng(31)
+    L = rng.integers(1, 13, size=24000).tolist()
+    w = workloads.custom(L, H=2, D=64, B=8, dtype="f16", seed=31)
+    eng, outs, ref = run_both(pa, w)
+    check_outputs(w, outs, ref)
+    (op,) = [i for i, o in enumerate(w.ops) if o[0] == "attend"]
+    q = pa.to_device_rows(w.query(op), w.dtype, eng.device)
+    n0 = pa.pa_launch_count()
+    again = eng.attend(w.ops[op][1], q, w.scale)
+    torch.cuda.synchronize()
+    assert pa.pa_launch_count() - n0 >= 2
+    assert torch.equal(again, outs[op])
+    # the fixed-scratch entry point launches once or refuses
+    tables, lens = eng.bm.block_tables(w.ops[op][1], eng.max_blocks)
+    tt, ll = torch.from_numpy(tables).to(eng.device), torch.from_numpy(lens).to(eng.device)
+    with pytest.raises(pa.PAError):
+        pa.pa_decode_static(q, eng.k_cache, eng.v_cache, tt, ll, w.scale, torch.empty_like(q))
+    assert pa.pa_get_device_status() == 0
