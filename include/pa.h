@@ -179,8 +179,11 @@ int pa_decode(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_c
  * T rows allow set PA_DEV_BAD_LEN and nothing is computed.  Frame ids outside
  * [0, num_blocks) set PA_DEV_BAD_BLOCK and read as zeros.  Uses the (device, stream)
  * workspace's work counter; one thread block per SM; tile pairs are taken longest
- * first.  PA_ERR_UNSUPPORTED when S + T/256 is too large for the block's shared memory
- * (about 8000).
+ * first.  Every thread block keeps the tile-pair offsets and order of the batch in
+ * shared memory (about 8000 entries, S + T/256 + 1 of them): a batch with more
+ * sequences than that runs as launches over consecutive ranges of sequences (q and
+ * out stay whole), one after another on the stream; PA_ERR_UNSUPPORTED only when T
+ * alone leaves no room (T above about two million rows).
  */
 int pa_prefill(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_cache,
                const pa_tensor* block_tables, const pa_tensor* context_lens,

@@ -1005,11 +1005,19 @@ int pa_prefill(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_
   if (max_blocks < 0 || (S > 1 && block_tables->stride[0] < max_blocks)) return PA_ERR_STRIDE;
   if (max_blocks * B > INT32_MAX || T > INT32_MAX || nb * B > INT32_MAX) return PA_ERR_UNSUPPORTED;
   if (S == 0 || T == 0) return PA_OK;
-  // a sequence with n query rows forms ceil(ceil(n / 128) / 2) <= n / 256 + 1 units
-  const int64_t unit_cap = S + (T + 255) / 256 + 1;
-  if (unit_cap > INT32_MAX ||
-      pa::prefill_smem_bytes(static_cast<int>(S), static_cast<int>(unit_cap)) > 227 * 1024)
-    return PA_ERR_UNSUPPORTED;
+  // A sequence with n query rows forms ceil(ceil(n / 128) / 2) <= n / 256 + 1 units, so
+  // n sequences of the batch form at most n + T / 256 + 1.  Every thread block keeps
+  // their unit offsets and order in shared memory: a batch larger than that runs as
+  // launches over consecutive ranges of sequences (q and out stay whole: query_start
+  // entries index all of q).
+  const int64_t tile_cap = (T + 255) / 256 + 1;
+  auto fits = [&](int64_t n) {
+    return n + tile_cap <= INT32_MAX &&
+           pa::prefill_smem_bytes(static_cast<int>(n), static_cast<int>(n + tile_cap)) <= 227 * 1024;
+  };
+  if (!fits(1)) return PA_ERR_UNSUPPORTED;
+  int64_t chunk = S;
+  while (!fits(chunk)) chunk = (chunk + 1) / 2;
   int dev;
   PA_TRY(current_device(&dev));
 
@@ -1029,7 +1037,6 @@ int pa_prefill(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_
   a.num_blocks = static_cast<int32_t>(nb);
   a.max_blocks = static_cast<int32_t>(max_blocks);
   a.T = static_cast<int32_t>(T);
-  a.unit_cap = static_cast<int32_t>(unit_cap);
   a.qk_scale_log2 = scale * 1.4426950408889634f;
   a.status = g_dev[dev].status;
 
@@ -1042,10 +1049,19 @@ int pa_prefill(const pa_tensor* q, const pa_tensor* k_cache, const pa_tensor* v_
   PA_TRY(workspace(dev, static_cast<cudaStream_t>(stream), 0, 0, &ws, &cnt_bytes));
   a.sched = static_cast<int32_t*>(ws);
   const int grid = g_dev[dev].num_sms;
-  const cudaError_t e = dt == PA_F16 ? pa::launch_prefill_f16(a, tq, tk, tv, grid, static_cast<cudaStream_t>(stream))
-                                     : pa::launch_prefill_bf16(a, tq, tk, tv, grid, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return PA_ERR_CUDA;
-  g_launches.fetch_add(1);
+  for (int64_t s0 = 0; s0 < S; s0 += chunk) {
+    const int64_t n = std::min(chunk, S - s0);
+    pa::PrefillArgs r = a;
+    r.block_tables = a.block_tables + s0 * a.bt_row;
+    r.context_lens = a.context_lens + s0;
+    r.query_start = a.query_start + s0;
+    r.S = static_cast<int32_t>(n);
+    r.unit_cap = static_cast<int32_t>(n + tile_cap);
+    const cudaError_t e = dt == PA_F16 ? pa::launch_prefill_f16(r, tq, tk, tv, grid, static_cast<cudaStream_t>(stream))
+                                       : pa::launch_prefill_bf16(r, tq, tk, tv, grid, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+    g_launches.fetch_add(1);
+  }
   return PA_OK;
 }
 

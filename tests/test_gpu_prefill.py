@@ -109,6 +109,25 @@ def test_many_items_per_block(pa):
     assert pa.pa_get_device_status() == 0
 
 
+def test_batch_larger_than_one_launch(pa):
+    """5000 sequences of 1-3 query rows: more than one launch's shared memory holds (unit
+    offsets and order per sequence), so pa_prefill runs consecutive ranges of sequences
+    as separate launches, q and out whole."""
+    rng = np.random.default_rng(41)
+    pre = rng.integers(0, 40, size=5000).tolist()
+    ch = rng.integers(1, 4, size=5000).tolist()
+    w = workloads.chunked_prefill(pre, ch, H=2, D=128, B=16, dtype="f16", seed=41)
+    eng, outs, ref = run_both(pa, w)
+    check_prefill(w, outs, ref)
+    (op,) = w.prefill_ops
+    n0 = pa.pa_launch_count()
+    again = eng.prefill(w.ops[op][1], w.ops[op][2], w.query(op), w.scale)
+    torch.cuda.synchronize()
+    assert pa.pa_launch_count() - n0 >= 2
+    assert torch.equal(again, outs[op])
+    assert pa.pa_get_device_status() == 0
+
+
 def test_prefill_one_query_matches_decode(pa):
     """A chunk of one query is a decode step: both kernels agree within tolerance."""
     L = [37, 300, 811, 1]
