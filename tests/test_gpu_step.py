@@ -82,6 +82,12 @@ CASES = [
     # 109 and 123 frames with the pairs in the launch parameters
     ("beam search, 316 copies in one step", lambda: workloads.beam_search(4, 30, 80, 4, H=2, B=16, dtype="f16",
                                                                          seed=78)),
+    # the boundary of the copies carried in the launch parameters: 256 (the most that fit)
+    # and 257 (uploaded) in the first step
+    ("beam search, 256 copies in one step", lambda: workloads.beam_search(1, 20, 257, 2, H=2, B=16, dtype="f16",
+                                                                         seed=79)),
+    ("beam search, 257 copies in one step", lambda: workloads.beam_search(1, 20, 258, 2, H=2, B=16, dtype="bf16",
+                                                                         seed=80)),
 ]
 
 
