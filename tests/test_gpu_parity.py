@@ -235,3 +235,17 @@ def test_batch_larger_than_one_launch(pa):
     with pytest.raises(pa.PAError):
         pa.pa_decode_static(q, eng.k_cache, eng.v_cache, tt, ll, w.scale, torch.empty_like(q))
     assert pa.pa_get_device_status() == 0
+
+
+@pytest.mark.parametrize("sigma", [3.0, 4.0])
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+def test_wide_value_range(pa, sigma, dtype):
+    """Queries, keys and values of spread sigma (scores of spread sigma^2): the running
+    max moves often and weights span many binades, whole and split into partitions.  The
+    2e-3 gate holds for unit-scale values; the fp32 score error grows with |q||k|, so the
+    gate scales with sigma here."""
+    w = workloads.custom([1, 17, 300, 1000, 2500], H=4, D=128, B=16, dtype=dtype, sigma=sigma, seed=int(sigma) + 40)
+    for part in (0, -1, 64):
+        eng, outs, ref = run_both(pa, w, params={"partition_tokens": part})
+        check_outputs(w, outs, ref, tol=2e-3 * sigma)
+    assert pa.pa_get_device_status() == 0
