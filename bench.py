@@ -541,7 +541,7 @@ def gpu_arm(args):
     if not args.no_extra:
         del bench
         torch.cuda.empty_cache()
-        line["extra"] = {"fixed_64x2048": fixed_variant(args, device), **bench_extras(device)}
+        line["extra"] = {"fixed_64x2048": _guarded(lambda: fixed_variant(args, device)), **bench_extras(device)}
     if not args.no_cpu:
         cpu = run_cpu_baseline(args.config, args.cpu_budget or 8.0)
         allc = run_cpu_all_cores(args.config, args.cpu_budget or 8.0)
@@ -550,6 +550,14 @@ def gpu_arm(args):
         cpu["all_cores"] = allc
         line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
+
+
+def _guarded(fn):
+    """fn(), or its error in one line: a failing extra figure must not lose the line."""
+    try:
+        return fn()
+    except Exception as e:  # noqa: BLE001
+        return {"error": f"{type(e).__name__}: {e}"[:300]}
 
 
 def fixed_variant(args, device):
@@ -959,7 +967,8 @@ def bench_extras(device, reps=10, flushed_reps=10):
     decode / prefill throughput against the block size."""
     peak, src = _peaks()
     out = {}
-    for key, name in (("2", "cfg2"), ("3", "cfg3"), ("3s", "cfg3_shared"), ("4", "cfg4")):
+
+    def decode_entry(key):
         f = decode_figures(key, reps, flushed_reps, device_rows=True, memset=False, append=(key == "4"),
                            sample_clocks=True)
         fl = f["flushed"]
@@ -979,21 +988,19 @@ def bench_extras(device, reps=10, flushed_reps=10):
             ent["cow_copies"] = f["cow_copies"]
         if "append" in f:
             ent["append"] = f["append"]
-        out[name] = ent
-    out["prefill"] = prefill_figures(reps, flushed_reps, e2e=False, device_rows=True, sample_clocks=True)
-    # the remaining next-step workloads, compact: each guarded, so that a failure here
-    # leaves its error in the line instead of losing the line
-    def guarded(fn):
-        try:
-            return fn()
-        except Exception as e:  # noqa: BLE001
-            return {"error": f"{type(e).__name__}: {e}"[:300]}
+        return ent
 
-    out["fork_trees"] = {"pa_decode": guarded(lambda: fork_tree_bench(emit=False)),
-                         "shared_prefix": guarded(lambda: fork_tree_bench(share=True, emit=False))}
-    out["prefix_caching"] = guarded(lambda: prefix_bench(emit=False))
-    out["split_layout"] = guarded(lambda: split_layout_bench(emit=False))
-    out["block_sweep"] = guarded(lambda: block_sweep(blocks=(8, 16, 32, 64), emit=False))
+    for key, name in (("2", "cfg2"), ("3", "cfg3"), ("3s", "cfg3_shared"), ("4", "cfg4")):
+        out[name] = _guarded(lambda k=key: decode_entry(k))
+    out["prefill"] = _guarded(lambda: prefill_figures(reps, flushed_reps, e2e=False, device_rows=True,
+                                                      sample_clocks=True))
+    # the remaining next-step workloads, compact; every entry is guarded, so that a
+    # failure leaves its error in the line instead of losing the line
+    out["fork_trees"] = {"pa_decode": _guarded(lambda: fork_tree_bench(emit=False)),
+                         "shared_prefix": _guarded(lambda: fork_tree_bench(share=True, emit=False))}
+    out["prefix_caching"] = _guarded(lambda: prefix_bench(emit=False))
+    out["split_layout"] = _guarded(lambda: split_layout_bench(emit=False))
+    out["block_sweep"] = _guarded(lambda: block_sweep(blocks=(8, 16, 32, 64), emit=False))
     return out
 
 
