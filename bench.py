@@ -425,30 +425,34 @@ def gpu_arm(args):
     # ---- end to end: host buffers, copies inside the timed region ---------------------------
     dt = bench.inputs[0][0].dtype
     S, H, D = bench.S, bench.H, bench.D
-    # Every step copies its k/v/q rows in from pinned host memory and its output back; the
-    # copies run on a copy stream, double-buffered, so step k+1's inputs and step k's
-    # output travel while step k+1 computes.
+    # Every step copies its k/v/q rows in from pinned host memory and its output back.  The
+    # copies run on a copy stream, pipelined a group of G steps ahead over 2G buffers: the
+    # inputs of the next group travel while this group computes, and each output goes back
+    # as soon as its step is done.  The compute stream waits on the copy stream once per
+    # group (a wait between two kernels costs the programmatic launch overlap of that pair).
     host_in = [tuple(x.cpu().pin_memory() for x in trip) for trip in bench.inputs]
-    nbuf = 2
+    G = 4
+    nbuf = 2 * G
     dev_in = [[torch.empty(S, H, D, dtype=dt, device=device) for _ in range(3)] for _ in range(nbuf)]
     dev_out = [torch.empty(S, H, D, dtype=dt, device=device) for _ in range(nbuf)]
     host_out = [torch.empty(S, H, D, dtype=dt).pin_memory() for _ in range(nbuf)]
     cs = torch.cuda.Stream(device)
-    ev_in = [torch.cuda.Event() for _ in range(nbuf)]    # buffer b's inputs have landed
-    ev_done = [torch.cuda.Event() for _ in range(nbuf)]  # the step that used buffer b has finished
-    ev_read = [torch.cuda.Event() for _ in range(nbuf)]  # buffer b's output has reached the host
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]    # the inputs of step k (buffer k mod nbuf) have landed
+    ev_done = [torch.cuda.Event() for _ in range(nbuf)]  # step k has finished
+    ev_read = [torch.cuda.Event() for _ in range(nbuf)]  # step k's output has reached the host
     mb = bench.eng.max_blocks
     h2d = 3 * S * H * D * bench.e + 4 * (4 * S + S * mb)
     d2h = S * H * D * bench.e
 
-    def load(k):
-        b = k % nbuf
+    def load_group(k0):
+        """Inputs of steps k0 .. k0 + G - 1 (their buffers last served steps k0 - nbuf ..)."""
         with torch.cuda.stream(cs):
-            if k >= nbuf:
-                cs.wait_event(ev_done[b])
-            for x, hx in zip(dev_in[b], host_in[k % 4]):
-                x.copy_(hx, non_blocking=True)
-            ev_in[b].record(cs)
+            if k0 >= nbuf:
+                cs.wait_event(ev_done[(k0 - nbuf + G - 1) % nbuf])
+            for k in range(k0, min(k0 + G, k_e2e)):
+                for x, hx in zip(dev_in[k % nbuf], host_in[k % 4]):
+                    x.copy_(hx, non_blocking=True)
+                ev_in[k % nbuf].record(cs)
 
     barrier()
     torch.cuda.synchronize()
@@ -456,14 +460,17 @@ def gpu_arm(args):
     e2e_bytes = 0
     e0.record(st)
     cs.wait_event(e0)
-    load(0)
+    load_group(0)
     for k in range(k_e2e):
         b = k % nbuf
-        if k + 1 < k_e2e:
-            load(k + 1)
-        st.wait_event(ev_in[b])
-        if k >= nbuf:
-            st.wait_event(ev_read[b])
+        if k % G == 0:
+            if k + G < k_e2e:
+                load_group(k + G)
+            # this group's inputs, and its output buffers free (their outputs, G steps and
+            # more before, read back)
+            st.wait_event(ev_in[(min(k + G, k_e2e) - 1) % nbuf])
+            if k >= nbuf:
+                st.wait_event(ev_read[(k + G - 1 - nbuf) % nbuf])
         out, _, lens = bench.eng.decode_step(bench.batches[(W + K + k) % R], dev_in[b][0], dev_in[b][1],
                                              dev_in[b][2], bench.scale, dev_out[b])
         ev_done[b].record(st)
