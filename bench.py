@@ -915,7 +915,8 @@ def prefill_figures(reps=20, flushed_reps=50, e2e=True, device_rows=False, sampl
         # End to end through host buffers: every step copies the chunk's queries and its
         # new K/V rows from pinned host memory, appends the rows at their slots (the
         # values already there: the cache is unchanged), prefills, and copies the output
-        # back.
+        # back.  The copies are pipelined over two buffer sets: step k+1's inputs travel on
+        # one copy stream and step k-1's output on another while step k computes.
         slot_list = []
         for s_, L_, n_ in zip(seqs, lens, counts):
             slot_list += [eng.bm.slot(s_, p_) for p_ in range(int(L_) - int(n_), int(L_))]
@@ -923,34 +924,63 @@ def prefill_figures(reps=20, flushed_reps=50, e2e=True, device_rows=False, sampl
         kn = eng.k_cache.view(-1, w.num_heads, w.head_dim)[slots.long()]
         vn = eng.v_cache.view(-1, w.num_heads, w.head_dim)[slots.long()]
         hq, hk, hv = (x.cpu().pin_memory() for x in (q, kn, vn))
-        hout = torch.empty_like(out, device="cpu").pin_memory()
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+        hout = [torch.empty_like(out, device="cpu").pin_memory() for _ in range(2)]
+        bufs = [(torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn), torch.empty_like(out))
+                for _ in range(2)]
+        cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_read = [torch.cuda.Event() for _ in range(2)]
         k_e2e = 10
 
-        def e2e_step():
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-            pa.pa_cache_append(dk, dv, slots, eng.k_cache, eng.v_cache)
-            pa.pa_prefill(dq, eng.k_cache, eng.v_cache, tt, ll, qq, w.scale, out)
-            hout.copy_(out, non_blocking=True)
+        def load(k):
+            dq, dk, dv, _ = bufs[k % 2]
+            with torch.cuda.stream(cin):
+                if k >= 2:
+                    cin.wait_event(ev_done[k % 2])
+                dq.copy_(hq, non_blocking=True)
+                dk.copy_(hk, non_blocking=True)
+                dv.copy_(hv, non_blocking=True)
+                ev_in[k % 2].record(cin)
 
-        for _ in range(3):
-            e2e_step()
+        def run(n):
+            load(0)
+            for k in range(n):
+                b_ = k % 2
+                dq, dk, dv, do = bufs[b_]
+                if k + 1 < n:
+                    load(k + 1)
+                st.wait_event(ev_in[b_])
+                if k >= 2:
+                    st.wait_event(ev_read[b_])
+                pa.pa_cache_append(dk, dv, slots, eng.k_cache, eng.v_cache)
+                pa.pa_prefill(dq, eng.k_cache, eng.v_cache, tt, ll, qq, w.scale, do)
+                ev_done[b_].record(st)
+                with torch.cuda.stream(cout):
+                    cout.wait_event(ev_done[b_])
+                    hout[b_].copy_(do, non_blocking=True)
+                    ev_read[b_].record(cout)
+            st.wait_stream(cin)
+            st.wait_stream(cout)
+
+        run(3)
         torch.cuda.synchronize()
         e0.record(st)
-        for _ in range(k_e2e):
-            e2e_step()
+        cin.wait_event(e0)
+        run(k_e2e)
         e1.record(st)
         torch.cuda.synchronize()
         e2e_us = e0.elapsed_time(e1) / k_e2e * 1e3
-        assert torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16))
+        for h_ in hout:
+            assert torch.equal(h_.view(torch.int16), out.cpu().view(torch.int16))
+        hout = hout[0]
         h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
         d2h = hout.numel() * hout.element_size()
         res["e2e"] = {"us_per_step": round(e2e_us, 2), "tflops": round(flops / (e2e_us * 1e-6) / 1e12, 1),
                       "steps": k_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                       "step": "queries and the chunk's K/V rows copied from pinned host memory, "
-                              "pa_cache_append of the chunk, pa_prefill, output copied back"}
+                              "pa_cache_append of the chunk, pa_prefill, output copied back; copies "
+                              "pipelined over two buffer sets on two copy streams"}
     del eng
     torch.cuda.empty_cache()
     return res
