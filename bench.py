@@ -540,7 +540,7 @@ def gpu_arm(args):
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "api": "PagedKVEngine.decode_step with q/k/v copied from pinned host buffers and out copied back "
-                   "every step (copies on a second stream, double-buffered)",
+                   "every step (copies on a second stream, pipelined a group of four steps ahead)",
         },
         "gpu_launches": launches,
         "clocks": clk,
